@@ -1,0 +1,233 @@
+"""Float64 CPU oracle of the routed-expert MoE layer with weight-only NVFP4 experts.
+
+TEST INFRASTRUCTURE ONLY.  The product (the CUDA library and its Python
+binding) never imports, calls or links this file; only tests, the smoke check
+and the benchmark's CPU-baseline leg do.
+
+What the layer computes, as the GLM-5.3-Flash pages describe it:
+
+* The routed experts are stored weight-only NVFP4: 4-bit values with one scale
+  per group of 16 and one per-tensor global scale ("tenhkspark/GLM-5.3-Flash-
+  NVFP4-Wabi", Config expectations: group_size = 16, weight_scale_2; "GLM-5.3-
+  Flash on Blackwell", The quantization: the routed-expert tensors go to 4-bit).
+* Activations stay BF16 and there is no activation scale: the weight-only path
+  dequantises to BF16 and never consumes an input scale ("GLM-5.3-Flash on
+  Blackwell", The model loaded, served an API, and produced garbage).
+* Routers are BF16 linears whose logits are an input here (same page, The
+  quantization: the routers stay BF16).
+
+Value formats (public definitions, decoded from bit fields here):
+* E2M1 (OCP Microscaling Formats v1.0, FP4): sign bit 3, exponent bits 2..1
+  (bias 1), mantissa bit 0; exponent 0 is subnormal m*0.5.  Values
+  {0, 0.5, 1, 1.5, 2, 3, 4, 6} x sign.
+* E4M3 (OCP 8-bit Floating Point Specification): sign bit 7, exponent bits 6..3
+  (bias 7), mantissa bits 2..0; exponent 0 is subnormal (m/8)*2**-6;
+  S.1111.111 is NaN; there is no infinity; the largest value is 448.
+
+Readings where the pages are silent (each is listed with its reason in the
+design notes):
+* nibble order: element 2j is the low nibble of byte j;
+* scale groups run along K (the reduction axis) of each output row;
+* three FP32 tensor scales per expert (gate, up, down), applied after the dot
+  product;
+* top-k: larger logit first, equal logits -> lower expert index first, NaN
+  ranks below -inf;
+* routing weights: softmax over the k selected logits, no extra factor;
+* permutation: expert-major, ascending flattened index t*k+j inside an expert;
+* SwiGLU: h = silu(gate) * up with silu(z) = z / (1 + exp(-z));
+* combine: out[t] = sum_j w[t][j] * y[t, j], summed in slot order j = 0..k-1.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "decode_e2m1", "decode_e4m3", "unpack_e2m1_codes", "dequant", "dequant_scaled_f32",
+    "bf16_bits_to_f64", "route", "permute", "silu", "expert_ffn", "expert_hidden",
+    "moe_forward", "RouteResult",
+]
+
+
+# ----------------------------------------------------------------------------
+# Formats
+# ----------------------------------------------------------------------------
+
+def decode_e2m1(codes) -> np.ndarray:
+    """E2M1 code (0..15) -> float64, from the bit fields."""
+    c = np.asarray(codes).astype(np.int64)
+    s = (c >> 3) & 1
+    e = (c >> 1) & 3
+    m = c & 1
+    mag = np.where(e == 0, m * 0.5, (1.0 + m / 2.0) * np.exp2(e - 1.0))
+    return np.where(s == 1, -mag, mag)
+
+
+def decode_e4m3(b) -> np.ndarray:
+    """OCP E4M3 byte -> float64 (NaN for S.1111.111), from the bit fields."""
+    c = np.asarray(b).astype(np.int64)
+    s = (c >> 7) & 1
+    e = (c >> 3) & 15
+    m = c & 7
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return np.where(s == 1, -mag, mag)
+
+
+def unpack_e2m1_codes(q) -> np.ndarray:
+    """[N][K/2] bytes -> [N][K] codes; element 2j is the low nibble of byte j."""
+    q = np.asarray(q, dtype=np.uint8)
+    out = np.empty(q.shape[:-1] + (q.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = q & 0xF
+    out[..., 1::2] = q >> 4
+    return out
+
+
+def dequant(q, s) -> np.ndarray:
+    """W[n][k] = e2m1(code[n][k]) * e4m3(s[n][k // 16]) in float64 (exact).
+
+    The per-tensor FP32 scale is not included; the FFN applies it after the
+    dot product.
+    """
+    codes = unpack_e2m1_codes(q)
+    vals = decode_e2m1(codes)
+    scales = decode_e4m3(s)
+    return vals * np.repeat(scales, 16, axis=-1)
+
+
+def dequant_scaled_f32(q, s, g) -> np.ndarray:
+    """Dequantised weight including the tensor scale, as one FP32 product.
+
+    e2m1 * e4m3 has at most 5 significant bits and lies in [2**-10, 2688], so
+    it is exact in float32; the single float32 multiply by g (round to
+    nearest even) is the only rounding.  This is the quantity the library's
+    dequantisation check returns.
+    """
+    w = dequant(q, s).astype(np.float32)
+    return (w * np.float32(g)).astype(np.float32)
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """BF16 bit patterns -> float64 (exact)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+# ----------------------------------------------------------------------------
+# Route and permute
+# ----------------------------------------------------------------------------
+
+class RouteResult:
+    def __init__(self, ids, weights, nan_count):
+        self.ids = ids              # int32 [T][k]
+        self.weights = weights      # float64 [T][k]
+        self.nan_count = nan_count  # number of NaN logits seen
+
+
+def route(logits, k: int) -> RouteResult:
+    """Top-k of each token's router logits, then softmax over the k chosen.
+
+    Order: larger logit first; equal logits -> lower expert index first; NaN
+    ranks below every number including -inf.  Weights: exp(l_j - max) /
+    sum_i exp(l_i - max) over the selected logits, with NaN taken as -inf.  If
+    every selected logit is -inf/NaN the weights are 1/k each (the limit of
+    equal logits); if the largest is +inf, the +inf entries share weight 1.
+    """
+    L = np.asarray(logits, dtype=np.float64)
+    T, E = L.shape
+    if not 1 <= k <= E:
+        raise ValueError("top_k must be in 1..E")
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    nan = np.isnan(L)
+    idx = np.arange(E)
+    for t in range(T):
+        clean = np.where(nan[t], 0.0, L[t])
+        order = np.lexsort((idx, -clean, nan[t].astype(np.int8)))
+        sel = order[:k]
+        ids[t] = sel
+        ls = np.where(nan[t, sel], -np.inf, L[t, sel])
+        m = ls.max()
+        if m == -np.inf:
+            w[t] = 1.0 / k
+        elif m == np.inf:
+            hit = (ls == np.inf).astype(np.float64)
+            w[t] = hit / hit.sum()
+        else:
+            ex = np.exp(ls - m)
+            w[t] = ex / ex.sum()
+    return RouteResult(ids, w, int(nan.sum()))
+
+
+def permute(ids, num_experts: int):
+    """Expert-major stable order of the T*k routed rows.
+
+    Returns (counts [E], offsets [E+1], perm [T*k]) where perm[p] is the
+    flattened index t*k+j of the row at position p; inside one expert the
+    flattened indices ascend.
+    """
+    flat = np.asarray(ids, dtype=np.int64).reshape(-1)
+    counts = np.bincount(flat, minlength=num_experts).astype(np.int32)
+    offsets = np.zeros(num_experts + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(counts)
+    perm = np.argsort(flat, kind="stable").astype(np.int32)
+    return counts, offsets, perm
+
+
+# ----------------------------------------------------------------------------
+# Expert FFN and the layer
+# ----------------------------------------------------------------------------
+
+def silu(z):
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def _expert_mats(w, e):
+    I = w.w13_q.shape[1] // 2
+    wg = dequant(w.w13_q[e, :I], w.w13_s[e, :I])
+    wu = dequant(w.w13_q[e, I:], w.w13_s[e, I:])
+    wd = dequant(w.w2_q[e], w.w2_s[e])
+    gs = w.gscale[e].astype(np.float64)
+    return wg, wu, wd, gs
+
+
+def expert_hidden(w, e: int, x) -> np.ndarray:
+    """h = silu(gs_g * Wg x) * (gs_u * Wu x) for the rows of x [m][H], float64."""
+    wg, wu, _, gs = _expert_mats(w, e)
+    x = np.asarray(x, dtype=np.float64)
+    return silu(gs[0] * (x @ wg.T)) * (gs[1] * (x @ wu.T))
+
+
+def expert_ffn(w, e: int, x) -> np.ndarray:
+    """FFN_e(x) = gs_d * Wd (silu(gs_g * Wg x) * (gs_u * Wu x)) for x [m][H]."""
+    wg, wu, wd, gs = _expert_mats(w, e)
+    x = np.asarray(x, dtype=np.float64)
+    h = silu(gs[0] * (x @ wg.T)) * (gs[1] * (x @ wu.T))
+    return gs[2] * (h @ wd.T)
+
+
+def moe_forward(logits, x_bits, weights, k: int, tokens=None, return_parts=False):
+    """out[t] = sum_{j<k} w[t][j] * FFN_{ids[t][j]}(x[t]) in float64.
+
+    logits [T][E] (float32 or float64), x_bits [T][H] BF16 bit patterns,
+    weights an ExpertWeights-like object with w13_q/w13_s/w2_q/w2_s/gscale.
+    tokens: optional subset of token indices (the output has one row per
+    listed token, in that order).  With return_parts, also returns the route
+    result and the per-slot expert outputs y [len(tokens)][k][H].
+    """
+    logits = np.asarray(logits)
+    T = logits.shape[0]
+    tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    r = route(logits[tok], k)
+    x = bf16_bits_to_f64(np.asarray(x_bits)[tok])
+    H = x.shape[1]
+    y = np.zeros((len(tok), k, H), dtype=np.float64)
+    for e in np.unique(r.ids):
+        rows, slots = np.nonzero(r.ids == e)
+        y[rows, slots] = expert_ffn(weights, int(e), x[rows])
+    out = np.zeros((len(tok), H), dtype=np.float64)
+    for j in range(k):
+        out += r.weights[:, j:j + 1] * y[:, j]
+    if return_parts:
+        return out, r, y
+    return out

@@ -1,0 +1,427 @@
+"""Pins for the CPU oracle: it is checked against things other than itself.
+
+* value tables and hand-worked bytes from the public format specifications
+  (tests/golden/*.txt, each with its source);
+* an exhaustive comparison of the E4M3 decoder with torch's float8_e4m3fn
+  conversion (a library routine);
+* a round trip through the independent NVFP4 encoder in synth/;
+* brute-force top-k and permutation with Python's sorted();
+* closed forms of the expert FFN (all-ones and an asymmetric gate/up case);
+* invariants: identical experts make routing irrelevant, top-1 routing reduces
+  to one dense FFN (checked with torch float64 matmuls on an independently
+  written table decode);
+* a scalar-loop brute force of the whole layer on tiny shapes.
+
+The mutation test at the end plants plausible mistakes in the oracle (on the
+CPU) and checks that at least one pin catches each.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import oracle.nvfp4_moe_oracle as OM
+from synth import quantize_nvfp4, make_inputs, CONFIGS, LayerConfig, make_layer_weights
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------------------
+# independent decoders used only by the pins (table + torch library routine)
+# ---------------------------------------------------------------------------
+
+def _e2m1_table():
+    return np.array([float(v) for _, v in _read_golden("e2m1_values.txt")], dtype=np.float64)
+
+
+def _torch_e4m3(b):
+    t = torch.from_numpy(np.ascontiguousarray(b, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def _indep_dequant(q, s):
+    """Table lookup for E2M1 + torch for E4M3; nibble order as documented."""
+    tab = _e2m1_table()
+    q = np.asarray(q, dtype=np.uint8)
+    lo, hi = tab[q & 15], tab[q >> 4]
+    vals = np.stack([lo, hi], axis=-1).reshape(q.shape[:-1] + (q.shape[-1] * 2,))
+    sc = _torch_e4m3(s)
+    return vals * np.repeat(sc, 16, axis=-1)
+
+
+class _W:
+    def __init__(self, w13_q, w13_s, w2_q, w2_s, gscale):
+        self.w13_q, self.w13_s, self.w2_q, self.w2_s, self.gscale = w13_q, w13_s, w2_q, w2_s, gscale
+
+
+def _random_weights(rng, E, H, I):
+    return _W(rng.integers(0, 256, (E, 2 * I, H // 2), dtype=np.uint8),
+              rng.integers(0x20, 0x48, (E, 2 * I, H // 16), dtype=np.uint8),
+              rng.integers(0, 256, (E, H, I // 2), dtype=np.uint8),
+              rng.integers(0x20, 0x48, (E, H, I // 16), dtype=np.uint8),
+              rng.uniform(0.001, 0.01, (E, 3)).astype(np.float32))
+
+
+def _bf16_bits(a):
+    from synth import f32_to_bf16_bits
+    return f32_to_bf16_bits(np.asarray(a, dtype=np.float32))
+
+
+# ---------------------------------------------------------------------------
+# the pin battery (each raises AssertionError on failure)
+# ---------------------------------------------------------------------------
+
+def pin_e2m1_table(o):
+    got = o.decode_e2m1(np.arange(16))
+    want = _e2m1_table()
+    assert np.array_equal(got, want), (got, want)
+    assert np.array_equal(np.signbit(got), np.signbit(want))
+
+
+def pin_e4m3(o):
+    for b, v in _read_golden("e4m3_worked.txt"):
+        got = float(o.decode_e4m3(int(b, 16)))
+        want = float(v)
+        if math.isnan(want):
+            assert math.isnan(got), b
+        else:
+            assert got == want and math.copysign(1, got) == math.copysign(1, want), (b, got, want)
+    allb = np.arange(256, dtype=np.uint8)
+    got = o.decode_e4m3(allb)
+    ref = _torch_e4m3(allb)
+    both_nan = np.isnan(got) & np.isnan(ref)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[~both_nan], ref[~both_nan])
+    assert set(np.nonzero(np.isnan(got))[0].tolist()) == {0x7F, 0xFF}
+    pos = got[:0x7F]
+    assert np.all(np.diff(pos) > 0)
+
+
+def pin_dequant_worked(o):
+    for byte, sc, g, e0, e1 in _read_golden("dequant_worked.txt"):
+        q = np.zeros((1, 8), np.uint8)
+        q[0, 0] = int(byte, 16)
+        s = np.array([[int(sc, 16)]], np.uint8)
+        got = o.dequant_scaled_f32(q, s, np.float32(float(g)))
+        assert got[0, 0] == np.float32(float(e0)) and got[0, 1] == np.float32(float(e1)), (byte, got[0, :2])
+        assert np.all(got[0, 2:] == 0)
+
+
+def pin_round_trip(o):
+    rng = np.random.default_rng(7)
+    n, k = 24, 64
+    codes = rng.integers(0, 16, (n, k), dtype=np.uint8)
+    # every 16-block holds a +-6 element so its amax/6 is its scale exactly
+    for r in range(n):
+        for b in range(k // 16):
+            codes[r, b * 16 + rng.integers(0, 16)] = rng.choice([7, 15])
+    q = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    # positive, non-zero, non-NaN scale codes, one block at 448 so g == 1
+    s = rng.integers(0x01, 0x7F, (n, k // 16), dtype=np.uint8)
+    s[0, 0] = 0x7E
+    w = o.dequant(q, s).astype(np.float32)
+    q2, s2, g = quantize_nvfp4(w)
+    assert g == np.float32(1.0)
+    assert np.array_equal(s2, s)
+    assert np.array_equal(q2, q)
+
+
+def _brute_topk(row, k):
+    key = []
+    for e, v in enumerate(row.tolist()):
+        rank = (1, 0.0) if math.isnan(v) else (0, -v)
+        key.append((rank, e))
+    return [e for _, e in sorted(key)[:k]]
+
+
+def pin_route(o):
+    rng = np.random.default_rng(3)
+    T, E = 40, 16
+    L = np.round(rng.standard_normal((T, E)) * 2) / 2    # many ties
+    L[3, :] = 0.25                                       # all equal
+    L[5, 2] = np.nan
+    L[6, [1, 4]] = -np.inf
+    for k in (1, 2, 5, 16):
+        r = o.route(L.astype(np.float32), k)
+        for t in range(T):
+            assert r.ids[t].tolist() == _brute_topk(L[t], k), (t, k)
+            ls = L[t, r.ids[t]]
+            ls = np.where(np.isnan(ls), -np.inf, ls)
+            ex = np.array([math.exp(v - ls.max()) for v in ls])
+            assert np.allclose(r.weights[t], ex / ex.sum(), rtol=1e-15, atol=0)
+        if k == 1:
+            assert np.all(r.weights == 1.0)
+    r = o.route(np.full((2, 8), 1.5, np.float32), 4)
+    assert r.ids.tolist() == [[0, 1, 2, 3]] * 2 and np.all(r.weights == 0.25)
+    r = o.route(np.array([[1.0, np.nan, 3.0, np.nan]], np.float32), 3)
+    assert r.ids.tolist() == [[2, 0, 1]] and r.nan_count == 2
+    w = r.weights[0]
+    assert w[2] == 0.0 and abs(w[0] - 1 / (1 + math.exp(-2))) < 1e-15
+
+
+def pin_permute(o):
+    rng = np.random.default_rng(11)
+    for T, k, E in ((1, 1, 4), (7, 3, 5), (33, 4, 9)):
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        cnt, off, perm = o.permute(ids, E)
+        flat = ids.reshape(-1).tolist()
+        want = [i for e in range(E) for i in range(T * k) if flat[i] == e]
+        assert perm.tolist() == want
+        assert off[-1] == T * k and off[0] == 0
+        assert cnt.tolist() == [flat.count(e) for e in range(E)]
+        assert sorted(perm.tolist()) == list(range(T * k))
+
+
+def _const_expert(H, I, gate_code, up_code, down_code, scale_code, gs):
+    w13_q = np.zeros((1, 2 * I, H // 2), np.uint8)
+    w13_q[0, :I] = gate_code | (gate_code << 4)
+    w13_q[0, I:] = up_code | (up_code << 4)
+    w2_q = np.full((1, H, I // 2), down_code | (down_code << 4), np.uint8)
+    return _W(w13_q, np.full((1, 2 * I, H // 16), scale_code, np.uint8),
+              w2_q, np.full((1, H, I // 16), scale_code, np.uint8),
+              np.array([gs], np.float32))
+
+
+def pin_ffn_closed_form(o):
+    # all-ones: every code 0x1 (0.5), scale 0x38 (1.0), g = 1, x = 1
+    H, I = 256, 512
+    w = _const_expert(H, I, 0x1, 0x1, 0x1, 0x38, [1.0, 1.0, 1.0])
+    y = o.expert_ffn(w, 0, np.ones((1, H)))
+    assert np.all(y == 2.0 ** 22), y[0, :4]
+    # asymmetric: gate -0.5*0.125, up 3*0.5, down 2*0.25; x = 1/64
+    H, I = 64, 32
+    w = _const_expert(H, I, 0x9, 0x5, 0x4, 0x38, [0.125, 0.5, 0.25])
+    x = np.full((1, H), 1.0 / 64)
+    g = 0.125 * (-0.5 * H / 64)
+    u = 0.5 * (3.0 * H / 64)
+    h = g / (1 + math.exp(-g)) * u
+    want = 0.25 * 2.0 * I * h
+    y = o.expert_ffn(w, 0, x)
+    assert np.allclose(y, want, rtol=1e-14, atol=0), (y[0, 0], want)
+
+
+def pin_identical_experts(o):
+    rng = np.random.default_rng(5)
+    E, H, I, T, k = 6, 32, 48, 5, 3
+    one = _random_weights(rng, 1, H, I)
+    w = _W(*(np.repeat(a, E, axis=0) for a in (one.w13_q, one.w13_s, one.w2_q, one.w2_s, one.gscale)))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    xb = _bf16_bits(rng.standard_normal((T, H)))
+    out = o.moe_forward(logits, xb, w, k)
+    ref = o.expert_ffn(w, 0, o.bf16_bits_to_f64(xb))
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def pin_top1_dense(o):
+    rng = np.random.default_rng(9)
+    E, H, I, T = 5, 48, 32, 7
+    w = _random_weights(rng, E, H, I)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    xb = _bf16_bits(rng.standard_normal((T, H)))
+    out = o.moe_forward(logits, xb, w, 1)
+    x = torch.from_numpy((xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+    for t in range(T):
+        e = int(np.argmax(logits[t]))
+        wg = torch.from_numpy(_indep_dequant(w.w13_q[e, :I], w.w13_s[e, :I]))
+        wu = torch.from_numpy(_indep_dequant(w.w13_q[e, I:], w.w13_s[e, I:]))
+        wd = torch.from_numpy(_indep_dequant(w.w2_q[e], w.w2_s[e]))
+        gs = [float(v) for v in w.gscale[e]]
+        h = torch.nn.functional.silu(gs[0] * (wg @ x[t])) * (gs[1] * (wu @ x[t]))
+        y = gs[2] * (wd @ h)
+        assert np.allclose(out[t], y.numpy(), rtol=1e-12, atol=1e-12 * float(y.abs().max()))
+
+
+def pin_brute_force_layer(o):
+    rng = np.random.default_rng(13)
+    E, H, I, T, k = 4, 32, 32, 3, 2
+    w = _random_weights(rng, E, H, I)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    xb = _bf16_bits(rng.standard_normal((T, H)))
+    out = o.moe_forward(logits, xb, w, k)
+    tab = _e2m1_table()
+    sc = lambda b: float(_torch_e4m3(np.array([b], np.uint8))[0])
+    nib = lambda q, n, kk: (int(q[n, kk // 2]) >> (4 * (kk % 2))) & 15
+    W = lambda q, s, n, kk: tab[nib(q, n, kk)] * sc(s[n, kk // 16])
+    for t in range(T):
+        xs = [float(v) for v in (xb[t].astype(np.uint32) << 16).view(np.float32)]
+        row = [float(v) for v in logits[t]]
+        chosen = sorted(range(E), key=lambda e: (-row[e], e))[:k]
+        mx = max(row[e] for e in chosen)
+        den = sum(math.exp(row[e] - mx) for e in chosen)
+        acc = [0.0] * H
+        for e in chosen:
+            wt = math.exp(row[e] - mx) / den
+            gs = [float(v) for v in w.gscale[e]]
+            hv = []
+            for n in range(I):
+                g = gs[0] * sum(W(w.w13_q[e], w.w13_s[e], n, kk) * xs[kk] for kk in range(H))
+                u = gs[1] * sum(W(w.w13_q[e], w.w13_s[e], I + n, kk) * xs[kk] for kk in range(H))
+                hv.append(g / (1 + math.exp(-g)) * u)
+            for d in range(H):
+                yd = gs[2] * sum(W(w.w2_q[e], w.w2_s[e], d, n) * hv[n] for n in range(I))
+                acc[d] += wt * yd
+        assert np.allclose(out[t], acc, rtol=1e-12, atol=1e-12 * max(abs(a) for a in acc))
+
+
+PINS = [pin_e2m1_table, pin_e4m3, pin_dequant_worked, pin_round_trip, pin_route,
+        pin_permute, pin_ffn_closed_form, pin_identical_experts, pin_top1_dense,
+        pin_brute_force_layer]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_pin(pin):
+    pin(OM)
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: each must be caught by at least one pin
+# ---------------------------------------------------------------------------
+
+def _mut_nibble_order(m):
+    orig = m.unpack_e2m1_codes
+    def f(q):
+        c = orig(q)
+        out = c.copy()
+        out[..., 0::2], out[..., 1::2] = c[..., 1::2], c[..., 0::2]
+        return out
+    m.unpack_e2m1_codes = f
+
+
+def _mut_e4m3_bias(m):
+    orig = m.decode_e4m3
+    m.decode_e4m3 = lambda b: orig(b) * 0.5
+
+
+def _mut_e2m1_subnormal(m):
+    orig = m.decode_e2m1
+    def f(c):
+        v = orig(c)
+        cc = np.asarray(c).astype(np.int64)
+        return np.where((cc & 7) == 1, np.sign(v) * 1.0, v)
+    m.decode_e2m1 = f
+
+
+def _mut_scale_group_shift(m):
+    orig_d = m.decode_e4m3
+    def deq(q, s):
+        codes = m.unpack_e2m1_codes(q)
+        vals = m.decode_e2m1(codes)
+        sc = np.roll(orig_d(s), 1, axis=-1)
+        return vals * np.repeat(sc, 16, axis=-1)
+    m.dequant = deq
+
+
+def _mut_gate_up_swap(m):
+    orig = m._expert_mats
+    def f(w, e):
+        wg, wu, wd, gs = orig(w, e)
+        return wu, wg, wd, gs[[1, 0, 2]]
+    m._expert_mats = f
+
+
+def _mut_drop_up_scale(m):
+    orig = m._expert_mats
+    def f(w, e):
+        wg, wu, wd, gs = orig(w, e)
+        gs = gs.copy(); gs[1] = 1.0
+        return wg, wu, wd, gs
+    m._expert_mats = f
+
+
+def _mut_tie_break(m):
+    orig = m.route
+    def f(logits, k):
+        L = np.asarray(logits)[:, ::-1]
+        r = orig(L, k)
+        r.ids = (L.shape[1] - 1 - r.ids).astype(np.int32)
+        return r
+    m.route = f
+
+
+def _mut_softmax_all(m):
+    orig = m.route
+    def f(logits, k):
+        r = orig(logits, k)
+        L = np.asarray(logits, dtype=np.float64)
+        ex = np.exp(L - L.max(axis=1, keepdims=True))
+        full = ex / ex.sum(axis=1, keepdims=True)
+        r.weights = np.take_along_axis(full, r.ids.astype(np.int64), axis=1)
+        return r
+    m.route = f
+
+
+def _mut_no_combine_weights(m):
+    orig = m.route
+    def f(logits, k):
+        r = orig(logits, k)
+        r.weights = np.ones_like(r.weights)
+        return r
+    m.route = f
+
+
+def _mut_silu_sign(m):
+    m.silu = lambda z: z / (1.0 + np.exp(z))
+
+
+def _mut_perm_unstable(m):
+    orig = m.permute
+    def f(ids, E):
+        c, o, p = orig(ids, E)
+        p = p.copy()
+        for e in range(E):
+            p[o[e]:o[e + 1]] = p[o[e]:o[e + 1]][::-1]
+        return c, o, p
+    m.permute = f
+
+
+MUTANTS = [_mut_nibble_order, _mut_e4m3_bias, _mut_e2m1_subnormal, _mut_scale_group_shift,
+           _mut_gate_up_swap, _mut_drop_up_scale, _mut_tie_break, _mut_softmax_all,
+           _mut_no_combine_weights, _mut_silu_sign, _mut_perm_unstable]
+
+
+@pytest.mark.parametrize("mutant", MUTANTS, ids=lambda f: f.__name__)
+def test_planted_mistake_is_caught(mutant, monkeypatch):
+    class Patcher:
+        def __setattr__(self, name, value):
+            monkeypatch.setattr(OM, name, value)
+
+        def __getattr__(self, name):
+            return getattr(OM, name)
+    mutant(Patcher())
+    caught = []
+    for pin in PINS:
+        try:
+            pin(OM)
+        except Exception as exc:  # an exception of any kind counts as caught
+            caught.append((pin.__name__, type(exc).__name__))
+    assert caught, f"{mutant.__name__} passed every pin"
+
+
+# ---------------------------------------------------------------------------
+# the input generator itself (inputs only, not the method)
+# ---------------------------------------------------------------------------
+
+def test_generator_is_deterministic_and_shared():
+    a = make_inputs("tiny")
+    b = make_inputs("tiny")
+    assert np.array_equal(a.logits, b.logits) and np.array_equal(a.x_bits, b.x_bits)
+    w1 = make_layer_weights(CONFIGS["tiny"])
+    assert w1.w13_q.shape == (8, 1024, 128) and w1.w2_s.shape == (8, 256, 32)
+    # the tensor scale is amax/(6*448): some block of each tensor hits scale 448
+    for e in range(8):
+        I = 512
+        assert np.any(w1.w13_s[e, :I] == 0x7E) and np.any(w1.w13_s[e, I:] == 0x7E)
+        assert np.any(w1.w2_s[e] == 0x7E)
