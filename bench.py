@@ -1,0 +1,391 @@
+"""Benchmark of the NVFP4 W4A16 MoE layer on GB300 (one JSON line on stdout).
+
+Workload: the 2-token MTP decode step of the GLM-5.3-Flash routed-expert layer
+(128 experts, hidden 4096, expert intermediate 1536, top-8, 1 token + 1
+speculative token), synthetic seeded inputs (synth/).  A step is one call of
+nvfp4_moe_forward: route -> permute -> gate/up GEMV + SwiGLU -> down GEMV ->
+weighted combine.
+
+Measured:
+* value: tokens/s with inputs resident in HBM; each step is one replay of a
+  CUDA graph holding one forward, timed with CUDA events on the launching
+  stream; L2 is flushed (256 MiB write) before every step, outside the events;
+* e2e: the same metric through the C ABI with the step's inputs copied from
+  pinned host memory and the output read back, all inside the events;
+* roofline: the gate/up GEMV (the kernel that streams 2/3 of the weight
+  bytes), algorithmic bytes per launch / its CUDA-event duration, against the
+  measured HBM copy bandwidth;
+* cpu_baseline: the float64 CPU oracle on a bounded sample of the same step.
+--impl reference times the oracle alone (the CPU reference arm).
+Multi-GPU: replicas only (one independent layer per rank, no collective in
+the data path); value is the tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s; decode weight GB/s & prefill TFLOP/s as % of GB300 roofline"
+WORKLOAD = "decode_mtp"
+FLUSH_BYTES = 256 << 20
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "decode_gemv_gateup_decode_mtp.json")
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _workload_desc(cfg):
+    return (f"{cfg.name}: E{cfg.num_experts} H{cfg.hidden} I{cfg.inter} top{cfg.top_k} T{cfg.tokens}, "
+            f"NVFP4 (E2M1 + E4M3/16 + FP32/tensor) experts, BF16 activations")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+_ORACLE_CHILD = r"""
+import sys, time, json, numpy as np
+sys.path.insert(0, sys.argv[1])
+import oracle
+d = np.load(sys.argv[2])
+E, k = int(d["E"]), int(d["k"])
+class W: pass
+w = W()
+w.w13_q = np.zeros((E,) + d["w13_q"].shape[1:], np.uint8); w.w13_s = np.zeros((E,) + d["w13_s"].shape[1:], np.uint8)
+w.w2_q = np.zeros((E,) + d["w2_q"].shape[1:], np.uint8); w.w2_s = np.zeros((E,) + d["w2_s"].shape[1:], np.uint8)
+w.gscale = np.ones((E, 3), np.float32)
+for i, e in enumerate(d["experts"]):
+    w.w13_q[e], w.w13_s[e], w.w2_q[e], w.w2_s[e], w.gscale[e] = d["w13_q"][i], d["w13_s"][i], d["w2_q"][i], d["w2_s"][i], d["gscale"][i]
+logits, x = d["logits"], d["x_bits"]
+mode, steps, warm = sys.argv[3], int(sys.argv[4]), int(sys.argv[5])
+times = []
+if mode == "baseline":
+    for _ in range(2):
+        t0 = time.perf_counter(); oracle.moe_forward(logits, x, w, k); times.append(time.perf_counter() - t0)
+else:
+    # one step = one routed row: route its token, run that expert's FFN, weight it
+    T = logits.shape[0]
+    xs = oracle.bf16_bits_to_f64(x)
+    for s in range(warm + steps):
+        t, j = s % T, (s // T) % k
+        t0 = time.perf_counter()
+        r = oracle.route(logits[t:t + 1], k)
+        y = r.weights[0, j] * oracle.expert_ffn(w, int(r.ids[0, j]), xs[t:t + 1])
+        dt = time.perf_counter() - t0
+        if s >= warm: times.append(dt)
+print(json.dumps({"times": times}))
+"""
+
+
+def _oracle_sample_file(inp, ids):
+    experts = np.unique(ids.reshape(-1))
+    w = inp.weights
+    fd, path = tempfile.mkstemp(suffix=".npz")
+    os.close(fd)
+    np.savez(path, E=inp.config.num_experts, k=inp.config.top_k, experts=experts,
+             w13_q=w.w13_q[experts], w13_s=w.w13_s[experts], w2_q=w.w2_q[experts], w2_s=w.w2_s[experts],
+             gscale=w.gscale[experts], logits=inp.logits, x_bits=inp.x_bits)
+    return path
+
+
+def _run_oracle_child(path, mode, steps=0, warm=0):
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[v] = "1"
+    r = subprocess.run([sys.executable, "-c", _ORACLE_CHILD, ROOT, path, mode, str(steps), str(warm)],
+                       capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])["times"]
+
+
+def _host_route_ids(logits, k):
+    # expert choice for sizing the CPU sample: larger logit first, lower index on ties
+    order = np.lexsort((np.broadcast_to(np.arange(logits.shape[1]), logits.shape), -logits), axis=1)
+    return order[:, :k]
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from synth import make_inputs
+    inp = make_inputs(args.workload)
+    cfg = inp.config
+    path = _oracle_sample_file(inp, _host_route_ids(inp.logits, cfg.top_k))
+    try:
+        times = _run_oracle_child(path, "reference", args.steps, args.warmup)
+    finally:
+        os.unlink(path)
+    sec = sum(times)
+    value = args.steps / cfg.top_k / sec   # one routed row (1/k of a token) per step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded PCG64, shapes of the pages' MTP decode step)",
+        "config": {"workload": _workload_desc(cfg)},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "one routed row per step (route its token, one expert FFN, weight), "
+                                   "float64 numpy, 1 thread; tokens/s = rows/s / top_k"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.fh = None
+
+    def start(self):
+        try:
+            self.fh = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS),
+                                          "--format=csv,noheader,nounits", "-lms", "20", "-i", str(self.idx)],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.seek(0)
+        rows = [r.split(",") for r in self.fh.read().strip().splitlines() if r.count(",") == len(self.FIELDS) - 1]
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[3 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _traffic_for(kernel_src):
+    """DRAM traffic per launch from the committed ncu summary, if the kernel
+    source is unchanged since it was captured; else None."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            rec = json.load(f)
+        with open(kernel_src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if rec.get("source_sha256") == sha:
+            return rec.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import nvfp4_weight_only_w4a16_gb300 as pkg
+    from synth import make_inputs
+    pkg.build()
+    inp = make_inputs(args.workload)
+    cfg = inp.config
+    T, k, H, E = cfg.tokens, cfg.top_k, cfg.hidden, cfg.num_experts
+    layer = pkg.MoELayer(E, H, cfg.inter, T, k, device=dev.index)
+    pkg.upload_layer(layer, inp.weights, dev)
+
+    logits = torch.from_numpy(inp.logits).to(dev)
+    x = torch.from_numpy(inp.x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    ids, _, _, _ = layer.nvfp4_moe_debug_route(logits, T, k)
+    distinct = int(torch.unique(ids).numel())
+
+    def barrier():
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        layer.nvfp4_moe_forward(logits, x, k, out)
+    torch.cuda.synchronize()
+    st, _ = layer.nvfp4_moe_get_status()
+    if st != 0:
+        raise RuntimeError(f"device status {pkg.STATUS[st]} after warm-up")
+
+    # one forward captured into a CUDA graph (launch-overhead free replay)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.nvfp4_moe_forward(logits, x, k, out)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.1)
+
+    # --- timed region: K graph replays, L2 flushed before each ---
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    for s, e in evs:
+        flush.zero_()
+        s.record(stream)
+        graph.replay()
+        e.record(stream)
+    barrier()
+    step_ms = [s.elapsed_time(e) for s, e in evs]
+
+    # --- per-kernel durations for the roofline (direct calls, stage events) ---
+    layer.nvfp4_moe_set_profiling(True)
+    barrier()
+    for _ in range(args.steps):
+        flush.zero_()
+        layer.nvfp4_moe_forward(logits, x, k, out)
+    barrier()
+    stage_ms, nfwd = layer.nvfp4_moe_get_stage_times()
+    layer.nvfp4_moe_set_profiling(False)
+
+    # --- end to end through the C ABI with host buffers ---
+    h_logits = torch.from_numpy(inp.logits).pin_memory()
+    h_x = torch.from_numpy(inp.x_bits.view(np.int16)).pin_memory()
+    h_out = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    d_x16 = x.view(torch.int16)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    for s, e in e2e_ev:
+        flush.zero_()
+        s.record(stream)
+        logits.copy_(h_logits, non_blocking=True)
+        d_x16.copy_(h_x, non_blocking=True)
+        layer.nvfp4_moe_forward(logits, x, k, out)
+        h_out.copy_(out.view(torch.int16), non_blocking=True)
+        e.record(stream)
+    barrier()
+    e2e_ms = [s.elapsed_time(e) for s, e in e2e_ev]
+    clocks = sampler.stop()
+    st, _ = layer.nvfp4_moe_get_status()
+    if st != 0:
+        raise RuntimeError(f"device status {pkg.STATUS[st]} after the timed region")
+
+    ms = statistics.mean(step_ms)
+    ms_e2e = statistics.mean(e2e_ms)
+    if ws > 1:
+        t = torch.tensor([ms, ms_e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, ms_e2e = float(t[0]), float(t[1])
+    value = ws * T / (ms / 1e3)
+    value_e2e = ws * T / (ms_e2e / 1e3)
+
+    # roofline of the gate/up GEMV: weights of the touched experts + activations
+    I = cfg.inter
+    gateup_bytes = distinct * (2 * I * H // 2 + 2 * I * H // 16) + T * H * 2 + T * k * I * 2
+    gateup_ms = stage_ms[1] / max(nfwd, 1)
+    achieved = gateup_bytes / (gateup_ms / 1e3) / 1e9
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["hbm_gbs"])
+        peak_src = "measured"
+    except Exception:
+        peak, peak_src = 6800.0, "fallback"
+    traffic = _traffic_for(os.path.join(ROOT, "nvfp4_weight_only_w4a16_gb300", "csrc", "decode.cu"))
+    layer_bytes = distinct * cfg.expert_bytes + T * H * 2 * 2 + T * E * 4
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        path = _oracle_sample_file(inp, ids.cpu().numpy())
+        try:
+            times = _run_oracle_child(path, "baseline")
+        finally:
+            os.unlink(path)
+        cpu = {"value": T / statistics.mean(times), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"the whole {T}-token step ({T * k} expert FFNs + combine), twice, float64 numpy, 1 thread"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "w4a16: e2m1*e4m3 weights -> fp16 mma, fp32 accumulate",
+            "data": "synthetic (seeded PCG64, shapes of the pages' MTP decode step)",
+            "config": {"workload": _workload_desc(cfg), "distinct_experts": distinct,
+                       "layer_weight_bytes_per_step": layer_bytes,
+                       "layer_weight_gbs": layer_bytes / (ms / 1e3) / 1e9,
+                       "l2": "flushed before every step (256 MiB write, outside the step events)",
+                       "launch": "CUDA graph replay of one nvfp4_moe_forward",
+                       "parallelism": f"replicas x{ws}",
+                       "stage_ms": {"route_permute": stage_ms[0] / max(nfwd, 1), "gate_up": gateup_ms,
+                                    "down": stage_ms[2] / max(nfwd, 1), "combine": stage_ms[3] / max(nfwd, 1)}},
+            "roofline": {"bound": "hbm", "kernel": "decode_gemv_kernel<gate/up>", "achieved": achieved,
+                         "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
+                         "algorithmic_bytes": gateup_bytes, "traffic": traffic},
+            "e2e": {"value": value_e2e, "unit": "tokens/s", "h2d_bytes_per_step": T * E * 4 + T * H * 2,
+                    "d2h_bytes_per_step": T * H * 2},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    layer.close()
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * nvfp4_moe.h -- C ABI of the routed-expert MoE layer with weight-only NVFP4
+ * (W4A16) experts, for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The layer (one call of nvfp4_moe_forward):
+ *   route   : top-k of each token's router logits, weights = softmax over the
+ *             k chosen logits;
+ *   permute : group the T*k routed rows by expert (stable);
+ *   gate/up : g = gs_g * (Wg x), u = gs_u * (Wu x), h = silu(g) * u;
+ *   down    : y = gs_d * (Wd h);
+ *   combine : out[t] = sum_j w[t][j] * y[t, j], rounded once to BF16.
+ *
+ * Sources.  The experts are "weight-only NVFP4": 4-bit values, one scale per
+ * 16 weights and a per-tensor global scale ("tenhkspark/GLM-5.3-Flash-NVFP4-
+ * Wabi", Config expectations: group_size = 16, weight_scale_2; "GLM-5.3-Flash
+ * on Blackwell", The quantization).  Activations are BF16 and there is NO
+ * activation scale anywhere in this interface: a weight-only MoE path that
+ * consumes an input scale read an uninitialised 0.0 and zeroed every expert
+ * ("GLM-5.3-Flash on Blackwell", The model loaded, served an API, and produced
+ * garbage).  The 4-bit values are OCP MX E2M1, the group scales OCP E4M3.
+ *
+ * Conventions for every call:
+ *   - returns a status, never throws, never prints unless NVFP4_MOE_LOG=1;
+ *   - device pointers are CUDA global-memory pointers on the handle's device;
+ *     the caller keeps ownership of every pointer it passes;
+ *   - work is enqueued on `stream`; only calls documented as synchronous
+ *     wait for the GPU;
+ *   - shape and pointer errors are detected on the host, before any launch.
+ */
+#ifndef NVFP4_MOE_H_
+#define NVFP4_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nvfp4_moe_status {
+  NVFP4_MOE_OK = 0,
+  NVFP4_MOE_ERR_INVALID_ARG = 1,       /* null handle/pointer, bad enum, misaligned pointer */
+  NVFP4_MOE_ERR_UNSUPPORTED_SHAPE = 2, /* T, top_k, E, H or I outside the supported range   */
+  NVFP4_MOE_ERR_NOT_PACKED = 3,        /* forward before a successful pack                  */
+  NVFP4_MOE_ERR_WORKSPACE = 4,         /* device allocation failed in create                */
+  NVFP4_MOE_ERR_CUDA = 5,              /* a CUDA runtime call failed (see status string)    */
+  NVFP4_MOE_ERR_TIMEOUT = 6,           /* a bounded device-side wait gave up                */
+  NVFP4_MOE_ERR_BAD_SCALE = 7,         /* tensor scale <= 0, NaN or Inf                     */
+  NVFP4_MOE_ERR_NOT_IMPLEMENTED = 8,
+  NVFP4_MOE_ERR_DEVICE_CHECK = 9       /* a device-side bounds check fired                  */
+} nvfp4_moe_status;
+
+typedef enum nvfp4_moe_logits_dtype {
+  NVFP4_MOE_LOGITS_F32 = 0,
+  NVFP4_MOE_LOGITS_BF16 = 1
+} nvfp4_moe_logits_dtype;
+
+typedef enum nvfp4_moe_path {
+  NVFP4_MOE_PATH_AUTO = 0,     /* T <= decode_max_tokens -> decode, else prefill */
+  NVFP4_MOE_PATH_DECODE = 1,   /* grouped GEMV, dequantised in registers          */
+  NVFP4_MOE_PATH_PREFILL = 2   /* grouped tcgen05 GEMM, dequantised in shared mem */
+} nvfp4_moe_path;
+
+/* Layer shape and limits, fixed at create.
+ *   num_experts       E, 1..256
+ *   hidden            H, multiple of 128, 128..16384
+ *   inter             I (expert intermediate size), multiple of 128, 128..16384
+ *   max_tokens        largest T a forward may pass (sizes the workspace), >= 1
+ *   max_top_k         largest top_k a forward may pass, 1..min(E, 16)
+ *   decode_max_tokens T at or below which AUTO picks the decode path, 0..16
+ *   logits_dtype      nvfp4_moe_logits_dtype of router_logits
+ *   device            CUDA device ordinal the handle lives on                 */
+typedef struct nvfp4_moe_config {
+  int num_experts;
+  int hidden;
+  int inter;
+  int max_tokens;
+  int max_top_k;
+  int decode_max_tokens;
+  int logits_dtype;
+  int device;
+} nvfp4_moe_config;
+
+typedef struct nvfp4_moe* nvfp4_moe_t;
+
+/* Allocate a handle: the packed-weight blob (E * 3*H*I * 9/16 bytes) and the
+ * forward workspace (sized for max_tokens * max_top_k routed rows), both on
+ * config->device.  Synchronous.  *out is NULL on failure. */
+nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* config, nvfp4_moe_t* out);
+
+/* Copy the experts into the handle's device layout: for every 128 weight rows
+ * and 64-element K chunk, 4096 bytes of codes ordered so that each 16-byte
+ * vector holds two rows x 16 elements (one scale group each), followed
+ * elsewhere by the matching 512 bytes of scales; the gate and up rows are
+ * interleaved in groups of 8.  Loads of this layout are 16-byte vectorised
+ * and fully coalesced on both the decode and the prefill path.
+ * All inputs are DEVICE pointers in the canonical layout, per expert e:
+ *   w13_q [E][2I][H/2]  uint8  E2M1 codes, gate rows 0..I-1 then up rows
+ *                              I..2I-1, row-major over K = H; element 2j in the
+ *                              low nibble of byte j, element 2j+1 in the high
+ *   w13_s [E][2I][H/16] uint8  E4M3 scale of elements 16g..16g+15 of the row
+ *   w2_q  [E][H][I/2]   uint8  down projection, same rules with K = I
+ *   w2_s  [E][H][I/16]  uint8
+ *   gscale [E][3]       float  per-tensor scales (gate, up, down)
+ * Every gscale must be finite and > 0, else NVFP4_MOE_ERR_BAD_SCALE and the
+ * handle stays unpacked (this reads gscale back to the host: synchronous).
+ * Inputs may be freed once the call returns. */
+nvfp4_moe_status nvfp4_moe_pack(nvfp4_moe_t h, const uint8_t* w13_q, const uint8_t* w13_s,
+                                const uint8_t* w2_q, const uint8_t* w2_s, const float* gscale,
+                                cudaStream_t stream);
+
+/* One forward of the layer, enqueued on `stream`; no host synchronisation and
+ * no allocation, so the call can be captured into a CUDA graph.
+ *   router_logits [T][E]  float or BF16 (config.logits_dtype), device
+ *   x             [T][H]  BF16 activations, device, 16-byte aligned
+ *   out           [T][H]  BF16 result, device, 16-byte aligned
+ * 1 <= T <= max_tokens, 1 <= top_k <= max_top_k.  Ties between equal logits
+ * go to the lower expert index; a NaN logit ranks below -inf and is counted
+ * (see nvfp4_moe_get_status).  Concurrent forwards on one handle race on its
+ * workspace: serialise them on one stream. */
+nvfp4_moe_status nvfp4_moe_forward(nvfp4_moe_t h, const void* router_logits, int T, int top_k,
+                                   const void* x, void* out, cudaStream_t stream);
+
+/* Synchronous: waits for the device, then reports the device-side status word
+ * accumulated since the last call (and clears it).  Returns NVFP4_MOE_OK,
+ * NVFP4_MOE_ERR_TIMEOUT or NVFP4_MOE_ERR_DEVICE_CHECK; *nan_logits (may be
+ * NULL) receives the number of NaN router logits seen. */
+nvfp4_moe_status nvfp4_moe_get_status(nvfp4_moe_t h, uint32_t* nan_logits);
+
+/* Force a path (testing and measurement); AUTO by default.  The environment
+ * variable NVFP4_MOE_FORCE_PATH=decode|prefill sets the default at create. */
+nvfp4_moe_status nvfp4_moe_set_path(nvfp4_moe_t h, int path);
+
+/* Per-stage timing.  With profiling on, every forward records CUDA events on
+ * its stream before and after each stage.  nvfp4_moe_get_stage_times
+ * (synchronous) returns in ms[0..3] the summed milliseconds of route+permute,
+ * gate/up GEMM, down GEMM and combine over the forwards since profiling was
+ * switched on or last read, and their number in *count; then it starts over.
+ * Do not switch profiling on while capturing a CUDA graph. */
+nvfp4_moe_status nvfp4_moe_set_profiling(nvfp4_moe_t h, int on);
+nvfp4_moe_status nvfp4_moe_get_stage_times(nvfp4_moe_t h, float* ms, int* count);
+
+/* Static text for a status code. */
+const char* nvfp4_moe_status_string(nvfp4_moe_status s);
+
+/* Text of the last error seen on this handle (CUDA error name, failed check). */
+const char* nvfp4_moe_last_error(nvfp4_moe_t h);
+
+/* Free the handle and its device memory (synchronises the device first). */
+void nvfp4_moe_destroy(nvfp4_moe_t h);
+
+/* ---- inspection entry points (same ABI; used by the parity tests) ------- */
+
+/* Route and permute exactly as the forward of the chosen path does, into
+ * caller DEVICE buffers: ids [T][top_k] int32, weights [T][top_k] float,
+ * offsets [E+1] int32, perm [T*top_k] int32 (flattened index t*top_k+j of the
+ * routed row at each expert-major position). */
+nvfp4_moe_status nvfp4_moe_debug_route(nvfp4_moe_t h, const void* router_logits, int T, int top_k,
+                                       int32_t* ids, float* weights, int32_t* offsets,
+                                       int32_t* perm, cudaStream_t stream);
+
+/* Dequantise one tensor of one expert from the PACKED blob into a caller
+ * DEVICE buffer of float [N][K]: value = fp32(e2m1 * e4m3) * gscale, one
+ * FP32 rounding.  which: 0 gate [I][H], 1 up [I][H], 2 down [H][I]. */
+nvfp4_moe_status nvfp4_moe_debug_dequant(nvfp4_moe_t h, int expert, int which, float* w_out,
+                                         cudaStream_t stream);
+
+/* Copy the last forward's intermediates, in expert-major routed-row order
+ * (row p = perm position p), into caller DEVICE buffers:
+ *   hidden [T*top_k][I] BF16 (h = silu(g)*u, rounded to BF16),
+ *   y      [T*top_k][H] float (expert output before the routing weight). */
+nvfp4_moe_status nvfp4_moe_debug_intermediates(nvfp4_moe_t h, void* hidden, float* y,
+                                               cudaStream_t stream);
+
+/* Fault injection for the bounded-wait test: fault = 1 makes the prefill
+ * producer issue no copies, so the consumers' waits expire (after about 2 s),
+ * the kernels record NVFP4_MOE_ERR_TIMEOUT in the status word and return;
+ * the GPU context stays usable.  fault = 0 restores normal operation. */
+nvfp4_moe_status nvfp4_moe_debug_set_fault(nvfp4_moe_t h, int fault);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_MOE_H_ */

@@ -1,0 +1,204 @@
+"""ctypes binding of libnvfp4moe.so: argument marshalling only.
+
+Every function here turns torch tensors into device pointers and sizes and
+calls the C entry point of the same name; all arithmetic of the layer runs in
+the library's CUDA kernels.  There is no fallback: if the library cannot be
+loaded, or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+from .build import LIB, ROOT
+
+STATUS = {
+    0: "NVFP4_MOE_OK", 1: "NVFP4_MOE_ERR_INVALID_ARG", 2: "NVFP4_MOE_ERR_UNSUPPORTED_SHAPE",
+    3: "NVFP4_MOE_ERR_NOT_PACKED", 4: "NVFP4_MOE_ERR_WORKSPACE", 5: "NVFP4_MOE_ERR_CUDA",
+    6: "NVFP4_MOE_ERR_TIMEOUT", 7: "NVFP4_MOE_ERR_BAD_SCALE", 8: "NVFP4_MOE_ERR_NOT_IMPLEMENTED",
+    9: "NVFP4_MOE_ERR_DEVICE_CHECK",
+}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
+HEADER = os.path.join(ROOT, "include", "nvfp4_moe.h")
+
+
+class Nvfp4MoeError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("num_experts", ctypes.c_int), ("hidden", ctypes.c_int), ("inter", ctypes.c_int),
+                ("max_tokens", ctypes.c_int), ("max_top_k", ctypes.c_int),
+                ("decode_max_tokens", ctypes.c_int), ("logits_dtype", ctypes.c_int),
+                ("device", ctypes.c_int)]
+
+
+_lib = None
+
+
+def header_functions():
+    """Names of the functions include/nvfp4_moe.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"\b(nvfp4_moe_[a-z_0-9]+)\s*\(", text)))
+
+
+def load_library(path: str | None = None):
+    """Load libnvfp4moe.so (raises if it is missing or incomplete)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB
+    if not os.path.exists(p):
+        raise FileNotFoundError(f"{p} is missing: run __graft_entry__.build() (nvcc, sm_103a) first")
+    lib = ctypes.CDLL(p)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    sigs = {
+        "nvfp4_moe_create": (i, [ctypes.POINTER(Config), ctypes.POINTER(vp)]),
+        "nvfp4_moe_pack": (i, [vp, vp, vp, vp, vp, vp, vp]),
+        "nvfp4_moe_forward": (i, [vp, vp, i, i, vp, vp, vp]),
+        "nvfp4_moe_get_status": (i, [vp, ctypes.POINTER(ctypes.c_uint32)]),
+        "nvfp4_moe_set_path": (i, [vp, i]),
+        "nvfp4_moe_status_string": (ctypes.c_char_p, [i]),
+        "nvfp4_moe_last_error": (ctypes.c_char_p, [vp]),
+        "nvfp4_moe_destroy": (None, [vp]),
+        "nvfp4_moe_debug_route": (i, [vp, vp, i, i, vp, vp, vp, vp, vp]),
+        "nvfp4_moe_debug_dequant": (i, [vp, i, i, vp, vp]),
+        "nvfp4_moe_debug_intermediates": (i, [vp, vp, vp, vp]),
+        "nvfp4_moe_debug_set_fault": (i, [vp, i]),
+        "nvfp4_moe_set_profiling": (i, [vp, i]),
+        "nvfp4_moe_get_stage_times": (i, [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class MoELayer:
+    """One handle of the library (nvfp4_moe_create ... nvfp4_moe_destroy)."""
+
+    def __init__(self, num_experts, hidden, inter, max_tokens, max_top_k, decode_max_tokens=16,
+                 logits_bf16=False, device=0):
+        self.lib = load_library()
+        self.cfg = Config(num_experts, hidden, inter, max_tokens, max_top_k, decode_max_tokens,
+                          1 if logits_bf16 else 0, device)
+        self.E, self.H, self.I = num_experts, hidden, inter
+        self.device = device
+        h = ctypes.c_void_p()
+        st = self.lib.nvfp4_moe_create(ctypes.byref(self.cfg), ctypes.byref(h))
+        if st != 0:
+            raise Nvfp4MoeError(st, "nvfp4_moe_create: " + self.lib.nvfp4_moe_status_string(st).decode())
+        self.h = h
+
+    def _check(self, st, what):
+        if st != 0:
+            msg = self.lib.nvfp4_moe_last_error(self.h).decode()
+            raise Nvfp4MoeError(st, f"{what}: {msg}")
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.nvfp4_moe_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def nvfp4_moe_pack(self, w13_q, w13_s, w2_q, w2_s, gscale, stream=None):
+        st = self.lib.nvfp4_moe_pack(self.h, _ptr(w13_q), _ptr(w13_s), _ptr(w2_q), _ptr(w2_s),
+                                     _ptr(gscale), _stream(stream))
+        self._check(st, "nvfp4_moe_pack")
+
+    def nvfp4_moe_forward(self, logits, x, top_k, out, stream=None):
+        T = x.shape[0]
+        st = self.lib.nvfp4_moe_forward(self.h, _ptr(logits), T, top_k, _ptr(x), _ptr(out), _stream(stream))
+        self._check(st, "nvfp4_moe_forward")
+        return out
+
+    def nvfp4_moe_forward_raw(self, logits_ptr, T, top_k, x_ptr, out_ptr, stream_handle):
+        """Pointer-level call (for benchmarks that time the bare ABI)."""
+        return self.lib.nvfp4_moe_forward(self.h, ctypes.c_void_p(logits_ptr), T, top_k, ctypes.c_void_p(x_ptr),
+                                          ctypes.c_void_p(out_ptr), ctypes.c_void_p(stream_handle))
+
+    def nvfp4_moe_get_status(self):
+        n = ctypes.c_uint32(0)
+        st = self.lib.nvfp4_moe_get_status(self.h, ctypes.byref(n))
+        return st, int(n.value)
+
+    def nvfp4_moe_set_path(self, path):
+        self._check(self.lib.nvfp4_moe_set_path(self.h, path), "nvfp4_moe_set_path")
+
+    def nvfp4_moe_debug_route(self, logits, T, top_k, stream=None):
+        import torch
+        dev = logits.device
+        ids = torch.empty((T, top_k), dtype=torch.int32, device=dev)
+        w = torch.empty((T, top_k), dtype=torch.float32, device=dev)
+        off = torch.empty((self.E + 1,), dtype=torch.int32, device=dev)
+        perm = torch.empty((T * top_k,), dtype=torch.int32, device=dev)
+        st = self.lib.nvfp4_moe_debug_route(self.h, _ptr(logits), T, top_k, _ptr(ids), _ptr(w), _ptr(off),
+                                            _ptr(perm), _stream(stream))
+        self._check(st, "nvfp4_moe_debug_route")
+        return ids, w, off, perm
+
+    def nvfp4_moe_debug_dequant(self, expert, which, via_bf16=False, stream=None):
+        import torch
+        n, k = (self.H, self.I) if which == 2 else (self.I, self.H)
+        out = torch.empty((n, k), dtype=torch.float32, device=f"cuda:{self.device}")
+        st = self.lib.nvfp4_moe_debug_dequant(self.h, expert, which | (4 if via_bf16 else 0), _ptr(out),
+                                              _stream(stream))
+        self._check(st, "nvfp4_moe_debug_dequant")
+        return out
+
+    def nvfp4_moe_debug_intermediates(self, rows, stream=None):
+        import torch
+        hid = torch.empty((rows, self.I), dtype=torch.bfloat16, device=f"cuda:{self.device}")
+        y = torch.empty((rows, self.H), dtype=torch.float32, device=f"cuda:{self.device}")
+        st = self.lib.nvfp4_moe_debug_intermediates(self.h, _ptr(hid), _ptr(y), _stream(stream))
+        self._check(st, "nvfp4_moe_debug_intermediates")
+        return hid, y
+
+    def nvfp4_moe_set_profiling(self, on):
+        self._check(self.lib.nvfp4_moe_set_profiling(self.h, 1 if on else 0), "nvfp4_moe_set_profiling")
+
+    def nvfp4_moe_get_stage_times(self):
+        ms = (ctypes.c_float * 4)()
+        n = ctypes.c_int(0)
+        self._check(self.lib.nvfp4_moe_get_stage_times(self.h, ms, ctypes.byref(n)), "nvfp4_moe_get_stage_times")
+        return [float(v) for v in ms], int(n.value)
+
+    def nvfp4_moe_debug_set_fault(self, fault):
+        self._check(self.lib.nvfp4_moe_debug_set_fault(self.h, fault), "nvfp4_moe_debug_set_fault")
+
+
+def upload_layer(layer: MoELayer, weights, device="cuda:0"):
+    """Copy an ExpertWeights-like set of numpy arrays to the device and pack it."""
+    import torch
+    t = lambda a: torch.from_numpy(a).to(device)
+    layer.nvfp4_moe_pack(t(weights.w13_q), t(weights.w13_s), t(weights.w2_q), t(weights.w2_s), t(weights.gscale))
+    torch.cuda.synchronize()

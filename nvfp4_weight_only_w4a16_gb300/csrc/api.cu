@@ -1,0 +1,438 @@
+// C ABI of the NVFP4 W4A16 MoE layer: handle, validation, dispatch.
+// Every entry point returns a status and never throws; shape and pointer
+// errors are caught here, before anything is enqueued.
+#include <cstdio>
+#include <cstdlib>
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/nvfp4_moe.h"
+#include "kernels.h"
+
+using namespace nvfp4moe;
+
+struct nvfp4_moe {
+  nvfp4_moe_config cfg;
+  int path = NVFP4_MOE_PATH_AUTO;
+  int num_sms = 0;
+  bool packed = false;
+  bool log = false;
+  bool logged_path[3] = {false, false, false};
+  uint8_t* blob = nullptr;
+  float* gscale = nullptr;
+  void* ws_mem = nullptr;
+  size_t ws_bytes = 0;
+  Workspace ws{};
+  PrefillMaps maps{};
+  int last_T = 0, last_k = 0;
+  int fault = 0;
+  bool profiling = false;
+  std::vector<cudaEvent_t> ev_pool;  // 5 events per profiled forward
+  size_t ev_used = 0;
+  char last_error[256] = {0};
+};
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) changed = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+nvfp4_moe_status fail(nvfp4_moe* h, nvfp4_moe_status s, const std::string& msg) {
+  if (h) snprintf(h->last_error, sizeof(h->last_error), "%s", msg.c_str());
+  if (h && h->log) fprintf(stderr, "[nvfp4_moe] %s\n", msg.c_str());
+  return s;
+}
+
+nvfp4_moe_status cuda_fail(nvfp4_moe* h, cudaError_t e, const char* where) {
+  return fail(h, NVFP4_MOE_ERR_CUDA, std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2D BF16 [rows][cols] row-major, box = 64 columns x 16 rows, 128B swizzle.
+bool encode_rows_map(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Carver {
+  size_t off = 0;
+  std::vector<std::pair<void**, size_t>> items;
+  template <class T>
+  void add(T** p, size_t count) {
+    items.push_back({reinterpret_cast<void**>(p), count * sizeof(T)});
+  }
+  size_t layout() {
+    off = 0;
+    for (auto& it : items) off = ((off + 255) & ~size_t(255)) + it.second;
+    return off + 256;
+  }
+  void assign(uint8_t* base) {
+    size_t o = 0;
+    for (auto& it : items) {
+      o = (o + 255) & ~size_t(255);
+      *it.first = base + o;
+      o += it.second;
+    }
+  }
+};
+
+int choose_path(const nvfp4_moe* h, int T, int k) {
+  if (h->path != NVFP4_MOE_PATH_AUTO) return h->path;
+  return (T <= h->cfg.decode_max_tokens && T <= kDecodeMaxTokens && T * k <= kDecodeMaxTokens * 16)
+             ? NVFP4_MOE_PATH_DECODE
+             : NVFP4_MOE_PATH_PREFILL;
+}
+
+nvfp4_moe_status check_forward_args(nvfp4_moe* h, const void* logits, int T, int top_k, int path) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (!h->packed) return fail(h, NVFP4_MOE_ERR_NOT_PACKED, "forward before a successful pack");
+  if (!logits) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "router_logits is NULL");
+  if (!aligned(logits, h->cfg.logits_dtype == NVFP4_MOE_LOGITS_BF16 ? 2 : 4))
+    return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "router_logits misaligned");
+  if (T < 1 || T > h->cfg.max_tokens) return fail(h, NVFP4_MOE_ERR_UNSUPPORTED_SHAPE, "T outside 1..max_tokens");
+  if (top_k < 1 || top_k > h->cfg.max_top_k || top_k > h->cfg.num_experts)
+    return fail(h, NVFP4_MOE_ERR_UNSUPPORTED_SHAPE, "top_k outside 1..min(max_top_k, E)");
+  if (path == NVFP4_MOE_PATH_DECODE && (T > kDecodeMaxTokens))
+    return fail(h, NVFP4_MOE_ERR_UNSUPPORTED_SHAPE, "decode path takes at most 16 tokens");
+  return NVFP4_MOE_OK;
+}
+
+LayerDims dims_of(const nvfp4_moe* h) {
+  return LayerDims{h->cfg.num_experts, h->cfg.hidden, h->cfg.inter, h->cfg.logits_dtype == NVFP4_MOE_LOGITS_BF16};
+}
+
+nvfp4_moe_status run_route(nvfp4_moe* h, const void* logits, const void* x, int T, int k, int path,
+                           cudaStream_t st) {
+  const LayerDims d = dims_of(h);
+  cudaError_t e = path == NVFP4_MOE_PATH_DECODE ? launch_route_decode(d, logits, x, T, k, h->ws, st)
+                                                : launch_route_prefill(d, logits, x, T, k, h->ws, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "route launch");
+  return NVFP4_MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nvfp4_moe_status_string(nvfp4_moe_status s) {
+  switch (s) {
+    case NVFP4_MOE_OK: return "ok";
+    case NVFP4_MOE_ERR_INVALID_ARG: return "invalid argument";
+    case NVFP4_MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case NVFP4_MOE_ERR_NOT_PACKED: return "weights not packed";
+    case NVFP4_MOE_ERR_WORKSPACE: return "device allocation failed";
+    case NVFP4_MOE_ERR_CUDA: return "CUDA error";
+    case NVFP4_MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case NVFP4_MOE_ERR_BAD_SCALE: return "tensor scale is zero, negative, NaN or Inf";
+    case NVFP4_MOE_ERR_NOT_IMPLEMENTED: return "not implemented";
+    case NVFP4_MOE_ERR_DEVICE_CHECK: return "device-side bounds check fired";
+  }
+  return "unknown status";
+}
+
+const char* nvfp4_moe_last_error(nvfp4_moe_t h) { return h ? h->last_error : "null handle"; }
+
+nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* c, nvfp4_moe_t* out) {
+  if (!out) return NVFP4_MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!c) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (c->num_experts < 1 || c->num_experts > 256) return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->hidden < 128 || c->hidden > 16384 || c->hidden % 128) return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->inter < 128 || c->inter > 16384 || c->inter % 128) return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->max_tokens < 1 || c->max_tokens > (1 << 20)) return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->max_top_k < 1 || c->max_top_k > 16 || c->max_top_k > c->num_experts) return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->decode_max_tokens < 0 || c->decode_max_tokens > kDecodeMaxTokens) return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->logits_dtype != NVFP4_MOE_LOGITS_F32 && c->logits_dtype != NVFP4_MOE_LOGITS_BF16)
+    return NVFP4_MOE_ERR_INVALID_ARG;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || c->device < 0 || c->device >= ndev) return NVFP4_MOE_ERR_INVALID_ARG;
+
+  nvfp4_moe* h = new (std::nothrow) nvfp4_moe();
+  if (!h) return NVFP4_MOE_ERR_WORKSPACE;
+  h->cfg = *c;
+  const char* lg = getenv("NVFP4_MOE_LOG");
+  h->log = lg && lg[0] == '1';
+  const char* fp = getenv("NVFP4_MOE_FORCE_PATH");
+  if (fp && !strcmp(fp, "decode")) h->path = NVFP4_MOE_PATH_DECODE;
+  if (fp && !strcmp(fp, "prefill")) h->path = NVFP4_MOE_PATH_PREFILL;
+
+  DeviceGuard g(c->device);
+  cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+  const int E = c->num_experts, H = c->hidden, I = c->inter;
+  const size_t R = (size_t)c->max_tokens * c->max_top_k;
+  const size_t Rm = R < 256 ? 256 : R;
+  const size_t maxU = (size_t)std::min(E, kDecodeMaxTokens * c->max_top_k);
+  const size_t ncta = ((size_t)c->max_tokens + kRouteTokPerCta - 1) / kRouteTokPerCta;
+  const size_t max_tiles = R / kTileRows + E + 1;
+  const size_t blob_bytes = (size_t)E * expert_layout(H, I).stride;
+
+  Carver cv;
+  Workspace& w = h->ws;
+  cv.add(&w.ids, Rm);
+  cv.add(&w.wts, Rm);
+  cv.add(&w.offsets, E + 1);
+  cv.add(&w.perm, Rm);
+  cv.add(&w.inv, Rm);
+  cv.add(&w.tch_expert, E);
+  cv.add(&w.tch_row0, E);
+  cv.add(&w.tch_rows, E);
+  cv.add(&w.num_touched, 1);
+  cv.add(&w.x16, (size_t)kDecodeMaxTokens * H);
+  cv.add(&w.xexp, kDecodeMaxTokens);
+  cv.add(&w.h, Rm * I);
+  cv.add(&w.hmax, Rm);
+  cv.add(&w.y, Rm * H);
+  cv.add(&w.part_gu, maxU * (2 * I / 64) * 1024);
+  cv.add(&w.cnt_gu, maxU * (2 * I / 64));
+  cv.add(&w.part_dn, maxU * (H / 64) * 1024);
+  cv.add(&w.cnt_dn, maxU * (H / 64));
+  cv.add(&w.blk_counts, ncta * E);
+  cv.add(&w.blk_base, ncta * E);
+  cv.add(&w.x_perm, Rm * H);
+  cv.add(&w.tile_expert, max_tiles);
+  cv.add(&w.tile_row0, max_tiles);
+  cv.add(&w.tile_rows, max_tiles);
+  cv.add(&w.num_tiles, 1);
+  cv.add(&w.status, 1);
+  h->ws_bytes = cv.layout();
+
+  if (cudaMalloc(&h->blob, blob_bytes) != cudaSuccess || cudaMalloc(&h->gscale, sizeof(float) * 3 * E) != cudaSuccess ||
+      cudaMalloc(&h->ws_mem, h->ws_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    nvfp4_moe_destroy(h);
+    return NVFP4_MOE_ERR_WORKSPACE;
+  }
+  cv.assign(static_cast<uint8_t*>(h->ws_mem));
+  if (cudaMemset(h->ws_mem, 0, h->ws_bytes) != cudaSuccess) {
+    nvfp4_moe_destroy(h);
+    return NVFP4_MOE_ERR_CUDA;
+  }
+  if (!encode_rows_map(&h->maps.x_perm, w.x_perm, Rm, H) || !encode_rows_map(&h->maps.h, w.h, Rm, I)) {
+    nvfp4_moe_destroy(h);
+    return NVFP4_MOE_ERR_CUDA;
+  }
+  *out = h;
+  return NVFP4_MOE_OK;
+}
+
+void nvfp4_moe_destroy(nvfp4_moe_t h) {
+  if (!h) return;
+  {
+    DeviceGuard g(h->cfg.device);
+    cudaDeviceSynchronize();
+    for (cudaEvent_t ev : h->ev_pool) cudaEventDestroy(ev);
+    if (h->blob) cudaFree(h->blob);
+    if (h->gscale) cudaFree(h->gscale);
+    if (h->ws_mem) cudaFree(h->ws_mem);
+  }
+  delete h;
+}
+
+nvfp4_moe_status nvfp4_moe_set_path(nvfp4_moe_t h, int path) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (path < NVFP4_MOE_PATH_AUTO || path > NVFP4_MOE_PATH_PREFILL) return NVFP4_MOE_ERR_INVALID_ARG;
+  h->path = path;
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_moe_set_profiling(nvfp4_moe_t h, int on) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  h->profiling = on != 0;
+  h->ev_used = 0;
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_moe_get_stage_times(nvfp4_moe_t h, float* ms, int* count) {
+  if (!h || !ms || !count) return NVFP4_MOE_ERR_INVALID_ARG;
+  DeviceGuard g(h->cfg.device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(h, e, "get_stage_times");
+  for (int i = 0; i < 4; ++i) ms[i] = 0.f;
+  const int n = (int)(h->ev_used / 5);
+  for (int f = 0; f < n; ++f)
+    for (int i = 0; i < 4; ++i) {
+      float t = 0.f;
+      e = cudaEventElapsedTime(&t, h->ev_pool[5 * f + i], h->ev_pool[5 * f + i + 1]);
+      if (e != cudaSuccess) return cuda_fail(h, e, "get_stage_times elapsed");
+      ms[i] += t;
+    }
+  *count = n;
+  h->ev_used = 0;
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_moe_debug_set_fault(nvfp4_moe_t h, int fault) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (fault < 0 || fault > 1) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_set_fault: unknown fault");
+  h->fault = fault;
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_moe_pack(nvfp4_moe_t h, const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
+                                const uint8_t* w2_s, const float* gscale, cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (!w13_q || !w13_s || !w2_q || !w2_s || !gscale) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "pack: NULL input");
+  if (!aligned(w13_q, 16) || !aligned(w2_q, 16) || !aligned(w13_s, 4) || !aligned(w2_s, 4) || !aligned(gscale, 4))
+    return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "pack: misaligned input");
+  DeviceGuard g(h->cfg.device);
+  const int E = h->cfg.num_experts;
+  std::vector<float> gs((size_t)3 * E);
+  cudaError_t e = cudaMemcpyAsync(gs.data(), gscale, sizeof(float) * gs.size(), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "pack: reading gscale");
+  for (size_t i = 0; i < gs.size(); ++i) {
+    const float v = gs[i];
+    if (!(v > 0.0f) || v != v || v > 3.4e38f) {
+      h->packed = false;
+      return fail(h, NVFP4_MOE_ERR_BAD_SCALE,
+                  "pack: tensor scale " + std::to_string(i % 3) + " of expert " + std::to_string(i / 3) + " is not finite > 0");
+    }
+  }
+  e = cudaMemcpyAsync(h->gscale, gscale, sizeof(float) * gs.size(), cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = launch_pack(w13_q, w13_s, w2_q, w2_s, h->blob, E, h->cfg.hidden, h->cfg.inter, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "pack launch");
+  h->packed = true;
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_moe_forward(nvfp4_moe_t h, const void* logits, int T, int top_k, const void* x, void* out,
+                                   cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  const int path = choose_path(h, T, top_k);
+  nvfp4_moe_status s = check_forward_args(h, logits, T, top_k, path);
+  if (s != NVFP4_MOE_OK) return s;
+  if (!x || !out) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "x or out is NULL");
+  if (!aligned(x, 16) || !aligned(out, 16)) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "x or out not 16-byte aligned");
+  DeviceGuard g(h->cfg.device);
+  if (h->log && !h->logged_path[path]) {
+    h->logged_path[path] = true;
+    fprintf(stderr, "[nvfp4_moe] forward T=%d top_k=%d -> %s path\n", T, top_k,
+            path == NVFP4_MOE_PATH_DECODE ? "decode (grouped GEMV)" : "prefill (tcgen05 grouped GEMM)");
+  }
+  cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  if (h->profiling) {
+    for (int i = 0; i < 5; ++i) {
+      if (h->ev_used == h->ev_pool.size()) {
+        cudaEvent_t e0;
+        if (cudaEventCreate(&e0) != cudaSuccess) return cuda_fail(h, cudaGetLastError(), "event create");
+        h->ev_pool.push_back(e0);
+      }
+      ev[i] = h->ev_pool[h->ev_used++];
+    }
+    cudaEventRecord(ev[0], st);
+  }
+  s = run_route(h, logits, x, T, top_k, path, st);
+  if (s != NVFP4_MOE_OK) return s;
+  if (ev[1]) cudaEventRecord(ev[1], st);
+  const LayerDims d = dims_of(h);
+  cudaError_t e;
+  if (path == NVFP4_MOE_PATH_DECODE)
+    e = launch_decode_ffn(d, h->blob, h->gscale, T, top_k, ev[2], h->num_sms, h->ws, st);
+  else
+    e = launch_prefill_ffn(d, h->blob, h->gscale, T, top_k, h->num_sms, h->maps, h->ws, h->fault, ev[2], st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "expert FFN launch");
+  if (ev[3]) cudaEventRecord(ev[3], st);
+  e = launch_combine(d, T, top_k, h->ws, out, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "combine launch");
+  if (ev[4]) cudaEventRecord(ev[4], st);
+  h->last_T = T;
+  h->last_k = top_k;
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_moe_get_status(nvfp4_moe_t h, uint32_t* nan_logits) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  DeviceGuard g(h->cfg.device);
+  DeviceStatus ds{};
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&ds, h->ws.status, sizeof(ds), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(h->ws.status, 0, sizeof(ds));
+  if (e != cudaSuccess) return cuda_fail(h, e, "get_status");
+  if (nan_logits) *nan_logits = ds.nan_logits;
+  if (ds.flags & kFlagTimeout)
+    return fail(h, NVFP4_MOE_ERR_TIMEOUT, "device wait timed out at site " + std::to_string(ds.where));
+  if (ds.flags & kFlagBounds)
+    return fail(h, NVFP4_MOE_ERR_DEVICE_CHECK, "device bounds check at site " + std::to_string(ds.where));
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_moe_debug_route(nvfp4_moe_t h, const void* logits, int T, int top_k, int32_t* ids,
+                                       float* weights, int32_t* offsets, int32_t* perm, cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  const int path = choose_path(h, T, top_k);
+  nvfp4_moe_status s = check_forward_args(h, logits, T, top_k, path);
+  if (s != NVFP4_MOE_OK) return s;
+  if (!ids || !weights || !offsets || !perm) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_route: NULL output");
+  DeviceGuard g(h->cfg.device);
+  s = run_route(h, logits, nullptr, T, top_k, path, st);
+  if (s != NVFP4_MOE_OK) return s;
+  const size_t n = (size_t)T * top_k;
+  cudaError_t e = cudaMemcpyAsync(ids, h->ws.ids, n * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(weights, h->ws.wts, n * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(offsets, h->ws.offsets, (h->cfg.num_experts + 1) * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(perm, h->ws.perm, n * 4, cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "debug_route copy");
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_moe_debug_dequant(nvfp4_moe_t h, int expert, int which, float* w_out, cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (!h->packed) return fail(h, NVFP4_MOE_ERR_NOT_PACKED, "debug_dequant before pack");
+  const int base = which & 3, via_bf16 = (which >> 2) & 1;
+  if (expert < 0 || expert >= h->cfg.num_experts || base > 2 || (which & ~7) || !w_out)
+    return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_dequant: bad expert/which/out");
+  DeviceGuard g(h->cfg.device);
+  cudaError_t e = launch_debug_dequant(h->blob, h->gscale, h->cfg.hidden, h->cfg.inter, expert, base, via_bf16, w_out, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "debug_dequant launch");
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_moe_debug_intermediates(nvfp4_moe_t h, void* hidden, float* y, cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (!h->last_T) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_intermediates before any forward");
+  if (!hidden || !y) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_intermediates: NULL output");
+  DeviceGuard g(h->cfg.device);
+  const size_t n = (size_t)h->last_T * h->last_k;
+  cudaError_t e = cudaMemcpyAsync(hidden, h->ws.h, n * h->cfg.inter * 2, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(y, h->ws.y, n * h->cfg.hidden * 4, cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "debug_intermediates copy");
+  return NVFP4_MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,138 @@
+// Shared device helpers for the NVFP4 W4A16 MoE kernels (sm_103a).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+namespace nvfp4moe {
+
+// ---------------------------------------------------------------------------
+// Device status word (one per handle, in device memory).
+// ---------------------------------------------------------------------------
+struct DeviceStatus {
+  unsigned int flags;       // bit 0: bounded wait timed out, bit 1: bounds check fired
+  unsigned int nan_logits;  // NaN router logits seen
+  unsigned int where;       // first failing site (for the log)
+  unsigned int pad;
+};
+constexpr unsigned int kFlagTimeout = 1u;
+constexpr unsigned int kFlagBounds = 2u;
+
+__device__ __forceinline__ void report(DeviceStatus* st, unsigned int flag, unsigned int where) {
+  if (atomicOr(&st->flags, flag) == 0u) st->where = where;
+}
+
+// ---------------------------------------------------------------------------
+// Packed-weight layout constants.
+//   Matrix W [N][K], N % 128 == 0, K % 64 == 0.  A "chunk" is 64 K-elements.
+//   Nibbles: for row block rb (128 rows), chunk c, sub-block sb (16 rows),
+//   lane t (0..31): 16 bytes at ((rb*nch + c)*8 + sb)*512 + t*16 holding
+//     bytes 0..7 : row rb*128+sb*16+t/4,   K elements 64c+16(t%4) .. +15
+//     bytes 8..15: the row 8 below, same K elements
+//   (byte j of each half holds elements 2j / 2j+1 in its low / high nibble).
+//   Scales: 2 bytes at ((rb*nch + c)*8 + sb)*64 + t*2: the E4M3 scale of the
+//   two rows' 16-element group.
+//   The gate/up matrix is stored row-interleaved: packed row 16g+r is gate
+//   feature 8g+r for r < 8 and up feature 8g+r-8 for r >= 8.
+// ---------------------------------------------------------------------------
+constexpr int kChunk = 64;
+constexpr int kSegBytes = 16;
+constexpr int kBlockRows = 128;
+
+struct ExpertLayout {
+  // byte offsets inside one expert's blob
+  size_t w13_nib, w2_nib, w13_sc, w2_sc, stride;
+};
+
+__host__ __device__ inline ExpertLayout expert_layout(int H, int I) {
+  ExpertLayout L;
+  size_t n13 = (size_t)2 * I * H, n2 = (size_t)H * I;
+  L.w13_nib = 0;
+  L.w2_nib = n13 / 2;
+  L.w13_sc = L.w2_nib + n2 / 2;
+  L.w2_sc = L.w13_sc + n13 / 16;
+  L.stride = L.w2_sc + n2 / 16;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// Format conversions.  The E2M1 and E4M3 conversions use the hardware cvt
+// instructions of sm_100-family GPUs; the product e2m1 * e4m3 (at most 5
+// significant bits, magnitude in [2^-10, 2688]) is exact in FP16.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low_bits) {
+  uint32_t r;
+  asm("{\n .reg .b8 b;\n cvt.u8.u32 b, %1;\n cvt.rn.f16x2.e2m1x2 %0, b;\n}" : "=r"(r) : "r"(byte_in_low_bits));
+  return r;
+}
+
+// Two E4M3 bytes (lo = bits 0..7, hi = bits 8..15) -> f16x2 {lo, hi}.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t r;
+  unsigned short s = (unsigned short)two_bytes;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(s));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// {x.lo, x.lo} and {x.hi, x.hi}
+__device__ __forceinline__ uint32_t dup_lo(uint32_t x) { return __byte_perm(x, 0, 0x1010); }
+__device__ __forceinline__ uint32_t dup_hi(uint32_t x) { return __byte_perm(x, 0, 0x3232); }
+
+// f16x2 (exact dequantised values) -> bf16x2, exact for these values.
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t v) {
+  __half2 h = *reinterpret_cast<__half2*>(&v);
+  float2 f = __half22float2(h);
+  __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// Order-preserving key of a float: larger float -> larger key; NaN -> 0
+// (below -inf, whose key is 0x007FFFFF).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  uint32_t b = __float_as_uint(f);
+  if (f != f) return 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// Power-of-two exponent p such that max * 2^-p lies in [2^13, 2^14): the
+// scaled row fits FP16 with headroom for the products' partial sums.
+__device__ __forceinline__ int prescale_exp(float amax) {
+  if (!(amax > 0.0f) || !isfinite(amax)) return 0;
+  return ilogbf(amax) - 13;
+}
+
+// ---------------------------------------------------------------------------
+// Warp MMA m16n8k16, FP16 inputs, FP32 accumulate.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 ldg_nc_na(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ldg_nc_u16(const void* p) {
+  unsigned short r;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return r;
+}
+
+}  // namespace nvfp4moe

@@ -1,0 +1,77 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda.h>
+#include "common.cuh"
+
+namespace nvfp4moe {
+
+// Device buffers of one handle.  R = max_tokens * max_top_k routed rows.
+struct Workspace {
+  int32_t* ids;        // [R]      expert of flattened row t*k+j
+  float* wts;          // [R]      routing weight of flattened row
+  int32_t* offsets;    // [E+1]    expert-major row offsets
+  int32_t* perm;       // [R]      position -> flattened row
+  int32_t* inv;        // [R]      flattened row -> position
+  int32_t* tch_expert; // [E]      touched experts (decode), ascending
+  int32_t* tch_row0;   // [E]
+  int32_t* tch_rows;   // [E]
+  int32_t* num_touched;// [1]
+  __half* x16;         // [Tdec][H] FP16 activations, per-token power-of-two prescale
+  int32_t* xexp;       // [Tdec]   prescale exponents
+  __nv_bfloat16* h;    // [R][I]   silu(g)*u rounded to BF16, position order
+  uint32_t* hmax;      // [R]      max |h| of each row (float bits, decode path)
+  float* y;            // [R][H]   expert outputs, position order
+  float* part_gu;      // stream-K partial sums, gate/up  [maxU * I/32][1024]
+  int32_t* cnt_gu;     // arrival counters                [maxU * I/32]
+  float* part_dn;      // stream-K partial sums, down     [maxU * H/64][1024]
+  int32_t* cnt_dn;     //                                 [maxU * H/64]
+  int32_t* blk_counts; // [ncta][E] per-CTA histogram (prefill)
+  int32_t* blk_base;   // [ncta][E] per-CTA base inside each expert
+  __nv_bfloat16* x_perm; // [R][H] gathered activations (prefill)
+  int32_t* tile_expert;  // [max_tiles] prefill m-tiles
+  int32_t* tile_row0;
+  int32_t* tile_rows;
+  int32_t* num_tiles;    // [1]
+  DeviceStatus* status;
+};
+
+struct LayerDims {
+  int E, H, I;
+  int logits_bf16;
+};
+
+constexpr int kRouteTokPerCta = 64;   // tokens per CTA in the prefill route kernels
+constexpr int kTileRows = 256;        // max routed rows per prefill m-tile (MMA N)
+constexpr int kDecodeMaxTokens = 16;
+
+cudaError_t launch_pack(const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
+                        const uint8_t* w2_s, uint8_t* blob, int E, int H, int I, cudaStream_t st);
+cudaError_t launch_debug_dequant(const uint8_t* blob, const float* gscale, int H, int I, int expert,
+                                 int which, int via_bf16, float* out, cudaStream_t st);
+
+cudaError_t launch_route_decode(const LayerDims& d, const void* logits, const void* x, int T, int k,
+                                const Workspace& ws, cudaStream_t st);
+cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const void* x, int T, int k,
+                                 const Workspace& ws, cudaStream_t st);
+
+// `mid` (may be null) is recorded on the stream between the gate/up and the
+// down kernels (per-stage timing).
+cudaError_t launch_decode_ffn(const LayerDims& d, const uint8_t* blob, const float* gscale, int T, int k,
+                              cudaEvent_t mid, int num_sms, const Workspace& ws, cudaStream_t st);
+
+struct PrefillMaps {
+  CUtensorMap x_perm;  // [R][H] bf16, box {64, 16}, 128B swizzle
+  CUtensorMap h;       // [R][I] bf16, box {64, 16}, 128B swizzle
+};
+cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const float* gscale, int T, int k,
+                               int num_sms, const PrefillMaps& maps, const Workspace& ws, int fault,
+                               cudaEvent_t mid, cudaStream_t st);
+size_t prefill_smem_bytes();
+
+cudaError_t launch_combine(const LayerDims& d, int T, int k, const Workspace& ws, void* out,
+                           cudaStream_t st);
+
+}  // namespace nvfp4moe

@@ -1,0 +1,412 @@
+// Prefill path: grouped GEMM over the routed rows of every expert on the
+// 5th-generation tensor cores (tcgen05.mma, BF16 x BF16 -> FP32 in TMEM).
+//
+// The weight-only NVFP4 experts are dequantised to BF16 -- never through an
+// activation scale ("GLM-5.3-Flash on Blackwell", The model loaded, served an
+// API, and produced garbage: the working backend dequantises to bf16 and
+// consumes no activation scale).
+//
+// One persistent CTA per SM, 10 warps, warp-specialised:
+//   warp 0      producer: cp.async.bulk of the packed FP4 tile + its scales and
+//               TMA (128B swizzle) of the routed activation rows, into a
+//               4-stage shared-memory ring, completion on mbarriers;
+//   warp 1      MMA issuer (one thread): 4 x tcgen05.mma (K=16) per 64-wide
+//               chunk, accumulator double-buffered in TMEM (2 x 256 columns);
+//               also owns the TMEM allocation;
+//   warps 2-5   dequantisers: E2M1 x E4M3 -> BF16 (exact) written straight
+//               into the 128B-swizzled K-major operand layout;
+//   warps 6-9   epilogue: tcgen05.ld of the accumulator, tensor scales, SwiGLU
+//               (gate/up) or the down-projection store.
+// Work unit = (m-tile of <= 256 routed rows of one expert, 128 weight rows).
+// MMA orientation: weights are the 128-row M operand, routed tokens the N
+// operand (16..256), so small per-expert token counts do not waste the
+// 128-row atom.  The gate/up weight rows are interleaved in groups of 8
+// (gate f..f+7, up f..f+7), so each gate accumulator row and its up partner
+// sit 8 TMEM lanes apart, inside one warp.
+// Every mbarrier wait is bounded; on expiry the kernel records a timeout in
+// the handle's status word and winds down instead of hanging.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nvfp4moe {
+
+namespace pf {
+constexpr int kStages = 4;
+constexpr int kAOff = 0;            // 128 rows x 128 B (BF16 x 64)
+constexpr int kBOff = 16384;        // up to 256 rows x 128 B
+constexpr int kRawOff = 49152;      // 4096 B packed nibbles (128 rows x 64)
+constexpr int kScOff = 53248;       // 512 B scales
+constexpr int kStageBytes = 54272;  // multiple of 1024
+constexpr int kBarOff = kStages * kStageBytes;
+constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + barriers + alignment slack
+constexpr int kThreads = 320;
+constexpr int kTmemCols = 512;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // a wait longer than 2 s is a fault
+}  // namespace pf
+
+size_t prefill_smem_bytes() { return pf::kSmemBytes; }
+
+struct PrefillArgs {
+  const uint8_t* blob;
+  size_t expert_stride;
+  size_t nib_off, sc_off;
+  const float* gscale;
+  int K;      // reduction length (H for gate/up, I for down)
+  int NB;     // 128-row weight blocks per expert
+  int H, I;
+  const int32_t* tile_expert;
+  const int32_t* tile_row0;
+  const int32_t* tile_rows;
+  const int32_t* num_tiles;
+  __nv_bfloat16* h;
+  float* y;
+  DeviceStatus* st;
+  int fault;  // 1: the producer issues nothing (tests the bounded waits)
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: false on timeout (recorded in the status word) or when
+// another role has already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          DeviceStatus* st, unsigned where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > pf::kTimeoutNs) {
+        *abort_flag = 1;
+        report(st, kFlagTimeout, where);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// K-major operand, 128B swizzle, 8-row atoms 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// kind::f16 instruction descriptor: D = F32, A = B = BF16, both K-major.
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Dequantise one packed 16-byte segment (rows R0, R0+8; K elements 16q..16q+15
+// of the chunk) into the swizzled BF16 operand tile at a_base.
+__device__ __forceinline__ void dequant_segment(const uint8_t* stage, uint32_t a_base, int seg) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(stage + pf::kRawOff + seg * 16);
+  const uint32_t sc = *reinterpret_cast<const uint16_t*>(stage + pf::kScOff + seg * 2);
+  const uint32_t s2 = e4m3x2_to_f16x2(sc);
+  const int R0 = (seg >> 5) * 16 + ((seg & 31) >> 2);
+  const int q = seg & 3;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int R = R0 + 8 * half;
+    const uint32_t sx = half ? dup_hi(s2) : dup_lo(s2);
+    const uint32_t w0 = half ? raw.z : raw.x, w1 = half ? raw.w : raw.y;
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t byte = (j < 4 ? w0 : w1) >> (8 * (j & 3));
+      o[j] = f16x2_to_bf16x2(hmul2_u32(e2m1x2_to_f16x2(byte), sx));
+    }
+    const uint32_t row_base = a_base + (uint32_t)((R >> 3) * 1024 + (R & 7) * 128);
+    const uint32_t c0 = (uint32_t)((2 * q) ^ (R & 7)), c1 = (uint32_t)((2 * q + 1) ^ (R & 7));
+    sts128(row_base + c0 * 16, o[0], o[1], o[2], o[3]);
+    sts128(row_base + c1 * 16, o[4], o[5], o[6], o[7]);
+  }
+}
+
+template <bool kGateUp>
+__global__ void __launch_bounds__(pf::kThreads, 1)
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, PrefillArgs a) {
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + pf::kBarOff);
+  uint64_t* aready = full + pf::kStages;
+  uint64_t* empty = aready + pf::kStages;
+  uint64_t* accfull = empty + pf::kStages;
+  uint64_t* accempty = accfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < pf::kStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(aready + s, 4);
+      mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accfull + b, 1);
+      mbar_init(accempty + b, 4);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(pf::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = *a.num_tiles;
+  const int total_units = num_tiles * a.NB;
+  const int nch = a.K / kChunk;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- producer ----------------
+      uint32_t it = 0;
+      for (int unit = blockIdx.x; unit < total_units && !*abort_flag && a.fault != 1; unit += gridDim.x) {
+        const int tile = unit / a.NB, nb = unit % a.NB;
+        const int e = a.tile_expert[tile], row0 = a.tile_row0[tile], rows = a.tile_rows[tile];
+        const int nbox = (rows + 15) >> 4;
+        const uint8_t* src_nib = a.blob + (size_t)e * a.expert_stride + a.nib_off + (size_t)nb * nch * 4096;
+        const uint8_t* src_sc = a.blob + (size_t)e * a.expert_stride + a.sc_off + (size_t)nb * nch * 512;
+        for (int c = 0; c < nch; ++c, ++it) {
+          const int s = it % pf::kStages;
+          const uint32_t ph = (it / pf::kStages) & 1u;
+          if (!mbar_wait(empty + s, ph ^ 1u, abort_flag, a.st, 1)) break;
+          uint8_t* stage = smem + s * pf::kStageBytes;
+          mbar_arrive_expect_tx(full + s, 4096u + 512u + (uint32_t)nbox * 2048u);
+          bulk_g2s(stage + pf::kRawOff, src_nib + (size_t)c * 4096, 4096, full + s);
+          bulk_g2s(stage + pf::kScOff, src_sc + (size_t)c * 512, 512, full + s);
+          for (int bx = 0; bx < nbox; ++bx)
+            tma_2d(stage + pf::kBOff + bx * 2048, &tmap_b, c * kChunk, row0 + 16 * bx, full + s);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      uint32_t it = 0, j = 0;
+      for (int unit = blockIdx.x; unit < total_units && !*abort_flag; unit += gridDim.x, ++j) {
+        const int tile = unit / a.NB;
+        const int rows = a.tile_rows[tile];
+        const int N = (rows + 15) & ~15;
+        const uint32_t idesc = idesc_bf16(128, N);
+        const uint32_t buf = j & 1u, aph = (j >> 1) & 1u;
+        if (!mbar_wait(accempty + buf, aph ^ 1u, abort_flag, a.st, 2)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * 256u;
+        bool ok = true;
+        for (int c = 0; c < nch; ++c, ++it) {
+          const int s = it % pf::kStages;
+          const uint32_t ph = (it / pf::kStages) & 1u;
+          if (!mbar_wait(aready + s, ph, abort_flag, a.st, 3) || !mbar_wait(full + s, ph, abort_flag, a.st, 4)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t* stage = smem + s * pf::kStageBytes;
+          const uint64_t ad = sw128_desc(smem_u32(stage + pf::kAOff));
+          const uint64_t bd = sw128_desc(smem_u32(stage + pf::kBOff));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, (c | kk) != 0 ? 1u : 0u);
+          umma_commit(empty + s);
+        }
+        if (!ok) break;
+        umma_commit(accfull + buf);
+      }
+    }
+  } else if (warp < 6) {
+    // ---------------- dequantisers (128 threads) ----------------
+    const int tau = threadIdx.x - 64;
+    uint32_t it = 0;
+    for (int unit = blockIdx.x; unit < total_units && !*abort_flag; unit += gridDim.x) {
+      bool ok = true;
+      for (int c = 0; c < nch; ++c, ++it) {
+        const int s = it % pf::kStages;
+        const uint32_t ph = (it / pf::kStages) & 1u;
+        if (!mbar_wait(full + s, ph, abort_flag, a.st, 5)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* stage = smem + s * pf::kStageBytes;
+        const uint32_t a_base = smem_u32(stage + pf::kAOff);
+        dequant_segment(stage, a_base, tau);
+        dequant_segment(stage, a_base, tau + 128);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(aready + s);
+      }
+      if (!ok) break;
+    }
+  } else {
+    // ---------------- epilogue (128 threads) ----------------
+    const int quarter = warp & 3;
+    const int i = 32 * quarter + lane;  // accumulator row (TMEM lane)
+    uint32_t j = 0;
+    for (int unit = blockIdx.x; unit < total_units && !*abort_flag; unit += gridDim.x, ++j) {
+      const int tile = unit / a.NB, nb = unit % a.NB;
+      const int e = a.tile_expert[tile], row0 = a.tile_row0[tile], rows = a.tile_rows[tile];
+      const int N = (rows + 15) & ~15;
+      const uint32_t buf = j & 1u, aph = (j >> 1) & 1u;
+      if (!mbar_wait(accfull + buf, aph, abort_flag, a.st, 6)) break;
+      tc_fence_after();
+      const float* gs = a.gscale + 3 * e;
+      const uint32_t tbase = tmem_base + ((uint32_t)(32 * quarter) << 16) + buf * 256u;
+      for (int col = 0; col < N; col += 16) {
+        uint32_t v[16];
+        tmem_ld16(tbase + (uint32_t)col, v);
+        if (kGateUp) {
+          const int R = 128 * nb + i;
+          const int f = 8 * (R >> 4) + (R & 7);
+          const bool is_gate = (R & 15) < 8;
+          const float gsg = gs[0], gsu = gs[1];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const float mine = __uint_as_float(v[jj]);
+            const float partner = __shfl_xor_sync(0xffffffffu, mine, 8);
+            if (is_gate && col + jj < rows) {
+              const float g = gsg * mine, u = gsu * partner;
+              a.h[(size_t)(row0 + col + jj) * a.I + f] = __float2bfloat16_rn(silu(g) * u);
+            }
+          }
+        } else {
+          const int d = 128 * nb + i;
+          const float gsd = gs[2];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            if (col + jj < rows) a.y[(size_t)(row0 + col + jj) * a.H + d] = gsd * __uint_as_float(v[jj]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(accempty + buf);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(pf::kTmemCols)
+                 : "memory");
+  }
+}
+
+cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const float* gscale, int T, int k,
+                               int num_sms, const PrefillMaps& maps, const Workspace& ws, int fault,
+                               cudaEvent_t mid, cudaStream_t st) {
+  (void)T;
+  (void)k;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e1 = cudaFuncSetAttribute(prefill_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          pf::kSmemBytes);
+    cudaError_t e2 = cudaFuncSetAttribute(prefill_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          pf::kSmemBytes);
+    if (e1 != cudaSuccess) return e1;
+    if (e2 != cudaSuccess) return e2;
+    attr_set = true;
+  }
+  const ExpertLayout L = expert_layout(d.H, d.I);
+  PrefillArgs a{};
+  a.blob = blob;
+  a.expert_stride = L.stride;
+  a.gscale = gscale;
+  a.H = d.H;
+  a.I = d.I;
+  a.tile_expert = ws.tile_expert;
+  a.tile_row0 = ws.tile_row0;
+  a.tile_rows = ws.tile_rows;
+  a.num_tiles = ws.num_tiles;
+  a.h = ws.h;
+  a.y = ws.y;
+  a.st = ws.status;
+  a.fault = fault;
+  // gate/up: 2I interleaved rows, K = H
+  a.nib_off = L.w13_nib;
+  a.sc_off = L.w13_sc;
+  a.K = d.H;
+  a.NB = 2 * d.I / 128;
+  prefill_gemm_kernel<true><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(maps.x_perm, a);
+  if (mid) cudaEventRecord(mid, st);
+  // down: H rows, K = I
+  a.nib_off = L.w2_nib;
+  a.sc_off = L.w2_sc;
+  a.K = d.I;
+  a.NB = d.H / 128;
+  prefill_gemm_kernel<false><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(maps.h, a);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4moe

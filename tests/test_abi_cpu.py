@@ -1,0 +1,77 @@
+"""Host-side checks of the C-ABI library that need no GPU.
+
+* the library builds for sm_103a and exports every function the header
+  declares;
+* argument validation happens on the host and returns the documented status
+  codes before anything touches a device.
+"""
+import ctypes
+
+import pytest
+
+import nvfp4_weight_only_w4a16_gb300 as P
+from nvfp4_weight_only_w4a16_gb300.binding import Config
+
+
+@pytest.fixture(scope="module")
+def lib():
+    P.build()
+    return P.load_library()
+
+
+def test_exports_every_header_symbol(lib):
+    names = P.header_functions()
+    assert "nvfp4_moe_create" in names and "nvfp4_moe_forward" in names and "nvfp4_moe_pack" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(10):
+        s = lib.nvfp4_moe_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.nvfp4_moe_status_string(99).decode() == "unknown status"
+
+
+def _create(lib, **kw):
+    base = dict(num_experts=8, hidden=256, inter=512, max_tokens=16, max_top_k=2,
+                decode_max_tokens=16, logits_dtype=0, device=0)
+    base.update(kw)
+    cfg = Config(**base)
+    h = ctypes.c_void_p()
+    return lib.nvfp4_moe_create(ctypes.byref(cfg), ctypes.byref(h)), h
+
+
+@pytest.mark.parametrize("kw", [
+    dict(num_experts=0), dict(num_experts=257), dict(hidden=100), dict(hidden=192),
+    dict(inter=64), dict(max_tokens=0), dict(max_top_k=0), dict(max_top_k=17),
+    dict(num_experts=4, max_top_k=5), dict(decode_max_tokens=17),
+])
+def test_create_rejects_bad_shapes(lib, kw):
+    st, h = _create(lib, **kw)
+    assert st == P.STATUS_CODE["NVFP4_MOE_ERR_UNSUPPORTED_SHAPE"]
+    assert not h.value
+
+
+def test_create_rejects_bad_dtype_and_nulls(lib):
+    st, h = _create(lib, logits_dtype=7)
+    assert st == P.STATUS_CODE["NVFP4_MOE_ERR_INVALID_ARG"]
+    assert lib.nvfp4_moe_create(None, None) == P.STATUS_CODE["NVFP4_MOE_ERR_INVALID_ARG"]
+
+
+def test_null_handle_calls(lib):
+    inv = P.STATUS_CODE["NVFP4_MOE_ERR_INVALID_ARG"]
+    assert lib.nvfp4_moe_forward(None, None, 1, 1, None, None, None) == inv
+    assert lib.nvfp4_moe_pack(None, None, None, None, None, None, None) == inv
+    assert lib.nvfp4_moe_set_path(None, 0) == inv
+    assert lib.nvfp4_moe_debug_dequant(None, 0, 0, None, None) == inv
+    assert lib.nvfp4_moe_debug_set_fault(None, 0) == inv
+    lib.nvfp4_moe_destroy(None)  # no-op
+
+
+def test_header_has_no_activation_scale():
+    # weight-only: the forward takes logits, x and out, never an input scale
+    text = open(P.binding.HEADER).read()
+    fwd = text[text.index("nvfp4_moe_status nvfp4_moe_forward("):]
+    fwd = fwd[:fwd.index(";")]
+    assert "scale" not in fwd
