@@ -56,6 +56,11 @@ typedef enum nvfp4_moe_logits_dtype {
   NVFP4_MOE_LOGITS_BF16 = 1
 } nvfp4_moe_logits_dtype;
 
+typedef enum nvfp4_moe_out_dtype {
+  NVFP4_MOE_OUT_BF16 = 0,      /* the layer's output rounded once to BF16 */
+  NVFP4_MOE_OUT_F32 = 1        /* the FP32 combine result, unrounded      */
+} nvfp4_moe_out_dtype;
+
 typedef enum nvfp4_moe_path {
   NVFP4_MOE_PATH_AUTO = 0,     /* T <= decode_max_tokens -> decode, else prefill */
   NVFP4_MOE_PATH_DECODE = 1,   /* grouped GEMV, dequantised in registers          */
@@ -70,7 +75,8 @@ typedef enum nvfp4_moe_path {
  *   max_top_k         largest top_k a forward may pass, 1..min(E, 16)
  *   decode_max_tokens T at or below which AUTO picks the decode path, 0..16
  *   logits_dtype      nvfp4_moe_logits_dtype of router_logits
- *   device            CUDA device ordinal the handle lives on                 */
+ *   device            CUDA device ordinal the handle lives on
+ *   out_dtype         nvfp4_moe_out_dtype of out (BF16 unless set)             */
 typedef struct nvfp4_moe_config {
   int num_experts;
   int hidden;
@@ -80,6 +86,7 @@ typedef struct nvfp4_moe_config {
   int decode_max_tokens;
   int logits_dtype;
   int device;
+  int out_dtype;
 } nvfp4_moe_config;
 
 typedef struct nvfp4_moe* nvfp4_moe_t;
@@ -114,7 +121,8 @@ nvfp4_moe_status nvfp4_moe_pack(nvfp4_moe_t h, const uint8_t* w13_q, const uint8
  * no allocation, so the call can be captured into a CUDA graph.
  *   router_logits [T][E]  float or BF16 (config.logits_dtype), device
  *   x             [T][H]  BF16 activations, device, 16-byte aligned
- *   out           [T][H]  BF16 result, device, 16-byte aligned
+ *   out           [T][H]  BF16 (or FP32, config.out_dtype) result, device,
+ *                         16-byte aligned
  * 1 <= T <= max_tokens, 1 <= top_k <= max_top_k.  Ties between equal logits
  * go to the lower expert index; a NaN logit ranks below -inf and is counted
  * (see nvfp4_moe_get_status).  Concurrent forwards on one handle race on its
@@ -159,6 +167,12 @@ void nvfp4_moe_destroy(nvfp4_moe_t h);
 nvfp4_moe_status nvfp4_moe_debug_route(nvfp4_moe_t h, const void* router_logits, int T, int top_k,
                                        int32_t* ids, float* weights, int32_t* offsets,
                                        int32_t* perm, cudaStream_t stream);
+
+/* Copy the handle's packed expert blob (E * 3*H*I*9/16 bytes, the layout
+ * described at nvfp4_moe_pack; per expert: gate/up codes [2I*H/2], down codes
+ * [H*I/2], gate/up scales [2I*H/16], down scales [H*I/16]) into a caller
+ * DEVICE buffer of at least that many bytes. */
+nvfp4_moe_status nvfp4_moe_debug_packed_blob(nvfp4_moe_t h, void* dst, size_t dst_bytes, cudaStream_t stream);
 
 /* Dequantise one tensor of one expert from the PACKED blob into a caller
  * DEVICE buffer of float [N][K]: value = fp32(e2m1 * e4m3) * gscale, one

@@ -34,7 +34,7 @@ class Config(ctypes.Structure):
     _fields_ = [("num_experts", ctypes.c_int), ("hidden", ctypes.c_int), ("inter", ctypes.c_int),
                 ("max_tokens", ctypes.c_int), ("max_top_k", ctypes.c_int),
                 ("decode_max_tokens", ctypes.c_int), ("logits_dtype", ctypes.c_int),
-                ("device", ctypes.c_int)]
+                ("device", ctypes.c_int), ("out_dtype", ctypes.c_int)]
 
 
 _lib = None
@@ -71,6 +71,7 @@ def load_library(path: str | None = None):
         "nvfp4_moe_debug_intermediates": (i, [vp, vp, vp, vp]),
         "nvfp4_moe_debug_set_fault": (i, [vp, i]),
         "nvfp4_moe_set_profiling": (i, [vp, i]),
+        "nvfp4_moe_debug_packed_blob": (i, [vp, vp, ctypes.c_size_t, vp]),
         "nvfp4_moe_get_stage_times": (i, [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sigs.items():
@@ -102,10 +103,11 @@ class MoELayer:
     """One handle of the library (nvfp4_moe_create ... nvfp4_moe_destroy)."""
 
     def __init__(self, num_experts, hidden, inter, max_tokens, max_top_k, decode_max_tokens=16,
-                 logits_bf16=False, device=0):
+                 logits_bf16=False, device=0, out_f32=False):
         self.lib = load_library()
         self.cfg = Config(num_experts, hidden, inter, max_tokens, max_top_k, decode_max_tokens,
-                          1 if logits_bf16 else 0, device)
+                          1 if logits_bf16 else 0, device, 1 if out_f32 else 0)
+        self.out_f32 = out_f32
         self.E, self.H, self.I = num_experts, hidden, inter
         self.device = device
         h = ctypes.c_void_p()
@@ -165,6 +167,14 @@ class MoELayer:
                                             _ptr(perm), _stream(stream))
         self._check(st, "nvfp4_moe_debug_route")
         return ids, w, off, perm
+
+    def nvfp4_moe_debug_packed_blob(self, stream=None):
+        import torch
+        n = self.E * 3 * self.H * self.I * 9 // 16
+        out = torch.empty((n,), dtype=torch.uint8, device=f"cuda:{self.device}")
+        st = self.lib.nvfp4_moe_debug_packed_blob(self.h, _ptr(out), n, _stream(stream))
+        self._check(st, "nvfp4_moe_debug_packed_blob")
+        return out
 
     def nvfp4_moe_debug_dequant(self, expert, which, via_bf16=False, stream=None):
         import torch

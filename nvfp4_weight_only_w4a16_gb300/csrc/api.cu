@@ -133,7 +133,8 @@ nvfp4_moe_status check_forward_args(nvfp4_moe* h, const void* logits, int T, int
 }
 
 LayerDims dims_of(const nvfp4_moe* h) {
-  return LayerDims{h->cfg.num_experts, h->cfg.hidden, h->cfg.inter, h->cfg.logits_dtype == NVFP4_MOE_LOGITS_BF16};
+  return LayerDims{h->cfg.num_experts, h->cfg.hidden, h->cfg.inter, h->cfg.logits_dtype == NVFP4_MOE_LOGITS_BF16,
+                   h->cfg.out_dtype == NVFP4_MOE_OUT_F32};
 }
 
 nvfp4_moe_status run_route(nvfp4_moe* h, const void* logits, const void* x, int T, int k, int path,
@@ -179,6 +180,7 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* c, nvfp4_moe_t* out) {
   if (c->decode_max_tokens < 0 || c->decode_max_tokens > kDecodeMaxTokens) return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
   if (c->logits_dtype != NVFP4_MOE_LOGITS_F32 && c->logits_dtype != NVFP4_MOE_LOGITS_BF16)
     return NVFP4_MOE_ERR_INVALID_ARG;
+  if (c->out_dtype != NVFP4_MOE_OUT_BF16 && c->out_dtype != NVFP4_MOE_OUT_F32) return NVFP4_MOE_ERR_INVALID_ARG;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || c->device < 0 || c->device >= ndev) return NVFP4_MOE_ERR_INVALID_ARG;
 
@@ -408,6 +410,17 @@ nvfp4_moe_status nvfp4_moe_debug_route(nvfp4_moe_t h, const void* logits, int T,
     e = cudaMemcpyAsync(offsets, h->ws.offsets, (h->cfg.num_experts + 1) * 4, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(perm, h->ws.perm, n * 4, cudaMemcpyDeviceToDevice, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "debug_route copy");
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_moe_debug_packed_blob(nvfp4_moe_t h, void* dst, size_t dst_bytes, cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (!h->packed) return fail(h, NVFP4_MOE_ERR_NOT_PACKED, "debug_packed_blob before pack");
+  const size_t n = (size_t)h->cfg.num_experts * expert_layout(h->cfg.hidden, h->cfg.inter).stride;
+  if (!dst || dst_bytes < n) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_packed_blob: destination too small");
+  DeviceGuard g(h->cfg.device);
+  cudaError_t e = cudaMemcpyAsync(dst, h->blob, n, cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "debug_packed_blob copy");
   return NVFP4_MOE_OK;
 }
 

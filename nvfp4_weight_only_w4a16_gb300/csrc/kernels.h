@@ -41,6 +41,7 @@ struct Workspace {
 struct LayerDims {
   int E, H, I;
   int logits_bf16;
+  int out_f32;
 };
 
 constexpr int kRouteTokPerCta = 64;   // tokens per CTA in the prefill route kernels

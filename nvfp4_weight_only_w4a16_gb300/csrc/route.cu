@@ -302,9 +302,10 @@ cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const v
 // Weighted combine: out[t][d] = sum_{j<k} w[t][j] * y[pos(t,j)][d] in FP32,
 // slot order j = 0..k-1, rounded once to BF16.  One thread per 8 outputs.
 // ---------------------------------------------------------------------------
+template <bool kOutF32>
 __global__ void __launch_bounds__(256) combine_kernel(int T, int k, int H, const float* __restrict__ y,
                                                       const float* __restrict__ wts, const int32_t* __restrict__ inv,
-                                                      __nv_bfloat16* __restrict__ out) {
+                                                      void* __restrict__ out) {
   const int per_row = H / 8;
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (size_t)T * per_row) return;
@@ -323,19 +324,27 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int k, int H, const
     acc[6] = fmaf(w, b.z, acc[6]);
     acc[7] = fmaf(w, b.w, acc[7]);
   }
+  if (kOutF32) {
+    float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (size_t)t * H) + 2 * d8;
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    return;
+  }
   uint32_t o[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
     o[q] = *reinterpret_cast<const uint32_t*>(&b2);
   }
-  reinterpret_cast<uint4*>(out + (size_t)t * H)[d8] = make_uint4(o[0], o[1], o[2], o[3]);
+  reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + (size_t)t * H)[d8] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 cudaError_t launch_combine(const LayerDims& d, int T, int k, const Workspace& ws, void* out, cudaStream_t st) {
   const size_t n = (size_t)T * (d.H / 8);
-  combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(T, k, d.H, ws.y, ws.wts, ws.inv,
-                                                              reinterpret_cast<__nv_bfloat16*>(out));
+  if (d.out_f32)
+    combine_kernel<true><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(T, k, d.H, ws.y, ws.wts, ws.inv, out);
+  else
+    combine_kernel<false><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(T, k, d.H, ws.y, ws.wts, ws.inv, out);
   return cudaGetLastError();
 }
 

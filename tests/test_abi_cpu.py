@@ -35,7 +35,7 @@ def test_status_strings(lib):
 
 def _create(lib, **kw):
     base = dict(num_experts=8, hidden=256, inter=512, max_tokens=16, max_top_k=2,
-                decode_max_tokens=16, logits_dtype=0, device=0)
+                decode_max_tokens=16, logits_dtype=0, device=0, out_dtype=0)
     base.update(kw)
     cfg = Config(**base)
     h = ctypes.c_void_p()
@@ -56,6 +56,8 @@ def test_create_rejects_bad_shapes(lib, kw):
 def test_create_rejects_bad_dtype_and_nulls(lib):
     st, h = _create(lib, logits_dtype=7)
     assert st == P.STATUS_CODE["NVFP4_MOE_ERR_INVALID_ARG"]
+    st, h = _create(lib, out_dtype=2)
+    assert st == P.STATUS_CODE["NVFP4_MOE_ERR_INVALID_ARG"]
     assert lib.nvfp4_moe_create(None, None) == P.STATUS_CODE["NVFP4_MOE_ERR_INVALID_ARG"]
 
 
@@ -66,6 +68,7 @@ def test_null_handle_calls(lib):
     assert lib.nvfp4_moe_set_path(None, 0) == inv
     assert lib.nvfp4_moe_debug_dequant(None, 0, 0, None, None) == inv
     assert lib.nvfp4_moe_debug_set_fault(None, 0) == inv
+    assert lib.nvfp4_moe_debug_packed_blob(None, None, 0, None) == inv
     lib.nvfp4_moe_destroy(None)  # no-op
 
 

@@ -5,7 +5,10 @@ Bars:
 * routing weights: |gpu - oracle| <= 2e-6 * oracle (FP32 softmax of <= 16
   logits against float64);
 * layer output: max|err| <= 2e-2 * RMS(oracle) and mean|err| / mean|oracle|
-  <= 5e-3, plus the magnitude check the weight-only serving postmortem asks
+  <= 5e-3 on the FP32 output; a BF16 output may in addition differ by the
+  final rounding, at most 2^-9 of each output (for heavy-tailed outputs, such
+  as the 16K-token workload with x20 outlier weights, rounding the exact
+  result to BF16 alone exceeds 2e-2 * RMS); plus the magnitude check the weight-only serving postmortem asks
   for ("GLM-5.3-Flash on Blackwell", The model loaded, served an API, and
   produced garbage: an inverted scale kept cosine 0.996 at 25x the
   magnitude): ||gpu|| / ||oracle|| in [0.99, 1.01] and cosine >= 0.9999.
@@ -27,9 +30,9 @@ DEV = "cuda:0"
 _LAYERS = {}
 
 
-def _layer(cfg: LayerConfig, max_tokens=None, logits_bf16=False):
+def _layer(cfg: LayerConfig, max_tokens=None, logits_bf16=False, out_f32=False):
     key = (cfg.num_experts, cfg.hidden, cfg.inter, cfg.outlier_frac, cfg.seed, max_tokens or cfg.tokens,
-           cfg.top_k, logits_bf16)
+           cfg.top_k, logits_bf16, out_f32)
     if key not in _LAYERS:
         # keep at most one large layer resident
         if cfg.num_experts * cfg.hidden * cfg.inter > (1 << 26):
@@ -37,7 +40,7 @@ def _layer(cfg: LayerConfig, max_tokens=None, logits_bf16=False):
                 _LAYERS.pop(k).close()
         P.build()
         L = P.MoELayer(cfg.num_experts, cfg.hidden, cfg.inter, max_tokens or cfg.tokens, max(cfg.top_k, 1),
-                       logits_bf16=logits_bf16)
+                       logits_bf16=logits_bf16, out_f32=out_f32)
         P.upload_layer(L, make_layer_weights(cfg), DEV)
         _LAYERS[key] = L
     return _LAYERS[key]
@@ -51,7 +54,7 @@ def _forward(L, logits, x_bits, k, path=P.PATH_AUTO):
     L.nvfp4_moe_set_path(path)
     T, H = x_bits.shape
     x = _dev(x_bits.view(np.int16)).view(torch.bfloat16)
-    out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    out = torch.empty((T, H), dtype=torch.float32 if L.out_f32 else torch.bfloat16, device=DEV)
     L.nvfp4_moe_forward(_dev(logits), x, k, out)
     torch.cuda.synchronize()
     st, nan = L.nvfp4_moe_get_status()
@@ -60,10 +63,11 @@ def _forward(L, logits, x_bits, k, path=P.PATH_AUTO):
     return out.float().cpu().numpy().astype(np.float64)
 
 
-def assert_layer_close(gpu, ref):
+def assert_layer_close(gpu, ref, bf16_out=True):
     err = np.abs(gpu - ref)
     rms = np.sqrt(np.mean(ref ** 2))
-    assert err.max() <= 2e-2 * rms, (err.max(), rms)
+    allow = 2.0 ** -9 * np.abs(gpu) if bf16_out else 0.0
+    assert np.all(err <= 2e-2 * rms + allow), (err.max(), rms)
     assert err.mean() / np.abs(ref).mean() <= 5e-3, err.mean() / np.abs(ref).mean()
     ratio = np.linalg.norm(gpu) / np.linalg.norm(ref)
     assert 0.99 <= ratio <= 1.01, ratio
@@ -119,6 +123,41 @@ def test_dequant_bit_exact_full_layer():
                 got = L.nvfp4_moe_debug_dequant(e, which, via).cpu().numpy()
                 ref = O.dequant_scaled_f32(q, s, g)
                 assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), (e, which, via)
+
+
+def _host_repack_expert(w13_q, w13_s, w2_q, w2_s, H, I):
+    """Independent numpy statement of the packed layout for one expert."""
+    def pack(q, s, N, K, interleave):
+        nch = K // 64
+        rows = np.arange(N)
+        if interleave:  # packed row 16g+r: gate feature 8g+r (r<8), up feature 8g+r-8
+            g, r = rows // 16, rows % 16
+            src = np.where(r < 8, 8 * g + r, N // 2 + 8 * g + (r - 8))
+        else:
+            src = rows
+        qq, ss = q[src], s[src]                      # rows in packed order
+        # [rb 128][sb 8][r 2][t4 8] x [c][q 4][8 bytes]
+        qb = qq.reshape(N // 128, 8, 2, 8, nch, 4, 8)
+        nib = qb.transpose(0, 4, 1, 3, 5, 2, 6)       # rb, c, sb, t4, q, half, bytes
+        sb_ = ss.reshape(N // 128, 8, 2, 8, nch, 4)
+        sc = sb_.transpose(0, 4, 1, 3, 5, 2)          # rb, c, sb, t4, q, half
+        return nib.reshape(-1), sc.reshape(-1)
+    n13, s13 = pack(w13_q, w13_s, 2 * I, H, True)
+    n2, s2 = pack(w2_q, w2_s, H, I, False)
+    return np.concatenate([n13, n2, s13, s2])
+
+
+@pytest.mark.parametrize("name,experts", [("tiny", None), ("decode_mtp", (0, 64, 127))])
+def test_packed_blob_matches_host_repack(name, experts):
+    cfg = CONFIGS[name]
+    L = _layer(cfg, max_tokens=1024 if cfg.num_experts == 128 else None)
+    w = make_layer_weights(cfg)
+    blob = L.nvfp4_moe_debug_packed_blob().cpu().numpy()
+    H, I = cfg.hidden, cfg.inter
+    stride = 3 * H * I * 9 // 16
+    for e in (range(cfg.num_experts) if experts is None else experts):
+        ref = _host_repack_expert(w.w13_q[e], w.w13_s[e], w.w2_q[e], w.w2_s[e], H, I)
+        assert np.array_equal(blob[e * stride:(e + 1) * stride], ref), e
 
 
 # ---------------------------------------------------------------------------
@@ -204,36 +243,43 @@ def test_intermediates_tiny(path):
         assert np.abs(y[p] - y_ref).max() <= 1e-2 * np.sqrt(np.mean(y_ref ** 2))
 
 
+@pytest.mark.parametrize("out_f32", [True, False])
 @pytest.mark.parametrize("name", ["decode_mtp", "decode_c16"])
-def test_forward_decode_full_size(name):
+def test_forward_decode_full_size(name, out_f32):
     inp = make_inputs(name)
     cfg = inp.config
-    L = _layer(cfg, max_tokens=1024)
+    L = _layer(cfg, max_tokens=1024, out_f32=out_f32)
     gpu = _forward(L, inp.logits, inp.x_bits, cfg.top_k)
     tokens = np.arange(cfg.tokens) if cfg.tokens <= 2 else np.array([0, 5, 10, 15])
     ref = O.moe_forward(inp.logits, inp.x_bits, inp.weights, cfg.top_k, tokens=tokens)
-    assert_layer_close(gpu[tokens], ref)
+    assert_layer_close(gpu[tokens], ref, bf16_out=not out_f32)
 
 
-def test_forward_prefill_1k_sampled():
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_forward_prefill_1k_sampled(out_f32):
     inp = make_inputs("prefill_1k")
     cfg = inp.config
-    L = _layer(cfg, max_tokens=1024)
+    L = _layer(cfg, max_tokens=1024, out_f32=out_f32)
     gpu = _forward(L, inp.logits, inp.x_bits, cfg.top_k)
     tokens = np.array([0, 1, 257, 511, 777, 1023])
     ref = O.moe_forward(inp.logits, inp.x_bits, inp.weights, cfg.top_k, tokens=tokens)
-    assert_layer_close(gpu[tokens], ref)
+    assert_layer_close(gpu[tokens], ref, bf16_out=not out_f32)
     assert np.all(np.isfinite(gpu))
 
 
-def test_forward_prefill_16k_sampled():
+_PF16K_REF = {}
+
+
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_forward_prefill_16k_sampled(out_f32):
     inp = make_inputs("prefill_16k")
     cfg = inp.config
-    L = _layer(cfg)
+    L = _layer(cfg, out_f32=out_f32)
     gpu = _forward(L, inp.logits, inp.x_bits, cfg.top_k)
     tokens = np.array([0, 4097, 16383])
-    ref = O.moe_forward(inp.logits, inp.x_bits, inp.weights, cfg.top_k, tokens=tokens)
-    assert_layer_close(gpu[tokens], ref)
+    if "ref" not in _PF16K_REF:
+        _PF16K_REF["ref"] = O.moe_forward(inp.logits, inp.x_bits, inp.weights, cfg.top_k, tokens=tokens)
+    assert_layer_close(gpu[tokens], _PF16K_REF["ref"], bf16_out=not out_f32)
     assert np.all(np.isfinite(gpu))
 
 
