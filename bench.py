@@ -238,6 +238,7 @@ def run_ours(args):
     cfg = inp.config
     T, k, H, E = cfg.tokens, cfg.top_k, cfg.hidden, cfg.num_experts
     layer = pkg.MoELayer(E, H, cfg.inter, T, k, device=dev.index)
+    n_ours = 4 if T <= 16 else 6     # kernels of ours per forward (decode / prefill path)
     pkg.upload_layer(layer, inp.weights, dev)
 
     logits = torch.from_numpy(inp.logits).to(dev)
@@ -326,29 +327,43 @@ def run_ours(args):
     value = ws * T / (ms / 1e3)
     value_e2e = ws * T / (ms_e2e / 1e3)
 
-    # roofline of the gate/up GEMV: weights of the touched experts + activations
     I = cfg.inter
-    gateup_bytes = distinct * (2 * I * H // 2 + 2 * I * H // 16) + T * H * 2 + T * k * I * 2
     gateup_ms = stage_ms[1] / max(nfwd, 1)
-    achieved = gateup_bytes / (gateup_ms / 1e3) / 1e9
+    layer_bytes = distinct * cfg.expert_bytes + T * H * 2 * 2 + T * E * 4
+    if T <= 16:
+        # decode: the gate/up GEMV streams the touched experts' gate/up weights once
+        kernel = "decode_gemv_kernel<gate/up>"
+        algo = distinct * (2 * I * H // 2 + 2 * I * H // 16) + T * H * 2 + T * k * I * 2
+        achieved = algo / (gateup_ms / 1e3) / 1e9
+        bound, unit, peak_key = "hbm", "GB/s", "hbm_gbs"
+        traffic = _traffic_for(os.path.join(ROOT, "nvfp4_weight_only_w4a16_gb300", "csrc", "decode.cu"))
+    else:
+        # prefill: the gate/up GEMM's dense flops on the tensor cores
+        kernel = "prefill_gemm_kernel<gate/up>"
+        algo = 2.0 * T * k * (2 * I) * H
+        achieved = algo / (gateup_ms / 1e3) / 1e12
+        bound, unit, peak_key = "tensor", "TFLOP/s", "bf16_tflops"
+        traffic = None
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peak = float(json.load(f)["hbm_gbs"])
+            peak = float(json.load(f)[peak_key])
         peak_src = "measured"
     except Exception:
-        peak, peak_src = 6800.0, "fallback"
-    traffic = _traffic_for(os.path.join(ROOT, "nvfp4_weight_only_w4a16_gb300", "csrc", "decode.cu"))
-    layer_bytes = distinct * cfg.expert_bytes + T * H * 2 * 2 + T * E * 4
+        peak, peak_src = (6800.0 if bound == "hbm" else 1900.0), "fallback"
+    layer_flops = 2.0 * T * k * 3 * H * I
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        path = _oracle_sample_file(inp, ids.cpu().numpy())
+        ns = min(T, 2)   # bounded sample: the first tokens of the step (the whole step at T = 2)
+        sub = make_inputs(cfg.with_tokens(ns)) if ns < T else inp
+        path = _oracle_sample_file(sub, ids.cpu().numpy()[:ns])
         try:
             times = _run_oracle_child(path, "baseline")
         finally:
             os.unlink(path)
-        cpu = {"value": T / statistics.mean(times), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"the whole {T}-token step ({T * k} expert FFNs + combine), twice, float64 numpy, 1 thread"}
+        cpu = {"value": ns / statistics.mean(times), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{ns} token(s) of the step ({ns * k} expert FFNs + combine), twice, float64 numpy, "
+                         f"1 thread"}
 
     if rank == 0:
         line = {
@@ -359,17 +374,18 @@ def run_ours(args):
             "config": {"workload": _workload_desc(cfg), "distinct_experts": distinct,
                        "layer_weight_bytes_per_step": layer_bytes,
                        "layer_weight_gbs": layer_bytes / (ms / 1e3) / 1e9,
+                       "layer_tflops": layer_flops / (ms / 1e3) / 1e12,
                        "l2": "flushed before every step (256 MiB write, outside the step events)",
                        "launch": "CUDA graph replay of one nvfp4_moe_forward",
                        "parallelism": f"replicas x{ws}",
                        "stage_ms": {"route_permute": stage_ms[0] / max(nfwd, 1), "gate_up": gateup_ms,
                                     "down": stage_ms[2] / max(nfwd, 1), "combine": stage_ms[3] / max(nfwd, 1)}},
-            "roofline": {"bound": "hbm", "kernel": "decode_gemv_kernel<gate/up>", "achieved": achieved,
-                         "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
-                         "algorithmic_bytes": gateup_bytes, "traffic": traffic},
+            "roofline": {"bound": bound, "kernel": kernel, "achieved": achieved, "peak": peak,
+                         "peak_source": peak_src, "unit": unit, "frac": achieved / peak,
+                         "algorithmic_per_launch": algo, "traffic": traffic},
             "e2e": {"value": value_e2e, "unit": "tokens/s", "h2d_bytes_per_step": T * E * 4 + T * H * 2,
                     "d2h_bytes_per_step": T * H * 2},
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": n_ours * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
