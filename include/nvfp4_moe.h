@@ -140,6 +140,34 @@ nvfp4_moe_status nvfp4_moe_get_status(nvfp4_moe_t h, uint32_t* nan_logits);
  * variable NVFP4_MOE_FORCE_PATH=decode|prefill sets the default at create. */
 nvfp4_moe_status nvfp4_moe_set_path(nvfp4_moe_t h, int path);
 
+/* Decode forward that allocates nothing.  The GLM-5.3-Flash pages have no
+ * counterpart to this call; it exists for callers that cannot call
+ * cudaMalloc and so cannot create a handle: code running while a CUDA graph
+ * is captured in global mode, plugins whose host framework owns and budgets
+ * every device byte, and static-memory runtimes that forbid allocation after
+ * start-up.  It computes what nvfp4_moe_forward computes on the decode path,
+ * from caller memory only:
+ *   packed_experts  DEVICE, 16-byte aligned, E * 3*H*I*9/16 bytes in the
+ *                   layout nvfp4_moe_pack writes (see nvfp4_moe_debug_packed_blob)
+ *   gscale [E][3]   DEVICE float tensor scales (finite, > 0: not re-checked)
+ *   router_logits [T][E] (logits_dtype), x [T][H] BF16, out [T][H] BF16
+ * 1 <= T <= 16, 1 <= top_k <= min(E, 16); H, I as in nvfp4_moe_config.
+ * All intermediates live in one static device array of 16 MiB that every GPU
+ * loading this library holds until the process exits.  A shape whose
+ * intermediates need more than that (about 7.3 MiB for E=128, H=4096,
+ * I=1536, T=2, top_k=8; the split-K partial sums grow with
+ * min(E, T*top_k) * (2I + H) * 64 bytes) returns
+ * NVFP4_MOE_ERR_UNSUPPORTED_SHAPE before anything is enqueued.  The regions
+ * that must start at zero are cleared by every call.  The first call on each
+ * device looks up the array's device address with that device current: make
+ * it before any stream capture.  Calls whose GPU work overlaps (other
+ * streams, concurrent graph replays) share the array and race: serialise
+ * them. */
+nvfp4_moe_status nvfp4_moe_forward_decode_static(const uint8_t* packed_experts, const float* gscale,
+                                                 int num_experts, int hidden, int inter,
+                                                 const void* router_logits, int logits_dtype, int T, int top_k,
+                                                 const void* x, void* out, cudaStream_t stream);
+
 /* Per-stage timing.  With profiling on, every forward records CUDA events on
  * its stream before and after each stage.  nvfp4_moe_get_stage_times
  * (synchronous) returns in ms[0..3] the summed milliseconds of route+permute,

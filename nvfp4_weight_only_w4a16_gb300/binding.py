@@ -72,6 +72,7 @@ def load_library(path: str | None = None):
         "nvfp4_moe_debug_set_fault": (i, [vp, i]),
         "nvfp4_moe_set_profiling": (i, [vp, i]),
         "nvfp4_moe_debug_packed_blob": (i, [vp, vp, ctypes.c_size_t, vp]),
+        "nvfp4_moe_forward_decode_static": (i, [vp, vp, i, i, i, vp, i, i, i, vp, vp, vp]),
         "nvfp4_moe_get_stage_times": (i, [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sigs.items():
@@ -204,6 +205,15 @@ class MoELayer:
 
     def nvfp4_moe_debug_set_fault(self, fault):
         self._check(self.lib.nvfp4_moe_debug_set_fault(self.h, fault), "nvfp4_moe_debug_set_fault")
+
+
+def nvfp4_moe_forward_decode_static(packed_experts, gscale, num_experts, hidden, inter, logits, top_k, x, out,
+                                    logits_bf16=False, stream=None):
+    """The allocation-free decode forward: every argument is caller memory."""
+    lib = load_library()
+    return lib.nvfp4_moe_forward_decode_static(_ptr(packed_experts), _ptr(gscale), num_experts, hidden, inter,
+                                               _ptr(logits), 1 if logits_bf16 else 0, x.shape[0], top_k,
+                                               _ptr(x), _ptr(out), _stream(stream))
 
 
 def upload_layer(layer: MoELayer, weights, device="cuda:0"):

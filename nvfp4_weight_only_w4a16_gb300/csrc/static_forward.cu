@@ -1,0 +1,148 @@
+// Allocation-free decode forward.
+//
+// Some callers cannot call cudaMalloc: code that runs while a CUDA graph is
+// being captured in global mode, plugins whose host framework owns every
+// device byte (a serving engine with its own memory pool and allocation
+// budget), and static-memory runtimes that allocate everything once at start
+// and forbid allocation afterwards.  They cannot create a handle, because
+// nvfp4_moe_create allocates the weight blob and the workspace.  This entry
+// point runs the decode path (route, gate/up GEMV, down GEMV, combine) with
+// the caller's own weight blob, activations and output; every intermediate
+// (routing tables, h, y, the GEMVs' split-K partial sums and counters) lives
+// in one file-scope __device__ array of kStaticScratchBytes.
+//
+// Consequences a caller must know:
+//  * every GPU that loads this library reserves the array until the process
+//    exits, whether or not this entry point is ever called;
+//  * on each device, the first call looks up the array's device address
+//    (cudaGetSymbolAddress) with that device current; make that first call
+//    before any stream capture;
+//  * all calls on a device share the array: calls whose work overlaps on the
+//    GPU (different streams, or graphs replayed concurrently) race and give
+//    wrong results; serialise them;
+//  * the array keeps the last call's contents; the regions that must start at
+//    zero are cleared (cudaMemsetAsync) by every call.
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/nvfp4_moe.h"
+#include "kernels.h"
+
+namespace nvfp4moe {
+
+constexpr size_t kStaticScratchBytes = 16u << 20;  // 16 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+struct StaticSetup {
+  uint8_t* scratch = nullptr;  // device address of g_static_scratch on this device
+  int num_sms = 0;
+};
+
+std::mutex g_setup_mutex;
+StaticSetup g_setup[kMaxDevices];
+
+// Once per device, with that device current.
+cudaError_t static_setup(int dev, StaticSetup* out) {
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (!g_setup[dev].scratch) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_setup[dev].scratch = static_cast<uint8_t*>(p);
+    g_setup[dev].num_sms = sms;
+  }
+  *out = g_setup[dev];
+  return cudaSuccess;
+}
+
+struct Region {
+  size_t off = 0;
+  template <class T>
+  T* take(uint8_t* base, size_t count) {
+    off = (off + 255) & ~size_t(255);
+    T* p = reinterpret_cast<T*>(base + off);
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+// Carves the decode workspace out of `base`; returns the bytes it needs.
+// With base == nullptr only the size is computed.  The zero-initialised
+// regions (split-K partials, counters, status) are contiguous at the front:
+// [0, *zero_bytes).
+size_t carve(uint8_t* base, int E, int H, int I, int T, int k, Workspace* ws, size_t* zero_bytes) {
+  const size_t R = (size_t)T * k;
+  const size_t maxU = std::min<size_t>((size_t)E, R);
+  uint8_t* b = base ? base : reinterpret_cast<uint8_t*>(0x100);
+  Region r;
+  Workspace w{};
+  w.part_gu = r.take<float>(b, maxU * (2 * I / 64) * 1024);
+  w.cnt_gu = r.take<int32_t>(b, maxU * (2 * I / 64));
+  w.part_dn = r.take<float>(b, maxU * (H / 64) * 1024);
+  w.cnt_dn = r.take<int32_t>(b, maxU * (H / 64));
+  w.status = r.take<DeviceStatus>(b, 1);
+  *zero_bytes = (r.off + 255) & ~size_t(255);
+  w.ids = r.take<int32_t>(b, R);
+  w.wts = r.take<float>(b, R);
+  w.offsets = r.take<int32_t>(b, E + 1);
+  w.perm = r.take<int32_t>(b, R);
+  w.inv = r.take<int32_t>(b, R);
+  w.tch_expert = r.take<int32_t>(b, E);
+  w.tch_row0 = r.take<int32_t>(b, E);
+  w.tch_rows = r.take<int32_t>(b, E);
+  w.num_touched = r.take<int32_t>(b, 1);
+  w.x16 = r.take<__half>(b, (size_t)T * H);
+  w.xexp = r.take<int32_t>(b, T);
+  w.h = r.take<__nv_bfloat16>(b, R * I);
+  w.hmax = r.take<uint32_t>(b, R);
+  w.y = r.take<float>(b, R * H);
+  if (base && ws) *ws = w;
+  return r.off;
+}
+
+bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace nvfp4moe
+
+using namespace nvfp4moe;
+
+extern "C" nvfp4_moe_status nvfp4_moe_forward_decode_static(const uint8_t* packed_experts, const float* gscale,
+                                                            int num_experts, int hidden, int inter,
+                                                            const void* router_logits, int logits_dtype, int T,
+                                                            int top_k, const void* x, void* out,
+                                                            cudaStream_t stream) {
+  const int E = num_experts, H = hidden, I = inter;
+  if (E < 1 || E > 256 || H < 128 || H > 16384 || H % 128 || I < 128 || I > 16384 || I % 128)
+    return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T < 1 || T > kDecodeMaxTokens || top_k < 1 || top_k > 16 || top_k > E) return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
+  if (logits_dtype != NVFP4_MOE_LOGITS_F32 && logits_dtype != NVFP4_MOE_LOGITS_BF16) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (!packed_experts || !gscale || !router_logits || !x || !out) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (!aligned_to(packed_experts, 16) || !aligned_to(x, 16) || !aligned_to(out, 16) || !aligned_to(gscale, 4) ||
+      !aligned_to(router_logits, logits_dtype == NVFP4_MOE_LOGITS_BF16 ? 2 : 4))
+    return NVFP4_MOE_ERR_INVALID_ARG;
+  size_t zero_bytes = 0;
+  if (carve(nullptr, E, H, I, T, top_k, nullptr, &zero_bytes) > kStaticScratchBytes)
+    return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;  // needs more than the static scratch holds
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_MOE_ERR_CUDA;
+  StaticSetup setup;
+  if (static_setup(dev, &setup) != cudaSuccess) return NVFP4_MOE_ERR_CUDA;
+
+  Workspace ws{};
+  carve(setup.scratch, E, H, I, T, top_k, &ws, &zero_bytes);
+  const LayerDims d{E, H, I, logits_dtype == NVFP4_MOE_LOGITS_BF16, 0};
+  cudaError_t e = cudaMemsetAsync(setup.scratch, 0, zero_bytes, stream);
+  if (e == cudaSuccess) e = launch_route_decode(d, router_logits, x, T, top_k, ws, stream);
+  if (e == cudaSuccess) e = launch_decode_ffn(d, packed_experts, gscale, T, top_k, nullptr, setup.num_sms, ws, stream);
+  if (e == cudaSuccess) e = launch_combine(d, T, top_k, ws, out, stream);
+  return e == cudaSuccess ? NVFP4_MOE_OK : NVFP4_MOE_ERR_CUDA;
+}
