@@ -12,9 +12,10 @@ Measured:
   stream; L2 is flushed (256 MiB write) before every step, outside the events;
 * e2e: the same metric through the C ABI with the step's inputs copied from
   pinned host memory and the output read back, all inside the events;
-* roofline: the gate/up GEMV (the kernel that streams 2/3 of the weight
-  bytes), algorithmic bytes per launch / its CUDA-event duration, against the
-  measured HBM copy bandwidth;
+* roofline: the fused decode kernel (route + gate/up + down + combine in one
+  launch), algorithmic bytes per launch (the touched experts' NVFP4 weights,
+  logits, x and out) / its CUDA-event duration, against the measured HBM copy
+  bandwidth (prefill workloads: the gate/up GEMM's flops against BF16 peak);
 * cpu_baseline: the float64 CPU oracle on a bounded sample of the same step.
 --impl reference times the oracle alone (the CPU reference arm).
 Multi-GPU: replicas only (one independent layer per rank, no collective in
@@ -40,7 +41,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE layer tokens/s; decode weight GB/s & prefill TFLOP/s as % of GB300 roofline"
 WORKLOAD = "decode_mtp"
 FLUSH_BYTES = 256 << 20
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "decode_gemv_gateup_decode_mtp.json")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "decode_fused_kernel_decode_mtp.json")
 
 
 def _args():
@@ -238,7 +239,7 @@ def run_ours(args):
     cfg = inp.config
     T, k, H, E = cfg.tokens, cfg.top_k, cfg.hidden, cfg.num_experts
     layer = pkg.MoELayer(E, H, cfg.inter, T, k, device=dev.index)
-    n_ours = 4 if T <= 16 else 6     # kernels of ours per forward (decode / prefill path)
+    n_ours = 1 if T <= 16 else 6     # kernels of ours per forward (decode / prefill path)
     pkg.upload_layer(layer, inp.weights, dev)
 
     logits = torch.from_numpy(inp.logits).to(dev)
@@ -331,9 +332,9 @@ def run_ours(args):
     gateup_ms = stage_ms[1] / max(nfwd, 1)
     layer_bytes = distinct * cfg.expert_bytes + T * H * 2 * 2 + T * E * 4
     if T <= 16:
-        # decode: the gate/up GEMV streams the touched experts' gate/up weights once
-        kernel = "decode_gemv_kernel<gate/up>"
-        algo = distinct * (2 * I * H // 2 + 2 * I * H // 16) + T * H * 2 + T * k * I * 2
+        # decode: one fused kernel streams every touched expert's weights once
+        kernel = "decode_fused_kernel"
+        algo = layer_bytes
         achieved = algo / (gateup_ms / 1e3) / 1e9
         bound, unit, peak_key = "hbm", "GB/s", "hbm_gbs"
         traffic = _traffic_for(os.path.join(ROOT, "nvfp4_weight_only_w4a16_gb300", "csrc", "decode.cu"))

@@ -202,6 +202,13 @@ nvfp4_moe_status nvfp4_moe_debug_route(nvfp4_moe_t h, const void* router_logits,
  * DEVICE buffer of at least that many bytes. */
 nvfp4_moe_status nvfp4_moe_debug_packed_blob(nvfp4_moe_t h, void* dst, size_t dst_bytes, cudaStream_t stream);
 
+/* Phase timeline of the decode kernel (handles created with the environment
+ * variable NVFP4_MOE_TRACE=1 only).  Synchronous.  Copies up to n values into
+ * host_dst: for each CTA c and warp w, 8 globaltimer nanosecond stamps at
+ * [(c*16 + w)*8]: kernel start, routed, gate/up done, first down wait over,
+ * down done, exit barrier passed (unused slots 0); clears the buffer. */
+nvfp4_moe_status nvfp4_moe_debug_trace(nvfp4_moe_t h, uint64_t* host_dst, size_t n, size_t* n_written);
+
 /* Dequantise one tensor of one expert from the PACKED blob into a caller
  * DEVICE buffer of float [N][K]: value = fp32(e2m1 * e4m3) * gscale, one
  * FP32 rounding.  which: 0 gate [I][H], 1 up [I][H], 2 down [H][I]. */

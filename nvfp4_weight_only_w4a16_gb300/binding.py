@@ -73,6 +73,8 @@ def load_library(path: str | None = None):
         "nvfp4_moe_set_profiling": (i, [vp, i]),
         "nvfp4_moe_debug_packed_blob": (i, [vp, vp, ctypes.c_size_t, vp]),
         "nvfp4_moe_forward_decode_static": (i, [vp, vp, i, i, i, vp, i, i, i, vp, vp, vp]),
+        "nvfp4_moe_debug_trace": (i, [vp, ctypes.POINTER(ctypes.c_uint64), ctypes.c_size_t,
+                                      ctypes.POINTER(ctypes.c_size_t)]),
         "nvfp4_moe_get_stage_times": (i, [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sigs.items():
@@ -168,6 +170,14 @@ class MoELayer:
                                             _ptr(perm), _stream(stream))
         self._check(st, "nvfp4_moe_debug_route")
         return ids, w, off, perm
+
+    def nvfp4_moe_debug_trace(self):
+        import numpy as np
+        n = 152 * 16 * 8 * 4
+        buf = (ctypes.c_uint64 * n)()
+        got = ctypes.c_size_t(0)
+        self._check(self.lib.nvfp4_moe_debug_trace(self.h, buf, n, ctypes.byref(got)), "nvfp4_moe_debug_trace")
+        return np.frombuffer(buf, dtype=np.uint64)[:got.value].copy()
 
     def nvfp4_moe_debug_packed_blob(self, stream=None):
         import torch

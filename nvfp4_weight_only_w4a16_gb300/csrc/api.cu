@@ -140,8 +140,10 @@ LayerDims dims_of(const nvfp4_moe* h) {
 nvfp4_moe_status run_route(nvfp4_moe* h, const void* logits, const void* x, int T, int k, int path,
                            cudaStream_t st) {
   const LayerDims d = dims_of(h);
-  cudaError_t e = path == NVFP4_MOE_PATH_DECODE ? launch_route_decode(d, logits, x, T, k, h->ws, st)
-                                                : launch_route_prefill(d, logits, x, T, k, h->ws, st);
+  cudaError_t e = path == NVFP4_MOE_PATH_DECODE
+                      ? launch_decode_forward(d, h->blob, h->gscale, logits, nullptr, T, k, nullptr, 1, h->num_sms,
+                                              h->ws, st)
+                      : launch_route_prefill(d, logits, x, T, k, h->ws, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "route launch");
   return NVFP4_MOE_OK;
 }
@@ -199,7 +201,7 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* c, nvfp4_moe_t* out) {
   const size_t R = (size_t)c->max_tokens * c->max_top_k;
   const size_t Rm = R < 256 ? 256 : R;
   const size_t maxU = (size_t)std::min(E, kDecodeMaxTokens * c->max_top_k);
-  const size_t ncta = ((size_t)c->max_tokens + kRouteTokPerCta - 1) / kRouteTokPerCta;
+  const size_t ncta = ((size_t)c->max_tokens + kRankTokens - 1) / kRankTokens;
   const size_t max_tiles = R / kTileRows + E + 1;
   const size_t blob_bytes = (size_t)E * expert_layout(H, I).stride;
 
@@ -223,14 +225,21 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* c, nvfp4_moe_t* out) {
   cv.add(&w.cnt_gu, maxU * (2 * I / 64));
   cv.add(&w.part_dn, maxU * (H / 64) * 1024);
   cv.add(&w.cnt_dn, maxU * (H / 64));
+  cv.add(&w.done_gu, maxU);
+  cv.add(&w.cmb, H / 64);
+  cv.add(&w.exit_cnt, 1);
   cv.add(&w.blk_counts, ncta * E);
   cv.add(&w.blk_base, ncta * E);
+  cv.add(&w.local_rank, Rm);
   cv.add(&w.x_perm, Rm * H);
   cv.add(&w.tile_expert, max_tiles);
   cv.add(&w.tile_row0, max_tiles);
   cv.add(&w.tile_rows, max_tiles);
   cv.add(&w.num_tiles, 1);
   cv.add(&w.status, 1);
+  const char* tr = getenv("NVFP4_MOE_TRACE");
+  const bool trace = tr && tr[0] == '1';
+  if (trace) cv.add(&w.trace, (size_t)h->num_sms * 16 * 8);
   h->ws_bytes = cv.layout();
 
   if (cudaMalloc(&h->blob, blob_bytes) != cudaSuccess || cudaMalloc(&h->gscale, sizeof(float) * 3 * E) != cudaSuccess ||
@@ -358,19 +367,25 @@ nvfp4_moe_status nvfp4_moe_forward(nvfp4_moe_t h, const void* logits, int T, int
     }
     cudaEventRecord(ev[0], st);
   }
-  s = run_route(h, logits, x, T, top_k, path, st);
-  if (s != NVFP4_MOE_OK) return s;
-  if (ev[1]) cudaEventRecord(ev[1], st);
   const LayerDims d = dims_of(h);
   cudaError_t e;
-  if (path == NVFP4_MOE_PATH_DECODE)
-    e = launch_decode_ffn(d, h->blob, h->gscale, T, top_k, ev[2], h->num_sms, h->ws, st);
-  else
+  if (path == NVFP4_MOE_PATH_DECODE) {
+    // one fused kernel: its time is reported as the gate/up stage
+    if (ev[1]) cudaEventRecord(ev[1], st);
+    e = launch_decode_forward(d, h->blob, h->gscale, logits, x, T, top_k, out, 0, h->num_sms, h->ws, st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");
+    if (ev[2]) cudaEventRecord(ev[2], st);
+    if (ev[3]) cudaEventRecord(ev[3], st);
+  } else {
+    s = run_route(h, logits, x, T, top_k, path, st);
+    if (s != NVFP4_MOE_OK) return s;
+    if (ev[1]) cudaEventRecord(ev[1], st);
     e = launch_prefill_ffn(d, h->blob, h->gscale, T, top_k, h->num_sms, h->maps, h->ws, h->fault, ev[2], st);
-  if (e != cudaSuccess) return cuda_fail(h, e, "expert FFN launch");
-  if (ev[3]) cudaEventRecord(ev[3], st);
-  e = launch_combine(d, T, top_k, h->ws, out, st);
-  if (e != cudaSuccess) return cuda_fail(h, e, "combine launch");
+    if (e != cudaSuccess) return cuda_fail(h, e, "expert FFN launch");
+    if (ev[3]) cudaEventRecord(ev[3], st);
+    e = launch_combine(d, T, top_k, h->ws, out, st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "combine launch");
+  }
   if (ev[4]) cudaEventRecord(ev[4], st);
   h->last_T = T;
   h->last_k = top_k;
@@ -410,6 +425,21 @@ nvfp4_moe_status nvfp4_moe_debug_route(nvfp4_moe_t h, const void* logits, int T,
     e = cudaMemcpyAsync(offsets, h->ws.offsets, (h->cfg.num_experts + 1) * 4, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(perm, h->ws.perm, n * 4, cudaMemcpyDeviceToDevice, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "debug_route copy");
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_moe_debug_trace(nvfp4_moe_t h, uint64_t* host_dst, size_t n, size_t* n_written) {
+  if (!h || !host_dst || !n_written) return NVFP4_MOE_ERR_INVALID_ARG;
+  *n_written = 0;
+  if (!h->ws.trace) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_trace: create the handle with NVFP4_MOE_TRACE=1");
+  DeviceGuard g(h->cfg.device);
+  const size_t total = (size_t)h->num_sms * 16 * 8;
+  const size_t m = n < total ? n : total;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(host_dst, h->ws.trace, m * 8, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(h->ws.trace, 0, total * 8);
+  if (e != cudaSuccess) return cuda_fail(h, e, "debug_trace");
+  *n_written = m;
   return NVFP4_MOE_OK;
 }
 

@@ -28,14 +28,19 @@ struct Workspace {
   int32_t* cnt_gu;     // arrival counters                [maxU * I/32]
   float* part_dn;      // stream-K partial sums, down     [maxU * H/64][1024]
   int32_t* cnt_dn;     //                                 [maxU * H/64]
-  int32_t* blk_counts; // [ncta][E] per-CTA histogram (prefill)
-  int32_t* blk_base;   // [ncta][E] per-CTA base inside each expert
+  int32_t* done_gu;    // finished gate/up blocks per touched expert [maxU] (decode)
+  int32_t* cmb;        // finished down blocks per 64-wide slice of H [H/64] (decode)
+  int32_t* exit_cnt;   // CTAs that finished the decode kernel [1]
+  int32_t* blk_counts; // [nrb][E] per-rank-block histogram (prefill)
+  int32_t* blk_base;   // [nrb][E] per-rank-block base inside each expert
+  int32_t* local_rank; // [R] rank of a routed row inside its rank block (prefill)
   __nv_bfloat16* x_perm; // [R][H] gathered activations (prefill)
   int32_t* tile_expert;  // [max_tiles] prefill m-tiles
   int32_t* tile_row0;
   int32_t* tile_rows;
   int32_t* num_tiles;    // [1]
   DeviceStatus* status;
+  unsigned long long* trace;  // optional per-warp phase stamps of the decode kernel (NVFP4_MOE_TRACE=1)
 };
 
 struct LayerDims {
@@ -44,7 +49,7 @@ struct LayerDims {
   int out_f32;
 };
 
-constexpr int kRouteTokPerCta = 64;   // tokens per CTA in the prefill route kernels
+constexpr int kRankTokens = 256;      // tokens per rank block in the prefill routing
 constexpr int kTileRows = 256;        // max routed rows per prefill m-tile (MMA N)
 constexpr int kDecodeMaxTokens = 16;
 
@@ -53,15 +58,16 @@ cudaError_t launch_pack(const uint8_t* w13_q, const uint8_t* w13_s, const uint8_
 cudaError_t launch_debug_dequant(const uint8_t* blob, const float* gscale, int H, int I, int expert,
                                  int which, int via_bf16, float* out, cudaStream_t st);
 
-cudaError_t launch_route_decode(const LayerDims& d, const void* logits, const void* x, int T, int k,
-                                const Workspace& ws, cudaStream_t st);
 cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const void* x, int T, int k,
                                  const Workspace& ws, cudaStream_t st);
 
-// `mid` (may be null) is recorded on the stream between the gate/up and the
-// down kernels (per-stage timing).
-cudaError_t launch_decode_ffn(const LayerDims& d, const uint8_t* blob, const float* gscale, int T, int k,
-                              cudaEvent_t mid, int num_sms, const Workspace& ws, cudaStream_t st);
+// The whole decode forward (route, gate/up, down, combine) as one cooperative
+// kernel; route_only = 1 runs the routing phase alone on one CTA and writes
+// the tables (ids, wts, offsets, perm, inv) to the workspace.
+cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const float* gscale, const void* logits,
+                                  const void* x, int T, int k, void* out, int route_only, int num_sms,
+                                  const Workspace& ws, cudaStream_t st);
+size_t decode_smem_bytes();
 
 struct PrefillMaps {
   CUtensorMap x_perm;  // [R][H] bf16, box {64, 16}, 128B swizzle

@@ -1,0 +1,120 @@
+// Routing primitives shared by the decode and prefill kernels.
+//
+// Readings (the pages do not state the scoring rule): top-k by logit, equal
+// logits -> lower expert index, NaN below -inf; weights = softmax over the k
+// chosen logits (NaN as -inf; all chosen -inf -> 1/k each; any +inf -> the +inf
+// entries share weight 1); rows ordered expert-major, ascending t*k+j inside
+// an expert.  The routers are BF16 linears ("GLM-5.3-Flash on Blackwell",
+// The quantization), so their logits are this layer's input.
+#pragma once
+#include "common.cuh"
+
+namespace nvfp4moe {
+
+__device__ __forceinline__ float load_logit(const void* logits, int bf16, size_t i) {
+  if (bf16) {
+    const unsigned short b = reinterpret_cast<const unsigned short*>(logits)[i];
+    return __uint_as_float((uint32_t)b << 16);
+  }
+  return reinterpret_cast<const float*>(logits)[i];
+}
+
+// One warp routes token t (E <= 256, k <= 16).  Lane j < k receives the j-th
+// choice in (*my_id, *my_w); returns the number of NaN logits of the token.
+__device__ __forceinline__ int warp_topk(const void* logits, int bf16, int E, int k, int t, int* my_id,
+                                         float* my_w) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long key[8];
+  float val[8];
+  int nan_count = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float v = load_logit(logits, bf16, (size_t)t * E + e);
+      nan_count += (v != v);
+      val[i] = v;
+      key[i] = ((unsigned long long)float_key(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
+    } else {
+      val[i] = 0.f;
+      key[i] = 0ull;
+    }
+  }
+  int id = -1;
+  float logit = 0.f;
+  for (int j = 0; j < k; ++j) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) best = key[i] > best ? key[i] : best;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+      best = other > best ? other : best;
+    }
+    const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+    float v = 0.f;
+    if ((e & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (lane + 32 * i == e) {
+          key[i] = 0ull;
+          v = val[i];
+        }
+    }
+    v = __shfl_sync(0xffffffffu, v, e & 31);
+    if (lane == j) {
+      id = e;
+      logit = v;
+    }
+  }
+  const float l = (lane < k) ? (logit != logit ? -INFINITY : logit) : -INFINITY;
+  float m = l;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float ex;
+  if (m == -INFINITY) {
+    ex = (lane < k) ? 1.0f : 0.0f;
+  } else if (m == INFINITY) {
+    ex = (lane < k && l == INFINITY) ? 1.0f : 0.0f;
+  } else {
+    ex = (lane < k) ? expf(l - m) : 0.0f;
+  }
+  float sum = 0.f;  // slot order j = 0..k-1, identical on every lane
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
+  *my_id = id;
+  *my_w = ex / sum;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) nan_count += __shfl_xor_sync(0xffffffffu, nan_count, o);
+  return nan_count;
+}
+
+// Exclusive scan of v over the block (<= 1024 threads, all call); *total gets
+// the sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* smem_warp /*[32]*/, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) smem_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = (blockDim.x + 31) >> 5;
+    int w = lane < nw ? smem_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    smem_warp[lane] = w;  // inclusive
+  }
+  __syncthreads();
+  const int before = warp ? smem_warp[warp - 1] : 0;
+  *total = smem_warp[((blockDim.x + 31) >> 5) - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+}  // namespace nvfp4moe

@@ -6,7 +6,8 @@
 // budget), and static-memory runtimes that allocate everything once at start
 // and forbid allocation afterwards.  They cannot create a handle, because
 // nvfp4_moe_create allocates the weight blob and the workspace.  This entry
-// point runs the decode path (route, gate/up GEMV, down GEMV, combine) with
+// point runs the decode path (one fused kernel: route, gate/up GEMV, down
+// GEMV, combine) with
 // the caller's own weight blob, activations and output; every intermediate
 // (routing tables, h, y, the GEMVs' split-K partial sums and counters) lives
 // in one file-scope __device__ array of kStaticScratchBytes.
@@ -87,6 +88,10 @@ size_t carve(uint8_t* base, int E, int H, int I, int T, int k, Workspace* ws, si
   w.cnt_gu = r.take<int32_t>(b, maxU * (2 * I / 64));
   w.part_dn = r.take<float>(b, maxU * (H / 64) * 1024);
   w.cnt_dn = r.take<int32_t>(b, maxU * (H / 64));
+  w.done_gu = r.take<int32_t>(b, maxU);
+  w.cmb = r.take<int32_t>(b, H / 64);
+  w.exit_cnt = r.take<int32_t>(b, 1);
+  w.hmax = r.take<uint32_t>(b, R);
   w.status = r.take<DeviceStatus>(b, 1);
   *zero_bytes = (r.off + 255) & ~size_t(255);
   w.ids = r.take<int32_t>(b, R);
@@ -101,7 +106,6 @@ size_t carve(uint8_t* base, int E, int H, int I, int T, int k, Workspace* ws, si
   w.x16 = r.take<__half>(b, (size_t)T * H);
   w.xexp = r.take<int32_t>(b, T);
   w.h = r.take<__nv_bfloat16>(b, R * I);
-  w.hmax = r.take<uint32_t>(b, R);
   w.y = r.take<float>(b, R * H);
   if (base && ws) *ws = w;
   return r.off;
@@ -141,8 +145,8 @@ extern "C" nvfp4_moe_status nvfp4_moe_forward_decode_static(const uint8_t* packe
   carve(setup.scratch, E, H, I, T, top_k, &ws, &zero_bytes);
   const LayerDims d{E, H, I, logits_dtype == NVFP4_MOE_LOGITS_BF16, 0};
   cudaError_t e = cudaMemsetAsync(setup.scratch, 0, zero_bytes, stream);
-  if (e == cudaSuccess) e = launch_route_decode(d, router_logits, x, T, top_k, ws, stream);
-  if (e == cudaSuccess) e = launch_decode_ffn(d, packed_experts, gscale, T, top_k, nullptr, setup.num_sms, ws, stream);
-  if (e == cudaSuccess) e = launch_combine(d, T, top_k, ws, out, stream);
+  if (e == cudaSuccess)
+    e = launch_decode_forward(d, packed_experts, gscale, router_logits, x, T, top_k, out, 0, setup.num_sms, ws,
+                              stream);
   return e == cudaSuccess ? NVFP4_MOE_OK : NVFP4_MOE_ERR_CUDA;
 }
