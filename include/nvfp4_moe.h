@@ -153,10 +153,11 @@ nvfp4_moe_status nvfp4_moe_set_path(nvfp4_moe_t h, int path);
  *   router_logits [T][E] (logits_dtype), x [T][H] BF16, out [T][H] BF16
  * 1 <= T <= 16, 1 <= top_k <= min(E, 16); H, I as in nvfp4_moe_config.
  * All intermediates live in one static device array of 16 MiB that every GPU
- * loading this library holds until the process exits.  A shape whose
- * intermediates need more than that (about 7.3 MiB for E=128, H=4096,
- * I=1536, T=2, top_k=8; the split-K partial sums grow with
- * min(E, T*top_k) * (2I + H) * 64 bytes) returns
+ * loading this library holds until the process exits.  This path gives each
+ * GPU warp whole row blocks (no split-K partial sums), so it needs about
+ * T*top_k*(2I + 4H) bytes plus small tables -- under 1 MiB for E=128, H=4096,
+ * I=1536, T=2, top_k=8 -- but balances less evenly than nvfp4_moe_forward.
+ * A shape needing more than the array returns
  * NVFP4_MOE_ERR_UNSUPPORTED_SHAPE before anything is enqueued.  The regions
  * that must start at zero are cleared by every call.  The first call on each
  * device looks up the array's device address with that device current: make

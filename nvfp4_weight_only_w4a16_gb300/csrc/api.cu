@@ -221,9 +221,9 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* c, nvfp4_moe_t* out) {
   cv.add(&w.h, Rm * I);
   cv.add(&w.hmax, Rm);
   cv.add(&w.y, Rm * H);
-  cv.add(&w.part_gu, maxU * (2 * I / 64) * 1024);
+  cv.add(&w.part_gu, decode_part_floats(h->num_sms, kDecodeMaxTokens));
   cv.add(&w.cnt_gu, maxU * (2 * I / 64));
-  cv.add(&w.part_dn, maxU * (H / 64) * 1024);
+  cv.add(&w.part_dn, decode_part_floats(h->num_sms, kDecodeMaxTokens));
   cv.add(&w.cnt_dn, maxU * (H / 64));
   cv.add(&w.done_gu, maxU);
   cv.add(&w.cmb, H / 64);

@@ -12,14 +12,17 @@
 // Design (GB300):
 //  * one launch per forward, one 16-warp CTA per SM (cooperative, so all CTAs
 //    are resident); every CTA routes the <= 16 tokens itself (a few KB of
-//    logits), so no routing tables cross CTAs before the GEMVs start;
+//    logits; one thread per logit ranks it against its row in shared memory
+//    when T*E <= 512), so no routing tables cross CTAs before the GEMVs start;
 //  * stream-K work split: the flat list of (touched expert, 64-row block,
 //    64-wide K chunk) items is cut into equal contiguous ranges, one per warp,
 //    so every SM streams the same number of weight bytes whatever the
 //    routing; partial sums of a block split across warps meet in an FP32
 //    buffer and the last warp to arrive (atomic counter) finishes the block;
-//  * each warp runs its own 3-stage cp.async ring in shared memory (weights,
-//    scales and the activation slice of a chunk), ~110 KB in flight per SM;
+//  * each warp runs its own ring in shared memory (3-4 stages): one lane
+//    issues cp.async.bulk copies of a chunk's codes (2 KB), scales (256 B) and
+//    the routed rows' activation slices (128 B each) onto the stage's
+//    mbarrier, so no per-thread copy is in flight when a warp fences;
 //  * dequantisation: hardware E2M1->FP16 converts (two weights each) times the
 //    E4M3 group scale in FP16 (exact); the dot products run on mma.sync
 //    m16n8k16 (FP16 in, FP32 accumulate) -- about one instruction per weight;
@@ -41,12 +44,13 @@ namespace dec {
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRG = 4;               // 16-row groups per 64-row block
-constexpr int kStages = 3;
 constexpr int kStA = 0;              // 4 x 512 B weight codes
 constexpr int kStS = 2048;           // 4 x 64 B scales
-constexpr int kStB = 2304;           // 2 token groups x 32 lanes x 32 B (BF16 activations)
-constexpr int kStageBytes = 4352;
-constexpr int kPartFloats = 1024;    // [rg 4][row 16][token 16]
+constexpr int kStB = 2304;           // NG token groups x 8 rows x 144 B (BF16 x 64, padded: no bank conflicts)
+constexpr int kRowPitch = 144;
+__host__ __device__ constexpr int stage_bytes(int ng) { return kStB + 8 * kRowPitch * ng; }
+// split-K partial sums: per warp, two slots (its first and its last segment),
+// each [rg 4][row 16][mslot] FP32 with mslot = min(T, 16)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 }  // namespace dec
 
@@ -91,6 +95,8 @@ struct FusedArgs {
   int32_t* cnt_gu;
   float* part_dn;
   int32_t* cnt_dn;
+  int mslot;     // token columns of a partial-sum slot
+  int no_split;  // 1: every warp takes whole blocks (no split-K, no partial-sum buffers)
   int32_t* done_gu;
   int32_t* cmb;
   int32_t* exit_cnt;
@@ -99,17 +105,29 @@ struct FusedArgs {
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }
-__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(smem_addr(bar)),
+               "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// global -> shared bulk copy completing on an mbarrier (16-byte aligned, size % 16 == 0)
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
 }
 __device__ __forceinline__ uint64_t now_ns() {
   uint64_t t;
@@ -123,6 +141,22 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
 }
 __device__ __forceinline__ bool aborted(const DeviceStatus* st) {
   return (*reinterpret_cast<const volatile unsigned*>(&st->flags) & kFlagTimeout) != 0;
+}
+
+// Bounded wait on a ring stage; false if this or another warp gave up.
+__device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, DeviceStatus* st) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = now_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 63u) {
+      if (aborted(st)) return false;
+      if (now_ns() - t0 > dec::kTimeoutNs) {
+        report(st, kFlagTimeout, 300);
+        return false;
+      }
+    }
+  }
 }
 
 // 8 E2M1 codes (one 32-bit word, element 2j in the low nibble of byte j) ->
@@ -141,36 +175,88 @@ __device__ __forceinline__ float pow2f(int p) {
 }
 
 // ---------------------------------------------------------------------------
-// Phase 0: every CTA routes the T tokens into shared memory.
+// Phase 0: every CTA routes the T tokens into shared memory, and takes each
+// token's max |x| for the FP16 prescale.  `scratch` (>= T*E*8 bytes) is the
+// ring memory, free until the GEMVs start.
 // ---------------------------------------------------------------------------
-__device__ void route_block(const FusedArgs& a, RouteSmem& rs) {
+__device__ void route_block(const FusedArgs& a, RouteSmem& rs, uint8_t* scratch) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int T = a.T, k = a.k, E = a.E, R = T * k;
+  const int T = a.T, k = a.k, E = a.E, R = T * k, TE = T * E;
+  const bool by_rank = TE <= dec::kThreads;  // one thread per logit
+  uint32_t* keys = reinterpret_cast<uint32_t*>(scratch);
+  float* vals = reinterpret_cast<float*>(scratch + 4 * dec::kThreads);
   if (tid < 16) rs.xmax[tid] = 0u;
   if (tid == 0) rs.nan = 0;
   __syncthreads();
-  if (warp < T) {
+  // logits -> orderable keys (rank path); per-token max |x| on every thread
+  int nan = 0;
+  if (by_rank && tid < TE) {
+    const float v = load_logit(a.logits, a.logits_bf16, tid);
+    nan = (v != v);
+    keys[tid] = float_key(v);
+    vals[tid] = v;
+  }
+  if (a.x) {  // 8 independent 16-byte loads in flight per thread
+    const int per_row = a.H / 8, n = T * per_row;
+    for (int base = tid; base < n; base += 8 * blockDim.x) {
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = base + j * blockDim.x;
+        if (i < n) {
+          const int t = i / per_row;
+          v[j] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H) + (i - t * per_row));
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = base + j * blockDim.x;
+        if (i < n) {
+          const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+          float m = 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[q] << 16)), fabsf(__uint_as_float(wv[q] & 0xFFFF0000u))));
+          atomicMax(&rs.xmax[i / per_row], __float_as_uint(m));
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (by_rank) {
+    // rank of logit (t, e) in its row: larger key first, lower index on ties
+    if (tid < TE) {
+      const int t = tid / E, e = tid - t * E;
+      const uint32_t kk = keys[tid];
+      const uint32_t* row = keys + t * E;
+      int r = 0;
+      for (int e2 = 0; e2 < E; ++e2) {
+        const uint32_t k2 = row[e2];
+        r += (k2 > kk) | ((k2 == kk) & (e2 < e));
+      }
+      if (r < k) {
+        rs.ids[t * k + r] = e;
+        rs.wts[t * k + r] = vals[tid];  // the chosen logit, turned into a weight below
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nan += __shfl_xor_sync(0xffffffffu, nan, o);
+    if (lane == 0 && nan) atomicAdd(&rs.nan, nan);
+    __syncthreads();
+    if (warp < T) {
+      const float w = warp_softmax_k(lane < k ? rs.wts[warp * k + lane] : 0.f, k);
+      __syncwarp();
+      if (lane < k) rs.wts[warp * k + lane] = w;
+    }
+  } else if (warp < T) {
     int id;
     float w;
-    const int nan = warp_topk(a.logits, a.logits_bf16, E, k, warp, &id, &w);
+    const int nt = warp_topk(a.logits, a.logits_bf16, E, k, warp, &id, &w);
     if (lane < k) {
       rs.ids[warp * k + lane] = id;
       rs.wts[warp * k + lane] = w;
     }
-    if (lane == 0 && nan) atomicAdd(&rs.nan, nan);
-  }
-  if (a.x) {  // per-token max |x| for the FP16 prescale
-    const int per_row = a.H / 8;
-    for (int i = tid; i < T * per_row; i += blockDim.x) {
-      const int t = i / per_row;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H) + (i - t * per_row));
-      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-      float m = 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[q] << 16)), fabsf(__uint_as_float(wv[q] & 0xFFFF0000u))));
-      atomicMax(&rs.xmax[t], __float_as_uint(m));
-    }
+    if (lane == 0 && nt) atomicAdd(&rs.nan, nt);
   }
   __syncthreads();
   int c = 0;
@@ -222,26 +308,38 @@ __device__ void finish_gateup(const FusedArgs& a, const RouteSmem& rs, int u, in
   const int e = rs.tch_e[u], row0 = rs.tch_r0[u], m = rs.tch_m[u];
   const int r0 = lane >> 2, q = lane & 3;
   const float gsg = a.gscale[3 * e], gsu = a.gscale[3 * e + 1];
+  float hmax[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // per token slot (i, c) of this lane
 #pragma unroll
-  for (int rg = 0; rg < dec::kRG; ++rg)
+  for (int i = 0; i < 2; ++i)
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int c = 0; c < 2; ++c) {
+      const int j = 8 * i + 2 * q + c;
+      if (j >= m) continue;
+      const int row = row0 + j;
+      const float s = pow2f(rs.xexp[rs.perm[row] / a.k]);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int j = 8 * i + 2 * q + c;
-        if (j >= m) continue;
-        const int row = row0 + j;
-        const float s = pow2f(rs.xexp[rs.perm[row] / a.k]);
+      for (int rg = 0; rg < dec::kRG; ++rg) {
         const float g = gsg * (acc[rg][i][c] * s);
         const float uu = gsu * (acc[rg][i][2 + c] * s);
         const __nv_bfloat16 hb = __float2bfloat16_rn(silu(g) * uu);
         const int f = 8 * (dec::kRG * b + rg) + r0;
         a.h[(size_t)row * a.I + f] = hb;
-        atomicMax(&a.hmax[row], __float_as_uint(fabsf(__bfloat162float(hb))));
+        hmax[i][c] = fmaxf(hmax[i][c], fabsf(__bfloat162float(hb)));
       }
-  __threadfence();
-  __syncwarp();
-  if (lane == 0) atomicAdd(&a.done_gu[u], 1);
+    }
+  // row maxima: reduce over the 8 lanes that share a token slot, then one
+  // atomic per row from this block
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float v = hmax[i][c];
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+      const int j = 8 * i + 2 * q + c;
+      if (r0 == 0 && j < m) atomicMax(&a.hmax[row0 + j], __float_as_uint(v));
+    }
 }
 
 __device__ void finish_down(const FusedArgs& a, const RouteSmem& rs, int u, int b, float (&acc)[dec::kRG][2][4],
@@ -264,14 +362,11 @@ __device__ void finish_down(const FusedArgs& a, const RouteSmem& rs, int u, int 
         a.y[(size_t)row * a.H + d + 8] = acc[rg][i][2 + c] * s;
       }
     }
-  __threadfence();
-  __syncwarp();
-  int last = 0;
-  if (lane == 0) last = (atomicAdd(&a.cmb[b], 1) + 1 == rs.U);
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __threadfence();
-  // combine the 64-wide slice of H for every token, slot order j = 0..k-1
+}
+
+// The 64-wide slice b of H is complete for every expert: out[t][slice] =
+// sum_j w[t][j] * y[pos(t,j)][slice], slot order j = 0..k-1.
+__device__ void combine_slice(const FusedArgs& a, const RouteSmem& rs, int b, int lane) {
   const int d = 64 * b + 2 * lane;
   for (int t = 0; t < a.T; ++t) {
     float s0 = 0.f, s1 = 0.f;
@@ -288,7 +383,6 @@ __device__ void finish_down(const FusedArgs& a, const RouteSmem& rs, int u, int 
           __floats2bfloat162_rn(s0, s1);
     }
   }
-  if (lane == 0) a.cmb[b] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -318,9 +412,14 @@ __device__ __forceinline__ ItemPos item_at(long long f, int nch, int nblk) {
   return p;
 }
 
-template <bool kGateUp>
-__device__ void run_phase(const FusedArgs& a, const RouteSmem& rs, uint8_t* ring, long long fbeg, long long fend,
-                          unsigned long long* tr = nullptr) {
+template <bool kGateUp, int S, int NG>
+__device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint64_t* bars, uint32_t& ring_it,
+                          long long F, long long W, long long wg, unsigned long long* tr) {
+  const int nch_ = kGateUp ? a.H / kChunk : a.I / kChunk;
+  // split-K: equal chunk ranges; no_split: equal ranges of whole blocks
+  const long long fbeg = a.no_split ? (F / nch_) * wg / W * nch_ : F * wg / W;
+  const long long fend = a.no_split ? (F / nch_) * (wg + 1) / W * nch_ : F * (wg + 1) / W;
+  constexpr int kStageBytes = dec::stage_bytes(NG);
   const int lane = threadIdx.x & 31, q = lane & 3, r0 = lane >> 2;
   const int K = kGateUp ? a.H : a.I;
   const int nch = K / kChunk;
@@ -331,16 +430,15 @@ __device__ void run_phase(const FusedArgs& a, const RouteSmem& rs, uint8_t* ring
   const int nf = (int)(fend - fbeg);
   if (nf <= 0) return;
 
-  // ---- producer state (runs kStages-1 items ahead of the consumer) ----
+  // ---- producer state (runs S-1 items ahead of the consumer) ----
   ItemPos ip = item_at(fbeg, nch, nblk);
-  int ip_u = -1;                         // expert whose per-segment data is cached below
-  const uint8_t* ip_nib = nullptr;       // lane's code pointer at chunk 0 of the block, per rg
+  int ip_u = -1, ip_m = 0;
+  const uint8_t* ip_nib = nullptr;
   const uint8_t* ip_sc = nullptr;
-  const __nv_bfloat16* ip_src[2] = {nullptr, nullptr};
-  int ip_b = -1;
+  const uint8_t* ip_row = nullptr;  // lane j < m: its routed row's activations (bytes)
   bool dead = false;
 
-  auto issue = [&](int slot) {
+  auto issue = [&](uint32_t it) {
     if (ip.u != ip_u) {
       const int u = ip.u;
       if (!kGateUp) {  // h of expert u must be complete
@@ -352,47 +450,42 @@ __device__ void run_phase(const FusedArgs& a, const RouteSmem& rs, uint8_t* ring
               report(a.st, kFlagTimeout, 100 + (unsigned)u);
               break;
             }
-            __nanosleep(100);
+            __nanosleep(64);
           }
         }
         __syncwarp();
         __threadfence();
+        // h was written through the generic proxy; the copies read it through the async proxy
+        asm volatile("fence.proxy.async.global;" ::: "memory");
         if (aborted(a.st)) dead = true;
         if (tr && lane == 0 && tr[3] == 0) tr[3] = now_ns();
       }
-      const int e = rs.tch_e[u], row0 = rs.tch_r0[u], m = rs.tch_m[u];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int j = 8 * i + r0;
-        ip_src[i] = nullptr;
-        if (j < m)
-          ip_src[i] = kGateUp ? a.x + (size_t)(rs.perm[row0 + j] / a.k) * a.H + 16 * q
-                              : a.h + (size_t)(row0 + j) * a.I + 16 * q;
-      }
+      const int e = rs.tch_e[u], row0 = rs.tch_r0[u];
+      ip_m = min(rs.tch_m[u], 8 * NG);
+      ip_row = nullptr;
+      if (lane < ip_m)
+        ip_row = kGateUp ? reinterpret_cast<const uint8_t*>(a.x + (size_t)(rs.perm[row0 + lane] / a.k) * a.H)
+                         : reinterpret_cast<const uint8_t*>(a.h + (size_t)(row0 + lane) * a.I);
       ip_nib = a.blob + (size_t)e * a.expert_stride + nib_off;
       ip_sc = a.blob + (size_t)e * a.expert_stride + sc_off;
       ip_u = u;
-      ip_b = -1;
     }
-    // (rb, c, sb) -> segment; the 4 row groups of block b are sub-blocks 4(b&1)..+3 of row block b>>1
+    const int slot = (int)(it % S);
+    uint8_t* st = ring + slot * kStageBytes;
+    uint64_t* bar = bars + slot;
+    // the 4 row groups of block b are sub-blocks 4(b&1)..+3 of 128-row block b>>1
     const size_t seg0 = ((size_t)(ip.b >> 1) * nch + ip.c) * 8 + 4 * (ip.b & 1);
-    uint8_t* st = ring + slot * dec::kStageBytes;
-#pragma unroll
-    for (int rg = 0; rg < dec::kRG; ++rg)
-      cp_async16(st + dec::kStA + rg * 512 + lane * 16, ip_nib + (seg0 + rg) * 512 + lane * 16);
-    if (lane < 16)
-      cp_async16(st + dec::kStS + (lane >> 2) * 64 + (lane & 3) * 16,
-                 ip_sc + (seg0 + (lane >> 2)) * 64 + (lane & 3) * 16);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const bool valid = ip_src[i] != nullptr;
-      const __nv_bfloat16* src = valid ? ip_src[i] + kChunk * ip.c : a.x;
-      // [group][half][lane] x 16 B: each 16-byte access of a warp is contiguous
-      uint8_t* dst = st + dec::kStB + i * 1024 + lane * 16;
-      cp_async16_zfill(dst, src, valid ? 16 : 0);
-      cp_async16_zfill(dst + 512, valid ? src + 8 : src, valid ? 16 : 0);
+    // earlier generic reads and writes of this memory come before the copies
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (lane == 0) {
+      mbar_expect_tx(bar, 2048u + 256u + 128u * (uint32_t)ip_m);
+      bulk_copy(st + dec::kStA, ip_nib + seg0 * 512, 2048, bar);
+      bulk_copy(st + dec::kStS, ip_sc + seg0 * 64, 256, bar);
     }
-    cp_async_commit();
+    __syncwarp();
+    if (lane < ip_m)
+      bulk_copy(st + dec::kStB + (lane >> 3) * 8 * dec::kRowPitch + (lane & 7) * dec::kRowPitch,
+                ip_row + (size_t)ip.c * 128, 128, bar);
     ip.next(nch, nblk);
   };
 
@@ -401,18 +494,19 @@ __device__ void run_phase(const FusedArgs& a, const RouteSmem& rs, uint8_t* ring
   float acc[dec::kRG][2][4];
   float bsc[2] = {1.f, 1.f};
   int seg_c0 = 0, m = 0, ng = 1;
+  const uint32_t it0 = ring_it;
+  int issued = 0, consumed = 0;
 
-#pragma unroll
-  for (int s = 0; s < dec::kStages - 1; ++s) {
-    if (s < nf) issue(s);
-    else cp_async_commit();
-  }
+  for (; issued < S - 1 && issued < nf; ++issued) issue(it0 + issued);
   for (int i = 0; i < nf && !dead; ++i) {
-    cp_async_wait<dec::kStages - 2>();
-    __syncwarp();
-    if (i + dec::kStages - 1 < nf) issue((i + dec::kStages - 1) % dec::kStages);
-    else cp_async_commit();
+    const uint32_t it = it0 + i;
+    if (issued < nf) issue(it0 + issued++);
     if (dead) break;
+    if (!ring_wait(bars + it % S, (it / S) & 1u, a.st)) {
+      dead = true;
+      break;
+    }
+    consumed = i + 1;
     const int u = cp.u, b = cp.b, c = cp.c;
     if (i == 0 || c == 0) {
       seg_c0 = c;
@@ -437,14 +531,15 @@ __device__ void run_phase(const FusedArgs& a, const RouteSmem& rs, uint8_t* ring
         bsc[gi] = pow2f(-p);
       }
     }
-    const uint8_t* st = ring + (i % dec::kStages) * dec::kStageBytes;
-    // activations: BF16 -> FP16 with the row prescale
+    const uint8_t* st = ring + (int)(it % S) * kStageBytes;
+    // activations: BF16 -> FP16 with the row prescale (rows >= m hold stale
+    // data; their MMA columns are never read)
     uint32_t bw[2][8];
 #pragma unroll
-    for (int gi = 0; gi < 2; ++gi) {
+    for (int gi = 0; gi < NG; ++gi) {
       if (gi < ng) {
-        const uint8_t* p = st + dec::kStB + gi * 1024 + lane * 16;
-        const uint4 u0 = *reinterpret_cast<const uint4*>(p), u1 = *reinterpret_cast<const uint4*>(p + 512);
+        const uint8_t* p = st + dec::kStB + gi * 8 * dec::kRowPitch + r0 * dec::kRowPitch + q * 32;
+        const uint4 u0 = *reinterpret_cast<const uint4*>(p), u1 = *reinterpret_cast<const uint4*>(p + 16);
         const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
         for (int z = 0; z < 8; ++z) {
@@ -477,94 +572,180 @@ __device__ void run_phase(const FusedArgs& a, const RouteSmem& rs, uint8_t* ring
         const uint32_t* r8w = kt < 2 ? cz : cw;
         const int o = 2 * (kt & 1);
         mma_f16_16816(acc[rg][0], r0w[o], r8w[o], r0w[o + 1], r8w[o + 1], bw[0][2 * kt], bw[0][2 * kt + 1]);
-        if (ng > 1)
+        if (NG > 1 && ng > 1)
           mma_f16_16816(acc[rg][1], r0w[o], r8w[o], r0w[o + 1], r8w[o + 1], bw[1][2 * kt], bw[1][2 * kt + 1]);
       }
     }
+    __syncwarp();  // every lane is done reading this stage before it is refilled
     cp.next(nch, nblk);
     const bool seg_end = (c == nch - 1) || (i == nf - 1);
     if (!seg_end) continue;
-    if (seg_c0 == 0 && c == nch - 1) {
+    if (seg_c0 == 0 && c == nch - 1) {  // the whole block is this warp's: finish it now, signal later
       if (kGateUp) finish_gateup(a, rs, u, b, acc, lane);
       else finish_down(a, rs, u, b, acc, lane);
       continue;
     }
-    // partial block: add into the FP32 buffer; the last arriver finishes it
-    const int blk = u * nblk + b;
-    float* part = (kGateUp ? a.part_gu : a.part_dn) + (size_t)blk * dec::kPartFloats;
-    int32_t* cnt = (kGateUp ? a.cnt_gu : a.cnt_dn) + blk;
+    // part of a block: store the partial sums into this warp's slot (0: its
+    // first segment, 1: its last); counted at the end of the phase
+    {
+      const int slot = (i + 1 - (c - seg_c0 + 1) == 0) ? 0 : 1;  // did the segment start at the range start?
+      float* part = (kGateUp ? a.part_gu : a.part_dn) + ((size_t)wg * 2 + slot) * 64 * a.mslot;
 #pragma unroll
-    for (int rg = 0; rg < dec::kRG; ++rg)
+      for (int rg = 0; rg < dec::kRG; ++rg)
 #pragma unroll
-      for (int gi = 0; gi < 2; ++gi)
+        for (int gi = 0; gi < 2; ++gi)
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int j = 8 * gi + 2 * q + cc;
-          if (j < m) {
-            atomicAdd(part + rg * 256 + r0 * 16 + j, acc[rg][gi][cc]);
-            atomicAdd(part + rg * 256 + (r0 + 8) * 16 + j, acc[rg][gi][2 + cc]);
+          for (int cc = 0; cc < 2; ++cc) {
+            const int j = 8 * gi + 2 * q + cc;
+            if (j < m) {
+              __stcg(part + (rg * 16 + r0) * a.mslot + j, acc[rg][gi][cc]);
+              __stcg(part + (rg * 16 + r0 + 8) * a.mslot + j, acc[rg][gi][2 + cc]);
+            }
           }
-        }
+    }
+  }
+
+  // ---- end of phase: one fence covers every store and partial sum above ----
+  if (!dead) {
+    const uint64_t t_fin = tr ? now_ns() : 0;
     __threadfence();
     __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-      const int add = c - seg_c0 + 1;
-      last = (atomicAdd(cnt, add) + add == nch);
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) continue;
-    __threadfence();
-#pragma unroll
-    for (int rg = 0; rg < dec::kRG; ++rg)
-#pragma unroll
-      for (int gi = 0; gi < 2; ++gi)
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int j = 8 * gi + 2 * q + cc;
-          if (j < m) {
-            float* p0 = part + rg * 256 + r0 * 16 + j;
-            float* p1 = part + rg * 256 + (r0 + 8) * 16 + j;
-            acc[rg][gi][cc] = __ldcg(p0);
-            acc[rg][gi][2 + cc] = __ldcg(p1);
-            __stcg(p0, 0.f);
-            __stcg(p1, 0.f);
-          }
+    // walk this warp's segments: count partial ones in; the last contributor
+    // of a block finishes it
+    uint64_t fin_mask = 0;
+    int si = 0;
+    // signals a finished block; used at once for segments past the 64-bit mask
+    auto signal = [&](int blk) {
+      const int u = blk / nblk, b = blk - (blk / nblk) * nblk;
+      if (kGateUp) {
+        if (lane == 0) atomicAdd(&a.done_gu[u], 1);
+      } else {
+        int lastc = 0;
+        if (lane == 0) lastc = (atomicAdd(&a.cmb[b], 1) + 1 == rs.U);
+        lastc = __shfl_sync(0xffffffffu, lastc, 0);
+        if (lastc) {
+          __threadfence();
+          combine_slice(a, rs, b, lane);
+          if (lane == 0) a.cmb[b] = 0;
         }
-    if (lane == 0) *cnt = 0;
-    if (kGateUp) finish_gateup(a, rs, u, b, acc, lane);
-    else finish_down(a, rs, u, b, acc, lane);
+      }
+    };
+    for (long long f = fbeg; f < fend; ++si) {
+      const int blk = (int)(f / nch), c0 = (int)(f % nch);
+      const int c1 = (int)min((long long)nch, c0 + (fend - f));
+      f += c1 - c0;
+      if (c0 == 0 && c1 == nch) {
+        if (si < 64) fin_mask |= 1ull << si;
+        else signal(blk);
+        continue;
+      }
+      int last = 0;
+      if (lane == 0) last = (atomicAdd((kGateUp ? a.cnt_gu : a.cnt_dn) + blk, c1 - c0) + (c1 - c0) == nch);
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (!last) continue;
+      __threadfence();
+      const int u = blk / nblk, b = blk - (blk / nblk) * nblk;
+      const int mm = rs.tch_m[u];
+#pragma unroll
+      for (int rg = 0; rg < dec::kRG; ++rg)
+#pragma unroll
+        for (int gi = 0; gi < 2; ++gi)
+#pragma unroll
+          for (int z = 0; z < 4; ++z) acc[rg][gi][z] = 0.f;
+      // contributors: the warps whose ranges meet [f0, f0 + nch)
+      const long long f0 = (long long)blk * nch;
+      const long long w_lo = ((f0 + 1) * W + F - 1) / F - 1, w_hi = ((f0 + nch) * W + F - 1) / F - 1;
+      for (long long w = w_lo; w <= w_hi; ++w) {
+        const long long s0 = F * w / W, s1 = F * (w + 1) / W;
+        if (s0 >= s1 || s1 <= f0 || s0 >= f0 + nch) continue;
+        const int slot = s0 >= f0 ? 0 : 1;
+        const float* part = (kGateUp ? a.part_gu : a.part_dn) + ((size_t)w * 2 + slot) * 64 * a.mslot;
+#pragma unroll
+        for (int rg = 0; rg < dec::kRG; ++rg)
+#pragma unroll
+          for (int gi = 0; gi < 2; ++gi)
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int j = 8 * gi + 2 * q + cc;
+              if (j < mm) {
+                acc[rg][gi][cc] += __ldcg(part + (rg * 16 + r0) * a.mslot + j);
+                acc[rg][gi][2 + cc] += __ldcg(part + (rg * 16 + r0 + 8) * a.mslot + j);
+              }
+            }
+      }
+      if (lane == 0) (kGateUp ? a.cnt_gu : a.cnt_dn)[blk] = 0;
+      if (kGateUp) finish_gateup(a, rs, u, b, acc, lane);
+      else finish_down(a, rs, u, b, acc, lane);
+      if (si < 64) {
+        fin_mask |= 1ull << si;
+      } else {
+        __threadfence();
+        __syncwarp();
+        signal(blk);
+      }
+    }
+    // signal the blocks this warp finished (after one more fence)
+    if (fin_mask) {
+      __threadfence();
+      __syncwarp();
+      si = 0;
+      for (long long f = fbeg; f < fend && si < 64; ++si) {
+        const int blk = (int)(f / nch), c0 = (int)(f % nch);
+        const int c1 = (int)min((long long)nch, c0 + (fend - f));
+        f += c1 - c0;
+        if ((fin_mask >> si) & 1ull) signal(blk);
+      }
+    }
+    if (tr && lane == 0) tr[kGateUp ? 6 : 7] += now_ns() - t_fin;
   }
-  cp_async_wait<0>();
-  __syncwarp();
+  // on a normal exit every issued stage was consumed; after an abort, give the
+  // copies still in flight a bounded chance to land before the ring is reused
+  if (dead) {
+    for (int i = consumed; i < issued; ++i) {
+      const uint32_t it = it0 + i;
+      const uint64_t t0 = now_ns();
+      while (!mbar_try_wait(bars + it % S, (it / S) & 1u) && now_ns() - t0 < dec::kTimeoutNs) {
+      }
+    }
+  }
+  ring_it = it0 + (uint32_t)issued;
 }
 
+template <int S, int NG>
 __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   RouteSmem& rs = *reinterpret_cast<RouteSmem*>(smem);
-  uint8_t* rings = smem + ((sizeof(RouteSmem) + 127) & ~size_t(127));
-  const int warp = threadIdx.x >> 5;
-  uint8_t* ring = rings + warp * dec::kStages * dec::kStageBytes;
+  const size_t route_bytes = (sizeof(RouteSmem) + 127) & ~size_t(127);
+  uint64_t* all_bars = reinterpret_cast<uint64_t*>(smem + route_bytes);
+  uint8_t* rings = smem + route_bytes + 128 * 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = rings + warp * S * dec::stage_bytes(NG);
+  uint64_t* bars = all_bars + warp * 8;
 
   const uint64_t t_start = now_ns();
-  route_block(a, rs);
+  route_block(a, rs, rings);
   if (a.route_only) return;
   unsigned long long* tr = a.trace ? a.trace + ((size_t)blockIdx.x * dec::kWarps + warp) * 8 : nullptr;
-  const int lane0 = (threadIdx.x & 31) == 0;
-  if (tr && lane0) {
+  if (tr && lane == 0) {
     tr[0] = t_start;
     tr[1] = now_ns();
   }
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(bars + s, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
 
   const long long W = (long long)gridDim.x * dec::kWarps;
   const long long wg = (long long)blockIdx.x * dec::kWarps + warp;
   const int U = rs.U;
+  uint32_t ring_it = 0;
   const long long F1 = (long long)U * (2 * a.I / 64) * (a.H / kChunk);
-  run_phase<true>(a, rs, ring, F1 * wg / W, F1 * (wg + 1) / W);
-  if (tr && lane0) tr[2] = now_ns();
+  run_phase<true, S, NG>(a, rs, ring, bars, ring_it, F1, W, wg, tr);
+  if (tr && lane == 0) tr[2] = now_ns();
   const long long F2 = (long long)U * (a.H / 64) * (a.I / kChunk);
-  run_phase<false>(a, rs, ring, F2 * wg / W, F2 * (wg + 1) / W, tr);
-  if (tr && lane0) tr[4] = now_ns();
+  run_phase<false, S, NG>(a, rs, ring, bars, ring_it, F2, W, wg, tr);
+  if (tr && lane == 0) tr[4] = now_ns();
 
   // the last CTA out resets the per-forward counters (and, after a timeout,
   // every partial sum) for the next forward
@@ -574,7 +755,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
     rs.last_cta = atomicAdd(a.exit_cnt, 1) == (int)gridDim.x - 1;
   }
   __syncthreads();
-  if (tr && lane0) tr[5] = now_ns();
+  if (tr && lane == 0) tr[5] = now_ns();
   if (!rs.last_cta) return;
   __threadfence();
   const int R = a.T * a.k;
@@ -582,8 +763,6 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
   for (int i = threadIdx.x; i < R; i += blockDim.x) a.hmax[i] = 0u;
   if (aborted(a.st)) {
     const size_t ngu = (size_t)U * (2 * a.I / 64), ndn = (size_t)U * (a.H / 64);
-    for (size_t i = threadIdx.x; i < ngu * dec::kPartFloats; i += blockDim.x) a.part_gu[i] = 0.f;
-    for (size_t i = threadIdx.x; i < ndn * dec::kPartFloats; i += blockDim.x) a.part_dn[i] = 0.f;
     for (size_t i = threadIdx.x; i < ngu; i += blockDim.x) a.cnt_gu[i] = 0;
     for (size_t i = threadIdx.x; i < ndn; i += blockDim.x) a.cnt_dn[i] = 0;
     for (int i = threadIdx.x; i < a.H / 64; i += blockDim.x) a.cmb[i] = 0;
@@ -592,17 +771,24 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
   if (threadIdx.x == 0) *a.exit_cnt = 0;
 }
 
-size_t decode_smem_bytes() {
-  return ((sizeof(RouteSmem) + 127) & ~size_t(127)) + (size_t)dec::kWarps * dec::kStages * dec::kStageBytes;
+// T <= 8: one token group per expert, 4 stages; T <= 16: two groups, 3 stages.
+static size_t smem_for(int S, int NG) {
+  return ((sizeof(RouteSmem) + 127) & ~size_t(127)) + 128 * 8 + (size_t)dec::kWarps * S * dec::stage_bytes(NG);
 }
+size_t decode_smem_bytes() { return smem_for(3, 2); }
 
 cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const float* gscale, const void* logits,
                                   const void* x, int T, int k, void* out, int route_only, int num_sms,
                                   const Workspace& ws, cudaStream_t st) {
   static int attr_done = 0;
-  const size_t smem = decode_smem_bytes();
+  const bool small = T <= 8;
+  const size_t smem = small ? smem_for(4, 1) : smem_for(3, 2);
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_for(4, 1));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_fused_kernel<3, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_for(3, 2));
     if (e != cudaSuccess) return e;
     attr_done = 1;
   }
@@ -638,6 +824,8 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
   a.cnt_gu = ws.cnt_gu;
   a.part_dn = ws.part_dn;
   a.cnt_dn = ws.cnt_dn;
+  a.mslot = T < 16 ? T : 16;
+  a.no_split = ws.part_gu == nullptr;
   a.done_gu = ws.done_gu;
   a.cmb = ws.cmb;
   a.exit_cnt = ws.exit_cnt;
@@ -653,7 +841,8 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = route_only ? 0 : 1;
-  return cudaLaunchKernelEx(&cfg, decode_fused_kernel, a);
+  return small ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<4, 1>, a)
+               : cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 2>, a);
 }
 
 }  // namespace nvfp4moe

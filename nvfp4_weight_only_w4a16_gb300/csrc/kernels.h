@@ -24,10 +24,10 @@ struct Workspace {
   __nv_bfloat16* h;    // [R][I]   silu(g)*u rounded to BF16, position order
   uint32_t* hmax;      // [R]      max |h| of each row (float bits, decode path)
   float* y;            // [R][H]   expert outputs, position order
-  float* part_gu;      // stream-K partial sums, gate/up  [maxU * I/32][1024]
-  int32_t* cnt_gu;     // arrival counters                [maxU * I/32]
-  float* part_dn;      // stream-K partial sums, down     [maxU * H/64][1024]
-  int32_t* cnt_dn;     //                                 [maxU * H/64]
+  float* part_gu;      // split-K partial sums, gate/up: per decode warp 2 slots of [64][min(T,16)]
+  int32_t* cnt_gu;     // arrival counters per gate/up block  [maxU * I/32]
+  float* part_dn;      // split-K partial sums, down: as part_gu
+  int32_t* cnt_dn;     // arrival counters per down block     [maxU * H/64]
   int32_t* done_gu;    // finished gate/up blocks per touched expert [maxU] (decode)
   int32_t* cmb;        // finished down blocks per 64-wide slice of H [H/64] (decode)
   int32_t* exit_cnt;   // CTAs that finished the decode kernel [1]
@@ -52,6 +52,11 @@ struct LayerDims {
 constexpr int kRankTokens = 256;      // tokens per rank block in the prefill routing
 constexpr int kTileRows = 256;        // max routed rows per prefill m-tile (MMA N)
 constexpr int kDecodeMaxTokens = 16;
+constexpr int kDecodeWarpsPerSm = 16;  // warps of the decode kernel's one CTA per SM
+// floats of the decode kernel's split-K partial-sum buffer (per phase)
+inline size_t decode_part_floats(int num_sms, int T) {
+  return (size_t)num_sms * kDecodeWarpsPerSm * 2 * 64 * (size_t)(T < 16 ? T : 16);
+}
 
 cudaError_t launch_pack(const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
                         const uint8_t* w2_s, uint8_t* blob, int E, int H, int I, cudaStream_t st);

@@ -31,15 +31,23 @@
 namespace nvfp4moe {
 
 namespace pf {
-constexpr int kStages = 4;
-constexpr int kAOff = 0;            // 128 rows x 128 B (BF16 x 64)
-constexpr int kBOff = 16384;        // up to 256 rows x 128 B
-constexpr int kRawOff = 49152;      // 4096 B packed nibbles (128 rows x 64)
-constexpr int kScOff = 53248;       // 512 B scales
-constexpr int kStageBytes = 54272;  // multiple of 1024
-constexpr int kBarOff = kStages * kStageBytes;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + barriers + alignment slack
-constexpr int kThreads = 320;
+// Shared-memory rings (each stage is one 64-wide K chunk of one work unit):
+//   A   : BF16 operand written by the dequantisers, read by tcgen05.mma
+//   B   : routed activation rows (TMA, 128B swizzle), up to 256 rows
+//   RAW : packed FP4 codes + scales of 128 weight rows (bulk copy) -- deep,
+//         so the HBM latency of the weight stream is covered
+constexpr int kAStages = 2;
+constexpr int kBStages = 4;
+constexpr int kRawStages = 12;
+constexpr int kAStageBytes = 16384;      // 128 rows x 128 B
+constexpr int kBStageBytes = 32768;      // up to 256 routed rows x 128 B
+constexpr int kRawStageBytes = 4608;     // 4096 B codes + 512 B scales
+constexpr int kAOff = 0;
+constexpr int kBOff = kAOff + kAStages * kAStageBytes;
+constexpr int kRawOff = kBOff + kBStages * kBStageBytes;
+constexpr int kBarOff = kRawOff + kRawStages * kRawStageBytes;
+constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
+constexpr int kThreads = 352;                     // 11 warps
 constexpr int kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // a wait longer than 2 s is a fault
 }  // namespace pf
@@ -163,9 +171,9 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 
 // Dequantise one packed 16-byte segment (rows R0, R0+8; K elements 16q..16q+15
 // of the chunk) into the swizzled BF16 operand tile at a_base.
-__device__ __forceinline__ void dequant_segment(const uint8_t* stage, uint32_t a_base, int seg) {
-  const uint4 raw = *reinterpret_cast<const uint4*>(stage + pf::kRawOff + seg * 16);
-  const uint32_t sc = *reinterpret_cast<const uint16_t*>(stage + pf::kScOff + seg * 2);
+__device__ __forceinline__ void dequant_segment(const uint8_t* raw_stage, uint32_t a_base, int seg) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(raw_stage + seg * 16);
+  const uint32_t sc = *reinterpret_cast<const uint16_t*>(raw_stage + 4096 + seg * 2);
   const uint32_t s2 = e4m3x2_to_f16x2(sc);
   const int R0 = (seg >> 5) * 16 + ((seg & 31) >> 2);
   const int q = seg & 3;
@@ -192,20 +200,30 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, PrefillArgs a) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + pf::kBarOff);
-  uint64_t* aready = full + pf::kStages;
-  uint64_t* empty = aready + pf::kStages;
-  uint64_t* accfull = empty + pf::kStages;
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + pf::kBarOff);
+  uint64_t* raw_empty = raw_full + pf::kRawStages;
+  uint64_t* a_full = raw_empty + pf::kRawStages;
+  uint64_t* a_empty = a_full + pf::kAStages;
+  uint64_t* b_full = a_empty + pf::kAStages;
+  uint64_t* b_empty = b_full + pf::kBStages;
+  uint64_t* accfull = b_empty + pf::kBStages;
   uint64_t* accempty = accfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < pf::kStages; ++s) {
-      mbar_init(full + s, 1);
-      mbar_init(aready + s, 4);
-      mbar_init(empty + s, 1);
+    for (int s = 0; s < pf::kRawStages; ++s) {
+      mbar_init(raw_full + s, 1);
+      mbar_init(raw_empty + s, 4);
+    }
+    for (int s = 0; s < pf::kAStages; ++s) {
+      mbar_init(a_full + s, 4);
+      mbar_init(a_empty + s, 1);
+    }
+    for (int s = 0; s < pf::kBStages; ++s) {
+      mbar_init(b_full + s, 1);
+      mbar_init(b_empty + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accfull + b, 1);
@@ -231,31 +249,28 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- producer ----------------
+      // ---------------- weight producer: packed codes + scales ----------------
       uint32_t it = 0;
       for (int unit = blockIdx.x; unit < total_units && !*abort_flag && a.fault != 1; unit += gridDim.x) {
         const int tile = unit / a.NB, nb = unit % a.NB;
-        const int e = a.tile_expert[tile], row0 = a.tile_row0[tile], rows = a.tile_rows[tile];
-        const int nbox = (rows + 15) >> 4;
+        const int e = a.tile_expert[tile];
         const uint8_t* src_nib = a.blob + (size_t)e * a.expert_stride + a.nib_off + (size_t)nb * nch * 4096;
         const uint8_t* src_sc = a.blob + (size_t)e * a.expert_stride + a.sc_off + (size_t)nb * nch * 512;
         for (int c = 0; c < nch; ++c, ++it) {
-          const int s = it % pf::kStages;
-          const uint32_t ph = (it / pf::kStages) & 1u;
-          if (!mbar_wait(empty + s, ph ^ 1u, abort_flag, a.st, 1)) break;
-          uint8_t* stage = smem + s * pf::kStageBytes;
-          mbar_arrive_expect_tx(full + s, 4096u + 512u + (uint32_t)nbox * 2048u);
-          bulk_g2s(stage + pf::kRawOff, src_nib + (size_t)c * 4096, 4096, full + s);
-          bulk_g2s(stage + pf::kScOff, src_sc + (size_t)c * 512, 512, full + s);
-          for (int bx = 0; bx < nbox; ++bx)
-            tma_2d(stage + pf::kBOff + bx * 2048, &tmap_b, c * kChunk, row0 + 16 * bx, full + s);
+          const int s = it % pf::kRawStages;
+          const uint32_t ph = (it / pf::kRawStages) & 1u;
+          if (!mbar_wait(raw_empty + s, ph ^ 1u, abort_flag, a.st, 1)) break;
+          uint8_t* st = smem + pf::kRawOff + s * pf::kRawStageBytes;
+          mbar_arrive_expect_tx(raw_full + s, 4096u + 512u);
+          bulk_g2s(st, src_nib + (size_t)c * 4096, 4096, raw_full + s);
+          bulk_g2s(st + 4096, src_sc + (size_t)c * 512, 512, raw_full + s);
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      uint32_t it = 0, j = 0;
+      uint32_t ia = 0, ib = 0, j = 0;
       for (int unit = blockIdx.x; unit < total_units && !*abort_flag; unit += gridDim.x, ++j) {
         const int tile = unit / a.NB;
         const int rows = a.tile_rows[tile];
@@ -266,46 +281,76 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * 256u;
         bool ok = true;
-        for (int c = 0; c < nch; ++c, ++it) {
-          const int s = it % pf::kStages;
-          const uint32_t ph = (it / pf::kStages) & 1u;
-          if (!mbar_wait(aready + s, ph, abort_flag, a.st, 3) || !mbar_wait(full + s, ph, abort_flag, a.st, 4)) {
+        for (int c = 0; c < nch; ++c, ++ia, ++ib) {
+          const int sa = ia % pf::kAStages, sb = ib % pf::kBStages;
+          if (!mbar_wait(a_full + sa, (ia / pf::kAStages) & 1u, abort_flag, a.st, 3) ||
+              !mbar_wait(b_full + sb, (ib / pf::kBStages) & 1u, abort_flag, a.st, 4)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint8_t* stage = smem + s * pf::kStageBytes;
-          const uint64_t ad = sw128_desc(smem_u32(stage + pf::kAOff));
-          const uint64_t bd = sw128_desc(smem_u32(stage + pf::kBOff));
+          const uint64_t ad = sw128_desc(smem_u32(smem + pf::kAOff + sa * pf::kAStageBytes));
+          const uint64_t bd = sw128_desc(smem_u32(smem + pf::kBOff + sb * pf::kBStageBytes));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             umma_bf16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, (c | kk) != 0 ? 1u : 0u);
-          umma_commit(empty + s);
+          umma_commit(a_empty + sa);
+          umma_commit(b_empty + sb);
         }
         if (!ok) break;
         umma_commit(accfull + buf);
       }
     }
-  } else if (warp < 6) {
-    // ---------------- dequantisers (128 threads) ----------------
-    const int tau = threadIdx.x - 64;
+  } else if (warp == 2) {
+    // ---------------- activation producer: TMA boxes of 16 routed rows ----------------
     uint32_t it = 0;
-    for (int unit = blockIdx.x; unit < total_units && !*abort_flag; unit += gridDim.x) {
+    for (int unit = blockIdx.x; unit < total_units && !*abort_flag && a.fault != 1; unit += gridDim.x) {
+      const int tile = unit / a.NB;
+      const int row0 = a.tile_row0[tile], rows = a.tile_rows[tile];
+      const int nbox = (rows + 15) >> 4;
       bool ok = true;
       for (int c = 0; c < nch; ++c, ++it) {
-        const int s = it % pf::kStages;
-        const uint32_t ph = (it / pf::kStages) & 1u;
-        if (!mbar_wait(full + s, ph, abort_flag, a.st, 5)) {
+        const int s = it % pf::kBStages;
+        const uint32_t ph = (it / pf::kBStages) & 1u;
+        int got = 1;
+        if (lane == 0) {
+          got = mbar_wait(b_empty + s, ph ^ 1u, abort_flag, a.st, 7);
+          if (got) mbar_arrive_expect_tx(b_full + s, (uint32_t)nbox * 2048u);
+        }
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
           ok = false;
           break;
         }
-        const uint8_t* stage = smem + s * pf::kStageBytes;
-        const uint32_t a_base = smem_u32(stage + pf::kAOff);
-        dequant_segment(stage, a_base, tau);
-        dequant_segment(stage, a_base, tau + 128);
+        uint8_t* st = smem + pf::kBOff + s * pf::kBStageBytes;
+        if (lane < nbox) tma_2d(st + lane * 2048, &tmap_b, c * kChunk, row0 + 16 * lane, b_full + s);
+        __syncwarp();
+      }
+      if (!ok) break;
+    }
+  } else if (warp < 7) {
+    // ---------------- dequantisers (128 threads) ----------------
+    const int tau = threadIdx.x - 96;
+    uint32_t ir = 0, ia = 0;
+    for (int unit = blockIdx.x; unit < total_units && !*abort_flag; unit += gridDim.x) {
+      bool ok = true;
+      for (int c = 0; c < nch; ++c, ++ir, ++ia) {
+        const int sr = ir % pf::kRawStages, sa = ia % pf::kAStages;
+        if (!mbar_wait(raw_full + sr, (ir / pf::kRawStages) & 1u, abort_flag, a.st, 5) ||
+            !mbar_wait(a_empty + sa, ((ia / pf::kAStages) & 1u) ^ 1u, abort_flag, a.st, 8)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* raw_stage = smem + pf::kRawOff + sr * pf::kRawStageBytes;
+        const uint32_t a_base = smem_u32(smem + pf::kAOff + sa * pf::kAStageBytes);
+        dequant_segment(raw_stage, a_base, tau);
+        dequant_segment(raw_stage, a_base, tau + 128);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(aready + s);
+        if (lane == 0) {
+          mbar_arrive(a_full + sa);
+          mbar_arrive(raw_empty + sr);
+        }
       }
       if (!ok) break;
     }

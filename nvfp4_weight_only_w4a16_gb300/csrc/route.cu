@@ -12,14 +12,14 @@ namespace nvfp4moe {
 // ---------------------------------------------------------------------------
 // Prefill: multi-CTA route, one-CTA scan, multi-CTA scatter + gather.
 // ---------------------------------------------------------------------------
-// K1: one warp per token (32 tokens per CTA): ids, weights, NaN count.
+// K1: one warp per token (8 tokens per CTA): ids, weights, NaN count.
 __global__ void __launch_bounds__(256) route_topk_kernel(const void* __restrict__ logits, int bf16, int T, int k,
                                                          int E, Workspace ws) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int nan_total = 0;
-  for (int tt = warp; tt < 32; tt += 8) {
-    const int t = blockIdx.x * 32 + tt;
-    if (t >= T) break;
+  {
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
     int id;
     float w;
     nan_total += warp_topk(logits, bf16, E, k, t, &id, &w);
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16*
 cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const void* x, int T, int k,
                                  const Workspace& ws, cudaStream_t st) {
   const int nrb = (T + kRankTokens - 1) / kRankTokens;
-  route_topk_kernel<<<(T + 31) / 32, 256, 0, st>>>(logits, d.logits_bf16, T, k, d.E, ws);
+  route_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, d.logits_bf16, T, k, d.E, ws);
   route_rank_kernel<<<nrb, 256, 0, st>>>(T, k, d.E, ws);
   route_scan_kernel<<<1, 1024, 0, st>>>(nrb, d.E, ws);
   const size_t rows = (size_t)T * k;

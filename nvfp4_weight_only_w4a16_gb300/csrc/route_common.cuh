@@ -19,6 +19,29 @@ __device__ __forceinline__ float load_logit(const void* logits, int bf16, size_t
   return reinterpret_cast<const float*>(logits)[i];
 }
 
+// Softmax over the k chosen logits of one token: lane j < k holds logit j
+// (NaN counts as -inf; all -inf -> 1/k each; any +inf -> the +inf entries
+// share weight 1).  Returns lane j's weight; the sum runs in slot order
+// j = 0..k-1 on every lane.
+__device__ __forceinline__ float warp_softmax_k(float logit, int k) {
+  const int lane = threadIdx.x & 31;
+  const float l = (lane < k) ? (logit != logit ? -INFINITY : logit) : -INFINITY;
+  float m = l;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float ex;
+  if (m == -INFINITY) {
+    ex = (lane < k) ? 1.0f : 0.0f;
+  } else if (m == INFINITY) {
+    ex = (lane < k && l == INFINITY) ? 1.0f : 0.0f;
+  } else {
+    ex = (lane < k) ? expf(l - m) : 0.0f;
+  }
+  float sum = 0.f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
+  return ex / sum;
+}
+
 // One warp routes token t (E <= 256, k <= 16).  Lane j < k receives the j-th
 // choice in (*my_id, *my_w); returns the number of NaN logits of the token.
 __device__ __forceinline__ int warp_topk(const void* logits, int bf16, int E, int k, int t, int* my_id,
@@ -67,22 +90,8 @@ __device__ __forceinline__ int warp_topk(const void* logits, int bf16, int E, in
       logit = v;
     }
   }
-  const float l = (lane < k) ? (logit != logit ? -INFINITY : logit) : -INFINITY;
-  float m = l;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float ex;
-  if (m == -INFINITY) {
-    ex = (lane < k) ? 1.0f : 0.0f;
-  } else if (m == INFINITY) {
-    ex = (lane < k && l == INFINITY) ? 1.0f : 0.0f;
-  } else {
-    ex = (lane < k) ? expf(l - m) : 0.0f;
-  }
-  float sum = 0.f;  // slot order j = 0..k-1, identical on every lane
-  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
   *my_id = id;
-  *my_w = ex / sum;
+  *my_w = warp_softmax_k(logit, k);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) nan_count += __shfl_xor_sync(0xffffffffu, nan_count, o);
   return nan_count;

@@ -78,15 +78,13 @@ struct Region {
 // With base == nullptr only the size is computed.  The zero-initialised
 // regions (split-K partials, counters, status) are contiguous at the front:
 // [0, *zero_bytes).
-size_t carve(uint8_t* base, int E, int H, int I, int T, int k, Workspace* ws, size_t* zero_bytes) {
+size_t carve(uint8_t* base, int E, int H, int I, int T, int k, int num_sms, Workspace* ws, size_t* zero_bytes) {
   const size_t R = (size_t)T * k;
   const size_t maxU = std::min<size_t>((size_t)E, R);
   uint8_t* b = base ? base : reinterpret_cast<uint8_t*>(0x100);
   Region r;
   Workspace w{};
-  w.part_gu = r.take<float>(b, maxU * (2 * I / 64) * 1024);
   w.cnt_gu = r.take<int32_t>(b, maxU * (2 * I / 64));
-  w.part_dn = r.take<float>(b, maxU * (H / 64) * 1024);
   w.cnt_dn = r.take<int32_t>(b, maxU * (H / 64));
   w.done_gu = r.take<int32_t>(b, maxU);
   w.cmb = r.take<int32_t>(b, H / 64);
@@ -94,6 +92,11 @@ size_t carve(uint8_t* base, int E, int H, int I, int T, int k, Workspace* ws, si
   w.hmax = r.take<uint32_t>(b, R);
   w.status = r.take<DeviceStatus>(b, 1);
   *zero_bytes = (r.off + 255) & ~size_t(255);
+  // no split-K partial-sum buffers here: with part_gu == nullptr the decode
+  // kernel gives every warp whole blocks
+  w.part_gu = nullptr;
+  w.part_dn = nullptr;
+  (void)num_sms;
   w.ids = r.take<int32_t>(b, R);
   w.wts = r.take<float>(b, R);
   w.offsets = r.take<int32_t>(b, E + 1);
@@ -132,17 +135,16 @@ extern "C" nvfp4_moe_status nvfp4_moe_forward_decode_static(const uint8_t* packe
   if (!aligned_to(packed_experts, 16) || !aligned_to(x, 16) || !aligned_to(out, 16) || !aligned_to(gscale, 4) ||
       !aligned_to(router_logits, logits_dtype == NVFP4_MOE_LOGITS_BF16 ? 2 : 4))
     return NVFP4_MOE_ERR_INVALID_ARG;
-  size_t zero_bytes = 0;
-  if (carve(nullptr, E, H, I, T, top_k, nullptr, &zero_bytes) > kStaticScratchBytes)
-    return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;  // needs more than the static scratch holds
-
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_MOE_ERR_CUDA;
   StaticSetup setup;
   if (static_setup(dev, &setup) != cudaSuccess) return NVFP4_MOE_ERR_CUDA;
+  size_t zero_bytes = 0;
+  if (carve(nullptr, E, H, I, T, top_k, setup.num_sms, nullptr, &zero_bytes) > kStaticScratchBytes)
+    return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;  // needs more than the static scratch holds
 
   Workspace ws{};
-  carve(setup.scratch, E, H, I, T, top_k, &ws, &zero_bytes);
+  carve(setup.scratch, E, H, I, T, top_k, setup.num_sms, &ws, &zero_bytes);
   const LayerDims d{E, H, I, logits_dtype == NVFP4_MOE_LOGITS_BF16, 0};
   cudaError_t e = cudaMemsetAsync(setup.scratch, 0, zero_bytes, stream);
   if (e == cudaSuccess)

@@ -58,11 +58,16 @@ def test_static_forward_matches_handle_forward_mtp():
     _run_both("decode_mtp", [slice(0, 2), slice(1, 2)])
 
 
+def test_static_forward_matches_handle_forward_c16():
+    _run_both("decode_c16", [slice(0, 16), slice(4, 12)])
+
+
 def test_static_forward_rejects_what_does_not_fit():
+    # 16 tokens x top-16 x (2*16384 + 4*16384) bytes of intermediates > 16 MiB
     P.build()
-    x = torch.zeros((16, 4096), dtype=torch.bfloat16, device=DEV)
-    logits = torch.zeros((16, 128), dtype=torch.float32, device=DEV)
+    x = torch.zeros((16, 16384), dtype=torch.bfloat16, device=DEV)
+    logits = torch.zeros((16, 256), dtype=torch.float32, device=DEV)
     blob = torch.zeros((16,), dtype=torch.uint8, device=DEV)
-    gs = torch.ones((128, 3), dtype=torch.float32, device=DEV)
-    st = P.binding.nvfp4_moe_forward_decode_static(blob, gs, 128, 4096, 1536, logits, 8, x, torch.empty_like(x))
+    gs = torch.ones((256, 3), dtype=torch.float32, device=DEV)
+    st = P.binding.nvfp4_moe_forward_decode_static(blob, gs, 256, 16384, 16384, logits, 16, x, torch.empty_like(x))
     assert st == P.STATUS_CODE["NVFP4_MOE_ERR_UNSUPPORTED_SHAPE"]
