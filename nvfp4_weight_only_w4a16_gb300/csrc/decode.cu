@@ -48,6 +48,8 @@ constexpr int kStA = 0;              // 4 x 512 B weight codes
 constexpr int kStS = 2048;           // 4 x 64 B scales
 constexpr int kStB = 2304;           // NG token groups x 8 rows x 144 B (BF16 x 64, padded: no bank conflicts)
 constexpr int kRowPitch = 144;
+constexpr int kSlotFloats = 15 * 64 * 8;              // shared-memory split-K slots (T <= 8)
+constexpr int kSlotBytes = kSlotFloats * 4 + 128;     // + 16 counters, padded
 __host__ __device__ constexpr int stage_bytes(int ng) { return kStB + 8 * kRowPitch * ng; }
 // split-K partial sums: per warp, two slots (its first and its last segment),
 // each [rg 4][row 16][mslot] FP32 with mslot = min(T, 16)
@@ -414,7 +416,8 @@ __device__ __forceinline__ ItemPos item_at(long long f, int nch, int nblk) {
 
 template <bool kGateUp, int S, int NG>
 __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint64_t* bars, uint32_t& ring_it,
-                          long long F, long long W, long long wg, unsigned long long* tr) {
+                          long long F, long long W, long long wg, unsigned long long* tr, float* part_s,
+                          int* cnt_s) {
   const int nch_ = kGateUp ? a.H / kChunk : a.I / kChunk;
   // split-K: equal chunk ranges; no_split: equal ranges of whole blocks
   const long long fbeg = a.no_split ? (F / nch_) * wg / W * nch_ : F * wg / W;
@@ -495,6 +498,11 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
   float bsc[2] = {1.f, 1.f};
   int seg_c0 = 0, m = 0, ng = 1;
   const uint32_t it0 = ring_it;
+  // blocks whose every contributor is a warp of this CTA reduce in shared memory
+  const long long cta_w0 = wg - (wg % dec::kWarps);
+  const long long cs0 = F * cta_w0 / W, cs1 = F * (cta_w0 + dec::kWarps) / W;
+  int seg_idx = 0;
+  uint64_t loop_fin = 0;  // CTA-internal blocks this warp finished during the loop
   int issued = 0, consumed = 0;
 
   for (; issued < S - 1 && issued < nf; ++issued) issue(it0 + issued);
@@ -581,12 +589,56 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
     const bool seg_end = (c == nch - 1) || (i == nf - 1);
     if (!seg_end) continue;
     if (seg_c0 == 0 && c == nch - 1) {  // the whole block is this warp's: finish it now, signal later
+      ++seg_idx;
       if (kGateUp) finish_gateup(a, rs, u, b, acc, lane);
       else finish_down(a, rs, u, b, acc, lane);
       continue;
     }
-    // part of a block: store the partial sums into this warp's slot (0: its
-    // first segment, 1: its last); counted at the end of the phase
+    const int seg_here = seg_idx++;
+    const long long f0 = (long long)(u * nblk + b) * nch;
+    if (part_s != nullptr && f0 >= cs0 && f0 + nch <= cs1) {
+      // split among warps of this CTA: shared-memory sum, the last one finishes
+      const long long wlo = ((f0 + 1) * W + F - 1) / F - 1;  // warp holding the block's first chunk
+      const int slot = (int)(wlo - cta_w0);                    // its boundary with the next warp
+      float* ps = part_s + slot * 64 * 8;
+#pragma unroll
+      for (int rg = 0; rg < dec::kRG; ++rg)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int j = 2 * q + cc;
+          if (j < m) {
+            atomicAdd(ps + (rg * 16 + r0) * 8 + j, acc[rg][0][cc]);
+            atomicAdd(ps + (rg * 16 + r0 + 8) * 8 + j, acc[rg][0][2 + cc]);
+          }
+        }
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        __threadfence_block();
+        const int add = c - seg_c0 + 1;
+        last = (atomicAdd(cnt_s + slot, add) + add == nch);
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        __threadfence_block();
+#pragma unroll
+        for (int rg = 0; rg < dec::kRG; ++rg)
+#pragma unroll
+          for (int gi = 0; gi < 2; ++gi)
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int j = 2 * q + cc;
+              acc[rg][gi][cc] = (gi == 0 && j < m) ? ps[(rg * 16 + r0) * 8 + j] : 0.f;
+              acc[rg][gi][2 + cc] = (gi == 0 && j < m) ? ps[(rg * 16 + r0 + 8) * 8 + j] : 0.f;
+            }
+        if (kGateUp) finish_gateup(a, rs, u, b, acc, lane);
+        else finish_down(a, rs, u, b, acc, lane);
+        if (seg_here < 64) loop_fin |= 1ull << seg_here;
+      }
+      continue;
+    }
+    // split across CTAs: store the partial sums into this warp's global slot
+    // (0: its first segment, 1: its last); counted at the end of the phase
     {
       const int slot = (i + 1 - (c - seg_c0 + 1) == 0) ? 0 : 1;  // did the segment start at the range start?
       float* part = (kGateUp ? a.part_gu : a.part_dn) + ((size_t)wg * 2 + slot) * 64 * a.mslot;
@@ -638,6 +690,10 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
         if (si < 64) fin_mask |= 1ull << si;
         else signal(blk);
         continue;
+      }
+      if (part_s != nullptr && (long long)blk * nch >= cs0 && (long long)blk * nch + nch <= cs1) {
+        if (si < 64 && ((loop_fin >> si) & 1ull)) fin_mask |= 1ull << si;
+        continue;  // reduced in shared memory; finished (or not) by the loop
       }
       int last = 0;
       if (lane == 0) last = (atomicAdd((kGateUp ? a.cnt_gu : a.cnt_dn) + blk, c1 - c0) + (c1 - c0) == nch);
@@ -717,7 +773,10 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
   RouteSmem& rs = *reinterpret_cast<RouteSmem*>(smem);
   const size_t route_bytes = (sizeof(RouteSmem) + 127) & ~size_t(127);
   uint64_t* all_bars = reinterpret_cast<uint64_t*>(smem + route_bytes);
-  uint8_t* rings = smem + route_bytes + 128 * 8;
+  // NG == 1: shared-memory split-K slots, one per boundary between the CTA's warps
+  float* part_s = NG == 1 ? reinterpret_cast<float*>(smem + route_bytes + 128 * 8) : nullptr;
+  int* cnt_s = NG == 1 ? reinterpret_cast<int*>(smem + route_bytes + 128 * 8 + dec::kSlotFloats * 4) : nullptr;
+  uint8_t* rings = smem + route_bytes + 128 * 8 + (NG == 1 ? dec::kSlotBytes : 0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = rings + warp * S * dec::stage_bytes(NG);
   uint64_t* bars = all_bars + warp * 8;
@@ -725,6 +784,14 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
   const uint64_t t_start = now_ns();
   route_block(a, rs, rings);
   if (a.route_only) return;
+  auto clear_slots = [&]() {
+    if (NG == 1) {
+      for (int i = threadIdx.x; i < dec::kSlotFloats; i += blockDim.x) part_s[i] = 0.f;
+      if (threadIdx.x < 16) cnt_s[threadIdx.x] = 0;
+    }
+  };
+  clear_slots();
+  __syncthreads();
   unsigned long long* tr = a.trace ? a.trace + ((size_t)blockIdx.x * dec::kWarps + warp) * 8 : nullptr;
   if (tr && lane == 0) {
     tr[0] = t_start;
@@ -741,10 +808,15 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
   const int U = rs.U;
   uint32_t ring_it = 0;
   const long long F1 = (long long)U * (2 * a.I / 64) * (a.H / kChunk);
-  run_phase<true, S, NG>(a, rs, ring, bars, ring_it, F1, W, wg, tr);
+  run_phase<true, S, NG>(a, rs, ring, bars, ring_it, F1, W, wg, tr, part_s, cnt_s);
   if (tr && lane == 0) tr[2] = now_ns();
+  if (NG == 1) {  // phase 2 reuses the shared-memory slots
+    __syncthreads();
+    clear_slots();
+    __syncthreads();
+  }
   const long long F2 = (long long)U * (a.H / 64) * (a.I / kChunk);
-  run_phase<false, S, NG>(a, rs, ring, bars, ring_it, F2, W, wg, tr);
+  run_phase<false, S, NG>(a, rs, ring, bars, ring_it, F2, W, wg, tr, part_s, cnt_s);
   if (tr && lane == 0) tr[4] = now_ns();
 
   // the last CTA out resets the per-forward counters (and, after a timeout,
@@ -771,9 +843,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
   if (threadIdx.x == 0) *a.exit_cnt = 0;
 }
 
-// T <= 8: one token group per expert, 4 stages; T <= 16: two groups, 3 stages.
+// T <= 8: one token group per expert, shared-memory split-K slots, 3 stages;
+// T <= 16: two groups, 3 stages, split-K through global slots only.
 static size_t smem_for(int S, int NG) {
-  return ((sizeof(RouteSmem) + 127) & ~size_t(127)) + 128 * 8 + (size_t)dec::kWarps * S * dec::stage_bytes(NG);
+  return ((sizeof(RouteSmem) + 127) & ~size_t(127)) + 128 * 8 + (NG == 1 ? dec::kSlotBytes : 0) +
+         (size_t)dec::kWarps * S * dec::stage_bytes(NG);
 }
 size_t decode_smem_bytes() { return smem_for(3, 2); }
 
@@ -782,10 +856,10 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
                                   const Workspace& ws, cudaStream_t st) {
   static int attr_done = 0;
   const bool small = T <= 8;
-  const size_t smem = small ? smem_for(4, 1) : smem_for(3, 2);
+  const size_t smem = small ? smem_for(3, 1) : smem_for(3, 2);
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem_for(4, 1));
+    cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<3, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_for(3, 1));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(decode_fused_kernel<3, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem_for(3, 2));
@@ -841,7 +915,7 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = route_only ? 0 : 1;
-  return small ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<4, 1>, a)
+  return small ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 1>, a)
                : cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 2>, a);
 }
 
