@@ -205,9 +205,14 @@ nvfp4_moe_status nvfp4_moe_debug_packed_blob(nvfp4_moe_t h, void* dst, size_t ds
 
 /* Phase timeline of the decode kernel (handles created with the environment
  * variable NVFP4_MOE_TRACE=1 only).  Synchronous.  Copies up to n values into
- * host_dst: for each CTA c and warp w, 8 globaltimer nanosecond stamps at
- * [(c*16 + w)*8]: kernel start, routed, gate/up done, first down wait over,
- * down done, exit barrier passed (unused slots 0); clears the buffer. */
+ * host_dst: for each CTA c and warp w, 16 values at [(c*16 + w)*16]:
+ * globaltimer nanosecond stamps 0 kernel start, 1 routed, 2 gate/up done,
+ * 3 first down wait over, 4 down done, 5 exit barrier passed; durations (ns)
+ * 6 gate/up and 7 down end-of-phase block finishing; stamps 8 inputs loaded,
+ * 9 top-k chosen, 10 expert offsets scanned (warp 0 of each CTA only),
+ * 11 gate/up stream ended, 12 down stream ended, 13 first gate/up stage
+ * landed; 14 and 15: the SM clock counter (clock64) at stamps 0 and 1;
+ * unused slots 0.  Clears the buffer. */
 nvfp4_moe_status nvfp4_moe_debug_trace(nvfp4_moe_t h, uint64_t* host_dst, size_t n, size_t* n_written);
 
 /* Dequantise one tensor of one expert from the PACKED blob into a caller

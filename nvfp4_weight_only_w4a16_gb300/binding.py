@@ -173,7 +173,7 @@ class MoELayer:
 
     def nvfp4_moe_debug_trace(self):
         import numpy as np
-        n = 152 * 16 * 8 * 4
+        n = 152 * 16 * 16 * 4
         buf = (ctypes.c_uint64 * n)()
         got = ctypes.c_size_t(0)
         self._check(self.lib.nvfp4_moe_debug_trace(self.h, buf, n, ctypes.byref(got)), "nvfp4_moe_debug_trace")

@@ -222,9 +222,9 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* c, nvfp4_moe_t* out) {
   cv.add(&w.hmax, Rm);
   cv.add(&w.y, Rm * H);
   cv.add(&w.part_gu, decode_part_floats(h->num_sms, kDecodeMaxTokens));
-  cv.add(&w.cnt_gu, maxU * (2 * I / 64));
+  cv.add(&w.cnt_gu, maxU * (2 * I / 16));
   cv.add(&w.part_dn, decode_part_floats(h->num_sms, kDecodeMaxTokens));
-  cv.add(&w.cnt_dn, maxU * (H / 64));
+  cv.add(&w.cnt_dn, maxU * (H / 16));
   cv.add(&w.done_gu, maxU);
   cv.add(&w.cmb, H / 64);
   cv.add(&w.exit_cnt, 1);
@@ -239,7 +239,7 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* c, nvfp4_moe_t* out) {
   cv.add(&w.status, 1);
   const char* tr = getenv("NVFP4_MOE_TRACE");
   const bool trace = tr && tr[0] == '1';
-  if (trace) cv.add(&w.trace, (size_t)h->num_sms * 16 * 8);
+  if (trace) cv.add(&w.trace, (size_t)h->num_sms * 16 * 16);
   h->ws_bytes = cv.layout();
 
   if (cudaMalloc(&h->blob, blob_bytes) != cudaSuccess || cudaMalloc(&h->gscale, sizeof(float) * 3 * E) != cudaSuccess ||
@@ -433,7 +433,7 @@ nvfp4_moe_status nvfp4_moe_debug_trace(nvfp4_moe_t h, uint64_t* host_dst, size_t
   *n_written = 0;
   if (!h->ws.trace) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_trace: create the handle with NVFP4_MOE_TRACE=1");
   DeviceGuard g(h->cfg.device);
-  const size_t total = (size_t)h->num_sms * 16 * 8;
+  const size_t total = (size_t)h->num_sms * 16 * 16;
   const size_t m = n < total ? n : total;
   cudaError_t e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = cudaMemcpy(host_dst, h->ws.trace, m * 8, cudaMemcpyDeviceToHost);

@@ -14,12 +14,15 @@
 //    are resident); every CTA routes the <= 16 tokens itself (a few KB of
 //    logits; one thread per logit ranks it against its row in shared memory
 //    when T*E <= 512), so no routing tables cross CTAs before the GEMVs start;
-//  * stream-K work split: the flat list of (touched expert, 64-row block,
-//    64-wide K chunk) items is cut into equal contiguous ranges, one per warp,
-//    so every SM streams the same number of weight bytes whatever the
-//    routing; partial sums of a block split across warps meet in an FP32
-//    buffer and the last warp to arrive (atomic counter) finishes the block;
-//  * each warp runs its own ring in shared memory (3-4 stages): one lane
+//  * work split in two levels, so every SM streams the same number of weight
+//    bytes whatever the routing: each CTA takes an equal share of the 16-row
+//    groups of the touched experts' matrices over the whole K axis (no row's
+//    sum crosses CTAs); inside the CTA the (64-row piece, 64-wide K chunk)
+//    items are cut into equal contiguous ranges, one per warp, and partial
+//    sums of a piece split across warps meet in shared memory (FP32 slots;
+//    for more than 8 tokens, per-warp global slots), the last warp to arrive
+//    finishing the piece;
+//  * each warp runs its own ring in shared memory (3 stages): one lane
 //    issues cp.async.bulk copies of a chunk's codes (2 KB), scales (256 B) and
 //    the routed rows' activation slices (128 B each) onto the stage's
 //    mbarrier, so no per-thread copy is in flight when a warp fences;
@@ -31,9 +34,11 @@
 //  * activations (x, then h) enter as FP16 after a per-row power-of-two
 //    prescale (exact for BF16 values within 2^31 of the row maximum), undone
 //    in FP32;
-//  * the down GEMV of expert u starts once all gate/up blocks of u are done
+//  * the down GEMV of expert u starts once all gate/up rows of u are done
 //    (per-expert counter, bounded wait); the last down block to finish a
 //    64-wide slice of H combines that slice for every token, in slot order.
+#include <cstdlib>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "route_common.cuh"
@@ -48,11 +53,12 @@ constexpr int kStA = 0;              // 4 x 512 B weight codes
 constexpr int kStS = 2048;           // 4 x 64 B scales
 constexpr int kStB = 2304;           // NG token groups x 8 rows x 144 B (BF16 x 64, padded: no bank conflicts)
 constexpr int kRowPitch = 144;
-constexpr int kSlotFloats = 15 * 64 * 8;              // shared-memory split-K slots (T <= 8)
-constexpr int kSlotBytes = kSlotFloats * 4 + 128;     // + 16 counters, padded
-__host__ __device__ constexpr int stage_bytes(int ng) { return kStB + 8 * kRowPitch * ng; }
-// split-K partial sums: per warp, two slots (its first and its last segment),
-// each [rg 4][row 16][mslot] FP32 with mslot = min(T, 16)
+constexpr int kSlots = kWarps - 1;   // shared-memory split-K slots: one per boundary between warps
+// a stage holds activation rows for min(T, 8) tokens (one group) or 16 (two)
+__host__ __device__ constexpr int stage_rows(int T) { return T <= 8 ? T : 16; }
+__host__ __device__ constexpr int stage_bytes_for(int T) { return kStB + kRowPitch * stage_rows(T); }
+// global split-K partial sums: per warp, two slots (its first and its last
+// segment), each [rg 4][row 16][mslot] FP32 with mslot = min(T, 16)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 }  // namespace dec
 
@@ -70,7 +76,6 @@ struct RouteSmem {
   int last_cta;
   unsigned xmax[16];
   int xexp[16];
-  int scan[32];
 };
 
 struct FusedArgs {
@@ -97,13 +102,17 @@ struct FusedArgs {
   int32_t* cnt_gu;
   float* part_dn;
   int32_t* cnt_dn;
-  int mslot;     // token columns of a partial-sum slot
-  int no_split;  // 1: every warp takes whole blocks (no split-K, no partial-sum buffers)
+  int mslot;      // token columns of a global partial-sum slot
+  int no_split;   // 1: no global partial-sum buffers
+  int slot_cols;  // token columns of a shared-memory split-K slot (0: none)
+  int slot_sets;  // 2: separate shared-memory slots per phase; 1: one set, cleared between phases
+  int xs_pitch;   // > 0: the tokens' FP16 activations are staged in shared memory, rows this many bytes apart
+  int stage_bytes;  // bytes of one ring stage
   int32_t* done_gu;
   int32_t* cmb;
   int32_t* exit_cnt;
   DeviceStatus* st;
-  unsigned long long* trace;  // optional: [cta][warp][8] globaltimer stamps
+  unsigned long long* trace;  // optional: [cta][warp][16] globaltimer stamps
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -177,117 +186,138 @@ __device__ __forceinline__ float pow2f(int p) {
 }
 
 // ---------------------------------------------------------------------------
-// Phase 0: every CTA routes the T tokens into shared memory, and takes each
-// token's max |x| for the FP16 prescale.  `scratch` (>= T*E*8 bytes) is the
-// ring memory, free until the GEMVs start.
+// Phase 0: every CTA routes the T tokens into shared memory (warp t picks
+// token t's experts), and takes each token's max |x| for the FP16 prescale
+// (16/T warps per token).
 // ---------------------------------------------------------------------------
-__device__ void route_block(const FusedArgs& a, RouteSmem& rs, uint8_t* scratch) {
+// xs != nullptr: the tokens' activations are also left in shared memory as
+// FP16 rows (xs_pitch bytes apart) after the per-token prescale.
+__device__ void route_block(const FusedArgs& a, RouteSmem& rs, uint8_t* xs, unsigned long long* tr0) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int T = a.T, k = a.k, E = a.E, R = T * k, TE = T * E;
-  const bool by_rank = TE <= dec::kThreads;  // one thread per logit
-  uint32_t* keys = reinterpret_cast<uint32_t*>(scratch);
-  float* vals = reinterpret_cast<float*>(scratch + 4 * dec::kThreads);
-  if (tid < 16) rs.xmax[tid] = 0u;
-  if (tid == 0) rs.nan = 0;
-  __syncthreads();
-  // logits -> orderable keys (rank path); per-token max |x| on every thread
-  int nan = 0;
-  if (by_rank && tid < TE) {
-    const float v = load_logit(a.logits, a.logits_bf16, tid);
-    nan = (v != v);
-    keys[tid] = float_key(v);
-    vals[tid] = v;
-  }
-  if (a.x) {  // 8 independent 16-byte loads in flight per thread
-    const int per_row = a.H / 8, n = T * per_row;
-    for (int base = tid; base < n; base += 8 * blockDim.x) {
+  const int T = a.T, k = a.k, E = a.E, R = T * k;
+  // loads first: token `warp`'s logits, and this warp's share of one x row
+  uint32_t key[8];
+  float val[8];
+  if (warp < T) warp_load_logits(a.logits, a.logits_bf16, E, warp, key, val);
+  const int wpt = dec::kWarps / T;  // warps per token row of x
+  const int xt = warp / wpt, xpart = warp - xt * wpt;
+  const int per_row = a.H / 8;  // 16-byte pieces per row
+  float xm = 0.f;
+  if (a.x && xt < T) {
+    const uint4* row = reinterpret_cast<const uint4*>(a.x + (size_t)xt * a.H);
+    for (int base = xpart * 32; base < per_row; base += 32 * wpt * 8) {
       uint4 v[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int i = base + j * blockDim.x;
-        if (i < n) {
-          const int t = i / per_row;
-          v[j] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H) + (i - t * per_row));
-        }
+        const int i = base + lane + j * 32 * wpt;
+        if (i < per_row) v[j] = __ldg(row + i);
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int i = base + j * blockDim.x;
-        if (i < n) {
+        const int i = base + lane + j * 32 * wpt;
+        if (i < per_row) {
           const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-          float m = 0.f;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[q] << 16)), fabsf(__uint_as_float(wv[q] & 0xFFFF0000u))));
-          atomicMax(&rs.xmax[i / per_row], __float_as_uint(m));
+            xm = fmaxf(xm, fmaxf(fabsf(__uint_as_float(wv[q] << 16)), fabsf(__uint_as_float(wv[q] & 0xFFFF0000u))));
+          if (xs) *reinterpret_cast<uint4*>(xs + (size_t)xt * a.xs_pitch + (size_t)i * 16) = v[j];
         }
       }
     }
   }
+  if (tid < 16) rs.xmax[tid] = 0u;
+  if (tid <= E) rs.off[tid] = 0;  // rows per expert, then offsets
+  if (tid == 0) rs.nan = 0;
   __syncthreads();
-  if (by_rank) {
-    // rank of logit (t, e) in its row: larger key first, lower index on ties
-    if (tid < TE) {
-      const int t = tid / E, e = tid - t * E;
-      const uint32_t kk = keys[tid];
-      const uint32_t* row = keys + t * E;
-      int r = 0;
-      for (int e2 = 0; e2 < E; ++e2) {
-        const uint32_t k2 = row[e2];
-        r += (k2 > kk) | ((k2 == kk) & (e2 < e));
-      }
-      if (r < k) {
-        rs.ids[t * k + r] = e;
-        rs.wts[t * k + r] = vals[tid];  // the chosen logit, turned into a weight below
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) nan += __shfl_xor_sync(0xffffffffu, nan, o);
-    if (lane == 0 && nan) atomicAdd(&rs.nan, nan);
-    __syncthreads();
-    if (warp < T) {
-      const float w = warp_softmax_k(lane < k ? rs.wts[warp * k + lane] : 0.f, k);
-      __syncwarp();
-      if (lane < k) rs.wts[warp * k + lane] = w;
-    }
-  } else if (warp < T) {
+  if (tr0 && tid == 0) tr0[8] = now_ns();
+  if (a.x && xt < T) {  // |x| >= 0: its bits order like the values
+    const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(xm));
+    if (lane == 0) atomicMax(&rs.xmax[xt], m);
+  }
+  if (warp < T) {
     int id;
-    float w;
-    const int nt = warp_topk(a.logits, a.logits_bf16, E, k, warp, &id, &w);
+    float logit;
+    const int nt = warp_select_topk(key, val, E, k, &id, &logit);
+    const float w = warp_softmax_k(logit, k);
     if (lane < k) {
       rs.ids[warp * k + lane] = id;
       rs.wts[warp * k + lane] = w;
+      atomicAdd(&rs.off[id], 1);
     }
     if (lane == 0 && nt) atomicAdd(&rs.nan, nt);
   }
   __syncthreads();
-  int c = 0;
-  if (tid < E)
-    for (int i = 0; i < R; ++i) c += (rs.ids[i] == tid);
-  int total = 0, touched = 0;
-  const int off = block_exclusive_scan(tid < E ? c : 0, rs.scan, &total);
-  const int slot = block_exclusive_scan((tid < E && c > 0) ? 1 : 0, rs.scan, &touched);
-  if (tid < E) {
-    rs.off[tid] = off;
-    if (c > 0) {
-      rs.tch_e[slot] = tid;
-      rs.tch_r0[slot] = off;
-      rs.tch_m[slot] = c;
+  if (tr0 && tid == 0) tr0[9] = now_ns();
+  if (warp == 0) {
+    // offsets (low 16 bits) and touched-expert slots (high 16 bits) in one
+    // warp scan; lane l owns experts 8l .. 8l+7 (E <= 256, R <= 256)
+    int cnt[8], s = 0, tc = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = 8 * lane + i;
+      cnt[i] = e < E ? rs.off[e] : 0;
+      s += cnt[i];
+      tc += cnt[i] > 0;
     }
+    const int v = s | (tc << 16);
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const int ex = inc - v;
+    int off = ex & 0xFFFF, slot = ex >> 16;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = 8 * lane + i;
+      if (e < E) {
+        rs.off[e] = off;
+        if (cnt[i] > 0) {
+          rs.tch_e[slot] = e;
+          rs.tch_r0[slot] = off;
+          rs.tch_m[slot] = cnt[i];
+          ++slot;
+        }
+        off += cnt[i];
+      }
+    }
+    if (lane == 31) {
+      rs.off[E] = inc & 0xFFFF;
+      rs.U = inc >> 16;
+    }
+  } else if (warp == 1 && lane < T) {
+    rs.xexp[lane] = max(-126, min(126, prescale_exp(__uint_as_float(rs.xmax[lane]))));
   }
-  if (tid == 0) {
-    rs.off[E] = total;
-    rs.U = touched;
-  }
-  if (tid < T) rs.xexp[tid] = max(-126, min(126, prescale_exp(__uint_as_float(rs.xmax[tid]))));
   __syncthreads();
-  if (tid < R) {
+  if (tr0 && tid == 0) tr0[10] = now_ns();
+  if (tid < R) {  // expert-major position: rank among the earlier rows of the same expert
     const int e = rs.ids[tid];
-    int rank = 0;
-    for (int j = 0; j < tid; ++j) rank += (rs.ids[j] == e);
+    int rank = 0, j = 0;
+    const int4* ids4 = reinterpret_cast<const int4*>(rs.ids);
+    for (; j + 4 <= tid; j += 4) {
+      const int4 q4 = ids4[j >> 2];
+      rank += (q4.x == e) + (q4.y == e) + (q4.z == e) + (q4.w == e);
+    }
+    for (; j < tid; ++j) rank += (rs.ids[j] == e);
     const int pos = rs.off[e] + rank;
     rs.perm[pos] = tid;
     rs.inv[tid] = pos;
+  }
+  if (xs) {  // BF16 -> FP16 in place, times 2^-xexp[t] (exact)
+    for (int i = tid; i < T * per_row; i += blockDim.x) {
+      const int t = i / per_row;
+      uint4* p = reinterpret_cast<uint4*>(xs + (size_t)t * a.xs_pitch + (size_t)(i - t * per_row) * 16);
+      const float sc = pow2f(-rs.xexp[t]);
+      const uint4 v = *p;
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int z = 0; z < 4; ++z) {
+        const __half2 hh = __floats2half2_rn(__uint_as_float(w[z] << 16) * sc, __uint_as_float(w[z] & 0xFFFF0000u) * sc);
+        w[z] = *reinterpret_cast<const uint32_t*>(&hh);
+      }
+      *p = make_uint4(w[0], w[1], w[2], w[3]);
+    }
   }
   __syncthreads();
   if (blockIdx.x == 0) {  // the tables, for inspection
@@ -303,10 +333,11 @@ __device__ void route_block(const FusedArgs& a, RouteSmem& rs, uint8_t* scratch)
 }
 
 // ---------------------------------------------------------------------------
-// Block finishing
+// Piece finishing.  A piece is the 16-row groups [rg0, rg0 + cnt) of 64-row
+// block b of touched expert u; acc[rg] holds group rg0 + rg.
 // ---------------------------------------------------------------------------
-__device__ void finish_gateup(const FusedArgs& a, const RouteSmem& rs, int u, int b, float (&acc)[dec::kRG][2][4],
-                              int lane) {
+__device__ void finish_gateup(const FusedArgs& a, const RouteSmem& rs, int u, int b, int rg0, int cnt,
+                              float (&acc)[dec::kRG][2][4], int lane) {
   const int e = rs.tch_e[u], row0 = rs.tch_r0[u], m = rs.tch_m[u];
   const int r0 = lane >> 2, q = lane & 3;
   const float gsg = a.gscale[3 * e], gsu = a.gscale[3 * e + 1];
@@ -321,16 +352,18 @@ __device__ void finish_gateup(const FusedArgs& a, const RouteSmem& rs, int u, in
       const float s = pow2f(rs.xexp[rs.perm[row] / a.k]);
 #pragma unroll
       for (int rg = 0; rg < dec::kRG; ++rg) {
+        if (rg >= cnt) break;
+        // packed rows 16g + r: gate row 8g + r (r < 8), up row 8g + r - 8
         const float g = gsg * (acc[rg][i][c] * s);
         const float uu = gsu * (acc[rg][i][2 + c] * s);
         const __nv_bfloat16 hb = __float2bfloat16_rn(silu(g) * uu);
-        const int f = 8 * (dec::kRG * b + rg) + r0;
+        const int f = 8 * (dec::kRG * b + rg0 + rg) + r0;
         a.h[(size_t)row * a.I + f] = hb;
         hmax[i][c] = fmaxf(hmax[i][c], fabsf(__bfloat162float(hb)));
       }
     }
   // row maxima: reduce over the 8 lanes that share a token slot, then one
-  // atomic per row from this block
+  // atomic per row from this piece
 #pragma unroll
   for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -344,8 +377,8 @@ __device__ void finish_gateup(const FusedArgs& a, const RouteSmem& rs, int u, in
     }
 }
 
-__device__ void finish_down(const FusedArgs& a, const RouteSmem& rs, int u, int b, float (&acc)[dec::kRG][2][4],
-                            int lane) {
+__device__ void finish_down(const FusedArgs& a, const RouteSmem& rs, int u, int b, int rg0, int cnt,
+                            float (&acc)[dec::kRG][2][4], int lane) {
   const int e = rs.tch_e[u], row0 = rs.tch_r0[u], m = rs.tch_m[u];
   const int r0 = lane >> 2, q = lane & 3;
   const float gsd = a.gscale[3 * e + 2];
@@ -359,7 +392,8 @@ __device__ void finish_down(const FusedArgs& a, const RouteSmem& rs, int u, int 
       const float s = gsd * pow2f(prescale_exp(__uint_as_float(__ldcg(a.hmax + row))));
 #pragma unroll
       for (int rg = 0; rg < dec::kRG; ++rg) {
-        const int d = 16 * (dec::kRG * b + rg) + r0;
+        if (rg >= cnt) break;
+        const int d = 16 * (dec::kRG * b + rg0 + rg) + r0;
         a.y[(size_t)row * a.H + d] = acc[rg][i][c] * s;
         a.y[(size_t)row * a.H + d + 8] = acc[rg][i][2 + c] * s;
       }
@@ -367,17 +401,23 @@ __device__ void finish_down(const FusedArgs& a, const RouteSmem& rs, int u, int 
 }
 
 // The 64-wide slice b of H is complete for every expert: out[t][slice] =
-// sum_j w[t][j] * y[pos(t,j)][slice], slot order j = 0..k-1.
+// sum_j w[t][j] * y[pos(t,j)][slice], slot order j = 0..k-1.  All k loads of
+// a token are issued before the first use (k <= 16).
 __device__ void combine_slice(const FusedArgs& a, const RouteSmem& rs, int b, int lane) {
   const int d = 64 * b + 2 * lane;
   for (int t = 0; t < a.T; ++t) {
+    float2 yy[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < a.k) yy[j] = __ldcg(reinterpret_cast<const float2*>(a.y + (size_t)rs.inv[t * a.k + j] * a.H + d));
     float s0 = 0.f, s1 = 0.f;
-    for (int j = 0; j < a.k; ++j) {
-      const float w = rs.wts[t * a.k + j];
-      const float2 yy = __ldcg(reinterpret_cast<const float2*>(a.y + (size_t)rs.inv[t * a.k + j] * a.H + d));
-      s0 = fmaf(w, yy.x, s0);
-      s1 = fmaf(w, yy.y, s1);
-    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < a.k) {
+        const float w = rs.wts[t * a.k + j];
+        s0 = fmaf(w, yy[j].x, s0);
+        s1 = fmaf(w, yy[j].y, s1);
+      }
     if (a.out_f32) {
       *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + (size_t)t * a.H + d) = make_float2(s0, s1);
     } else {
@@ -388,138 +428,224 @@ __device__ void combine_slice(const FusedArgs& a, const RouteSmem& rs, int b, in
 }
 
 // ---------------------------------------------------------------------------
-// Phases 1 and 2: stream-K GEMV over this warp's range of chunks.
+// Phases 1 and 2.  Work split: the units of a phase are the 16-row groups of
+// the touched experts' matrices (gate/up: 2I/16 per expert, down: H/16),
+// numbered expert-major.  CTA c takes units [g0, g1) (equal counts) over the
+// whole K axis, so no output row's sum crosses CTAs.  Inside the CTA, the
+// units of one 64-row block form a piece of nch 64-wide K chunks, and the
+// (piece, chunk) items are cut into 16 equal contiguous warp ranges: split-K
+// inside the CTA only.
 // ---------------------------------------------------------------------------
-// Position in the flat (touched expert u, 64-row block b, chunk c) list.
-struct ItemPos {
-  int u, b, c;
-  __device__ __forceinline__ void next(int nch, int nblk) {
-    if (++c == nch) {
-      c = 0;
-      if (++b == nblk) {
-        b = 0;
-        ++u;
-      }
+struct CtaWork {
+  int g0, g1;     // this CTA's units
+  int B0;         // global 64-row block of piece 0
+  int nch, nblk;  // chunks per piece; 64-row blocks per expert
+  int nit;        // items: pieces x nch
+  __device__ __forceinline__ void piece(int p, int* u, int* b, int* rg0, int* cnt) const {
+    const int B = B0 + p;
+    const int lo = max(g0, 4 * B), hi = min(g1, 4 * B + 4);
+    *u = B / nblk;
+    *b = B - *u * nblk;
+    *rg0 = lo - 4 * B;
+    *cnt = hi - lo;
+  }
+  __device__ __forceinline__ int unit_of(int p) const { return max(g0, 4 * (B0 + p)); }  // a piece's id
+  // Warps split the CTA's items by an estimate of their time: a ring stage
+  // costs about as much as four 16-row groups of a 64-wide chunk on top of
+  // its bytes, so item i (piece p, chunk c) weighs kItemCost + cnt_p and
+  // starts at cum(i) = nch * (units before p + kItemCost * p) + c * (kItemCost
+  // + cnt_p); warp w takes the items with T_w <= cum(i) < T_w+1, T_w =
+  // floor(cum(nit) * w / 16).
+  static constexpr int kItemCost = 4;
+  __device__ __forceinline__ long long cum(int i) const {
+    const int p = i / nch;
+    const int lo = unit_of(p), hi = min(g1, 4 * (B0 + p) + 4);
+    return (long long)nch * ((lo - g0) + kItemCost * p) + (long long)(i - p * nch) * (kItemCost + hi - lo);
+  }
+  __device__ __forceinline__ long long total() const {
+    return (long long)nch * ((g1 - g0) + kItemCost * (nit / nch));
+  }
+  __device__ __forceinline__ int range_lo(int w) const {
+    if (w <= 0 || nit == 0) return 0;
+    if (w >= dec::kWarps) return nit;
+    const long long T = total() * w / dec::kWarps;
+    int lo = 0, hi = nit;  // the first item with cum >= T (cum is increasing)
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (cum(mid) >= T) hi = mid;
+      else lo = mid + 1;
     }
+    return lo;
+  }
+  // the warp whose range [range_lo(w), range_lo(w + 1)) holds item i
+  __device__ __forceinline__ int warp_of(int i) const {
+    const long long tot = total();
+    return (int)(((cum(i) + 1) * dec::kWarps + tot - 1) / tot) - 1;
   }
 };
 
-__device__ __forceinline__ ItemPos item_at(long long f, int nch, int nblk) {
-  const int fi = (int)f;  // < 2^31: at most 256 experts x 512 blocks x 256 chunks
-  const int blk = fi / nch;
-  ItemPos p;
-  p.c = fi - blk * nch;
-  p.u = blk / nblk;
-  p.b = blk - p.u * nblk;
-  return p;
+__device__ __forceinline__ CtaWork cta_work(long long units, int per_expert, int nch) {
+  CtaWork w;
+  const long long C = gridDim.x;
+  w.g0 = (int)(units * blockIdx.x / C);
+  w.g1 = (int)(units * (blockIdx.x + 1) / C);
+  w.nch = nch;
+  w.nblk = per_expert / 4;
+  w.B0 = w.g0 >> 2;
+  w.nit = w.g1 > w.g0 ? (((w.g1 - 1) >> 2) - w.B0 + 1) * nch : 0;
+  return w;
 }
 
-template <bool kGateUp, int S, int NG>
+// kXs (gate/up only): the routed tokens' activations are already in shared
+// memory as prescaled FP16 rows (xs, xs_pitch bytes apart), so stages carry
+// weights only.  Every stage's weight copies are issued before its activation
+// copies; at the start of the down phase all S-1 weight copies go out before
+// the wait for the expert's h, so they land while the gate/up phase finishes.
+template <bool kGateUp, int S, int NG, bool kXs>
 __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint64_t* bars, uint32_t& ring_it,
-                          long long F, long long W, long long wg, unsigned long long* tr, float* part_s,
-                          int* cnt_s) {
-  const int nch_ = kGateUp ? a.H / kChunk : a.I / kChunk;
-  // split-K: equal chunk ranges; no_split: equal ranges of whole blocks
-  const long long fbeg = a.no_split ? (F / nch_) * wg / W * nch_ : F * wg / W;
-  const long long fend = a.no_split ? (F / nch_) * (wg + 1) / W * nch_ : F * (wg + 1) / W;
-  constexpr int kStageBytes = dec::stage_bytes(NG);
-  const int lane = threadIdx.x & 31, q = lane & 3, r0 = lane >> 2;
-  const int K = kGateUp ? a.H : a.I;
-  const int nch = K / kChunk;
-  const int nblk = kGateUp ? (2 * a.I / 64) : (a.H / 64);
-  const int nblk_gu = 2 * a.I / 64;
+                          const CtaWork& cw, unsigned long long* tr, float* part_s, int* cnt_s,
+                          const uint8_t* xs) {
+  const int kStageBytes = a.stage_bytes;
+  const int srows = dec::stage_rows(a.T);  // activation rows a stage holds
+  constexpr bool kActCopies = !(kGateUp && kXs);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3, r0 = lane >> 2;
+  const int nch = cw.nch;
+  const int gu_units = 2 * a.I / 16;
+  const int scol = a.slot_cols;  // token columns of a shared-memory slot
   const size_t nib_off = kGateUp ? a.nib13 : a.nib2;
   const size_t sc_off = kGateUp ? a.sc13 : a.sc2;
-  const int nf = (int)(fend - fbeg);
+  // without shared-memory slots or global partial buffers: whole pieces per warp
+  const bool whole_only = a.no_split && part_s == nullptr;
+  int ibeg, iend;
+  if (whole_only) {
+    const int np = cw.nit / nch;
+    ibeg = np * warp / dec::kWarps * nch;
+    iend = np * (warp + 1) / dec::kWarps * nch;
+  } else {
+    ibeg = cw.range_lo(warp);
+    iend = cw.range_lo(warp + 1);
+  }
+  const int nf = iend - ibeg;
   if (nf <= 0) return;
-
-  // ---- producer state (runs S-1 items ahead of the consumer) ----
-  ItemPos ip = item_at(fbeg, nch, nblk);
-  int ip_u = -1, ip_m = 0;
-  const uint8_t* ip_nib = nullptr;
-  const uint8_t* ip_sc = nullptr;
-  const uint8_t* ip_row = nullptr;  // lane j < m: its routed row's activations (bytes)
+  const uint32_t it0 = ring_it;
   bool dead = false;
 
-  auto issue = [&](uint32_t it) {
-    if (ip.u != ip_u) {
-      const int u = ip.u;
-      if (!kGateUp) {  // h of expert u must be complete
-        if (lane == 0) {
-          const uint64_t t0 = now_ns();
-          while (ld_acquire(a.done_gu + u) < nblk_gu) {
-            if (aborted(a.st)) break;
-            if (now_ns() - t0 > dec::kTimeoutNs) {
-              report(a.st, kFlagTimeout, 100 + (unsigned)u);
-              break;
-            }
-            __nanosleep(64);
-          }
-        }
-        __syncwarp();
-        __threadfence();
-        // h was written through the generic proxy; the copies read it through the async proxy
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        if (aborted(a.st)) dead = true;
-        if (tr && lane == 0 && tr[3] == 0) tr[3] = now_ns();
-      }
-      const int e = rs.tch_e[u], row0 = rs.tch_r0[u];
-      ip_m = min(rs.tch_m[u], 8 * NG);
-      ip_row = nullptr;
-      if (lane < ip_m)
-        ip_row = kGateUp ? reinterpret_cast<const uint8_t*>(a.x + (size_t)(rs.perm[row0 + lane] / a.k) * a.H)
-                         : reinterpret_cast<const uint8_t*>(a.h + (size_t)(row0 + lane) * a.I);
-      ip_nib = a.blob + (size_t)e * a.expert_stride + nib_off;
-      ip_sc = a.blob + (size_t)e * a.expert_stride + sc_off;
-      ip_u = u;
+  // ---- producer: weight copies (with the stage's byte count), then
+  // activation copies, S-1 items ahead of the consumer ----
+  int wpp = ibeg / nch, wpc = ibeg - (ibeg / nch) * nch, wp_cur = -1, w_cnt = 0, w_m = 0;
+  size_t w_seg = 0;
+  const uint8_t* w_nib = nullptr;
+  const uint8_t* w_sc = nullptr;
+  auto issue_w = [&](uint32_t it) {
+    if (wpp != wp_cur) {
+      int u, b, rg0, cnt;
+      cw.piece(wpp, &u, &b, &rg0, &cnt);
+      const int e = rs.tch_e[u];
+      w_m = kActCopies ? min(rs.tch_m[u], 8 * NG) : 0;
+      w_nib = a.blob + (size_t)e * a.expert_stride + nib_off;
+      w_sc = a.blob + (size_t)e * a.expert_stride + sc_off;
+      // 16-row group g of 128-row block B2 at K chunk c is 512-byte segment
+      // (B2 * nch + c) * 8 + (g & 7); 64-row block b is groups 4(b&1)..+3 of B2 = b >> 1
+      w_seg = (size_t)(b >> 1) * nch * 8 + 4 * (b & 1) + rg0;
+      w_cnt = cnt;
+      wp_cur = wpp;
     }
-    const int slot = (int)(it % S);
-    uint8_t* st = ring + slot * kStageBytes;
-    uint64_t* bar = bars + slot;
-    // the 4 row groups of block b are sub-blocks 4(b&1)..+3 of 128-row block b>>1
-    const size_t seg0 = ((size_t)(ip.b >> 1) * nch + ip.c) * 8 + 4 * (ip.b & 1);
+    uint64_t* bar = bars + (int)(it % S);
+    uint8_t* st = ring + (int)(it % S) * kStageBytes;
+    const size_t seg0 = w_seg + (size_t)wpc * 8;
     // earlier generic reads and writes of this memory come before the copies
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (lane == 0) {
-      mbar_expect_tx(bar, 2048u + 256u + 128u * (uint32_t)ip_m);
-      bulk_copy(st + dec::kStA, ip_nib + seg0 * 512, 2048, bar);
-      bulk_copy(st + dec::kStS, ip_sc + seg0 * 64, 256, bar);
+      mbar_expect_tx(bar, (uint32_t)w_cnt * (512u + 64u) + 128u * (uint32_t)w_m);
+      bulk_copy(st + dec::kStA, w_nib + seg0 * 512, 512u * (uint32_t)w_cnt, bar);
+      bulk_copy(st + dec::kStS, w_sc + seg0 * 64, 64u * (uint32_t)w_cnt, bar);
     }
-    __syncwarp();
-    if (lane < ip_m)
+    if (++wpc == nch) {
+      wpc = 0;
+      ++wpp;
+    }
+  };
+  int app = ibeg / nch, apc = ibeg - (ibeg / nch) * nch, ap_cur = -1, ap_u = -1, a_m = 0;
+  const uint8_t* a_row = nullptr;  // lane j < m: its routed row's activations (bytes)
+  auto issue_a = [&](uint32_t it) {
+    if (!kActCopies) return;
+    if (app != ap_cur) {
+      int u, b, rg0, cnt;
+      cw.piece(app, &u, &b, &rg0, &cnt);
+      if (u != ap_u) {
+        if (!kGateUp) {  // h of expert u must be complete
+          if (lane == 0) {
+            const uint64_t t0 = now_ns();
+            while (ld_acquire(a.done_gu + u) < gu_units) {
+              if (aborted(a.st)) break;
+              if (now_ns() - t0 > dec::kTimeoutNs) {
+                report(a.st, kFlagTimeout, 100 + (unsigned)u);
+                break;
+              }
+              __nanosleep(64);
+            }
+          }
+          __syncwarp();
+          __threadfence();
+          // h was written through the generic proxy; the copies read it through the async proxy
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          if (aborted(a.st)) dead = true;
+          if (tr && lane == 0 && tr[3] == 0) tr[3] = now_ns();
+        }
+        const int row0 = rs.tch_r0[u];
+        a_m = min(rs.tch_m[u], 8 * NG);
+        a_row = nullptr;
+        if (lane < a_m)
+          a_row = kGateUp ? reinterpret_cast<const uint8_t*>(a.x + (size_t)(rs.perm[row0 + lane] / a.k) * a.H)
+                          : reinterpret_cast<const uint8_t*>(a.h + (size_t)(row0 + lane) * a.I);
+        ap_u = u;
+      }
+      ap_cur = app;
+    }
+    uint8_t* st = ring + (int)(it % S) * kStageBytes;
+    __syncwarp();  // the stage's expect_tx (lane 0) comes first
+    if (lane < a_m)
       bulk_copy(st + dec::kStB + (lane >> 3) * 8 * dec::kRowPitch + (lane & 7) * dec::kRowPitch,
-                ip_row + (size_t)ip.c * 128, 128, bar);
-    ip.next(nch, nblk);
+                a_row + (size_t)apc * 128, 128, bars + (int)(it % S));
+    if (++apc == nch) {
+      apc = 0;
+      ++app;
+    }
   };
 
   // ---- consumer state ----
-  ItemPos cp = item_at(fbeg, nch, nblk);
+  int cpi = ibeg / nch, cc = ibeg - (ibeg / nch) * nch;
   float acc[dec::kRG][2][4];
   float bsc[2] = {1.f, 1.f};
-  int seg_c0 = 0, m = 0, ng = 1;
-  const uint32_t it0 = ring_it;
-  // blocks whose every contributor is a warp of this CTA reduce in shared memory
-  const long long cta_w0 = wg - (wg % dec::kWarps);
-  const long long cs0 = F * cta_w0 / W, cs1 = F * (cta_w0 + dec::kWarps) / W;
-  int seg_idx = 0;
-  uint64_t loop_fin = 0;  // CTA-internal blocks this warp finished during the loop
+  const uint8_t* xrow = nullptr;  // kXs: this lane's token row
+  int seg_c0 = 0, m = 0, ng = 1, cu = 0, cb = 0, crg0 = 0, ccnt = 0;
+  bool fin_head = false, fin_tail = false;  // split segments this warp finished in the loop
   int issued = 0, consumed = 0;
 
-  for (; issued < S - 1 && issued < nf; ++issued) issue(it0 + issued);
+  const int pro = min(S - 1, nf);
+  for (int j = 0; j < pro; ++j) issue_w(it0 + j);
+  for (int j = 0; j < pro; ++j) issue_a(it0 + j);
+  issued = pro;
   for (int i = 0; i < nf && !dead; ++i) {
     const uint32_t it = it0 + i;
-    if (issued < nf) issue(it0 + issued++);
+    if (issued < nf) {
+      issue_w(it0 + issued);
+      issue_a(it0 + issued);
+      ++issued;
+    }
     if (dead) break;
     if (!ring_wait(bars + it % S, (it / S) & 1u, a.st)) {
       dead = true;
       break;
     }
+    if (kGateUp && i == 0 && tr && lane == 0) tr[13] = now_ns();
     consumed = i + 1;
-    const int u = cp.u, b = cp.b, c = cp.c;
+    const int c = cc, p = cpi;
     if (i == 0 || c == 0) {
       seg_c0 = c;
-      const int row0 = rs.tch_r0[u];
-      m = rs.tch_m[u];
+      cw.piece(p, &cu, &cb, &crg0, &ccnt);
+      const int row0 = rs.tch_r0[cu];
+      m = rs.tch_m[cu];
       ng = (m + 7) >> 3;
 #pragma unroll
       for (int rg = 0; rg < dec::kRG; ++rg)
@@ -527,57 +653,71 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
         for (int gi = 0; gi < 2; ++gi)
 #pragma unroll
           for (int z = 0; z < 4; ++z) acc[rg][gi][z] = 0.f;
+      if (kXs) {
+        // rows >= m read row 0's token (their MMA columns are never used)
+        xrow = xs + (size_t)(rs.perm[row0 + (r0 < m ? r0 : 0)] / a.k) * a.xs_pitch + q * 32;
+      } else {
 #pragma unroll
-      for (int gi = 0; gi < 2; ++gi) {
-        const int j = 8 * gi + r0;
-        int p = 0;
-        if (j < m) {
-          const int row = row0 + j;
-          p = kGateUp ? rs.xexp[rs.perm[row] / a.k]
-                      : max(-126, min(126, prescale_exp(__uint_as_float(__ldcg(a.hmax + row)))));
+        for (int gi = 0; gi < 2; ++gi) {
+          const int j = 8 * gi + r0;
+          int pe = 0;
+          if (j < m) {
+            const int row = row0 + j;
+            pe = kGateUp ? rs.xexp[rs.perm[row] / a.k]
+                         : max(-126, min(126, prescale_exp(__uint_as_float(__ldcg(a.hmax + row)))));
+          }
+          bsc[gi] = pow2f(-pe);
         }
-        bsc[gi] = pow2f(-p);
       }
     }
     const uint8_t* st = ring + (int)(it % S) * kStageBytes;
-    // activations: BF16 -> FP16 with the row prescale (rows >= m hold stale
-    // data; their MMA columns are never read)
+    // activations: FP16 after the row prescale (rows >= m hold stale data;
+    // their MMA columns are never read)
     uint32_t bw[2][8];
+    if (kXs) {
+      const uint4 u0 = *reinterpret_cast<const uint4*>(xrow + (size_t)c * 128);
+      const uint4 u1 = *reinterpret_cast<const uint4*>(xrow + (size_t)c * 128 + 16);
+      bw[0][0] = u0.x, bw[0][1] = u0.y, bw[0][2] = u0.z, bw[0][3] = u0.w;
+      bw[0][4] = u1.x, bw[0][5] = u1.y, bw[0][6] = u1.z, bw[0][7] = u1.w;
+    } else {
 #pragma unroll
-    for (int gi = 0; gi < NG; ++gi) {
-      if (gi < ng) {
-        const uint8_t* p = st + dec::kStB + gi * 8 * dec::kRowPitch + r0 * dec::kRowPitch + q * 32;
-        const uint4 u0 = *reinterpret_cast<const uint4*>(p), u1 = *reinterpret_cast<const uint4*>(p + 16);
-        const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      for (int gi = 0; gi < NG; ++gi) {
+        if (gi < ng) {
+          const int srow = 8 * gi + r0 < srows ? 8 * gi + r0 : 0;  // rows past the stage's read row 0
+          const uint8_t* pa = st + dec::kStB + srow * dec::kRowPitch + q * 32;
+          const uint4 u0 = *reinterpret_cast<const uint4*>(pa), u1 = *reinterpret_cast<const uint4*>(pa + 16);
+          const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-        for (int z = 0; z < 8; ++z) {
-          const __half2 hh = __floats2half2_rn(__uint_as_float(w[z] << 16) * bsc[gi],
-                                               __uint_as_float(w[z] & 0xFFFF0000u) * bsc[gi]);
-          bw[gi][z] = *reinterpret_cast<const uint32_t*>(&hh);
+          for (int z = 0; z < 8; ++z) {
+            const __half2 hh = __floats2half2_rn(__uint_as_float(w[z] << 16) * bsc[gi],
+                                                 __uint_as_float(w[z] & 0xFFFF0000u) * bsc[gi]);
+            bw[gi][z] = *reinterpret_cast<const uint32_t*>(&hh);
+          }
         }
       }
     }
 #pragma unroll
     for (int rg = 0; rg < dec::kRG; ++rg) {
+      if (rg >= ccnt) break;
       const uint4 raw = *reinterpret_cast<const uint4*>(st + dec::kStA + rg * 512 + lane * 16);
       const uint32_t s2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(st + dec::kStS + rg * 64 + lane * 2));
       const uint32_t s0 = dup_lo(s2), s1 = dup_hi(s2);
-      uint32_t cx[4], cy[4], cz[4], cw[4];
+      uint32_t cx[4], cy[4], cz[4], cw4[4];
       e2m1x8_to_f16(raw.x, cx);
       e2m1x8_to_f16(raw.y, cy);
       e2m1x8_to_f16(raw.z, cz);
-      e2m1x8_to_f16(raw.w, cw);
+      e2m1x8_to_f16(raw.w, cw4);
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         cx[t] = hmul2_u32(cx[t], s0);
         cy[t] = hmul2_u32(cy[t], s0);
         cz[t] = hmul2_u32(cz[t], s1);
-        cw[t] = hmul2_u32(cw[t], s1);
+        cw4[t] = hmul2_u32(cw4[t], s1);
       }
 #pragma unroll
       for (int kt = 0; kt < 4; ++kt) {
         const uint32_t* r0w = kt < 2 ? cx : cy;
-        const uint32_t* r8w = kt < 2 ? cz : cw;
+        const uint32_t* r8w = kt < 2 ? cz : cw4;
         const int o = 2 * (kt & 1);
         mma_f16_16816(acc[rg][0], r0w[o], r8w[o], r0w[o + 1], r8w[o + 1], bw[0][2 * kt], bw[0][2 * kt + 1]);
         if (NG > 1 && ng > 1)
@@ -585,32 +725,34 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
       }
     }
     __syncwarp();  // every lane is done reading this stage before it is refilled
-    cp.next(nch, nblk);
+    if (++cc == nch) {
+      cc = 0;
+      ++cpi;
+    }
     const bool seg_end = (c == nch - 1) || (i == nf - 1);
     if (!seg_end) continue;
-    if (seg_c0 == 0 && c == nch - 1) {  // the whole block is this warp's: finish it now, signal later
-      ++seg_idx;
-      if (kGateUp) finish_gateup(a, rs, u, b, acc, lane);
-      else finish_down(a, rs, u, b, acc, lane);
+    if (seg_c0 == 0 && c == nch - 1) {  // the whole piece is this warp's: finish it now, signal later
+      if (kGateUp) finish_gateup(a, rs, cu, cb, crg0, ccnt, acc, lane);
+      else finish_down(a, rs, cu, cb, crg0, ccnt, acc, lane);
       continue;
     }
-    const int seg_here = seg_idx++;
-    const long long f0 = (long long)(u * nblk + b) * nch;
-    if (part_s != nullptr && f0 >= cs0 && f0 + nch <= cs1) {
+    const bool head = (i - (c - seg_c0)) == 0;  // the segment starts this warp's range
+    if (part_s != nullptr) {
       // split among warps of this CTA: shared-memory sum, the last one finishes
-      const long long wlo = ((f0 + 1) * W + F - 1) / F - 1;  // warp holding the block's first chunk
-      const int slot = (int)(wlo - cta_w0);                    // its boundary with the next warp
-      float* ps = part_s + slot * 64 * 8;
+      const int slot = cw.warp_of(p * nch);  // the warp holding the piece's first chunk
+      float* ps = part_s + slot * 64 * scol;
 #pragma unroll
-      for (int rg = 0; rg < dec::kRG; ++rg)
+      for (int rg = 0; rg < dec::kRG; ++rg) {
+        if (rg >= ccnt) break;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int j = 2 * q + cc;
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int j = 2 * q + h2;
           if (j < m) {
-            atomicAdd(ps + (rg * 16 + r0) * 8 + j, acc[rg][0][cc]);
-            atomicAdd(ps + (rg * 16 + r0 + 8) * 8 + j, acc[rg][0][2 + cc]);
+            atomicAdd(ps + (rg * 16 + r0) * scol + j, acc[rg][0][h2]);
+            atomicAdd(ps + (rg * 16 + r0 + 8) * scol + j, acc[rg][0][2 + h2]);
           }
         }
+      }
       __syncwarp();
       int last = 0;
       if (lane == 0) {
@@ -626,81 +768,63 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
 #pragma unroll
           for (int gi = 0; gi < 2; ++gi)
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              const int j = 2 * q + cc;
-              acc[rg][gi][cc] = (gi == 0 && j < m) ? ps[(rg * 16 + r0) * 8 + j] : 0.f;
-              acc[rg][gi][2 + cc] = (gi == 0 && j < m) ? ps[(rg * 16 + r0 + 8) * 8 + j] : 0.f;
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int j = 2 * q + h2;
+              const bool ok = gi == 0 && j < m && rg < ccnt;
+              acc[rg][gi][h2] = ok ? ps[(rg * 16 + r0) * scol + j] : 0.f;
+              acc[rg][gi][2 + h2] = ok ? ps[(rg * 16 + r0 + 8) * scol + j] : 0.f;
             }
-        if (kGateUp) finish_gateup(a, rs, u, b, acc, lane);
-        else finish_down(a, rs, u, b, acc, lane);
-        if (seg_here < 64) loop_fin |= 1ull << seg_here;
+        if (kGateUp) finish_gateup(a, rs, cu, cb, crg0, ccnt, acc, lane);
+        else finish_down(a, rs, cu, cb, crg0, ccnt, acc, lane);
+        if (head) fin_head = true;
+        else fin_tail = true;
       }
       continue;
     }
-    // split across CTAs: store the partial sums into this warp's global slot
-    // (0: its first segment, 1: its last); counted at the end of the phase
+    // no shared-memory slots: store the partial sums into this warp's global
+    // slot (0: its first segment, 1: its last); counted in at the end of the phase
     {
-      const int slot = (i + 1 - (c - seg_c0 + 1) == 0) ? 0 : 1;  // did the segment start at the range start?
-      float* part = (kGateUp ? a.part_gu : a.part_dn) + ((size_t)wg * 2 + slot) * 64 * a.mslot;
+      float* part = (kGateUp ? a.part_gu : a.part_dn) +
+                    (((size_t)blockIdx.x * dec::kWarps + warp) * 2 + (head ? 0 : 1)) * 64 * a.mslot;
 #pragma unroll
-      for (int rg = 0; rg < dec::kRG; ++rg)
+      for (int rg = 0; rg < dec::kRG; ++rg) {
+        if (rg >= ccnt) break;
 #pragma unroll
         for (int gi = 0; gi < 2; ++gi)
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int j = 8 * gi + 2 * q + cc;
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int j = 8 * gi + 2 * q + h2;
             if (j < m) {
-              __stcg(part + (rg * 16 + r0) * a.mslot + j, acc[rg][gi][cc]);
-              __stcg(part + (rg * 16 + r0 + 8) * a.mslot + j, acc[rg][gi][2 + cc]);
+              __stcg(part + (rg * 16 + r0) * a.mslot + j, acc[rg][gi][h2]);
+              __stcg(part + (rg * 16 + r0 + 8) * a.mslot + j, acc[rg][gi][2 + h2]);
             }
           }
+      }
     }
   }
+  if (tr && lane == 0) tr[kGateUp ? 11 : 12] = now_ns();
 
   // ---- end of phase: one fence covers every store and partial sum above ----
   if (!dead) {
     const uint64_t t_fin = tr ? now_ns() : 0;
     __threadfence();
     __syncwarp();
-    // walk this warp's segments: count partial ones in; the last contributor
-    // of a block finishes it
-    uint64_t fin_mask = 0;
-    int si = 0;
-    // signals a finished block; used at once for segments past the 64-bit mask
-    auto signal = [&](int blk) {
-      const int u = blk / nblk, b = blk - (blk / nblk) * nblk;
-      if (kGateUp) {
-        if (lane == 0) atomicAdd(&a.done_gu[u], 1);
-      } else {
-        int lastc = 0;
-        if (lane == 0) lastc = (atomicAdd(&a.cmb[b], 1) + 1 == rs.U);
-        lastc = __shfl_sync(0xffffffffu, lastc, 0);
-        if (lastc) {
-          __threadfence();
-          combine_slice(a, rs, b, lane);
-          if (lane == 0) a.cmb[b] = 0;
-        }
-      }
-    };
-    for (long long f = fbeg; f < fend; ++si) {
-      const int blk = (int)(f / nch), c0 = (int)(f % nch);
-      const int c1 = (int)min((long long)nch, c0 + (fend - f));
+    // pass 1: count the split segments that went through global slots in; the
+    // last contributor of a piece finishes it
+    for (int f = ibeg; f < iend;) {
+      const int p = f / nch, c0 = f - (f / nch) * nch;
+      const int c1 = min(nch, c0 + (iend - f));
+      const bool head = f == ibeg;
       f += c1 - c0;
-      if (c0 == 0 && c1 == nch) {
-        if (si < 64) fin_mask |= 1ull << si;
-        else signal(blk);
-        continue;
-      }
-      if (part_s != nullptr && (long long)blk * nch >= cs0 && (long long)blk * nch + nch <= cs1) {
-        if (si < 64 && ((loop_fin >> si) & 1ull)) fin_mask |= 1ull << si;
-        continue;  // reduced in shared memory; finished (or not) by the loop
-      }
+      if ((c0 == 0 && c1 == nch) || part_s != nullptr) continue;
+      int32_t* cnt = (kGateUp ? a.cnt_gu : a.cnt_dn) + cw.unit_of(p);
       int last = 0;
-      if (lane == 0) last = (atomicAdd((kGateUp ? a.cnt_gu : a.cnt_dn) + blk, c1 - c0) + (c1 - c0) == nch);
+      if (lane == 0) last = (atomicAdd(cnt, c1 - c0) + (c1 - c0) == nch);
       last = __shfl_sync(0xffffffffu, last, 0);
       if (!last) continue;
       __threadfence();
-      const int u = blk / nblk, b = blk - (blk / nblk) * nblk;
+      int u, b, rg0, pcnt;
+      cw.piece(p, &u, &b, &rg0, &pcnt);
       const int mm = rs.tch_m[u];
 #pragma unroll
       for (int rg = 0; rg < dec::kRG; ++rg)
@@ -708,48 +832,56 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
         for (int gi = 0; gi < 2; ++gi)
 #pragma unroll
           for (int z = 0; z < 4; ++z) acc[rg][gi][z] = 0.f;
-      // contributors: the warps whose ranges meet [f0, f0 + nch)
-      const long long f0 = (long long)blk * nch;
-      const long long w_lo = ((f0 + 1) * W + F - 1) / F - 1, w_hi = ((f0 + nch) * W + F - 1) / F - 1;
-      for (long long w = w_lo; w <= w_hi; ++w) {
-        const long long s0 = F * w / W, s1 = F * (w + 1) / W;
-        if (s0 >= s1 || s1 <= f0 || s0 >= f0 + nch) continue;
-        const int slot = s0 >= f0 ? 0 : 1;
-        const float* part = (kGateUp ? a.part_gu : a.part_dn) + ((size_t)w * 2 + slot) * 64 * a.mslot;
+      // contributors: this CTA's warps whose ranges meet the piece's items
+      const int i0 = p * nch, i1 = i0 + nch;
+      for (int w = cw.warp_of(i0); w <= cw.warp_of(i1 - 1); ++w) {
+        const int s0 = cw.range_lo(w), s1 = cw.range_lo(w + 1);
+        if (s0 >= s1 || s1 <= i0 || s0 >= i1) continue;
+        const float* part = (kGateUp ? a.part_gu : a.part_dn) +
+                            (((size_t)blockIdx.x * dec::kWarps + w) * 2 + (s0 >= i0 ? 0 : 1)) * 64 * a.mslot;
 #pragma unroll
-        for (int rg = 0; rg < dec::kRG; ++rg)
+        for (int rg = 0; rg < dec::kRG; ++rg) {
+          if (rg >= pcnt) break;
 #pragma unroll
           for (int gi = 0; gi < 2; ++gi)
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              const int j = 8 * gi + 2 * q + cc;
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int j = 8 * gi + 2 * q + h2;
               if (j < mm) {
-                acc[rg][gi][cc] += __ldcg(part + (rg * 16 + r0) * a.mslot + j);
-                acc[rg][gi][2 + cc] += __ldcg(part + (rg * 16 + r0 + 8) * a.mslot + j);
+                acc[rg][gi][h2] += __ldcg(part + (rg * 16 + r0) * a.mslot + j);
+                acc[rg][gi][2 + h2] += __ldcg(part + (rg * 16 + r0 + 8) * a.mslot + j);
               }
             }
+        }
       }
-      if (lane == 0) (kGateUp ? a.cnt_gu : a.cnt_dn)[blk] = 0;
-      if (kGateUp) finish_gateup(a, rs, u, b, acc, lane);
-      else finish_down(a, rs, u, b, acc, lane);
-      if (si < 64) {
-        fin_mask |= 1ull << si;
-      } else {
-        __threadfence();
-        __syncwarp();
-        signal(blk);
-      }
+      if (lane == 0) *cnt = 0;
+      if (kGateUp) finish_gateup(a, rs, u, b, rg0, pcnt, acc, lane);
+      else finish_down(a, rs, u, b, rg0, pcnt, acc, lane);
+      if (head) fin_head = true;
+      else fin_tail = true;
     }
-    // signal the blocks this warp finished (after one more fence)
-    if (fin_mask) {
-      __threadfence();
-      __syncwarp();
-      si = 0;
-      for (long long f = fbeg; f < fend && si < 64; ++si) {
-        const int blk = (int)(f / nch), c0 = (int)(f % nch);
-        const int c1 = (int)min((long long)nch, c0 + (fend - f));
-        f += c1 - c0;
-        if ((fin_mask >> si) & 1ull) signal(blk);
+    // pass 2: after one more fence, signal every piece this warp finished
+    __threadfence();
+    __syncwarp();
+    for (int f = ibeg; f < iend;) {
+      const int p = f / nch, c0 = f - (f / nch) * nch;
+      const int c1 = min(nch, c0 + (iend - f));
+      const bool head = f == ibeg;
+      f += c1 - c0;
+      if (!((c0 == 0 && c1 == nch) || (head ? fin_head : fin_tail))) continue;
+      int u, b, rg0, pcnt;
+      cw.piece(p, &u, &b, &rg0, &pcnt);
+      if (kGateUp) {
+        if (lane == 0) atomicAdd(&a.done_gu[u], pcnt);
+      } else {
+        int lastc = 0;
+        if (lane == 0) lastc = (atomicAdd(&a.cmb[b], pcnt) + pcnt == dec::kRG * rs.U);
+        lastc = __shfl_sync(0xffffffffu, lastc, 0);
+        if (lastc) {
+          __threadfence();
+          combine_slice(a, rs, b, lane);
+          if (lane == 0) a.cmb[b] = 0;
+        }
       }
     }
     if (tr && lane == 0) tr[kGateUp ? 6 : 7] += now_ns() - t_fin;
@@ -770,57 +902,69 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
 template <int S, int NG>
 __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
+  const uint64_t t_start = now_ns();
+  const long long c_start = clock64();
+  // shared memory: routing tables | ring barriers | per-warp rings | split-K
+  // slot counters [2][16] | slots [slot_sets][15][64 rows][slot_cols] | staged FP16 activations
   RouteSmem& rs = *reinterpret_cast<RouteSmem*>(smem);
   const size_t route_bytes = (sizeof(RouteSmem) + 127) & ~size_t(127);
   uint64_t* all_bars = reinterpret_cast<uint64_t*>(smem + route_bytes);
-  // NG == 1: shared-memory split-K slots, one per boundary between the CTA's warps
-  float* part_s = NG == 1 ? reinterpret_cast<float*>(smem + route_bytes + 128 * 8) : nullptr;
-  int* cnt_s = NG == 1 ? reinterpret_cast<int*>(smem + route_bytes + 128 * 8 + dec::kSlotFloats * 4) : nullptr;
-  uint8_t* rings = smem + route_bytes + 128 * 8 + (NG == 1 ? dec::kSlotBytes : 0);
+  uint8_t* rings = smem + route_bytes + 128 * 8;
+  uint8_t* tail = rings + (size_t)dec::kWarps * S * a.stage_bytes;
+  int* cnt_all = reinterpret_cast<int*>(tail);
+  float* slots = reinterpret_cast<float*>(tail + 128);
+  const int slot_floats = dec::kSlots * 64 * a.slot_cols;
+  uint8_t* xs = a.xs_pitch > 0 ? tail + 128 + (size_t)a.slot_sets * slot_floats * 4 : nullptr;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t* ring = rings + warp * S * dec::stage_bytes(NG);
+  uint8_t* ring = rings + (size_t)warp * S * a.stage_bytes;
   uint64_t* bars = all_bars + warp * 8;
-
-  const uint64_t t_start = now_ns();
-  route_block(a, rs, rings);
-  if (a.route_only) return;
-  auto clear_slots = [&]() {
-    if (NG == 1) {
-      for (int i = threadIdx.x; i < dec::kSlotFloats; i += blockDim.x) part_s[i] = 0.f;
-      if (threadIdx.x < 16) cnt_s[threadIdx.x] = 0;
-    }
+  auto clear_slots = [&](int sets) {
+    for (int i = threadIdx.x; i < sets * slot_floats; i += blockDim.x) slots[i] = 0.f;
+    if (threadIdx.x < 32) cnt_all[threadIdx.x] = 0;
   };
-  clear_slots();
-  __syncthreads();
-  unsigned long long* tr = a.trace ? a.trace + ((size_t)blockIdx.x * dec::kWarps + warp) * 8 : nullptr;
+  // ring barriers and slots are set up while routing runs (its barriers order them)
+  if (!a.route_only) {
+    if (lane == 0) {
+      for (int s = 0; s < S; ++s) mbar_init(bars + s, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (a.slot_cols) clear_slots(a.slot_sets);
+  }
+  route_block(a, rs, xs, a.trace ? a.trace + (size_t)blockIdx.x * dec::kWarps * 16 : nullptr);
+  if (a.route_only) return;
+  unsigned long long* tr = a.trace ? a.trace + ((size_t)blockIdx.x * dec::kWarps + warp) * 16 : nullptr;
   if (tr && lane == 0) {
     tr[0] = t_start;
     tr[1] = now_ns();
-  }
-  if (lane == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(bars + s, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tr[14] = (unsigned long long)c_start;
+    tr[15] = (unsigned long long)clock64();
   }
   __syncwarp();
 
-  const long long W = (long long)gridDim.x * dec::kWarps;
-  const long long wg = (long long)blockIdx.x * dec::kWarps + warp;
   const int U = rs.U;
   uint32_t ring_it = 0;
-  const long long F1 = (long long)U * (2 * a.I / 64) * (a.H / kChunk);
-  run_phase<true, S, NG>(a, rs, ring, bars, ring_it, F1, W, wg, tr, part_s, cnt_s);
+  const CtaWork w1 = cta_work((long long)U * (2 * a.I / 16), 2 * a.I / 16, a.H / kChunk);
+  float* slots1 = a.slot_cols ? slots : nullptr;
+  if (xs)
+    run_phase<true, S, NG, true>(a, rs, ring, bars, ring_it, w1, tr, slots1, cnt_all, xs);
+  else
+    run_phase<true, S, NG, false>(a, rs, ring, bars, ring_it, w1, tr, slots1, cnt_all, nullptr);
   if (tr && lane == 0) tr[2] = now_ns();
-  if (NG == 1) {  // phase 2 reuses the shared-memory slots
+  float* slots2 = slots1;
+  if (a.slot_cols && a.slot_sets == 2) {
+    slots2 = slots + slot_floats;  // the down phase has its own slots: no CTA barrier here
+  } else if (a.slot_cols) {        // one set, reused by the down phase
     __syncthreads();
-    clear_slots();
+    clear_slots(1);
     __syncthreads();
   }
-  const long long F2 = (long long)U * (a.H / 64) * (a.I / kChunk);
-  run_phase<false, S, NG>(a, rs, ring, bars, ring_it, F2, W, wg, tr, part_s, cnt_s);
+  const CtaWork w2 = cta_work((long long)U * (a.H / 16), a.H / 16, a.I / kChunk);
+  run_phase<false, S, NG, false>(a, rs, ring, bars, ring_it, w2, tr, slots2,
+                                 cnt_all + (a.slot_sets == 2 ? 16 : 0), nullptr);
   if (tr && lane == 0) tr[4] = now_ns();
 
   // the last CTA out resets the per-forward counters (and, after a timeout,
-  // every partial sum) for the next forward
+  // every arrival counter) for the next forward
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -834,7 +978,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
   for (int i = threadIdx.x; i < U; i += blockDim.x) a.done_gu[i] = 0;
   for (int i = threadIdx.x; i < R; i += blockDim.x) a.hmax[i] = 0u;
   if (aborted(a.st)) {
-    const size_t ngu = (size_t)U * (2 * a.I / 64), ndn = (size_t)U * (a.H / 64);
+    const size_t ngu = (size_t)U * (2 * a.I / 16), ndn = (size_t)U * (a.H / 16);
     for (size_t i = threadIdx.x; i < ngu; i += blockDim.x) a.cnt_gu[i] = 0;
     for (size_t i = threadIdx.x; i < ndn; i += blockDim.x) a.cnt_dn[i] = 0;
     for (int i = threadIdx.x; i < a.H / 64; i += blockDim.x) a.cmb[i] = 0;
@@ -843,29 +987,65 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
   if (threadIdx.x == 0) *a.exit_cnt = 0;
 }
 
-// T <= 8: one token group per expert, shared-memory split-K slots, 3 stages;
-// T <= 16: two groups, 3 stages, split-K through global slots only.
-static size_t smem_for(int S, int NG) {
-  return ((sizeof(RouteSmem) + 127) & ~size_t(127)) + 128 * 8 + (NG == 1 ? dec::kSlotBytes : 0) +
-         (size_t)dec::kWarps * S * dec::stage_bytes(NG);
+// Shared memory: T <= 8 (one token group per expert) adds split-K slots,
+// one set per phase when both fit, and stages the tokens' activations when
+// they fit too, with the deepest rings (3..5 stages per warp) that leave room
+// for both; T <= 16: two token groups, 3 stages, split-K through global
+// slots only.  Environment variables (read once): NVFP4_MOE_DECODE_STAGES
+// caps the ring depth, NVFP4_MOE_DECODE_STAGE_X=0 turns activation staging off.
+struct DecodeSmemPlan {
+  size_t bytes;
+  int stages, slot_cols, slot_sets, xs_pitch;
+};
+static int decode_stage_cap() {
+  static const int cap = [] {
+    const char* s = getenv("NVFP4_MOE_DECODE_STAGES");
+    const int v = s ? atoi(s) : 5;
+    return v < 2 ? 2 : (v > 5 ? 5 : v);
+  }();
+  return cap;
 }
-size_t decode_smem_bytes() { return smem_for(3, 2); }
+static DecodeSmemPlan plan_smem(int T, int H, int smem_max) {
+  const size_t base = ((sizeof(RouteSmem) + 127) & ~size_t(127)) + 128 * 8 + 128;
+  const size_t ring1 = (size_t)dec::kWarps * dec::stage_bytes_for(T);  // one stage per warp
+  const int cap = decode_stage_cap();
+  if (T > 8) {
+    const int S = cap < 3 ? cap : 3;
+    return DecodeSmemPlan{base + S * ring1, S, 0, 0, 0};
+  }
+  const size_t slot_b = (size_t)dec::kSlots * 64 * T * 4;
+  const size_t xs_b = (size_t)T * (2 * H + 16);
+  static const bool stage_x = [] {
+    const char* s = getenv("NVFP4_MOE_DECODE_STAGE_X");
+    return !(s && s[0] == '0');
+  }();
+  for (int S = cap; S >= 3 && stage_x; --S)
+    if (base + S * ring1 + 2 * slot_b + xs_b <= (size_t)smem_max)
+      return DecodeSmemPlan{base + S * ring1 + 2 * slot_b + xs_b, S, T, 2, 2 * H + 16};
+  const int S = cap < 3 ? cap : 3;
+  if (base + S * ring1 + 2 * slot_b <= (size_t)smem_max) return DecodeSmemPlan{base + S * ring1 + 2 * slot_b, S, T, 2, 0};
+  return DecodeSmemPlan{base + S * ring1 + slot_b, S, T, 1, 0};
+}
 
 cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const float* gscale, const void* logits,
                                   const void* x, int T, int k, void* out, int route_only, int num_sms,
                                   const Workspace& ws, cudaStream_t st) {
-  static int attr_done = 0;
-  const bool small = T <= 8;
-  const size_t smem = small ? smem_for(3, 1) : smem_for(3, 2);
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<3, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem_for(3, 1));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_fused_kernel<3, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem_for(3, 2));
+  static int smem_max = 0;
+  if (!smem_max) {
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    const void* fns[] = {(const void*)decode_fused_kernel<2, 1>, (const void*)decode_fused_kernel<3, 1>,
+                         (const void*)decode_fused_kernel<4, 1>, (const void*)decode_fused_kernel<5, 1>,
+                         (const void*)decode_fused_kernel<2, 2>, (const void*)decode_fused_kernel<3, 2>};
+    for (const void* f : fns)
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     if (e != cudaSuccess) return e;
-    attr_done = 1;
+    smem_max = optin;
   }
+  const bool small = T <= 8;
+  const DecodeSmemPlan plan = plan_smem(T, d.H, smem_max);
+  if (plan.bytes > (size_t)smem_max) return cudaErrorInvalidConfiguration;
   const ExpertLayout L = expert_layout(d.H, d.I);
   FusedArgs a{};
   a.blob = blob;
@@ -900,6 +1080,10 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
   a.cnt_dn = ws.cnt_dn;
   a.mslot = T < 16 ? T : 16;
   a.no_split = ws.part_gu == nullptr;
+  a.slot_cols = plan.slot_cols;
+  a.slot_sets = plan.slot_sets;
+  a.xs_pitch = plan.xs_pitch;
+  a.stage_bytes = dec::stage_bytes_for(T);
   a.done_gu = ws.done_gu;
   a.cmb = ws.cmb;
   a.exit_cnt = ws.exit_cnt;
@@ -908,15 +1092,21 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(route_only ? 1 : num_sms);
   cfg.blockDim = dim3(dec::kThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = plan.bytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = route_only ? 0 : 1;
-  return small ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 1>, a)
-               : cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 2>, a);
+  if (!small) return plan.stages == 2 ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<2, 2>, a)
+                                      : cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 2>, a);
+  switch (plan.stages) {
+    case 2: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<2, 1>, a);
+    case 3: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 1>, a);
+    case 4: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<4, 1>, a);
+    default: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<5, 1>, a);
+  }
 }
 
 }  // namespace nvfp4moe

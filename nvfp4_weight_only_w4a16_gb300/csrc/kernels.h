@@ -25,11 +25,11 @@ struct Workspace {
   uint32_t* hmax;      // [R]      max |h| of each row (float bits, decode path)
   float* y;            // [R][H]   expert outputs, position order
   float* part_gu;      // split-K partial sums, gate/up: per decode warp 2 slots of [64][min(T,16)]
-  int32_t* cnt_gu;     // arrival counters per gate/up block  [maxU * I/32]
+  int32_t* cnt_gu;     // arrival counters per gate/up 16-row group [maxU * I/8]
   float* part_dn;      // split-K partial sums, down: as part_gu
-  int32_t* cnt_dn;     // arrival counters per down block     [maxU * H/64]
-  int32_t* done_gu;    // finished gate/up blocks per touched expert [maxU] (decode)
-  int32_t* cmb;        // finished down blocks per 64-wide slice of H [H/64] (decode)
+  int32_t* cnt_dn;     // arrival counters per down 16-row group    [maxU * H/16]
+  int32_t* done_gu;    // finished gate/up 16-row groups per touched expert [maxU] (decode)
+  int32_t* cmb;        // finished down 16-row groups per 64-wide slice of H [H/64] (decode)
   int32_t* exit_cnt;   // CTAs that finished the decode kernel [1]
   int32_t* blk_counts; // [nrb][E] per-rank-block histogram (prefill)
   int32_t* blk_base;   // [nrb][E] per-rank-block base inside each expert
@@ -72,7 +72,6 @@ cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const v
 cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const float* gscale, const void* logits,
                                   const void* x, int T, int k, void* out, int route_only, int num_sms,
                                   const Workspace& ws, cudaStream_t st);
-size_t decode_smem_bytes();
 
 struct PrefillMaps {
   CUtensorMap x_perm;  // [R][H] bf16, box {64, 16}, 128B swizzle

@@ -42,59 +42,78 @@ __device__ __forceinline__ float warp_softmax_k(float logit, int k) {
   return ex / sum;
 }
 
-// One warp routes token t (E <= 256, k <= 16).  Lane j < k receives the j-th
-// choice in (*my_id, *my_w); returns the number of NaN logits of the token.
-__device__ __forceinline__ int warp_topk(const void* logits, int bf16, int E, int k, int t, int* my_id,
-                                         float* my_w) {
+// Lane l of a warp takes the logits e = l + 32 i (i < 8, e < E <= 256) of
+// token t as order keys (float_key: larger value -> larger key, NaN lowest).
+// The loads are only issued here; nothing waits for them.
+__device__ __forceinline__ void warp_load_logits(const void* logits, int bf16, int E, int t, uint32_t (&key)[8],
+                                                 float (&val)[8]) {
   const int lane = threadIdx.x & 31;
-  unsigned long long key[8];
-  float val[8];
-  int nan_count = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    if (e < E) {
-      const float v = load_logit(logits, bf16, (size_t)t * E + e);
-      nan_count += (v != v);
-      val[i] = v;
-      key[i] = ((unsigned long long)float_key(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
-    } else {
-      val[i] = 0.f;
-      key[i] = 0ull;
-    }
+    val[i] = e < E ? load_logit(logits, bf16, (size_t)t * E + e) : 0.f;
   }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) key[i] = float_key(val[i]);
+}
+
+// The k largest keys of the warp (k <= min(E, 16)) in order: largest value
+// first, the lower expert index first among equal values.  Each round takes
+// the warp maximum key (redux.sync), then the lowest index holding it.  Lane
+// j < k receives choice j in (*my_id, *my_logit); returns the token's NaN
+// count.
+__device__ __forceinline__ int warp_select_topk(const uint32_t (&key)[8], const float (&val)[8], int E, int k,
+                                                int* my_id, float* my_logit) {
+  const int lane = threadIdx.x & 31;
+  unsigned avail = 0;
+  int nan = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (lane + 32 * i < E) {
+      avail |= 1u << i;
+      nan += (val[i] != val[i]);
+    }
   int id = -1;
   float logit = 0.f;
   for (int j = 0; j < k; ++j) {
-    unsigned long long best = 0ull;
+    uint32_t bk = 0;
+    int bi = -1;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) best = key[i] > best ? key[i] : best;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
-    }
-    const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+    for (int i = 0; i < 8; ++i)
+      if (((avail >> i) & 1u) && (bi < 0 || key[i] > bk)) {
+        bk = key[i];
+        bi = i;
+      }
+    const uint32_t M = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t cand = (bi >= 0 && bk == M) ? (uint32_t)(lane + 32 * bi) : 0xFFFFu;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
     float v = 0.f;
-    if ((e & 31) == lane) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (lane + 32 * i == e) {
-          key[i] = 0ull;
-          v = val[i];
-        }
-    }
-    v = __shfl_sync(0xffffffffu, v, e & 31);
+    for (int i = 0; i < 8; ++i)
+      if (bi == i) v = val[i];
+    v = __shfl_sync(0xffffffffu, v, (int)(win & 31u));
+    if (lane == (int)(win & 31u)) avail &= ~(1u << (win >> 5));
     if (lane == j) {
-      id = e;
+      id = (int)win;
       logit = v;
     }
   }
   *my_id = id;
+  *my_logit = logit;
+  return (int)__reduce_add_sync(0xffffffffu, (unsigned)nan);
+}
+
+// One warp routes token t (E <= 256, k <= 16).  Lane j < k receives the j-th
+// choice in (*my_id, *my_w); returns the number of NaN logits of the token.
+__device__ __forceinline__ int warp_topk(const void* logits, int bf16, int E, int k, int t, int* my_id,
+                                         float* my_w) {
+  uint32_t key[8];
+  float val[8];
+  warp_load_logits(logits, bf16, E, t, key, val);
+  float logit;
+  const int nan = warp_select_topk(key, val, E, k, my_id, &logit);
   *my_w = warp_softmax_k(logit, k);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) nan_count += __shfl_xor_sync(0xffffffffu, nan_count, o);
-  return nan_count;
+  return nan;
 }
 
 // Exclusive scan of v over the block (<= 1024 threads, all call); *total gets

@@ -84,8 +84,8 @@ size_t carve(uint8_t* base, int E, int H, int I, int T, int k, int num_sms, Work
   uint8_t* b = base ? base : reinterpret_cast<uint8_t*>(0x100);
   Region r;
   Workspace w{};
-  w.cnt_gu = r.take<int32_t>(b, maxU * (2 * I / 64));
-  w.cnt_dn = r.take<int32_t>(b, maxU * (H / 64));
+  w.cnt_gu = r.take<int32_t>(b, maxU * (2 * I / 16));
+  w.cnt_dn = r.take<int32_t>(b, maxU * (H / 16));
   w.done_gu = r.take<int32_t>(b, maxU);
   w.cmb = r.take<int32_t>(b, H / 64);
   w.exit_cnt = r.take<int32_t>(b, 1);
