@@ -94,10 +94,12 @@ __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t v) {
 }
 
 // Order-preserving key of a float: larger float -> larger key; NaN -> 0
-// (below -inf, whose key is 0x007FFFFF).
+// (below -inf, whose key is 0x007FFFFF); -0 and +0 share one key, as they
+// compare equal.
 __device__ __forceinline__ uint32_t float_key(float f) {
-  uint32_t b = __float_as_uint(f);
   if (f != f) return 0u;
+  if (f == 0.0f) return 0x80000000u;
+  const uint32_t b = __float_as_uint(f);
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 

@@ -184,9 +184,13 @@ def test_route_edge_cases():
     logits[2, :] = -np.inf
     logits[3, 7] = np.inf
     logits[4, [3, 9]] = np.inf
+    logits[5, :] = -1.0                         # -0 and +0 compare equal: lower index first
+    logits[5, 6] = 0.0
+    logits[5, 1] = -0.0
     for path in (P.PATH_PREFILL,):
         r = _check_route(L, logits, 3, 40, path)
     assert r.ids[0].tolist() == [0, 1, 2]
+    assert r.ids[5].tolist()[:2] == [1, 6]
     for k in (1, 2, 3):
         _check_route(L, logits, k, 40, P.PATH_PREFILL)
         _check_route(L, logits[:16], k, 40, P.PATH_DECODE)
