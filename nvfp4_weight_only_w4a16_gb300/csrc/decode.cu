@@ -35,8 +35,9 @@
 //    prescale (exact for BF16 values within 2^31 of the row maximum), undone
 //    in FP32;
 //  * the down GEMV of expert u starts once all gate/up rows of u are done
-//    (per-expert counter, bounded wait); the last down block to finish a
-//    64-wide slice of H combines that slice for every token, in slot order.
+//    (per-expert counter, bounded wait); the combine is spread over every
+//    warp as (64-wide slice of H, token) tasks, each starting once its slice
+//    is finished for every expert, summing in slot order.
 #include <cstdlib>
 
 #include "common.cuh"
@@ -400,30 +401,54 @@ __device__ void finish_down(const FusedArgs& a, const RouteSmem& rs, int u, int 
     }
 }
 
-// The 64-wide slice b of H is complete for every expert: out[t][slice] =
-// sum_j w[t][j] * y[pos(t,j)][slice], slot order j = 0..k-1.  All k loads of
-// a token are issued before the first use (k <= 16).
-__device__ void combine_slice(const FusedArgs& a, const RouteSmem& rs, int b, int lane) {
+// Token t's 64-wide slice b of the output, once slice b is complete for
+// every expert: out[t][slice] = sum_j w[t][j] * y[pos(t,j)][slice], slot
+// order j = 0..k-1.  All k loads are issued before the first use (k <= 16).
+__device__ void combine_slice_token(const FusedArgs& a, const RouteSmem& rs, int b, int t, int lane) {
   const int d = 64 * b + 2 * lane;
-  for (int t = 0; t < a.T; ++t) {
-    float2 yy[16];
+  float2 yy[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (j < a.k) yy[j] = __ldcg(reinterpret_cast<const float2*>(a.y + (size_t)rs.inv[t * a.k + j] * a.H + d));
-    float s0 = 0.f, s1 = 0.f;
+  for (int j = 0; j < 16; ++j)
+    if (j < a.k) yy[j] = __ldcg(reinterpret_cast<const float2*>(a.y + (size_t)rs.inv[t * a.k + j] * a.H + d));
+  float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (j < a.k) {
-        const float w = rs.wts[t * a.k + j];
-        s0 = fmaf(w, yy[j].x, s0);
-        s1 = fmaf(w, yy[j].y, s1);
-      }
-    if (a.out_f32) {
-      *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + (size_t)t * a.H + d) = make_float2(s0, s1);
-    } else {
-      *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(a.out) + (size_t)t * a.H + d) =
-          __floats2bfloat162_rn(s0, s1);
+  for (int j = 0; j < 16; ++j)
+    if (j < a.k) {
+      const float w = rs.wts[t * a.k + j];
+      s0 = fmaf(w, yy[j].x, s0);
+      s1 = fmaf(w, yy[j].y, s1);
     }
+  if (a.out_f32) {
+    *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + (size_t)t * a.H + d) = make_float2(s0, s1);
+  } else {
+    *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(a.out) + (size_t)t * a.H + d) =
+        __floats2bfloat162_rn(s0, s1);
+  }
+}
+
+// The combine, spread over every warp of the grid: task (slice b, token t),
+// warp wg takes tasks wg, wg + W, ...; a task starts once all 4U 16-row groups
+// of slice b are finished (counter cmb[b], bounded wait).
+__device__ void combine_tasks(const FusedArgs& a, const RouteSmem& rs, long long wg, long long W, int lane) {
+  const int nslices = a.H / 64;
+  const int target = dec::kRG * rs.U;
+  for (long long task = wg; task < (long long)nslices * a.T; task += W) {
+    const int t = (int)(task / nslices), b = (int)(task - (long long)t * nslices);
+    if (lane == 0) {
+      const uint64_t t0 = now_ns();
+      while (ld_acquire(a.cmb + b) < target) {
+        if (aborted(a.st)) break;
+        if (now_ns() - t0 > dec::kTimeoutNs) {
+          report(a.st, kFlagTimeout, 400 + (unsigned)b);
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
+    __syncwarp();
+    if (aborted(a.st)) return;
+    __threadfence();
+    combine_slice_token(a, rs, b, t, lane);
   }
 }
 
@@ -745,13 +770,15 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
       for (int rg = 0; rg < dec::kRG; ++rg) {
         if (rg >= ccnt) break;
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int j = 2 * q + h2;
-          if (j < m) {
-            atomicAdd(ps + (rg * 16 + r0) * scol + j, acc[rg][0][h2]);
-            atomicAdd(ps + (rg * 16 + r0 + 8) * scol + j, acc[rg][0][2 + h2]);
+        for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int j = 8 * gi + 2 * q + h2;
+            if (j < m) {
+              atomicAdd(ps + (rg * 16 + r0) * scol + j, acc[rg][gi][h2]);
+              atomicAdd(ps + (rg * 16 + r0 + 8) * scol + j, acc[rg][gi][2 + h2]);
+            }
           }
-        }
       }
       __syncwarp();
       int last = 0;
@@ -769,8 +796,8 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
           for (int gi = 0; gi < 2; ++gi)
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-              const int j = 2 * q + h2;
-              const bool ok = gi == 0 && j < m && rg < ccnt;
+              const int j = 8 * gi + 2 * q + h2;
+              const bool ok = gi < NG && j < m && rg < ccnt;
               acc[rg][gi][h2] = ok ? ps[(rg * 16 + r0) * scol + j] : 0.f;
               acc[rg][gi][2 + h2] = ok ? ps[(rg * 16 + r0 + 8) * scol + j] : 0.f;
             }
@@ -874,14 +901,7 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
       if (kGateUp) {
         if (lane == 0) atomicAdd(&a.done_gu[u], pcnt);
       } else {
-        int lastc = 0;
-        if (lane == 0) lastc = (atomicAdd(&a.cmb[b], pcnt) + pcnt == dec::kRG * rs.U);
-        lastc = __shfl_sync(0xffffffffu, lastc, 0);
-        if (lastc) {
-          __threadfence();
-          combine_slice(a, rs, b, lane);
-          if (lane == 0) a.cmb[b] = 0;
-        }
+        if (lane == 0) atomicAdd(&a.cmb[b], pcnt);
       }
     }
     if (tr && lane == 0) tr[kGateUp ? 6 : 7] += now_ns() - t_fin;
@@ -962,6 +982,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
   run_phase<false, S, NG, false>(a, rs, ring, bars, ring_it, w2, tr, slots2,
                                  cnt_all + (a.slot_sets == 2 ? 16 : 0), nullptr);
   if (tr && lane == 0) tr[4] = now_ns();
+  combine_tasks(a, rs, (long long)blockIdx.x * dec::kWarps + warp, (long long)gridDim.x * dec::kWarps, lane);
 
   // the last CTA out resets the per-forward counters (and, after a timeout,
   // every arrival counter) for the next forward
@@ -977,11 +998,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
   const int R = a.T * a.k;
   for (int i = threadIdx.x; i < U; i += blockDim.x) a.done_gu[i] = 0;
   for (int i = threadIdx.x; i < R; i += blockDim.x) a.hmax[i] = 0u;
+  for (int i = threadIdx.x; i < a.H / 64; i += blockDim.x) a.cmb[i] = 0;
   if (aborted(a.st)) {
     const size_t ngu = (size_t)U * (2 * a.I / 16), ndn = (size_t)U * (a.H / 16);
     for (size_t i = threadIdx.x; i < ngu; i += blockDim.x) a.cnt_gu[i] = 0;
     for (size_t i = threadIdx.x; i < ndn; i += blockDim.x) a.cnt_dn[i] = 0;
-    for (int i = threadIdx.x; i < a.H / 64; i += blockDim.x) a.cmb[i] = 0;
   }
   __syncthreads();
   if (threadIdx.x == 0) *a.exit_cnt = 0;
@@ -990,9 +1011,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
 // Shared memory: T <= 8 (one token group per expert) adds split-K slots,
 // one set per phase when both fit, and stages the tokens' activations when
 // they fit too, with the deepest rings (3..5 stages per warp) that leave room
-// for both; T <= 16: two token groups, 3 stages, split-K through global
-// slots only.  Environment variables (read once): NVFP4_MOE_DECODE_STAGES
-// caps the ring depth, NVFP4_MOE_DECODE_STAGE_X=0 turns activation staging off.
+// for both; T <= 16 (two token groups): 2 stages and one set of split-K slots
+// (cleared between the phases).  Environment variables (read once):
+// NVFP4_MOE_DECODE_STAGES caps the ring depth, NVFP4_MOE_DECODE_STAGE_X=0
+// turns activation staging off, NVFP4_MOE_DECODE_T16_SLOTS=0 gives T > 8
+// three stages and global split-K slots instead.
 struct DecodeSmemPlan {
   size_t bytes;
   int stages, slot_cols, slot_sets, xs_pitch;
@@ -1009,7 +1032,14 @@ static DecodeSmemPlan plan_smem(int T, int H, int smem_max) {
   const size_t base = ((sizeof(RouteSmem) + 127) & ~size_t(127)) + 128 * 8 + 128;
   const size_t ring1 = (size_t)dec::kWarps * dec::stage_bytes_for(T);  // one stage per warp
   const int cap = decode_stage_cap();
-  if (T > 8) {
+  if (T > 8) {  // two ring stages and one set of shared-memory split-K slots, else three stages
+    static const bool slots16 = [] {
+      const char* s = getenv("NVFP4_MOE_DECODE_T16_SLOTS");
+      return !(s && s[0] == '0');
+    }();
+    const size_t slot_b = (size_t)dec::kSlots * 64 * T * 4;
+    if (slots16 && base + 2 * ring1 + slot_b <= (size_t)smem_max)
+      return DecodeSmemPlan{base + 2 * ring1 + slot_b, 2, T, 1, 0};
     const int S = cap < 3 ? cap : 3;
     return DecodeSmemPlan{base + S * ring1, S, 0, 0, 0};
   }
