@@ -207,28 +207,42 @@ def expert_ffn(w, e: int, x) -> np.ndarray:
     return gs[2] * (h @ wd.T)
 
 
-def moe_forward(logits, x_bits, weights, k: int, tokens=None, return_parts=False):
-    """out[t] = sum_{j<k} w[t][j] * FFN_{ids[t][j]}(x[t]) in float64.
+def moe_forward(logits, x_bits, weights, k: int, tokens=None, return_parts=False, num_shared: int = 0):
+    """out[t] = sum_{j<k} w[t][j] * FFN_{ids[t][j]}(x[t]) (+ FFN_E(x[t])) in float64.
 
     logits [T][E] (float32 or float64), x_bits [T][H] BF16 bit patterns,
     weights an ExpertWeights-like object with w13_q/w13_s/w2_q/w2_s/gscale.
+    num_shared = 1: weights also hold expert E (E = logits.shape[1]), the
+    layer's single shared expert, which every token uses with weight 1 on top
+    of its routed experts ("GLM-5.3-Flash on Blackwell", The model loaded,
+    served an API, and produced garbage: the model keeps running "on
+    attention and the single shared expert" when every routed expert is
+    zeroed; "GLM-5.3-Flash-NVFP4-h — W4A16 dense-side quantization": the shared
+    experts' gate/up/down are W4A16 NVFP4 with 16-element groups).  Its output
+    is added after the routed sum.
     tokens: optional subset of token indices (the output has one row per
     listed token, in that order).  With return_parts, also returns the route
-    result and the per-slot expert outputs y [len(tokens)][k][H].
+    result and the per-slot expert outputs y [len(tokens)][k + num_shared][H]
+    (the shared expert's in the last slot).
     """
+    if num_shared not in (0, 1):
+        raise ValueError("num_shared must be 0 or 1")
     logits = np.asarray(logits)
-    T = logits.shape[0]
+    T, E = logits.shape
     tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     r = route(logits[tok], k)
     x = bf16_bits_to_f64(np.asarray(x_bits)[tok])
     H = x.shape[1]
-    y = np.zeros((len(tok), k, H), dtype=np.float64)
+    y = np.zeros((len(tok), k + num_shared, H), dtype=np.float64)
     for e in np.unique(r.ids):
         rows, slots = np.nonzero(r.ids == e)
         y[rows, slots] = expert_ffn(weights, int(e), x[rows])
     out = np.zeros((len(tok), H), dtype=np.float64)
     for j in range(k):
         out += r.weights[:, j:j + 1] * y[:, j]
+    if num_shared:
+        y[:, k] = expert_ffn(weights, E, x)
+        out += y[:, k]
     if return_parts:
         return out, r, y
     return out

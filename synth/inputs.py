@@ -58,11 +58,12 @@ class LayerConfig:
     outlier_mult: float = 1.0
     weight_std: float = 0.02
     seed: int = 0
+    shared: int = 0                 # 1: one shared expert (weights of expert index num_experts)
 
     def with_tokens(self, tokens: int) -> "LayerConfig":
         return LayerConfig(self.name, self.num_experts, self.hidden, self.inter,
                            self.top_k, tokens, self.logits_bias, self.outlier_frac,
-                           self.outlier_mult, self.weight_std, self.seed)
+                           self.outlier_mult, self.weight_std, self.seed, self.shared)
 
     @property
     def expert_bytes(self) -> int:
@@ -83,6 +84,9 @@ CONFIGS = {
     # 16K-token prefill over 256 experts, Zipf(1.1) popularity, 1% x20 outliers.
     "prefill_16k": LayerConfig("prefill_16k", 256, 4096, 1536, 8, 16384, "zipf1.1",
                                0.01, 20.0),
+    # The tiny layer and the MTP step with the layer's single shared expert.
+    "tiny_shared": LayerConfig("tiny_shared", 8, 256, 512, 2, 16, shared=1),
+    "decode_mtp_shared": LayerConfig("decode_mtp_shared", 128, 4096, 1536, 8, 2, shared=1),
 }
 
 
@@ -222,7 +226,8 @@ def _worker(args):
 
 
 def _weight_key(cfg: LayerConfig):
-    return (cfg.num_experts, cfg.hidden, cfg.inter, cfg.outlier_frac,
+    # routed experts 0..E-1, then the shared expert (if any) as expert E
+    return (cfg.num_experts + cfg.shared, cfg.hidden, cfg.inter, cfg.outlier_frac,
             cfg.outlier_mult, cfg.weight_std, cfg.seed)
 
 
@@ -255,7 +260,8 @@ def _layer_weights_cached(key) -> ExpertWeights:
 
 
 def make_layer_weights(cfg: LayerConfig) -> ExpertWeights:
-    """All experts' NVFP4 bytes for cfg (cached per weight recipe)."""
+    """All experts' NVFP4 bytes for cfg (cached per weight recipe); with a
+    shared expert, num_experts + 1 of them."""
     return _layer_weights_cached(_weight_key(cfg))
 
 

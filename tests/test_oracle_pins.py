@@ -276,9 +276,44 @@ def pin_brute_force_layer(o):
         assert np.allclose(out[t], acc, rtol=1e-12, atol=1e-12 * max(abs(a) for a in acc))
 
 
+def pin_shared_expert(o):
+    # closed form: routed experts and the shared expert all-ones (each FFN
+    # gives 2^22 at x = 1); routed weights sum to 1, the shared one adds 1
+    H, I, E, k = 256, 512, 3, 2
+    one = _const_expert(H, I, 0x1, 0x1, 0x1, 0x38, [1.0, 1.0, 1.0])
+    w = _W(*(np.repeat(a, E + 1, axis=0) for a in (one.w13_q, one.w13_s, one.w2_q, one.w2_s, one.gscale)))
+    logits = np.array([[0.3, -1.0, 2.0], [0.0, 0.0, 0.0]], np.float32)
+    xb = _bf16_bits(np.ones((2, H)))
+    out = o.moe_forward(logits, xb, w, k, num_shared=1)
+    assert np.all(out == 2.0 ** 23), out[:, :4]
+    # brute force: scalar loops for the shared expert on a tiny layer
+    rng = np.random.default_rng(17)
+    E, H, I, T, k = 3, 32, 16, 2, 1
+    w = _random_weights(rng, E + 1, H, I)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    xb = _bf16_bits(rng.standard_normal((T, H)))
+    base = o.moe_forward(logits, xb, w, k)
+    out = o.moe_forward(logits, xb, w, k, num_shared=1)
+    tab = _e2m1_table()
+    sc = lambda b: float(_torch_e4m3(np.array([b], np.uint8))[0])
+    nib = lambda q, n, kk: (int(q[n, kk // 2]) >> (4 * (kk % 2))) & 15
+    W = lambda q, s, n, kk: tab[nib(q, n, kk)] * sc(s[n, kk // 16])
+    gs = [float(v) for v in w.gscale[E]]
+    for t in range(T):
+        xs = [float(v) for v in (xb[t].astype(np.uint32) << 16).view(np.float32)]
+        hv = []
+        for n in range(I):
+            g = gs[0] * sum(W(w.w13_q[E], w.w13_s[E], n, kk) * xs[kk] for kk in range(H))
+            u = gs[1] * sum(W(w.w13_q[E], w.w13_s[E], I + n, kk) * xs[kk] for kk in range(H))
+            hv.append(g / (1 + math.exp(-g)) * u)
+        for d in range(H):
+            yd = gs[2] * sum(W(w.w2_q[E], w.w2_s[E], d, n) * hv[n] for n in range(I))
+            assert abs(out[t, d] - (base[t, d] + yd)) <= 1e-12 * max(1.0, abs(yd))
+
+
 PINS = [pin_e2m1_table, pin_e4m3, pin_dequant_worked, pin_round_trip, pin_route,
         pin_permute, pin_ffn_closed_form, pin_identical_experts, pin_top1_dense,
-        pin_brute_force_layer]
+        pin_brute_force_layer, pin_shared_expert]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -387,9 +422,29 @@ def _mut_perm_unstable(m):
     m.permute = f
 
 
+def _mut_shared_dropped(m):
+    orig = m.moe_forward
+    def f(logits, x_bits, weights, k, tokens=None, return_parts=False, num_shared=0):
+        return orig(logits, x_bits, weights, k, tokens, return_parts, 0)
+    m.moe_forward = f
+
+
+def _mut_shared_routed_weight(m):  # the shared expert scaled by the first routing weight
+    orig = m.moe_forward
+    def f(logits, x_bits, weights, k, tokens=None, return_parts=False, num_shared=0):
+        out = orig(logits, x_bits, weights, k, tokens, return_parts, 0)
+        if not num_shared:
+            return out
+        r = m.route(np.asarray(logits), k)
+        x = m.bf16_bits_to_f64(np.asarray(x_bits))
+        return out + r.weights[:, :1] * m.expert_ffn(weights, np.asarray(logits).shape[1], x)
+    m.moe_forward = f
+
+
 MUTANTS = [_mut_nibble_order, _mut_e4m3_bias, _mut_e2m1_subnormal, _mut_scale_group_shift,
            _mut_gate_up_swap, _mut_drop_up_scale, _mut_tie_break, _mut_softmax_all,
-           _mut_no_combine_weights, _mut_silu_sign, _mut_perm_unstable]
+           _mut_no_combine_weights, _mut_silu_sign, _mut_perm_unstable, _mut_shared_dropped,
+           _mut_shared_routed_weight]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS, ids=lambda f: f.__name__)
