@@ -76,7 +76,16 @@ typedef enum nvfp4_moe_path {
  *   decode_max_tokens T at or below which AUTO picks the decode path, 0..16
  *   logits_dtype      nvfp4_moe_logits_dtype of router_logits
  *   device            CUDA device ordinal the handle lives on
- *   out_dtype         nvfp4_moe_out_dtype of out (BF16 unless set)             */
+ *   out_dtype         nvfp4_moe_out_dtype of out (BF16 unless set)
+ *   num_shared_experts S, 0 or 1: the layer's single shared expert, used by
+ *                     every token with weight 1 on top of its top_k routed
+ *                     experts and added after them ("GLM-5.3-Flash on
+ *                     Blackwell", The model loaded, served an API, and produced
+ *                     garbage: "the single shared expert"; "GLM-5.3-Flash-NVFP4-h
+ *                     — W4A16 dense-side quantization": shared experts in W4A16
+ *                     NVFP4).  It has the routed experts' H and I, is packed as
+ *                     expert E (after the E routed ones) and needs
+ *                     E + S <= 256 and max_top_k + S <= 16.                     */
 typedef struct nvfp4_moe_config {
   int num_experts;
   int hidden;
@@ -87,13 +96,14 @@ typedef struct nvfp4_moe_config {
   int logits_dtype;
   int device;
   int out_dtype;
+  int num_shared_experts;
 } nvfp4_moe_config;
 
 typedef struct nvfp4_moe* nvfp4_moe_t;
 
-/* Allocate a handle: the packed-weight blob (E * 3*H*I * 9/16 bytes) and the
- * forward workspace (sized for max_tokens * max_top_k routed rows), both on
- * config->device.  Synchronous.  *out is NULL on failure. */
+/* Allocate a handle: the packed-weight blob ((E + S) * 3*H*I * 9/16 bytes) and
+ * the forward workspace (sized for max_tokens * (max_top_k + S) routed rows),
+ * both on config->device.  Synchronous.  *out is NULL on failure. */
 nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* config, nvfp4_moe_t* out);
 
 /* Copy the experts into the handle's device layout: for every 128 weight rows
@@ -102,7 +112,8 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* config, nvfp4_moe_t* o
  * elsewhere by the matching 512 bytes of scales; the gate and up rows are
  * interleaved in groups of 8.  Loads of this layout are 16-byte vectorised
  * and fully coalesced on both the decode and the prefill path.
- * All inputs are DEVICE pointers in the canonical layout, per expert e:
+ * All inputs are DEVICE pointers in the canonical layout, per expert e (E
+ * below counts the shared expert too when the handle has one: it is the last):
  *   w13_q [E][2I][H/2]  uint8  E2M1 codes, gate rows 0..I-1 then up rows
  *                              I..2I-1, row-major over K = H; element 2j in the
  *                              low nibble of byte j, element 2j+1 in the high
@@ -190,9 +201,10 @@ void nvfp4_moe_destroy(nvfp4_moe_t h);
 /* ---- inspection entry points (same ABI; used by the parity tests) ------- */
 
 /* Route and permute exactly as the forward of the chosen path does, into
- * caller DEVICE buffers: ids [T][top_k] int32, weights [T][top_k] float,
- * offsets [E+1] int32, perm [T*top_k] int32 (flattened index t*top_k+j of the
- * routed row at each expert-major position). */
+ * caller DEVICE buffers, with K = top_k + S slots per token (the shared
+ * expert, id E, weight 1, in the last): ids [T][K] int32, weights [T][K]
+ * float, offsets [E+S+1] int32, perm [T*K] int32 (flattened index t*K+j of
+ * the routed row at each expert-major position). */
 nvfp4_moe_status nvfp4_moe_debug_route(nvfp4_moe_t h, const void* router_logits, int T, int top_k,
                                        int32_t* ids, float* weights, int32_t* offsets,
                                        int32_t* perm, cudaStream_t stream);
@@ -223,8 +235,8 @@ nvfp4_moe_status nvfp4_moe_debug_dequant(nvfp4_moe_t h, int expert, int which, f
 
 /* Copy the last forward's intermediates, in expert-major routed-row order
  * (row p = perm position p), into caller DEVICE buffers:
- *   hidden [T*top_k][I] BF16 (h = silu(g)*u, rounded to BF16),
- *   y      [T*top_k][H] float (expert output before the routing weight). */
+ *   hidden [T*K][I] BF16 (h = silu(g)*u, rounded to BF16; K = top_k + S),
+ *   y      [T*K][H] float (expert output before the routing weight). */
 nvfp4_moe_status nvfp4_moe_debug_intermediates(nvfp4_moe_t h, void* hidden, float* y,
                                                cudaStream_t stream);
 

@@ -34,7 +34,8 @@ class Config(ctypes.Structure):
     _fields_ = [("num_experts", ctypes.c_int), ("hidden", ctypes.c_int), ("inter", ctypes.c_int),
                 ("max_tokens", ctypes.c_int), ("max_top_k", ctypes.c_int),
                 ("decode_max_tokens", ctypes.c_int), ("logits_dtype", ctypes.c_int),
-                ("device", ctypes.c_int), ("out_dtype", ctypes.c_int)]
+                ("device", ctypes.c_int), ("out_dtype", ctypes.c_int),
+                ("num_shared_experts", ctypes.c_int)]
 
 
 _lib = None
@@ -106,12 +107,13 @@ class MoELayer:
     """One handle of the library (nvfp4_moe_create ... nvfp4_moe_destroy)."""
 
     def __init__(self, num_experts, hidden, inter, max_tokens, max_top_k, decode_max_tokens=16,
-                 logits_bf16=False, device=0, out_f32=False):
+                 logits_bf16=False, device=0, out_f32=False, num_shared_experts=0):
         self.lib = load_library()
         self.cfg = Config(num_experts, hidden, inter, max_tokens, max_top_k, decode_max_tokens,
-                          1 if logits_bf16 else 0, device, 1 if out_f32 else 0)
+                          1 if logits_bf16 else 0, device, 1 if out_f32 else 0, num_shared_experts)
         self.out_f32 = out_f32
         self.E, self.H, self.I = num_experts, hidden, inter
+        self.S = num_shared_experts  # the shared expert is expert E of the blob
         self.device = device
         h = ctypes.c_void_p()
         st = self.lib.nvfp4_moe_create(ctypes.byref(self.cfg), ctypes.byref(h))
@@ -162,10 +164,11 @@ class MoELayer:
     def nvfp4_moe_debug_route(self, logits, T, top_k, stream=None):
         import torch
         dev = logits.device
-        ids = torch.empty((T, top_k), dtype=torch.int32, device=dev)
-        w = torch.empty((T, top_k), dtype=torch.float32, device=dev)
-        off = torch.empty((self.E + 1,), dtype=torch.int32, device=dev)
-        perm = torch.empty((T * top_k,), dtype=torch.int32, device=dev)
+        K = top_k + self.S  # slots per token; the shared expert's is last
+        ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+        w = torch.empty((T, K), dtype=torch.float32, device=dev)
+        off = torch.empty((self.E + self.S + 1,), dtype=torch.int32, device=dev)
+        perm = torch.empty((T * K,), dtype=torch.int32, device=dev)
         st = self.lib.nvfp4_moe_debug_route(self.h, _ptr(logits), T, top_k, _ptr(ids), _ptr(w), _ptr(off),
                                             _ptr(perm), _stream(stream))
         self._check(st, "nvfp4_moe_debug_route")
@@ -181,7 +184,7 @@ class MoELayer:
 
     def nvfp4_moe_debug_packed_blob(self, stream=None):
         import torch
-        n = self.E * 3 * self.H * self.I * 9 // 16
+        n = (self.E + self.S) * 3 * self.H * self.I * 9 // 16
         out = torch.empty((n,), dtype=torch.uint8, device=f"cuda:{self.device}")
         st = self.lib.nvfp4_moe_debug_packed_blob(self.h, _ptr(out), n, _stream(stream))
         self._check(st, "nvfp4_moe_debug_packed_blob")

@@ -113,7 +113,8 @@ struct Carver {
 
 int choose_path(const nvfp4_moe* h, int T, int k) {
   if (h->path != NVFP4_MOE_PATH_AUTO) return h->path;
-  return (T <= h->cfg.decode_max_tokens && T <= kDecodeMaxTokens && T * k <= kDecodeMaxTokens * 16)
+  return (T <= h->cfg.decode_max_tokens && T <= kDecodeMaxTokens &&
+          T * (k + h->cfg.num_shared_experts) <= kDecodeMaxTokens * 16)
              ? NVFP4_MOE_PATH_DECODE
              : NVFP4_MOE_PATH_PREFILL;
 }
@@ -129,12 +130,15 @@ nvfp4_moe_status check_forward_args(nvfp4_moe* h, const void* logits, int T, int
     return fail(h, NVFP4_MOE_ERR_UNSUPPORTED_SHAPE, "top_k outside 1..min(max_top_k, E)");
   if (path == NVFP4_MOE_PATH_DECODE && (T > kDecodeMaxTokens))
     return fail(h, NVFP4_MOE_ERR_UNSUPPORTED_SHAPE, "decode path takes at most 16 tokens");
+  if (path == NVFP4_MOE_PATH_DECODE && T * (top_k + h->cfg.num_shared_experts) > kDecodeMaxTokens * 16)
+    return fail(h, NVFP4_MOE_ERR_UNSUPPORTED_SHAPE, "decode path takes at most 256 routed rows");
   return NVFP4_MOE_OK;
 }
 
 LayerDims dims_of(const nvfp4_moe* h) {
-  return LayerDims{h->cfg.num_experts, h->cfg.hidden, h->cfg.inter, h->cfg.logits_dtype == NVFP4_MOE_LOGITS_BF16,
-                   h->cfg.out_dtype == NVFP4_MOE_OUT_F32};
+  return LayerDims{h->cfg.num_experts + h->cfg.num_shared_experts, h->cfg.hidden, h->cfg.inter,
+                   h->cfg.logits_dtype == NVFP4_MOE_LOGITS_BF16, h->cfg.out_dtype == NVFP4_MOE_OUT_F32,
+                   h->cfg.num_experts, h->cfg.num_shared_experts};
 }
 
 nvfp4_moe_status run_route(nvfp4_moe* h, const void* logits, const void* x, int T, int k, int path,
@@ -183,6 +187,9 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* c, nvfp4_moe_t* out) {
   if (c->logits_dtype != NVFP4_MOE_LOGITS_F32 && c->logits_dtype != NVFP4_MOE_LOGITS_BF16)
     return NVFP4_MOE_ERR_INVALID_ARG;
   if (c->out_dtype != NVFP4_MOE_OUT_BF16 && c->out_dtype != NVFP4_MOE_OUT_F32) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (c->num_shared_experts < 0 || c->num_shared_experts > 1) return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->num_experts + c->num_shared_experts > 256 || c->max_top_k + c->num_shared_experts > 16)
+    return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || c->device < 0 || c->device >= ndev) return NVFP4_MOE_ERR_INVALID_ARG;
 
@@ -197,10 +204,12 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* c, nvfp4_moe_t* out) {
 
   DeviceGuard g(c->device);
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, c->device);
-  const int E = c->num_experts, H = c->hidden, I = c->inter;
-  const size_t R = (size_t)c->max_tokens * c->max_top_k;
+  // E: experts in the blob (routed + shared); K: routed-row slots per token
+  const int E = c->num_experts + c->num_shared_experts, H = c->hidden, I = c->inter;
+  const int K = c->max_top_k + c->num_shared_experts;
+  const size_t R = (size_t)c->max_tokens * K;
   const size_t Rm = R < 256 ? 256 : R;
-  const size_t maxU = (size_t)std::min(E, kDecodeMaxTokens * c->max_top_k);
+  const size_t maxU = (size_t)std::min(E, kDecodeMaxTokens * K);
   const size_t ncta = ((size_t)c->max_tokens + kRankTokens - 1) / kRankTokens;
   const size_t max_tiles = R / kTileRows + E + 1;
   const size_t blob_bytes = (size_t)E * expert_layout(H, I).stride;
@@ -321,7 +330,7 @@ nvfp4_moe_status nvfp4_moe_pack(nvfp4_moe_t h, const uint8_t* w13_q, const uint8
   if (!aligned(w13_q, 16) || !aligned(w2_q, 16) || !aligned(w13_s, 4) || !aligned(w2_s, 4) || !aligned(gscale, 4))
     return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "pack: misaligned input");
   DeviceGuard g(h->cfg.device);
-  const int E = h->cfg.num_experts;
+  const int E = h->cfg.num_experts + h->cfg.num_shared_experts;
   std::vector<float> gs((size_t)3 * E);
   cudaError_t e = cudaMemcpyAsync(gs.data(), gscale, sizeof(float) * gs.size(), cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
@@ -388,7 +397,7 @@ nvfp4_moe_status nvfp4_moe_forward(nvfp4_moe_t h, const void* logits, int T, int
   }
   if (ev[4]) cudaEventRecord(ev[4], st);
   h->last_T = T;
-  h->last_k = top_k;
+  h->last_k = top_k + h->cfg.num_shared_experts;  // routed-row slots per token
   return NVFP4_MOE_OK;
 }
 
@@ -418,11 +427,12 @@ nvfp4_moe_status nvfp4_moe_debug_route(nvfp4_moe_t h, const void* logits, int T,
   DeviceGuard g(h->cfg.device);
   s = run_route(h, logits, nullptr, T, top_k, path, st);
   if (s != NVFP4_MOE_OK) return s;
-  const size_t n = (size_t)T * top_k;
+  const size_t n = (size_t)T * (top_k + h->cfg.num_shared_experts);
   cudaError_t e = cudaMemcpyAsync(ids, h->ws.ids, n * 4, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(weights, h->ws.wts, n * 4, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess)
-    e = cudaMemcpyAsync(offsets, h->ws.offsets, (h->cfg.num_experts + 1) * 4, cudaMemcpyDeviceToDevice, st);
+    e = cudaMemcpyAsync(offsets, h->ws.offsets, (h->cfg.num_experts + h->cfg.num_shared_experts + 1) * 4,
+                        cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(perm, h->ws.perm, n * 4, cudaMemcpyDeviceToDevice, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "debug_route copy");
   return NVFP4_MOE_OK;
@@ -446,7 +456,8 @@ nvfp4_moe_status nvfp4_moe_debug_trace(nvfp4_moe_t h, uint64_t* host_dst, size_t
 nvfp4_moe_status nvfp4_moe_debug_packed_blob(nvfp4_moe_t h, void* dst, size_t dst_bytes, cudaStream_t st) {
   if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
   if (!h->packed) return fail(h, NVFP4_MOE_ERR_NOT_PACKED, "debug_packed_blob before pack");
-  const size_t n = (size_t)h->cfg.num_experts * expert_layout(h->cfg.hidden, h->cfg.inter).stride;
+  const size_t n = (size_t)(h->cfg.num_experts + h->cfg.num_shared_experts) *
+                   expert_layout(h->cfg.hidden, h->cfg.inter).stride;
   if (!dst || dst_bytes < n) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_packed_blob: destination too small");
   DeviceGuard g(h->cfg.device);
   cudaError_t e = cudaMemcpyAsync(dst, h->blob, n, cudaMemcpyDeviceToDevice, st);
@@ -458,7 +469,7 @@ nvfp4_moe_status nvfp4_moe_debug_dequant(nvfp4_moe_t h, int expert, int which, f
   if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
   if (!h->packed) return fail(h, NVFP4_MOE_ERR_NOT_PACKED, "debug_dequant before pack");
   const int base = which & 3, via_bf16 = (which >> 2) & 1;
-  if (expert < 0 || expert >= h->cfg.num_experts || base > 2 || (which & ~7) || !w_out)
+  if (expert < 0 || expert >= h->cfg.num_experts + h->cfg.num_shared_experts || base > 2 || (which & ~7) || !w_out)
     return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_dequant: bad expert/which/out");
   DeviceGuard g(h->cfg.device);
   cudaError_t e = launch_debug_dequant(h->blob, h->gscale, h->cfg.hidden, h->cfg.inter, expert, base, via_bf16, w_out, st);

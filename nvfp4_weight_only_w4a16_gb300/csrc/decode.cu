@@ -84,7 +84,8 @@ struct FusedArgs {
   size_t expert_stride;
   size_t nib13, sc13, nib2, sc2;
   const float* gscale;
-  int E, H, I, T, k;
+  int E, H, I, T, k;  // E experts (routed + shared), k slots per token (top_k + shared)
+  int Er, topk;       // routed experts (logits per token), routed choices per token
   const void* logits;
   int logits_bf16;
   const __nv_bfloat16* x;
@@ -195,11 +196,13 @@ __device__ __forceinline__ float pow2f(int p) {
 // FP16 rows (xs_pitch bytes apart) after the per-token prescale.
 __device__ void route_block(const FusedArgs& a, RouteSmem& rs, uint8_t* xs, unsigned long long* tr0) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int T = a.T, k = a.k, E = a.E, R = T * k;
+  // k slots per token: top_k routed choices, then the shared expert (id Er)
+  // when the layer has one; E experts in all
+  const int T = a.T, k = a.k, E = a.E, Er = a.Er, topk = a.topk, R = T * k;
   // loads first: token `warp`'s logits, and this warp's share of one x row
   uint32_t key[8];
   float val[8];
-  if (warp < T) warp_load_logits(a.logits, a.logits_bf16, E, warp, key, val);
+  if (warp < T) warp_load_logits(a.logits, a.logits_bf16, Er, warp, key, val);
   const int wpt = dec::kWarps / T;  // warps per token row of x
   const int xt = warp / wpt, xpart = warp - xt * wpt;
   const int per_row = a.H / 8;  // 16-byte pieces per row
@@ -238,12 +241,16 @@ __device__ void route_block(const FusedArgs& a, RouteSmem& rs, uint8_t* xs, unsi
   if (warp < T) {
     int id;
     float logit;
-    const int nt = warp_select_topk(key, val, E, k, &id, &logit);
-    const float w = warp_softmax_k(logit, k);
-    if (lane < k) {
+    const int nt = warp_select_topk(key, val, Er, topk, &id, &logit);
+    const float w = warp_softmax_k(logit, topk);
+    if (lane < topk) {
       rs.ids[warp * k + lane] = id;
       rs.wts[warp * k + lane] = w;
       atomicAdd(&rs.off[id], 1);
+    } else if (lane < k) {  // the shared expert: every token, weight 1
+      rs.ids[warp * k + lane] = Er;
+      rs.wts[warp * k + lane] = 1.0f;
+      atomicAdd(&rs.off[Er], 1);
     }
     if (lane == 0 && nt) atomicAdd(&rs.nan, nt);
   }
@@ -1086,10 +1093,12 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
   a.sc2 = L.w2_sc;
   a.gscale = gscale;
   a.E = d.E;
+  a.Er = d.Er;
   a.H = d.H;
   a.I = d.I;
   a.T = T;
-  a.k = k;
+  a.k = k + d.S;
+  a.topk = k;
   a.logits = logits;
   a.logits_bf16 = d.logits_bf16;
   a.x = reinterpret_cast<const __nv_bfloat16*>(x);

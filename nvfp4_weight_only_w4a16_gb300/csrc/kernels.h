@@ -44,9 +44,11 @@ struct Workspace {
 };
 
 struct LayerDims {
-  int E, H, I;
+  int E, H, I;     // E: experts in the blob (routed + shared)
   int logits_bf16;
   int out_f32;
+  int Er;          // routed experts: router logits per token
+  int S;           // shared experts (0 or 1): slots per token = top_k + S
 };
 
 constexpr int kRankTokens = 256;      // tokens per rank block in the prefill routing

@@ -12,9 +12,11 @@ namespace nvfp4moe {
 // ---------------------------------------------------------------------------
 // Prefill: multi-CTA route, one-CTA scan, multi-CTA scatter + gather.
 // ---------------------------------------------------------------------------
-// K1: one warp per token (8 tokens per CTA): ids, weights, NaN count.
+// K1: one warp per token (8 tokens per CTA): ids, weights, NaN count.  A
+// token has k slots: its topk routed choices over the Er routed experts, then
+// (k > topk) the shared expert, id Er, with weight 1.
 __global__ void __launch_bounds__(256) route_topk_kernel(const void* __restrict__ logits, int bf16, int T, int k,
-                                                         int E, Workspace ws) {
+                                                         int topk, int Er, Workspace ws) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int nan_total = 0;
   {
@@ -22,10 +24,13 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const void* __restrict_
     if (t >= T) return;
     int id;
     float w;
-    nan_total += warp_topk(logits, bf16, E, k, t, &id, &w);
-    if (lane < k) {
+    nan_total += warp_topk(logits, bf16, Er, topk, t, &id, &w);
+    if (lane < topk) {
       ws.ids[(size_t)t * k + lane] = id;
       ws.wts[(size_t)t * k + lane] = w;
+    } else if (lane < k) {
+      ws.ids[(size_t)t * k + lane] = Er;
+      ws.wts[(size_t)t * k + lane] = 1.0f;
     }
   }
   if (lane == 0 && nan_total) atomicAdd(&ws.status->nan_logits, (unsigned)nan_total);
@@ -122,10 +127,11 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16*
   for (int v = lane; v < H / 8; v += 32) dst[v] = __ldg(src + v);
 }
 
-cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const void* x, int T, int k,
+cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const void* x, int T, int top_k,
                                  const Workspace& ws, cudaStream_t st) {
   const int nrb = (T + kRankTokens - 1) / kRankTokens;
-  route_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, d.logits_bf16, T, k, d.E, ws);
+  const int k = top_k + d.S;  // slots per token
+  route_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, d.logits_bf16, T, k, top_k, d.Er, ws);
   route_rank_kernel<<<nrb, 256, 0, st>>>(T, k, d.E, ws);
   route_scan_kernel<<<1, 1024, 0, st>>>(nrb, d.E, ws);
   const size_t rows = (size_t)T * k;
@@ -136,7 +142,8 @@ cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const v
 
 // ---------------------------------------------------------------------------
 // Weighted combine: out[t][d] = sum_{j<k} w[t][j] * y[pos(t,j)][d] in FP32,
-// slot order j = 0..k-1, rounded once to BF16.  One thread per 8 outputs.
+// slot order j = 0..k-1 (a shared expert is the last slot, weight 1),
+// rounded once to BF16.  One thread per 8 outputs.
 // ---------------------------------------------------------------------------
 template <bool kOutF32>
 __global__ void __launch_bounds__(256) combine_kernel(int T, int k, int H, const float* __restrict__ y,
@@ -175,8 +182,9 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int k, int H, const
   reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + (size_t)t * H)[d8] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-cudaError_t launch_combine(const LayerDims& d, int T, int k, const Workspace& ws, void* out, cudaStream_t st) {
+cudaError_t launch_combine(const LayerDims& d, int T, int top_k, const Workspace& ws, void* out, cudaStream_t st) {
   const size_t n = (size_t)T * (d.H / 8);
+  const int k = top_k + d.S;  // slots per token; the shared expert's is last
   if (d.out_f32)
     combine_kernel<true><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(T, k, d.H, ws.y, ws.wts, ws.inv, out);
   else

@@ -35,7 +35,7 @@ def test_status_strings(lib):
 
 def _create(lib, **kw):
     base = dict(num_experts=8, hidden=256, inter=512, max_tokens=16, max_top_k=2,
-                decode_max_tokens=16, logits_dtype=0, device=0, out_dtype=0)
+                decode_max_tokens=16, logits_dtype=0, device=0, out_dtype=0, num_shared_experts=0)
     base.update(kw)
     cfg = Config(**base)
     h = ctypes.c_void_p()
@@ -46,6 +46,8 @@ def _create(lib, **kw):
     dict(num_experts=0), dict(num_experts=257), dict(hidden=100), dict(hidden=192),
     dict(inter=64), dict(max_tokens=0), dict(max_top_k=0), dict(max_top_k=17),
     dict(num_experts=4, max_top_k=5), dict(decode_max_tokens=17),
+    dict(num_shared_experts=2), dict(num_shared_experts=-1),
+    dict(num_experts=256, num_shared_experts=1), dict(num_experts=32, max_top_k=16, num_shared_experts=1),
 ])
 def test_create_rejects_bad_shapes(lib, kw):
     st, h = _create(lib, **kw)
