@@ -63,7 +63,8 @@ def _dist():
 
 
 def _workload_desc(cfg):
-    return (f"{cfg.name}: E{cfg.num_experts} H{cfg.hidden} I{cfg.inter} top{cfg.top_k} T{cfg.tokens}, "
+    shared = " + 1 shared expert" if cfg.shared else ""
+    return (f"{cfg.name}: E{cfg.num_experts} H{cfg.hidden} I{cfg.inter} top{cfg.top_k}{shared} T{cfg.tokens}, "
             f"NVFP4 (E2M1 + E4M3/16 + FP32/tensor) experts, BF16 activations")
 
 
@@ -76,7 +77,7 @@ import sys, time, json, numpy as np
 sys.path.insert(0, sys.argv[1])
 import oracle
 d = np.load(sys.argv[2])
-E, k = int(d["E"]), int(d["k"])
+E, k, S = int(d["E"]), int(d["k"]), int(d["S"])
 class W: pass
 w = W()
 w.w13_q = np.zeros((E,) + d["w13_q"].shape[1:], np.uint8); w.w13_s = np.zeros((E,) + d["w13_s"].shape[1:], np.uint8)
@@ -89,7 +90,7 @@ mode, steps, warm = sys.argv[3], int(sys.argv[4]), int(sys.argv[5])
 times = []
 if mode == "baseline":
     for _ in range(2):
-        t0 = time.perf_counter(); oracle.moe_forward(logits, x, w, k); times.append(time.perf_counter() - t0)
+        t0 = time.perf_counter(); oracle.moe_forward(logits, x, w, k, num_shared=S); times.append(time.perf_counter() - t0)
 else:
     # one step = one routed row: route its token, run that expert's FFN, weight it
     T = logits.shape[0]
@@ -110,7 +111,8 @@ def _oracle_sample_file(inp, ids):
     w = inp.weights
     fd, path = tempfile.mkstemp(suffix=".npz")
     os.close(fd)
-    np.savez(path, E=inp.config.num_experts, k=inp.config.top_k, experts=experts,
+    np.savez(path, E=inp.config.num_experts + inp.config.shared, k=inp.config.top_k, S=inp.config.shared,
+             experts=experts,
              w13_q=w.w13_q[experts], w13_s=w.w13_s[experts], w2_q=w.w2_q[experts], w2_s=w.w2_s[experts],
              gscale=w.gscale[experts], logits=inp.logits, x_bits=inp.x_bits)
     return path
@@ -238,7 +240,8 @@ def run_ours(args):
     inp = make_inputs(args.workload)
     cfg = inp.config
     T, k, H, E = cfg.tokens, cfg.top_k, cfg.hidden, cfg.num_experts
-    layer = pkg.MoELayer(E, H, cfg.inter, T, k, device=dev.index)
+    S = cfg.shared
+    layer = pkg.MoELayer(E, H, cfg.inter, T, k, device=dev.index, num_shared_experts=S)
     n_ours = 1 if T <= 16 else 6     # kernels of ours per forward (decode / prefill path)
     pkg.upload_layer(layer, inp.weights, dev)
 
@@ -341,7 +344,7 @@ def run_ours(args):
     else:
         # prefill: the gate/up GEMM's dense flops on the tensor cores
         kernel = "prefill_gemm_kernel<gate/up>"
-        algo = 2.0 * T * k * (2 * I) * H
+        algo = 2.0 * T * (k + S) * (2 * I) * H
         achieved = algo / (gateup_ms / 1e3) / 1e12
         bound, unit, peak_key = "tensor", "TFLOP/s", "bf16_tflops"
         traffic = None
@@ -351,7 +354,7 @@ def run_ours(args):
         peak_src = "measured"
     except Exception:
         peak, peak_src = (6800.0 if bound == "hbm" else 1900.0), "fallback"
-    layer_flops = 2.0 * T * k * 3 * H * I
+    layer_flops = 2.0 * T * (k + S) * 3 * H * I
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -363,7 +366,7 @@ def run_ours(args):
         finally:
             os.unlink(path)
         cpu = {"value": ns / statistics.mean(times), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{ns} token(s) of the step ({ns * k} expert FFNs + combine), twice, float64 numpy, "
+               "sample": f"{ns} token(s) of the step ({ns * (k + S)} expert FFNs + combine), twice, float64 numpy, "
                          f"1 thread"}
 
     if rank == 0:
