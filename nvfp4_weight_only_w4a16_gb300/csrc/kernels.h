@@ -52,7 +52,7 @@ struct LayerDims {
 };
 
 constexpr int kRankTokens = 256;      // tokens per rank block in the prefill routing
-constexpr int kTileRows = 256;        // max routed rows per prefill m-tile (MMA N)
+constexpr int kTileRows = 128;        // max routed rows per prefill m-tile (MMA N)
 constexpr int kDecodeMaxTokens = 16;
 constexpr int kDecodeWarpsPerSm = 16;  // warps of the decode kernel's one CTA per SM
 // floats of the decode kernel's split-K partial-sum buffer (per phase)

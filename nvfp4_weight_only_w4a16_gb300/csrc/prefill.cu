@@ -6,23 +6,28 @@
 // API, and produced garbage: the working backend dequantises to bf16 and
 // consumes no activation scale).
 //
-// One persistent CTA per SM, 10 warps, warp-specialised:
-//   warp 0      producer: cp.async.bulk of the packed FP4 tile + its scales and
-//               TMA (128B swizzle) of the routed activation rows, into a
-//               4-stage shared-memory ring, completion on mbarriers;
-//   warp 1      MMA issuer (one thread): 4 x tcgen05.mma (K=16) per 64-wide
-//               chunk, accumulator double-buffered in TMEM (2 x 256 columns);
-//               also owns the TMEM allocation;
-//   warps 2-5   dequantisers: E2M1 x E4M3 -> BF16 (exact) written straight
+// One persistent CTA per SM, 15 warps, warp-specialised:
+//   warp 0      weight producer: cp.async.bulk of the packed FP4 chunks (+
+//               scales) of a unit's two 128-row weight blocks into a
+//               10-stage ring, completion on mbarriers;
+//   warp 1      MMA issuer (one thread): per 64-wide K chunk 2 x 4
+//               tcgen05.mma (K=16), one per weight block, both reading the
+//               same activation tile; accumulators double-buffered in TMEM
+//               (2 buffers x 2 blocks x 128 columns); also owns the TMEM
+//               allocation;
+//   warp 2      activation producer: TMA (128B swizzle) boxes of 16 routed rows;
+//   warps 3-10  dequantisers: E2M1 x E4M3 -> BF16 (exact) written straight
 //               into the 128B-swizzled K-major operand layout;
-//   warps 6-9   epilogue: tcgen05.ld of the accumulator, tensor scales, SwiGLU
-//               (gate/up) or the down-projection store.
-// Work unit = (m-tile of <= 256 routed rows of one expert, 128 weight rows).
-// MMA orientation: weights are the 128-row M operand, routed tokens the N
-// operand (16..256), so small per-expert token counts do not waste the
-// 128-row atom.  The gate/up weight rows are interleaved in groups of 8
-// (gate f..f+7, up f..f+7), so each gate accumulator row and its up partner
-// sit 8 TMEM lanes apart, inside one warp.
+//   warps 11-14 epilogue: tcgen05.ld of the accumulators, tensor scales,
+//               SwiGLU (gate/up) or the down-projection store.
+// Work unit = (m-tile of <= 128 routed rows of one expert, two 128-row weight
+// blocks).  MMA orientation: weights are the 128-row M operand, routed tokens
+// the N operand (16..128).  Two weight blocks per activation tile halve the
+// activation bytes each MMA FLOP costs (shared memory and L2), and a
+// tcgen05.commit -- which waits for the tensor pipe to drain the MMAs it
+// covers -- is paid once per 8 MMAs instead of per 4.  The gate/up weight rows
+// are interleaved in groups of 8 (gate f..f+7, up f..f+7), so each gate
+// accumulator row and its up partner sit 8 TMEM lanes apart, inside one warp.
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the handle's status word and winds down instead of hanging.
 #include "common.cuh"
@@ -38,16 +43,20 @@ namespace pf {
 //         so the HBM latency of the weight stream is covered
 constexpr int kAStages = 2;
 constexpr int kBStages = 4;
-constexpr int kRawStages = 12;
-constexpr int kAStageBytes = 16384;      // 128 rows x 128 B
-constexpr int kBStageBytes = 32768;      // up to 256 routed rows x 128 B
-constexpr int kRawStageBytes = 4608;     // 4096 B codes + 512 B scales
+constexpr int kRawStages = 10;
+constexpr int kBlocks = 2;                // 128-row weight blocks per work unit
+constexpr int kABlockBytes = 16384;       // one block's chunk: 128 rows x 128 B (BF16)
+constexpr int kAStageBytes = kBlocks * kABlockBytes;
+constexpr int kBStageBytes = 16384;       // up to 128 routed rows x 128 B
+constexpr int kRawBlockBytes = 4608;      // one block's chunk: 4096 B codes + 512 B scales
+constexpr int kRawStageBytes = kBlocks * kRawBlockBytes;
 constexpr int kAOff = 0;
 constexpr int kBOff = kAOff + kAStages * kAStageBytes;
 constexpr int kRawOff = kBOff + kBStages * kBStageBytes;
 constexpr int kBarOff = kRawOff + kRawStages * kRawStageBytes;
 constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
-constexpr int kThreads = 352;                     // 11 warps
+constexpr int kThreads = 480;                     // 15 warps
+constexpr int kDequantWarps = 8;
 constexpr int kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // a wait longer than 2 s is a fault
 }  // namespace pf
@@ -215,10 +224,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < pf::kRawStages; ++s) {
       mbar_init(raw_full + s, 1);
-      mbar_init(raw_empty + s, 4);
+      mbar_init(raw_empty + s, pf::kDequantWarps);
     }
     for (int s = 0; s < pf::kAStages; ++s) {
-      mbar_init(a_full + s, 4);
+      mbar_init(a_full + s, pf::kDequantWarps);
       mbar_init(a_empty + s, 1);
     }
     for (int s = 0; s < pf::kBStages; ++s) {
@@ -243,27 +252,33 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // work unit = (tile, pair of 128-row weight blocks 2p and 2p+1; the second
+  // may not exist when the block count is odd)
   const int num_tiles = *a.num_tiles;
-  const int total_units = num_tiles * a.NB;
+  const int NP = (a.NB + 1) / 2;
+  const int total_units = num_tiles * NP;
   const int nch = a.K / kChunk;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- weight producer: packed codes + scales ----------------
+      // ---------------- weight producer: packed codes + scales of both blocks ----------------
       uint32_t it = 0;
       for (int unit = blockIdx.x; unit < total_units && !*abort_flag && a.fault != 1; unit += gridDim.x) {
-        const int tile = unit / a.NB, nb = unit % a.NB;
+        const int tile = unit / NP, nb0 = 2 * (unit % NP);
+        const int nblk = nb0 + 1 < a.NB ? 2 : 1;
         const int e = a.tile_expert[tile];
-        const uint8_t* src_nib = a.blob + (size_t)e * a.expert_stride + a.nib_off + (size_t)nb * nch * 4096;
-        const uint8_t* src_sc = a.blob + (size_t)e * a.expert_stride + a.sc_off + (size_t)nb * nch * 512;
+        const uint8_t* src_nib = a.blob + (size_t)e * a.expert_stride + a.nib_off + (size_t)nb0 * nch * 4096;
+        const uint8_t* src_sc = a.blob + (size_t)e * a.expert_stride + a.sc_off + (size_t)nb0 * nch * 512;
         for (int c = 0; c < nch; ++c, ++it) {
           const int s = it % pf::kRawStages;
           const uint32_t ph = (it / pf::kRawStages) & 1u;
           if (!mbar_wait(raw_empty + s, ph ^ 1u, abort_flag, a.st, 1)) break;
           uint8_t* st = smem + pf::kRawOff + s * pf::kRawStageBytes;
-          mbar_arrive_expect_tx(raw_full + s, 4096u + 512u);
-          bulk_g2s(st, src_nib + (size_t)c * 4096, 4096, raw_full + s);
-          bulk_g2s(st + 4096, src_sc + (size_t)c * 512, 512, raw_full + s);
+          mbar_arrive_expect_tx(raw_full + s, (uint32_t)nblk * (4096u + 512u));
+          for (int j = 0; j < nblk; ++j) {  // block nb0 + j's chunk c: 4096 B codes, 512 B scales
+            bulk_g2s(st + j * pf::kRawBlockBytes, src_nib + ((size_t)j * nch + c) * 4096, 4096, raw_full + s);
+            bulk_g2s(st + j * pf::kRawBlockBytes + 4096, src_sc + ((size_t)j * nch + c) * 512, 512, raw_full + s);
+          }
         }
       }
     }
@@ -272,14 +287,15 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       // ---------------- MMA issuer ----------------
       uint32_t ia = 0, ib = 0, j = 0;
       for (int unit = blockIdx.x; unit < total_units && !*abort_flag; unit += gridDim.x, ++j) {
-        const int tile = unit / a.NB;
+        const int tile = unit / NP, nb0 = 2 * (unit % NP);
+        const int nblk = nb0 + 1 < a.NB ? 2 : 1;
         const int rows = a.tile_rows[tile];
         const int N = (rows + 15) & ~15;
         const uint32_t idesc = idesc_bf16(128, N);
         const uint32_t buf = j & 1u, aph = (j >> 1) & 1u;
         if (!mbar_wait(accempty + buf, aph ^ 1u, abort_flag, a.st, 2)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * 256u;
+        const uint32_t d_tmem = tmem_base + buf * 256u;  // block b's accumulator at + 128 b
         bool ok = true;
         for (int c = 0; c < nch; ++c, ++ia, ++ib) {
           const int sa = ia % pf::kAStages, sb = ib % pf::kBStages;
@@ -292,8 +308,12 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           const uint64_t ad = sw128_desc(smem_u32(smem + pf::kAOff + sa * pf::kAStageBytes));
           const uint64_t bd = sw128_desc(smem_u32(smem + pf::kBOff + sb * pf::kBStageBytes));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, (c | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc = (c | kk) != 0 ? 1u : 0u;
+            umma_bf16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, acc);
+            if (nblk > 1)  // block 1's operand tile is 16 KB further (1024 in the 16-byte units)
+              umma_bf16(d_tmem + 128u, ad + (uint64_t)(pf::kABlockBytes >> 4) + 2u * kk, bd + 2u * kk, idesc, acc);
+          }
           umma_commit(a_empty + sa);
           umma_commit(b_empty + sb);
         }
@@ -305,7 +325,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     // ---------------- activation producer: TMA boxes of 16 routed rows ----------------
     uint32_t it = 0;
     for (int unit = blockIdx.x; unit < total_units && !*abort_flag && a.fault != 1; unit += gridDim.x) {
-      const int tile = unit / a.NB;
+      const int tile = unit / NP;
       const int row0 = a.tile_row0[tile], rows = a.tile_rows[tile];
       const int nbox = (rows + 15) >> 4;
       bool ok = true;
@@ -328,11 +348,12 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       }
       if (!ok) break;
     }
-  } else if (warp < 7) {
-    // ---------------- dequantisers (128 threads) ----------------
+  } else if (warp < 3 + pf::kDequantWarps) {
+    // ---------------- dequantisers (256 threads; per chunk, one 16-byte segment of each block) ----------------
     const int tau = threadIdx.x - 96;
     uint32_t ir = 0, ia = 0;
     for (int unit = blockIdx.x; unit < total_units && !*abort_flag; unit += gridDim.x) {
+      const int nblk = 2 * (unit % NP) + 1 < a.NB ? 2 : 1;
       bool ok = true;
       for (int c = 0; c < nch; ++c, ++ir, ++ia) {
         const int sr = ir % pf::kRawStages, sa = ia % pf::kAStages;
@@ -344,7 +365,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const uint8_t* raw_stage = smem + pf::kRawOff + sr * pf::kRawStageBytes;
         const uint32_t a_base = smem_u32(smem + pf::kAOff + sa * pf::kAStageBytes);
         dequant_segment(raw_stage, a_base, tau);
-        dequant_segment(raw_stage, a_base, tau + 128);
+        if (nblk > 1) dequant_segment(raw_stage + pf::kRawBlockBytes, a_base + pf::kABlockBytes, tau);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
@@ -355,42 +376,46 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       if (!ok) break;
     }
   } else {
-    // ---------------- epilogue (128 threads) ----------------
+    // ---------------- epilogue (128 threads; warp w reads TMEM lanes 32 (w % 4) ..) ----------------
     const int quarter = warp & 3;
     const int i = 32 * quarter + lane;  // accumulator row (TMEM lane)
     uint32_t j = 0;
     for (int unit = blockIdx.x; unit < total_units && !*abort_flag; unit += gridDim.x, ++j) {
-      const int tile = unit / a.NB, nb = unit % a.NB;
+      const int tile = unit / NP, nb0 = 2 * (unit % NP);
+      const int nblk = nb0 + 1 < a.NB ? 2 : 1;
       const int e = a.tile_expert[tile], row0 = a.tile_row0[tile], rows = a.tile_rows[tile];
       const int N = (rows + 15) & ~15;
       const uint32_t buf = j & 1u, aph = (j >> 1) & 1u;
       if (!mbar_wait(accfull + buf, aph, abort_flag, a.st, 6)) break;
       tc_fence_after();
       const float* gs = a.gscale + 3 * e;
-      const uint32_t tbase = tmem_base + ((uint32_t)(32 * quarter) << 16) + buf * 256u;
-      for (int col = 0; col < N; col += 16) {
-        uint32_t v[16];
-        tmem_ld16(tbase + (uint32_t)col, v);
-        if (kGateUp) {
-          const int R = 128 * nb + i;
-          const int f = 8 * (R >> 4) + (R & 7);
-          const bool is_gate = (R & 15) < 8;
-          const float gsg = gs[0], gsu = gs[1];
+      for (int blk = 0; blk < nblk; ++blk) {
+        const int nb = nb0 + blk;
+        const uint32_t tbase = tmem_base + ((uint32_t)(32 * quarter) << 16) + buf * 256u + (uint32_t)(128 * blk);
+        for (int col = 0; col < N; col += 16) {
+          uint32_t v[16];
+          tmem_ld16(tbase + (uint32_t)col, v);
+          if (kGateUp) {
+            const int R = 128 * nb + i;
+            const int f = 8 * (R >> 4) + (R & 7);
+            const bool is_gate = (R & 15) < 8;
+            const float gsg = gs[0], gsu = gs[1];
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const float mine = __uint_as_float(v[jj]);
-            const float partner = __shfl_xor_sync(0xffffffffu, mine, 8);
-            if (is_gate && col + jj < rows) {
-              const float g = gsg * mine, u = gsu * partner;
-              a.h[(size_t)(row0 + col + jj) * a.I + f] = __float2bfloat16_rn(silu(g) * u);
+            for (int jj = 0; jj < 16; ++jj) {
+              const float mine = __uint_as_float(v[jj]);
+              const float partner = __shfl_xor_sync(0xffffffffu, mine, 8);
+              if (is_gate && col + jj < rows) {
+                const float g = gsg * mine, u = gsu * partner;
+                a.h[(size_t)(row0 + col + jj) * a.I + f] = __float2bfloat16_rn(silu(g) * u);
+              }
             }
-          }
-        } else {
-          const int d = 128 * nb + i;
-          const float gsd = gs[2];
+          } else {
+            const int d = 128 * nb + i;
+            const float gsd = gs[2];
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            if (col + jj < rows) a.y[(size_t)(row0 + col + jj) * a.H + d] = gsd * __uint_as_float(v[jj]);
+            for (int jj = 0; jj < 16; ++jj)
+              if (col + jj < rows) a.y[(size_t)(row0 + col + jj) * a.H + d] = gsd * __uint_as_float(v[jj]);
+          }
         }
       }
       tc_fence_before();
