@@ -246,3 +246,17 @@ def moe_forward(logits, x_bits, weights, k: int, tokens=None, return_parts=False
     if return_parts:
         return out, r, y
     return out
+
+
+def linear_forward(x_bits, w_q, w_s, gscale: float) -> np.ndarray:
+    """A W4A16 NVFP4 dense linear: out[t] = gs * W x[t] in float64.
+
+    W [N][K] in the canonical NVFP4 layout (codes [N][K/2], E4M3 scales
+    [N][K/16]) with one FP32 tensor scale gs, x [T][K] BF16 bit patterns.  The
+    same weight-only format the routed experts use also covers the dense
+    projections ("GLM-5.3-Flash-NVFP4-h — W4A16 dense-side quantization": the
+    attention linears, shared experts and lm_head quantised to W4A16 NVFP4
+    with 16-element groups, activations left in BF16).
+    """
+    x = bf16_bits_to_f64(np.asarray(x_bits))
+    return float(gscale) * (x @ dequant(w_q, w_s).T)

@@ -311,9 +311,35 @@ def pin_shared_expert(o):
             assert abs(out[t, d] - (base[t, d] + yd)) <= 1e-12 * max(1.0, abs(yd))
 
 
+def pin_linear(o):
+    # closed form: codes 0x1 (0.5) and 0x9 (-0.5) alternating by row, scale
+    # 0x38 (1.0), gs = 0.25, x = 1 -> out[n] = +-0.25 * 0.5 * K
+    N, K = 32, 64
+    q = np.where((np.arange(N) % 2 == 0)[:, None], 0x11, 0x99).astype(np.uint8) * np.ones((1, K // 2), np.uint8)
+    s = np.full((N, K // 16), 0x38, np.uint8)
+    out = o.linear_forward(_bf16_bits(np.ones((3, K))), q, s, 0.25)
+    want = np.where(np.arange(N) % 2 == 0, 1.0, -1.0) * 0.25 * 0.5 * K
+    assert np.all(out == want[None, :]), out[0, :4]
+    # brute force: scalar loops on a small random matrix
+    rng = np.random.default_rng(23)
+    N, K, T = 16, 48, 3
+    q = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    s = rng.integers(0x20, 0x48, (N, K // 16), dtype=np.uint8)
+    xb = _bf16_bits(rng.standard_normal((T, K)))
+    out = o.linear_forward(xb, q, s, 0.75)
+    tab = _e2m1_table()
+    sc = lambda b: float(_torch_e4m3(np.array([b], np.uint8))[0])
+    for t in range(T):
+        xs = [float(v) for v in (xb[t].astype(np.uint32) << 16).view(np.float32)]
+        for n in range(N):
+            acc = sum(tab[(int(q[n, kk // 2]) >> (4 * (kk % 2))) & 15] * sc(s[n, kk // 16]) * xs[kk]
+                      for kk in range(K))
+            assert abs(out[t, n] - 0.75 * acc) <= 1e-12 * max(1.0, abs(acc))
+
+
 PINS = [pin_e2m1_table, pin_e4m3, pin_dequant_worked, pin_round_trip, pin_route,
         pin_permute, pin_ffn_closed_form, pin_identical_experts, pin_top1_dense,
-        pin_brute_force_layer, pin_shared_expert]
+        pin_brute_force_layer, pin_shared_expert, pin_linear]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -441,7 +467,20 @@ def _mut_shared_routed_weight(m):  # the shared expert scaled by the first routi
     m.moe_forward = f
 
 
-MUTANTS = [_mut_nibble_order, _mut_e4m3_bias, _mut_e2m1_subnormal, _mut_scale_group_shift,
+def _mut_linear_transposed(m):  # W^T x instead of W x (square shapes would hide it)
+    def f(x_bits, w_q, w_s, gscale):
+        x = m.bf16_bits_to_f64(np.asarray(x_bits))
+        W = m.dequant(w_q, w_s)
+        return float(gscale) * (x[:, :W.shape[0]] @ W[:, :x.shape[1]][:, :W.shape[0]])
+    m.linear_forward = f
+
+
+def _mut_linear_no_gscale(m):
+    orig = m.linear_forward
+    m.linear_forward = lambda x_bits, w_q, w_s, gscale: orig(x_bits, w_q, w_s, 1.0)
+
+
+MUTANTS = [_mut_linear_transposed, _mut_linear_no_gscale, _mut_nibble_order, _mut_e4m3_bias, _mut_e2m1_subnormal, _mut_scale_group_shift,
            _mut_gate_up_swap, _mut_drop_up_scale, _mut_tie_break, _mut_softmax_all,
            _mut_no_combine_weights, _mut_silu_sign, _mut_perm_unstable, _mut_shared_dropped,
            _mut_shared_routed_weight]
