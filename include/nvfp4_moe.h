@@ -246,6 +246,63 @@ nvfp4_moe_status nvfp4_moe_debug_intermediates(nvfp4_moe_t h, void* hidden, floa
  * the GPU context stays usable.  fault = 0 restores normal operation. */
 nvfp4_moe_status nvfp4_moe_debug_set_fault(nvfp4_moe_t h, int fault);
 
+/* ---------------------------------------------------------------------------
+ * Dense W4A16 NVFP4 linear: out[t] = gs * W x[t] for one weight matrix W
+ * [N][K] in the same weight-only format as the experts (E2M1 codes, one E4M3
+ * scale per 16 elements of a row, one FP32 tensor scale gs; activations
+ * BF16, no activation scale).  The dense side of the model -- the attention
+ * projections, the shared experts and lm_head -- is quantised this way
+ * ("GLM-5.3-Flash-NVFP4-h — W4A16 dense-side quantization", opening summary
+ * and Config expectations: W4A16_NVFP4 modules with group_size = 16).  It
+ * runs on the same two paths as the MoE layer, as a one-matrix case: T <= 16
+ * on the decode GEMV kernel, larger T on the tcgen05 GEMM kernel, both
+ * writing out directly (no routing, no combine).
+ *
+ * A linear handle is an nvfp4_moe_t: nvfp4_moe_destroy, nvfp4_moe_set_path,
+ * nvfp4_moe_get_status, nvfp4_moe_set_profiling / get_stage_times,
+ * nvfp4_moe_debug_packed_blob and nvfp4_moe_debug_set_fault apply to it;
+ * nvfp4_moe_pack, nvfp4_moe_forward, nvfp4_moe_debug_route and
+ * nvfp4_moe_debug_intermediates return NVFP4_MOE_ERR_INVALID_ARG and
+ * nvfp4_moe_debug_dequant NVFP4_MOE_ERR_NOT_IMPLEMENTED on it; the linear
+ * calls below return NVFP4_MOE_ERR_INVALID_ARG on an MoE handle.
+ * ------------------------------------------------------------------------- */
+typedef struct nvfp4_linear_config {
+  int out_features;      /* N: 16..16384, a multiple of 16 */
+  int in_features;       /* K: 128..16384, a multiple of 128 */
+  int max_tokens;        /* largest T of any forward, 1..2^20 */
+  int decode_max_tokens; /* 0..16: T <= this takes the decode (GEMV) path */
+  int out_dtype;         /* nvfp4_moe_out_dtype */
+  int device;            /* CUDA device ordinal */
+} nvfp4_linear_config;
+
+/* Allocate a linear handle: the packed matrix (Np*K*9/16 bytes, Np = N
+ * rounded up to a multiple of 128; the padding rows hold zeros and are never
+ * written out) and a small workspace (tables for max_tokens rows; no
+ * activation copies), on config->device.  Synchronous.  *out is NULL on
+ * failure. */
+nvfp4_moe_status nvfp4_linear_create(const nvfp4_linear_config* config, nvfp4_moe_t* out);
+
+/* Copy W into the handle's device layout (the per-128-row, per-64-K-chunk
+ * layout nvfp4_moe_pack writes for one down matrix).  DEVICE inputs:
+ *   w_q [N][K/2]  uint8  E2M1 codes, row-major; element 2j in the low nibble
+ *                        of byte j, element 2j+1 in the high (16-byte aligned)
+ *   w_s [N][K/16] uint8  E4M3 scale of elements 16g..16g+15 of the row
+ *   gscale [1]    float  the tensor scale: finite and > 0, else
+ *                        NVFP4_MOE_ERR_BAD_SCALE and the handle stays unpacked
+ * Synchronous (reads gscale back to the host).  Inputs may be freed once the
+ * call returns. */
+nvfp4_moe_status nvfp4_linear_pack(nvfp4_moe_t h, const uint8_t* w_q, const uint8_t* w_s, const float* gscale,
+                                   cudaStream_t stream);
+
+/* out [T][N] = gs * x [T][K] W^T, accumulated in FP32 and rounded once to
+ * BF16 (or stored as FP32, config.out_dtype); x BF16 and out DEVICE, both
+ * 16-byte aligned, 1 <= T <= max_tokens.  Enqueued on `stream`, no host
+ * synchronisation and no allocation; the prefill path encodes a TMA
+ * descriptor for x on the host each call, so a captured graph replays with
+ * the x pointer it was captured with.  Concurrent forwards on one handle
+ * race on its workspace: serialise them on one stream. */
+nvfp4_moe_status nvfp4_linear_forward(nvfp4_moe_t h, int T, const void* x, void* out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

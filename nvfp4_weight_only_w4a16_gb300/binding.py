@@ -38,6 +38,11 @@ class Config(ctypes.Structure):
                 ("num_shared_experts", ctypes.c_int)]
 
 
+class LinearConfig(ctypes.Structure):
+    _fields_ = [("out_features", ctypes.c_int), ("in_features", ctypes.c_int), ("max_tokens", ctypes.c_int),
+                ("decode_max_tokens", ctypes.c_int), ("out_dtype", ctypes.c_int), ("device", ctypes.c_int)]
+
+
 _lib = None
 
 
@@ -45,7 +50,7 @@ def header_functions():
     """Names of the functions include/nvfp4_moe.h declares."""
     with open(HEADER) as f:
         text = f.read()
-    return sorted(set(re.findall(r"\b(nvfp4_moe_[a-z_0-9]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(nvfp4_(?:moe|linear)_[a-z_0-9]+)\s*\(", text)))
 
 
 def load_library(path: str | None = None):
@@ -77,6 +82,9 @@ def load_library(path: str | None = None):
         "nvfp4_moe_debug_trace": (i, [vp, ctypes.POINTER(ctypes.c_uint64), ctypes.c_size_t,
                                       ctypes.POINTER(ctypes.c_size_t)]),
         "nvfp4_moe_get_stage_times": (i, [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
+        "nvfp4_linear_create": (i, [ctypes.POINTER(LinearConfig), ctypes.POINTER(vp)]),
+        "nvfp4_linear_pack": (i, [vp, vp, vp, vp, vp]),
+        "nvfp4_linear_forward": (i, [vp, i, vp, vp, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -218,6 +226,44 @@ class MoELayer:
 
     def nvfp4_moe_debug_set_fault(self, fault):
         self._check(self.lib.nvfp4_moe_debug_set_fault(self.h, fault), "nvfp4_moe_debug_set_fault")
+
+
+class Linear(MoELayer):
+    """A dense W4A16 NVFP4 linear handle (nvfp4_linear_create ... nvfp4_moe_destroy)."""
+
+    def __init__(self, out_features, in_features, max_tokens, decode_max_tokens=16, device=0, out_f32=False):
+        self.lib = load_library()
+        self.cfg = LinearConfig(out_features, in_features, max_tokens, decode_max_tokens, 1 if out_f32 else 0, device)
+        self.out_f32 = out_f32
+        self.N, self.K = out_features, in_features
+        self.device = device
+        h = ctypes.c_void_p()
+        st = self.lib.nvfp4_linear_create(ctypes.byref(self.cfg), ctypes.byref(h))
+        if st != 0:
+            raise Nvfp4MoeError(st, "nvfp4_linear_create: " + self.lib.nvfp4_moe_status_string(st).decode())
+        self.h = h
+
+    def nvfp4_linear_pack(self, w_q, w_s, gscale, stream=None):
+        st = self.lib.nvfp4_linear_pack(self.h, _ptr(w_q), _ptr(w_s), _ptr(gscale), _stream(stream))
+        self._check(st, "nvfp4_linear_pack")
+
+    def nvfp4_linear_forward(self, x, out, stream=None):
+        st = self.lib.nvfp4_linear_forward(self.h, x.shape[0], _ptr(x), _ptr(out), _stream(stream))
+        self._check(st, "nvfp4_linear_forward")
+        return out
+
+    def nvfp4_linear_forward_raw(self, T, x_ptr, out_ptr, stream_handle):
+        """Pointer-level call (for benchmarks that time the bare ABI)."""
+        return self.lib.nvfp4_linear_forward(self.h, T, ctypes.c_void_p(x_ptr), ctypes.c_void_p(out_ptr),
+                                             ctypes.c_void_p(stream_handle))
+
+    def nvfp4_moe_debug_packed_blob(self, stream=None):
+        import torch
+        n = (self.N + 127) // 128 * 128 * self.K * 9 // 16  # rows padded to whole 128-row blocks
+        out = torch.empty((n,), dtype=torch.uint8, device=f"cuda:{self.device}")
+        st = self.lib.nvfp4_moe_debug_packed_blob(self.h, _ptr(out), n, _stream(stream))
+        self._check(st, "nvfp4_moe_debug_packed_blob")
+        return out
 
 
 def nvfp4_moe_forward_decode_static(packed_experts, gscale, num_experts, hidden, inter, logits, top_k, x, out,

@@ -16,6 +16,8 @@ using namespace nvfp4moe;
 
 struct nvfp4_moe {
   nvfp4_moe_config cfg;
+  bool linear = false;  // a dense linear (nvfp4_linear_create): cfg holds E = 1, hidden = N padded to 128, inter = K
+  int lin_n = 0;        // a dense linear's N (output features)
   int path = NVFP4_MOE_PATH_AUTO;
   int num_sms = 0;
   bool packed = false;
@@ -121,6 +123,7 @@ int choose_path(const nvfp4_moe* h, int T, int k) {
 
 nvfp4_moe_status check_forward_args(nvfp4_moe* h, const void* logits, int T, int top_k, int path) {
   if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (h->linear) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "a dense-linear handle: call nvfp4_linear_forward");
   if (!h->packed) return fail(h, NVFP4_MOE_ERR_NOT_PACKED, "forward before a successful pack");
   if (!logits) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "router_logits is NULL");
   if (!aligned(logits, h->cfg.logits_dtype == NVFP4_MOE_LOGITS_BF16 ? 2 : 4))
@@ -138,7 +141,30 @@ nvfp4_moe_status check_forward_args(nvfp4_moe* h, const void* logits, int T, int
 LayerDims dims_of(const nvfp4_moe* h) {
   return LayerDims{h->cfg.num_experts + h->cfg.num_shared_experts, h->cfg.hidden, h->cfg.inter,
                    h->cfg.logits_dtype == NVFP4_MOE_LOGITS_BF16, h->cfg.out_dtype == NVFP4_MOE_OUT_F32,
-                   h->cfg.num_experts, h->cfg.num_shared_experts};
+                   h->cfg.num_experts, h->cfg.num_shared_experts, h->linear ? 1 : 0, h->lin_n};
+}
+
+size_t blob_bytes_of(const nvfp4_moe_config& c, bool linear) {
+  return linear ? linear_layout(c.hidden, c.inter).stride
+                : (size_t)(c.num_experts + c.num_shared_experts) * expert_layout(c.hidden, c.inter).stride;
+}
+
+// Handle allocation shared by the MoE layer and the dense linear (c already
+// validated; a linear's c holds one expert with hidden = N and inter = K).
+nvfp4_moe_status create_handle(const nvfp4_moe_config* c, bool linear, int lin_n, nvfp4_moe_t* out);
+
+// Forward events: 5 per profiled forward (ev[i] stays NULL when profiling is off).
+nvfp4_moe_status take_events(nvfp4_moe* h, cudaEvent_t (&ev)[5]) {
+  if (!h->profiling) return NVFP4_MOE_OK;
+  for (int i = 0; i < 5; ++i) {
+    if (h->ev_used == h->ev_pool.size()) {
+      cudaEvent_t e0;
+      if (cudaEventCreate(&e0) != cudaSuccess) return cuda_fail(h, cudaGetLastError(), "event create");
+      h->ev_pool.push_back(e0);
+    }
+    ev[i] = h->ev_pool[h->ev_used++];
+  }
+  return NVFP4_MOE_OK;
 }
 
 nvfp4_moe_status run_route(nvfp4_moe* h, const void* logits, const void* x, int T, int k, int path,
@@ -192,10 +218,18 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* c, nvfp4_moe_t* out) {
     return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || c->device < 0 || c->device >= ndev) return NVFP4_MOE_ERR_INVALID_ARG;
+  return create_handle(c, false, 0, out);
+}
 
+}  // extern "C"
+
+namespace {
+nvfp4_moe_status create_handle(const nvfp4_moe_config* c, bool linear, int lin_n, nvfp4_moe_t* out) {
   nvfp4_moe* h = new (std::nothrow) nvfp4_moe();
   if (!h) return NVFP4_MOE_ERR_WORKSPACE;
   h->cfg = *c;
+  h->linear = linear;
+  h->lin_n = lin_n;
   const char* lg = getenv("NVFP4_MOE_LOG");
   h->log = lg && lg[0] == '1';
   const char* fp = getenv("NVFP4_MOE_FORCE_PATH");
@@ -212,7 +246,10 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* c, nvfp4_moe_t* out) {
   const size_t maxU = (size_t)std::min(E, kDecodeMaxTokens * K);
   const size_t ncta = ((size_t)c->max_tokens + kRankTokens - 1) / kRankTokens;
   const size_t max_tiles = R / kTileRows + E + 1;
-  const size_t blob_bytes = (size_t)E * expert_layout(H, I).stride;
+  const size_t blob_bytes = blob_bytes_of(*c, linear);
+  // a dense linear reads x and writes out directly: no permuted copies, no
+  // hidden rows, no FP32 expert outputs
+  const size_t RmH = linear ? 1 : Rm * H, RmI = linear ? 1 : Rm * I;
 
   Carver cv;
   Workspace& w = h->ws;
@@ -227,9 +264,9 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* c, nvfp4_moe_t* out) {
   cv.add(&w.num_touched, 1);
   cv.add(&w.x16, (size_t)kDecodeMaxTokens * H);
   cv.add(&w.xexp, kDecodeMaxTokens);
-  cv.add(&w.h, Rm * I);
+  cv.add(&w.h, RmI);
   cv.add(&w.hmax, Rm);
-  cv.add(&w.y, Rm * H);
+  cv.add(&w.y, RmH);
   cv.add(&w.part_gu, decode_part_floats(h->num_sms, kDecodeMaxTokens));
   cv.add(&w.cnt_gu, maxU * (2 * I / 16));
   cv.add(&w.part_dn, decode_part_floats(h->num_sms, kDecodeMaxTokens));
@@ -240,7 +277,7 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* c, nvfp4_moe_t* out) {
   cv.add(&w.blk_counts, ncta * E);
   cv.add(&w.blk_base, ncta * E);
   cv.add(&w.local_rank, Rm);
-  cv.add(&w.x_perm, Rm * H);
+  cv.add(&w.x_perm, RmH);
   cv.add(&w.tile_expert, max_tiles);
   cv.add(&w.tile_row0, max_tiles);
   cv.add(&w.tile_rows, max_tiles);
@@ -262,13 +299,16 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* c, nvfp4_moe_t* out) {
     nvfp4_moe_destroy(h);
     return NVFP4_MOE_ERR_CUDA;
   }
-  if (!encode_rows_map(&h->maps.x_perm, w.x_perm, Rm, H) || !encode_rows_map(&h->maps.h, w.h, Rm, I)) {
+  if (!linear && (!encode_rows_map(&h->maps.x_perm, w.x_perm, Rm, H) || !encode_rows_map(&h->maps.h, w.h, Rm, I))) {
     nvfp4_moe_destroy(h);
     return NVFP4_MOE_ERR_CUDA;
   }
   *out = h;
   return NVFP4_MOE_OK;
 }
+}  // namespace
+
+extern "C" {
 
 void nvfp4_moe_destroy(nvfp4_moe_t h) {
   if (!h) return;
@@ -326,6 +366,7 @@ nvfp4_moe_status nvfp4_moe_debug_set_fault(nvfp4_moe_t h, int fault) {
 nvfp4_moe_status nvfp4_moe_pack(nvfp4_moe_t h, const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
                                 const uint8_t* w2_s, const float* gscale, cudaStream_t st) {
   if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (h->linear) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "a dense-linear handle: call nvfp4_linear_pack");
   if (!w13_q || !w13_s || !w2_q || !w2_s || !gscale) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "pack: NULL input");
   if (!aligned(w13_q, 16) || !aligned(w2_q, 16) || !aligned(w13_s, 4) || !aligned(w2_s, 4) || !aligned(gscale, 4))
     return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "pack: misaligned input");
@@ -365,17 +406,9 @@ nvfp4_moe_status nvfp4_moe_forward(nvfp4_moe_t h, const void* logits, int T, int
             path == NVFP4_MOE_PATH_DECODE ? "decode (grouped GEMV)" : "prefill (tcgen05 grouped GEMM)");
   }
   cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
-  if (h->profiling) {
-    for (int i = 0; i < 5; ++i) {
-      if (h->ev_used == h->ev_pool.size()) {
-        cudaEvent_t e0;
-        if (cudaEventCreate(&e0) != cudaSuccess) return cuda_fail(h, cudaGetLastError(), "event create");
-        h->ev_pool.push_back(e0);
-      }
-      ev[i] = h->ev_pool[h->ev_used++];
-    }
-    cudaEventRecord(ev[0], st);
-  }
+  s = take_events(h, ev);
+  if (s != NVFP4_MOE_OK) return s;
+  if (ev[0]) cudaEventRecord(ev[0], st);
   const LayerDims d = dims_of(h);
   cudaError_t e;
   if (path == NVFP4_MOE_PATH_DECODE) {
@@ -389,7 +422,8 @@ nvfp4_moe_status nvfp4_moe_forward(nvfp4_moe_t h, const void* logits, int T, int
     s = run_route(h, logits, x, T, top_k, path, st);
     if (s != NVFP4_MOE_OK) return s;
     if (ev[1]) cudaEventRecord(ev[1], st);
-    e = launch_prefill_ffn(d, h->blob, h->gscale, T, top_k, h->num_sms, h->maps, h->ws, h->fault, ev[2], st);
+    e = launch_prefill_ffn(d, h->blob, h->gscale, T, top_k, h->num_sms, h->maps, h->ws, h->fault, ev[2],
+                           nullptr, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "expert FFN launch");
     if (ev[3]) cudaEventRecord(ev[3], st);
     e = launch_combine(d, T, top_k, h->ws, out, st);
@@ -456,8 +490,7 @@ nvfp4_moe_status nvfp4_moe_debug_trace(nvfp4_moe_t h, uint64_t* host_dst, size_t
 nvfp4_moe_status nvfp4_moe_debug_packed_blob(nvfp4_moe_t h, void* dst, size_t dst_bytes, cudaStream_t st) {
   if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
   if (!h->packed) return fail(h, NVFP4_MOE_ERR_NOT_PACKED, "debug_packed_blob before pack");
-  const size_t n = (size_t)(h->cfg.num_experts + h->cfg.num_shared_experts) *
-                   expert_layout(h->cfg.hidden, h->cfg.inter).stride;
+  const size_t n = blob_bytes_of(h->cfg, h->linear);
   if (!dst || dst_bytes < n) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_packed_blob: destination too small");
   DeviceGuard g(h->cfg.device);
   cudaError_t e = cudaMemcpyAsync(dst, h->blob, n, cudaMemcpyDeviceToDevice, st);
@@ -467,6 +500,7 @@ nvfp4_moe_status nvfp4_moe_debug_packed_blob(nvfp4_moe_t h, void* dst, size_t ds
 
 nvfp4_moe_status nvfp4_moe_debug_dequant(nvfp4_moe_t h, int expert, int which, float* w_out, cudaStream_t st) {
   if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (h->linear) return fail(h, NVFP4_MOE_ERR_NOT_IMPLEMENTED, "debug_dequant: not for a dense-linear handle");
   if (!h->packed) return fail(h, NVFP4_MOE_ERR_NOT_PACKED, "debug_dequant before pack");
   const int base = which & 3, via_bf16 = (which >> 2) & 1;
   if (expert < 0 || expert >= h->cfg.num_experts + h->cfg.num_shared_experts || base > 2 || (which & ~7) || !w_out)
@@ -479,6 +513,7 @@ nvfp4_moe_status nvfp4_moe_debug_dequant(nvfp4_moe_t h, int expert, int which, f
 
 nvfp4_moe_status nvfp4_moe_debug_intermediates(nvfp4_moe_t h, void* hidden, float* y, cudaStream_t st) {
   if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (h->linear) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_intermediates: a dense linear has none");
   if (!h->last_T) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_intermediates before any forward");
   if (!hidden || !y) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_intermediates: NULL output");
   DeviceGuard g(h->cfg.device);
@@ -486,6 +521,104 @@ nvfp4_moe_status nvfp4_moe_debug_intermediates(nvfp4_moe_t h, void* hidden, floa
   cudaError_t e = cudaMemcpyAsync(hidden, h->ws.h, n * h->cfg.inter * 2, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(y, h->ws.y, n * h->cfg.hidden * 4, cudaMemcpyDeviceToDevice, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "debug_intermediates copy");
+  return NVFP4_MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Dense W4A16 NVFP4 linear: one matrix, every token, no routing.
+// ---------------------------------------------------------------------------
+nvfp4_moe_status nvfp4_linear_create(const nvfp4_linear_config* c, nvfp4_moe_t* out) {
+  if (!out) return NVFP4_MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!c) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (c->out_features < 16 || c->out_features > 16384 || c->out_features % 16) return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->in_features < 128 || c->in_features > 16384 || c->in_features % 128) return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->max_tokens < 1 || c->max_tokens > (1 << 20)) return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->decode_max_tokens < 0 || c->decode_max_tokens > kDecodeMaxTokens) return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->out_dtype != NVFP4_MOE_OUT_BF16 && c->out_dtype != NVFP4_MOE_OUT_F32) return NVFP4_MOE_ERR_INVALID_ARG;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || c->device < 0 || c->device >= ndev) return NVFP4_MOE_ERR_INVALID_ARG;
+  nvfp4_moe_config m{};
+  m.num_experts = 1;
+  m.hidden = (c->out_features + 127) / 128 * 128;  // whole 128-row blocks; the padding rows are zero
+  m.inter = c->in_features;
+  m.max_tokens = c->max_tokens;
+  m.max_top_k = 1;
+  m.decode_max_tokens = c->decode_max_tokens;
+  m.logits_dtype = NVFP4_MOE_LOGITS_F32;
+  m.out_dtype = c->out_dtype;
+  m.device = c->device;
+  m.num_shared_experts = 0;
+  return create_handle(&m, true, c->out_features, out);
+}
+
+nvfp4_moe_status nvfp4_linear_pack(nvfp4_moe_t h, const uint8_t* w_q, const uint8_t* w_s, const float* gscale,
+                                   cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (!h->linear) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "not a dense-linear handle: call nvfp4_moe_pack");
+  if (!w_q || !w_s || !gscale) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "linear_pack: NULL input");
+  if (!aligned(w_q, 16) || !aligned(w_s, 4) || !aligned(gscale, 4))
+    return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "linear_pack: misaligned input");
+  DeviceGuard g(h->cfg.device);
+  float gs = 0.f;
+  cudaError_t e = cudaMemcpyAsync(&gs, gscale, sizeof(float), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "linear_pack: reading gscale");
+  if (!(gs > 0.0f) || gs != gs || gs > 3.4e38f) {
+    h->packed = false;
+    return fail(h, NVFP4_MOE_ERR_BAD_SCALE, "linear_pack: the tensor scale is not finite > 0");
+  }
+  // the kernels read the down-projection scale of "expert" 0: slot 2 of 3
+  const float gs3[3] = {gs, gs, gs};
+  e = cudaMemcpyAsync(h->gscale, gs3, sizeof(gs3), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = launch_pack_linear(w_q, w_s, h->blob, h->lin_n, h->cfg.hidden, h->cfg.inter, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);  // gs3 lives on this frame
+  if (e != cudaSuccess) return cuda_fail(h, e, "linear_pack launch");
+  h->packed = true;
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_linear_forward(nvfp4_moe_t h, int T, const void* x, void* out, cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (!h->linear) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "not a dense-linear handle: call nvfp4_moe_forward");
+  if (!h->packed) return fail(h, NVFP4_MOE_ERR_NOT_PACKED, "linear_forward before a successful pack");
+  if (T < 1 || T > h->cfg.max_tokens) return fail(h, NVFP4_MOE_ERR_UNSUPPORTED_SHAPE, "T outside 1..max_tokens");
+  if (!x || !out) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "x or out is NULL");
+  if (!aligned(x, 16) || !aligned(out, 16)) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "x or out not 16-byte aligned");
+  const int path = choose_path(h, T, 1);
+  if (path == NVFP4_MOE_PATH_DECODE && T > kDecodeMaxTokens)
+    return fail(h, NVFP4_MOE_ERR_UNSUPPORTED_SHAPE, "decode path takes at most 16 tokens");
+  DeviceGuard g(h->cfg.device);
+  PrefillMaps maps{};
+  if (path == NVFP4_MOE_PATH_PREFILL && !encode_rows_map(&maps.h, const_cast<void*>(x), (uint64_t)T, h->cfg.inter))
+    return fail(h, NVFP4_MOE_ERR_CUDA, "linear_forward: cuTensorMapEncodeTiled failed for x");
+  if (h->log && !h->logged_path[path]) {
+    h->logged_path[path] = true;
+    fprintf(stderr, "[nvfp4_moe] linear forward T=%d -> %s path\n", T,
+            path == NVFP4_MOE_PATH_DECODE ? "decode (GEMV)" : "prefill (tcgen05 GEMM)");
+  }
+  cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  nvfp4_moe_status s = take_events(h, ev);
+  if (s != NVFP4_MOE_OK) return s;
+  if (ev[0]) cudaEventRecord(ev[0], st);
+  const LayerDims d = dims_of(h);
+  cudaError_t e;
+  if (path == NVFP4_MOE_PATH_DECODE) {
+    if (ev[1]) cudaEventRecord(ev[1], st);
+    if (ev[2]) cudaEventRecord(ev[2], st);
+    e = launch_decode_forward(d, h->blob, h->gscale, nullptr, x, T, 1, out, 0, h->num_sms, h->ws, st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "linear decode launch");
+  } else {
+    e = launch_route_linear(T, h->ws, st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "linear tables launch");
+    if (ev[1]) cudaEventRecord(ev[1], st);
+    e = launch_prefill_ffn(d, h->blob, h->gscale, T, 1, h->num_sms, maps, h->ws, h->fault, ev[2], out, st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "linear GEMM launch");
+  }
+  if (ev[3]) cudaEventRecord(ev[3], st);
+  if (ev[4]) cudaEventRecord(ev[4], st);
+  h->last_T = T;
+  h->last_k = 1;
   return NVFP4_MOE_OK;
 }
 

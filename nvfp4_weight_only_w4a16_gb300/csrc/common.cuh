@@ -45,6 +45,19 @@ struct ExpertLayout {
   size_t w13_nib, w2_nib, w13_sc, w2_sc, stride;
 };
 
+// A dense linear W [N][K] packed on its own, like an expert's down matrix
+// (N output rows, K reduction): codes, then scales; no gate/up part.
+__host__ __device__ inline ExpertLayout linear_layout(int N, int K) {
+  ExpertLayout L;
+  const size_t n = (size_t)N * K;
+  L.w13_nib = 0;
+  L.w13_sc = 0;
+  L.w2_nib = 0;
+  L.w2_sc = n / 2;
+  L.stride = n / 2 + n / 16;
+  return L;
+}
+
 __host__ __device__ inline ExpertLayout expert_layout(int H, int I) {
   ExpertLayout L;
   size_t n13 = (size_t)2 * I * H, n2 = (size_t)H * I;

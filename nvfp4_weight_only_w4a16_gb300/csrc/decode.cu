@@ -86,6 +86,8 @@ struct FusedArgs {
   const float* gscale;
   int E, H, I, T, k;  // E experts (routed + shared), k slots per token (top_k + shared)
   int Er, topk;       // routed experts (logits per token), routed choices per token
+  int linear;         // 1: a dense linear: no routing, no gate/up; x [T][I] feeds the down GEMV
+  int n_out;          // a dense linear's output features (<= H; rows past it are padding)
   const void* logits;
   int logits_bf16;
   const __nv_bfloat16* x;
@@ -202,13 +204,14 @@ __device__ void route_block(const FusedArgs& a, RouteSmem& rs, uint8_t* xs, unsi
   // loads first: token `warp`'s logits, and this warp's share of one x row
   uint32_t key[8];
   float val[8];
-  if (warp < T) warp_load_logits(a.logits, a.logits_bf16, Er, warp, key, val);
+  if (warp < T && !a.linear) warp_load_logits(a.logits, a.logits_bf16, Er, warp, key, val);
   const int wpt = dec::kWarps / T;  // warps per token row of x
   const int xt = warp / wpt, xpart = warp - xt * wpt;
-  const int per_row = a.H / 8;  // 16-byte pieces per row
+  const int xcols = a.linear ? a.I : a.H;  // a linear's x rows have its K = I columns
+  const int per_row = xcols / 8;           // 16-byte pieces per row
   float xm = 0.f;
   if (a.x && xt < T) {
-    const uint4* row = reinterpret_cast<const uint4*>(a.x + (size_t)xt * a.H);
+    const uint4* row = reinterpret_cast<const uint4*>(a.x + (size_t)xt * xcols);
     for (int base = xpart * 32; base < per_row; base += 32 * wpt * 8) {
       uint4 v[8];
 #pragma unroll
@@ -238,7 +241,13 @@ __device__ void route_block(const FusedArgs& a, RouteSmem& rs, uint8_t* xs, unsi
     const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(xm));
     if (lane == 0) atomicMax(&rs.xmax[xt], m);
   }
-  if (warp < T) {
+  if (warp < T && a.linear) {  // a dense linear: every token to its one matrix, weight 1
+    if (lane == 0) {
+      rs.ids[warp] = 0;
+      rs.wts[warp] = 1.0f;
+      atomicAdd(&rs.off[0], 1);
+    }
+  } else if (warp < T) {
     int id;
     float logit;
     const int nt = warp_select_topk(key, val, Er, topk, &id, &logit);
@@ -397,7 +406,25 @@ __device__ void finish_down(const FusedArgs& a, const RouteSmem& rs, int u, int 
       const int j = 8 * i + 2 * q + c;
       if (j >= m) continue;
       const int row = row0 + j;
-      const float s = gsd * pow2f(prescale_exp(__uint_as_float(__ldcg(a.hmax + row))));
+      const float s = gsd * pow2f(a.linear ? rs.xexp[rs.perm[row]]
+                                           : prescale_exp(__uint_as_float(__ldcg(a.hmax + row))));
+      if (a.linear) {  // one slot per token, weight 1: the result is the output row itself
+        const size_t o = (size_t)rs.perm[row] * a.n_out;
+#pragma unroll
+        for (int rg = 0; rg < dec::kRG; ++rg) {
+          if (rg >= cnt) break;
+          const int d = 16 * (dec::kRG * b + rg0 + rg) + r0;
+          if (d >= a.n_out) break;  // a 16-row group is all padding or all real: n_out % 16 == 0
+          if (a.out_f32) {
+            reinterpret_cast<float*>(a.out)[o + d] = acc[rg][i][c] * s;
+            reinterpret_cast<float*>(a.out)[o + d + 8] = acc[rg][i][2 + c] * s;
+          } else {
+            reinterpret_cast<__nv_bfloat16*>(a.out)[o + d] = __float2bfloat16_rn(acc[rg][i][c] * s);
+            reinterpret_cast<__nv_bfloat16*>(a.out)[o + d + 8] = __float2bfloat16_rn(acc[rg][i][2 + c] * s);
+          }
+        }
+        continue;
+      }
 #pragma unroll
       for (int rg = 0; rg < dec::kRG; ++rg) {
         if (rg >= cnt) break;
@@ -605,7 +632,7 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
       int u, b, rg0, cnt;
       cw.piece(app, &u, &b, &rg0, &cnt);
       if (u != ap_u) {
-        if (!kGateUp) {  // h of expert u must be complete
+        if (!kGateUp && !a.linear) {  // h of expert u must be complete
           if (lane == 0) {
             const uint64_t t0 = now_ns();
             while (ld_acquire(a.done_gu + u) < gu_units) {
@@ -628,8 +655,9 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
         a_m = min(rs.tch_m[u], 8 * NG);
         a_row = nullptr;
         if (lane < a_m)
-          a_row = kGateUp ? reinterpret_cast<const uint8_t*>(a.x + (size_t)(rs.perm[row0 + lane] / a.k) * a.H)
-                          : reinterpret_cast<const uint8_t*>(a.h + (size_t)(row0 + lane) * a.I);
+          a_row = kGateUp    ? reinterpret_cast<const uint8_t*>(a.x + (size_t)(rs.perm[row0 + lane] / a.k) * a.H)
+                  : a.linear ? reinterpret_cast<const uint8_t*>(a.x + (size_t)rs.perm[row0 + lane] * a.I)
+                             : reinterpret_cast<const uint8_t*>(a.h + (size_t)(row0 + lane) * a.I);
         ap_u = u;
       }
       ap_cur = app;
@@ -695,8 +723,8 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
           int pe = 0;
           if (j < m) {
             const int row = row0 + j;
-            pe = kGateUp ? rs.xexp[rs.perm[row] / a.k]
-                         : max(-126, min(126, prescale_exp(__uint_as_float(__ldcg(a.hmax + row)))));
+            pe = (kGateUp || a.linear) ? rs.xexp[rs.perm[row] / a.k]
+                                       : max(-126, min(126, prescale_exp(__uint_as_float(__ldcg(a.hmax + row)))));
           }
           bsc[gi] = pow2f(-pe);
         }
@@ -970,26 +998,29 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
 
   const int U = rs.U;
   uint32_t ring_it = 0;
-  const CtaWork w1 = cta_work((long long)U * (2 * a.I / 16), 2 * a.I / 16, a.H / kChunk);
   float* slots1 = a.slot_cols ? slots : nullptr;
-  if (xs)
-    run_phase<true, S, NG, true>(a, rs, ring, bars, ring_it, w1, tr, slots1, cnt_all, xs);
-  else
-    run_phase<true, S, NG, false>(a, rs, ring, bars, ring_it, w1, tr, slots1, cnt_all, nullptr);
-  if (tr && lane == 0) tr[2] = now_ns();
   float* slots2 = slots1;
-  if (a.slot_cols && a.slot_sets == 2) {
-    slots2 = slots + slot_floats;  // the down phase has its own slots: no CTA barrier here
-  } else if (a.slot_cols) {        // one set, reused by the down phase
-    __syncthreads();
-    clear_slots(1);
-    __syncthreads();
+  if (!a.linear) {  // a dense linear has no gate/up phase: its x goes straight to the down GEMV
+    const CtaWork w1 = cta_work((long long)U * (2 * a.I / 16), 2 * a.I / 16, a.H / kChunk);
+    if (xs)
+      run_phase<true, S, NG, true>(a, rs, ring, bars, ring_it, w1, tr, slots1, cnt_all, xs);
+    else
+      run_phase<true, S, NG, false>(a, rs, ring, bars, ring_it, w1, tr, slots1, cnt_all, nullptr);
+    if (tr && lane == 0) tr[2] = now_ns();
+    if (a.slot_cols && a.slot_sets == 2) {
+      slots2 = slots + slot_floats;  // the down phase has its own slots: no CTA barrier here
+    } else if (a.slot_cols) {        // one set, reused by the down phase
+      __syncthreads();
+      clear_slots(1);
+      __syncthreads();
+    }
   }
   const CtaWork w2 = cta_work((long long)U * (a.H / 16), a.H / 16, a.I / kChunk);
   run_phase<false, S, NG, false>(a, rs, ring, bars, ring_it, w2, tr, slots2,
                                  cnt_all + (a.slot_sets == 2 ? 16 : 0), nullptr);
   if (tr && lane == 0) tr[4] = now_ns();
-  combine_tasks(a, rs, (long long)blockIdx.x * dec::kWarps + warp, (long long)gridDim.x * dec::kWarps, lane);
+  if (!a.linear)
+    combine_tasks(a, rs, (long long)blockIdx.x * dec::kWarps + warp, (long long)gridDim.x * dec::kWarps, lane);
 
   // the last CTA out resets the per-forward counters (and, after a timeout,
   // every arrival counter) for the next forward
@@ -1007,7 +1038,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
   for (int i = threadIdx.x; i < R; i += blockDim.x) a.hmax[i] = 0u;
   for (int i = threadIdx.x; i < a.H / 64; i += blockDim.x) a.cmb[i] = 0;
   if (aborted(a.st)) {
-    const size_t ngu = (size_t)U * (2 * a.I / 16), ndn = (size_t)U * (a.H / 16);
+    const size_t ngu = a.linear ? 0 : (size_t)U * (2 * a.I / 16), ndn = (size_t)U * (a.H / 16);
     for (size_t i = threadIdx.x; i < ngu; i += blockDim.x) a.cnt_gu[i] = 0;
     for (size_t i = threadIdx.x; i < ndn; i += blockDim.x) a.cnt_dn[i] = 0;
   }
@@ -1035,10 +1066,16 @@ static int decode_stage_cap() {
   }();
   return cap;
 }
-static DecodeSmemPlan plan_smem(int T, int H, int smem_max) {
+static DecodeSmemPlan plan_smem(int T, int H, int linear, int smem_max) {
   const size_t base = ((sizeof(RouteSmem) + 127) & ~size_t(127)) + 128 * 8 + 128;
   const size_t ring1 = (size_t)dec::kWarps * dec::stage_bytes_for(T);  // one stage per warp
   const int cap = decode_stage_cap();
+  if (linear && T <= 8) {  // one phase: one set of slots, no staged activations, the deepest ring that fits
+    const size_t slot_b = (size_t)dec::kSlots * 64 * T * 4;
+    for (int S = cap; S > 3; --S)
+      if (base + S * ring1 + slot_b <= (size_t)smem_max) return DecodeSmemPlan{base + S * ring1 + slot_b, S, T, 1, 0};
+    return DecodeSmemPlan{base + 3 * ring1 + slot_b, cap < 3 ? cap : 3, T, 1, 0};
+  }
   if (T > 8) {  // two ring stages and one set of shared-memory split-K slots, else three stages
     static const bool slots16 = [] {
       const char* s = getenv("NVFP4_MOE_DECODE_T16_SLOTS");
@@ -1081,9 +1118,9 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
     smem_max = optin;
   }
   const bool small = T <= 8;
-  const DecodeSmemPlan plan = plan_smem(T, d.H, smem_max);
+  const DecodeSmemPlan plan = plan_smem(T, d.H, d.linear, smem_max);
   if (plan.bytes > (size_t)smem_max) return cudaErrorInvalidConfiguration;
-  const ExpertLayout L = expert_layout(d.H, d.I);
+  const ExpertLayout L = d.linear ? linear_layout(d.H, d.I) : expert_layout(d.H, d.I);
   FusedArgs a{};
   a.blob = blob;
   a.expert_stride = L.stride;
@@ -1099,6 +1136,8 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
   a.T = T;
   a.k = k + d.S;
   a.topk = k;
+  a.linear = d.linear;
+  a.n_out = d.n_out;
   a.logits = logits;
   a.logits_bf16 = d.logits_bf16;
   a.x = reinterpret_cast<const __nv_bfloat16*>(x);

@@ -49,6 +49,10 @@ struct LayerDims {
   int out_f32;
   int Er;          // routed experts: router logits per token
   int S;           // shared experts (0 or 1): slots per token = top_k + S
+  int linear;      // 1: a dense linear: one "expert" holding only a down matrix [H][I] (linear_layout),
+                   // no routing and no gate/up; x [T][I] is the down GEMM's input
+  int n_out;       // a dense linear's output features N <= H (H = N rounded up to 128; the
+                   // padded rows are zero): out is [T][n_out]
 };
 
 constexpr int kRankTokens = 256;      // tokens per rank block in the prefill routing
@@ -60,6 +64,9 @@ inline size_t decode_part_floats(int num_sms, int T) {
   return (size_t)num_sms * kDecodeWarpsPerSm * 2 * 64 * (size_t)(T < 16 ? T : 16);
 }
 
+// W [N][K] into linear_layout(Np, K), Np = N rounded up to 128; rows N..Np-1 packed as zeros.
+cudaError_t launch_pack_linear(const uint8_t* w_q, const uint8_t* w_s, uint8_t* blob, int N, int Np, int K,
+                               cudaStream_t st);
 cudaError_t launch_pack(const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
                         const uint8_t* w2_s, uint8_t* blob, int E, int H, int I, cudaStream_t st);
 cudaError_t launch_debug_dequant(const uint8_t* blob, const float* gscale, int H, int I, int expert,
@@ -75,13 +82,19 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
                                   const void* x, int T, int k, void* out, int route_only, int num_sms,
                                   const Workspace& ws, cudaStream_t st);
 
+// A dense linear's tables: every token to matrix 0 with weight 1, identity
+// perm/inv, offsets {0, T}, and the m-tiles of 128 rows in token order.
+cudaError_t launch_route_linear(int T, const Workspace& ws, cudaStream_t st);
+
 struct PrefillMaps {
   CUtensorMap x_perm;  // [R][H] bf16, box {64, 16}, 128B swizzle
-  CUtensorMap h;       // [R][I] bf16, box {64, 16}, 128B swizzle
+  CUtensorMap h;       // [R][I] bf16, box {64, 16}, 128B swizzle (a dense linear: its x [T][I])
 };
+// The grouped gate/up and down GEMMs; a dense linear (d.linear) runs the
+// down GEMM alone and writes its rows to out (unused otherwise).
 cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const float* gscale, int T, int k,
                                int num_sms, const PrefillMaps& maps, const Workspace& ws, int fault,
-                               cudaEvent_t mid, cudaStream_t st);
+                               cudaEvent_t mid, void* out, cudaStream_t st);
 size_t prefill_smem_bytes();
 
 cudaError_t launch_combine(const LayerDims& d, int T, int k, const Workspace& ws, void* out,

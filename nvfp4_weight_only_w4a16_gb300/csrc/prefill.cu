@@ -77,6 +77,10 @@ struct PrefillArgs {
   const int32_t* num_tiles;
   __nv_bfloat16* h;
   float* y;
+  void* out;     // a dense linear writes its rows here directly (row = token)
+  int out_f32;   // out is FP32 (else BF16)
+  int linear;    // 1: a dense linear (one matrix, rows in token order, weight 1)
+  int n_out;     // a dense linear's output features: out is [T][n_out], rows d >= n_out are padding
   DeviceStatus* st;
   int fault;  // 1: the producer issues nothing (tests the bounded waits)
 };
@@ -412,9 +416,22 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           } else {
             const int d = 128 * nb + i;
             const float gsd = gs[2];
+            if (a.linear && a.out_f32) {
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-              if (col + jj < rows) a.y[(size_t)(row0 + col + jj) * a.H + d] = gsd * __uint_as_float(v[jj]);
+              for (int jj = 0; jj < 16; ++jj)
+                if (col + jj < rows && d < a.n_out)
+                  reinterpret_cast<float*>(a.out)[(size_t)(row0 + col + jj) * a.n_out + d] = gsd * __uint_as_float(v[jj]);
+            } else if (a.linear) {
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj)
+                if (col + jj < rows && d < a.n_out)
+                  reinterpret_cast<__nv_bfloat16*>(a.out)[(size_t)(row0 + col + jj) * a.n_out + d] =
+                      __float2bfloat16_rn(gsd * __uint_as_float(v[jj]));
+            } else {
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj)
+                if (col + jj < rows) a.y[(size_t)(row0 + col + jj) * a.H + d] = gsd * __uint_as_float(v[jj]);
+            }
           }
         }
       }
@@ -435,7 +452,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 
 cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const float* gscale, int T, int k,
                                int num_sms, const PrefillMaps& maps, const Workspace& ws, int fault,
-                               cudaEvent_t mid, cudaStream_t st) {
+                               cudaEvent_t mid, void* out, cudaStream_t st) {
   (void)T;
   (void)k;
   static bool attr_set = false;
@@ -448,7 +465,7 @@ cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const fl
     if (e2 != cudaSuccess) return e2;
     attr_set = true;
   }
-  const ExpertLayout L = expert_layout(d.H, d.I);
+  const ExpertLayout L = d.linear ? linear_layout(d.H, d.I) : expert_layout(d.H, d.I);
   PrefillArgs a{};
   a.blob = blob;
   a.expert_stride = L.stride;
@@ -461,14 +478,19 @@ cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const fl
   a.num_tiles = ws.num_tiles;
   a.h = ws.h;
   a.y = ws.y;
+  a.out = out;
+  a.out_f32 = d.out_f32;
+  a.linear = d.linear;
+  a.n_out = d.n_out;
   a.st = ws.status;
   a.fault = fault;
-  // gate/up: 2I interleaved rows, K = H
-  a.nib_off = L.w13_nib;
-  a.sc_off = L.w13_sc;
-  a.K = d.H;
-  a.NB = 2 * d.I / 128;
-  prefill_gemm_kernel<true><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(maps.x_perm, a);
+  if (!d.linear) {  // gate/up: 2I interleaved rows, K = H
+    a.nib_off = L.w13_nib;
+    a.sc_off = L.w13_sc;
+    a.K = d.H;
+    a.NB = 2 * d.I / 128;
+    prefill_gemm_kernel<true><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(maps.x_perm, a);
+  }
   if (mid) cudaEventRecord(mid, st);
   // down: H rows, K = I
   a.nib_off = L.w2_nib;

@@ -140,6 +140,33 @@ cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const v
   return cudaGetLastError();
 }
 
+// A dense linear: identity tables and 128-row m-tiles in token order.
+__global__ void __launch_bounds__(256) route_linear_kernel(int T, Workspace ws) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < T) {
+    ws.ids[i] = 0;
+    ws.wts[i] = 1.0f;
+    ws.perm[i] = i;
+    ws.inv[i] = i;
+  }
+  const int ntiles = (T + kTileRows - 1) / kTileRows;
+  if (i < ntiles) {
+    ws.tile_expert[i] = 0;
+    ws.tile_row0[i] = i * kTileRows;
+    ws.tile_rows[i] = min(kTileRows, T - i * kTileRows);
+  }
+  if (i == 0) {
+    ws.offsets[0] = 0;
+    ws.offsets[1] = T;
+    *ws.num_tiles = ntiles;
+  }
+}
+
+cudaError_t launch_route_linear(int T, const Workspace& ws, cudaStream_t st) {
+  route_linear_kernel<<<(T + 255) / 256, 256, 0, st>>>(T, ws);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------------------
 // Weighted combine: out[t][d] = sum_{j<k} w[t][j] * y[pos(t,j)][d] in FP32,
 // slot order j = 0..k-1 (a shared expert is the last slot, weight 1),

@@ -145,7 +145,7 @@ extern "C" nvfp4_moe_status nvfp4_moe_forward_decode_static(const uint8_t* packe
 
   Workspace ws{};
   carve(setup.scratch, E, H, I, T, top_k, setup.num_sms, &ws, &zero_bytes);
-  const LayerDims d{E, H, I, logits_dtype == NVFP4_MOE_LOGITS_BF16, 0, E, 0};
+  const LayerDims d{E, H, I, logits_dtype == NVFP4_MOE_LOGITS_BF16, 0, E, 0, 0, 0};
   cudaError_t e = cudaMemsetAsync(setup.scratch, 0, zero_bytes, stream);
   if (e == cudaSuccess)
     e = launch_decode_forward(d, packed_experts, gscale, router_logits, x, T, top_k, out, 0, setup.num_sms, ws,

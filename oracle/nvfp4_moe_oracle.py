@@ -44,7 +44,7 @@ import numpy as np
 __all__ = [
     "decode_e2m1", "decode_e4m3", "unpack_e2m1_codes", "dequant", "dequant_scaled_f32",
     "bf16_bits_to_f64", "route", "permute", "silu", "expert_ffn", "expert_hidden",
-    "moe_forward", "RouteResult",
+    "moe_forward", "linear_forward", "RouteResult",
 ]
 
 

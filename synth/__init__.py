@@ -18,4 +18,8 @@ from .inputs import (  # noqa: F401
     encode_e4m3_rne,
     encode_e2m1_rne,
     f32_to_bf16_bits,
+    LINEAR_CONFIGS,
+    LinearConfig,
+    LinearInputs,
+    make_linear_inputs,
 )

@@ -290,3 +290,68 @@ def make_inputs(name_or_cfg, tokens: int | None = None) -> LayerInputs:
         cfg = cfg.with_tokens(tokens)
     logits, x_bits, bias = make_activations(cfg)
     return LayerInputs(cfg, logits, x_bits, make_layer_weights(cfg), bias)
+
+
+# ----------------------------------------------------------------------------
+# Dense W4A16 linears
+# ----------------------------------------------------------------------------
+# The dense side of the model (attention linears, shared experts, lm_head) in
+# the same weight-only NVFP4 format ("GLM-5.3-Flash-NVFP4-h — W4A16
+# dense-side quantization", opening summary).  The one dense shape the pages
+# print is the fused KDA in_proj, N = 12576 outputs over K = 4096
+# ("tacos4me/GLM-5.3-Flash-NVFP4-FP8ATTN-512K", The kernel story); it runs at
+# the MTP decode step (2 tokens) and at a 1024-token prefill piece.  Weights
+# W ~ N(0, std) [N][K] are encoded by quantize_nvfp4 from the stream
+# SeedSequence(seed, spawn_key=(2,)); x [T][K] (standard normal, rounded to
+# BF16) from SeedSequence(seed, spawn_key=(3,)).
+
+@dataclass(frozen=True)
+class LinearConfig:
+    name: str
+    out_features: int   # N
+    in_features: int    # K
+    tokens: int         # T
+    weight_std: float = 0.02
+    seed: int = 0
+
+    def with_tokens(self, tokens: int) -> "LinearConfig":
+        return LinearConfig(self.name, self.out_features, self.in_features, tokens, self.weight_std, self.seed)
+
+    @property
+    def weight_bytes(self) -> int:
+        n = self.out_features * self.in_features
+        return n // 2 + n // 16
+
+
+LINEAR_CONFIGS = {
+    # small, N not a multiple of 128 (the last 128-row block is padded), ragged T
+    "linear_tiny": LinearConfig("linear_tiny", 272, 256, 37),
+    "kda_in_proj_mtp": LinearConfig("kda_in_proj_mtp", 12576, 4096, 2),
+    "kda_in_proj_1k": LinearConfig("kda_in_proj_1k", 12576, 4096, 1024),
+}
+
+
+@dataclass
+class LinearInputs:
+    config: LinearConfig
+    w_q: np.ndarray     # u8 [N][K/2]
+    w_s: np.ndarray     # u8 [N][K/16]
+    gscale: np.float32  # the tensor scale
+    x_bits: np.ndarray  # u16 [T][K]  BF16 bit patterns
+
+
+@lru_cache(maxsize=2)
+def _linear_weights_cached(N: int, K: int, std: float, seed: int):
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(2,))))
+    w = rng.standard_normal((N, K), dtype=np.float32) * np.float32(std)
+    return quantize_nvfp4(w)
+
+
+def make_linear_inputs(name_or_cfg, tokens: int | None = None) -> LinearInputs:
+    cfg = LINEAR_CONFIGS[name_or_cfg] if isinstance(name_or_cfg, str) else name_or_cfg
+    if tokens is not None:
+        cfg = cfg.with_tokens(tokens)
+    q, s, g = _linear_weights_cached(cfg.out_features, cfg.in_features, cfg.weight_std, cfg.seed)
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(cfg.seed, spawn_key=(3,))))
+    x = rng.standard_normal((cfg.tokens, cfg.in_features), dtype=np.float32)
+    return LinearInputs(cfg, q, s, np.float32(g), f32_to_bf16_bits(x))

@@ -22,6 +22,7 @@ def lib():
 def test_exports_every_header_symbol(lib):
     names = P.header_functions()
     assert "nvfp4_moe_create" in names and "nvfp4_moe_forward" in names and "nvfp4_moe_pack" in names
+    assert "nvfp4_linear_create" in names and "nvfp4_linear_forward" in names and "nvfp4_linear_pack" in names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -78,5 +79,39 @@ def test_header_has_no_activation_scale():
     # weight-only: the forward takes logits, x and out, never an input scale
     text = open(P.binding.HEADER).read()
     fwd = text[text.index("nvfp4_moe_status nvfp4_moe_forward("):]
+    fwd = fwd[:fwd.index(";")]
+    assert "scale" not in fwd
+
+
+def _create_linear(lib, **kw):
+    base = dict(out_features=272, in_features=256, max_tokens=16, decode_max_tokens=16, out_dtype=0, device=0)
+    base.update(kw)
+    cfg = P.binding.LinearConfig(**base)
+    h = ctypes.c_void_p()
+    return lib.nvfp4_linear_create(ctypes.byref(cfg), ctypes.byref(h)), h
+
+
+@pytest.mark.parametrize("kw", [
+    dict(out_features=0), dict(out_features=8), dict(out_features=100), dict(out_features=16400),
+    dict(in_features=64), dict(in_features=200), dict(max_tokens=0), dict(decode_max_tokens=17),
+])
+def test_linear_create_rejects_bad_shapes(lib, kw):
+    st, h = _create_linear(lib, **kw)
+    assert st == P.STATUS_CODE["NVFP4_MOE_ERR_UNSUPPORTED_SHAPE"]
+    assert not h.value
+
+
+def test_linear_null_and_bad_args(lib):
+    inv = P.STATUS_CODE["NVFP4_MOE_ERR_INVALID_ARG"]
+    st, h = _create_linear(lib, out_dtype=3)
+    assert st == inv and not h.value
+    assert lib.nvfp4_linear_create(None, None) == inv
+    assert lib.nvfp4_linear_pack(None, None, None, None, None) == inv
+    assert lib.nvfp4_linear_forward(None, 1, None, None, None) == inv
+
+
+def test_linear_header_has_no_activation_scale():
+    text = open(P.binding.HEADER).read()
+    fwd = text[text.index("nvfp4_moe_status nvfp4_linear_forward("):]
     fwd = fwd[:fwd.index(";")]
     assert "scale" not in fwd

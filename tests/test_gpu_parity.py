@@ -6,9 +6,10 @@ Bars:
   logits against float64);
 * layer output: max|err| <= 2e-2 * RMS(oracle) and mean|err| / mean|oracle|
   <= 5e-3 on the FP32 output; a BF16 output may in addition differ by the
-  final rounding, at most 2^-9 of each output (for heavy-tailed outputs, such
-  as the 16K-token workload with x20 outlier weights, rounding the exact
-  result to BF16 alone exceeds 2e-2 * RMS); plus the magnitude check the weight-only serving postmortem asks
+  final rounding, at most 2^-8 of each output (BF16 keeps 8 significant
+  bits; for heavy-tailed outputs, such as the 16K-token workload with x20
+  outlier weights, rounding the exact result to BF16 alone exceeds 2e-2 *
+  RMS); plus the magnitude check the weight-only serving postmortem asks
   for ("GLM-5.3-Flash on Blackwell", The model loaded, served an API, and
   produced garbage: an inverted scale kept cosine 0.996 at 25x the
   magnitude): ||gpu|| / ||oracle|| in [0.99, 1.01] and cosine >= 0.9999.
@@ -66,7 +67,7 @@ def _forward(L, logits, x_bits, k, path=P.PATH_AUTO):
 def assert_layer_close(gpu, ref, bf16_out=True):
     err = np.abs(gpu - ref)
     rms = np.sqrt(np.mean(ref ** 2))
-    allow = 2.0 ** -9 * np.abs(gpu) if bf16_out else 0.0
+    allow = 2.0 ** -8 * np.abs(gpu) if bf16_out else 0.0
     assert np.all(err <= 2e-2 * rms + allow), (err.max(), rms)
     assert err.mean() / np.abs(ref).mean() <= 5e-3, err.mean() / np.abs(ref).mean()
     ratio = np.linalg.norm(gpu) / np.linalg.norm(ref)
