@@ -18,6 +18,9 @@ Measured:
   bandwidth (prefill workloads: the gate/up GEMM's flops against BF16 peak);
 * cpu_baseline: the float64 CPU oracle on a bounded sample of the same step.
 --impl reference times the oracle alone (the CPU reference arm).
+--workload kda_in_proj_mtp | kda_in_proj_1k | linear_tiny runs the dense
+W4A16 linear instead (nvfp4_linear_forward on the fused KDA in_proj shape,
+N=12576 K=4096, at T=2 and T=1024), with the same keys.
 Multi-GPU: replicas only (one independent layer per rank, no collective in
 the data path); value is the tokens of all ranks over the slowest rank's time.
 """
@@ -399,12 +402,220 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# Dense W4A16 linear workloads (--workload kda_in_proj_mtp | kda_in_proj_1k | linear_tiny)
+# ---------------------------------------------------------------------------
+
+LINEAR_METRIC = "W4A16 NVFP4 dense linear tokens/s; decode weight GB/s & prefill TFLOP/s as % of GB300 roofline"
+
+_LINEAR_ORACLE_CHILD = r"""
+import sys, time, json, numpy as np
+sys.path.insert(0, sys.argv[1])
+import oracle
+d = np.load(sys.argv[2])
+reps = int(sys.argv[3])
+times = []
+for _ in range(reps):
+    t0 = time.perf_counter(); oracle.linear_forward(d["x_bits"], d["w_q"], d["w_s"], float(d["g"])); times.append(time.perf_counter() - t0)
+print(json.dumps({"times": times}))
+"""
+
+
+def _linear_desc(cfg):
+    return (f"{cfg.name}: dense linear N{cfg.out_features} K{cfg.in_features} T{cfg.tokens}, NVFP4 "
+            f"(E2M1 + E4M3/16 + FP32/tensor) weights, BF16 activations")
+
+
+def _time_linear_oracle(inp, ns, reps):
+    fd, path = tempfile.mkstemp(suffix=".npz")
+    os.close(fd)
+    np.savez(path, x_bits=inp.x_bits[:ns], w_q=inp.w_q, w_s=inp.w_s, g=np.float32(inp.gscale))
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[v] = "1"
+    try:
+        r = subprocess.run([sys.executable, "-c", _LINEAR_ORACLE_CHILD, ROOT, path, str(reps)],
+                           capture_output=True, text=True, env=env)
+    finally:
+        os.unlink(path)
+    if r.returncode != 0:
+        raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])["times"]
+
+
+def run_linear_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from synth import make_linear_inputs
+    inp = make_linear_inputs(args.workload)
+    cfg = inp.config
+    times = _time_linear_oracle(inp, 1, args.warmup + args.steps)[args.warmup:]
+    sec = sum(times)
+    value = args.steps / sec   # one token per step
+    line = {
+        "impl": "reference", "metric": LINEAR_METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded PCG64, the pages' fused KDA in_proj shape)",
+        "config": {"workload": _linear_desc(cfg)},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "one token per step (dequantise W, one float64 GEMV), 1 thread"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_linear(args):
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import nvfp4_weight_only_w4a16_gb300 as pkg
+    from synth import make_linear_inputs
+    pkg.build()
+    inp = make_linear_inputs(args.workload)
+    cfg = inp.config
+    T, N, K = cfg.tokens, cfg.out_features, cfg.in_features
+    lin = pkg.Linear(N, K, T, device=dev.index)
+    lin.nvfp4_linear_pack(torch.from_numpy(inp.w_q).to(dev), torch.from_numpy(inp.w_s).to(dev),
+                          torch.tensor([float(inp.gscale)], dtype=torch.float32, device=dev))
+    decode = T <= 16
+    n_ours = 1 if decode else 2     # the GEMV kernel / the tables kernel + the GEMM
+    x = torch.from_numpy(inp.x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        lin.nvfp4_linear_forward(x, out)
+    torch.cuda.synchronize()
+    st, _ = lin.nvfp4_moe_get_status()
+    if st != 0:
+        raise RuntimeError(f"device status {pkg.STATUS[st]} after warm-up")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        lin.nvfp4_linear_forward(x, out)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.1)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    for s, e in evs:
+        flush.zero_()
+        s.record(stream)
+        graph.replay()
+        e.record(stream)
+    barrier()
+    step_ms = [s.elapsed_time(e) for s, e in evs]
+
+    lin.nvfp4_moe_set_profiling(True)
+    barrier()
+    for _ in range(args.steps):
+        flush.zero_()
+        lin.nvfp4_linear_forward(x, out)
+    barrier()
+    stage_ms, nfwd = lin.nvfp4_moe_get_stage_times()
+    lin.nvfp4_moe_set_profiling(False)
+
+    h_x = torch.from_numpy(inp.x_bits.view(np.int16)).pin_memory()
+    h_out = torch.empty((T, N), dtype=torch.int16).pin_memory()
+    d_x16 = x.view(torch.int16)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    for s, e in e2e_ev:
+        flush.zero_()
+        s.record(stream)
+        d_x16.copy_(h_x, non_blocking=True)
+        lin.nvfp4_linear_forward(x, out)
+        h_out.copy_(out.view(torch.int16), non_blocking=True)
+        e.record(stream)
+    barrier()
+    e2e_ms = [s.elapsed_time(e) for s, e in e2e_ev]
+    clocks = sampler.stop()
+    st, _ = lin.nvfp4_moe_get_status()
+    if st != 0:
+        raise RuntimeError(f"device status {pkg.STATUS[st]} after the timed region")
+
+    ms, ms_e2e = statistics.mean(step_ms), statistics.mean(e2e_ms)
+    if ws > 1:
+        t = torch.tensor([ms, ms_e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, ms_e2e = float(t[0]), float(t[1])
+    value, value_e2e = ws * T / (ms / 1e3), ws * T / (ms_e2e / 1e3)
+    kern_ms = stage_ms[2] / max(nfwd, 1)   # the GEMV / GEMM launch (tables kernel excluded)
+    wbytes = cfg.weight_bytes
+    if decode:
+        kernel, bound, unit, peak_key = "decode_fused_kernel (linear)", "hbm", "GB/s", "hbm_gbs"
+        algo = wbytes + T * K * 2 + T * N * 2
+        achieved = algo / (kern_ms / 1e3) / 1e9
+    else:
+        kernel, bound, unit, peak_key = "prefill_gemm_kernel<down> (linear)", "tensor", "TFLOP/s", "bf16_tflops"
+        algo = 2.0 * T * N * K
+        achieved = algo / (kern_ms / 1e3) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)[peak_key])
+        peak_src = "measured"
+    except Exception:
+        peak, peak_src = (6800.0 if bound == "hbm" else 1900.0), "fallback"
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        times = _time_linear_oracle(inp, 1, 2)
+        cpu = {"value": 1 / statistics.mean(times), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": "1 token of the step (dequantise W, one float64 GEMV), twice, 1 thread"}
+    if rank == 0:
+        line = {
+            "metric": LINEAR_METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "w4a16: e2m1*e4m3 weights -> fp16/bf16 mma, fp32 accumulate",
+            "data": "synthetic (seeded PCG64, the pages' fused KDA in_proj shape)",
+            "config": {"workload": _linear_desc(cfg), "weight_bytes": wbytes,
+                       "weight_gbs": wbytes / (ms / 1e3) / 1e9, "tflops": 2.0 * T * N * K / (ms / 1e3) / 1e12,
+                       "kernel_ms": kern_ms,
+                       "l2": "flushed before every step (256 MiB write, outside the step events)",
+                       "launch": "CUDA graph replay of one nvfp4_linear_forward",
+                       "parallelism": f"replicas x{ws}"},
+            "roofline": {"bound": bound, "kernel": kernel, "achieved": achieved, "peak": peak,
+                         "peak_source": peak_src, "unit": unit, "frac": achieved / peak,
+                         "algorithmic_per_launch": algo, "traffic": None},
+            "e2e": {"value": value_e2e, "unit": "tokens/s", "h2d_bytes_per_step": T * K * 2,
+                    "d2h_bytes_per_step": T * N * 2},
+            "gpu_launches": n_ours * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    lin.close()
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = _args()
+    from synth import LINEAR_CONFIGS
+    linear = args.workload in LINEAR_CONFIGS
     if args.impl == "reference":
-        run_reference(args)
+        (run_linear_reference if linear else run_reference)(args)
     else:
-        run_ours(args)
+        (run_linear if linear else run_ours)(args)
 
 
 if __name__ == "__main__":
