@@ -32,7 +32,8 @@ design notes):
   product;
 * top-k: larger logit first, equal logits -> lower expert index first, NaN
   ranks below -inf;
-* routing weights: softmax over the k selected logits, no extra factor;
+* routing weights: softmax over the k selected logits, no extra factor (the
+  sigmoid / bias-corrected / unnormalised / scaled variants: route_scored);
 * permutation: expert-major, ascending flattened index t*k+j inside an expert;
 * SwiGLU: h = silu(gate) * up with silu(z) = z / (1 + exp(-z));
 * combine: out[t] = sum_j w[t][j] * y[t, j], summed in slot order j = 0..k-1.
@@ -43,7 +44,7 @@ import numpy as np
 
 __all__ = [
     "decode_e2m1", "decode_e4m3", "unpack_e2m1_codes", "dequant", "dequant_scaled_f32",
-    "bf16_bits_to_f64", "route", "permute", "silu", "expert_ffn", "expert_hidden",
+    "bf16_bits_to_f64", "route", "route_scored", "router_logits", "permute", "silu", "expert_ffn", "expert_hidden",
     "moe_forward", "linear_forward", "RouteResult",
 ]
 
@@ -159,6 +160,78 @@ def route(logits, k: int) -> RouteResult:
     return RouteResult(ids, w, int(nan.sum()))
 
 
+def route_scored(logits, k: int, score: str = "softmax", renormalize: bool = True, scale: float = 1.0,
+                 bias=None) -> RouteResult:
+    """Top-k routing with a choice of scoring rule (the router variants).
+
+    The pages keep the routers as BF16 linears and say nothing more about how
+    their outputs become expert choices and weights ("GLM-5.3-Flash on
+    Blackwell", The quantization: the routers stay BF16; "tenhkspark/GLM-5.3-
+    Flash-NVFP4-Wabi", Config expectations: the per-layer mlp.gate routers are
+    excluded from quantisation).  The variants, each a plain reading:
+
+    * score = "softmax": s_e = exp(l_e - max) / sum over ALL experts; with
+      renormalize the chosen k weights are divided by their own sum, which is
+      the same as softmax over the k chosen logits (route());
+    * score = "sigmoid": s_e = 1 / (1 + exp(-l_e)); with renormalize the
+      chosen weights are s_j / sum of the chosen s (1/k each if that sum is 0);
+    * bias [E] (optional): added to s_e for the CHOICE only ("bias-
+      corrected" selection); the weights use s_e without it;
+    * scale: every final weight is multiplied by it.
+    The choice orders experts by s_e + bias_e: larger first, equal values ->
+    lower expert index first, a NaN logit below everything (its s counts as 0
+    in the weights).  Softmax edge cases follow route(): all -inf -> equal s,
+    any +inf -> the +inf entries share s = 1.
+    """
+    L = np.asarray(logits, dtype=np.float64)
+    T, E = L.shape
+    if not 1 <= k <= E:
+        raise ValueError("top_k must be in 1..E")
+    if score not in ("softmax", "sigmoid"):
+        raise ValueError("score must be softmax or sigmoid")
+    b = np.zeros(E) if bias is None else np.asarray(bias, dtype=np.float64)
+    nan = np.isnan(L)
+    idx = np.arange(E)
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    for t in range(T):
+        l = np.where(nan[t], -np.inf, L[t])
+        if score == "sigmoid":
+            with np.errstate(over="ignore"):
+                s = 1.0 / (1.0 + np.exp(-l))
+        else:
+            m = l.max()
+            if m == -np.inf:
+                s = np.full(E, 1.0 / E)
+            elif m == np.inf:
+                hit = (l == np.inf).astype(np.float64)
+                s = hit / hit.sum()
+            else:
+                ex = np.exp(l - m)
+                s = ex / ex.sum()
+        choice = s + b
+        order = np.lexsort((idx, -np.where(nan[t], 0.0, choice), nan[t].astype(np.int8)))
+        sel = order[:k]
+        ids[t] = sel
+        ws = np.where(nan[t, sel], 0.0, s[sel])
+        if renormalize:
+            tot = ws.sum()
+            ws = ws / tot if tot > 0 else np.full(k, 1.0 / k)
+        w[t] = scale * ws
+    return RouteResult(ids, w, int(nan.sum()))
+
+
+def router_logits(x_bits, w_router_bits) -> np.ndarray:
+    """The router linear: logits[t][e] = sum_h x[t][h] * W[e][h] in float64.
+
+    x [T][H] and W [E][H] are BF16 bit patterns (the routers stay BF16:
+    "GLM-5.3-Flash on Blackwell", The quantization); no linear bias.
+    """
+    x = bf16_bits_to_f64(np.asarray(x_bits))
+    wr = bf16_bits_to_f64(np.asarray(w_router_bits))
+    return x @ wr.T
+
+
 def permute(ids, num_experts: int):
     """Expert-major stable order of the T*k routed rows.
 
@@ -207,7 +280,8 @@ def expert_ffn(w, e: int, x) -> np.ndarray:
     return gs[2] * (h @ wd.T)
 
 
-def moe_forward(logits, x_bits, weights, k: int, tokens=None, return_parts=False, num_shared: int = 0):
+def moe_forward(logits, x_bits, weights, k: int, tokens=None, return_parts=False, num_shared: int = 0,
+                scoring=None):
     """out[t] = sum_{j<k} w[t][j] * FFN_{ids[t][j]}(x[t]) (+ FFN_E(x[t])) in float64.
 
     logits [T][E] (float32 or float64), x_bits [T][H] BF16 bit patterns,
@@ -224,13 +298,15 @@ def moe_forward(logits, x_bits, weights, k: int, tokens=None, return_parts=False
     listed token, in that order).  With return_parts, also returns the route
     result and the per-slot expert outputs y [len(tokens)][k + num_shared][H]
     (the shared expert's in the last slot).
+    scoring: None for route(), else the keyword arguments of route_scored
+    (score, renormalize, scale, bias).
     """
     if num_shared not in (0, 1):
         raise ValueError("num_shared must be 0 or 1")
     logits = np.asarray(logits)
     T, E = logits.shape
     tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
-    r = route(logits[tok], k)
+    r = route(logits[tok], k) if scoring is None else route_scored(logits[tok], k, **scoring)
     x = bf16_bits_to_f64(np.asarray(x_bits)[tok])
     H = x.shape[1]
     y = np.zeros((len(tok), k + num_shared, H), dtype=np.float64)

@@ -15,6 +15,7 @@
 The mutation test at the end plants plausible mistakes in the oracle (on the
 CPU) and checks that at least one pin catches each.
 """
+import itertools
 import math
 import os
 
@@ -337,9 +338,80 @@ def pin_linear(o):
             assert abs(out[t, n] - 0.75 * acc) <= 1e-12 * max(1.0, abs(acc))
 
 
+def _logit(p):
+    return math.log(p / (1.0 - p))
+
+
+def pin_route_scored(o):
+    # (1) the choice maximises the sum of s + bias over all k-subsets (a
+    # formulation independent of sorting), and the chosen experts come in
+    # descending s + bias; weights = chosen s (no bias), renormalised, scaled
+    rng = np.random.default_rng(41)
+    T, E = 25, 7
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    b = rng.standard_normal(E) * 0.3
+    for k in (1, 3, 7):
+        r = o.route_scored(L, k, "sigmoid", True, 2.5, b)
+        for t in range(T):
+            sg = [1.0 / (1.0 + math.exp(-float(v))) for v in L[t]]
+            ch = [sg[e] + b[e] for e in range(E)]
+            best = max(itertools.combinations(range(E), k), key=lambda c: sum(ch[e] for e in c))
+            assert sorted(r.ids[t].tolist()) == sorted(best), (t, k)
+            got = [ch[e] for e in r.ids[t]]
+            assert got == sorted(got, reverse=True)
+            tot = sum(sg[e] for e in best)
+            for j, e in enumerate(r.ids[t]):
+                assert abs(r.weights[t, j] - 2.5 * sg[e] / tot) <= 1e-14
+    # (2) closed forms with s = p exactly chosen: logits = logit(p)
+    p = [0.1, 0.2, 0.4, 0.6, 0.8, 0.9]
+    Lp = np.array([[_logit(v) for v in p]])
+    r = o.route_scored(Lp, 3, "sigmoid", True, 1.0)
+    assert r.ids.tolist() == [[5, 4, 3]] and np.allclose(r.weights, [[0.9 / 2.3, 0.8 / 2.3, 0.6 / 2.3]], rtol=1e-14)
+    r = o.route_scored(Lp, 3, "sigmoid", False, 2.0)
+    assert np.allclose(r.weights, [[1.8, 1.6, 1.2]], rtol=1e-14)
+    # the bias moves the choice, not the weight: expert 0 (s = 0.1) + 1 wins
+    r = o.route_scored(Lp, 3, "sigmoid", True, 1.0, [1.0, 0, 0, 0, 0, 0])
+    assert r.ids.tolist() == [[0, 5, 4]] and np.allclose(r.weights, [[0.1 / 1.8, 0.9 / 1.8, 0.8 / 1.8]], rtol=1e-14)
+    # (3) softmax without renormalisation: the full softmax at the chosen
+    Lq = np.log(np.array([[1.0, 2.0, 3.0, 4.0]]))
+    r = o.route_scored(Lq, 2, "softmax", False, 1.0)
+    assert r.ids.tolist() == [[3, 2]] and np.allclose(r.weights, [[0.4, 0.3]], rtol=1e-14)
+    r = o.route_scored(np.zeros((1, 8)), 3, "softmax", False, 3.0)
+    assert r.ids.tolist() == [[0, 1, 2]] and np.allclose(r.weights, 3.0 / 8, rtol=1e-15)
+    # with renormalisation it is route() (softmax over the chosen logits)
+    ra, rb = o.route(L, 3), o.route_scored(L, 3, "softmax", True, 1.0)
+    assert np.array_equal(ra.ids, rb.ids) and np.allclose(ra.weights, rb.weights, rtol=1e-14, atol=0)
+    # (4) edge cases: NaN never beats a number and weighs 0; s = 0 everywhere -> 1/k each
+    r = o.route_scored(np.array([[np.nan, 0.0, np.nan]]), 2, "sigmoid", True, 1.0)
+    assert r.ids.tolist() == [[1, 0]] and r.weights.tolist() == [[1.0, 0.0]] and r.nan_count == 2
+    r = o.route_scored(np.full((1, 4), -np.inf), 2, "sigmoid", True, 1.0)
+    assert r.ids.tolist() == [[0, 1]] and r.weights.tolist() == [[0.5, 0.5]]
+    r = o.route_scored(np.array([[np.inf, 0.0, np.inf, 1.0]]), 3, "sigmoid", False, 1.0)
+    assert r.ids.tolist() == [[0, 2, 3]] and np.allclose(r.weights, [[1.0, 1.0, 1 / (1 + math.exp(-1))]])
+
+
+def pin_router_logits(o):
+    # closed form: x = 1, row e of W constant c_e -> logit e = H * c_e
+    H, E = 64, 5
+    c = np.array([0.5, -1.0, 2.0, 0.25, -0.125])
+    out = o.router_logits(_bf16_bits(np.ones((2, H))), _bf16_bits(np.repeat(c[:, None], H, axis=1)))
+    assert np.all(out == H * c[None, :])
+    # brute force: scalar loops, E != H so a transposed product cannot pass
+    rng = np.random.default_rng(8)
+    T, E, H = 3, 5, 24
+    xb, wb = _bf16_bits(rng.standard_normal((T, H))), _bf16_bits(rng.standard_normal((E, H)))
+    out = o.router_logits(xb, wb)
+    f = lambda bits: [float(v) for v in (bits.astype(np.uint32) << 16).view(np.float32)]
+    for t in range(T):
+        xs = f(xb[t])
+        for e in range(E):
+            ws = f(wb[e])
+            assert abs(out[t, e] - math.fsum(a * b for a, b in zip(xs, ws))) <= 1e-12
+
+
 PINS = [pin_e2m1_table, pin_e4m3, pin_dequant_worked, pin_round_trip, pin_route,
         pin_permute, pin_ffn_closed_form, pin_identical_experts, pin_top1_dense,
-        pin_brute_force_layer, pin_shared_expert, pin_linear]
+        pin_brute_force_layer, pin_shared_expert, pin_linear, pin_route_scored, pin_router_logits]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -480,7 +552,54 @@ def _mut_linear_no_gscale(m):
     m.linear_forward = lambda x_bits, w_q, w_s, gscale: orig(x_bits, w_q, w_s, 1.0)
 
 
-MUTANTS = [_mut_linear_transposed, _mut_linear_no_gscale, _mut_nibble_order, _mut_e4m3_bias, _mut_e2m1_subnormal, _mut_scale_group_shift,
+def _mut_bias_in_weights(m):  # the selection bias leaks into the weights
+    orig = m.route_scored
+    def f(logits, k, score="softmax", renormalize=True, scale=1.0, bias=None):
+        r = orig(logits, k, score, renormalize, scale, bias)
+        if bias is not None and score == "sigmoid":
+            L = np.asarray(logits, dtype=np.float64)
+            s = 1.0 / (1.0 + np.exp(-np.take_along_axis(L, r.ids.astype(np.int64), axis=1)))
+            ws = s + np.asarray(bias, dtype=np.float64)[r.ids]
+            r.weights = scale * (ws / ws.sum(axis=1, keepdims=True) if renormalize else ws)
+        return r
+    m.route_scored = f
+
+
+def _mut_select_without_bias(m):
+    orig = m.route_scored
+    m.route_scored = lambda logits, k, score="softmax", renormalize=True, scale=1.0, bias=None: orig(
+        logits, k, score, renormalize, scale, None)
+
+
+def _mut_ignore_renormalize(m):
+    orig = m.route_scored
+    m.route_scored = lambda logits, k, score="softmax", renormalize=True, scale=1.0, bias=None: orig(
+        logits, k, score, True, scale, bias)
+
+
+def _mut_ignore_scale(m):
+    orig = m.route_scored
+    m.route_scored = lambda logits, k, score="softmax", renormalize=True, scale=1.0, bias=None: orig(
+        logits, k, score, renormalize, 1.0, bias)
+
+
+def _mut_sigmoid_as_softmax(m):
+    orig = m.route_scored
+    m.route_scored = lambda logits, k, score="softmax", renormalize=True, scale=1.0, bias=None: orig(
+        logits, k, "softmax", renormalize, scale, bias)
+
+
+def _mut_router_transposed(m):  # logits from the first E columns of W^T-shaped product
+    def f(x_bits, w_bits):
+        x = m.bf16_bits_to_f64(np.asarray(x_bits))
+        W = m.bf16_bits_to_f64(np.asarray(w_bits))
+        E = W.shape[0]
+        return x[:, :E] @ W[:, :E].T if x.shape[1] >= E else x @ W.T
+    m.router_logits = f
+
+
+MUTANTS = [_mut_bias_in_weights, _mut_select_without_bias, _mut_ignore_renormalize, _mut_ignore_scale,
+           _mut_sigmoid_as_softmax, _mut_router_transposed, _mut_linear_transposed, _mut_linear_no_gscale, _mut_nibble_order, _mut_e4m3_bias, _mut_e2m1_subnormal, _mut_scale_group_shift,
            _mut_gate_up_swap, _mut_drop_up_scale, _mut_tie_break, _mut_softmax_all,
            _mut_no_combine_weights, _mut_silu_sign, _mut_perm_unstable, _mut_shared_dropped,
            _mut_shared_routed_weight]
