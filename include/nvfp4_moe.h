@@ -61,6 +61,11 @@ typedef enum nvfp4_moe_out_dtype {
   NVFP4_MOE_OUT_F32 = 1        /* the FP32 combine result, unrounded      */
 } nvfp4_moe_out_dtype;
 
+typedef enum nvfp4_moe_score {
+  NVFP4_MOE_SCORE_SOFTMAX = 0,
+  NVFP4_MOE_SCORE_SIGMOID = 1
+} nvfp4_moe_score;
+
 typedef enum nvfp4_moe_path {
   NVFP4_MOE_PATH_AUTO = 0,     /* T <= decode_max_tokens -> decode, else prefill */
   NVFP4_MOE_PATH_DECODE = 1,   /* grouped GEMV, dequantised in registers          */
@@ -179,6 +184,24 @@ nvfp4_moe_status nvfp4_moe_forward_decode_static(const uint8_t* packed_experts, 
                                                  int num_experts, int hidden, int inter,
                                                  const void* router_logits, int logits_dtype, int T, int top_k,
                                                  const void* x, void* out, cudaStream_t stream);
+
+/* Scoring rule of the route step (the router variants).  The pages keep the
+ * routers as BF16 linears and do not state how their outputs become choices
+ * and weights ("GLM-5.3-Flash on Blackwell", The quantization); the default
+ * is softmax over the k chosen logits.  With s_e = softmax over all experts
+ * (NVFP4_MOE_SCORE_SOFTMAX) or sigmoid(l_e) (NVFP4_MOE_SCORE_SIGMOID):
+ *   choice : the k largest s_e + bias_e (bias NULL: the k largest logits,
+ *            the same order), equal values -> lower expert index, NaN last;
+ *   weights: the chosen s_e (never the bias); renormalize = 1 divides them
+ *            by their sum over the k slots (softmax: the default rule;
+ *            sigmoid: 1/k each if the sum is 0); then times scale.
+ * bias: DEVICE float [num_experts] or NULL, copied on `stream` (the copy is
+ * ordered before later forwards on that stream); scale finite and > 0.  A
+ * shared expert keeps weight 1 under every rule.  Applies to later forwards
+ * and nvfp4_moe_debug_route; a dense-linear handle returns
+ * NVFP4_MOE_ERR_INVALID_ARG. */
+nvfp4_moe_status nvfp4_moe_set_scoring(nvfp4_moe_t h, int score_func, int renormalize, float scale,
+                                       const float* bias, cudaStream_t stream);
 
 /* Per-stage timing.  With profiling on, every forward records CUDA events on
  * its stream before and after each stage.  nvfp4_moe_get_stage_times

@@ -21,6 +21,7 @@ STATUS = {
 }
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
+SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 HEADER = os.path.join(ROOT, "include", "nvfp4_moe.h")
 
 
@@ -82,6 +83,7 @@ def load_library(path: str | None = None):
         "nvfp4_moe_debug_trace": (i, [vp, ctypes.POINTER(ctypes.c_uint64), ctypes.c_size_t,
                                       ctypes.POINTER(ctypes.c_size_t)]),
         "nvfp4_moe_get_stage_times": (i, [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
+        "nvfp4_moe_set_scoring": (i, [vp, i, i, f, vp, vp]),
         "nvfp4_linear_create": (i, [ctypes.POINTER(LinearConfig), ctypes.POINTER(vp)]),
         "nvfp4_linear_pack": (i, [vp, vp, vp, vp, vp]),
         "nvfp4_linear_forward": (i, [vp, i, vp, vp, vp]),
@@ -223,6 +225,13 @@ class MoELayer:
         n = ctypes.c_int(0)
         self._check(self.lib.nvfp4_moe_get_stage_times(self.h, ms, ctypes.byref(n)), "nvfp4_moe_get_stage_times")
         return [float(v) for v in ms], int(n.value)
+
+    def nvfp4_moe_set_scoring(self, score="softmax", renormalize=True, scale=1.0, bias=None, stream=None):
+        """score: "softmax" | "sigmoid"; bias: a CUDA float32 tensor [num_experts] or None."""
+        code = {"softmax": SCORE_SOFTMAX, "sigmoid": SCORE_SIGMOID}[score]
+        st = self.lib.nvfp4_moe_set_scoring(self.h, code, 1 if renormalize else 0, float(scale), _ptr(bias),
+                                            _stream(stream))
+        self._check(st, "nvfp4_moe_set_scoring")
 
     def nvfp4_moe_debug_set_fault(self, fault):
         self._check(self.lib.nvfp4_moe_debug_set_fault(self.h, fault), "nvfp4_moe_debug_set_fault")

@@ -18,6 +18,8 @@ struct nvfp4_moe {
   nvfp4_moe_config cfg;
   bool linear = false;  // a dense linear (nvfp4_linear_create): cfg holds E = 1, hidden = N padded to 128, inter = K
   int lin_n = 0;        // a dense linear's N (output features)
+  RouteParams rp{};     // scoring rule (nvfp4_moe_set_scoring); rp.bias points at `bias` when set
+  float* bias = nullptr;  // [num_experts] device copy of the choice bias
   int path = NVFP4_MOE_PATH_AUTO;
   int num_sms = 0;
   bool packed = false;
@@ -139,9 +141,11 @@ nvfp4_moe_status check_forward_args(nvfp4_moe* h, const void* logits, int T, int
 }
 
 LayerDims dims_of(const nvfp4_moe* h) {
-  return LayerDims{h->cfg.num_experts + h->cfg.num_shared_experts, h->cfg.hidden, h->cfg.inter,
-                   h->cfg.logits_dtype == NVFP4_MOE_LOGITS_BF16, h->cfg.out_dtype == NVFP4_MOE_OUT_F32,
-                   h->cfg.num_experts, h->cfg.num_shared_experts, h->linear ? 1 : 0, h->lin_n};
+  LayerDims d{h->cfg.num_experts + h->cfg.num_shared_experts, h->cfg.hidden, h->cfg.inter,
+              h->cfg.logits_dtype == NVFP4_MOE_LOGITS_BF16, h->cfg.out_dtype == NVFP4_MOE_OUT_F32,
+              h->cfg.num_experts, h->cfg.num_shared_experts, h->linear ? 1 : 0, h->lin_n};
+  d.rp = h->rp;
+  return d;
 }
 
 size_t blob_bytes_of(const nvfp4_moe_config& c, bool linear) {
@@ -289,7 +293,7 @@ nvfp4_moe_status create_handle(const nvfp4_moe_config* c, bool linear, int lin_n
   h->ws_bytes = cv.layout();
 
   if (cudaMalloc(&h->blob, blob_bytes) != cudaSuccess || cudaMalloc(&h->gscale, sizeof(float) * 3 * E) != cudaSuccess ||
-      cudaMalloc(&h->ws_mem, h->ws_bytes) != cudaSuccess) {
+      cudaMalloc(&h->bias, sizeof(float) * E) != cudaSuccess || cudaMalloc(&h->ws_mem, h->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
     nvfp4_moe_destroy(h);
     return NVFP4_MOE_ERR_WORKSPACE;
@@ -318,6 +322,7 @@ void nvfp4_moe_destroy(nvfp4_moe_t h) {
     for (cudaEvent_t ev : h->ev_pool) cudaEventDestroy(ev);
     if (h->blob) cudaFree(h->blob);
     if (h->gscale) cudaFree(h->gscale);
+    if (h->bias) cudaFree(h->bias);
     if (h->ws_mem) cudaFree(h->ws_mem);
   }
   delete h;
@@ -353,6 +358,27 @@ nvfp4_moe_status nvfp4_moe_get_stage_times(nvfp4_moe_t h, float* ms, int* count)
     }
   *count = n;
   h->ev_used = 0;
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_moe_set_scoring(nvfp4_moe_t h, int score_func, int renormalize, float scale,
+                                       const float* bias, cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (h->linear) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "set_scoring: a dense linear has no routing");
+  if (score_func != NVFP4_MOE_SCORE_SOFTMAX && score_func != NVFP4_MOE_SCORE_SIGMOID)
+    return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "set_scoring: unknown score function");
+  if (renormalize != 0 && renormalize != 1) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "set_scoring: renormalize is 0 or 1");
+  if (!(scale > 0.0f) || scale > 3.4e38f) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "set_scoring: scale must be finite > 0");
+  if (bias && !aligned(bias, 4)) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "set_scoring: bias misaligned");
+  DeviceGuard g(h->cfg.device);
+  if (bias) {
+    cudaError_t e = cudaMemcpyAsync(h->bias, bias, sizeof(float) * h->cfg.num_experts, cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "set_scoring: bias copy");
+  }
+  h->rp.score = score_func;
+  h->rp.renorm = renormalize;
+  h->rp.scale = scale;
+  h->rp.bias = bias ? h->bias : nullptr;
   return NVFP4_MOE_OK;
 }
 

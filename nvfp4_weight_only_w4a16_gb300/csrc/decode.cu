@@ -87,6 +87,7 @@ struct FusedArgs {
   int E, H, I, T, k;  // E experts (routed + shared), k slots per token (top_k + shared)
   int Er, topk;       // routed experts (logits per token), routed choices per token
   int linear;         // 1: a dense linear: no routing, no gate/up; x [T][I] feeds the down GEMV
+  RouteParams rp;     // scoring rule of the route step
   int n_out;          // a dense linear's output features (<= H; rows past it are padding)
   const void* logits;
   int logits_bf16;
@@ -250,8 +251,11 @@ __device__ void route_block(const FusedArgs& a, RouteSmem& rs, uint8_t* xs, unsi
   } else if (warp < T) {
     int id;
     float logit;
+    SoftmaxStats sst{0.f, 0.f, 0};
+    if (a.rp.score == 0 && (a.rp.bias || !a.rp.renorm)) sst = warp_softmax_stats(val, Er);
+    warp_bias_keys(a.rp, Er, val, key, sst);
     const int nt = warp_select_topk(key, val, Er, topk, &id, &logit);
-    const float w = warp_softmax_k(logit, topk);
+    const float w = warp_route_weight(a.rp, logit, topk, Er, sst);
     if (lane < topk) {
       rs.ids[warp * k + lane] = id;
       rs.wts[warp * k + lane] = w;
@@ -1138,6 +1142,7 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
   a.topk = k;
   a.linear = d.linear;
   a.n_out = d.n_out;
+  a.rp = d.rp;
   a.logits = logits;
   a.logits_bf16 = d.logits_bf16;
   a.x = reinterpret_cast<const __nv_bfloat16*>(x);

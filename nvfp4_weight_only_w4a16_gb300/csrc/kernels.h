@@ -43,6 +43,14 @@ struct Workspace {
   unsigned long long* trace;  // optional per-warp phase stamps of the decode kernel (NVFP4_MOE_TRACE=1)
 };
 
+// The route step's scoring rule (defaults: softmax over the chosen logits).
+struct RouteParams {
+  int score = 0;                 // 0: softmax over all experts, 1: sigmoid
+  int renorm = 1;                // divide the chosen weights by their sum
+  float scale = 1.0f;            // every final weight times this
+  const float* bias = nullptr;   // [Er] device, added to the scores for the choice only
+};
+
 struct LayerDims {
   int E, H, I;     // E: experts in the blob (routed + shared)
   int logits_bf16;
@@ -53,6 +61,7 @@ struct LayerDims {
                    // no routing and no gate/up; x [T][I] is the down GEMM's input
   int n_out;       // a dense linear's output features N <= H (H = N rounded up to 128; the
                    // padded rows are zero): out is [T][n_out]
+  RouteParams rp;  // scoring rule of the route step
 };
 
 constexpr int kRankTokens = 256;      // tokens per rank block in the prefill routing

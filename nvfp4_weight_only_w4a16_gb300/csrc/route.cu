@@ -16,7 +16,7 @@ namespace nvfp4moe {
 // token has k slots: its topk routed choices over the Er routed experts, then
 // (k > topk) the shared expert, id Er, with weight 1.
 __global__ void __launch_bounds__(256) route_topk_kernel(const void* __restrict__ logits, int bf16, int T, int k,
-                                                         int topk, int Er, Workspace ws) {
+                                                         int topk, int Er, RouteParams rp, Workspace ws) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int nan_total = 0;
   {
@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const void* __restrict_
     if (t >= T) return;
     int id;
     float w;
-    nan_total += warp_topk(logits, bf16, Er, topk, t, &id, &w);
+    nan_total += warp_topk(logits, bf16, Er, topk, t, rp, &id, &w);
     if (lane < topk) {
       ws.ids[(size_t)t * k + lane] = id;
       ws.wts[(size_t)t * k + lane] = w;
@@ -131,7 +131,7 @@ cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const v
                                  const Workspace& ws, cudaStream_t st) {
   const int nrb = (T + kRankTokens - 1) / kRankTokens;
   const int k = top_k + d.S;  // slots per token
-  route_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, d.logits_bf16, T, k, top_k, d.Er, ws);
+  route_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, d.logits_bf16, T, k, top_k, d.Er, d.rp, ws);
   route_rank_kernel<<<nrb, 256, 0, st>>>(T, k, d.E, ws);
   route_scan_kernel<<<1, 1024, 0, st>>>(nrb, d.E, ws);
   const size_t rows = (size_t)T * k;

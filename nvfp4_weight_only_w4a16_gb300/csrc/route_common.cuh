@@ -8,6 +8,7 @@
 // The quantization), so their logits are this layer's input.
 #pragma once
 #include "common.cuh"
+#include "kernels.h"
 
 namespace nvfp4moe {
 
@@ -103,16 +104,106 @@ __device__ __forceinline__ int warp_select_topk(const uint32_t (&key)[8], const 
   return (int)__reduce_add_sync(0xffffffffu, (unsigned)nan);
 }
 
+// ---------------------------------------------------------------------------
+// Scoring variants (RouteParams).  s_e = softmax over all E logits, or
+// sigmoid(l_e).  The choice runs on s_e + bias_e when a bias is given, else
+// on the logits themselves (both scores are strictly increasing in the logit,
+// so that is their exact order).  Weights: the chosen s (no bias), divided by
+// their sum over the k slots when renorm (softmax: softmax over the chosen
+// logits; sigmoid: 1/k each if the sum is 0), then times scale.  NaN logits
+// count as -inf in the scores.
+// ---------------------------------------------------------------------------
+struct SoftmaxStats {
+  float m;    // max logit (NaN as -inf)
+  float sum;  // sum of exp(l - m) over all E (m finite)
+  int ninf;   // logits equal to +inf
+};
+
+__device__ __forceinline__ SoftmaxStats warp_softmax_stats(const float (&val)[8], int E) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY;
+  int ninf = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (lane + 32 * i < E && val[i] == val[i]) {
+      m = fmaxf(m, val[i]);
+      ninf += val[i] == INFINITY;
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float sum = 0.f;
+  if (m != INFINITY && m != -INFINITY) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (lane + 32 * i < E && val[i] == val[i]) sum += expf(val[i] - m);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  return SoftmaxStats{m, sum, (int)__reduce_add_sync(0xffffffffu, (unsigned)ninf)};
+}
+
+// s of one logit under the full softmax (stats over all E experts)
+__device__ __forceinline__ float softmax_score(float l, const SoftmaxStats& st, int E) {
+  if (l != l) return 0.f;
+  if (st.m == -INFINITY) return 1.0f / (float)E;
+  if (st.m == INFINITY) return l == INFINITY ? 1.0f / (float)st.ninf : 0.f;
+  return expf(l - st.m) / st.sum;
+}
+
+__device__ __forceinline__ float sigmoid_score(float l) {
+  if (l != l) return 0.f;
+  return 1.0f / (1.0f + expf(-l));
+}
+
+// With a bias, re-key the warp's logits by s_e + bias_e (NaN logits keep the
+// lowest key).  Without one the logit keys stand.
+__device__ __forceinline__ void warp_bias_keys(const RouteParams& rp, int E, const float (&val)[8],
+                                               uint32_t (&key)[8], const SoftmaxStats& st) {
+  if (!rp.bias) return;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E && val[i] == val[i]) {
+      const float sc = rp.score ? sigmoid_score(val[i]) : softmax_score(val[i], st, E);
+      key[i] = float_key(sc + __ldg(rp.bias + e));
+    }
+  }
+}
+
+// Lane j < k holds its chosen logit; returns its final weight (all lanes call).
+__device__ __forceinline__ float warp_route_weight(const RouteParams& rp, float logit, int k, int E,
+                                                   const SoftmaxStats& st) {
+  const int lane = threadIdx.x & 31;
+  float w;
+  if (rp.score == 0 && rp.renorm) {
+    w = warp_softmax_k(logit, k);
+  } else {
+    float s = 0.f;
+    if (lane < k) s = rp.score ? sigmoid_score(logit) : softmax_score(logit, st, E);
+    w = s;
+    if (rp.renorm) {
+      float sum = 0.f;
+      for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, s, j);
+      w = sum > 0.f ? s / sum : 1.0f / (float)k;
+    }
+  }
+  return w * rp.scale;
+}
+
 // One warp routes token t (E <= 256, k <= 16).  Lane j < k receives the j-th
 // choice in (*my_id, *my_w); returns the number of NaN logits of the token.
-__device__ __forceinline__ int warp_topk(const void* logits, int bf16, int E, int k, int t, int* my_id,
-                                         float* my_w) {
+__device__ __forceinline__ int warp_topk(const void* logits, int bf16, int E, int k, int t, const RouteParams& rp,
+                                         int* my_id, float* my_w) {
   uint32_t key[8];
   float val[8];
   warp_load_logits(logits, bf16, E, t, key, val);
+  SoftmaxStats st{0.f, 0.f, 0};
+  if (rp.score == 0 && (rp.bias || !rp.renorm)) st = warp_softmax_stats(val, E);
+  warp_bias_keys(rp, E, val, key, st);
   float logit;
   const int nan = warp_select_topk(key, val, E, k, my_id, &logit);
-  *my_w = warp_softmax_k(logit, k);
+  *my_w = warp_route_weight(rp, logit, k, E, st);
   return nan;
 }
 
