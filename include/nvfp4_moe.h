@@ -203,6 +203,28 @@ nvfp4_moe_status nvfp4_moe_forward_decode_static(const uint8_t* packed_experts, 
 nvfp4_moe_status nvfp4_moe_set_scoring(nvfp4_moe_t h, int score_func, int renormalize, float scale,
                                        const float* bias, cudaStream_t stream);
 
+/* The router linear inside the library.  The routers stay BF16 linears
+ * ("GLM-5.3-Flash on Blackwell", The quantization; "tenhkspark/GLM-5.3-Flash-
+ * NVFP4-Wabi", Config expectations: the mlp.gate routers are excluded from
+ * quantisation), so their logits can be computed here instead of passed in:
+ *   nvfp4_moe_set_router copies w_router, DEVICE BF16 [num_experts][hidden]
+ *   (16-byte aligned), into the handle (allocates once, then reuses; ordered
+ *   on `stream`);
+ *   nvfp4_moe_forward_routed is nvfp4_moe_forward with
+ *   logits[t][e] = sum_h x[t][h] * w_router[e][h], accumulated in FP32 (no
+ *   linear bias), computed on the GPU first: a GEMV kernel for T <= 16, the
+ *   tcgen05 GEMM for larger T (its TMA descriptor over x is encoded on the
+ *   host each call, so a captured graph replays with the x it was captured
+ *   with).  Its time counts as route + permute in the stage times.
+ *   nvfp4_moe_debug_logits copies the last forward_routed's logits
+ *   [T][num_experts] FP32 to a DEVICE buffer.
+ * NVFP4_MOE_ERR_INVALID_ARG: forward_routed before set_router, or a dense-
+ * linear handle. */
+nvfp4_moe_status nvfp4_moe_set_router(nvfp4_moe_t h, const void* w_router, cudaStream_t stream);
+nvfp4_moe_status nvfp4_moe_forward_routed(nvfp4_moe_t h, int T, int top_k, const void* x, void* out,
+                                          cudaStream_t stream);
+nvfp4_moe_status nvfp4_moe_debug_logits(nvfp4_moe_t h, float* logits, cudaStream_t stream);
+
 /* Per-stage timing.  With profiling on, every forward records CUDA events on
  * its stream before and after each stage.  nvfp4_moe_get_stage_times
  * (synchronous) returns in ms[0..3] the summed milliseconds of route+permute,

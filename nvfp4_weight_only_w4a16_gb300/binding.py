@@ -84,6 +84,9 @@ def load_library(path: str | None = None):
                                       ctypes.POINTER(ctypes.c_size_t)]),
         "nvfp4_moe_get_stage_times": (i, [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
         "nvfp4_moe_set_scoring": (i, [vp, i, i, f, vp, vp]),
+        "nvfp4_moe_set_router": (i, [vp, vp, vp]),
+        "nvfp4_moe_forward_routed": (i, [vp, i, i, vp, vp, vp]),
+        "nvfp4_moe_debug_logits": (i, [vp, vp, vp]),
         "nvfp4_linear_create": (i, [ctypes.POINTER(LinearConfig), ctypes.POINTER(vp)]),
         "nvfp4_linear_pack": (i, [vp, vp, vp, vp, vp]),
         "nvfp4_linear_forward": (i, [vp, i, vp, vp, vp]),
@@ -232,6 +235,26 @@ class MoELayer:
         st = self.lib.nvfp4_moe_set_scoring(self.h, code, 1 if renormalize else 0, float(scale), _ptr(bias),
                                             _stream(stream))
         self._check(st, "nvfp4_moe_set_scoring")
+
+    def nvfp4_moe_set_router(self, w_router, stream=None):
+        """w_router: a CUDA BF16 tensor [num_experts][hidden]."""
+        self._check(self.lib.nvfp4_moe_set_router(self.h, _ptr(w_router), _stream(stream)), "nvfp4_moe_set_router")
+
+    def nvfp4_moe_forward_routed(self, x, top_k, out, stream=None):
+        st = self.lib.nvfp4_moe_forward_routed(self.h, x.shape[0], top_k, _ptr(x), _ptr(out), _stream(stream))
+        self._check(st, "nvfp4_moe_forward_routed")
+        return out
+
+    def nvfp4_moe_forward_routed_raw(self, T, top_k, x_ptr, out_ptr, stream_handle):
+        """Pointer-level call (for benchmarks that time the bare ABI)."""
+        return self.lib.nvfp4_moe_forward_routed(self.h, T, top_k, ctypes.c_void_p(x_ptr), ctypes.c_void_p(out_ptr),
+                                                 ctypes.c_void_p(stream_handle))
+
+    def nvfp4_moe_debug_logits(self, T, stream=None):
+        import torch
+        out = torch.empty((T, self.E), dtype=torch.float32, device=f"cuda:{self.device}")
+        self._check(self.lib.nvfp4_moe_debug_logits(self.h, _ptr(out), _stream(stream)), "nvfp4_moe_debug_logits")
+        return out
 
     def nvfp4_moe_debug_set_fault(self, fault):
         self._check(self.lib.nvfp4_moe_debug_set_fault(self.h, fault), "nvfp4_moe_debug_set_fault")

@@ -20,6 +20,9 @@ struct nvfp4_moe {
   int lin_n = 0;        // a dense linear's N (output features)
   RouteParams rp{};     // scoring rule (nvfp4_moe_set_scoring); rp.bias points at `bias` when set
   float* bias = nullptr;  // [num_experts] device copy of the choice bias
+  void* w_router = nullptr;  // [num_experts][hidden] BF16 router weight (nvfp4_moe_set_router)
+  CUtensorMap w_router_map{};  // over w_router, box {64, 128}, 128B swizzle
+  bool have_router = false;
   int path = NVFP4_MOE_PATH_AUTO;
   int num_sms = 0;
   bool packed = false;
@@ -32,6 +35,7 @@ struct nvfp4_moe {
   Workspace ws{};
   PrefillMaps maps{};
   int last_T = 0, last_k = 0;
+  bool last_routed = false;
   int fault = 0;
   bool profiling = false;
   std::vector<cudaEvent_t> ev_pool;  // 5 events per profiled forward
@@ -80,13 +84,13 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2D BF16 [rows][cols] row-major, box = 64 columns x 16 rows, 128B swizzle.
-bool encode_rows_map(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols) {
+// 2D BF16 [rows][cols] row-major, box = 64 columns x box_rows rows, 128B swizzle.
+bool encode_rows_map(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols, uint32_t box_rows = 16) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 16};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -172,8 +176,9 @@ nvfp4_moe_status take_events(nvfp4_moe* h, cudaEvent_t (&ev)[5]) {
 }
 
 nvfp4_moe_status run_route(nvfp4_moe* h, const void* logits, const void* x, int T, int k, int path,
-                           cudaStream_t st) {
-  const LayerDims d = dims_of(h);
+                           cudaStream_t st, int logits_bf16 = -1) {
+  LayerDims d = dims_of(h);
+  if (logits_bf16 >= 0) d.logits_bf16 = logits_bf16;
   cudaError_t e = path == NVFP4_MOE_PATH_DECODE
                       ? launch_decode_forward(d, h->blob, h->gscale, logits, nullptr, T, k, nullptr, 1, h->num_sms,
                                               h->ws, st)
@@ -249,7 +254,8 @@ nvfp4_moe_status create_handle(const nvfp4_moe_config* c, bool linear, int lin_n
   const size_t Rm = R < 256 ? 256 : R;
   const size_t maxU = (size_t)std::min(E, kDecodeMaxTokens * K);
   const size_t ncta = ((size_t)c->max_tokens + kRankTokens - 1) / kRankTokens;
-  const size_t max_tiles = R / kTileRows + E + 1;
+  // m-tiles: the MoE's (<= R/128 + E + 1) and the router GEMM's (<= one per SM)
+  const size_t max_tiles = std::max(R / kTileRows + E + 1, (size_t)h->num_sms + 2);
   const size_t blob_bytes = blob_bytes_of(*c, linear);
   // a dense linear reads x and writes out directly: no permuted copies, no
   // hidden rows, no FP32 expert outputs
@@ -287,6 +293,8 @@ nvfp4_moe_status create_handle(const nvfp4_moe_config* c, bool linear, int lin_n
   cv.add(&w.tile_rows, max_tiles);
   cv.add(&w.num_tiles, 1);
   cv.add(&w.status, 1);
+  cv.add(&w.logits, linear ? 1 : (size_t)c->max_tokens * c->num_experts);
+  cv.add(&w.ones3, 3);
   const char* tr = getenv("NVFP4_MOE_TRACE");
   const bool trace = tr && tr[0] == '1';
   if (trace) cv.add(&w.trace, (size_t)h->num_sms * 16 * 16);
@@ -299,7 +307,9 @@ nvfp4_moe_status create_handle(const nvfp4_moe_config* c, bool linear, int lin_n
     return NVFP4_MOE_ERR_WORKSPACE;
   }
   cv.assign(static_cast<uint8_t*>(h->ws_mem));
-  if (cudaMemset(h->ws_mem, 0, h->ws_bytes) != cudaSuccess) {
+  const float ones[3] = {1.0f, 1.0f, 1.0f};
+  if (cudaMemset(h->ws_mem, 0, h->ws_bytes) != cudaSuccess ||
+      cudaMemcpy(w.ones3, ones, sizeof(ones), cudaMemcpyHostToDevice) != cudaSuccess) {
     nvfp4_moe_destroy(h);
     return NVFP4_MOE_ERR_CUDA;
   }
@@ -323,6 +333,7 @@ void nvfp4_moe_destroy(nvfp4_moe_t h) {
     if (h->blob) cudaFree(h->blob);
     if (h->gscale) cudaFree(h->gscale);
     if (h->bias) cudaFree(h->bias);
+    if (h->w_router) cudaFree(h->w_router);
     if (h->ws_mem) cudaFree(h->ws_mem);
   }
   delete h;
@@ -417,15 +428,24 @@ nvfp4_moe_status nvfp4_moe_pack(nvfp4_moe_t h, const uint8_t* w13_q, const uint8
   return NVFP4_MOE_OK;
 }
 
-nvfp4_moe_status nvfp4_moe_forward(nvfp4_moe_t h, const void* logits, int T, int top_k, const void* x, void* out,
-                                   cudaStream_t st) {
-  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+// One forward.  routed: the logits are computed here from x and the router
+// weight (into the workspace) instead of being passed in.
+nvfp4_moe_status forward_impl(nvfp4_moe* h, const void* logits, int T, int top_k, const void* x, void* out,
+                              cudaStream_t st, bool routed) {
   const int path = choose_path(h, T, top_k);
-  nvfp4_moe_status s = check_forward_args(h, logits, T, top_k, path);
+  nvfp4_moe_status s = check_forward_args(h, routed ? h->ws.logits : logits, T, top_k, path);
   if (s != NVFP4_MOE_OK) return s;
   if (!x || !out) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "x or out is NULL");
   if (!aligned(x, 16) || !aligned(out, 16)) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "x or out not 16-byte aligned");
+  if (routed && !h->have_router) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "forward_routed before set_router");
   DeviceGuard g(h->cfg.device);
+  CUtensorMap x_map{};
+  if (routed && T > kDecodeMaxTokens &&
+      !encode_rows_map(&x_map, const_cast<void*>(x), (uint64_t)T, (uint64_t)h->cfg.hidden))
+    return fail(h, NVFP4_MOE_ERR_CUDA, "forward_routed: cuTensorMapEncodeTiled failed for x");
   if (h->log && !h->logged_path[path]) {
     h->logged_path[path] = true;
     fprintf(stderr, "[nvfp4_moe] forward T=%d top_k=%d -> %s path\n", T, top_k,
@@ -435,8 +455,24 @@ nvfp4_moe_status nvfp4_moe_forward(nvfp4_moe_t h, const void* logits, int T, int
   s = take_events(h, ev);
   if (s != NVFP4_MOE_OK) return s;
   if (ev[0]) cudaEventRecord(ev[0], st);
-  const LayerDims d = dims_of(h);
+  LayerDims d = dims_of(h);
   cudaError_t e;
+  if (routed) {  // the router linear, timed with route + permute
+    const int Er = h->cfg.num_experts, H = h->cfg.hidden;
+    if (T <= kDecodeMaxTokens) {
+      e = launch_router_gemv(x, h->w_router, T, Er, H, h->ws.logits, st);
+    } else {
+      // token tiles small enough to give every SM a unit (16..128 rows)
+      int rows = (T + h->num_sms - 1) / h->num_sms;
+      rows = std::min(kTileRows, std::max(16, (rows + 15) / 16 * 16));
+      e = launch_route_linear(T, rows, h->ws, st);
+      if (e == cudaSuccess)
+        e = launch_router_gemm(x_map, h->w_router_map, Er, H, h->num_sms, h->ws.ones3, h->ws, h->ws.logits, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(h, e, "router launch");
+    logits = h->ws.logits;
+    d.logits_bf16 = 0;
+  }
   if (path == NVFP4_MOE_PATH_DECODE) {
     // one fused kernel: its time is reported as the gate/up stage
     if (ev[1]) cudaEventRecord(ev[1], st);
@@ -445,7 +481,7 @@ nvfp4_moe_status nvfp4_moe_forward(nvfp4_moe_t h, const void* logits, int T, int
     if (ev[2]) cudaEventRecord(ev[2], st);
     if (ev[3]) cudaEventRecord(ev[3], st);
   } else {
-    s = run_route(h, logits, x, T, top_k, path, st);
+    s = run_route(h, logits, x, T, top_k, path, st, d.logits_bf16);
     if (s != NVFP4_MOE_OK) return s;
     if (ev[1]) cudaEventRecord(ev[1], st);
     e = launch_prefill_ffn(d, h->blob, h->gscale, T, top_k, h->num_sms, h->maps, h->ws, h->fault, ev[2],
@@ -458,6 +494,53 @@ nvfp4_moe_status nvfp4_moe_forward(nvfp4_moe_t h, const void* logits, int T, int
   if (ev[4]) cudaEventRecord(ev[4], st);
   h->last_T = T;
   h->last_k = top_k + h->cfg.num_shared_experts;  // routed-row slots per token
+  h->last_routed = routed;
+  return NVFP4_MOE_OK;
+}
+}  // namespace
+
+extern "C" {
+
+nvfp4_moe_status nvfp4_moe_forward(nvfp4_moe_t h, const void* logits, int T, int top_k, const void* x, void* out,
+                                   cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  return forward_impl(h, logits, T, top_k, x, out, st, false);
+}
+
+nvfp4_moe_status nvfp4_moe_set_router(nvfp4_moe_t h, const void* w_router, cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (h->linear) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "set_router: a dense linear has no router");
+  if (!w_router || !aligned(w_router, 16)) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "set_router: NULL or misaligned");
+  DeviceGuard g(h->cfg.device);
+  const size_t n = (size_t)h->cfg.num_experts * h->cfg.hidden * 2;
+  if (!h->w_router && cudaMalloc(&h->w_router, n) != cudaSuccess) {
+    cudaGetLastError();
+    h->w_router = nullptr;
+    return fail(h, NVFP4_MOE_ERR_WORKSPACE, "set_router: device allocation failed");
+  }
+  cudaError_t e = cudaMemcpyAsync(h->w_router, w_router, n, cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "set_router copy");
+  if (!encode_rows_map(&h->w_router_map, h->w_router, (uint64_t)h->cfg.num_experts, (uint64_t)h->cfg.hidden, 128))
+    return fail(h, NVFP4_MOE_ERR_CUDA, "set_router: cuTensorMapEncodeTiled failed");
+  h->have_router = true;
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_moe_forward_routed(nvfp4_moe_t h, int T, int top_k, const void* x, void* out,
+                                          cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  return forward_impl(h, nullptr, T, top_k, x, out, st, true);
+}
+
+nvfp4_moe_status nvfp4_moe_debug_logits(nvfp4_moe_t h, float* logits, cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (!h->last_T || !h->last_routed)
+    return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_logits: no nvfp4_moe_forward_routed yet");
+  if (!logits) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_logits: NULL output");
+  DeviceGuard g(h->cfg.device);
+  cudaError_t e = cudaMemcpyAsync(logits, h->ws.logits, (size_t)h->last_T * h->cfg.num_experts * 4,
+                                  cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "debug_logits copy");
   return NVFP4_MOE_OK;
 }
 
@@ -635,7 +718,7 @@ nvfp4_moe_status nvfp4_linear_forward(nvfp4_moe_t h, int T, const void* x, void*
     e = launch_decode_forward(d, h->blob, h->gscale, nullptr, x, T, 1, out, 0, h->num_sms, h->ws, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "linear decode launch");
   } else {
-    e = launch_route_linear(T, h->ws, st);
+    e = launch_route_linear(T, kTileRows, h->ws, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "linear tables launch");
     if (ev[1]) cudaEventRecord(ev[1], st);
     e = launch_prefill_ffn(d, h->blob, h->gscale, T, 1, h->num_sms, maps, h->ws, h->fault, ev[2], out, st);
@@ -645,6 +728,7 @@ nvfp4_moe_status nvfp4_linear_forward(nvfp4_moe_t h, int T, const void* x, void*
   if (ev[4]) cudaEventRecord(ev[4], st);
   h->last_T = T;
   h->last_k = 1;
+  h->last_routed = false;
   return NVFP4_MOE_OK;
 }
 

@@ -40,6 +40,8 @@ struct Workspace {
   int32_t* tile_rows;
   int32_t* num_tiles;    // [1]
   DeviceStatus* status;
+  float* logits;         // [max_tokens][Er] router logits (nvfp4_moe_forward_routed)
+  float* ones3;          // [3] 1.0f: tensor scales of the BF16 router GEMM
   unsigned long long* trace;  // optional per-warp phase stamps of the decode kernel (NVFP4_MOE_TRACE=1)
 };
 
@@ -92,8 +94,17 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
                                   const Workspace& ws, cudaStream_t st);
 
 // A dense linear's tables: every token to matrix 0 with weight 1, identity
-// perm/inv, offsets {0, T}, and the m-tiles of 128 rows in token order.
-cudaError_t launch_route_linear(int T, const Workspace& ws, cudaStream_t st);
+// perm/inv, offsets {0, T}, and m-tiles of tile_rows (16..128, a multiple of
+// 16) rows in token order.
+cudaError_t launch_route_linear(int T, int tile_rows, const Workspace& ws, cudaStream_t st);
+
+// The router linear logits [T][E] = x [T][H] . W [E][H]^T (BF16 in, FP32 out):
+// a GEMV kernel for T <= 16, else the tcgen05 GEMM over the m-tiles that
+// launch_route_linear wrote (x_map: x [T][H], box {64, 16}; w_map: W [E][H],
+// box {64, 128}; ones3: a device float[3] of ones).
+cudaError_t launch_router_gemv(const void* x, const void* w, int T, int E, int H, float* logits, cudaStream_t st);
+cudaError_t launch_router_gemm(const CUtensorMap& x_map, const CUtensorMap& w_map, int E, int H, int num_sms,
+                               const float* ones3, const Workspace& ws, float* logits, cudaStream_t st);
 
 struct PrefillMaps {
   CUtensorMap x_perm;  // [R][H] bf16, box {64, 16}, 128B swizzle

@@ -208,9 +208,13 @@ __device__ __forceinline__ void dequant_segment(const uint8_t* raw_stage, uint32
   }
 }
 
-template <bool kGateUp>
+// kBf16W: the weights are a plain BF16 matrix (the router): warp 0 moves its
+// 128-row x 64-column tiles straight into the operand ring by TMA (128B
+// swizzle, the layout the dequantisers write), and the dequantisers idle.
+template <bool kGateUp, bool kBf16W = false>
 __global__ void __launch_bounds__(pf::kThreads, 1)
-    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, PrefillArgs a) {
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_w,
+                        PrefillArgs a) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + pf::kBarOff);
@@ -231,7 +235,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       mbar_init(raw_empty + s, pf::kDequantWarps);
     }
     for (int s = 0; s < pf::kAStages; ++s) {
-      mbar_init(a_full + s, pf::kDequantWarps);
+      mbar_init(a_full + s, kBf16W ? 1 : pf::kDequantWarps);
       mbar_init(a_empty + s, 1);
     }
     for (int s = 0; s < pf::kBStages; ++s) {
@@ -263,7 +267,29 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   const int total_units = num_tiles * NP;
   const int nch = a.K / kChunk;
 
-  if (warp == 0) {
+  if (warp == 0 && kBf16W) {
+    if (lane == 0) {
+      // ---------------- weight producer (BF16 weights): TMA tiles into the operand ring ----------------
+      uint32_t ia = 0;
+      for (int unit = blockIdx.x; unit < total_units && !*abort_flag && a.fault != 1; unit += gridDim.x) {
+        const int nb0 = 2 * (unit % NP);
+        const int nblk = nb0 + 1 < a.NB ? 2 : 1;
+        bool ok = true;
+        for (int c = 0; c < nch; ++c, ++ia) {
+          const int sa = ia % pf::kAStages;
+          if (!mbar_wait(a_empty + sa, ((ia / pf::kAStages) & 1u) ^ 1u, abort_flag, a.st, 9)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + pf::kAOff + sa * pf::kAStageBytes;
+          mbar_arrive_expect_tx(a_full + sa, (uint32_t)nblk * (uint32_t)pf::kABlockBytes);
+          for (int j = 0; j < nblk; ++j)  // rows past the matrix read as zeros
+            tma_2d(st + j * pf::kABlockBytes, &tmap_w, c * kChunk, (nb0 + j) * 128, a_full + sa);
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       // ---------------- weight producer: packed codes + scales of both blocks ----------------
       uint32_t it = 0;
@@ -352,6 +378,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       }
       if (!ok) break;
     }
+  } else if (kBf16W && warp < 3 + pf::kDequantWarps) {
+    // BF16 weights: nothing to dequantise
   } else if (warp < 3 + pf::kDequantWarps) {
     // ---------------- dequantisers (256 threads; per chunk, one 16-byte segment of each block) ----------------
     const int tau = threadIdx.x - 96;
@@ -450,21 +478,26 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   }
 }
 
+static cudaError_t set_prefill_attrs() {
+  static bool attr_set = false;
+  if (attr_set) return cudaSuccess;
+  const void* fns[] = {(const void*)prefill_gemm_kernel<true>, (const void*)prefill_gemm_kernel<false>,
+                       (const void*)prefill_gemm_kernel<false, true>};
+  for (const void* f : fns) {
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::kSmemBytes);
+    if (e != cudaSuccess) return e;
+  }
+  attr_set = true;
+  return cudaSuccess;
+}
+
 cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const float* gscale, int T, int k,
                                int num_sms, const PrefillMaps& maps, const Workspace& ws, int fault,
                                cudaEvent_t mid, void* out, cudaStream_t st) {
   (void)T;
   (void)k;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e1 = cudaFuncSetAttribute(prefill_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          pf::kSmemBytes);
-    cudaError_t e2 = cudaFuncSetAttribute(prefill_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          pf::kSmemBytes);
-    if (e1 != cudaSuccess) return e1;
-    if (e2 != cudaSuccess) return e2;
-    attr_set = true;
-  }
+  cudaError_t ea = set_prefill_attrs();
+  if (ea != cudaSuccess) return ea;
   const ExpertLayout L = d.linear ? linear_layout(d.H, d.I) : expert_layout(d.H, d.I);
   PrefillArgs a{};
   a.blob = blob;
@@ -489,7 +522,7 @@ cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const fl
     a.sc_off = L.w13_sc;
     a.K = d.H;
     a.NB = 2 * d.I / 128;
-    prefill_gemm_kernel<true><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(maps.x_perm, a);
+    prefill_gemm_kernel<true><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(maps.x_perm, maps.x_perm, a);
   }
   if (mid) cudaEventRecord(mid, st);
   // down: H rows, K = I
@@ -497,7 +530,30 @@ cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const fl
   a.sc_off = L.w2_sc;
   a.K = d.I;
   a.NB = d.H / 128;
-  prefill_gemm_kernel<false><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(maps.h, a);
+  prefill_gemm_kernel<false><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(maps.h, maps.h, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_gemm(const CUtensorMap& x_map, const CUtensorMap& w_map, int E, int H, int num_sms,
+                               const float* ones3, const Workspace& ws, float* logits, cudaStream_t st) {
+  cudaError_t ea = set_prefill_attrs();
+  if (ea != cudaSuccess) return ea;
+  PrefillArgs a{};
+  a.gscale = ones3;  // "expert" 0, down-projection slot: 1.0
+  a.K = H;
+  a.NB = (E + 127) / 128;
+  a.H = a.NB * 128;
+  a.I = H;
+  a.tile_expert = ws.tile_expert;
+  a.tile_row0 = ws.tile_row0;
+  a.tile_rows = ws.tile_rows;
+  a.num_tiles = ws.num_tiles;
+  a.out = logits;
+  a.out_f32 = 1;
+  a.linear = 1;
+  a.n_out = E;
+  a.st = ws.status;
+  prefill_gemm_kernel<false, true><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(x_map, w_map, a);
   return cudaGetLastError();
 }
 

@@ -140,8 +140,9 @@ cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const v
   return cudaGetLastError();
 }
 
-// A dense linear: identity tables and 128-row m-tiles in token order.
-__global__ void __launch_bounds__(256) route_linear_kernel(int T, Workspace ws) {
+// A dense linear: identity tables and m-tiles of tile_rows (<= 128) rows in
+// token order.
+__global__ void __launch_bounds__(256) route_linear_kernel(int T, int tile_rows, Workspace ws) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < T) {
     ws.ids[i] = 0;
@@ -149,11 +150,11 @@ __global__ void __launch_bounds__(256) route_linear_kernel(int T, Workspace ws) 
     ws.perm[i] = i;
     ws.inv[i] = i;
   }
-  const int ntiles = (T + kTileRows - 1) / kTileRows;
+  const int ntiles = (T + tile_rows - 1) / tile_rows;
   if (i < ntiles) {
     ws.tile_expert[i] = 0;
-    ws.tile_row0[i] = i * kTileRows;
-    ws.tile_rows[i] = min(kTileRows, T - i * kTileRows);
+    ws.tile_row0[i] = i * tile_rows;
+    ws.tile_rows[i] = min(tile_rows, T - i * tile_rows);
   }
   if (i == 0) {
     ws.offsets[0] = 0;
@@ -162,8 +163,63 @@ __global__ void __launch_bounds__(256) route_linear_kernel(int T, Workspace ws) 
   }
 }
 
-cudaError_t launch_route_linear(int T, const Workspace& ws, cudaStream_t st) {
-  route_linear_kernel<<<(T + 255) / 256, 256, 0, st>>>(T, ws);
+cudaError_t launch_route_linear(int T, int tile_rows, const Workspace& ws, cudaStream_t st) {
+  if (tile_rows < 16 || tile_rows > kTileRows || tile_rows % 16) return cudaErrorInvalidValue;
+  const int n = max(T, (T + tile_rows - 1) / tile_rows);
+  route_linear_kernel<<<(n + 255) / 256, 256, 0, st>>>(T, tile_rows, ws);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Router linear for a few tokens (T <= 16): logits[t][e] = x[t] . W[e] in
+// FP32 from BF16 x [T][H] and W [E][H].  One CTA per expert; each thread takes
+// 16-byte pieces of the row (8 columns), the 8 warps' partial sums are added
+// in warp order.  The routers stay BF16 ("GLM-5.3-Flash on Blackwell", The
+// quantization).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) router_gemv_kernel(const __nv_bfloat16* __restrict__ x,
+                                                          const __nv_bfloat16* __restrict__ w, int T, int H,
+                                                          float* __restrict__ logits, int E) {
+  __shared__ float part[8][16];
+  const int e = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float acc[16];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) acc[t] = 0.f;
+  const uint4* wr = reinterpret_cast<const uint4*>(w + (size_t)e * H);
+  for (int p = threadIdx.x; p < H / 8; p += blockDim.x) {
+    const uint4 wv = __ldg(wr + p);
+    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      if (t >= T) break;
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + p);
+      const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[t] = fmaf(__uint_as_float(xx[q] << 16), __uint_as_float(ww[q] << 16), acc[t]);
+        acc[t] = fmaf(__uint_as_float(xx[q] & 0xFFFF0000u), __uint_as_float(ww[q] & 0xFFFF0000u), acc[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    float v = acc[t];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) part[warp][t] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < T) {
+    float v = 0.f;
+    for (int j = 0; j < 8; ++j) v += part[j][threadIdx.x];
+    logits[(size_t)threadIdx.x * E + e] = v;
+  }
+}
+
+cudaError_t launch_router_gemv(const void* x, const void* w, int T, int E, int H, float* logits, cudaStream_t st) {
+  if (T < 1 || T > 16) return cudaErrorInvalidValue;
+  router_gemv_kernel<<<E, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x),
+                                        reinterpret_cast<const __nv_bfloat16*>(w), T, H, logits, E);
   return cudaGetLastError();
 }
 

@@ -22,4 +22,5 @@ from .inputs import (  # noqa: F401
     LinearConfig,
     LinearInputs,
     make_linear_inputs,
+    make_router_weight,
 )

@@ -355,3 +355,12 @@ def make_linear_inputs(name_or_cfg, tokens: int | None = None) -> LinearInputs:
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(cfg.seed, spawn_key=(3,))))
     x = rng.standard_normal((cfg.tokens, cfg.in_features), dtype=np.float32)
     return LinearInputs(cfg, q, s, np.float32(g), f32_to_bf16_bits(x))
+
+
+def make_router_weight(cfg: LayerConfig) -> np.ndarray:
+    """BF16 bit patterns of a router linear W [E][H] (routed experts only),
+    N(0, 1/H) from SeedSequence(seed, spawn_key=(4,)), so that the logits of
+    N(0, 1) activations are about N(0, 1) like the given-logits workloads."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(cfg.seed, spawn_key=(4,))))
+    w = rng.standard_normal((cfg.num_experts, cfg.hidden), dtype=np.float32) / np.float32(np.sqrt(cfg.hidden))
+    return f32_to_bf16_bits(w)
