@@ -55,6 +55,8 @@ def _args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--router", action="store_true",
+                    help="compute the router logits in the library (nvfp4_moe_forward_routed) inside each step")
     return ap.parse_args()
 
 
@@ -238,7 +240,7 @@ def run_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
 
     import nvfp4_weight_only_w4a16_gb300 as pkg
-    from synth import make_inputs
+    from synth import make_inputs, make_router_weight
     pkg.build()
     inp = make_inputs(args.workload)
     cfg = inp.config
@@ -254,6 +256,17 @@ def run_ours(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    if args.router:
+        # the logits come from the router linear on the GPU inside every step
+        layer.nvfp4_moe_set_router(torch.from_numpy(make_router_weight(cfg).view(np.int16)).to(dev).view(torch.bfloat16))
+        layer.nvfp4_moe_forward_routed(x, k, out)
+        torch.cuda.synchronize()
+        logits = layer.nvfp4_moe_debug_logits(T)
+        fwd = lambda: layer.nvfp4_moe_forward_routed(x, k, out)
+    else:
+        fwd = lambda: layer.nvfp4_moe_forward(logits, x, k, out)
+    n_ours += (1 if T <= 16 else 2) if args.router else 0
+
     ids, _, _, _ = layer.nvfp4_moe_debug_route(logits, T, k)
     distinct = int(torch.unique(ids).numel())
 
@@ -264,7 +277,7 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     for _ in range(args.warmup):
-        layer.nvfp4_moe_forward(logits, x, k, out)
+        fwd()
     torch.cuda.synchronize()
     st, _ = layer.nvfp4_moe_get_status()
     if st != 0:
@@ -273,7 +286,7 @@ def run_ours(args):
     # one forward captured into a CUDA graph (launch-overhead free replay)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        layer.nvfp4_moe_forward(logits, x, k, out)
+        fwd()
     for _ in range(3):
         graph.replay()
     torch.cuda.synchronize()
@@ -298,7 +311,7 @@ def run_ours(args):
     barrier()
     for _ in range(args.steps):
         flush.zero_()
-        layer.nvfp4_moe_forward(logits, x, k, out)
+        fwd()
     barrier()
     stage_ms, nfwd = layer.nvfp4_moe_get_stage_times()
     layer.nvfp4_moe_set_profiling(False)
@@ -313,9 +326,10 @@ def run_ours(args):
     for s, e in e2e_ev:
         flush.zero_()
         s.record(stream)
-        logits.copy_(h_logits, non_blocking=True)
+        if not args.router:
+            logits.copy_(h_logits, non_blocking=True)
         d_x16.copy_(h_x, non_blocking=True)
-        layer.nvfp4_moe_forward(logits, x, k, out)
+        fwd()
         h_out.copy_(out.view(torch.int16), non_blocking=True)
         e.record(stream)
     barrier()
@@ -378,19 +392,22 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "w4a16: e2m1*e4m3 weights -> fp16 mma, fp32 accumulate",
             "data": "synthetic (seeded PCG64, shapes of the pages' MTP decode step)",
-            "config": {"workload": _workload_desc(cfg), "distinct_experts": distinct,
+            "config": {"workload": _workload_desc(cfg) + (" + BF16 router linear" if args.router else ""),
+                       "distinct_experts": distinct,
                        "layer_weight_bytes_per_step": layer_bytes,
                        "layer_weight_gbs": layer_bytes / (ms / 1e3) / 1e9,
                        "layer_tflops": layer_flops / (ms / 1e3) / 1e12,
                        "l2": "flushed before every step (256 MiB write, outside the step events)",
-                       "launch": "CUDA graph replay of one nvfp4_moe_forward",
+                       "launch": "CUDA graph replay of one " + (
+                           "nvfp4_moe_forward_routed (router linear on the GPU)" if args.router else "nvfp4_moe_forward"),
                        "parallelism": f"replicas x{ws}",
                        "stage_ms": {"route_permute": stage_ms[0] / max(nfwd, 1), "gate_up": gateup_ms,
                                     "down": stage_ms[2] / max(nfwd, 1), "combine": stage_ms[3] / max(nfwd, 1)}},
             "roofline": {"bound": bound, "kernel": kernel, "achieved": achieved, "peak": peak,
                          "peak_source": peak_src, "unit": unit, "frac": achieved / peak,
                          "algorithmic_per_launch": algo, "traffic": traffic},
-            "e2e": {"value": value_e2e, "unit": "tokens/s", "h2d_bytes_per_step": T * E * 4 + T * H * 2,
+            "e2e": {"value": value_e2e, "unit": "tokens/s",
+                    "h2d_bytes_per_step": (0 if args.router else T * E * 4) + T * H * 2,
                     "d2h_bytes_per_step": T * H * 2},
             "gpu_launches": n_ours * args.steps,
             "clocks": clocks,

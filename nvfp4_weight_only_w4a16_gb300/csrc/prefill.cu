@@ -55,6 +55,14 @@ constexpr int kBOff = kAOff + kAStages * kAStageBytes;
 constexpr int kRawOff = kBOff + kBStages * kBStageBytes;
 constexpr int kBarOff = kRawOff + kRawStages * kRawStageBytes;
 constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
+// BF16-weight mode (no packed ring): the operand ring takes the packed ring's
+// space too -- stages 0, 1 in the A region, 2, 3 in the RAW region.
+constexpr int kAStagesW = kAStages + (kRawStages * kRawStageBytes) / kAStageBytes;
+static_assert(kAStagesW <= kRawStages, "BF16-mode operand barriers reuse the packed ring's");
+static_assert(kRawOff % 1024 == 0 && kAStageBytes % 1024 == 0, "128B-swizzled stages need 1024-byte alignment");
+__host__ __device__ constexpr int a_stage_off(int s) {
+  return s < kAStages ? kAOff + s * kAStageBytes : kRawOff + (s - kAStages) * kAStageBytes;
+}
 constexpr int kThreads = 480;                     // 15 warps
 constexpr int kDequantWarps = 8;
 constexpr int kTmemCols = 512;
@@ -222,6 +230,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   uint64_t* a_full = raw_empty + pf::kRawStages;
   uint64_t* a_empty = a_full + pf::kAStages;
   uint64_t* b_full = a_empty + pf::kAStages;
+  // the operand ring's barriers and depth (BF16 mode: the packed ring's barriers)
+  uint64_t* af = kBf16W ? raw_full : a_full;
+  uint64_t* ae = kBf16W ? raw_empty : a_empty;
+  constexpr int nAS = kBf16W ? pf::kAStagesW : pf::kAStages;
   uint64_t* b_empty = b_full + pf::kBStages;
   uint64_t* accfull = b_empty + pf::kBStages;
   uint64_t* accempty = accfull + 2;
@@ -232,7 +244,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < pf::kRawStages; ++s) {
       mbar_init(raw_full + s, 1);
-      mbar_init(raw_empty + s, pf::kDequantWarps);
+      mbar_init(raw_empty + s, kBf16W ? 1 : pf::kDequantWarps);
     }
     for (int s = 0; s < pf::kAStages; ++s) {
       mbar_init(a_full + s, kBf16W ? 1 : pf::kDequantWarps);
@@ -276,15 +288,15 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const int nblk = nb0 + 1 < a.NB ? 2 : 1;
         bool ok = true;
         for (int c = 0; c < nch; ++c, ++ia) {
-          const int sa = ia % pf::kAStages;
-          if (!mbar_wait(a_empty + sa, ((ia / pf::kAStages) & 1u) ^ 1u, abort_flag, a.st, 9)) {
+          const int sa = ia % nAS;
+          if (!mbar_wait(ae + sa, ((ia / nAS) & 1u) ^ 1u, abort_flag, a.st, 9)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + pf::kAOff + sa * pf::kAStageBytes;
-          mbar_arrive_expect_tx(a_full + sa, (uint32_t)nblk * (uint32_t)pf::kABlockBytes);
+          uint8_t* st = smem + pf::a_stage_off(sa);
+          mbar_arrive_expect_tx(af + sa, (uint32_t)nblk * (uint32_t)pf::kABlockBytes);
           for (int j = 0; j < nblk; ++j)  // rows past the matrix read as zeros
-            tma_2d(st + j * pf::kABlockBytes, &tmap_w, c * kChunk, (nb0 + j) * 128, a_full + sa);
+            tma_2d(st + j * pf::kABlockBytes, &tmap_w, c * kChunk, (nb0 + j) * 128, af + sa);
         }
         if (!ok) break;
       }
@@ -328,14 +340,14 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const uint32_t d_tmem = tmem_base + buf * 256u;  // block b's accumulator at + 128 b
         bool ok = true;
         for (int c = 0; c < nch; ++c, ++ia, ++ib) {
-          const int sa = ia % pf::kAStages, sb = ib % pf::kBStages;
-          if (!mbar_wait(a_full + sa, (ia / pf::kAStages) & 1u, abort_flag, a.st, 3) ||
+          const int sa = ia % nAS, sb = ib % pf::kBStages;
+          if (!mbar_wait(af + sa, (ia / nAS) & 1u, abort_flag, a.st, 3) ||
               !mbar_wait(b_full + sb, (ib / pf::kBStages) & 1u, abort_flag, a.st, 4)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sw128_desc(smem_u32(smem + pf::kAOff + sa * pf::kAStageBytes));
+          const uint64_t ad = sw128_desc(smem_u32(smem + pf::a_stage_off(sa)));
           const uint64_t bd = sw128_desc(smem_u32(smem + pf::kBOff + sb * pf::kBStageBytes));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
@@ -344,7 +356,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             if (nblk > 1)  // block 1's operand tile is 16 KB further (1024 in the 16-byte units)
               umma_bf16(d_tmem + 128u, ad + (uint64_t)(pf::kABlockBytes >> 4) + 2u * kk, bd + 2u * kk, idesc, acc);
           }
-          umma_commit(a_empty + sa);
+          umma_commit(ae + sa);
           umma_commit(b_empty + sb);
         }
         if (!ok) break;
