@@ -45,7 +45,8 @@ import numpy as np
 __all__ = [
     "decode_e2m1", "decode_e4m3", "unpack_e2m1_codes", "dequant", "dequant_scaled_f32",
     "bf16_bits_to_f64", "route", "route_scored", "router_logits", "permute", "silu", "expert_ffn", "expert_hidden",
-    "moe_forward", "linear_forward", "RouteResult",
+    "moe_forward", "linear_forward", "RouteResult", "encode_e2m1", "encode_e4m3", "quantize_act_nvfp4",
+    "moe_forward_w4a4",
 ]
 
 
@@ -321,6 +322,100 @@ def moe_forward(logits, x_bits, weights, k: int, tokens=None, return_parts=False
         out += y[:, k]
     if return_parts:
         return out, r, y
+    return out
+
+
+# ----------------------------------------------------------------------------
+# W4A4 comparison variant: activations quantised to NVFP4 with an input scale
+# ----------------------------------------------------------------------------
+# The stock checkpoint's routed experts are W4A4 NVFP4: activations are also
+# quantised to 4 bits with 16-element E4M3 block scales against a per-module
+# FP32 `input_scale` ("tenhkspark/GLM-5.3-Flash-NVFP4-Wabi", opening summary:
+# the routed experts keep the stock W4A4 NVFP4 quantisation; "GLM-5.3-Flash on
+# Blackwell", The model loaded, served an API, and produced garbage: a W4A4
+# MoE path consumed an uninitialised input_scale of 0.0 and zeroed every
+# expert; "tacos4me/GLM-5.3-Flash-NVFP4-FP8ATTN-512K", Input-scales provenance:
+# a placeholder input_scale of 1.0 made small-amax blocks underflow to zero).
+# The block rule is the weight rule applied to activations: per 16 consecutive
+# K elements, scale = E4M3(amax / (6 * input_scale)), code = E2M1(v / (scale *
+# input_scale)), both round-to-nearest-even, saturating; value = code * scale
+# * input_scale.  The decisions are taken in FP32, in this order of operations,
+# as the kernels take them.
+
+_E2M1_POS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _rne_to_grid(a, grid):
+    """Round |values| a (float64, >= 0) to the nearest of the increasing grid
+    (index = code), ties to the even code, saturating at the top."""
+    a = np.minimum(a, grid[-1])
+    hi = np.searchsorted(grid, a, side="left")          # first grid value >= a
+    hi = np.minimum(hi, len(grid) - 1)
+    lo = np.maximum(hi - 1, 0)
+    dlo, dhi = a - grid[lo], grid[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    return np.where(pick_hi, hi, lo)
+
+
+def encode_e2m1(v) -> np.ndarray:
+    """float -> E2M1 code, round-to-nearest-even, saturating at +-6."""
+    v = np.asarray(v, dtype=np.float64)
+    code = _rne_to_grid(np.abs(v), _E2M1_POS)
+    return (code | (np.signbit(v).astype(np.int64) << 3)).astype(np.uint8)
+
+
+def encode_e4m3(v) -> np.ndarray:
+    """float >= 0 -> E4M3 code, round-to-nearest-even, saturating at 448."""
+    grid = decode_e4m3(np.arange(127))                  # codes 0..126: 0 .. 448
+    return _rne_to_grid(np.asarray(v, dtype=np.float64), grid).astype(np.uint8)
+
+
+def quantize_act_nvfp4(v, input_scale: float):
+    """v [..][K] (K % 16 == 0) -> its W4A4 value without the input scale,
+    code * scale (float64, exact), plus the E4M3 scale codes [..][K/16]."""
+    v = np.asarray(v, dtype=np.float32)
+    isf = np.float32(input_scale)
+    blk = v.reshape(v.shape[:-1] + (v.shape[-1] // 16, 16))
+    amax = np.max(np.abs(blk), axis=-1)
+    denom = np.float32(np.float32(6.0) * isf)
+    sc = encode_e4m3((amax / denom).astype(np.float32))
+    sv = decode_e4m3(sc)
+    step = (sv.astype(np.float32) * isf).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = (blk / step[..., None]).astype(np.float32)
+    q = np.where(step[..., None] > 0, q, np.float32(0))
+    codes = encode_e2m1(q)
+    vals = decode_e2m1(codes) * sv[..., None]
+    return vals.reshape(v.shape), sc
+
+
+def moe_forward_w4a4(logits, x_bits, weights, k: int, input_scale, tokens=None, num_shared: int = 0,
+                     scoring=None):
+    """The layer with W4A4 routed experts: for routed row (t, e),
+    x^ = Q(x[t]; is[e][0]), g = gs_g is0 Wg x^, u = gs_u is0 Wu x^,
+    h = silu(g) u, h^ = Q(float32(h); is[e][1]), y = gs_d is1 Wd h^, and
+    out[t] = sum_j w_j y_j (+ the shared expert, which stays W4A16).
+    input_scale [E][2] float32 (w13, w2), each finite and > 0."""
+    iscale = np.asarray(input_scale, dtype=np.float32)
+    if not np.all(np.isfinite(iscale)) or np.any(iscale <= 0):
+        raise ValueError("every input_scale must be finite and > 0")
+    logits = np.asarray(logits)
+    T, E = logits.shape
+    tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    r = route(logits[tok], k) if scoring is None else route_scored(logits[tok], k, **scoring)
+    x = bf16_bits_to_f64(np.asarray(x_bits)[tok])
+    out = np.zeros_like(x)
+    for e in np.unique(r.ids):
+        rows, slots = np.nonzero(r.ids == e)
+        wg, wu, wd, gs = _expert_mats(weights, int(e))
+        is0, is1 = float(iscale[e, 0]), float(iscale[e, 1])
+        xq, _ = quantize_act_nvfp4(x[rows], is0)
+        h = silu(gs[0] * is0 * (xq @ wg.T)) * (gs[1] * is0 * (xq @ wu.T))
+        hq, _ = quantize_act_nvfp4(h.astype(np.float32), is1)
+        y = gs[2] * is1 * (hq @ wd.T)
+        out[rows] += r.weights[rows, slots][:, None] * y
+    if num_shared:
+        out += expert_ffn(weights, E, x)
     return out
 
 

@@ -409,9 +409,77 @@ def pin_router_logits(o):
             assert abs(out[t, e] - math.fsum(a * b for a, b in zip(xs, ws))) <= 1e-12
 
 
+def pin_act_quant(o):
+    # E2M1 round-to-nearest-even at every midpoint of {0, .5, 1, 1.5, 2, 3, 4, 6}
+    # (ties go to the even code), saturation at 6, sign bit 3
+    cases = {0.24: 0, 0.25: 0, 0.26: 1, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6, 5.01: 7,
+             6.0: 7, 100.0: 7, -0.75: 10, -5.5: 15}
+    got = o.encode_e2m1(np.array(list(cases)))
+    assert got.tolist() == list(cases.values()), got
+    # E4M3 encoder against torch's float8_e4m3fn cast (round-to-nearest-even)
+    # on a dense sweep and on every midpoint of the grid, within [0, 448]
+    grid = _torch_e4m3(np.arange(127, dtype=np.uint8))
+    mids = (grid[:-1] + grid[1:]) / 2
+    v = np.concatenate([np.linspace(0, 448, 40001), mids, grid]).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(o.encode_e4m3(v), ref)
+    assert o.encode_e4m3(np.array([449.0, 1e6], np.float32)).tolist() == [126, 126]
+    # a block already on the grid comes back exactly: values c * s * is
+    iscale = 0.5
+    row = np.array([6, -3, 1.5, 0.5, 0, 4, -6, 2, 1, -1, 3, 0.5, -0.5, 2, 4, 6], np.float64) * 1.25 * iscale
+    vals, sc = o.quantize_act_nvfp4(row[None, :].astype(np.float32), iscale)
+    assert np.array_equal(vals[0] * iscale, row) and sc.tolist() == [[0x3A]]
+    # the placeholder input_scale = 1.0: a block with amax 1e-3 underflows to
+    # zero (its scale 1e-3/6 is below the smallest E4M3 value), a calibrated
+    # input scale keeps it
+    small = np.full((1, 16), 1e-3, np.float32)
+    assert np.all(o.quantize_act_nvfp4(small, 1.0)[0] == 0)
+    cal = 1e-3 / (6 * 448)
+    assert np.allclose(o.quantize_act_nvfp4(small, cal)[0] * cal, 1e-3, rtol=0.07)
+    # every value within half a grid step of its input (inside the range)
+    rng = np.random.default_rng(12)
+    xv = rng.standard_normal((64, 64)).astype(np.float32)
+    vals, sc = o.quantize_act_nvfp4(xv, 4.0 / 2688)
+    step = o.decode_e4m3(sc) * np.float32(4.0 / 2688)
+    err = np.abs(vals * np.float32(4.0 / 2688) - xv).reshape(64, 4, 16)
+    assert np.all(err <= step[..., None] * 1.0 + 1e-12)
+
+
+def pin_w4a4_closed_form(o):
+    # one expert, codes 0x1 (0.5), scales 1.0, gs = 1; x = 1, is = (1/8, 8).
+    # x: scale E4M3(1 / 0.75) = 1.375, code E2M1(1 / 0.171875 = 5.82) = 6,
+    #    x^ = 8.25; g = u = 0.125 * 0.5 * 256 * 8.25 = 132; h = 132 * 132 = 17424
+    # h: scale E4M3(17424 / 48 = 363) = 352, code E2M1(17424 / 2816 = 6.1875)
+    #    saturates to 6, h^ = 2112; y = 8 * 0.5 * 512 * 2112 = 4325376
+    H, I = 256, 512
+    w = _const_expert(H, I, 0x1, 0x1, 0x1, 0x38, [1.0, 1.0, 1.0])
+    out = o.moe_forward_w4a4(np.zeros((2, 1), np.float32), _bf16_bits(np.ones((2, H))), w, 1,
+                             np.array([[0.125, 8.0]], np.float32))
+    assert np.all(out == 4325376.0), out[0, :4]
+    try:
+        o.moe_forward_w4a4(np.zeros((1, 1), np.float32), _bf16_bits(np.ones((1, H))), w, 1,
+                           np.array([[0.0, 1.0]], np.float32))
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("input_scale 0 accepted")
+    # W4A4 sits near, but not on, the W4A16 layer: mean relative deviation
+    # between 0.3% and 30% on random data
+    rng = np.random.default_rng(31)
+    E, H, I, T, k = 4, 64, 32, 6, 2
+    wts = _random_weights(rng, E, H, I)
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    xb = _bf16_bits(rng.standard_normal((T, H)))
+    a16 = o.moe_forward(L, xb, wts, k)
+    a4 = o.moe_forward_w4a4(L, xb, wts, k, np.array([[4.0 / 2688, 0.02]] * E, np.float32))
+    rel = np.abs(a4 - a16).mean() / np.abs(a16).mean()
+    assert 0.003 < rel < 0.3, rel
+
+
 PINS = [pin_e2m1_table, pin_e4m3, pin_dequant_worked, pin_round_trip, pin_route,
         pin_permute, pin_ffn_closed_form, pin_identical_experts, pin_top1_dense,
-        pin_brute_force_layer, pin_shared_expert, pin_linear, pin_route_scored, pin_router_logits]
+        pin_brute_force_layer, pin_shared_expert, pin_linear, pin_route_scored, pin_router_logits,
+        pin_act_quant, pin_w4a4_closed_form]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -598,7 +666,45 @@ def _mut_router_transposed(m):  # logits from the first E columns of W^T-shaped 
     m.router_logits = f
 
 
-MUTANTS = [_mut_bias_in_weights, _mut_select_without_bias, _mut_ignore_renormalize, _mut_ignore_scale,
+def _mut_w4a4_input_scale_dropped(m):  # the quantised x used without multiplying is0 back
+    orig = m.quantize_act_nvfp4
+    calls = {"n": 0}
+    def f(v, input_scale):
+        vals, sc = orig(v, input_scale)
+        calls["n"] += 1
+        return (vals * np.float32(input_scale) if calls["n"] % 2 == 1 else vals), sc
+    m.quantize_act_nvfp4 = f
+
+
+def _mut_w4a4_h_unquantised(m):
+    orig = m.quantize_act_nvfp4
+    def f(v, input_scale):
+        vals, sc = orig(v, input_scale)
+        if np.asarray(v).dtype == np.float32 and np.abs(v).max() > 100:  # the h call of the closed form
+            return np.asarray(v, np.float64) / np.float32(input_scale), sc
+        return vals, sc
+    m.quantize_act_nvfp4 = f
+
+
+def _mut_rne_ties_up(m):
+    def g(a, grid):
+        a = np.minimum(a, grid[-1])
+        hi = np.minimum(np.searchsorted(grid, a, side="left"), len(grid) - 1)
+        lo = np.maximum(hi - 1, 0)
+        return np.where(grid[hi] - a <= a - grid[lo], hi, lo)
+    m._rne_to_grid = g
+
+
+def _mut_e4m3_truncate(m):
+    def f(v):
+        grid = m.decode_e4m3(np.arange(127))
+        a = np.minimum(np.asarray(v, dtype=np.float64), 448.0)
+        return (np.searchsorted(grid, a, side="right") - 1).astype(np.uint8)
+    m.encode_e4m3 = f
+
+
+MUTANTS = [_mut_w4a4_input_scale_dropped, _mut_w4a4_h_unquantised, _mut_rne_ties_up, _mut_e4m3_truncate,
+           _mut_bias_in_weights, _mut_select_without_bias, _mut_ignore_renormalize, _mut_ignore_scale,
            _mut_sigmoid_as_softmax, _mut_router_transposed, _mut_linear_transposed, _mut_linear_no_gscale, _mut_nibble_order, _mut_e4m3_bias, _mut_e2m1_subnormal, _mut_scale_group_shift,
            _mut_gate_up_swap, _mut_drop_up_scale, _mut_tie_break, _mut_softmax_all,
            _mut_no_combine_weights, _mut_silu_sign, _mut_perm_unstable, _mut_shared_dropped,
