@@ -337,10 +337,12 @@ def moe_forward(logits, x_bits, weights, k: int, tokens=None, return_parts=False
 # expert; "tacos4me/GLM-5.3-Flash-NVFP4-FP8ATTN-512K", Input-scales provenance:
 # a placeholder input_scale of 1.0 made small-amax blocks underflow to zero).
 # The block rule is the weight rule applied to activations: per 16 consecutive
-# K elements, scale = E4M3(amax / (6 * input_scale)), code = E2M1(v / (scale *
-# input_scale)), both round-to-nearest-even, saturating; value = code * scale
-# * input_scale.  The decisions are taken in FP32, in this order of operations,
-# as the kernels take them.
+# K elements, scale = E4M3(amax / (6 * input_scale)), code = E2M1(v *
+# (1 / (scale * input_scale))), both round-to-nearest-even, saturating; value
+# = code * scale * input_scale.  The decisions are taken in FP32, in this
+# order of operations (one reciprocal per block, then a product per element),
+# as the kernels take them; the pages fix neither.  h is rounded to BF16
+# before it is quantised, as it is between the GEMMs of the W4A16 layer.
 
 _E2M1_POS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 
@@ -382,7 +384,8 @@ def quantize_act_nvfp4(v, input_scale: float):
     sv = decode_e4m3(sc)
     step = (sv.astype(np.float32) * isf).astype(np.float32)
     with np.errstate(divide="ignore", invalid="ignore"):
-        q = (blk / step[..., None]).astype(np.float32)
+        rcp = (np.float32(1.0) / step).astype(np.float32)
+        q = (blk * rcp[..., None]).astype(np.float32)
     q = np.where(step[..., None] > 0, q, np.float32(0))
     codes = encode_e2m1(q)
     vals = decode_e2m1(codes) * sv[..., None]
@@ -393,7 +396,7 @@ def moe_forward_w4a4(logits, x_bits, weights, k: int, input_scale, tokens=None, 
                      scoring=None):
     """The layer with W4A4 routed experts: for routed row (t, e),
     x^ = Q(x[t]; is[e][0]), g = gs_g is0 Wg x^, u = gs_u is0 Wu x^,
-    h = silu(g) u, h^ = Q(float32(h); is[e][1]), y = gs_d is1 Wd h^, and
+    h = silu(g) u, h^ = Q(bf16(h); is[e][1]), y = gs_d is1 Wd h^, and
     out[t] = sum_j w_j y_j (+ the shared expert, which stays W4A16).
     input_scale [E][2] float32 (w13, w2), each finite and > 0."""
     iscale = np.asarray(input_scale, dtype=np.float32)
@@ -411,12 +414,21 @@ def moe_forward_w4a4(logits, x_bits, weights, k: int, input_scale, tokens=None, 
         is0, is1 = float(iscale[e, 0]), float(iscale[e, 1])
         xq, _ = quantize_act_nvfp4(x[rows], is0)
         h = silu(gs[0] * is0 * (xq @ wg.T)) * (gs[1] * is0 * (xq @ wu.T))
-        hq, _ = quantize_act_nvfp4(h.astype(np.float32), is1)
+        hq, _ = quantize_act_nvfp4(bf16_bits_to_f64(_round_bf16_bits(h)).astype(np.float32), is1)
         y = gs[2] * is1 * (hq @ wd.T)
         out[rows] += r.weights[rows, slots][:, None] * y
     if num_shared:
         out += expert_ffn(weights, E, x)
     return out
+
+
+def _round_bf16_bits(v) -> np.ndarray:
+    """float64 -> BF16 bit patterns: rounded to float32 first, as the kernels
+    hold h, then to BF16 with round-to-nearest-even."""
+    f = np.asarray(v, dtype=np.float64).astype(np.float32)
+    b = f.view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return b.astype(np.uint16)
 
 
 def linear_forward(x_bits, w_q, w_s, gscale: float) -> np.ndarray:

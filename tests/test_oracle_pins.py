@@ -448,8 +448,9 @@ def pin_act_quant(o):
 def pin_w4a4_closed_form(o):
     # one expert, codes 0x1 (0.5), scales 1.0, gs = 1; x = 1, is = (1/8, 8).
     # x: scale E4M3(1 / 0.75) = 1.375, code E2M1(1 / 0.171875 = 5.82) = 6,
-    #    x^ = 8.25; g = u = 0.125 * 0.5 * 256 * 8.25 = 132; h = 132 * 132 = 17424
-    # h: scale E4M3(17424 / 48 = 363) = 352, code E2M1(17424 / 2816 = 6.1875)
+    #    x^ = 8.25; g = u = 0.125 * 0.5 * 256 * 8.25 = 132; h = 132 * 132 = 17424,
+    #    BF16(h) = 17408
+    # h: scale E4M3(17408 / 48 = 362.7) = 352, code E2M1(17408 / 2816 = 6.18)
     #    saturates to 6, h^ = 2112; y = 8 * 0.5 * 512 * 2112 = 4325376
     H, I = 256, 512
     w = _const_expert(H, I, 0x1, 0x1, 0x1, 0x38, [1.0, 1.0, 1.0])
