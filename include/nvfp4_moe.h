@@ -225,6 +225,22 @@ nvfp4_moe_status nvfp4_moe_forward_routed(nvfp4_moe_t h, int T, int top_k, const
                                           cudaStream_t stream);
 nvfp4_moe_status nvfp4_moe_debug_logits(nvfp4_moe_t h, float* logits, cudaStream_t stream);
 
+/* W4A4 comparison variant.  The stock checkpoint's routed experts are W4A4
+ * NVFP4: activations are quantised to NVFP4 too, against a per-module FP32
+ * input scale ("tenhkspark/GLM-5.3-Flash-NVFP4-Wabi", opening summary).
+ * With input_scale set (DEVICE float [num_experts][2]: the gate/up input
+ * scale, then the down input scale, of every routed expert; each finite and
+ * > 0, else NVFP4_MOE_ERR_BAD_SCALE -- an input scale of 0 zeroes every expert,
+ * "GLM-5.3-Flash on Blackwell", The model loaded, served an API, and produced
+ * garbage), every routed expert quantises its input x and its hidden h
+ * (rounded to BF16 first) per 16 elements: scale = E4M3(amax / (6 is)),
+ * code = E2M1(v / (scale is)), round-to-nearest-even, saturating; the input
+ * scales multiply the tensor scales after the dot products.  The shared
+ * expert stays W4A16.  The quantised values are exact in BF16/FP16, so the
+ * products run on the same tensor-core paths as W4A16.  NULL turns the
+ * variant off.  Synchronous (reads the scales back to check them). */
+nvfp4_moe_status nvfp4_moe_set_act_quant(nvfp4_moe_t h, const float* input_scale, cudaStream_t stream);
+
 /* Per-stage timing.  With profiling on, every forward records CUDA events on
  * its stream before and after each stage.  nvfp4_moe_get_stage_times
  * (synchronous) returns in ms[0..3] the summed milliseconds of route+permute,

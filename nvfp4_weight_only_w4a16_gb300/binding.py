@@ -85,6 +85,7 @@ def load_library(path: str | None = None):
         "nvfp4_moe_get_stage_times": (i, [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
         "nvfp4_moe_set_scoring": (i, [vp, i, i, f, vp, vp]),
         "nvfp4_moe_set_router": (i, [vp, vp, vp]),
+        "nvfp4_moe_set_act_quant": (i, [vp, vp, vp]),
         "nvfp4_moe_forward_routed": (i, [vp, i, i, vp, vp, vp]),
         "nvfp4_moe_debug_logits": (i, [vp, vp, vp]),
         "nvfp4_linear_create": (i, [ctypes.POINTER(LinearConfig), ctypes.POINTER(vp)]),
@@ -235,6 +236,11 @@ class MoELayer:
         st = self.lib.nvfp4_moe_set_scoring(self.h, code, 1 if renormalize else 0, float(scale), _ptr(bias),
                                             _stream(stream))
         self._check(st, "nvfp4_moe_set_scoring")
+
+    def nvfp4_moe_set_act_quant(self, input_scale, stream=None):
+        """input_scale: a CUDA float32 tensor [num_experts][2] (W4A4), or None (W4A16)."""
+        st = self.lib.nvfp4_moe_set_act_quant(self.h, _ptr(input_scale), _stream(stream))
+        self._check(st, "nvfp4_moe_set_act_quant")
 
     def nvfp4_moe_set_router(self, w_router, stream=None):
         """w_router: a CUDA BF16 tensor [num_experts][hidden]."""

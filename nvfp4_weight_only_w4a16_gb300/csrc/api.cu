@@ -23,6 +23,12 @@ struct nvfp4_moe {
   void* w_router = nullptr;  // [num_experts][hidden] BF16 router weight (nvfp4_moe_set_router)
   CUtensorMap w_router_map{};  // over w_router, box {64, 128}, 128B swizzle
   bool have_router = false;
+  // W4A4 comparison variant (nvfp4_moe_set_act_quant)
+  bool w4a4 = false;
+  float* in_scale = nullptr;     // [E][2] device input scales (w13, w2); shared expert's unused
+  float* gs_eff = nullptr;       // [E][3] device tensor scales with the input scales folded in
+  std::vector<float> gs_host;    // [E][3] the packed tensor scales
+  std::vector<float> is_host;    // [E][2]
   int path = NVFP4_MOE_PATH_AUTO;
   int num_sms = 0;
   bool packed = false;
@@ -149,6 +155,7 @@ LayerDims dims_of(const nvfp4_moe* h) {
               h->cfg.logits_dtype == NVFP4_MOE_LOGITS_BF16, h->cfg.out_dtype == NVFP4_MOE_OUT_F32,
               h->cfg.num_experts, h->cfg.num_shared_experts, h->linear ? 1 : 0, h->lin_n};
   d.rp = h->rp;
+  d.in_scale = h->w4a4 ? h->in_scale : nullptr;
   return d;
 }
 
@@ -160,6 +167,23 @@ size_t blob_bytes_of(const nvfp4_moe_config& c, bool linear) {
 // Handle allocation shared by the MoE layer and the dense linear (c already
 // validated; a linear's c holds one expert with hidden = N and inter = K).
 nvfp4_moe_status create_handle(const nvfp4_moe_config* c, bool linear, int lin_n, nvfp4_moe_t* out);
+
+// W4A4: tensor scales with the input scales folded in (routed experts: gate and
+// up times is_w13, down times is_w2; the shared expert keeps its own).
+nvfp4_moe_status upload_gs_eff(nvfp4_moe* h, cudaStream_t st) {
+  const int E = h->cfg.num_experts + h->cfg.num_shared_experts, Er = h->cfg.num_experts;
+  if (h->gs_host.size() != (size_t)3 * E) return NVFP4_MOE_OK;  // not packed yet: pack uploads it
+  std::vector<float> g(h->gs_host);
+  for (int e = 0; e < Er; ++e) {
+    g[3 * e] *= h->is_host[2 * e];
+    g[3 * e + 1] *= h->is_host[2 * e];
+    g[3 * e + 2] *= h->is_host[2 * e + 1];
+  }
+  cudaError_t err = cudaMemcpyAsync(h->gs_eff, g.data(), sizeof(float) * g.size(), cudaMemcpyHostToDevice, st);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(st);  // g lives on this frame
+  if (err != cudaSuccess) return cuda_fail(h, err, "W4A4 tensor scales upload");
+  return NVFP4_MOE_OK;
+}
 
 // Forward events: 5 per profiled forward (ev[i] stays NULL when profiling is off).
 nvfp4_moe_status take_events(nvfp4_moe* h, cudaEvent_t (&ev)[5]) {
@@ -301,7 +325,8 @@ nvfp4_moe_status create_handle(const nvfp4_moe_config* c, bool linear, int lin_n
   h->ws_bytes = cv.layout();
 
   if (cudaMalloc(&h->blob, blob_bytes) != cudaSuccess || cudaMalloc(&h->gscale, sizeof(float) * 3 * E) != cudaSuccess ||
-      cudaMalloc(&h->bias, sizeof(float) * E) != cudaSuccess || cudaMalloc(&h->ws_mem, h->ws_bytes) != cudaSuccess) {
+      cudaMalloc(&h->bias, sizeof(float) * E) != cudaSuccess || cudaMalloc(&h->in_scale, sizeof(float) * 2 * E) != cudaSuccess ||
+      cudaMalloc(&h->gs_eff, sizeof(float) * 3 * E) != cudaSuccess || cudaMalloc(&h->ws_mem, h->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
     nvfp4_moe_destroy(h);
     return NVFP4_MOE_ERR_WORKSPACE;
@@ -334,6 +359,8 @@ void nvfp4_moe_destroy(nvfp4_moe_t h) {
     if (h->gscale) cudaFree(h->gscale);
     if (h->bias) cudaFree(h->bias);
     if (h->w_router) cudaFree(h->w_router);
+    if (h->in_scale) cudaFree(h->in_scale);
+    if (h->gs_eff) cudaFree(h->gs_eff);
     if (h->ws_mem) cudaFree(h->ws_mem);
   }
   delete h;
@@ -393,6 +420,36 @@ nvfp4_moe_status nvfp4_moe_set_scoring(nvfp4_moe_t h, int score_func, int renorm
   return NVFP4_MOE_OK;
 }
 
+nvfp4_moe_status nvfp4_moe_set_act_quant(nvfp4_moe_t h, const float* input_scale, cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (h->linear) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "set_act_quant: not for a dense-linear handle");
+  if (!input_scale) {
+    h->w4a4 = false;
+    return NVFP4_MOE_OK;
+  }
+  if (!aligned(input_scale, 4)) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "set_act_quant: misaligned input_scale");
+  DeviceGuard g(h->cfg.device);
+  const int E = h->cfg.num_experts + h->cfg.num_shared_experts, Er = h->cfg.num_experts;
+  std::vector<float> is((size_t)2 * E, 0.0f);
+  cudaError_t e = cudaMemcpyAsync(is.data(), input_scale, sizeof(float) * 2 * Er, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "set_act_quant: reading input_scale");
+  for (int i = 0; i < 2 * Er; ++i) {
+    const float v = is[i];
+    if (!(v > 0.0f) || v != v || v > 3.4e38f) {
+      h->w4a4 = false;
+      return fail(h, NVFP4_MOE_ERR_BAD_SCALE, "set_act_quant: input scale " + std::to_string(i % 2) + " of expert " +
+                                                  std::to_string(i / 2) + " is not finite > 0");
+    }
+  }
+  e = cudaMemcpyAsync(h->in_scale, is.data(), sizeof(float) * is.size(), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "set_act_quant: input_scale upload");
+  h->is_host = is;
+  h->w4a4 = true;
+  return upload_gs_eff(h, st);
+}
+
 nvfp4_moe_status nvfp4_moe_debug_set_fault(nvfp4_moe_t h, int fault) {
   if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
   if (fault < 0 || fault > 1) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_set_fault: unknown fault");
@@ -424,6 +481,11 @@ nvfp4_moe_status nvfp4_moe_pack(nvfp4_moe_t h, const uint8_t* w13_q, const uint8
   e = cudaMemcpyAsync(h->gscale, gscale, sizeof(float) * gs.size(), cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = launch_pack(w13_q, w13_s, w2_q, w2_s, h->blob, E, h->cfg.hidden, h->cfg.inter, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "pack launch");
+  h->gs_host = gs;
+  if (h->w4a4) {
+    nvfp4_moe_status s2 = upload_gs_eff(h, st);
+    if (s2 != NVFP4_MOE_OK) return s2;
+  }
   h->packed = true;
   return NVFP4_MOE_OK;
 }
@@ -456,6 +518,7 @@ nvfp4_moe_status forward_impl(nvfp4_moe* h, const void* logits, int T, int top_k
   if (s != NVFP4_MOE_OK) return s;
   if (ev[0]) cudaEventRecord(ev[0], st);
   LayerDims d = dims_of(h);
+  const float* gsc = h->w4a4 ? h->gs_eff : h->gscale;  // W4A4: input scales folded in
   cudaError_t e;
   if (routed) {  // the router linear, timed with route + permute
     const int Er = h->cfg.num_experts, H = h->cfg.hidden;
@@ -476,7 +539,7 @@ nvfp4_moe_status forward_impl(nvfp4_moe* h, const void* logits, int T, int top_k
   if (path == NVFP4_MOE_PATH_DECODE) {
     // one fused kernel: its time is reported as the gate/up stage
     if (ev[1]) cudaEventRecord(ev[1], st);
-    e = launch_decode_forward(d, h->blob, h->gscale, logits, x, T, top_k, out, 0, h->num_sms, h->ws, st);
+    e = launch_decode_forward(d, h->blob, gsc, logits, x, T, top_k, out, 0, h->num_sms, h->ws, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");
     if (ev[2]) cudaEventRecord(ev[2], st);
     if (ev[3]) cudaEventRecord(ev[3], st);
@@ -484,7 +547,7 @@ nvfp4_moe_status forward_impl(nvfp4_moe* h, const void* logits, int T, int top_k
     s = run_route(h, logits, x, T, top_k, path, st, d.logits_bf16);
     if (s != NVFP4_MOE_OK) return s;
     if (ev[1]) cudaEventRecord(ev[1], st);
-    e = launch_prefill_ffn(d, h->blob, h->gscale, T, top_k, h->num_sms, h->maps, h->ws, h->fault, ev[2],
+    e = launch_prefill_ffn(d, h->blob, gsc, T, top_k, h->num_sms, h->maps, h->ws, h->fault, ev[2],
                            nullptr, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "expert FFN launch");
     if (ev[3]) cudaEventRecord(ev[3], st);

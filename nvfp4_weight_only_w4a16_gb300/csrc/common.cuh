@@ -106,6 +106,79 @@ __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t v) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
+// 8 E2M1 codes (nibble j = element j) -> 4 f16x2 {element 2j, element 2j+1}.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+
+// ---------------------------------------------------------------------------
+// W4A4 activation quantisation (NVFP4 activations with a per-module input
+// scale is, the stock routed-expert format: "tenhkspark/GLM-5.3-Flash-NVFP4-
+// Wabi", opening summary).  Per block of 16 values: scale = E4M3(amax /
+// fl(6 is)), r = fl(1 / fl(scale * is)), code = E2M1(v * r); both conversions
+// round to nearest even and saturate.  The values returned are code * scale,
+// exact in FP16 and BF16; the input scale is applied after the dot product.
+// ---------------------------------------------------------------------------
+struct ActBlockScale {
+  uint32_t s2;  // f16x2 {scale, scale}
+  float r;      // 1 / (scale * is), 0 when the scale is 0
+};
+__device__ __forceinline__ ActBlockScale act_block_scale(float amax, float is) {
+  const float st = __fdiv_rn(amax, __fmul_rn(6.0f, is));
+  unsigned short sc;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(sc) : "f"(st));
+  const uint32_t s2 = e4m3x2_to_f16x2(sc);
+  const float sv = __half2float(__ushort_as_half((unsigned short)(s2 & 0xFFFFu)));
+  const float step = __fmul_rn(sv, is);
+  return ActBlockScale{s2, step > 0.f ? __frcp_rn(step) : 0.f};
+}
+
+// E2M1 codes of v[0..7] (already multiplied by r), nibble j = code of v[j].
+__device__ __forceinline__ uint32_t e2m1x8_rn(const float* v) {
+  uint32_t r;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
+// One block of 16 values -> 8 f16x2 of code * scale (in element order).
+__device__ __forceinline__ void act_quant16_f16(const float (&v)[16], float is, uint32_t (&out)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const ActBlockScale bs = act_block_scale(amax, is);
+  float q[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) q[i] = __fmul_rn(v[i], bs.r);
+  uint32_t c[4];
+  e2m1x8_to_f16x2x4(e2m1x8_rn(q), c);
+#pragma unroll
+  for (int z = 0; z < 4; ++z) out[z] = hmul2_u32(c[z], bs.s2);
+  e2m1x8_to_f16x2x4(e2m1x8_rn(q + 8), c);
+#pragma unroll
+  for (int z = 0; z < 4; ++z) out[4 + z] = hmul2_u32(c[z], bs.s2);
+}
+
+// One value of a block whose scale is bs -> code * scale.
+__device__ __forceinline__ float act_quant1(float v, const ActBlockScale& bs) {
+  uint32_t b;
+  asm("{\n .reg .b8 c;\n cvt.rn.satfinite.e2m1x2.f32 c, %1, %1;\n cvt.u32.u8 %0, c;\n}"
+      : "=r"(b)
+      : "f"(__fmul_rn(v, bs.r)));
+  const uint32_t f = hmul2_u32(e2m1x2_to_f16x2(b), bs.s2);
+  return __half2float(__ushort_as_half((unsigned short)(f & 0xFFFFu)));
+}
+
 // Order-preserving key of a float: larger float -> larger key; NaN -> 0
 // (below -inf, whose key is 0x007FFFFF); -0 and +0 share one key, as they
 // compare equal.

@@ -88,6 +88,7 @@ struct FusedArgs {
   int Er, topk;       // routed experts (logits per token), routed choices per token
   int linear;         // 1: a dense linear: no routing, no gate/up; x [T][I] feeds the down GEMV
   RouteParams rp;     // scoring rule of the route step
+  const float* in_scale;  // W4A4 routed experts: [E][2] input scales (w13, w2), else nullptr
   int n_out;          // a dense linear's output features (<= H; rows past it are padding)
   const void* logits;
   int logits_bf16;
@@ -370,7 +371,8 @@ __device__ void finish_gateup(const FusedArgs& a, const RouteSmem& rs, int u, in
       const int j = 8 * i + 2 * q + c;
       if (j >= m) continue;
       const int row = row0 + j;
-      const float s = pow2f(rs.xexp[rs.perm[row] / a.k]);
+      // W4A4 routed experts take unscaled quantised activations (no prescale)
+      const float s = (a.in_scale && e < a.Er) ? 1.0f : pow2f(rs.xexp[rs.perm[row] / a.k]);
 #pragma unroll
       for (int rg = 0; rg < dec::kRG; ++rg) {
         if (rg >= cnt) break;
@@ -410,8 +412,10 @@ __device__ void finish_down(const FusedArgs& a, const RouteSmem& rs, int u, int 
       const int j = 8 * i + 2 * q + c;
       if (j >= m) continue;
       const int row = row0 + j;
-      const float s = gsd * pow2f(a.linear ? rs.xexp[rs.perm[row]]
-                                           : prescale_exp(__uint_as_float(__ldcg(a.hmax + row))));
+      const float s = (a.in_scale && e < a.Er)
+                          ? gsd
+                          : gsd * pow2f(a.linear ? rs.xexp[rs.perm[row]]
+                                                 : prescale_exp(__uint_as_float(__ldcg(a.hmax + row))));
       if (a.linear) {  // one slot per token, weight 1: the result is the output row itself
         const size_t o = (size_t)rs.perm[row] * a.n_out;
 #pragma unroll
@@ -683,6 +687,8 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
   float bsc[2] = {1.f, 1.f};
   const uint8_t* xrow = nullptr;  // kXs: this lane's token row
   int seg_c0 = 0, m = 0, ng = 1, cu = 0, cb = 0, crg0 = 0, ccnt = 0;
+  bool q4 = false;  // this piece's activations are quantised to NVFP4 (W4A4 routed expert)
+  float q4_is = 0.f;
   bool fin_head = false, fin_tail = false;  // split segments this warp finished in the loop
   int issued = 0, consumed = 0;
 
@@ -710,6 +716,8 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
       cw.piece(p, &cu, &cb, &crg0, &ccnt);
       const int row0 = rs.tch_r0[cu];
       m = rs.tch_m[cu];
+      q4 = a.in_scale != nullptr && rs.tch_e[cu] < a.Er;
+      if (q4) q4_is = __ldg(a.in_scale + 2 * rs.tch_e[cu] + (kGateUp ? 0 : 1));
       ng = (m + 7) >> 3;
 #pragma unroll
       for (int rg = 0; rg < dec::kRG; ++rg)
@@ -751,11 +759,21 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
           const uint8_t* pa = st + dec::kStB + srow * dec::kRowPitch + q * 32;
           const uint4 u0 = *reinterpret_cast<const uint4*>(pa), u1 = *reinterpret_cast<const uint4*>(pa + 16);
           const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+          if (q4) {  // this lane's 16 K elements are one NVFP4 block
+            float v[16];
 #pragma unroll
-          for (int z = 0; z < 8; ++z) {
-            const __half2 hh = __floats2half2_rn(__uint_as_float(w[z] << 16) * bsc[gi],
-                                                 __uint_as_float(w[z] & 0xFFFF0000u) * bsc[gi]);
-            bw[gi][z] = *reinterpret_cast<const uint32_t*>(&hh);
+            for (int z = 0; z < 8; ++z) {
+              v[2 * z] = __uint_as_float(w[z] << 16);
+              v[2 * z + 1] = __uint_as_float(w[z] & 0xFFFF0000u);
+            }
+            act_quant16_f16(v, q4_is, bw[gi]);
+          } else {
+#pragma unroll
+            for (int z = 0; z < 8; ++z) {
+              const __half2 hh = __floats2half2_rn(__uint_as_float(w[z] << 16) * bsc[gi],
+                                                   __uint_as_float(w[z] & 0xFFFF0000u) * bsc[gi]);
+              bw[gi][z] = *reinterpret_cast<const uint32_t*>(&hh);
+            }
           }
         }
       }
@@ -1070,7 +1088,7 @@ static int decode_stage_cap() {
   }();
   return cap;
 }
-static DecodeSmemPlan plan_smem(int T, int H, int linear, int smem_max) {
+static DecodeSmemPlan plan_smem(int T, int H, int linear, bool no_xs, int smem_max) {
   const size_t base = ((sizeof(RouteSmem) + 127) & ~size_t(127)) + 128 * 8 + 128;
   const size_t ring1 = (size_t)dec::kWarps * dec::stage_bytes_for(T);  // one stage per warp
   const int cap = decode_stage_cap();
@@ -1097,7 +1115,7 @@ static DecodeSmemPlan plan_smem(int T, int H, int linear, int smem_max) {
     const char* s = getenv("NVFP4_MOE_DECODE_STAGE_X");
     return !(s && s[0] == '0');
   }();
-  for (int S = cap; S >= 3 && stage_x; --S)
+  for (int S = cap; S >= 3 && stage_x && !no_xs; --S)
     if (base + S * ring1 + 2 * slot_b + xs_b <= (size_t)smem_max)
       return DecodeSmemPlan{base + S * ring1 + 2 * slot_b + xs_b, S, T, 2, 2 * H + 16};
   const int S = cap < 3 ? cap : 3;
@@ -1122,7 +1140,8 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
     smem_max = optin;
   }
   const bool small = T <= 8;
-  const DecodeSmemPlan plan = plan_smem(T, d.H, d.linear, smem_max);
+  // W4A4 quantises activations from their BF16 values: no staged FP16 copy
+  const DecodeSmemPlan plan = plan_smem(T, d.H, d.linear, d.in_scale != nullptr, smem_max);
   if (plan.bytes > (size_t)smem_max) return cudaErrorInvalidConfiguration;
   const ExpertLayout L = d.linear ? linear_layout(d.H, d.I) : expert_layout(d.H, d.I);
   FusedArgs a{};
@@ -1143,6 +1162,7 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
   a.linear = d.linear;
   a.n_out = d.n_out;
   a.rp = d.rp;
+  a.in_scale = d.in_scale;
   a.logits = logits;
   a.logits_bf16 = d.logits_bf16;
   a.x = reinterpret_cast<const __nv_bfloat16*>(x);

@@ -64,6 +64,8 @@ struct LayerDims {
   int n_out;       // a dense linear's output features N <= H (H = N rounded up to 128; the
                    // padded rows are zero): out is [T][n_out]
   RouteParams rp;  // scoring rule of the route step
+  const float* in_scale = nullptr;  // W4A4 routed experts: [E][2] input scales (w13, w2); the
+                                    // caller passes tensor scales with them folded in
 };
 
 constexpr int kRankTokens = 256;      // tokens per rank block in the prefill routing

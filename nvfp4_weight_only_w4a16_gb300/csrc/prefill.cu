@@ -89,6 +89,8 @@ struct PrefillArgs {
   int out_f32;   // out is FP32 (else BF16)
   int linear;    // 1: a dense linear (one matrix, rows in token order, weight 1)
   int n_out;     // a dense linear's output features: out is [T][n_out], rows d >= n_out are padding
+  const float* in_scale;  // W4A4 routed experts (e < Er): [E][2] input scales, else nullptr
+  int Er;
   DeviceStatus* st;
   int fault;  // 1: the producer issues nothing (tests the bounded waits)
 };
@@ -444,14 +446,25 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             const int f = 8 * (R >> 4) + (R & 7);
             const bool is_gate = (R & 15) < 8;
             const float gsg = gs[0], gsu = gs[1];
+            // W4A4 routed expert: h (rounded to BF16) is quantised to NVFP4 with the
+            // w2 input scale; this warp's 16 gate lanes hold one 16-feature block
+            const bool q4 = a.in_scale != nullptr && e < a.Er;
+            const float is1 = q4 ? __ldg(a.in_scale + 2 * e + 1) : 0.f;
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const float mine = __uint_as_float(v[jj]);
               const float partner = __shfl_xor_sync(0xffffffffu, mine, 8);
-              if (is_gate && col + jj < rows) {
-                const float g = gsg * mine, u = gsu * partner;
-                a.h[(size_t)(row0 + col + jj) * a.I + f] = __float2bfloat16_rn(silu(g) * u);
+              float hv = 0.f;
+              if (is_gate) hv = __bfloat162float(__float2bfloat16_rn(silu(gsg * mine) * (gsu * partner)));
+              if (q4) {
+                float am = is_gate ? fabsf(hv) : 0.f;  // lane bit 3 (gate / up) is never flipped
+                am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+                am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+                am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+                am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 16));
+                hv = act_quant1(hv, act_block_scale(am, is1));
               }
+              if (is_gate && col + jj < rows) a.h[(size_t)(row0 + col + jj) * a.I + f] = __float2bfloat16_rn(hv);
             }
           } else {
             const int d = 128 * nb + i;
@@ -527,6 +540,8 @@ cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const fl
   a.out_f32 = d.out_f32;
   a.linear = d.linear;
   a.n_out = d.n_out;
+  a.in_scale = d.in_scale;
+  a.Er = d.Er;
   a.st = ws.status;
   a.fault = fault;
   if (!d.linear) {  // gate/up: 2I interleaved rows, K = H

@@ -109,8 +109,11 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int nblocks, int E, Wo
 
 // K4: one warp per routed row: its position, perm/inv, and (unless only
 // routing) the copy of x[t] into position order.
+// W4A4 (in_scale set, routed experts e < Er): the copy holds x quantised to
+// NVFP4 with the expert's w13 input scale, as code * scale in BF16 (exact).
 __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int k,
-                                                            int E, int H, Workspace ws) {
+                                                            int E, int H, const float* __restrict__ in_scale,
+                                                            int Er, Workspace ws) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t i = (size_t)blockIdx.x * 8 + warp;
   if (i >= (size_t)T * k) return;
@@ -124,7 +127,27 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16*
   if (x == nullptr) return;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
   uint4* dst = reinterpret_cast<uint4*>(ws.x_perm + (size_t)pos * H);
-  for (int v = lane; v < H / 8; v += 32) dst[v] = __ldg(src + v);
+  if (in_scale == nullptr || e >= Er) {
+    for (int v = lane; v < H / 8; v += 32) dst[v] = __ldg(src + v);
+    return;
+  }
+  const float is = __ldg(in_scale + 2 * e);
+  for (int b = lane; b < H / 16; b += 32) {  // one 16-element block per lane
+    const uint4 u0 = __ldg(src + 2 * b), u1 = __ldg(src + 2 * b + 1);
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    float v[16];
+#pragma unroll
+    for (int z = 0; z < 8; ++z) {
+      v[2 * z] = __uint_as_float(w[z] << 16);
+      v[2 * z + 1] = __uint_as_float(w[z] & 0xFFFF0000u);
+    }
+    uint32_t o[8];
+    act_quant16_f16(v, is, o);
+#pragma unroll
+    for (int z = 0; z < 8; ++z) o[z] = f16x2_to_bf16x2(o[z]);
+    dst[2 * b] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[2 * b + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
 }
 
 cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const void* x, int T, int top_k,
@@ -136,7 +159,7 @@ cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const v
   route_scan_kernel<<<1, 1024, 0, st>>>(nrb, d.E, ws);
   const size_t rows = (size_t)T * k;
   route_scatter_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), T,
-                                                                   k, d.E, d.H, ws);
+                                                                   k, d.E, d.H, d.in_scale, d.Er, ws);
   return cudaGetLastError();
 }
 

@@ -23,4 +23,5 @@ from .inputs import (  # noqa: F401
     LinearInputs,
     make_linear_inputs,
     make_router_weight,
+    make_input_scales,
 )

@@ -364,3 +364,15 @@ def make_router_weight(cfg: LayerConfig) -> np.ndarray:
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(cfg.seed, spawn_key=(4,))))
     w = rng.standard_normal((cfg.num_experts, cfg.hidden), dtype=np.float32) / np.float32(np.sqrt(cfg.hidden))
     return f32_to_bf16_bits(w)
+
+
+def make_input_scales(cfg: LayerConfig) -> np.ndarray:
+    """W4A4 input scales [E][2] (w13, w2) for the comparison variant: static
+    calibration constants amax / (6 * 448) with amax = 4.5 for x ~ N(0, 1)
+    and 0.125 * sqrt(H) for the hidden h (its typical largest magnitude for
+    N(0, 0.02) weights); shared experts get 1.0 (unused, they stay W4A16)."""
+    E = cfg.num_experts + cfg.shared
+    s = np.ones((E, 2), np.float32)
+    s[:cfg.num_experts, 0] = np.float32(4.5 / 2688.0)
+    s[:cfg.num_experts, 1] = np.float32(0.125 * np.sqrt(cfg.hidden) / 2688.0)
+    return s
