@@ -55,6 +55,8 @@ def _args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--w4a4", action="store_true",
+                    help="the W4A4 comparison variant (activations quantised to NVFP4 with input scales)")
     ap.add_argument("--router", action="store_true",
                     help="compute the router logits in the library (nvfp4_moe_forward_routed) inside each step")
     return ap.parse_args()
@@ -240,7 +242,7 @@ def run_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
 
     import nvfp4_weight_only_w4a16_gb300 as pkg
-    from synth import make_inputs, make_router_weight
+    from synth import make_inputs, make_router_weight, make_input_scales
     pkg.build()
     inp = make_inputs(args.workload)
     cfg = inp.config
@@ -249,6 +251,8 @@ def run_ours(args):
     layer = pkg.MoELayer(E, H, cfg.inter, T, k, device=dev.index, num_shared_experts=S)
     n_ours = 1 if T <= 16 else 6     # kernels of ours per forward (decode / prefill path)
     pkg.upload_layer(layer, inp.weights, dev)
+    if args.w4a4:
+        layer.nvfp4_moe_set_act_quant(torch.from_numpy(make_input_scales(cfg)).to(dev))
 
     logits = torch.from_numpy(inp.logits).to(dev)
     x = torch.from_numpy(inp.x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -392,7 +396,8 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "w4a16: e2m1*e4m3 weights -> fp16 mma, fp32 accumulate",
             "data": "synthetic (seeded PCG64, shapes of the pages' MTP decode step)",
-            "config": {"workload": _workload_desc(cfg) + (" + BF16 router linear" if args.router else ""),
+            "config": {"workload": _workload_desc(cfg) + (" + BF16 router linear" if args.router else "") +
+                                   (" [W4A4 comparison variant: NVFP4 activations]" if args.w4a4 else ""),
                        "distinct_experts": distinct,
                        "layer_weight_bytes_per_step": layer_bytes,
                        "layer_weight_gbs": layer_bytes / (ms / 1e3) / 1e9,

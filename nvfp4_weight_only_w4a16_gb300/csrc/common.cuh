@@ -118,17 +118,19 @@ __device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) 
 // ---------------------------------------------------------------------------
 // W4A4 activation quantisation (NVFP4 activations with a per-module input
 // scale is, the stock routed-expert format: "tenhkspark/GLM-5.3-Flash-NVFP4-
-// Wabi", opening summary).  Per block of 16 values: scale = E4M3(amax /
-// fl(6 is)), r = fl(1 / fl(scale * is)), code = E2M1(v * r); both conversions
-// round to nearest even and saturate.  The values returned are code * scale,
-// exact in FP16 and BF16; the input scale is applied after the dot product.
+// Wabi", opening summary).  With inv6 = fl(1 / fl(6 is)) per module, per
+// block of 16 values: scale = E4M3(fl(amax * inv6)), r = fl(1 / fl(scale *
+// is)), code = E2M1(fl(v * r)); both conversions round to nearest even and
+// saturate.  The values returned are code * scale, exact in FP16 and BF16;
+// the input scale is applied after the dot product.
 // ---------------------------------------------------------------------------
 struct ActBlockScale {
   uint32_t s2;  // f16x2 {scale, scale}
   float r;      // 1 / (scale * is), 0 when the scale is 0
 };
-__device__ __forceinline__ ActBlockScale act_block_scale(float amax, float is) {
-  const float st = __fdiv_rn(amax, __fmul_rn(6.0f, is));
+__device__ __forceinline__ float act_inv6(float is) { return __frcp_rn(__fmul_rn(6.0f, is)); }
+__device__ __forceinline__ ActBlockScale act_block_scale(float amax, float inv6, float is) {
+  const float st = __fmul_rn(amax, inv6);
   unsigned short sc;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(sc) : "f"(st));
   const uint32_t s2 = e4m3x2_to_f16x2(sc);
@@ -152,11 +154,11 @@ __device__ __forceinline__ uint32_t e2m1x8_rn(const float* v) {
 }
 
 // One block of 16 values -> 8 f16x2 of code * scale (in element order).
-__device__ __forceinline__ void act_quant16_f16(const float (&v)[16], float is, uint32_t (&out)[8]) {
+__device__ __forceinline__ void act_quant16_f16(const float (&v)[16], float is, float inv6, uint32_t (&out)[8]) {
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const ActBlockScale bs = act_block_scale(amax, is);
+  const ActBlockScale bs = act_block_scale(amax, inv6, is);
   float q[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) q[i] = __fmul_rn(v[i], bs.r);

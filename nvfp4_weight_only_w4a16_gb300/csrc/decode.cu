@@ -688,7 +688,7 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
   const uint8_t* xrow = nullptr;  // kXs: this lane's token row
   int seg_c0 = 0, m = 0, ng = 1, cu = 0, cb = 0, crg0 = 0, ccnt = 0;
   bool q4 = false;  // this piece's activations are quantised to NVFP4 (W4A4 routed expert)
-  float q4_is = 0.f;
+  float q4_is = 0.f, q4_inv6 = 0.f;
   bool fin_head = false, fin_tail = false;  // split segments this warp finished in the loop
   int issued = 0, consumed = 0;
 
@@ -717,7 +717,10 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
       const int row0 = rs.tch_r0[cu];
       m = rs.tch_m[cu];
       q4 = a.in_scale != nullptr && rs.tch_e[cu] < a.Er;
-      if (q4) q4_is = __ldg(a.in_scale + 2 * rs.tch_e[cu] + (kGateUp ? 0 : 1));
+      if (q4) {
+        q4_is = __ldg(a.in_scale + 2 * rs.tch_e[cu] + (kGateUp ? 0 : 1));
+        q4_inv6 = act_inv6(q4_is);
+      }
       ng = (m + 7) >> 3;
 #pragma unroll
       for (int rg = 0; rg < dec::kRG; ++rg)
@@ -766,7 +769,7 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
               v[2 * z] = __uint_as_float(w[z] << 16);
               v[2 * z + 1] = __uint_as_float(w[z] & 0xFFFF0000u);
             }
-            act_quant16_f16(v, q4_is, bw[gi]);
+            act_quant16_f16(v, q4_is, q4_inv6, bw[gi]);
           } else {
 #pragma unroll
             for (int z = 0; z < 8; ++z) {

@@ -448,23 +448,38 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             const float gsg = gs[0], gsu = gs[1];
             // W4A4 routed expert: h (rounded to BF16) is quantised to NVFP4 with the
             // w2 input scale; this warp's 16 gate lanes hold one 16-feature block
-            const bool q4 = a.in_scale != nullptr && e < a.Er;
-            const float is1 = q4 ? __ldg(a.in_scale + 2 * e + 1) : 0.f;
+            if (a.in_scale != nullptr && e < a.Er) {
+              const float is1 = __ldg(a.in_scale + 2 * e + 1), inv6 = act_inv6(is1);
+              float hv[16], am[16];
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const float mine = __uint_as_float(v[jj]);
-              const float partner = __shfl_xor_sync(0xffffffffu, mine, 8);
-              float hv = 0.f;
-              if (is_gate) hv = __bfloat162float(__float2bfloat16_rn(silu(gsg * mine) * (gsu * partner)));
-              if (q4) {
-                float am = is_gate ? fabsf(hv) : 0.f;  // lane bit 3 (gate / up) is never flipped
-                am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-                am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-                am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
-                am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 16));
-                hv = act_quant1(hv, act_block_scale(am, is1));
+              for (int jj = 0; jj < 16; ++jj) {
+                const float mine = __uint_as_float(v[jj]);
+                const float partner = __shfl_xor_sync(0xffffffffu, mine, 8);
+                hv[jj] = is_gate ? __bfloat162float(__float2bfloat16_rn(silu(gsg * mine) * (gsu * partner))) : 0.f;
+                am[jj] = fabsf(hv[jj]);
               }
-              if (is_gate && col + jj < rows) a.h[(size_t)(row0 + col + jj) * a.I + f] = __float2bfloat16_rn(hv);
+              // block maxima over the 16 gate lanes (lane bit 3, gate / up, is never flipped)
+#pragma unroll
+              for (int o = 1; o <= 16; o <<= 1) {
+                if (o == 8) continue;
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) am[jj] = fmaxf(am[jj], __shfl_xor_sync(0xffffffffu, am[jj], o));
+              }
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) {
+                const float q = act_quant1(hv[jj], act_block_scale(am[jj], inv6, is1));
+                if (is_gate && col + jj < rows) a.h[(size_t)(row0 + col + jj) * a.I + f] = __float2bfloat16_rn(q);
+              }
+            } else {
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) {
+                const float mine = __uint_as_float(v[jj]);
+                const float partner = __shfl_xor_sync(0xffffffffu, mine, 8);
+                if (is_gate && col + jj < rows) {
+                  const float g = gsg * mine, u = gsu * partner;
+                  a.h[(size_t)(row0 + col + jj) * a.I + f] = __float2bfloat16_rn(silu(g) * u);
+                }
+              }
             }
           } else {
             const int d = 128 * nb + i;

@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16*
     for (int v = lane; v < H / 8; v += 32) dst[v] = __ldg(src + v);
     return;
   }
-  const float is = __ldg(in_scale + 2 * e);
+  const float is = __ldg(in_scale + 2 * e), inv6 = act_inv6(is);
   for (int b = lane; b < H / 16; b += 32) {  // one 16-element block per lane
     const uint4 u0 = __ldg(src + 2 * b), u1 = __ldg(src + 2 * b + 1);
     const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16*
       v[2 * z + 1] = __uint_as_float(w[z] & 0xFFFF0000u);
     }
     uint32_t o[8];
-    act_quant16_f16(v, is, o);
+    act_quant16_f16(v, is, inv6, o);
 #pragma unroll
     for (int z = 0; z < 8; ++z) o[z] = f16x2_to_bf16x2(o[z]);
     dst[2 * b] = make_uint4(o[0], o[1], o[2], o[3]);

@@ -337,11 +337,11 @@ def moe_forward(logits, x_bits, weights, k: int, tokens=None, return_parts=False
 # expert; "tacos4me/GLM-5.3-Flash-NVFP4-FP8ATTN-512K", Input-scales provenance:
 # a placeholder input_scale of 1.0 made small-amax blocks underflow to zero).
 # The block rule is the weight rule applied to activations: per 16 consecutive
-# K elements, scale = E4M3(amax / (6 * input_scale)), code = E2M1(v *
+# K elements, scale = E4M3(amax * (1 / (6 * input_scale))), code = E2M1(v *
 # (1 / (scale * input_scale))), both round-to-nearest-even, saturating; value
 # = code * scale * input_scale.  The decisions are taken in FP32, in this
-# order of operations (one reciprocal per block, then a product per element),
-# as the kernels take them; the pages fix neither.  h is rounded to BF16
+# order of operations (one reciprocal of 6 * input_scale per module, one per
+# block, then products), as the kernels take them; the pages fix neither.  h is rounded to BF16
 # before it is quantised, as it is between the GEMMs of the W4A16 layer.
 
 _E2M1_POS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
@@ -379,8 +379,8 @@ def quantize_act_nvfp4(v, input_scale: float):
     isf = np.float32(input_scale)
     blk = v.reshape(v.shape[:-1] + (v.shape[-1] // 16, 16))
     amax = np.max(np.abs(blk), axis=-1)
-    denom = np.float32(np.float32(6.0) * isf)
-    sc = encode_e4m3((amax / denom).astype(np.float32))
+    inv6 = np.float32(np.float32(1.0) / np.float32(np.float32(6.0) * isf))
+    sc = encode_e4m3((amax * inv6).astype(np.float32))
     sv = decode_e4m3(sc)
     step = (sv.astype(np.float32) * isf).astype(np.float32)
     with np.errstate(divide="ignore", invalid="ignore"):
