@@ -206,7 +206,8 @@ __device__ void route_block(const FusedArgs& a, RouteSmem& rs, uint8_t* xs, unsi
   // loads first: token `warp`'s logits, and this warp's share of one x row
   uint32_t key[8];
   float val[8];
-  if (warp < T && !a.linear) warp_load_logits(a.logits, a.logits_bf16, Er, warp, key, val);
+  // the logit loads are only issued here; their keys are taken after the x loads below are issued too
+  if (warp < T && !a.linear) warp_issue_logits(a.logits, a.logits_bf16, Er, warp, val);
   const int wpt = dec::kWarps / T;  // warps per token row of x
   const int xt = warp / wpt, xpart = warp - xt * wpt;
   const int xcols = a.linear ? a.I : a.H;  // a linear's x rows have its K = I columns
@@ -234,6 +235,7 @@ __device__ void route_block(const FusedArgs& a, RouteSmem& rs, uint8_t* xs, unsi
       }
     }
   }
+  if (warp < T && !a.linear) warp_logit_keys(val, key);
   if (tid < 16) rs.xmax[tid] = 0u;
   if (tid <= E) rs.off[tid] = 0;  // rows per expert, then offsets
   if (tid == 0) rs.nan = 0;
@@ -568,7 +570,9 @@ __device__ __forceinline__ CtaWork cta_work(long long units, int per_expert, int
 // weights only.  Every stage's weight copies are issued before its activation
 // copies; at the start of the down phase all S-1 weight copies go out before
 // the wait for the expert's h, so they land while the gate/up phase finishes.
-template <bool kGateUp, int S, int NG, bool kXs>
+// kQ4: the W4A4 variant is compiled in (the per-lane activation quantisation
+// sits in the hot loop, so the W4A16 kernels leave it out).
+template <bool kGateUp, int S, int NG, bool kXs, bool kQ4>
 __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint64_t* bars, uint32_t& ring_it,
                           const CtaWork& cw, unsigned long long* tr, float* part_s, int* cnt_s,
                           const uint8_t* xs) {
@@ -716,7 +720,7 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
       cw.piece(p, &cu, &cb, &crg0, &ccnt);
       const int row0 = rs.tch_r0[cu];
       m = rs.tch_m[cu];
-      q4 = a.in_scale != nullptr && rs.tch_e[cu] < a.Er;
+      q4 = kQ4 && a.in_scale != nullptr && rs.tch_e[cu] < a.Er;
       if (q4) {
         q4_is = __ldg(a.in_scale + 2 * rs.tch_e[cu] + (kGateUp ? 0 : 1));
         q4_inv6 = act_inv6(q4_is);
@@ -762,7 +766,7 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
           const uint8_t* pa = st + dec::kStB + srow * dec::kRowPitch + q * 32;
           const uint4 u0 = *reinterpret_cast<const uint4*>(pa), u1 = *reinterpret_cast<const uint4*>(pa + 16);
           const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-          if (q4) {  // this lane's 16 K elements are one NVFP4 block
+          if (kQ4 && q4) {  // this lane's 16 K elements are one NVFP4 block
             float v[16];
 #pragma unroll
             for (int z = 0; z < 8; ++z) {
@@ -894,6 +898,7 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
   // ---- end of phase: one fence covers every store and partial sum above ----
   if (!dead) {
     const uint64_t t_fin = tr ? now_ns() : 0;
+    bool fin_global = false;
     __threadfence();
     __syncwarp();
     // pass 1: count the split segments that went through global slots in; the
@@ -946,10 +951,14 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
       else finish_down(a, rs, u, b, rg0, pcnt, acc, lane);
       if (head) fin_head = true;
       else fin_tail = true;
+      fin_global = true;
     }
-    // pass 2: after one more fence, signal every piece this warp finished
-    __threadfence();
-    __syncwarp();
+    // pass 2: after one more fence (only if pass 1 wrote results), signal
+    // every piece this warp finished
+    if (fin_global) {
+      __threadfence();
+      __syncwarp();
+    }
     for (int f = ibeg; f < iend;) {
       const int p = f / nch, c0 = f - (f / nch) * nch;
       const int c1 = min(nch, c0 + (iend - f));
@@ -979,7 +988,7 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
   ring_it = it0 + (uint32_t)issued;
 }
 
-template <int S, int NG>
+template <int S, int NG, bool kQ4>
 __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const uint64_t t_start = now_ns();
@@ -1028,9 +1037,9 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
   if (!a.linear) {  // a dense linear has no gate/up phase: its x goes straight to the down GEMV
     const CtaWork w1 = cta_work((long long)U * (2 * a.I / 16), 2 * a.I / 16, a.H / kChunk);
     if (xs)
-      run_phase<true, S, NG, true>(a, rs, ring, bars, ring_it, w1, tr, slots1, cnt_all, xs);
+      run_phase<true, S, NG, true, kQ4>(a, rs, ring, bars, ring_it, w1, tr, slots1, cnt_all, xs);
     else
-      run_phase<true, S, NG, false>(a, rs, ring, bars, ring_it, w1, tr, slots1, cnt_all, nullptr);
+      run_phase<true, S, NG, false, kQ4>(a, rs, ring, bars, ring_it, w1, tr, slots1, cnt_all, nullptr);
     if (tr && lane == 0) tr[2] = now_ns();
     if (a.slot_cols && a.slot_sets == 2) {
       slots2 = slots + slot_floats;  // the down phase has its own slots: no CTA barrier here
@@ -1041,7 +1050,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
     }
   }
   const CtaWork w2 = cta_work((long long)U * (a.H / 16), a.H / 16, a.I / kChunk);
-  run_phase<false, S, NG, false>(a, rs, ring, bars, ring_it, w2, tr, slots2,
+  run_phase<false, S, NG, false, kQ4>(a, rs, ring, bars, ring_it, w2, tr, slots2,
                                  cnt_all + (a.slot_sets == 2 ? 16 : 0), nullptr);
   if (tr && lane == 0) tr[4] = now_ns();
   if (!a.linear)
@@ -1134,9 +1143,11 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
     int dev = 0, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    const void* fns[] = {(const void*)decode_fused_kernel<2, 1>, (const void*)decode_fused_kernel<3, 1>,
-                         (const void*)decode_fused_kernel<4, 1>, (const void*)decode_fused_kernel<5, 1>,
-                         (const void*)decode_fused_kernel<2, 2>, (const void*)decode_fused_kernel<3, 2>};
+    const void* fns[] = {(const void*)decode_fused_kernel<2, 1, false>, (const void*)decode_fused_kernel<3, 1, false>,
+                         (const void*)decode_fused_kernel<4, 1, false>, (const void*)decode_fused_kernel<5, 1, false>,
+                         (const void*)decode_fused_kernel<2, 2, false>, (const void*)decode_fused_kernel<3, 2, false>,
+                         (const void*)decode_fused_kernel<3, 1, true>,  (const void*)decode_fused_kernel<2, 2, true>,
+                         (const void*)decode_fused_kernel<3, 2, true>};
     for (const void* f : fns)
       if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     if (e != cudaSuccess) return e;
@@ -1205,13 +1216,19 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = route_only ? 0 : 1;
-  if (!small) return plan.stages == 2 ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<2, 2>, a)
-                                      : cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 2>, a);
+  if (d.in_scale) {  // W4A4: its own instantiations (three-stage rings for T <= 8)
+    if (!small) return plan.stages == 2 ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<2, 2, true>, a)
+                                        : cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 2, true>, a);
+    if (plan.stages != 3) return cudaErrorInvalidConfiguration;  // the ring depth must match the kernel's
+    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 1, true>, a);
+  }
+  if (!small) return plan.stages == 2 ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<2, 2, false>, a)
+                                      : cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 2, false>, a);
   switch (plan.stages) {
-    case 2: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<2, 1>, a);
-    case 3: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 1>, a);
-    case 4: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<4, 1>, a);
-    default: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<5, 1>, a);
+    case 2: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<2, 1, false>, a);
+    case 3: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 1, false>, a);
+    case 4: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<4, 1, false>, a);
+    default: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<5, 1, false>, a);
   }
 }
 

@@ -58,6 +58,20 @@ __device__ __forceinline__ void warp_load_logits(const void* logits, int bf16, i
   for (int i = 0; i < 8; ++i) key[i] = float_key(val[i]);
 }
 
+// The same in two steps, so that other loads can be issued in between.
+__device__ __forceinline__ void warp_issue_logits(const void* logits, int bf16, int E, int t, float (&val)[8]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    val[i] = e < E ? load_logit(logits, bf16, (size_t)t * E + e) : 0.f;
+  }
+}
+__device__ __forceinline__ void warp_logit_keys(const float (&val)[8], uint32_t (&key)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) key[i] = float_key(val[i]);
+}
+
 // The k largest keys of the warp (k <= min(E, 16)) in order: largest value
 // first, the lower expert index first among equal values.  Each round takes
 // the warp maximum key (redux.sync), then the lowest index holding it.  Lane
