@@ -215,6 +215,19 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def replica_throughput(ms, ms_e2e, tokens_per_rank, ws, device):
+    """Replicas only: every rank runs its own copy of the layer on its own
+    tokens.  The step time is the slowest rank's (MAX over ranks), and the
+    whole job's throughput is all ranks' tokens over that time.  Returns
+    (ms, ms_e2e, tokens/s, e2e tokens/s)."""
+    import torch
+    if ws > 1:
+        t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, ms_e2e = float(t[0]), float(t[1])
+    return ms, ms_e2e, ws * tokens_per_rank / (ms / 1e3), ws * tokens_per_rank / (ms_e2e / 1e3)
+
+
 def _traffic_for(kernel_src):
     """DRAM traffic per launch from the committed ncu summary, if the kernel
     source is unchanged since it was captured; else None."""
@@ -345,12 +358,7 @@ def run_ours(args):
 
     ms = statistics.mean(step_ms)
     ms_e2e = statistics.mean(e2e_ms)
-    if ws > 1:
-        t = torch.tensor([ms, ms_e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
-    value = ws * T / (ms / 1e3)
-    value_e2e = ws * T / (ms_e2e / 1e3)
+    ms, ms_e2e, value, value_e2e = replica_throughput(ms, ms_e2e, T, ws, dev)
 
     I = cfg.inter
     gateup_ms = stage_ms[1] / max(nfwd, 1)
@@ -575,12 +583,7 @@ def run_linear(args):
     if st != 0:
         raise RuntimeError(f"device status {pkg.STATUS[st]} after the timed region")
 
-    ms, ms_e2e = statistics.mean(step_ms), statistics.mean(e2e_ms)
-    if ws > 1:
-        t = torch.tensor([ms, ms_e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
-    value, value_e2e = ws * T / (ms / 1e3), ws * T / (ms_e2e / 1e3)
+    ms, ms_e2e, value, value_e2e = replica_throughput(statistics.mean(step_ms), statistics.mean(e2e_ms), T, ws, dev)
     kern_ms = stage_ms[2] / max(nfwd, 1)   # the GEMV / GEMM launch (tables kernel excluded)
     wbytes = cfg.weight_bytes
     if decode:
