@@ -19,6 +19,13 @@
  * ("GLM-5.3-Flash on Blackwell", The model loaded, served an API, and produced
  * garbage).  The 4-bit values are OCP MX E2M1, the group scales OCP E4M3.
  *
+ * Beyond that forward the same kernels serve: a shared expert
+ * (config.num_shared_experts), the routing variants (nvfp4_moe_set_scoring),
+ * the BF16 router linear on the GPU (nvfp4_moe_set_router /
+ * nvfp4_moe_forward_routed), the W4A4 comparison variant
+ * (nvfp4_moe_set_act_quant), a dense W4A16 NVFP4 linear (nvfp4_linear_*) and
+ * an allocation-free decode forward (nvfp4_moe_forward_decode_static).
+ *
  * Conventions for every call:
  *   - returns a status, never throws, never prints unless NVFP4_MOE_LOG=1;
  *   - device pointers are CUDA global-memory pointers on the handle's device;
