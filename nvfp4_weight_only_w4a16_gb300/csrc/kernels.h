@@ -68,7 +68,7 @@ struct LayerDims {
                                     // caller passes tensor scales with them folded in
 };
 
-constexpr int kRankTokens = 256;      // tokens per rank block in the prefill routing
+constexpr int kRankTokens = 64;       // tokens per rank block in the prefill routing (8 per warp)
 constexpr int kTileRows = 128;        // max routed rows per prefill m-tile (MMA N)
 constexpr int kDecodeMaxTokens = 16;
 constexpr int kDecodeWarpsPerSm = 16;  // warps of the decode kernel's one CTA per SM

@@ -45,13 +45,16 @@ __global__ void __launch_bounds__(256) route_rank_kernel(int T, int k, int E, Wo
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x) (&cnt[0][0])[i] = 0;
   __syncthreads();
-  const int t = blockIdx.x * kRankTokens + warp * 32 + lane;
-  const bool valid = t < T;
+  // kRankTokens / 8 tokens per warp, one per lane: the turn-taking loop below
+  // is serial, so a short one (and more blocks) routes a chunk faster
+  constexpr int kPerWarp = kRankTokens / 8;
+  const int t = blockIdx.x * kRankTokens + warp * kPerWarp + lane;
+  const bool valid = lane < kPerWarp && t < T;
   int ids[16], rank[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) ids[j] = (valid && j < k) ? ws.ids[(size_t)t * k + j] : -1;
   // lanes take turns in token order; each bumps its experts' counters
-  for (int l = 0; l < 32; ++l) {
+  for (int l = 0; l < kPerWarp; ++l) {
     if (lane == l) {
 #pragma unroll
       for (int j = 0; j < 16; ++j)
@@ -83,7 +86,18 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int nblocks, int E, Wo
   const int e = threadIdx.x;
   int running = 0;
   if (e < E) {
-    for (int c = 0; c < nblocks; ++c) {
+    int c = 0;
+    for (; c + 8 <= nblocks; c += 8) {  // eight loads in flight, then the running sums
+      int v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = ws.blk_counts[(size_t)(c + q) * E + e];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        ws.blk_base[(size_t)(c + q) * E + e] = running;
+        running += v[q];
+      }
+    }
+    for (; c < nblocks; ++c) {
       const int v = ws.blk_counts[(size_t)c * E + e];
       ws.blk_base[(size_t)c * E + e] = running;
       running += v;
