@@ -240,9 +240,10 @@ nvfp4_moe_status nvfp4_moe_debug_logits(nvfp4_moe_t h, float* logits, cudaStream
  * > 0, else NVFP4_MOE_ERR_BAD_SCALE -- an input scale of 0 zeroes every expert,
  * "GLM-5.3-Flash on Blackwell", The model loaded, served an API, and produced
  * garbage), every routed expert quantises its input x and its hidden h
- * (rounded to BF16 first) per 16 elements: scale = E4M3(amax / (6 is)),
- * code = E2M1(v / (scale is)), round-to-nearest-even, saturating; the input
- * scales multiply the tensor scales after the dot products.  The shared
+ * (rounded to BF16 first) per 16 elements: scale = E4M3(amax * fl(1/fl(6 is))),
+ * code = E2M1(v * fl(1/fl(scale is))), round-to-nearest-even, saturating,
+ * in FP32 in that order; the input scales multiply the tensor scales after
+ * the dot products.  The shared
  * expert stays W4A16.  The quantised values are exact in BF16/FP16, so the
  * products run on the same tensor-core paths as W4A16.  NULL turns the
  * variant off.  Synchronous (reads the scales back to check them). */
