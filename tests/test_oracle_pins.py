@@ -202,6 +202,8 @@ def pin_ffn_closed_form(o):
     w = _const_expert(H, I, 0x1, 0x1, 0x1, 0x38, [1.0, 1.0, 1.0])
     y = o.expert_ffn(w, 0, np.ones((1, H)))
     assert np.all(y == 2.0 ** 22), y[0, :4]
+    # its hidden activation: g = u = 0.5 * 256 = 128, silu(128) = 128 in float64, h = 2^14
+    assert np.all(o.expert_hidden(w, 0, np.ones((1, H))) == 2.0 ** 14)
     # asymmetric: gate -0.5*0.125, up 3*0.5, down 2*0.25; x = 1/64
     H, I = 64, 32
     w = _const_expert(H, I, 0x9, 0x5, 0x4, 0x38, [0.125, 0.5, 0.25])
