@@ -1,0 +1,61 @@
+"""Host-side guarantees about the product path (no GPU needed).
+
+* The package and its library never reach the oracle: no file of the
+  package imports, opens or names it, so no result can come from a CPU path.
+* A missing library is an error, never a fallback.
+* The benchmark reports DRAM traffic only while the kernel source is the one
+  the committed ncu record was taken from.
+"""
+import hashlib
+import json
+import os
+import re
+
+import pytest
+
+import nvfp4_weight_only_w4a16_gb300 as P
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+PKG = os.path.join(ROOT, "nvfp4_weight_only_w4a16_gb300")
+
+
+def _package_files():
+    for d, _, files in os.walk(PKG):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                yield os.path.join(d, f)
+    yield os.path.join(ROOT, "include", "nvfp4_moe.h")
+
+
+def test_package_never_reaches_the_oracle():
+    pat = re.compile(r"\boracle\b")
+    for path in _package_files():
+        text = open(path, encoding="utf-8").read()
+        for ln, line in enumerate(text.splitlines(), 1):
+            assert not pat.search(line), f"{os.path.relpath(path, ROOT)}:{ln}: {line.strip()}"
+
+
+def test_missing_library_is_an_error(tmp_path):
+    with pytest.raises(FileNotFoundError):
+        P.load_library(str(tmp_path / "libnvfp4moe.so"))
+
+
+def test_traffic_record_follows_the_kernel_source(tmp_path, monkeypatch):
+    import bench
+    src = tmp_path / "kernel.cu"
+    src.write_text("// kernel source v1\n")
+    rec = tmp_path / "record.json"
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()
+    rec.write_text(json.dumps({"source_sha256": sha, "dram_bytes_per_launch": 12345}))
+    monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(rec))
+    assert bench._traffic_for(str(src)) == 12345
+    src.write_text("// kernel source v2\n")   # the kernel changed since the capture
+    assert bench._traffic_for(str(src)) is None
+
+
+def test_committed_traffic_record_is_consistent():
+    rec = json.load(open(os.path.join(ROOT, "profiles", "decode_fused_kernel_decode_mtp.json")))
+    assert rec["dram_bytes_per_launch"] == rec["dram_bytes_read_per_launch"] + rec["dram_bytes_write_per_launch"]
+    src = os.path.join(ROOT, rec["source_file"])
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["source_sha256"]:
+        pytest.skip("decode.cu changed since the committed ncu capture: the bench reports traffic = null")
