@@ -565,9 +565,9 @@ __device__ __forceinline__ CtaWork cta_work(long long units, int per_expert, int
   return w;
 }
 
-// kXs (gate/up only): the routed tokens' activations are already in shared
-// memory as prescaled FP16 rows (xs, xs_pitch bytes apart), so stages carry
-// weights only.  Every stage's weight copies are issued before its activation
+// kXs: the routed tokens' activations are already in shared memory as
+// prescaled FP16 rows (xs, xs_pitch bytes apart), so stages carry weights
+// only (the gate/up phase of few-token steps, and a dense linear's one phase).  Every stage's weight copies are issued before its activation
 // copies; at the start of the down phase all S-1 weight copies go out before
 // the wait for the expert's h, so they land while the gate/up phase finishes.
 // kQ4: the W4A4 variant is compiled in (the per-lane activation quantisation
@@ -578,7 +578,7 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
                           const uint8_t* xs) {
   const int kStageBytes = a.stage_bytes;
   const int srows = dec::stage_rows(a.T);  // activation rows a stage holds
-  constexpr bool kActCopies = !(kGateUp && kXs);
+  constexpr bool kActCopies = !kXs;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3, r0 = lane >> 2;
   const int nch = cw.nch;
   const int gu_units = 2 * a.I / 16;
@@ -988,7 +988,9 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
   ring_it = it0 + (uint32_t)issued;
 }
 
-template <int S, int NG, bool kQ4>
+// kLin: a dense linear with its x staged in shared memory (its one phase reads
+// the tokens' rows from there); the other linear cases run the general kernel.
+template <int S, int NG, bool kQ4, bool kLin = false>
 __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const uint64_t t_start = now_ns();
@@ -1034,7 +1036,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
   uint32_t ring_it = 0;
   float* slots1 = a.slot_cols ? slots : nullptr;
   float* slots2 = slots1;
-  if (!a.linear) {  // a dense linear has no gate/up phase: its x goes straight to the down GEMV
+  if (!kLin && !a.linear) {  // a dense linear has no gate/up phase: its x goes straight to the down GEMV
     const CtaWork w1 = cta_work((long long)U * (2 * a.I / 16), 2 * a.I / 16, a.H / kChunk);
     if (xs)
       run_phase<true, S, NG, true, kQ4>(a, rs, ring, bars, ring_it, w1, tr, slots1, cnt_all, xs);
@@ -1050,8 +1052,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
     }
   }
   const CtaWork w2 = cta_work((long long)U * (a.H / 16), a.H / 16, a.I / kChunk);
-  run_phase<false, S, NG, false, kQ4>(a, rs, ring, bars, ring_it, w2, tr, slots2,
-                                 cnt_all + (a.slot_sets == 2 ? 16 : 0), nullptr);
+  if constexpr (kLin)
+    run_phase<false, S, NG, true, false>(a, rs, ring, bars, ring_it, w2, tr, slots2, cnt_all, xs);
+  else
+    run_phase<false, S, NG, false, kQ4>(a, rs, ring, bars, ring_it, w2, tr, slots2,
+                                        cnt_all + (a.slot_sets == 2 ? 16 : 0), nullptr);
   if (tr && lane == 0) tr[4] = now_ns();
   if (!a.linear)
     combine_tasks(a, rs, (long long)blockIdx.x * dec::kWarps + warp, (long long)gridDim.x * dec::kWarps, lane);
@@ -1104,8 +1109,12 @@ static DecodeSmemPlan plan_smem(int T, int H, int linear, bool no_xs, int smem_m
   const size_t base = ((sizeof(RouteSmem) + 127) & ~size_t(127)) + 128 * 8 + 128;
   const size_t ring1 = (size_t)dec::kWarps * dec::stage_bytes_for(T);  // one stage per warp
   const int cap = decode_stage_cap();
-  if (linear && T <= 8) {  // one phase: one set of slots, no staged activations, the deepest ring that fits
+  if (linear && T <= 8) {  // one phase: one set of slots; x staged (H = the linear's K) when it fits
     const size_t slot_b = (size_t)dec::kSlots * 64 * T * 4;
+    const size_t xs_b = (size_t)T * (2 * H + 16);
+    for (int S = cap; S >= 3; --S)
+      if (base + S * ring1 + slot_b + xs_b <= (size_t)smem_max)
+        return DecodeSmemPlan{base + S * ring1 + slot_b + xs_b, S, T, 1, 2 * H + 16};
     for (int S = cap; S > 3; --S)
       if (base + S * ring1 + slot_b <= (size_t)smem_max) return DecodeSmemPlan{base + S * ring1 + slot_b, S, T, 1, 0};
     return DecodeSmemPlan{base + 3 * ring1 + slot_b, cap < 3 ? cap : 3, T, 1, 0};
@@ -1147,7 +1156,10 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
                          (const void*)decode_fused_kernel<4, 1, false>, (const void*)decode_fused_kernel<5, 1, false>,
                          (const void*)decode_fused_kernel<2, 2, false>, (const void*)decode_fused_kernel<3, 2, false>,
                          (const void*)decode_fused_kernel<3, 1, true>,  (const void*)decode_fused_kernel<2, 2, true>,
-                         (const void*)decode_fused_kernel<3, 2, true>};
+                         (const void*)decode_fused_kernel<3, 2, true>,
+                         (const void*)decode_fused_kernel<3, 1, false, true>,
+                         (const void*)decode_fused_kernel<4, 1, false, true>,
+                         (const void*)decode_fused_kernel<5, 1, false, true>};
     for (const void* f : fns)
       if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     if (e != cudaSuccess) return e;
@@ -1155,7 +1167,7 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
   }
   const bool small = T <= 8;
   // W4A4 quantises activations from their BF16 values: no staged FP16 copy
-  const DecodeSmemPlan plan = plan_smem(T, d.H, d.linear, d.in_scale != nullptr, smem_max);
+  const DecodeSmemPlan plan = plan_smem(T, d.linear ? d.I : d.H, d.linear, d.in_scale != nullptr, smem_max);
   if (plan.bytes > (size_t)smem_max) return cudaErrorInvalidConfiguration;
   const ExpertLayout L = d.linear ? linear_layout(d.H, d.I) : expert_layout(d.H, d.I);
   FusedArgs a{};
@@ -1216,6 +1228,14 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = route_only ? 0 : 1;
+  if (d.linear && plan.xs_pitch > 0) {  // a dense linear with its x staged in shared memory
+    switch (plan.stages) {
+      case 3: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 1, false, true>, a);
+      case 4: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<4, 1, false, true>, a);
+      case 5: return cudaLaunchKernelEx(&cfg, decode_fused_kernel<5, 1, false, true>, a);
+      default: return cudaErrorInvalidConfiguration;  // the ring depth must match the kernel's
+    }
+  }
   if (d.in_scale) {  // W4A4: its own instantiations (three-stage rings for T <= 8)
     if (!small) return plan.stages == 2 ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<2, 2, true>, a)
                                         : cudaLaunchKernelEx(&cfg, decode_fused_kernel<3, 2, true>, a);
