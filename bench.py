@@ -228,15 +228,24 @@ def replica_throughput(ms, ms_e2e, tokens_per_rank, ws, device):
     return ms, ms_e2e, ws * tokens_per_rank / (ms / 1e3), ws * tokens_per_rank / (ms_e2e / 1e3)
 
 
+def code_fingerprint(text):
+    """sha256 of a CUDA/C++ source with its comments and whitespace removed:
+    it changes when the code does, not when a comment does."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return hashlib.sha256(re.sub(r"\s+", "", text).encode()).hexdigest()
+
+
 def _traffic_for(kernel_src):
-    """DRAM traffic per launch from the committed ncu summary, if the kernel
-    source is unchanged since it was captured; else None."""
+    """DRAM traffic per launch from the committed ncu summary, if the kernel's
+    code is unchanged since it was captured; else None."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             rec = json.load(f)
-        with open(kernel_src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
-        if rec.get("source_sha256") == sha:
+        with open(kernel_src, encoding="utf-8") as f:
+            fp = code_fingerprint(f.read())
+        if rec.get("code_sha256") == fp:
             return rec.get("dram_bytes_per_launch")
     except Exception:
         pass

@@ -11,21 +11,23 @@
 //
 // Design (GB300):
 //  * one launch per forward, one 16-warp CTA per SM (cooperative, so all CTAs
-//    are resident); every CTA routes the <= 16 tokens itself (a few KB of
-//    logits; one thread per logit ranks it against its row in shared memory
-//    when T*E <= 512), so no routing tables cross CTAs before the GEMVs start;
+//    are resident); every CTA routes the <= 16 tokens itself (one warp per
+//    token: redux.sync top-k over its logits, then the scoring rule), so no
+//    routing tables cross CTAs before the GEMVs start;
 //  * work split in two levels, so every SM streams the same number of weight
 //    bytes whatever the routing: each CTA takes an equal share of the 16-row
 //    groups of the touched experts' matrices over the whole K axis (no row's
 //    sum crosses CTAs); inside the CTA the (64-row piece, 64-wide K chunk)
-//    items are cut into equal contiguous ranges, one per warp, and partial
-//    sums of a piece split across warps meet in shared memory (FP32 slots;
-//    for more than 8 tokens, per-warp global slots), the last warp to arrive
-//    finishing the piece;
-//  * each warp runs its own ring in shared memory (3 stages): one lane
-//    issues cp.async.bulk copies of a chunk's codes (2 KB), scales (256 B) and
+//    items are cut into contiguous ranges of equal estimated time, one per
+//    warp, and partial sums of a piece split across warps meet in shared
+//    memory (FP32 slots; global slots when the shared ones do not fit), the
+//    last warp to arrive finishing the piece;
+//  * each warp runs its own ring in shared memory (2 to 5 stages, as deep as
+//    the shared memory left allows): one lane issues cp.async.bulk copies of
+//    a chunk's codes (up to 2 KB), scales and -- unless the tokens'
+//    activations are staged once per CTA in shared memory (few tokens) --
 //    the routed rows' activation slices (128 B each) onto the stage's
-//    mbarrier, so no per-thread copy is in flight when a warp fences;
+//    mbarrier;
 //  * dequantisation: hardware E2M1->FP16 converts (two weights each) times the
 //    E4M3 group scale in FP16 (exact); the dot products run on mma.sync
 //    m16n8k16 (FP16 in, FP32 accumulate) -- about one instruction per weight;
@@ -37,7 +39,11 @@
 //  * the down GEMV of expert u starts once all gate/up rows of u are done
 //    (per-expert counter, bounded wait); the combine is spread over every
 //    warp as (64-wide slice of H, token) tasks, each starting once its slice
-//    is finished for every expert, summing in slot order.
+//    is finished for every expert, summing in slot order;
+//  * the same kernel runs a dense linear (one matrix, no routing, the down
+//    phase alone, rows written straight to out) and, as separate template
+//    instantiations, the W4A4 comparison variant (each lane quantises its
+//    16-element activation block to NVFP4 before the MMA).
 #include <cstdlib>
 
 #include "common.cuh"

@@ -6,7 +6,6 @@
 * The benchmark reports DRAM traffic only while the kernel source is the one
   the committed ncu record was taken from.
 """
-import hashlib
 import json
 import os
 import re
@@ -40,22 +39,24 @@ def test_missing_library_is_an_error(tmp_path):
         P.load_library(str(tmp_path / "libnvfp4moe.so"))
 
 
-def test_traffic_record_follows_the_kernel_source(tmp_path, monkeypatch):
+def test_traffic_record_follows_the_kernel_code(tmp_path, monkeypatch):
     import bench
     src = tmp_path / "kernel.cu"
-    src.write_text("// kernel source v1\n")
+    src.write_text("// v1\n__global__ void k(int* p) { p[0] = 1; }\n")
     rec = tmp_path / "record.json"
-    sha = hashlib.sha256(src.read_bytes()).hexdigest()
-    rec.write_text(json.dumps({"source_sha256": sha, "dram_bytes_per_launch": 12345}))
+    rec.write_text(json.dumps({"code_sha256": bench.code_fingerprint(src.read_text()), "dram_bytes_per_launch": 12345}))
     monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(rec))
     assert bench._traffic_for(str(src)) == 12345
-    src.write_text("// kernel source v2\n")   # the kernel changed since the capture
-    assert bench._traffic_for(str(src)) is None
+    src.write_text("/* a new comment */\n__global__ void k(int* p) {\n  p[0] = 1;  // same code\n}\n")
+    assert bench._traffic_for(str(src)) == 12345   # comments and layout do not matter
+    src.write_text("__global__ void k(int* p) { p[0] = 2; }\n")
+    assert bench._traffic_for(str(src)) is None    # the code changed since the capture
 
 
 def test_committed_traffic_record_is_consistent():
     rec = json.load(open(os.path.join(ROOT, "profiles", "decode_fused_kernel_decode_mtp.json")))
     assert rec["dram_bytes_per_launch"] == rec["dram_bytes_read_per_launch"] + rec["dram_bytes_write_per_launch"]
+    import bench
     src = os.path.join(ROOT, rec["source_file"])
-    if hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["source_sha256"]:
-        pytest.skip("decode.cu changed since the committed ncu capture: the bench reports traffic = null")
+    if bench.code_fingerprint(open(src, encoding="utf-8").read()) != rec["code_sha256"]:
+        pytest.skip("decode.cu's code changed since the committed ncu capture: the bench reports traffic = null")
