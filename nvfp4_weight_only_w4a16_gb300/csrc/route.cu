@@ -287,19 +287,20 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int k, int H, const
     acc[6] = fmaf(w, b.z, acc[6]);
     acc[7] = fmaf(w, b.w, acc[7]);
   }
-  if (kOutF32) {
+  if constexpr (kOutF32) {
     float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (size_t)t * H) + 2 * d8;
     o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    return;
-  }
-  uint32_t o[4];
+  } else {
+    uint32_t o[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-    o[q] = *reinterpret_cast<const uint32_t*>(&b2);
+    for (int q = 0; q < 4; ++q) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+      o[q] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + (size_t)t * H)[d8] =
+        make_uint4(o[0], o[1], o[2], o[3]);
   }
-  reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + (size_t)t * H)[d8] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 cudaError_t launch_combine(const LayerDims& d, int T, int top_k, const Workspace& ws, void* out, cudaStream_t st) {
