@@ -337,12 +337,15 @@ def moe_forward(logits, x_bits, weights, k: int, tokens=None, return_parts=False
 # expert; "tacos4me/GLM-5.3-Flash-NVFP4-FP8ATTN-512K", Input-scales provenance:
 # a placeholder input_scale of 1.0 made small-amax blocks underflow to zero).
 # The block rule is the weight rule applied to activations: per 16 consecutive
-# K elements, scale = E4M3(amax * (1 / (6 * input_scale))), code = E2M1(v *
-# (1 / (scale * input_scale))), both round-to-nearest-even, saturating; value
-# = code * scale * input_scale.  The decisions are taken in FP32, in this
-# order of operations (one reciprocal of 6 * input_scale per module, one per
-# block, then products), as the kernels take them; the pages fix neither.  h is rounded to BF16
-# before it is quantised, as it is between the GEMMs of the W4A16 layer.
+# K elements, scale = E4M3(amax / (6 * input_scale)) and code = E2M1(v /
+# (scale * input_scale)), both round-to-nearest-even and saturating; value =
+# code * scale * input_scale.  The pages fix no precision or order of
+# operations for these quotients, so the oracle takes the plain definition:
+# both quotients in float64.  For float32 operands that decides exactly as
+# real arithmetic does (a quotient of two floats with at most 28 significant
+# bits is either exactly on a rounding midpoint or at least 2**-33 of its
+# value away from it, far above float64's 2**-53 rounding).  h is rounded to
+# BF16 before it is quantised, as it is between the GEMMs of the W4A16 layer.
 
 _E2M1_POS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 
@@ -374,19 +377,21 @@ def encode_e4m3(v) -> np.ndarray:
 
 def quantize_act_nvfp4(v, input_scale: float):
     """v [..][K] (K % 16 == 0) -> its W4A4 value without the input scale,
-    code * scale (float64, exact), plus the E4M3 scale codes [..][K/16]."""
-    v = np.asarray(v, dtype=np.float32)
-    isf = np.float32(input_scale)
+    code * scale (float64, exact), plus the E4M3 scale codes [..][K/16].
+
+    Per block of 16: scale = E4M3_RNE(amax / (6 * is)), then code =
+    E2M1_RNE(v / (scale * is)) (a zero scale gives zero codes); every
+    quotient in float64 from the exact float64 values of v and is.
+    """
+    v = np.asarray(v).astype(np.float64)
+    isf = float(np.float32(input_scale))
     blk = v.reshape(v.shape[:-1] + (v.shape[-1] // 16, 16))
     amax = np.max(np.abs(blk), axis=-1)
-    inv6 = np.float32(np.float32(1.0) / np.float32(np.float32(6.0) * isf))
-    sc = encode_e4m3((amax * inv6).astype(np.float32))
+    sc = encode_e4m3(amax / (6.0 * isf))
     sv = decode_e4m3(sc)
-    step = (sv.astype(np.float32) * isf).astype(np.float32)
+    step = sv * isf
     with np.errstate(divide="ignore", invalid="ignore"):
-        rcp = (np.float32(1.0) / step).astype(np.float32)
-        q = (blk * rcp[..., None]).astype(np.float32)
-    q = np.where(step[..., None] > 0, q, np.float32(0))
+        q = np.where(step[..., None] > 0, blk / step[..., None], 0.0)
     codes = encode_e2m1(q)
     vals = decode_e2m1(codes) * sv[..., None]
     return vals.reshape(v.shape), sc

@@ -214,6 +214,11 @@ def pin_ffn_closed_form(o):
     want = 0.25 * 2.0 * I * h
     y = o.expert_ffn(w, 0, x)
     assert np.allclose(y, want, rtol=1e-14, atol=0), (y[0, 0], want)
+    # the same asymmetric expert's hidden activation (gate scale != up scale,
+    # gate code != up code): a swap of the two tensor scales or of gate and
+    # up inside expert_hidden changes it
+    hid = o.expert_hidden(w, 0, x)
+    assert np.allclose(hid, h, rtol=1e-14, atol=0), (hid[0, 0], h)
 
 
 def pin_identical_experts(o):
@@ -438,6 +443,17 @@ def pin_act_quant(o):
     assert np.all(o.quantize_act_nvfp4(small, 1.0)[0] == 0)
     cal = 1e-3 / (6 * 448)
     assert np.allclose(o.quantize_act_nvfp4(small, cal)[0] * cal, 1e-3, rtol=0.07)
+    # the plain definition decides exact midpoints by ties-to-even: with is =
+    # 0.9012069702148438 and a block scale of 1.0, v = 2.5 * is is exactly on
+    # the midpoint between codes 2 and 3, so it goes to 2 (an FP32 evaluation
+    # as v * fl(1 / fl(scale * is)) gives 2.5000002 and picks 3)
+    is_mid = np.float32(0.9012069702148438)
+    blk = np.zeros((1, 16), np.float64)
+    blk[0, 0] = float(np.float32(6.0 * float(is_mid)))
+    blk[0, 1] = 2.5 * float(is_mid)
+    assert float(np.float32(blk[0, 1])) == blk[0, 1]
+    vals, sc = o.quantize_act_nvfp4(blk.astype(np.float32), is_mid)
+    assert sc.tolist() == [[0x38]] and vals[0, 1] == 2.0 and vals[0, 0] == 6.0, (sc, vals[0, :2])
     # every value within half a grid step of its input (inside the range)
     rng = np.random.default_rng(12)
     xv = rng.standard_normal((64, 64)).astype(np.float32)
@@ -706,7 +722,33 @@ def _mut_e4m3_truncate(m):
     m.encode_e4m3 = f
 
 
-MUTANTS = [_mut_w4a4_input_scale_dropped, _mut_w4a4_h_unquantised, _mut_rne_ties_up, _mut_e4m3_truncate,
+def _mut_hidden_scale_swap(m):  # gate and up tensor scales swapped inside expert_hidden alone
+    def f(w, e, x):
+        wg, wu, _, gs = m._expert_mats(w, e)
+        x = np.asarray(x, dtype=np.float64)
+        return m.silu(gs[1] * (x @ wg.T)) * (gs[0] * (x @ wu.T))
+    m.expert_hidden = f
+
+
+def _mut_w4a4_fp32_order(m):  # the quantiser's quotients evaluated as FP32 products of reciprocals
+    def f(v, input_scale):
+        v = np.asarray(v, dtype=np.float32)
+        isf = np.float32(input_scale)
+        blk = v.reshape(v.shape[:-1] + (v.shape[-1] // 16, 16))
+        amax = np.max(np.abs(blk), axis=-1)
+        inv6 = np.float32(np.float32(1.0) / np.float32(np.float32(6.0) * isf))
+        sc = m.encode_e4m3((amax * inv6).astype(np.float32))
+        sv = m.decode_e4m3(sc)
+        step = (sv.astype(np.float32) * isf).astype(np.float32)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            rcp = (np.float32(1.0) / step).astype(np.float32)
+            q = (blk * rcp[..., None]).astype(np.float32)
+        q = np.where(step[..., None] > 0, q, np.float32(0))
+        return (m.decode_e2m1(m.encode_e2m1(q)) * sv[..., None]).reshape(v.shape), sc
+    m.quantize_act_nvfp4 = f
+
+
+MUTANTS = [_mut_hidden_scale_swap, _mut_w4a4_fp32_order, _mut_w4a4_input_scale_dropped, _mut_w4a4_h_unquantised, _mut_rne_ties_up, _mut_e4m3_truncate,
            _mut_bias_in_weights, _mut_select_without_bias, _mut_ignore_renormalize, _mut_ignore_scale,
            _mut_sigmoid_as_softmax, _mut_router_transposed, _mut_linear_transposed, _mut_linear_no_gscale, _mut_nibble_order, _mut_e4m3_bias, _mut_e2m1_subnormal, _mut_scale_group_shift,
            _mut_gate_up_swap, _mut_drop_up_scale, _mut_tie_break, _mut_softmax_all,
