@@ -1,10 +1,12 @@
 """Benchmark of the NVFP4 W4A16 MoE layer on GB300 (one JSON line on stdout).
 
-Workload: the 2-token MTP decode step of the GLM-5.3-Flash routed-expert layer
-(128 experts, hidden 4096, expert intermediate 1536, top-8, 1 token + 1
-speculative token), synthetic seeded inputs (synth/).  A step is one call of
-nvfp4_moe_forward: route -> permute -> gate/up GEMV + SwiGLU -> down GEMV ->
-weighted combine.
+Headline workload: the 2-token MTP decode step of the GLM-5.3-Flash routed-
+expert layer (128 experts, hidden 4096, expert intermediate 1536, top-8, 1
+token + 1 speculative token), synthetic seeded inputs (synth/).  A step is one
+call of nvfp4_moe_forward: route -> permute -> gate/up GEMV + SwiGLU -> down
+GEMV -> weighted combine.  The same line carries, under config.secondary, the
+16-token decode step and the 1024- and 16384-token prefill workloads, each with
+its own step time, tokens/s and dominant-kernel roofline.
 
 Measured:
 * value: tokens/s with inputs resident in HBM; each step is one replay of a
@@ -12,12 +14,14 @@ Measured:
   stream; L2 is flushed (256 MiB write) before every step, outside the events;
 * e2e: the same metric through the C ABI with the step's inputs copied from
   pinned host memory and the output read back, all inside the events;
-* roofline: the fused decode kernel (route + gate/up + down + combine in one
-  launch), algorithmic bytes per launch (the touched experts' NVFP4 weights,
-  logits, x and out) / its CUDA-event duration, against the measured HBM copy
-  bandwidth (prefill workloads: the gate/up GEMM's flops against BF16 peak);
-* cpu_baseline: the float64 CPU oracle on a bounded sample of the same step.
---impl reference times the oracle alone (the CPU reference arm).
+* roofline: the dominant kernel, its algorithmic work per launch over its
+  CUDA-event duration on the library's stream: decode, the fused kernel's
+  bytes (the touched experts' NVFP4 weights, logits, x and out) against the
+  measured HBM copy bandwidth; prefill, the gate/up GEMM's flops against the
+  measured BF16 tensor-core peak;
+* cpu_baseline: the float64 CPU oracle on a bounded sample of the step (at
+  most 16 tokens), over a process pool with one process per visible core.
+--impl reference times the oracle alone the same way (the CPU reference arm).
 --workload kda_in_proj_mtp | kda_in_proj_1k | linear_tiny runs the dense
 W4A16 linear instead (nvfp4_linear_forward on the fused KDA in_proj shape,
 N=12576 K=4096, at T=2 and T=1024), with the same keys.
@@ -55,6 +59,8 @@ def _args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="time only --workload (the default line also carries decode_c16, prefill_1k, prefill_16k)")
     ap.add_argument("--w4a4", action="store_true",
                     help="the W4A4 comparison variant (activations quantised to NVFP4 with input scales)")
     ap.add_argument("--router", action="store_true",
@@ -76,70 +82,48 @@ def _workload_desc(cfg):
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle timing (the baseline and the reference arm)
+# CPU oracle timing (the baseline and the reference arm): the float64 oracle,
+# unchanged, over a spawn process pool, one task per touched expert, one BLAS
+# thread per process, as many processes as cores visible to this process
 # ---------------------------------------------------------------------------
 
-_ORACLE_CHILD = r"""
-import sys, time, json, numpy as np
-sys.path.insert(0, sys.argv[1])
-import oracle
-d = np.load(sys.argv[2])
-E, k, S = int(d["E"]), int(d["k"]), int(d["S"])
-class W: pass
-w = W()
-w.w13_q = np.zeros((E,) + d["w13_q"].shape[1:], np.uint8); w.w13_s = np.zeros((E,) + d["w13_s"].shape[1:], np.uint8)
-w.w2_q = np.zeros((E,) + d["w2_q"].shape[1:], np.uint8); w.w2_s = np.zeros((E,) + d["w2_s"].shape[1:], np.uint8)
-w.gscale = np.ones((E, 3), np.float32)
-for i, e in enumerate(d["experts"]):
-    w.w13_q[e], w.w13_s[e], w.w2_q[e], w.w2_s[e], w.gscale[e] = d["w13_q"][i], d["w13_s"][i], d["w2_q"][i], d["w2_s"][i], d["gscale"][i]
-logits, x = d["logits"], d["x_bits"]
-mode, steps, warm = sys.argv[3], int(sys.argv[4]), int(sys.argv[5])
-times = []
-if mode == "baseline":
-    for _ in range(2):
-        t0 = time.perf_counter(); oracle.moe_forward(logits, x, w, k, num_shared=S); times.append(time.perf_counter() - t0)
-else:
-    # one step = one routed row: route its token, run that expert's FFN, weight it
-    T = logits.shape[0]
-    xs = oracle.bf16_bits_to_f64(x)
+def _time_oracle_steps(inp, steps, warm, pool):
+    """Wall time of each of `steps` full layer steps of the oracle (after
+    `warm` untimed ones) on the pool."""
+    from oracle.pool import moe_forward_pool
+    cfg = inp.config
+    times = []
     for s in range(warm + steps):
-        t, j = s % T, (s // T) % k
         t0 = time.perf_counter()
-        r = oracle.route(logits[t:t + 1], k)
-        y = r.weights[0, j] * oracle.expert_ffn(w, int(r.ids[0, j]), xs[t:t + 1])
-        dt = time.perf_counter() - t0
-        if s >= warm: times.append(dt)
-print(json.dumps({"times": times}))
-"""
+        moe_forward_pool(inp.logits, inp.x_bits, inp.weights, cfg.top_k, num_shared=cfg.shared, pool=pool)
+        if s >= warm:
+            times.append(time.perf_counter() - t0)
+    return times
 
 
-def _oracle_sample_file(inp, ids):
-    experts = np.unique(ids.reshape(-1))
-    w = inp.weights
-    fd, path = tempfile.mkstemp(suffix=".npz")
-    os.close(fd)
-    np.savez(path, E=inp.config.num_experts + inp.config.shared, k=inp.config.top_k, S=inp.config.shared,
-             experts=experts,
-             w13_q=w.w13_q[experts], w13_s=w.w13_s[experts], w2_q=w.w2_q[experts], w2_s=w.w2_s[experts],
-             gscale=w.gscale[experts], logits=inp.logits, x_bits=inp.x_bits)
-    return path
+def _oracle_sample(inp):
+    """A bounded sample of the workload for the CPU legs: at most 16 tokens."""
+    from synth import make_inputs
+    ns = min(inp.config.tokens, 16)
+    return (make_inputs(inp.config.with_tokens(ns)) if ns < inp.config.tokens else inp), ns
 
 
-def _run_oracle_child(path, mode, steps=0, warm=0):
-    env = dict(os.environ)
-    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
-        env[v] = "1"
-    r = subprocess.run([sys.executable, "-c", _ORACLE_CHILD, ROOT, path, mode, str(steps), str(warm)],
-                       capture_output=True, text=True, env=env)
-    if r.returncode != 0:
-        raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
-    return json.loads(r.stdout.strip().splitlines()[-1])["times"]
-
-
-def _host_route_ids(logits, k):
-    # expert choice for sizing the CPU sample: larger logit first, lower index on ties
-    order = np.lexsort((np.broadcast_to(np.arange(logits.shape[1]), logits.shape), -logits), axis=1)
-    return order[:, :k]
+def cpu_baseline(inp, reps=3):
+    """The oracle on the host's cores, timed on a bounded sample of the step."""
+    from oracle.pool import make_pool
+    sub, ns = _oracle_sample(inp)
+    pool, n = make_pool()
+    try:
+        times = _time_oracle_steps(sub, reps, 1, pool)
+    finally:
+        pool.close()
+        pool.join()
+    cfg = inp.config
+    return {"value": ns / statistics.mean(times), "unit": "tokens/s", "cores": n, "kind": "oracle",
+            "sample": f"{ns} token(s) of the step ({ns * (cfg.top_k + cfg.shared)} routed rows), the whole "
+                      f"float64 layer (route, expert FFNs, combine), {reps} timed repetitions after one warm-up; "
+                      f"a spawn pool of {n} processes (one per core in os.sched_getaffinity), one task per "
+                      f"touched expert, 1 BLAS thread each"}
 
 
 def run_reference(args):
@@ -147,24 +131,27 @@ def run_reference(args):
     if rank != 0:
         return
     from synth import make_inputs
+    from oracle.pool import make_pool
     inp = make_inputs(args.workload)
-    cfg = inp.config
-    path = _oracle_sample_file(inp, _host_route_ids(inp.logits, cfg.top_k))
+    sub, ns = _oracle_sample(inp)
+    pool, n = make_pool()
     try:
-        times = _run_oracle_child(path, "reference", args.steps, args.warmup)
+        times = _time_oracle_steps(sub, args.steps, args.warmup, pool)
     finally:
-        os.unlink(path)
+        pool.close()
+        pool.join()
     sec = sum(times)
-    value = args.steps / cfg.top_k / sec   # one routed row (1/k of a token) per step
+    value = args.steps * ns / sec
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded PCG64, shapes of the pages' MTP decode step)",
-        "config": {"workload": _workload_desc(cfg)},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": "one routed row per step (route its token, one expert FFN, weight), "
-                                   "float64 numpy, 1 thread; tokens/s = rows/s / top_k"},
+        "data": "synthetic (seeded PCG64, shapes of the pages' workloads)",
+        "config": {"workload": _workload_desc(inp.config)},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n, "kind": "oracle",
+                         "sample": f"each step the whole float64 layer on {ns} token(s) of the workload "
+                                   f"(route, expert FFNs, combine), a spawn pool of {n} processes, one task "
+                                   f"per touched expert, 1 BLAS thread each"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -252,6 +239,148 @@ def _traffic_for(kernel_src):
     return None
 
 
+def _peak(key, fallback):
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)[key]), "measured"
+    except Exception:
+        return fallback, "fallback"
+
+
+def measure_layer(name, steps, warmup, dev, flush, barrier, ws=1, router=False, w4a4=False):
+    """One workload's timed steps on this GPU.  Returns a dict: step time,
+    tokens/s, end-to-end tokens/s through the C ABI with host buffers, the
+    dominant kernel's roofline, and per-stage times (prefill)."""
+    import torch
+    import nvfp4_weight_only_w4a16_gb300 as pkg
+    from synth import make_inputs, make_router_weight, make_input_scales
+    inp = make_inputs(name)
+    cfg = inp.config
+    T, k, H, E, I, S = cfg.tokens, cfg.top_k, cfg.hidden, cfg.num_experts, cfg.inter, cfg.shared
+    decode = T <= 16
+    layer = pkg.MoELayer(E, H, I, T, k, device=dev.index, num_shared_experts=S)
+    n_ours = 1 if decode else 6     # kernels of ours per forward (decode / prefill path)
+    pkg.upload_layer(layer, inp.weights, dev)
+    if w4a4:
+        layer.nvfp4_moe_set_act_quant(torch.from_numpy(make_input_scales(cfg)).to(dev))
+    logits = torch.from_numpy(inp.logits).to(dev)
+    x = torch.from_numpy(inp.x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    if router:
+        # the logits come from the router linear on the GPU inside every step
+        layer.nvfp4_moe_set_router(torch.from_numpy(make_router_weight(cfg).view(np.int16)).to(dev).view(torch.bfloat16))
+        layer.nvfp4_moe_forward_routed(x, k, out)
+        torch.cuda.synchronize()
+        logits = layer.nvfp4_moe_debug_logits(T)
+        fwd = lambda: layer.nvfp4_moe_forward_routed(x, k, out)
+        n_ours += 1 if decode else 2
+    else:
+        fwd = lambda: layer.nvfp4_moe_forward(logits, x, k, out)
+    ids, _, _, _ = layer.nvfp4_moe_debug_route(logits, T, k)
+    distinct = int(torch.unique(ids).numel())
+
+    for _ in range(warmup):
+        fwd()
+    torch.cuda.synchronize()
+    st, _ = layer.nvfp4_moe_get_status()
+    if st != 0:
+        raise RuntimeError(f"{name}: device status {pkg.STATUS[st]} after warm-up")
+
+    # one forward captured into a CUDA graph (launch-overhead free replay)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fwd()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # --- timed region: graph replays, L2 flushed before each ---
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier()
+    for s, e in evs:
+        flush.zero_()
+        s.record(stream)
+        graph.replay()
+        e.record(stream)
+    barrier()
+    step_ms = [s.elapsed_time(e) for s, e in evs]
+
+    # --- per-kernel durations (direct calls, events inside the library on its stream) ---
+    layer.nvfp4_moe_set_profiling(True)
+    barrier()
+    for _ in range(steps):
+        flush.zero_()
+        fwd()
+    barrier()
+    stage_ms, nfwd = layer.nvfp4_moe_get_stage_times()
+    layer.nvfp4_moe_set_profiling(False)
+    stage_ms = [v / max(nfwd, 1) for v in stage_ms]
+
+    # --- end to end through the C ABI with host buffers ---
+    h_logits = torch.from_numpy(inp.logits).pin_memory()
+    h_x = torch.from_numpy(inp.x_bits.view(np.int16)).pin_memory()
+    h_out = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    d_x16 = x.view(torch.int16)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier()
+    for s, e in e2e_ev:
+        flush.zero_()
+        s.record(stream)
+        if not router:
+            logits.copy_(h_logits, non_blocking=True)
+        d_x16.copy_(h_x, non_blocking=True)
+        fwd()
+        h_out.copy_(out.view(torch.int16), non_blocking=True)
+        e.record(stream)
+    barrier()
+    e2e_ms = [s.elapsed_time(e) for s, e in e2e_ev]
+    st, _ = layer.nvfp4_moe_get_status()
+    if st != 0:
+        raise RuntimeError(f"{name}: device status {pkg.STATUS[st]} after the timed region")
+    layer.close()
+
+    ms, ms_e2e, value, value_e2e = replica_throughput(statistics.mean(step_ms), statistics.mean(e2e_ms), T, ws, dev)
+    layer_bytes = distinct * cfg.expert_bytes + T * H * 2 * 2 + T * E * 4
+    layer_flops = 2.0 * T * (k + S) * 3 * H * I
+    if decode:
+        # decode: one fused kernel streams every touched expert's weights once
+        kernel = "decode_fused_kernel"
+        kern_ms = stage_ms[1]
+        algo = layer_bytes
+        achieved = algo / (kern_ms / 1e3) / 1e9
+        bound, unit = "hbm", "GB/s"
+        peak, peak_src = _peak("hbm_gbs", 6800.0)
+        traffic = _traffic_for(os.path.join(ROOT, "nvfp4_weight_only_w4a16_gb300", "csrc", "decode.cu")) \
+            if name == WORKLOAD and not (router or w4a4) else None
+        stages = {"decode_fused_kernel (route + gate/up + down + combine)": kern_ms}
+    else:
+        # prefill: the gate/up GEMM's dense flops on the tensor cores
+        kernel = "prefill_gemm_kernel<gate/up>"
+        kern_ms = stage_ms[1]
+        algo = 2.0 * T * (k + S) * (2 * I) * H
+        achieved = algo / (kern_ms / 1e3) / 1e12
+        bound, unit = "tensor", "TFLOP/s"
+        peak, peak_src = _peak("bf16_tflops", 1900.0)
+        traffic = None
+        stages = {"route_permute" + (" (+ router linear)" if router else ""): stage_ms[0],
+                  "gate_up": stage_ms[1], "down": stage_ms[2], "combine": stage_ms[3]}
+    return {
+        "inp": inp, "ms": ms, "ms_e2e": ms_e2e, "value": value, "value_e2e": value_e2e,
+        "distinct": distinct, "layer_bytes": layer_bytes, "layer_flops": layer_flops,
+        "n_ours": n_ours, "stages": stages,
+        "roofline": {"bound": bound, "kernel": kernel, "achieved": achieved, "peak": peak,
+                     "peak_source": peak_src, "unit": unit, "frac": achieved / peak,
+                     "algorithmic_per_launch": algo, "kernel_ms": kern_ms, "traffic": traffic},
+        "e2e": {"value": value_e2e, "unit": "tokens/s",
+                "h2d_bytes_per_step": (0 if router else T * E * 4) + T * H * 2,
+                "d2h_bytes_per_step": T * H * 2},
+    }
+
+
+SECONDARY = ("decode_c16", "prefill_1k", "prefill_16k")
+
+
 def run_ours(args):
     import torch
     ws, rank, local = _dist()
@@ -264,37 +393,8 @@ def run_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
 
     import nvfp4_weight_only_w4a16_gb300 as pkg
-    from synth import make_inputs, make_router_weight, make_input_scales
     pkg.build()
-    inp = make_inputs(args.workload)
-    cfg = inp.config
-    T, k, H, E = cfg.tokens, cfg.top_k, cfg.hidden, cfg.num_experts
-    S = cfg.shared
-    layer = pkg.MoELayer(E, H, cfg.inter, T, k, device=dev.index, num_shared_experts=S)
-    n_ours = 1 if T <= 16 else 6     # kernels of ours per forward (decode / prefill path)
-    pkg.upload_layer(layer, inp.weights, dev)
-    if args.w4a4:
-        layer.nvfp4_moe_set_act_quant(torch.from_numpy(make_input_scales(cfg)).to(dev))
-
-    logits = torch.from_numpy(inp.logits).to(dev)
-    x = torch.from_numpy(inp.x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
-    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-
-    if args.router:
-        # the logits come from the router linear on the GPU inside every step
-        layer.nvfp4_moe_set_router(torch.from_numpy(make_router_weight(cfg).view(np.int16)).to(dev).view(torch.bfloat16))
-        layer.nvfp4_moe_forward_routed(x, k, out)
-        torch.cuda.synchronize()
-        logits = layer.nvfp4_moe_debug_logits(T)
-        fwd = lambda: layer.nvfp4_moe_forward_routed(x, k, out)
-    else:
-        fwd = lambda: layer.nvfp4_moe_forward(logits, x, k, out)
-    n_ours += (1 if T <= 16 else 2) if args.router else 0
-
-    ids, _, _, _ = layer.nvfp4_moe_debug_route(logits, T, k)
-    distinct = int(torch.unique(ids).numel())
 
     def barrier():
         torch.cuda.synchronize()
@@ -302,141 +402,53 @@ def run_ours(args):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
-        fwd()
-    torch.cuda.synchronize()
-    st, _ = layer.nvfp4_moe_get_status()
-    if st != 0:
-        raise RuntimeError(f"device status {pkg.STATUS[st]} after warm-up")
-
-    # one forward captured into a CUDA graph (launch-overhead free replay)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        fwd()
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-
     sampler = ClockSampler(dev.index)
     sampler.start()
     time.sleep(0.1)
-
-    # --- timed region: K graph replays, L2 flushed before each ---
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    barrier()
-    for s, e in evs:
-        flush.zero_()
-        s.record(stream)
-        graph.replay()
-        e.record(stream)
-    barrier()
-    step_ms = [s.elapsed_time(e) for s, e in evs]
-
-    # --- per-kernel durations for the roofline (direct calls, stage events) ---
-    layer.nvfp4_moe_set_profiling(True)
-    barrier()
-    for _ in range(args.steps):
-        flush.zero_()
-        fwd()
-    barrier()
-    stage_ms, nfwd = layer.nvfp4_moe_get_stage_times()
-    layer.nvfp4_moe_set_profiling(False)
-
-    # --- end to end through the C ABI with host buffers ---
-    h_logits = torch.from_numpy(inp.logits).pin_memory()
-    h_x = torch.from_numpy(inp.x_bits.view(np.int16)).pin_memory()
-    h_out = torch.empty((T, H), dtype=torch.int16).pin_memory()
-    d_x16 = x.view(torch.int16)
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    barrier()
-    for s, e in e2e_ev:
-        flush.zero_()
-        s.record(stream)
-        if not args.router:
-            logits.copy_(h_logits, non_blocking=True)
-        d_x16.copy_(h_x, non_blocking=True)
-        fwd()
-        h_out.copy_(out.view(torch.int16), non_blocking=True)
-        e.record(stream)
-    barrier()
-    e2e_ms = [s.elapsed_time(e) for s, e in e2e_ev]
+    m = measure_layer(args.workload, args.steps, args.warmup, dev, flush, barrier, ws, args.router, args.w4a4)
+    secondary = {}
+    if args.workload == WORKLOAD and not (args.router or args.w4a4 or args.no_secondary):
+        for name in SECONDARY:
+            r = measure_layer(name, min(args.steps, 30), max(3, min(args.warmup, 5)), dev, flush, barrier, ws)
+            secondary[name] = {
+                "workload": _workload_desc(r["inp"].config), "distinct_experts": r["distinct"],
+                "ms_per_step": r["ms"], "tokens_per_s": r["value"], "e2e_tokens_per_s": r["value_e2e"],
+                "layer_weight_gbs": r["layer_bytes"] / (r["ms"] / 1e3) / 1e9,
+                "layer_tflops": r["layer_flops"] / (r["ms"] / 1e3) / 1e12,
+                "stage_ms": r["stages"], "roofline": r["roofline"], "gpu_launches_per_step": r["n_ours"],
+            }
     clocks = sampler.stop()
-    st, _ = layer.nvfp4_moe_get_status()
-    if st != 0:
-        raise RuntimeError(f"device status {pkg.STATUS[st]} after the timed region")
-
-    ms = statistics.mean(step_ms)
-    ms_e2e = statistics.mean(e2e_ms)
-    ms, ms_e2e, value, value_e2e = replica_throughput(ms, ms_e2e, T, ws, dev)
-
-    I = cfg.inter
-    gateup_ms = stage_ms[1] / max(nfwd, 1)
-    layer_bytes = distinct * cfg.expert_bytes + T * H * 2 * 2 + T * E * 4
-    if T <= 16:
-        # decode: one fused kernel streams every touched expert's weights once
-        kernel = "decode_fused_kernel"
-        algo = layer_bytes
-        achieved = algo / (gateup_ms / 1e3) / 1e9
-        bound, unit, peak_key = "hbm", "GB/s", "hbm_gbs"
-        traffic = _traffic_for(os.path.join(ROOT, "nvfp4_weight_only_w4a16_gb300", "csrc", "decode.cu"))
-    else:
-        # prefill: the gate/up GEMM's dense flops on the tensor cores
-        kernel = "prefill_gemm_kernel<gate/up>"
-        algo = 2.0 * T * (k + S) * (2 * I) * H
-        achieved = algo / (gateup_ms / 1e3) / 1e12
-        bound, unit, peak_key = "tensor", "TFLOP/s", "bf16_tflops"
-        traffic = None
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peak = float(json.load(f)[peak_key])
-        peak_src = "measured"
-    except Exception:
-        peak, peak_src = (6800.0 if bound == "hbm" else 1900.0), "fallback"
-    layer_flops = 2.0 * T * (k + S) * 3 * H * I
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        ns = min(T, 2)   # bounded sample: the first tokens of the step (the whole step at T = 2)
-        sub = make_inputs(cfg.with_tokens(ns)) if ns < T else inp
-        path = _oracle_sample_file(sub, ids.cpu().numpy()[:ns])
-        try:
-            times = _run_oracle_child(path, "baseline")
-        finally:
-            os.unlink(path)
-        cpu = {"value": ns / statistics.mean(times), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{ns} token(s) of the step ({ns * (k + S)} expert FFNs + combine), twice, float64 numpy, "
-                         f"1 thread"}
+        cpu = cpu_baseline(m["inp"])
 
     if rank == 0:
+        cfg = m["inp"].config
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "w4a16: e2m1*e4m3 weights -> fp16 mma, fp32 accumulate",
-            "data": "synthetic (seeded PCG64, shapes of the pages' MTP decode step)",
+            "metric": METRIC, "value": m["value"], "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": m["ms"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "w4a16: e2m1*e4m3 weights -> fp16/bf16 mma, fp32 accumulate",
+            "data": "synthetic (seeded PCG64, shapes of the pages' workloads)",
             "config": {"workload": _workload_desc(cfg) + (" + BF16 router linear" if args.router else "") +
                                    (" [W4A4 comparison variant: NVFP4 activations]" if args.w4a4 else ""),
-                       "distinct_experts": distinct,
-                       "layer_weight_bytes_per_step": layer_bytes,
-                       "layer_weight_gbs": layer_bytes / (ms / 1e3) / 1e9,
-                       "layer_tflops": layer_flops / (ms / 1e3) / 1e12,
+                       "distinct_experts": m["distinct"],
+                       "layer_weight_bytes_per_step": m["layer_bytes"],
+                       "layer_weight_gbs": m["layer_bytes"] / (m["ms"] / 1e3) / 1e9,
+                       "layer_tflops": m["layer_flops"] / (m["ms"] / 1e3) / 1e12,
                        "l2": "flushed before every step (256 MiB write, outside the step events)",
                        "launch": "CUDA graph replay of one " + (
                            "nvfp4_moe_forward_routed (router linear on the GPU)" if args.router else "nvfp4_moe_forward"),
                        "parallelism": f"replicas x{ws}",
-                       "stage_ms": {"route_permute": stage_ms[0] / max(nfwd, 1), "gate_up": gateup_ms,
-                                    "down": stage_ms[2] / max(nfwd, 1), "combine": stage_ms[3] / max(nfwd, 1)}},
-            "roofline": {"bound": bound, "kernel": kernel, "achieved": achieved, "peak": peak,
-                         "peak_source": peak_src, "unit": unit, "frac": achieved / peak,
-                         "algorithmic_per_launch": algo, "traffic": traffic},
-            "e2e": {"value": value_e2e, "unit": "tokens/s",
-                    "h2d_bytes_per_step": (0 if args.router else T * E * 4) + T * H * 2,
-                    "d2h_bytes_per_step": T * H * 2},
-            "gpu_launches": n_ours * args.steps,
+                       "stage_ms": m["stages"],
+                       "secondary": secondary},
+            "roofline": m["roofline"],
+            "e2e": m["e2e"],
+            "gpu_launches": m["n_ours"] * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
-    layer.close()
     if ws > 1:
         torch.distributed.destroy_process_group()
 

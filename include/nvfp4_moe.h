@@ -176,21 +176,41 @@ nvfp4_moe_status nvfp4_moe_set_path(nvfp4_moe_t h, int path);
  *   router_logits [T][E] (logits_dtype), x [T][H] BF16, out [T][H] BF16
  * 1 <= T <= 16, 1 <= top_k <= min(E, 16); H, I as in nvfp4_moe_config.
  * All intermediates live in one static device array of 16 MiB that every GPU
- * loading this library holds until the process exits.  This path gives each
- * GPU warp whole row blocks (no split-K partial sums), so it needs about
- * T*top_k*(2I + 4H) bytes plus small tables -- under 1 MiB for E=128, H=4096,
- * I=1536, T=2, top_k=8 -- but balances less evenly than nvfp4_moe_forward.
+ * loading this library holds until the process exits.  It needs about
+ * T*top_k*(4.25*I + 4*H) + 36*H bytes plus small tables -- under 1 MiB for
+ * E=128, H=4096, I=1536, T=2, top_k=8.
  * A shape needing more than the array returns
  * NVFP4_MOE_ERR_UNSUPPORTED_SHAPE before anything is enqueued.  The regions
  * that must start at zero are cleared by every call.  The first call on each
- * device looks up the array's device address with that device current: make
- * it before any stream capture.  Calls whose GPU work overlaps (other
- * streams, concurrent graph replays) share the array and race: serialise
- * them. */
+ * device looks up the array's device address and sets the decode kernels'
+ * shared-memory attribute, with that device current: make it before any
+ * stream capture.  Device ordinals 0..63 only (NVFP4_MOE_ERR_INVALID_ARG
+ * above).  Calls whose GPU work overlaps (other streams, concurrent graph
+ * replays) share the array and race: serialise them.  The call returns once
+ * the work is enqueued; device-side errors (a bounded wait that gave up,
+ * leaving a partial output; NaN router logits) are collected in a status word
+ * inside the array that no call clears: read it with
+ * nvfp4_moe_static_get_status. */
 nvfp4_moe_status nvfp4_moe_forward_decode_static(const uint8_t* packed_experts, const float* gscale,
                                                  int num_experts, int hidden, int inter,
                                                  const void* router_logits, int logits_dtype, int T, int top_k,
                                                  const void* x, void* out, cudaStream_t stream);
+
+/* Synchronous: waits for the current device, then reports and clears the
+ * status word that nvfp4_moe_forward_decode_static calls on this device have
+ * accumulated since the last read: NVFP4_MOE_OK, NVFP4_MOE_ERR_TIMEOUT (some
+ * call's bounded wait gave up and its output is incomplete) or
+ * NVFP4_MOE_ERR_DEVICE_CHECK; *nan_logits (may be NULL) receives the number
+ * of NaN router logits those calls saw.  Like the forward it allocates
+ * nothing; NVFP4_MOE_ERR_CUDA if a CUDA call fails. */
+nvfp4_moe_status nvfp4_moe_static_get_status(uint32_t* nan_logits);
+
+/* Fault injection for the allocation-free path's bounded-wait test, process-
+ * wide: fault = 1 makes later nvfp4_moe_forward_decode_static calls issue no
+ * weight copies, so their waits expire (after about 2 s) and report
+ * NVFP4_MOE_ERR_TIMEOUT through nvfp4_moe_static_get_status; the GPU context
+ * stays usable.  fault = 0 restores normal operation. */
+nvfp4_moe_status nvfp4_moe_static_debug_set_fault(int fault);
 
 /* Scoring rule of the route step (the router variants).  The pages keep the
  * routers as BF16 linears and do not state how their outputs become choices
@@ -304,16 +324,35 @@ nvfp4_moe_status nvfp4_moe_debug_dequant(nvfp4_moe_t h, int expert, int which, f
 
 /* Copy the last forward's intermediates, in expert-major routed-row order
  * (row p = perm position p), into caller DEVICE buffers:
- *   hidden [T*K][I] BF16 (h = silu(g)*u, rounded to BF16; K = top_k + S),
+ *   hidden [T*K][I] float: h = silu(g)*u as the down GEMM consumed it, after
+ *          its rounding to 16 bits (K = top_k + S),
  *   y      [T*K][H] float (expert output before the routing weight). */
 nvfp4_moe_status nvfp4_moe_debug_intermediates(nvfp4_moe_t h, void* hidden, float* y,
                                                cudaStream_t stream);
 
 /* Fault injection for the bounded-wait test: fault = 1 makes the prefill
- * producer issue no copies, so the consumers' waits expire (after about 2 s),
- * the kernels record NVFP4_MOE_ERR_TIMEOUT in the status word and return;
- * the GPU context stays usable.  fault = 0 restores normal operation. */
+ * producer and the decode kernel issue no copies, so the consumers' waits
+ * expire (after about 2 s), the kernels record NVFP4_MOE_ERR_TIMEOUT in the
+ * status word and return; the GPU context stays usable.  fault = 0 restores
+ * normal operation. */
 nvfp4_moe_status nvfp4_moe_debug_set_fault(nvfp4_moe_t h, int fault);
+
+/* Fill every workspace buffer that each forward rewrites before it reads it
+ * (routing tables, gathered and hidden activations, expert outputs, the
+ * decode kernels' activation rows) with `byte`, on `stream`; the counters and
+ * the status word keep their values.  A forward after it must give
+ * bit-identical results: no kernel reads memory it has not written in the
+ * same forward (the unused MMA columns that read such rows are never kept).
+ * Tests use 0xFF (NaN in FP16, BF16 and FP32). */
+nvfp4_moe_status nvfp4_moe_debug_poison_workspace(nvfp4_moe_t h, int byte, cudaStream_t stream);
+
+/* Host only (no GPU needed): the status code a device status word stands for
+ * -- bit 0 a bounded wait that gave up (NVFP4_MOE_ERR_TIMEOUT), bit 1 a
+ * device-side bounds check that fired (NVFP4_MOE_ERR_DEVICE_CHECK; the checks
+ * run when the handle was created with NVFP4_MOE_CHECKS=1), none
+ * NVFP4_MOE_OK.  nvfp4_moe_get_status and nvfp4_moe_static_get_status decode
+ * the words they read this way. */
+nvfp4_moe_status nvfp4_moe_decode_status_word(uint32_t flags);
 
 /* ---------------------------------------------------------------------------
  * Dense W4A16 NVFP4 linear: out[t] = gs * W x[t] for one weight matrix W

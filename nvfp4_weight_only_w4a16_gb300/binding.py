@@ -80,6 +80,10 @@ def load_library(path: str | None = None):
         "nvfp4_moe_set_profiling": (i, [vp, i]),
         "nvfp4_moe_debug_packed_blob": (i, [vp, vp, ctypes.c_size_t, vp]),
         "nvfp4_moe_forward_decode_static": (i, [vp, vp, i, i, i, vp, i, i, i, vp, vp, vp]),
+        "nvfp4_moe_static_get_status": (i, [ctypes.POINTER(ctypes.c_uint32)]),
+        "nvfp4_moe_static_debug_set_fault": (i, [i]),
+        "nvfp4_moe_debug_poison_workspace": (i, [vp, i, vp]),
+        "nvfp4_moe_decode_status_word": (i, [ctypes.c_uint32]),
         "nvfp4_moe_debug_trace": (i, [vp, ctypes.POINTER(ctypes.c_uint64), ctypes.c_size_t,
                                       ctypes.POINTER(ctypes.c_size_t)]),
         "nvfp4_moe_get_stage_times": (i, [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
@@ -215,7 +219,7 @@ class MoELayer:
 
     def nvfp4_moe_debug_intermediates(self, rows, stream=None):
         import torch
-        hid = torch.empty((rows, self.I), dtype=torch.bfloat16, device=f"cuda:{self.device}")
+        hid = torch.empty((rows, self.I), dtype=torch.float32, device=f"cuda:{self.device}")
         y = torch.empty((rows, self.H), dtype=torch.float32, device=f"cuda:{self.device}")
         st = self.lib.nvfp4_moe_debug_intermediates(self.h, _ptr(hid), _ptr(y), _stream(stream))
         self._check(st, "nvfp4_moe_debug_intermediates")
@@ -261,6 +265,10 @@ class MoELayer:
         out = torch.empty((T, self.E), dtype=torch.float32, device=f"cuda:{self.device}")
         self._check(self.lib.nvfp4_moe_debug_logits(self.h, _ptr(out), _stream(stream)), "nvfp4_moe_debug_logits")
         return out
+
+    def nvfp4_moe_debug_poison_workspace(self, byte=0xFF, stream=None):
+        self._check(self.lib.nvfp4_moe_debug_poison_workspace(self.h, int(byte), _stream(stream)),
+                    "nvfp4_moe_debug_poison_workspace")
 
     def nvfp4_moe_debug_set_fault(self, fault):
         self._check(self.lib.nvfp4_moe_debug_set_fault(self.h, fault), "nvfp4_moe_debug_set_fault")
@@ -311,6 +319,19 @@ def nvfp4_moe_forward_decode_static(packed_experts, gscale, num_experts, hidden,
     return lib.nvfp4_moe_forward_decode_static(_ptr(packed_experts), _ptr(gscale), num_experts, hidden, inter,
                                                _ptr(logits), 1 if logits_bf16 else 0, x.shape[0], top_k,
                                                _ptr(x), _ptr(out), _stream(stream))
+
+
+def nvfp4_moe_static_get_status():
+    """(status, nan_logits) of the allocation-free path on the current device
+    (synchronous; reads and clears the status word)."""
+    lib = load_library()
+    n = ctypes.c_uint32(0)
+    st = lib.nvfp4_moe_static_get_status(ctypes.byref(n))
+    return st, int(n.value)
+
+
+def nvfp4_moe_static_debug_set_fault(fault):
+    return load_library().nvfp4_moe_static_debug_set_fault(int(fault))
 
 
 def upload_layer(layer: MoELayer, weights, device="cuda:0"):

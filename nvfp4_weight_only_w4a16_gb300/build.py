@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libnvfp4moe.so")
-SOURCES = ["api.cu", "pack.cu", "route.cu", "decode.cu", "prefill.cu", "static_forward.cu"]
+SOURCES = ["api.cu", "pack.cu", "route.cu", "decode.cu", "decode_stream.cu", "prefill.cu", "static_forward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I" + os.path.join(ROOT, "include")]

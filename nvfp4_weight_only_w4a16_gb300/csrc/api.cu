@@ -27,6 +27,9 @@ struct nvfp4_moe {
   bool w4a4 = false;
   float* in_scale = nullptr;     // [E][2] device input scales (w13, w2); shared expert's unused
   float* gs_eff = nullptr;       // [E][3] device tensor scales with the input scales folded in
+  float* hbound = nullptr;       // [E] max_f ||Wg_f|| ||Wu_f|| (written at pack): sizes h's FP16 prescale
+  std::vector<std::pair<uint8_t*, size_t>> data_regions;  // workspace buffers every forward rewrites
+  int checks = 0;  // NVFP4_MOE_CHECKS=1 at create: kernels check table-derived indices
   std::vector<float> gs_host;    // [E][3] the packed tensor scales
   std::vector<float> is_host;    // [E][2]
   int path = NVFP4_MOE_PATH_AUTO;
@@ -41,6 +44,7 @@ struct nvfp4_moe {
   Workspace ws{};
   PrefillMaps maps{};
   int last_T = 0, last_k = 0;
+  int last_hsrc = 0;  // where the last forward's hidden activations are (launch_hidden_to_f32's src)
   bool last_routed = false;
   int fault = 0;
   bool profiling = false;
@@ -106,9 +110,11 @@ bool encode_rows_map(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols,
 struct Carver {
   size_t off = 0;
   std::vector<std::pair<void**, size_t>> items;
+  std::vector<bool> is_data;  // rewritten by every forward before it is read (no counter, no constant)
   template <class T>
-  void add(T** p, size_t count) {
+  void add(T** p, size_t count, bool data = false) {
     items.push_back({reinterpret_cast<void**>(p), count * sizeof(T)});
+    is_data.push_back(data);
   }
   size_t layout() {
     off = 0;
@@ -156,6 +162,9 @@ LayerDims dims_of(const nvfp4_moe* h) {
               h->cfg.num_experts, h->cfg.num_shared_experts, h->linear ? 1 : 0, h->lin_n};
   d.rp = h->rp;
   d.in_scale = h->w4a4 ? h->in_scale : nullptr;
+  d.gs = h->w4a4 ? h->gs_eff : h->gscale;
+  d.hbound = h->hbound;
+  d.checks = h->checks;
   return d;
 }
 
@@ -199,14 +208,28 @@ nvfp4_moe_status take_events(nvfp4_moe* h, cudaEvent_t (&ev)[5]) {
   return NVFP4_MOE_OK;
 }
 
+// The decode forward takes the streaming kernel wherever it applies (W4A16
+// routed experts); NVFP4_MOE_DECODE_KERNEL=fused keeps the earlier fused
+// kernel for comparison.
+bool use_stream(const nvfp4_moe* h, const LayerDims& d, int T, int k) {
+  static const bool fused = [] {
+    const char* s = getenv("NVFP4_MOE_DECODE_KERNEL");
+    return s && !strcmp(s, "fused");
+  }();
+  (void)h;
+  return !fused && stream_supported(d, T, k);
+}
+
 nvfp4_moe_status run_route(nvfp4_moe* h, const void* logits, const void* x, int T, int k, int path,
                            cudaStream_t st, int logits_bf16 = -1) {
   LayerDims d = dims_of(h);
   if (logits_bf16 >= 0) d.logits_bf16 = logits_bf16;
-  cudaError_t e = path == NVFP4_MOE_PATH_DECODE
-                      ? launch_decode_forward(d, h->blob, h->gscale, logits, nullptr, T, k, nullptr, 1, h->num_sms,
-                                              h->ws, st)
-                      : launch_route_prefill(d, logits, x, T, k, h->ws, st);
+  cudaError_t e = path != NVFP4_MOE_PATH_DECODE ? launch_route_prefill(d, logits, x, T, k, h->ws, st)
+                   : use_stream(h, d, T, k)
+                       ? launch_decode_stream(d, h->blob, h->gscale, logits, nullptr, T, k, nullptr, 1, h->num_sms,
+                                              h->ws, 0, st)
+                       : launch_decode_forward(d, h->blob, h->gscale, logits, nullptr, T, k, nullptr, 1, h->num_sms,
+                                               h->ws, 0, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "route launch");
   return NVFP4_MOE_OK;
 }
@@ -265,6 +288,8 @@ nvfp4_moe_status create_handle(const nvfp4_moe_config* c, bool linear, int lin_n
   h->lin_n = lin_n;
   const char* lg = getenv("NVFP4_MOE_LOG");
   h->log = lg && lg[0] == '1';
+  const char* ck = getenv("NVFP4_MOE_CHECKS");
+  h->checks = ck && ck[0] == '1';
   const char* fp = getenv("NVFP4_MOE_FORCE_PATH");
   if (fp && !strcmp(fp, "decode")) h->path = NVFP4_MOE_PATH_DECODE;
   if (fp && !strcmp(fp, "prefill")) h->path = NVFP4_MOE_PATH_PREFILL;
@@ -287,37 +312,45 @@ nvfp4_moe_status create_handle(const nvfp4_moe_config* c, bool linear, int lin_n
 
   Carver cv;
   Workspace& w = h->ws;
-  cv.add(&w.ids, Rm);
-  cv.add(&w.wts, Rm);
-  cv.add(&w.offsets, E + 1);
-  cv.add(&w.perm, Rm);
-  cv.add(&w.inv, Rm);
-  cv.add(&w.tch_expert, E);
-  cv.add(&w.tch_row0, E);
-  cv.add(&w.tch_rows, E);
+  cv.add(&w.ids, Rm, true);
+  cv.add(&w.wts, Rm, true);
+  cv.add(&w.offsets, E + 1, true);
+  cv.add(&w.perm, Rm, true);
+  cv.add(&w.inv, Rm, true);
+  cv.add(&w.tch_expert, E, true);
+  cv.add(&w.tch_row0, E, true);
+  cv.add(&w.tch_rows, E, true);
   cv.add(&w.num_touched, 1);
-  cv.add(&w.x16, (size_t)kDecodeMaxTokens * H);
-  cv.add(&w.xexp, kDecodeMaxTokens);
-  cv.add(&w.h, RmI);
+  cv.add(&w.x16, (size_t)kDecodeMaxTokens * H, true);
+  cv.add(&w.xexp, kDecodeMaxTokens, true);
+  cv.add(&w.h, RmI, true);
   cv.add(&w.hmax, Rm);
-  cv.add(&w.y, RmH);
-  cv.add(&w.part_gu, decode_part_floats(h->num_sms, kDecodeMaxTokens));
+  cv.add(&w.y, RmH, true);
+  cv.add(&w.part_gu, decode_part_floats(h->num_sms, kDecodeMaxTokens), true);
   cv.add(&w.cnt_gu, maxU * (2 * I / 16));
-  cv.add(&w.part_dn, decode_part_floats(h->num_sms, kDecodeMaxTokens));
+  cv.add(&w.part_dn, decode_part_floats(h->num_sms, kDecodeMaxTokens), true);
   cv.add(&w.cnt_dn, maxU * (H / 16));
   cv.add(&w.done_gu, maxU);
   cv.add(&w.cmb, H / 64);
   cv.add(&w.exit_cnt, 1);
-  cv.add(&w.blk_counts, ncta * E);
-  cv.add(&w.blk_base, ncta * E);
-  cv.add(&w.local_rank, Rm);
-  cv.add(&w.x_perm, RmH);
-  cv.add(&w.tile_expert, max_tiles);
-  cv.add(&w.tile_row0, max_tiles);
-  cv.add(&w.tile_rows, max_tiles);
-  cv.add(&w.num_tiles, 1);
+  w.act_rows = kDecodeMaxTokens * K;
+  cv.add(&w.act_h, linear ? 16 : stream_act_h_bytes(I, w.act_rows), true);
+  cv.add(&w.act_x, linear ? 16 : stream_act_x_bytes(H), true);
+  cv.add(&w.wctr, 1);
+  cv.add(&w.done_c, maxU * (I / 64));
+  cv.add(&w.x_ready, H / 64);
+  cv.add(&w.blk_counts, ncta * E, true);
+  cv.add(&w.blk_base, ncta * E, true);
+  cv.add(&w.local_rank, Rm, true);
+  cv.add(&w.x_perm, RmH, true);
+  cv.add(&w.pexp_x, Rm, true);
+  cv.add(&w.pexp_h, Rm, true);
+  cv.add(&w.tile_expert, max_tiles, true);
+  cv.add(&w.tile_row0, max_tiles, true);
+  cv.add(&w.tile_rows, max_tiles, true);
+  cv.add(&w.num_tiles, 1, true);
   cv.add(&w.status, 1);
-  cv.add(&w.logits, linear ? 1 : (size_t)c->max_tokens * c->num_experts);
+  cv.add(&w.logits, linear ? 1 : (size_t)c->max_tokens * c->num_experts, true);
   cv.add(&w.ones3, 3);
   const char* tr = getenv("NVFP4_MOE_TRACE");
   const bool trace = tr && tr[0] == '1';
@@ -326,12 +359,15 @@ nvfp4_moe_status create_handle(const nvfp4_moe_config* c, bool linear, int lin_n
 
   if (cudaMalloc(&h->blob, blob_bytes) != cudaSuccess || cudaMalloc(&h->gscale, sizeof(float) * 3 * E) != cudaSuccess ||
       cudaMalloc(&h->bias, sizeof(float) * E) != cudaSuccess || cudaMalloc(&h->in_scale, sizeof(float) * 2 * E) != cudaSuccess ||
-      cudaMalloc(&h->gs_eff, sizeof(float) * 3 * E) != cudaSuccess || cudaMalloc(&h->ws_mem, h->ws_bytes) != cudaSuccess) {
+      cudaMalloc(&h->gs_eff, sizeof(float) * 3 * E) != cudaSuccess || cudaMalloc(&h->hbound, sizeof(float) * E) != cudaSuccess ||
+      cudaMalloc(&h->ws_mem, h->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
     nvfp4_moe_destroy(h);
     return NVFP4_MOE_ERR_WORKSPACE;
   }
   cv.assign(static_cast<uint8_t*>(h->ws_mem));
+  for (size_t i = 0; i < cv.items.size(); ++i)
+    if (cv.is_data[i]) h->data_regions.push_back({static_cast<uint8_t*>(*cv.items[i].first), cv.items[i].second});
   const float ones[3] = {1.0f, 1.0f, 1.0f};
   if (cudaMemset(h->ws_mem, 0, h->ws_bytes) != cudaSuccess ||
       cudaMemcpy(w.ones3, ones, sizeof(ones), cudaMemcpyHostToDevice) != cudaSuccess) {
@@ -361,6 +397,7 @@ void nvfp4_moe_destroy(nvfp4_moe_t h) {
     if (h->w_router) cudaFree(h->w_router);
     if (h->in_scale) cudaFree(h->in_scale);
     if (h->gs_eff) cudaFree(h->gs_eff);
+    if (h->hbound) cudaFree(h->hbound);
     if (h->ws_mem) cudaFree(h->ws_mem);
   }
   delete h;
@@ -450,6 +487,23 @@ nvfp4_moe_status nvfp4_moe_set_act_quant(nvfp4_moe_t h, const float* input_scale
   return upload_gs_eff(h, st);
 }
 
+nvfp4_moe_status nvfp4_moe_debug_poison_workspace(nvfp4_moe_t h, int byte, cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (byte < 0 || byte > 255) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_poison_workspace: byte out of range");
+  DeviceGuard g(h->cfg.device);
+  for (const auto& r : h->data_regions) {
+    const cudaError_t e = cudaMemsetAsync(r.first, byte, r.second, st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "debug_poison_workspace");
+  }
+  return NVFP4_MOE_OK;
+}
+
+nvfp4_moe_status nvfp4_moe_decode_status_word(uint32_t flags) {
+  if (flags & kFlagTimeout) return NVFP4_MOE_ERR_TIMEOUT;
+  if (flags & kFlagBounds) return NVFP4_MOE_ERR_DEVICE_CHECK;
+  return NVFP4_MOE_OK;
+}
+
 nvfp4_moe_status nvfp4_moe_debug_set_fault(nvfp4_moe_t h, int fault) {
   if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
   if (fault < 0 || fault > 1) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_set_fault: unknown fault");
@@ -480,6 +534,7 @@ nvfp4_moe_status nvfp4_moe_pack(nvfp4_moe_t h, const uint8_t* w13_q, const uint8
   }
   e = cudaMemcpyAsync(h->gscale, gscale, sizeof(float) * gs.size(), cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = launch_pack(w13_q, w13_s, w2_q, w2_s, h->blob, E, h->cfg.hidden, h->cfg.inter, st);
+  if (e == cudaSuccess) e = launch_gateup_bound(w13_q, w13_s, E, h->cfg.hidden, h->cfg.inter, h->hbound, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "pack launch");
   h->gs_host = gs;
   if (h->w4a4) {
@@ -539,7 +594,10 @@ nvfp4_moe_status forward_impl(nvfp4_moe* h, const void* logits, int T, int top_k
   if (path == NVFP4_MOE_PATH_DECODE) {
     // one fused kernel: its time is reported as the gate/up stage
     if (ev[1]) cudaEventRecord(ev[1], st);
-    e = launch_decode_forward(d, h->blob, gsc, logits, x, T, top_k, out, 0, h->num_sms, h->ws, st);
+    const bool stream = use_stream(h, d, T, top_k);
+    e = stream ? launch_decode_stream(d, h->blob, gsc, logits, x, T, top_k, out, 0, h->num_sms, h->ws, h->fault, st)
+               : launch_decode_forward(d, h->blob, gsc, logits, x, T, top_k, out, 0, h->num_sms, h->ws, h->fault, st);
+    h->last_hsrc = stream ? 1 : 0;
     if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");
     if (ev[2]) cudaEventRecord(ev[2], st);
     if (ev[3]) cudaEventRecord(ev[3], st);
@@ -553,6 +611,7 @@ nvfp4_moe_status forward_impl(nvfp4_moe* h, const void* logits, int T, int top_k
     if (ev[3]) cudaEventRecord(ev[3], st);
     e = launch_combine(d, T, top_k, h->ws, out, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "combine launch");
+    h->last_hsrc = 2;
   }
   if (ev[4]) cudaEventRecord(ev[4], st);
   h->last_T = T;
@@ -690,7 +749,7 @@ nvfp4_moe_status nvfp4_moe_debug_intermediates(nvfp4_moe_t h, void* hidden, floa
   if (!hidden || !y) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "debug_intermediates: NULL output");
   DeviceGuard g(h->cfg.device);
   const size_t n = (size_t)h->last_T * h->last_k;
-  cudaError_t e = cudaMemcpyAsync(hidden, h->ws.h, n * h->cfg.inter * 2, cudaMemcpyDeviceToDevice, st);
+  cudaError_t e = launch_hidden_to_f32(h->ws, h->last_hsrc, (int)n, h->cfg.inter, static_cast<float*>(hidden), st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(y, h->ws.y, n * h->cfg.hidden * 4, cudaMemcpyDeviceToDevice, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "debug_intermediates copy");
   return NVFP4_MOE_OK;
@@ -778,7 +837,7 @@ nvfp4_moe_status nvfp4_linear_forward(nvfp4_moe_t h, int T, const void* x, void*
   if (path == NVFP4_MOE_PATH_DECODE) {
     if (ev[1]) cudaEventRecord(ev[1], st);
     if (ev[2]) cudaEventRecord(ev[2], st);
-    e = launch_decode_forward(d, h->blob, h->gscale, nullptr, x, T, 1, out, 0, h->num_sms, h->ws, st);
+    e = launch_decode_forward(d, h->blob, h->gscale, nullptr, x, T, 1, out, 0, h->num_sms, h->ws, h->fault, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "linear decode launch");
   } else {
     e = launch_route_linear(T, kTileRows, h->ws, st);

@@ -45,6 +45,7 @@
 //    instantiations, the W4A4 comparison variant (each lane quantises its
 //    16-element activation block to NVFP4 before the MMA).
 #include <cstdlib>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -124,6 +125,8 @@ struct FusedArgs {
   int32_t* cmb;
   int32_t* exit_cnt;
   DeviceStatus* st;
+  DeviceStatus* st_sticky;    // optional: the last CTA ORs this launch's status into it
+  int fault;                  // 1: no weight or activation copy is issued (tests the bounded waits)
   unsigned long long* trace;  // optional: [cta][warp][16] globaltimer stamps
 };
 
@@ -632,7 +635,7 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
     const size_t seg0 = w_seg + (size_t)wpc * 8;
     // earlier generic reads and writes of this memory come before the copies
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    if (lane == 0) {
+    if (lane == 0 && !a.fault) {
       mbar_expect_tx(bar, (uint32_t)w_cnt * (512u + 64u) + 128u * (uint32_t)w_m);
       bulk_copy(st + dec::kStA, w_nib + seg0 * 512, 512u * (uint32_t)w_cnt, bar);
       bulk_copy(st + dec::kStS, w_sc + seg0 * 64, 64u * (uint32_t)w_cnt, bar);
@@ -682,7 +685,7 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
     }
     uint8_t* st = ring + (int)(it % S) * kStageBytes;
     __syncwarp();  // the stage's expect_tx (lane 0) comes first
-    if (lane < a_m)
+    if (lane < a_m && !a.fault)
       bulk_copy(st + dec::kStB + (lane >> 3) * 8 * dec::kRowPitch + (lane & 7) * dec::kRowPitch,
                 a_row + (size_t)apc * 128, 128, bars + (int)(it % S));
     if (++apc == nch) {
@@ -983,7 +986,8 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
   }
   // on a normal exit every issued stage was consumed; after an abort, give the
   // copies still in flight a bounded chance to land before the ring is reused
-  if (dead) {
+  // (with the test fault set, no copy was ever issued)
+  if (dead && !a.fault) {
     for (int i = consumed; i < issued; ++i) {
       const uint32_t it = it0 + i;
       const uint64_t t0 = now_ns();
@@ -1078,6 +1082,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1) decode_fused_kernel(FusedArg
   if (tr && lane == 0) tr[5] = now_ns();
   if (!rs.last_cta) return;
   __threadfence();
+  if (a.st_sticky && threadIdx.x == 0) {  // every CTA's reports are in: carry them over
+    const unsigned f = atomicOr(&a.st->flags, 0u), n = atomicAdd(&a.st->nan_logits, 0u);
+    if (f && atomicOr(&a.st_sticky->flags, f) == 0u) a.st_sticky->where = *reinterpret_cast<volatile unsigned*>(&a.st->where);
+    if (n) atomicAdd(&a.st_sticky->nan_logits, n);
+  }
   const int R = a.T * a.k;
   for (int i = threadIdx.x; i < U; i += blockDim.x) a.done_gu[i] = 0;
   for (int i = threadIdx.x; i < R; i += blockDim.x) a.hmax[i] = 0u;
@@ -1150,27 +1159,42 @@ static DecodeSmemPlan plan_smem(int T, int H, int linear, bool no_xs, int smem_m
   return DecodeSmemPlan{base + S * ring1 + slot_b, S, T, 1, 0};
 }
 
+// The opt-in shared-memory size of every decode kernel instantiation,
+// set once per device (function attributes belong to each device's context).
+cudaError_t decode_prepare_device(int dev, int* smem_max) {
+  constexpr int kCached = 64;
+  static std::mutex mu;
+  static int cached[kCached] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < kCached && cached[dev]) {
+    *smem_max = cached[dev];
+    return cudaSuccess;
+  }
+  int optin = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  const void* fns[] = {(const void*)decode_fused_kernel<2, 1, false>, (const void*)decode_fused_kernel<3, 1, false>,
+                       (const void*)decode_fused_kernel<4, 1, false>, (const void*)decode_fused_kernel<5, 1, false>,
+                       (const void*)decode_fused_kernel<2, 2, false>, (const void*)decode_fused_kernel<3, 2, false>,
+                       (const void*)decode_fused_kernel<3, 1, true>,  (const void*)decode_fused_kernel<2, 2, true>,
+                       (const void*)decode_fused_kernel<3, 2, true>,
+                       (const void*)decode_fused_kernel<3, 1, false, true>,
+                       (const void*)decode_fused_kernel<4, 1, false, true>,
+                       (const void*)decode_fused_kernel<5, 1, false, true>};
+  for (const void* f : fns)
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kCached) cached[dev] = optin;
+  *smem_max = optin;
+  return cudaSuccess;
+}
+
 cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const float* gscale, const void* logits,
                                   const void* x, int T, int k, void* out, int route_only, int num_sms,
-                                  const Workspace& ws, cudaStream_t st) {
-  static int smem_max = 0;
-  if (!smem_max) {
-    int dev = 0, optin = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    const void* fns[] = {(const void*)decode_fused_kernel<2, 1, false>, (const void*)decode_fused_kernel<3, 1, false>,
-                         (const void*)decode_fused_kernel<4, 1, false>, (const void*)decode_fused_kernel<5, 1, false>,
-                         (const void*)decode_fused_kernel<2, 2, false>, (const void*)decode_fused_kernel<3, 2, false>,
-                         (const void*)decode_fused_kernel<3, 1, true>,  (const void*)decode_fused_kernel<2, 2, true>,
-                         (const void*)decode_fused_kernel<3, 2, true>,
-                         (const void*)decode_fused_kernel<3, 1, false, true>,
-                         (const void*)decode_fused_kernel<4, 1, false, true>,
-                         (const void*)decode_fused_kernel<5, 1, false, true>};
-    for (const void* f : fns)
-      if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-    if (e != cudaSuccess) return e;
-    smem_max = optin;
-  }
+                                  const Workspace& ws, int fault, cudaStream_t st) {
+  int dev = 0, smem_max = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de == cudaSuccess) de = decode_prepare_device(dev, &smem_max);
+  if (de != cudaSuccess) return de;
   const bool small = T <= 8;
   // W4A4 quantises activations from their BF16 values: no staged FP16 copy
   const DecodeSmemPlan plan = plan_smem(T, d.linear ? d.I : d.H, d.linear, d.in_scale != nullptr, smem_max);
@@ -1223,6 +1247,8 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
   a.cmb = ws.cmb;
   a.exit_cnt = ws.exit_cnt;
   a.st = ws.status;
+  a.st_sticky = ws.status_sticky;
+  a.fault = fault;
   a.trace = ws.trace;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(route_only ? 1 : num_sms);

@@ -34,12 +34,22 @@ struct Workspace {
   int32_t* blk_counts; // [nrb][E] per-rank-block histogram (prefill)
   int32_t* blk_base;   // [nrb][E] per-rank-block base inside each expert
   int32_t* local_rank; // [R] rank of a routed row inside its rank block (prefill)
-  __nv_bfloat16* x_perm; // [R][H] gathered activations (prefill)
+  __nv_bfloat16* x_perm; // [R][H] gathered activations (prefill; the MoE's in FP16 times 2^-pexp_x[row])
+  int32_t* pexp_x;       // [R] prefill: power-of-two prescale exponent of each gathered x row
+  int32_t* pexp_h;       // [R] prefill: the same for each h row (FP16 in h), from the Cauchy-Schwarz bound
   int32_t* tile_expert;  // [max_tiles] prefill m-tiles
   int32_t* tile_row0;
   int32_t* tile_rows;
   int32_t* num_tiles;    // [1]
+  // streaming decode kernel (decode_stream.cu)
+  uint8_t* act_h;       // [I/64][act_rows][144 B] h rows per 64-wide chunk: FP16 times 2^-p, float 2^p at +128
+  uint8_t* act_x;       // [H/64][16][144 B] x rows per chunk, same form (steps whose x is not kept in shared memory)
+  int act_rows;         // rows of act_h per chunk (>= T * slots of any decode step)
+  int32_t* wctr;        // [1] work items claimed beyond the first one per CTA
+  int32_t* done_c;      // [maxU][I/64] gate/up epilogue warps done per (touched expert, chunk of h)
+  int32_t* x_ready;     // [H/64] tokens of act_x converted per chunk
   DeviceStatus* status;
+  DeviceStatus* status_sticky;  // optional (decode): a status word that outlives the launch's own
   float* logits;         // [max_tokens][Er] router logits (nvfp4_moe_forward_routed)
   float* ones3;          // [3] 1.0f: tensor scales of the BF16 router GEMM
   unsigned long long* trace;  // optional per-warp phase stamps of the decode kernel (NVFP4_MOE_TRACE=1)
@@ -66,6 +76,9 @@ struct LayerDims {
   RouteParams rp;  // scoring rule of the route step
   const float* in_scale = nullptr;  // W4A4 routed experts: [E][2] input scales (w13, w2); the
                                     // caller passes tensor scales with them folded in
+  const float* gs = nullptr;        // [E][3] the forward's tensor scales (prefill routing sizes h's prescale)
+  const float* hbound = nullptr;    // [E] max_f ||Wg_f|| ||Wu_f|| (launch_gateup_bound)
+  int checks = 0;                   // 1: kernels check table-derived indices (NVFP4_MOE_CHECKS=1)
 };
 
 constexpr int kRankTokens = 64;       // tokens per rank block in the prefill routing (8 per warp)
@@ -80,6 +93,10 @@ inline size_t decode_part_floats(int num_sms, int T) {
 // W [N][K] into linear_layout(Np, K), Np = N rounded up to 128; rows N..Np-1 packed as zeros.
 cudaError_t launch_pack_linear(const uint8_t* w_q, const uint8_t* w_s, uint8_t* blob, int N, int Np, int K,
                                cudaStream_t st);
+// hb [E]: per expert, max over features f of ||Wg_f|| ||Wu_f|| (dequantised
+// rows without the tensor scales) -- the bound that sizes h's FP16 prescale.
+cudaError_t launch_gateup_bound(const uint8_t* w13_q, const uint8_t* w13_s, int E, int H, int I, float* hb,
+                                cudaStream_t st);
 cudaError_t launch_pack(const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
                         const uint8_t* w2_s, uint8_t* blob, int E, int H, int I, cudaStream_t st);
 cudaError_t launch_debug_dequant(const uint8_t* blob, const float* gscale, int H, int I, int expert,
@@ -91,9 +108,29 @@ cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const v
 // The whole decode forward (route, gate/up, down, combine) as one cooperative
 // kernel; route_only = 1 runs the routing phase alone on one CTA and writes
 // the tables (ids, wts, offsets, perm, inv) to the workspace.
+// fault = 1 issues no copies, so the kernel's bounded waits expire (tests).
 cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const float* gscale, const void* logits,
                                   const void* x, int T, int k, void* out, int route_only, int num_sms,
-                                  const Workspace& ws, cudaStream_t st);
+                                  const Workspace& ws, int fault, cudaStream_t st);
+// Sets, once per device, the decode kernels' opt-in shared-memory size; returns it.
+cudaError_t decode_prepare_device(int dev, int* smem_max);
+
+// The streaming decode kernel (decode_stream.cu): the MoE decode forward for
+// 1..16 tokens with dynamically claimed work items; route_only = 1 runs the
+// routing alone on one CTA and writes the tables.  stream_supported says
+// whether a layer and step can take it (W4A16 routed experts, not a dense
+// linear, top_k + shared <= 17).
+bool stream_supported(const LayerDims& d, int T, int k);
+cudaError_t launch_decode_stream(const LayerDims& d, const uint8_t* blob, const float* gscale, const void* logits,
+                                 const void* x, int T, int k, void* out, int route_only, int num_sms,
+                                 const Workspace& ws, int fault, cudaStream_t st);
+cudaError_t stream_prepare_device(int dev, int* smem_max);
+size_t stream_act_h_bytes(int I, int rows);
+// The hidden activations the last forward consumed, as FP32 [R][I]: src 0 --
+// the BF16 rows in ws.h; src 1 -- the streaming decode kernel's chunk rows;
+// src 2 -- the prefill GEMMs' FP16 rows in ws.h with pexp_h.
+cudaError_t launch_hidden_to_f32(const Workspace& ws, int src, int R, int I, float* out, cudaStream_t st);
+size_t stream_act_x_bytes(int H);
 
 // A dense linear's tables: every token to matrix 0 with weight 1, identity
 // perm/inv, offsets {0, T}, and m-tiles of tile_rows (16..128, a multiple of

@@ -104,6 +104,53 @@ __global__ void debug_dequant_kernel(const uint8_t* __restrict__ blob_e, const f
   }
 }
 
+// Per expert e: the largest product ||Wg_f|| ||Wu_f|| (Euclidean norms of the
+// dequantised gate and up rows of feature f, e2m1 * e4m3 without the tensor
+// scales) over its features, written as float bits by atomicMax (hb starts
+// at zero).  With the tensor scales and ||x||^2 it bounds every |h| of a
+// routed row: |silu(g)| <= |g| <= gs_g ||Wg_f|| ||x|| (Cauchy-Schwarz) and
+// |u| <= gs_u ||Wu_f|| ||x||, which sizes the power-of-two prescale of h for
+// the prefill down GEMM's FP16 operand.  One warp per (expert, feature);
+// canonical layout: gate rows 0..I-1, up rows I..2I-1.
+__global__ void gateup_bound_kernel(const uint8_t* __restrict__ w13_q, const uint8_t* __restrict__ w13_s, int E,
+                                    int H, int I, float* __restrict__ hb) {
+  const size_t wid = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= (size_t)E * I) return;
+  const int e = (int)(wid / I), f = (int)(wid - (size_t)e * I);
+  float ss[2];
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    const size_t row = (size_t)e * 2 * I + (size_t)w * I + f;
+    const uint8_t* q = w13_q + row * (H / 2);
+    const uint8_t* sc = w13_s + row * (H / 16);
+    float acc = 0.f;
+    for (int j = lane; j < H / 2; j += 32) {  // byte j: elements 2j, 2j+1 of group j / 8
+      const uint32_t v = e2m1x2_to_f16x2(q[j]);
+      const uint32_t s2 = e4m3x2_to_f16x2(sc[j >> 3]);
+      const float s = __half2float(__ushort_as_half((unsigned short)(s2 & 0xFFFFu)));
+      const float a0 = __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))) * s;
+      const float a1 = __half2float(__ushort_as_half((unsigned short)(v >> 16))) * s;
+      acc = fmaf(a0, a0, fmaf(a1, a1, acc));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    ss[w] = acc;
+  }
+  // FP32 sums of at most 16384 exact squares: a relative margin of 2^-10 keeps it an upper bound
+  const float b = sqrtf(ss[0]) * sqrtf(ss[1]) * (1.0f + 1.0f / 1024.0f);
+  if (lane == 0 && b > 0.f) atomicMax(reinterpret_cast<unsigned*>(hb + e), __float_as_uint(b));
+}
+
+cudaError_t launch_gateup_bound(const uint8_t* w13_q, const uint8_t* w13_s, int E, int H, int I, float* hb,
+                                cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(hb, 0, sizeof(float) * E, st);
+  if (e != cudaSuccess) return e;
+  const size_t warps = (size_t)E * I;
+  gateup_bound_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(w13_q, w13_s, E, H, I, hb);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_pack(const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q,
                         const uint8_t* w2_s, uint8_t* blob, int E, int H, int I, cudaStream_t st) {
   const ExpertLayout L = expert_layout(H, I);

@@ -6,6 +6,13 @@
 // API, and produced garbage: the working backend dequantises to bf16 and
 // consumes no activation scale).
 //
+// The MoE's GEMMs run on FP16 operands (kF16): the dequantised weights
+// (e2m1 * e4m3, exact in FP16), the gathered x rows and h, each row scaled by a
+// power of two that the epilogues undo in FP32 (x: its largest magnitude in
+// [2^13, 2^14); h: a Cauchy-Schwarz bound on its row, see route.cu), so h
+// keeps 11 significant bits between the GEMMs.  The dense linear and the
+// router GEMM stay on BF16 operands (the caller's BF16 x, the BF16 router).
+//
 // One persistent CTA per SM, 15 warps, warp-specialised:
 //   warp 0      weight producer: cp.async.bulk of the packed FP4 chunks (+
 //               scales) of a unit's two 128-row weight blocks into a
@@ -30,6 +37,8 @@
 // accumulator row and its up partner sit 8 TMEM lanes apart, inside one warp.
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the handle's status word and winds down instead of hanging.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -93,6 +102,10 @@ struct PrefillArgs {
   int Er;
   DeviceStatus* st;
   int fault;  // 1: the producer issues nothing (tests the bounded waits)
+  const int32_t* pexp_x;  // [R] FP16 operand rows: x row p was scaled by 2^-pexp_x[p] (kF16)
+  const int32_t* pexp_h;  // [R] and h row p by 2^-pexp_h[p]
+  int checks;             // 1: check the m-tile table against its ranges (kFlagBounds; the unit is skipped)
+  int E, R;               // experts in the blob, routed rows (for the checks)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -161,9 +174,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// kind::f16 instruction descriptor: D = F32, A = B = BF16, both K-major.
+// kind::f16 instruction descriptor: D = F32, A = B = BF16 (or both F16), both K-major.
 __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
@@ -193,7 +209,9 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 }
 
 // Dequantise one packed 16-byte segment (rows R0, R0+8; K elements 16q..16q+15
-// of the chunk) into the swizzled BF16 operand tile at a_base.
+// of the chunk) into the swizzled 16-bit operand tile at a_base (FP16 when
+// kF16, else BF16; both exact).
+template <bool kF16>
 __device__ __forceinline__ void dequant_segment(const uint8_t* raw_stage, uint32_t a_base, int seg) {
   const uint4 raw = *reinterpret_cast<const uint4*>(raw_stage + seg * 16);
   const uint32_t sc = *reinterpret_cast<const uint16_t*>(raw_stage + 4096 + seg * 2);
@@ -209,7 +227,8 @@ __device__ __forceinline__ void dequant_segment(const uint8_t* raw_stage, uint32
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint32_t byte = (j < 4 ? w0 : w1) >> (8 * (j & 3));
-      o[j] = f16x2_to_bf16x2(hmul2_u32(e2m1x2_to_f16x2(byte), sx));
+      const uint32_t v = hmul2_u32(e2m1x2_to_f16x2(byte), sx);
+      o[j] = kF16 ? v : f16x2_to_bf16x2(v);
     }
     const uint32_t row_base = a_base + (uint32_t)((R >> 3) * 1024 + (R & 7) * 128);
     const uint32_t c0 = (uint32_t)((2 * q) ^ (R & 7)), c1 = (uint32_t)((2 * q + 1) ^ (R & 7));
@@ -221,7 +240,7 @@ __device__ __forceinline__ void dequant_segment(const uint8_t* raw_stage, uint32
 // kBf16W: the weights are a plain BF16 matrix (the router): warp 0 moves its
 // 128-row x 64-column tiles straight into the operand ring by TMA (128B
 // swizzle, the layout the dequantisers write), and the dequantisers idle.
-template <bool kGateUp, bool kBf16W = false>
+template <bool kGateUp, bool kBf16W = false, bool kF16 = false>
 __global__ void __launch_bounds__(pf::kThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_w,
                         PrefillArgs a) {
@@ -311,6 +330,12 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const int tile = unit / NP, nb0 = 2 * (unit % NP);
         const int nblk = nb0 + 1 < a.NB ? 2 : 1;
         const int e = a.tile_expert[tile];
+        if (a.checks && (e < 0 || e >= a.E || a.tile_row0[tile] < 0 || a.tile_rows[tile] < 1 ||
+                         a.tile_rows[tile] > kTileRows || a.tile_row0[tile] + a.tile_rows[tile] > a.R)) {
+          report(a.st, kFlagBounds, 810);
+          *abort_flag = 1;
+          break;
+        }
         const uint8_t* src_nib = a.blob + (size_t)e * a.expert_stride + a.nib_off + (size_t)nb0 * nch * 4096;
         const uint8_t* src_sc = a.blob + (size_t)e * a.expert_stride + a.sc_off + (size_t)nb0 * nch * 512;
         for (int c = 0; c < nch; ++c, ++it) {
@@ -335,7 +360,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const int nblk = nb0 + 1 < a.NB ? 2 : 1;
         const int rows = a.tile_rows[tile];
         const int N = (rows + 15) & ~15;
-        const uint32_t idesc = idesc_bf16(128, N);
+        const uint32_t idesc = kF16 ? idesc_f16(128, N) : idesc_bf16(128, N);
         const uint32_t buf = j & 1u, aph = (j >> 1) & 1u;
         if (!mbar_wait(accempty + buf, aph ^ 1u, abort_flag, a.st, 2)) break;
         tc_fence_after();
@@ -410,8 +435,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         }
         const uint8_t* raw_stage = smem + pf::kRawOff + sr * pf::kRawStageBytes;
         const uint32_t a_base = smem_u32(smem + pf::kAOff + sa * pf::kAStageBytes);
-        dequant_segment(raw_stage, a_base, tau);
-        if (nblk > 1) dequant_segment(raw_stage + pf::kRawBlockBytes, a_base + pf::kABlockBytes, tau);
+        dequant_segment<kF16>(raw_stage, a_base, tau);
+        if (nblk > 1) dequant_segment<kF16>(raw_stage + pf::kRawBlockBytes, a_base + pf::kABlockBytes, tau);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
@@ -448,12 +473,17 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             const float gsg = gs[0], gsu = gs[1];
             // W4A4 routed expert: h (rounded to BF16) is quantised to NVFP4 with the
             // w2 input scale; this warp's 16 gate lanes hold one 16-feature block
+            // the x rows entered scaled by 2^-pexp_x (FP16 operands): undo it per column
+            float sx[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              sx[jj] = (kF16 && col + jj < rows) ? __int_as_float((127 + __ldg(a.pexp_x + row0 + col + jj)) << 23) : 1.0f;
             if (a.in_scale != nullptr && e < a.Er) {
               const float is1 = __ldg(a.in_scale + 2 * e + 1), inv6 = act_inv6(is1);
               float hv[16], am[16];
 #pragma unroll
               for (int jj = 0; jj < 16; ++jj) {
-                const float mine = __uint_as_float(v[jj]);
+                const float mine = __uint_as_float(v[jj]) * sx[jj];
                 const float partner = __shfl_xor_sync(0xffffffffu, mine, 8);
                 hv[jj] = is_gate ? __bfloat162float(__float2bfloat16_rn(silu(gsg * mine) * (gsu * partner))) : 0.f;
                 am[jj] = fabsf(hv[jj]);
@@ -468,16 +498,25 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 #pragma unroll
               for (int jj = 0; jj < 16; ++jj) {
                 const float q = act_quant1(hv[jj], act_block_scale(am[jj], inv6, is1));
-                if (is_gate && col + jj < rows) a.h[(size_t)(row0 + col + jj) * a.I + f] = __float2bfloat16_rn(q);
+                if (is_gate && col + jj < rows) {
+                  const size_t o = (size_t)(row0 + col + jj) * a.I + f;
+                  if (kF16) reinterpret_cast<__half*>(a.h)[o] = __float2half_rn(q);  // code * scale: exact
+                  else a.h[o] = __float2bfloat16_rn(q);
+                }
               }
             } else {
 #pragma unroll
               for (int jj = 0; jj < 16; ++jj) {
-                const float mine = __uint_as_float(v[jj]);
+                const float mine = __uint_as_float(v[jj]) * sx[jj];
                 const float partner = __shfl_xor_sync(0xffffffffu, mine, 8);
                 if (is_gate && col + jj < rows) {
                   const float g = gsg * mine, u = gsu * partner;
-                  a.h[(size_t)(row0 + col + jj) * a.I + f] = __float2bfloat16_rn(silu(g) * u);
+                  const size_t o = (size_t)(row0 + col + jj) * a.I + f;
+                  if (kF16)  // h times 2^-pexp_h as the down GEMM's FP16 operand (11 significant bits)
+                    reinterpret_cast<__half*>(a.h)[o] = __float2half_rn(
+                        silu(g) * u * __int_as_float((127 - __ldg(a.pexp_h + row0 + col + jj)) << 23));
+                  else
+                    a.h[o] = __float2bfloat16_rn(silu(g) * u);
                 }
               }
             }
@@ -498,7 +537,11 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             } else {
 #pragma unroll
               for (int jj = 0; jj < 16; ++jj)
-                if (col + jj < rows) a.y[(size_t)(row0 + col + jj) * a.H + d] = gsd * __uint_as_float(v[jj]);
+                if (col + jj < rows) {
+                  // h row p entered scaled by 2^-pexp_h[p]
+                  const float sh = kF16 ? __int_as_float((127 + __ldg(a.pexp_h + row0 + col + jj)) << 23) : 1.0f;
+                  a.y[(size_t)(row0 + col + jj) * a.H + d] = gsd * (__uint_as_float(v[jj]) * sh);
+                }
             }
           }
         }
@@ -518,24 +561,31 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   }
 }
 
+// The opt-in shared-memory size of every prefill kernel instantiation, set once
+// per device (function attributes belong to each device's context).
 static cudaError_t set_prefill_attrs() {
-  static bool attr_set = false;
-  if (attr_set) return cudaSuccess;
+  constexpr int kCached = 64;
+  static std::mutex mu;
+  static bool done[kCached] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < kCached && done[dev]) return cudaSuccess;
   const void* fns[] = {(const void*)prefill_gemm_kernel<true>, (const void*)prefill_gemm_kernel<false>,
-                       (const void*)prefill_gemm_kernel<false, true>};
+                       (const void*)prefill_gemm_kernel<false, true>, (const void*)prefill_gemm_kernel<true, false, true>,
+                       (const void*)prefill_gemm_kernel<false, false, true>};
   for (const void* f : fns) {
-    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::kSmemBytes);
+    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::kSmemBytes);
     if (e != cudaSuccess) return e;
   }
-  attr_set = true;
+  if (dev >= 0 && dev < kCached) done[dev] = true;
   return cudaSuccess;
 }
 
 cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const float* gscale, int T, int k,
                                int num_sms, const PrefillMaps& maps, const Workspace& ws, int fault,
                                cudaEvent_t mid, void* out, cudaStream_t st) {
-  (void)T;
-  (void)k;
   cudaError_t ea = set_prefill_attrs();
   if (ea != cudaSuccess) return ea;
   const ExpertLayout L = d.linear ? linear_layout(d.H, d.I) : expert_layout(d.H, d.I);
@@ -559,12 +609,17 @@ cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const fl
   a.Er = d.Er;
   a.st = ws.status;
   a.fault = fault;
-  if (!d.linear) {  // gate/up: 2I interleaved rows, K = H
+  a.pexp_x = ws.pexp_x;
+  a.pexp_h = ws.pexp_h;
+  a.checks = d.checks;
+  a.E = d.E;
+  a.R = T * (k + d.S);
+  if (!d.linear) {  // gate/up: 2I interleaved rows, K = H (FP16 operands)
     a.nib_off = L.w13_nib;
     a.sc_off = L.w13_sc;
     a.K = d.H;
     a.NB = 2 * d.I / 128;
-    prefill_gemm_kernel<true><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(maps.x_perm, maps.x_perm, a);
+    prefill_gemm_kernel<true, false, true><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(maps.x_perm, maps.x_perm, a);
   }
   if (mid) cudaEventRecord(mid, st);
   // down: H rows, K = I
@@ -572,7 +627,10 @@ cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const fl
   a.sc_off = L.w2_sc;
   a.K = d.I;
   a.NB = d.H / 128;
-  prefill_gemm_kernel<false><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(maps.h, maps.h, a);
+  if (d.linear)  // the caller's BF16 x
+    prefill_gemm_kernel<false><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(maps.h, maps.h, a);
+  else
+    prefill_gemm_kernel<false, false, true><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(maps.h, maps.h, a);
   return cudaGetLastError();
 }
 

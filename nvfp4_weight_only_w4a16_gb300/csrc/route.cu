@@ -122,12 +122,20 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int nblocks, int E, Wo
 }
 
 // K4: one warp per routed row: its position, perm/inv, and (unless only
-// routing) the copy of x[t] into position order.
-// W4A4 (in_scale set, routed experts e < Er): the copy holds x quantised to
-// NVFP4 with the expert's w13 input scale, as code * scale in BF16 (exact).
+// routing) the copy of x[t] into position order as the FP16 operand of the
+// grouped GEMMs:
+//  * W4A16 experts: x times 2^-px, px such that the row's largest magnitude
+//    lands in [2^13, 2^14) (exact for every BF16 value within 2^31 of it);
+//    and the exponent ph of the row's h: the bound B = gs_g gs_u hb[e] ||x||^2
+//    on every |h| of the row (|silu(g)| <= |g| <= gs_g ||Wg_f|| ||x|| and
+//    |u| <= gs_u ||Wu_f|| ||x||, Cauchy-Schwarz; hb from launch_gateup_bound)
+//    times 2^-ph stays below 2^13, so h times 2^-ph fits FP16;
+//  * W4A4 experts (in_scale set, e < Er): x quantised to NVFP4 with the
+//    expert's w13 input scale, code * scale (exact in FP16), px = ph = 0.
 __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int k,
                                                             int E, int H, const float* __restrict__ in_scale,
-                                                            int Er, Workspace ws) {
+                                                            int Er, const float* __restrict__ gs,
+                                                            const float* __restrict__ hbound, Workspace ws) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t i = (size_t)blockIdx.x * 8 + warp;
   if (i >= (size_t)T * k) return;
@@ -142,12 +150,53 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16*
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
   uint4* dst = reinterpret_cast<uint4*>(ws.x_perm + (size_t)pos * H);
   if (in_scale == nullptr || e >= Er) {
-    for (int v = lane; v < H / 8; v += 32) dst[v] = __ldg(src + v);
+    // pass 1: the row's largest magnitude and squared norm
+    float m = 0.f, n2 = 0.f;
+    for (int v = lane; v < H / 8; v += 32) {
+      const uint4 u = __ldg(src + v);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int z = 0; z < 4; ++z) {
+        const float lo = __uint_as_float(w[z] << 16), hi = __uint_as_float(w[z] & 0xFFFF0000u);
+        m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
+        n2 = fmaf(lo, lo, fmaf(hi, hi, n2));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+    }
+    const int px = max(-126, min(126, prescale_exp(m)));
+    // FP32 sums and products: a factor 2 of margin keeps B an upper bound
+    const float B = 2.0f * __ldg(gs + 3 * e) * __ldg(gs + 3 * e + 1) * __ldg(hbound + e) * n2;
+    const int ph = B > 3.0e38f ? 126 : max(-126, min(126, prescale_exp(B)));
+    if (lane == 0) {
+      ws.pexp_x[pos] = px;
+      ws.pexp_h[pos] = ph;
+    }
+    const float sc = __int_as_float((127 - px) << 23);
+    // pass 2: the scaled FP16 row (the source is in L1/L2 now)
+    for (int v = lane; v < H / 8; v += 32) {
+      const uint4 u = __ldg(src + v);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int z = 0; z < 4; ++z) {
+        const __half2 hh = __floats2half2_rn(__uint_as_float(w[z] << 16) * sc, __uint_as_float(w[z] & 0xFFFF0000u) * sc);
+        o[z] = *reinterpret_cast<const uint32_t*>(&hh);
+      }
+      dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
     return;
   }
+  if (lane == 0) {
+    ws.pexp_x[pos] = 0;
+    ws.pexp_h[pos] = 0;
+  }
   const float is = __ldg(in_scale + 2 * e), inv6 = act_inv6(is);
-  for (int b = lane; b < H / 16; b += 32) {  // one 16-element block per lane
-    const uint4 u0 = __ldg(src + 2 * b), u1 = __ldg(src + 2 * b + 1);
+  for (int bk = lane; bk < H / 16; bk += 32) {  // one 16-element block per lane
+    const uint4 u0 = __ldg(src + 2 * bk), u1 = __ldg(src + 2 * bk + 1);
     const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
     float v[16];
 #pragma unroll
@@ -157,10 +206,8 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const __nv_bfloat16*
     }
     uint32_t o[8];
     act_quant16_f16(v, is, inv6, o);
-#pragma unroll
-    for (int z = 0; z < 8; ++z) o[z] = f16x2_to_bf16x2(o[z]);
-    dst[2 * b] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[2 * b + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    dst[2 * bk] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[2 * bk + 1] = make_uint4(o[4], o[5], o[6], o[7]);
   }
 }
 
@@ -173,7 +220,7 @@ cudaError_t launch_route_prefill(const LayerDims& d, const void* logits, const v
   route_scan_kernel<<<1, 1024, 0, st>>>(nrb, d.E, ws);
   const size_t rows = (size_t)T * k;
   route_scatter_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), T,
-                                                                   k, d.E, d.H, d.in_scale, d.Er, ws);
+                                                                   k, d.E, d.H, d.in_scale, d.Er, d.gs, d.hbound, ws);
   return cudaGetLastError();
 }
 

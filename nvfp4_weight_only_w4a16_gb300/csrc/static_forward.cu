@@ -22,9 +22,14 @@
 //    GPU (different streams, or graphs replayed concurrently) race and give
 //    wrong results; serialise them;
 //  * the array keeps the last call's contents; the regions that must start at
-//    zero are cleared (cudaMemsetAsync) by every call.
+//    zero are cleared (cudaMemsetAsync) by every call;
+//  * device-side errors (a bounded wait that gave up, NaN router logits) of
+//    every call are carried into a status word at the start of the array,
+//    which no call clears: nvfp4_moe_static_get_status reads and clears it.
 #include <algorithm>
+#include <atomic>
 #include <mutex>
+#include <string>
 
 #include "../../include/nvfp4_moe.h"
 #include "kernels.h"
@@ -45,16 +50,21 @@ struct StaticSetup {
 
 std::mutex g_setup_mutex;
 StaticSetup g_setup[kMaxDevices];
+std::atomic<int> g_fault{0};  // test hook: 1 makes the next calls issue no weight copies
 
-// Once per device, with that device current.
+// Once per device, with that device current: the array's device address, the
+// SM count and the decode kernels' shared-memory attribute.
 cudaError_t static_setup(int dev, StaticSetup* out) {
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (!g_setup[dev].scratch) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) return e;
-    int sms = 0;
+    int sms = 0, smem = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = decode_prepare_device(dev, &smem);
+    if (e == cudaSuccess) e = stream_prepare_device(dev, &smem);
     if (e != cudaSuccess) return e;
     g_setup[dev].scratch = static_cast<uint8_t*>(p);
     g_setup[dev].num_sms = sms;
@@ -74,24 +84,32 @@ struct Region {
   }
 };
 
+// The status word that outlives each call, at the start of the array.
+constexpr size_t kStickyBytes = 256;
+
 // Carves the decode workspace out of `base`; returns the bytes it needs.
-// With base == nullptr only the size is computed.  The zero-initialised
-// regions (split-K partials, counters, status) are contiguous at the front:
-// [0, *zero_bytes).
-size_t carve(uint8_t* base, int E, int H, int I, int T, int k, int num_sms, Workspace* ws, size_t* zero_bytes) {
+// With base == nullptr only the size is computed.  [0, kStickyBytes) holds the
+// status word carried across calls; the regions every call zeroes (counters,
+// the call's own status) follow contiguously: [kStickyBytes, *zero_end).
+size_t carve(uint8_t* base, int E, int H, int I, int T, int k, int num_sms, Workspace* ws, size_t* zero_end) {
   const size_t R = (size_t)T * k;
   const size_t maxU = std::min<size_t>((size_t)E, R);
   uint8_t* b = base ? base : reinterpret_cast<uint8_t*>(0x100);
   Region r;
   Workspace w{};
+  w.status_sticky = r.take<DeviceStatus>(b, 1);
+  r.off = kStickyBytes;
   w.cnt_gu = r.take<int32_t>(b, maxU * (2 * I / 16));
   w.cnt_dn = r.take<int32_t>(b, maxU * (H / 16));
   w.done_gu = r.take<int32_t>(b, maxU);
   w.cmb = r.take<int32_t>(b, H / 64);
   w.exit_cnt = r.take<int32_t>(b, 1);
   w.hmax = r.take<uint32_t>(b, R);
+  w.wctr = r.take<int32_t>(b, 1);
+  w.done_c = r.take<int32_t>(b, maxU * (I / 64));
+  w.x_ready = r.take<int32_t>(b, H / 64);
   w.status = r.take<DeviceStatus>(b, 1);
-  *zero_bytes = (r.off + 255) & ~size_t(255);
+  *zero_end = (r.off + 255) & ~size_t(255);
   // no split-K partial-sum buffers here: with part_gu == nullptr the decode
   // kernel gives every warp whole blocks
   w.part_gu = nullptr;
@@ -110,6 +128,9 @@ size_t carve(uint8_t* base, int E, int H, int I, int T, int k, int num_sms, Work
   w.xexp = r.take<int32_t>(b, T);
   w.h = r.take<__nv_bfloat16>(b, R * I);
   w.y = r.take<float>(b, R * H);
+  w.act_rows = (int)R;
+  w.act_h = r.take<uint8_t>(b, stream_act_h_bytes(I, (int)R));
+  w.act_x = r.take<uint8_t>(b, stream_act_x_bytes(H));
   if (base && ws) *ws = w;
   return r.off;
 }
@@ -136,19 +157,44 @@ extern "C" nvfp4_moe_status nvfp4_moe_forward_decode_static(const uint8_t* packe
       !aligned_to(router_logits, logits_dtype == NVFP4_MOE_LOGITS_BF16 ? 2 : 4))
     return NVFP4_MOE_ERR_INVALID_ARG;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_MOE_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_MOE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return NVFP4_MOE_ERR_INVALID_ARG;  // device ordinals 0..63 only
   StaticSetup setup;
   if (static_setup(dev, &setup) != cudaSuccess) return NVFP4_MOE_ERR_CUDA;
-  size_t zero_bytes = 0;
-  if (carve(nullptr, E, H, I, T, top_k, setup.num_sms, nullptr, &zero_bytes) > kStaticScratchBytes)
+  size_t zero_end = 0;
+  if (carve(nullptr, E, H, I, T, top_k, setup.num_sms, nullptr, &zero_end) > kStaticScratchBytes)
     return NVFP4_MOE_ERR_UNSUPPORTED_SHAPE;  // needs more than the static scratch holds
 
   Workspace ws{};
-  carve(setup.scratch, E, H, I, T, top_k, setup.num_sms, &ws, &zero_bytes);
+  carve(setup.scratch, E, H, I, T, top_k, setup.num_sms, &ws, &zero_end);
   const LayerDims d{E, H, I, logits_dtype == NVFP4_MOE_LOGITS_BF16, 0, E, 0, 0, 0};
-  cudaError_t e = cudaMemsetAsync(setup.scratch, 0, zero_bytes, stream);
+  cudaError_t e = cudaMemsetAsync(setup.scratch + kStickyBytes, 0, zero_end - kStickyBytes, stream);
   if (e == cudaSuccess)
-    e = launch_decode_forward(d, packed_experts, gscale, router_logits, x, T, top_k, out, 0, setup.num_sms, ws,
-                              stream);
+    e = stream_supported(d, T, top_k)
+            ? launch_decode_stream(d, packed_experts, gscale, router_logits, x, T, top_k, out, 0, setup.num_sms, ws,
+                                   g_fault.load(), stream)
+            : launch_decode_forward(d, packed_experts, gscale, router_logits, x, T, top_k, out, 0, setup.num_sms, ws,
+                                    g_fault.load(), stream);
   return e == cudaSuccess ? NVFP4_MOE_OK : NVFP4_MOE_ERR_CUDA;
+}
+
+extern "C" nvfp4_moe_status nvfp4_moe_static_get_status(uint32_t* nan_logits) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_MOE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return NVFP4_MOE_ERR_INVALID_ARG;
+  StaticSetup setup;
+  if (static_setup(dev, &setup) != cudaSuccess) return NVFP4_MOE_ERR_CUDA;
+  DeviceStatus ds{};
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&ds, setup.scratch, sizeof(ds), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(setup.scratch, 0, sizeof(ds));
+  if (e != cudaSuccess) return NVFP4_MOE_ERR_CUDA;
+  if (nan_logits) *nan_logits = ds.nan_logits;
+  return nvfp4_moe_decode_status_word(ds.flags);
+}
+
+extern "C" nvfp4_moe_status nvfp4_moe_static_debug_set_fault(int fault) {
+  if (fault < 0 || fault > 1) return NVFP4_MOE_ERR_INVALID_ARG;
+  g_fault.store(fault);
+  return NVFP4_MOE_OK;
 }

@@ -115,3 +115,14 @@ def test_linear_header_has_no_activation_scale():
     fwd = text[text.index("nvfp4_moe_status nvfp4_linear_forward("):]
     fwd = fwd[:fwd.index(";")]
     assert "scale" not in fwd
+
+
+def test_status_word_decoding_on_the_host():
+    """The device status word's bits map to status codes without a GPU: bit 0
+    a bounded wait that gave up, bit 1 a device-side bounds check."""
+    lib = P.binding.load_library()
+    code = P.STATUS_CODE
+    assert lib.nvfp4_moe_decode_status_word(0) == code["NVFP4_MOE_OK"]
+    assert lib.nvfp4_moe_decode_status_word(1) == code["NVFP4_MOE_ERR_TIMEOUT"]
+    assert lib.nvfp4_moe_decode_status_word(2) == code["NVFP4_MOE_ERR_DEVICE_CHECK"]
+    assert lib.nvfp4_moe_decode_status_word(3) == code["NVFP4_MOE_ERR_TIMEOUT"]

@@ -16,7 +16,7 @@ import oracle as O
 from synth import CONFIGS, LinearConfig, make_inputs, make_input_scales, make_linear_inputs, make_router_weight
 import nvfp4_weight_only_w4a16_gb300 as P
 from tests.test_gpu_parity import DEV, _dev
-from tests.test_gpu_w4a4 import _check_layer
+from tests.test_gpu_w4a4 import check_w4a4_layer
 from tests.test_gpu_linear import _abs_sum, _check, _run
 
 pytestmark = pytest.mark.gpu
@@ -44,8 +44,7 @@ def test_shared_router_sigmoid_bias_w4a4_together(path):
         assert L.nvfp4_moe_get_status()[0] == 0
         logits = L.nvfp4_moe_debug_logits(cfg.tokens).cpu().numpy()
         sc = dict(score="sigmoid", renormalize=True, scale=1.5, bias=bias)
-        ref = O.moe_forward_w4a4(logits, inp.x_bits, inp.weights, cfg.top_k, iscale, num_shared=1, scoring=sc)
-        _check_layer(out.float().cpu().numpy().astype(np.float64), ref)
+        check_w4a4_layer(out.float().cpu().numpy().astype(np.float64), inp, iscale, logits=logits, scoring=sc)
     finally:
         L.close()
 

@@ -13,17 +13,28 @@ Bars:
   for ("GLM-5.3-Flash on Blackwell", The model loaded, served an API, and
   produced garbage: an inverted scale kept cosine 0.996 at 25x the
   magnitude): ||gpu|| / ||oracle|| in [0.99, 1.01] and cosine >= 0.9999.
-Full-size workloads compare sampled tokens, which the oracle computes one by
-one; routing and permutation are compared on every token.
+Every workload is compared on every token: the oracle's layer at 1K and 16K
+tokens runs over a process pool (oracle.pool: the oracle's own expert FFNs,
+one task per expert) once per session, cached in memory and under
+tests/.oracle_cache (git-ignored).  Per routed row, h and y are checked
+element-wise against intervals derived from the oracle and the kernels' FP32
+arithmetic (tests/intervals.py): every row of the tiny layer and of the
+decode workloads, and at 1K and 16K every row of the most-used expert (all
+its 128-row m-tiles, the partial last one included) and of the three
+least-used experts.
 """
+import hashlib
+import os
 import numpy as np
 import pytest
 
 torch = pytest.importorskip("torch")
 
 import oracle as O
+from oracle.pool import moe_forward_pool
 from synth import CONFIGS, make_inputs, make_layer_weights, LayerConfig, f32_to_bf16_bits
 import nvfp4_weight_only_w4a16_gb300 as P
+from tests.intervals import _mats, hidden_bounds_w4a16, down_bounds_w4a16, assert_inside
 
 pytestmark = pytest.mark.gpu
 
@@ -49,6 +60,40 @@ def _layer(cfg: LayerConfig, max_tokens=None, logits_bf16=False, out_f32=False):
 
 def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+_REF = {}
+_CACHE_DIR = os.path.join(os.path.dirname(__file__), ".oracle_cache")
+
+
+def _source_key(name):
+    h = hashlib.sha256(name.encode())
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for d in ("oracle", "synth"):
+        for f in sorted(os.listdir(os.path.join(root, d))):
+            if f.endswith(".py"):
+                with open(os.path.join(root, d, f), "rb") as fh:
+                    h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def layer_reference(name):
+    """The oracle's layer output [T][H] (float64) on every token of a
+    workload, via the process pool; cached in memory and on disk."""
+    if name in _REF:
+        return _REF[name]
+    path = os.path.join(_CACHE_DIR, f"{name}-{_source_key(name)}.npy")
+    if os.path.exists(path):
+        _REF[name] = np.load(path)
+        return _REF[name]
+    inp = make_inputs(name)
+    out = moe_forward_pool(inp.logits, inp.x_bits, inp.weights, inp.config.top_k,
+                           num_shared=inp.config.shared)
+    os.makedirs(_CACHE_DIR, exist_ok=True)
+    np.save(path + ".tmp.npy", out)
+    os.replace(path + ".tmp.npy", path)
+    _REF[name] = out
+    return out
 
 
 def _forward(L, logits, x_bits, k, path=P.PATH_AUTO):
@@ -225,27 +270,44 @@ def test_forward_tiny(path):
     assert_layer_close(gpu, ref)
 
 
+def check_rows(L, inp, rows, k=None):
+    """h and y of routed rows (positions, expert-major) against the interval
+    checks: h inside the BF16 interval of the oracle's expert, y inside the
+    down projection of the GPU's own h."""
+    cfg = inp.config
+    k = k or cfg.top_k
+    T = cfg.tokens
+    R = T * (k + cfg.shared)
+    hid, y = L.nvfp4_moe_debug_intermediates(R)
+    rows = np.asarray(rows, dtype=np.int64)
+    sel = torch.from_numpy(rows).to(hid.device)
+    hid = hid[sel].float().cpu().numpy().astype(np.float64)
+    y = y[sel].cpu().numpy().astype(np.float64)
+    r = O.route(inp.logits, k)
+    ids = r.ids
+    if cfg.shared:
+        ids = np.concatenate([ids, np.full((T, 1), cfg.num_experts, np.int32)], axis=1)
+    _, _, perm = O.permute(ids, cfg.num_experts + cfg.shared)
+    flat = perm[rows]
+    tok, slot = flat // ids.shape[1], flat % ids.shape[1]
+    ex = ids[tok, slot]
+    x = O.bf16_bits_to_f64(inp.x_bits)
+    for e in np.unique(ex):
+        m = ex == e
+        mats = _mats(inp.weights, int(e))
+        hl, hh = hidden_bounds_w4a16(mats, x[tok[m]])
+        assert_inside(hid[m], hl, hh, ("h", int(e)))
+        yl, yh = down_bounds_w4a16(mats, hid[m])
+        assert_inside(y[m], yl, yh, ("y", int(e)))
+
+
 @pytest.mark.parametrize("path", [P.PATH_DECODE, P.PATH_PREFILL])
 def test_intermediates_tiny(path):
     inp = make_inputs("tiny")
     cfg = inp.config
     L = _layer(cfg)
     _forward(L, inp.logits, inp.x_bits, cfg.top_k, path)
-    T, k = cfg.tokens, cfg.top_k
-    hid, y = L.nvfp4_moe_debug_intermediates(T * k)
-    hid = hid.float().cpu().numpy().astype(np.float64)
-    y = y.cpu().numpy().astype(np.float64)
-    r = O.route(inp.logits, k)
-    _, _, perm = O.permute(r.ids, cfg.num_experts)
-    x = O.bf16_bits_to_f64(inp.x_bits)
-    for p in range(T * k):
-        t, j = divmod(int(perm[p]), k)
-        e = int(r.ids[t, j])
-        h_ref = O.expert_hidden(inp.weights, e, x[t:t + 1])[0]
-        # h is rounded to BF16 once: relative error <= 2^-8 of each element
-        assert np.all(np.abs(hid[p] - h_ref) <= 2.0 ** -8 * np.abs(h_ref) + 1e-6 * np.abs(h_ref).max())
-        y_ref = O.expert_ffn(inp.weights, e, x[t:t + 1])[0]
-        assert np.abs(y[p] - y_ref).max() <= 1e-2 * np.sqrt(np.mean(y_ref ** 2))
+    check_rows(L, inp, range(cfg.tokens * cfg.top_k))
 
 
 @pytest.mark.parametrize("out_f32", [True, False])
@@ -255,37 +317,36 @@ def test_forward_decode_full_size(name, out_f32):
     cfg = inp.config
     L = _layer(cfg, max_tokens=1024, out_f32=out_f32)
     gpu = _forward(L, inp.logits, inp.x_bits, cfg.top_k)
-    tokens = np.arange(cfg.tokens) if cfg.tokens <= 2 else np.array([0, 5, 10, 15])
-    ref = O.moe_forward(inp.logits, inp.x_bits, inp.weights, cfg.top_k, tokens=tokens)
-    assert_layer_close(gpu[tokens], ref, bf16_out=not out_f32)
+    ref = O.moe_forward(inp.logits, inp.x_bits, inp.weights, cfg.top_k)
+    assert_layer_close(gpu, ref, bf16_out=not out_f32)
+    if out_f32:
+        check_rows(L, inp, range(cfg.tokens * cfg.top_k))
+
+
+def _edge_rows(cfg, logits, k):
+    """Positions of every row of the most-used expert and of the three
+    least-used (touched) experts."""
+    r = O.route(logits, k)
+    cnt, off, _ = O.permute(r.ids, cfg.num_experts)
+    used = np.nonzero(cnt)[0]
+    picks = [int(used[np.argmax(cnt[used])])] + [int(e) for e in used[np.argsort(cnt[used], kind="stable")[:3]]]
+    rows = np.concatenate([np.arange(off[e], off[e + 1]) for e in picks])
+    return rows, picks, cnt
 
 
 @pytest.mark.parametrize("out_f32", [True, False])
-def test_forward_prefill_1k_sampled(out_f32):
-    inp = make_inputs("prefill_1k")
+@pytest.mark.parametrize("name", ["prefill_1k", "prefill_16k"])
+def test_forward_prefill_every_token(name, out_f32):
+    inp = make_inputs(name)
     cfg = inp.config
-    L = _layer(cfg, max_tokens=1024, out_f32=out_f32)
+    L = _layer(cfg, max_tokens=1024 if cfg.num_experts == 128 else None, out_f32=out_f32)
     gpu = _forward(L, inp.logits, inp.x_bits, cfg.top_k)
-    tokens = np.array([0, 1, 257, 511, 777, 1023])
-    ref = O.moe_forward(inp.logits, inp.x_bits, inp.weights, cfg.top_k, tokens=tokens)
-    assert_layer_close(gpu[tokens], ref, bf16_out=not out_f32)
     assert np.all(np.isfinite(gpu))
-
-
-_PF16K_REF = {}
-
-
-@pytest.mark.parametrize("out_f32", [True, False])
-def test_forward_prefill_16k_sampled(out_f32):
-    inp = make_inputs("prefill_16k")
-    cfg = inp.config
-    L = _layer(cfg, out_f32=out_f32)
-    gpu = _forward(L, inp.logits, inp.x_bits, cfg.top_k)
-    tokens = np.array([0, 4097, 16383])
-    if "ref" not in _PF16K_REF:
-        _PF16K_REF["ref"] = O.moe_forward(inp.logits, inp.x_bits, inp.weights, cfg.top_k, tokens=tokens)
-    assert_layer_close(gpu[tokens], _PF16K_REF["ref"], bf16_out=not out_f32)
-    assert np.all(np.isfinite(gpu))
+    assert_layer_close(gpu, layer_reference(name), bf16_out=not out_f32)
+    if out_f32:
+        rows, picks, cnt = _edge_rows(cfg, inp.logits, cfg.top_k)
+        assert cnt[picks[0]] > 128 and cnt[picks[0]] % 128 != 0   # several m-tiles and a partial last one
+        check_rows(L, inp, rows)
 
 
 @pytest.mark.parametrize("T,path", [(1, P.PATH_DECODE), (1, P.PATH_PREFILL), (37, P.PATH_PREFILL),
@@ -301,7 +362,7 @@ def test_forward_ragged_and_degenerate(T, path):
 
 @pytest.mark.parametrize("path", [P.PATH_DECODE, P.PATH_PREFILL])
 def test_all_tokens_to_one_expert(path):
-    T = 16 if path == P.PATH_DECODE else 300   # 300 rows > one 256-row m-tile
+    T = 16 if path == P.PATH_DECODE else 300   # 300 rows of one expert: three 128-row m-tiles, the last partial
     cfg = CONFIGS["tiny"].with_tokens(T)
     inp = make_inputs(cfg)
     logits = inp.logits.copy()
@@ -370,12 +431,13 @@ def test_errors_are_reported():
     L.close()
 
 
-def test_bounded_wait_reports_timeout():
+@pytest.mark.parametrize("path", [P.PATH_PREFILL, P.PATH_DECODE])
+def test_bounded_wait_reports_timeout(path):
     cfg = CONFIGS["tiny"]
     inp = make_inputs(cfg)
     L = P.MoELayer(cfg.num_experts, cfg.hidden, cfg.inter, 64, cfg.top_k)
     P.upload_layer(L, make_layer_weights(cfg), DEV)
-    L.nvfp4_moe_set_path(P.PATH_PREFILL)
+    L.nvfp4_moe_set_path(path)
     L.nvfp4_moe_debug_set_fault(1)
     x = _dev(inp.x_bits.view(np.int16)).view(torch.bfloat16)
     out = torch.empty((cfg.tokens, cfg.hidden), dtype=torch.bfloat16, device=DEV)
@@ -384,6 +446,6 @@ def test_bounded_wait_reports_timeout():
     assert st == P.STATUS_CODE["NVFP4_MOE_ERR_TIMEOUT"]
     # the context is still usable and the next forward is correct
     L.nvfp4_moe_debug_set_fault(0)
-    gpu = _forward(L, inp.logits, inp.x_bits, cfg.top_k, P.PATH_PREFILL)
+    gpu = _forward(L, inp.logits, inp.x_bits, cfg.top_k, path)
     assert_layer_close(gpu, O.moe_forward(inp.logits, inp.x_bits, inp.weights, cfg.top_k))
     L.close()

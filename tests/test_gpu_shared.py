@@ -14,7 +14,7 @@ import torch
 import nvfp4_weight_only_w4a16_gb300 as P
 from oracle import nvfp4_moe_oracle as O
 from synth import CONFIGS, LayerConfig, make_inputs, make_layer_weights
-from tests.test_gpu_parity import DEV, _dev, _forward, assert_layer_close
+from tests.test_gpu_parity import check_rows, DEV, _dev, _forward, assert_layer_close
 
 pytestmark = pytest.mark.gpu
 
@@ -94,16 +94,7 @@ def test_intermediates_shared_tiny():
     _forward(L, inp.logits, inp.x_bits, cfg.top_k, P.PATH_DECODE)
     T, k, E = cfg.tokens, cfg.top_k, cfg.num_experts
     K = k + 1
-    hid, y = L.nvfp4_moe_debug_intermediates(T * K)
-    y = y.cpu().numpy().astype(np.float64)
-    r = O.route(inp.logits, k)
-    ids = np.concatenate([r.ids, np.full((T, 1), E, np.int32)], axis=1)
-    _, _, perm = O.permute(ids, E + 1)
-    x = O.bf16_bits_to_f64(inp.x_bits)
-    for p in range(T * K):
-        t, j = divmod(int(perm[p]), K)
-        y_ref = O.expert_ffn(inp.weights, int(ids[t, j]), x[t:t + 1])[0]
-        assert np.abs(y[p] - y_ref).max() <= 1e-2 * np.sqrt(np.mean(y_ref ** 2))
+    check_rows(L, inp, range(T * K))
 
 
 def test_forward_shared_mtp_full_size():

@@ -26,8 +26,12 @@ checks built on that, element by element, per routed row:
 * y: the down projection of the admissible h^ (from the GPU's own h), within
   the FP32 summation bound.
 The layer output is checked element-wise at the W4A16 bounds (max|err| <=
-2e-2 RMS plus the BF16 output rounding, mean relative error <= 5e-3), with
-the norm ratio and cosine checks.
+2e-2 RMS plus the BF16 output rounding, mean relative error <= 5e-3) on the
+error beyond a flip allowance: per element, the spread of every layer value
+the admissible decisions can reach (the intervals above carried through the
+combine).  The allowance is not small: with these input scales about 0.25% of
+the x elements sit within D of a midpoint, and one flip moves a whole token's
+expert output.
 """
 import numpy as np
 import pytest
@@ -41,124 +45,8 @@ from tests.test_gpu_parity import DEV, _dev, _layer, _forward, assert_layer_clos
 
 pytestmark = pytest.mark.gpu
 
-D = 4 * 2.0 ** -24          # relative error of the kernels' FP32 quantiser quotients
-U24 = 2.0 ** -24            # FP32 unit roundoff
-
-
-def _q_e2m1(v):
-    """Signed E2M1 quantisation of float64 values (monotone non-decreasing)."""
-    return O.decode_e2m1(O.encode_e2m1(v))
-
-
-def _widen(v, rel):
-    return v - rel * np.abs(v), v + rel * np.abs(v)
-
-
-def _bf16(v):
-    """float64 -> nearest BF16 value (via FP32, as the kernels hold h), float64."""
-    f = np.asarray(v, dtype=np.float64).astype(np.float32)
-    b = f.view(np.uint32).astype(np.uint64)
-    b = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint32) << 16
-    return b.astype(np.uint32).view(np.float32).astype(np.float64)
-
-
-def _scale_candidates(lo, hi, is_):
-    """E4M3 scale values the kernel may pick for blocks whose inputs lie in
-    [lo, hi] element-wise ([nb][16] each): the RNE of every amax in range,
-    widened by D.  Returns a list (per block) of float64 scale values."""
-    mlo = np.where((lo <= 0) & (hi >= 0), 0.0, np.minimum(np.abs(lo), np.abs(hi))).max(axis=-1)
-    mhi = np.maximum(np.abs(lo), np.abs(hi)).max(axis=-1)
-    c0 = O.encode_e4m3(mlo / (6.0 * is_) * (1 - D)).astype(np.int64)
-    c1 = O.encode_e4m3(mhi / (6.0 * is_) * (1 + D)).astype(np.int64)
-    return [O.decode_e4m3(np.arange(a, b + 1)) for a, b in zip(c0, c1)]
-
-
-def _code_range(lo, hi, sv, is_):
-    """Admissible code*scale values (min, max) per element for scale sv."""
-    if sv == 0:
-        z = np.zeros_like(lo)
-        return z, z
-    a, _ = _widen(lo / (sv * is_), D)
-    _, b = _widen(hi / (sv * is_), D)
-    return _q_e2m1(a) * sv, _q_e2m1(b) * sv
-
-
-def quant_box(lo, hi, is_):
-    """Element-wise bounds [vmin, vmax] (code * scale, without is) of every
-    quantisation the kernel may produce for inputs in [lo, hi] ([..][K])."""
-    shp = lo.shape
-    lo = lo.reshape(-1, 16)
-    hi = hi.reshape(-1, 16)
-    vmin = np.empty_like(lo)
-    vmax = np.empty_like(lo)
-    for i, cands in enumerate(_scale_candidates(lo, hi, is_)):
-        mins, maxs = zip(*(_code_range(lo[i], hi[i], sv, is_) for sv in cands))
-        vmin[i] = np.min(mins, axis=0)
-        vmax[i] = np.max(maxs, axis=0)
-    return vmin.reshape(shp), vmax.reshape(shp)
-
-
-def assert_valid_quantisation(V, lo, hi, is_):
-    """Every 16-block of V (code * scale, float64) is the quantisation, with
-    one admissible scale, of inputs inside [lo, hi]."""
-    V = V.reshape(-1, 16)
-    lo = lo.reshape(-1, 16)
-    hi = hi.reshape(-1, 16)
-    grid = O.decode_e2m1(np.arange(16))
-    for i, cands in enumerate(_scale_candidates(lo, hi, is_)):
-        ok = False
-        for sv in cands:
-            cmin, cmax = _code_range(lo[i], hi[i], sv, is_)
-            on_grid = np.all(np.isin(V[i] / sv, grid)) if sv > 0 else np.all(V[i] == 0)
-            if on_grid and np.all(V[i] >= cmin) and np.all(V[i] <= cmax):
-                ok = True
-                break
-        assert ok, (i, V[i], lo[i], hi[i], cands)
-
-
-def _silu_range(gl, gh):
-    zs = -1.2784645427610738   # the minimum of silu
-    a, b = O.silu(gl), O.silu(gh)
-    lo = np.where((gl <= zs) & (zs <= gh), O.silu(np.float64(zs)), np.minimum(a, b))
-    return lo, np.maximum(a, b)
-
-
-def _mul_range(a1, a2, b1, b2):
-    p = np.stack([a1 * b1, a1 * b2, a2 * b1, a2 * b2])
-    return p.min(axis=0), p.max(axis=0)
-
-
-def _mats(w, e):
-    I = w.w13_q.shape[1] // 2
-    return (O.dequant(w.w13_q[e, :I], w.w13_s[e, :I]), O.dequant(w.w13_q[e, I:], w.w13_s[e, I:]),
-            O.dequant(w.w2_q[e], w.w2_s[e]), w.gscale[e].astype(np.float64))
-
-
-def _dot_box(W, vmin, vmax, scale, K):
-    """scale * W v over v in [vmin, vmax], widened by the FP32 accumulation and
-    the FP32 products with the tensor scale."""
-    mid, rad = (vmin + vmax) / 2, (vmax - vmin) / 2
-    absw = np.abs(W)
-    c = scale * (W @ mid)
-    r = scale * (absw @ rad) + scale * 4 * (K + 2) * U24 * (absw @ np.maximum(np.abs(vmin), np.abs(vmax)))
-    r = r + 3 * U24 * np.abs(c)
-    return c - r, c + r
-
-
-def hidden_bounds(mats, e, x_row, iscale):
-    """BF16 h interval [lo, hi] of one routed row (expert e with its
-    dequantised matrices, token row x)."""
-    wg, wu, _, gs = mats
-    is0 = float(np.float32(iscale[e, 0]))
-    H = x_row.shape[-1]
-    xmin, xmax = quant_box(x_row, x_row, is0)
-    gl, gh = _dot_box(wg, xmin, xmax, gs[0] * is0, H)
-    ul, uh = _dot_box(wu, xmin, xmax, gs[1] * is0, H)
-    sl, sh = _silu_range(gl, gh)
-    hl, hh = _mul_range(sl, sh, ul, uh)
-    hl, _ = _widen(hl, 8 * U24)
-    _, hh = _widen(hh, 8 * U24)
-    return _bf16(hl), _bf16(hh)
+from tests.intervals import (D, U24, quant_box, assert_valid_quantisation, _mats, _dot_box,
+                             hidden_bounds, w4a4_layer_allowance, assert_w4a4_layer)
 
 
 def _check_rows(L, inp, iscale, path, rows_to_check):
@@ -195,9 +83,22 @@ def _check_rows(L, inp, iscale, path, rows_to_check):
         assert bad.size == 0, (p, bad[:8], y[n][bad[:8]], yl[bad[:8]], yh[bad[:8]])
 
 
-def _check_layer(gpu, ref):
-    assert np.all(np.isfinite(gpu))
-    assert_layer_close(gpu, ref)
+def check_w4a4_layer(gpu, inp, iscale, tokens=None, logits=None, scoring=None):
+    """The layer against the oracle, element-wise, beyond the flip allowance
+    (every output value the kernels' admissible quantiser decisions can reach)."""
+    cfg = inp.config
+    tok = np.arange(cfg.tokens) if tokens is None else np.asarray(tokens)
+    lg = inp.logits if logits is None else logits
+    ref = O.moe_forward_w4a4(lg, inp.x_bits, inp.weights, cfg.top_k, iscale, tokens=tok, num_shared=cfg.shared,
+                             scoring=scoring)
+    r = O.route(lg[tok], cfg.top_k) if scoring is None else O.route_scored(lg[tok], cfg.top_k, **scoring)
+    ids, wts = r.ids, r.weights
+    if cfg.shared:
+        ids = np.concatenate([ids, np.full((len(tok), 1), cfg.num_experts, np.int32)], axis=1)
+        wts = np.concatenate([wts, np.ones((len(tok), 1))], axis=1)
+    A = w4a4_layer_allowance(inp.weights, inp.x_bits, ids, wts, iscale, cfg.num_experts, tok)
+    assert_w4a4_layer(gpu, ref, A)
+    return ref
 
 
 @pytest.mark.parametrize("path", [P.PATH_DECODE, P.PATH_PREFILL])
@@ -212,8 +113,7 @@ def test_w4a4_tiny(path):
         _check_rows(L, inp, iscale, path, range(cfg.tokens * cfg.top_k))
     finally:
         L.nvfp4_moe_set_act_quant(None)
-    ref = O.moe_forward_w4a4(inp.logits, inp.x_bits, inp.weights, cfg.top_k, iscale)
-    _check_layer(gpu, ref)
+    check_w4a4_layer(gpu, inp, iscale)
     # W4A4 is not W4A16: the two differ by the activation quantisation
     a16 = O.moe_forward(inp.logits, inp.x_bits, inp.weights, cfg.top_k)
     assert np.linalg.norm(gpu - a16) / np.linalg.norm(a16) > 1e-2
@@ -241,8 +141,7 @@ def test_w4a4_full_size(name, path):
         tok = list(range(cfg.tokens))
     else:
         tok = sorted({0, 1, 2, cfg.tokens // 2 - 1, cfg.tokens - 1})
-    ref = O.moe_forward_w4a4(inp.logits, inp.x_bits, inp.weights, cfg.top_k, iscale, tokens=tok)
-    _check_layer(gpu[tok], ref)
+    check_w4a4_layer(gpu[tok], inp, iscale, tokens=tok)
 
 
 def test_w4a4_shared_expert_stays_w4a16():
@@ -255,8 +154,7 @@ def test_w4a4_shared_expert_stays_w4a16():
     try:
         for path in (P.PATH_DECODE, P.PATH_PREFILL):
             gpu = _forward(L, inp.logits, inp.x_bits, cfg.top_k, path)
-            ref = O.moe_forward_w4a4(inp.logits, inp.x_bits, inp.weights, cfg.top_k, iscale, num_shared=1)
-            _check_layer(gpu, ref)
+            check_w4a4_layer(gpu, inp, iscale)
     finally:
         L.nvfp4_moe_set_act_quant(None)
 

@@ -1,6 +1,6 @@
 """The W4A4 GPU tests' interval checks, exercised on the CPU.
 
-The checks in tests/test_gpu_w4a4.py accept a kernel's quantisation where it
+The checks in tests/intervals.py (used by tests/test_gpu_w4a4.py) accept a kernel's quantisation where it
 equals the oracle's, or where it is the neighbour and the exact quotient lies
 within D = 4 * 2^-24 (relative) of a rounding midpoint.  Here: the oracle's
 own result passes; an FP32 evaluation in the kernels' operation order (the
@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from tests.test_gpu_w4a4 import assert_valid_quantisation, quant_box, D
+from tests.intervals import assert_valid_quantisation, quant_box, D
 
 
 def _fp32_order(v, input_scale):
@@ -90,3 +90,42 @@ def test_input_intervals_widen_the_admissible_set():
     vmin, vmax = quant_box(lo, hi, is_)
     assert vmin[1] == 2.0 and vmax[1] == 3.0
     assert D < 1e-6
+
+
+def _layer_fp32_order(inp, iscale, monkeypatch):
+    """The oracle's W4A4 layer with its quantiser evaluated in the kernels'
+    FP32 operation order (a stand-in for a correct GPU result)."""
+    import oracle.nvfp4_moe_oracle as OM
+    monkeypatch.setattr(OM, "quantize_act_nvfp4",
+                        lambda v, i: (_fp32_order(np.asarray(v, np.float32).reshape(-1, np.asarray(v).shape[-1]), i)
+                                      .reshape(np.asarray(v).shape), None))
+    cfg = inp.config
+    out = O.moe_forward_w4a4(inp.logits, inp.x_bits, inp.weights, cfg.top_k, iscale, num_shared=cfg.shared)
+    monkeypatch.undo()
+    return out
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_shared"])
+def test_layer_allowance_admits_fp32_order_and_rejects_a_wrong_scale(name, monkeypatch):
+    from synth import make_inputs, make_input_scales
+    from tests.intervals import w4a4_layer_allowance, assert_w4a4_layer
+    inp = make_inputs(name)
+    cfg = inp.config
+    iscale = make_input_scales(cfg)
+    ref = O.moe_forward_w4a4(inp.logits, inp.x_bits, inp.weights, cfg.top_k, iscale, num_shared=cfg.shared)
+    r = O.route(inp.logits, cfg.top_k)
+    ids, wts = r.ids, r.weights
+    if cfg.shared:
+        ids = np.concatenate([ids, np.full((cfg.tokens, 1), cfg.num_experts, np.int32)], axis=1)
+        wts = np.concatenate([wts, np.ones((cfg.tokens, 1))], axis=1)
+    A = w4a4_layer_allowance(inp.weights, inp.x_bits, ids, wts, iscale, cfg.num_experts, np.arange(cfg.tokens))
+    got = _layer_fp32_order(inp, iscale, monkeypatch)
+    assert np.abs(got - ref).max() > 1e-2 * np.sqrt(np.mean(ref ** 2))   # the flips are really there
+    assert_w4a4_layer(got, ref, A)
+    # one expert's x input scale off by a factor 1.37 (a power of two would
+    # only move every block scale by that power: the values stay the same)
+    bad_scale = iscale.copy()
+    bad_scale[int(r.ids[0, 0]), 0] *= np.float32(1.37)
+    wrong = O.moe_forward_w4a4(inp.logits, inp.x_bits, inp.weights, cfg.top_k, bad_scale, num_shared=cfg.shared)
+    with pytest.raises(AssertionError):
+        assert_w4a4_layer(wrong, ref, A)
