@@ -47,9 +47,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(LIBDIR, exist_ok=True)
     nvcc = _nvcc()
 
+    # NVFP4_MOE_NVCC_DEFINES="NAME=VALUE ...": compile-time tuning constants (e.g. the
+    # prefill rings' NVFP4_MOE_PF_STAGES_A/_B/_RAW); none by default
+    defines = ["-D" + d for d in os.environ.get("NVFP4_MOE_NVCC_DEFINES", "").split()]
+
     def compile_one(src):
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [nvcc, *FLAGS, *ARCH, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc, *FLAGS, *defines, *ARCH, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -32,8 +32,8 @@
 //    own power-of-two scale (the chunk's largest magnitude in [2^13, 2^14):
 //    exact for every value within 2^31 of it that has at most 11 significant
 //    bits), stored next to the row; each chunk's partial sums are multiplied
-//    back by the scale in FP32.  x is converted once per CTA into shared
-//    memory (few tokens) or once per chunk by one CTA into global memory; the
+//    back by the scale in FP32.  x is converted once per chunk, by one CTA,
+//    into global memory, and each stage carries its chunks' T token rows; the
 //    gate/up epilogue of an item produces one whole chunk of h (its 64
 //    features), so it writes h in that form: FP16, 11 significant bits;
 //  * gate/up columns are the step's tokens (every token through every touched
@@ -54,10 +54,14 @@
 namespace nvfp4moe {
 
 namespace dstr {
-constexpr int kConsumers = 8;                     // consumer warps: one per 16-row group of a 128-row block
-constexpr int kThreads = (kConsumers + 1) * 32;   // + one producer warp
+constexpr int kGroupWarps = 8;                    // consumer warps of a group: one per 16-row group of a block
+constexpr int kGroups = 2;                        // consumer groups, taking alternate stages
+constexpr int kConsumers = kGroups * kGroupWarps;
+constexpr int kThreads = (kConsumers + 2) * 32;   // + one producer warp + one signal warp
 constexpr int kProducer = kConsumers;             // the producer's warp index
-constexpr int kCPS = 4;                           // 64-wide K chunks per stage
+constexpr int kSignaller = kConsumers + 1;        // the signal warp's index
+constexpr int kSig = 8;                           // depth of each group's completion queue
+constexpr int kCPS = 4;                           // 64-wide K chunks per stage (at most)
 constexpr int kCodes = kCPS * 4096;               // 128 rows x 4 chunks of E2M1 codes
 constexpr int kScales = kCPS * 512;               // their E4M3 scales
 constexpr int kAct = kCodes + kScales;            // activation rows of the stage's chunks
@@ -66,7 +70,7 @@ constexpr int kMaxSlots = 17;                     // slots per token: top_k <= 1
 constexpr int kMaxR = kDecodeMaxTokens * kMaxSlots;
 constexpr int kMaxE = 288;                        // routed + shared experts (9 per lane in the scan)
 constexpr int kMaxStages = 12;
-constexpr int kXsPairs = 16;                      // (token, chunk) pairs per consumer warp in the shared x copy
+constexpr int kXChunks = 8;                       // chunks of x one CTA converts with its loads issued up front
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 }  // namespace dstr
 
@@ -81,11 +85,16 @@ struct StreamSmem {
   int tch_r0[dstr::kMaxE];
   int tch_m[dstr::kMaxE];
   unsigned tch_mask[dstr::kMaxE];  // tokens routed to the touched expert
-  float cmax[8][16];               // gate/up epilogue: per 16-row group, per column, max |h|
+  float cmax[2][8][16];             // gate/up epilogue, per group: per 16-row group, per column, max |h|
   int meta[dstr::kMaxStages][4];   // item, stage within the item, chunks in the stage
+  int sig[2][dstr::kSig];          // per group: completed items for the signal warp (-1: no more)
   int U, nan, last_cta;
   alignas(8) uint64_t full[dstr::kMaxStages];
   alignas(8) uint64_t empty[dstr::kMaxStages];
+  alignas(8) uint64_t sig_full[2][dstr::kSig];   // the group's warps are done with the item
+  alignas(8) uint64_t sig_empty[2][dstr::kSig];  // the signal warp has published it
+  alignas(8) uint64_t red_full[2][8];            // [item parity][16-row group]: the helper's half is in
+  alignas(8) uint64_t red_empty[2][8];           // the owner has taken it
 };
 
 struct StreamArgs {
@@ -106,20 +115,21 @@ struct StreamArgs {
   int32_t* perm;
   int32_t* inv;
   uint8_t* act_h;     // [I/64][rdec][kRow]: h rows per chunk, FP16 with their scale
-  uint8_t* act_x;     // [H/64][8 NG][kRow]: x rows per chunk (when not kept in shared memory)
+  uint8_t* act_x;     // [H/64][T][kRow]: x rows per chunk
   int rdec;           // rows of act_h per chunk
   float* y;           // [R][H] expert outputs, position order
   int32_t* wctr;      // claimed items beyond the first gridDim.x
-  int32_t* done_c;    // [maxU][I/64]: gate/up epilogue warps done per (touched expert, chunk of h)
-  int32_t* cmb;       // finished down epilogue warps per 128-wide output slice
+  int32_t* done_c;    // [maxU][I/64]: 1 once (touched expert, chunk of h) is written
+  int32_t* cmb;       // finished down items per 128-wide output slice
   int32_t* x_ready;   // tokens converted per chunk of x (act_x)
   int32_t* exit_cnt;
   DeviceStatus* st;
   DeviceStatus* st_sticky;
   int fault;          // 1: the producer issues nothing (tests the bounded waits)
   int stages, stage_bytes;
-  int xs;             // 1: x is converted into shared memory by every CTA
   int checks;         // 1: check table-derived indices (kFlagBounds; the access is skipped)
+  int pf_dist;        // stages ahead of the ring whose weights are prefetched into L2 (0: none)
+  int cps;            // 64-wide K chunks per stage (4, or fewer for small H and I: two or more stages per item)
   unsigned long long* trace;  // optional: [cta][16] phase stamps (see decode_stream_kernel)
 };
 
@@ -151,6 +161,9 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                    saddr(dst)),
                "l"(src), "r"(bytes), "r"(saddr(bar))
                : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ uint64_t gtime() {
   uint64_t t;
@@ -235,14 +248,19 @@ __device__ __forceinline__ void convert_chunk_row(uint32_t two_bf16, uint8_t* ds
 // touched-expert list with each expert's token mask.  CTA 0 also writes the
 // tables out.
 // ---------------------------------------------------------------------------
-__device__ void stream_route(const StreamArgs& a, StreamSmem& ss, unsigned long long* tr) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
-  const int T = a.T, k = a.k, E = a.E, Er = a.Er, topk = a.topk, R = T * k;
-  float val[2][8];
-  uint32_t key[2][8];
+// The logit loads of this warp's tokens (issued first thing, so their latency
+// overlaps everything else the kernel does before routing).
+__device__ __forceinline__ void stream_route_issue(const StreamArgs& a, float (&val)[2][8]) {
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
   for (int r = 0; r < 2; ++r)
-    if (warp + r * nw < T) warp_issue_logits(a.logits, a.logits_bf16, Er, warp + r * nw, val[r]);
+    if (warp + r * nw < a.T) warp_issue_logits(a.logits, a.logits_bf16, a.Er, warp + r * nw, val[r]);
+}
+
+__device__ void stream_route(const StreamArgs& a, StreamSmem& ss, float (&val)[2][8], unsigned long long* tr) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+  const int T = a.T, k = a.k, E = a.E, Er = a.Er, topk = a.topk, R = T * k;
+  uint32_t key[2][8];
   for (int i = tid; i <= E; i += blockDim.x) ss.off[i] = 0;
   if (tid == 0) ss.nan = 0;
   __syncthreads();
@@ -392,28 +410,79 @@ __device__ __forceinline__ void mma_tile(const AFrag& f, const uint8_t* tile, fl
   }
 }
 
-// One stage's work of consumer warp sb: its 16-row group of NC chunks (all
-// fragments loaded first, so the NC chains overlap).  xtile: the first
-// chunk's activation rows when x sits in shared memory (rows `xpitch` chunks
-// apart), else null (the stage carries them, rows_pad rows per chunk).
+// One stage's raw operands for consumer warp sb, in registers: its 16-row
+// group's codes and scales of each of the NC chunks, and each chunk's
+// activation fragments (B) with their column scales.  Once they are loaded
+// the stage's shared memory can be refilled while the warp computes.
 template <int NG, int NC>
-__device__ __forceinline__ void consume_stage(const uint8_t* stg, const uint8_t* xtile, size_t xpitch, int sb,
-                                              float (&acc)[NG][4], int lane) {
-  AFrag f[NC];
+struct StageRegs {
+  uint4 raw[NC];
+  uint16_t sc[NC];
+  uint4 b[NC][NG][2];
+  float cs[NC][NG][2];
+};
+// The stage carries each chunk's activation rows, `pitch` bytes apart (T rows
+// of kRow bytes); reads past a chunk's rows land in the next chunk's rows or
+// the ring's tail pad -- MMA columns that no epilogue keeps.
+template <int NG, int NC>
+__device__ __forceinline__ void load_stage(const uint8_t* stg, int pitch, int sb, int lane, StageRegs<NG, NC>& r) {
+  const int g = lane >> 2, q = lane & 3;
 #pragma unroll
-  for (int cs = 0; cs < NC; ++cs) load_a(stg + cs * 4096 + sb * 512, stg + dstr::kCodes + cs * 512 + sb * 64, lane, f[cs]);
+  for (int c = 0; c < NC; ++c) {
+    r.raw[c] = *reinterpret_cast<const uint4*>(stg + c * 4096 + sb * 512 + lane * 16);
+    r.sc[c] = *reinterpret_cast<const uint16_t*>(stg + dstr::kCodes + c * 512 + sb * 64 + lane * 2);
+    const uint8_t* tile = stg + dstr::kAct + c * pitch;
 #pragma unroll
-  for (int cs = 0; cs < NC; ++cs)
-    mma_tile<NG>(f[cs], xtile ? xtile + cs * xpitch : stg + dstr::kAct + cs * (8 * NG) * dstr::kRow, acc, lane);
+    for (int gi = 0; gi < NG; ++gi) {
+      const uint8_t* pb = tile + (8 * gi + g) * dstr::kRow + q * 32;
+      r.b[c][gi][0] = *reinterpret_cast<const uint4*>(pb);
+      r.b[c][gi][1] = *reinterpret_cast<const uint4*>(pb + 16);
+      const int c0 = 8 * gi + 2 * q;
+      r.cs[c][gi][0] = *reinterpret_cast<const float*>(tile + c0 * dstr::kRow + 128);
+      r.cs[c][gi][1] = *reinterpret_cast<const float*>(tile + (c0 + 1) * dstr::kRow + 128);
+    }
+  }
+}
+template <int NG, int NC>
+__device__ __forceinline__ void compute_stage(const StageRegs<NG, NC>& r, float (&acc)[NG][4]) {
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    AFrag f;
+    const uint32_t s2 = e4m3x2_to_f16x2(r.sc[c]);
+    const uint32_t s0 = dup_lo(s2), s1 = dup_hi(s2);
+    e2m1x8_to_f16x2x4(r.raw[c].x, f.x);
+    e2m1x8_to_f16x2x4(r.raw[c].y, f.y);
+    e2m1x8_to_f16x2x4(r.raw[c].z, f.z);
+    e2m1x8_to_f16x2x4(r.raw[c].w, f.w);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      f.x[t] = hmul2_u32(f.x[t], s0);
+      f.y[t] = hmul2_u32(f.y[t], s0);
+      f.z[t] = hmul2_u32(f.z[t], s1);
+      f.w[t] = hmul2_u32(f.w[t], s1);
+    }
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
+      const uint4 b0 = r.b[c][gi][0], b1 = r.b[c][gi][1];
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_f16_16816(d, f.x[0], f.z[0], f.x[1], f.z[1], b0.x, b0.y);
+      mma_f16_16816(d, f.x[2], f.z[2], f.x[3], f.z[3], b0.z, b0.w);
+      mma_f16_16816(d, f.y[0], f.w[0], f.y[1], f.w[1], b1.x, b1.y);
+      mma_f16_16816(d, f.y[2], f.w[2], f.y[3], f.w[3], b1.z, b1.w);
+      acc[gi][0] = fmaf(d[0], r.cs[c][gi][0], acc[gi][0]);
+      acc[gi][1] = fmaf(d[1], r.cs[c][gi][1], acc[gi][1]);
+      acc[gi][2] = fmaf(d[2], r.cs[c][gi][0], acc[gi][2]);
+      acc[gi][3] = fmaf(d[3], r.cs[c][gi][1], acc[gi][3]);
+    }
+  }
 }
 
 // Gate/up epilogue of item (u, b) on the 8 consumer warps (16-row group sb):
 // h for the 64 features of chunk b, kept for the routed tokens, as the FP16
-// chunk rows with their scale in act_h; then each warp counts itself in for
-// (u, chunk b).
+// chunk rows with their scale in act_h (published by the signal warp).
 template <int NG>
-__device__ void epilogue_gateup(const StreamArgs& a, StreamSmem& ss, int u, int b, int sb, const float (&acc)[NG][4],
-                                int lane) {
+__device__ void epilogue_gateup(const StreamArgs& a, StreamSmem& ss, int u, int b, int sb, int grp,
+                                const float (&acc)[NG][4], int lane) {
   const int e = ss.tch_e[u], row0 = ss.tch_r0[u];
   const unsigned mask = ss.tch_mask[u];
   const int g = lane >> 2, q = lane & 3;
@@ -432,9 +501,9 @@ __device__ void epilogue_gateup(const StreamArgs& a, StreamSmem& ss, int u, int 
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-      if (g == 0) ss.cmax[sb][t] = m;
+      if (g == 0) ss.cmax[grp][sb][t] = m;
     }
-  named_sync(1, dstr::kConsumers * 32);
+  named_sync(1 + grp, dstr::kGroupWarps * 32);
 #pragma unroll
   for (int gi = 0; gi < NG; ++gi)
 #pragma unroll
@@ -443,7 +512,7 @@ __device__ void epilogue_gateup(const StreamArgs& a, StreamSmem& ss, int u, int 
       if (t >= a.T || !((mask >> t) & 1u)) continue;
       float m = 0.f;
 #pragma unroll
-      for (int s = 0; s < 8; ++s) m = fmaxf(m, ss.cmax[s][t]);
+      for (int s = 0; s < 8; ++s) m = fmaxf(m, ss.cmax[grp][s][t]);
       const int p = max(-126, min(126, prescale_exp(m)));
       const int pos = row0 + __popc(mask & ((1u << t) - 1u));
       if (a.checks && (pos < 0 || pos >= a.T * a.k)) {
@@ -457,15 +526,10 @@ __device__ void epilogue_gateup(const StreamArgs& a, StreamSmem& ss, int u, int 
     }
   // the rows are read by other CTAs' bulk copies (the async proxy)
   asm volatile("fence.proxy.async.global;" ::: "memory");
-  __syncwarp();
-  if (lane == 0) {
-    __threadfence();
-    atomicAdd(a.done_c + (size_t)u * (a.I / 64) + b, 1);
-  }
 }
 
 // Down epilogue of item (u, b): y rows 128 b + 16 sb + g (+8) for the
-// expert's routed rows; each warp counts itself in for output slice b.
+// expert's routed rows (counted in for output slice b by the signal warp).
 template <int NG>
 __device__ void epilogue_down(const StreamArgs& a, const StreamSmem& ss, int u, int b, int sb,
                               const float (&acc)[NG][4], int lane) {
@@ -484,19 +548,14 @@ __device__ void epilogue_down(const StreamArgs& a, const StreamSmem& ss, int u, 
         yr[d0 + 8] = acc[gi][2 + c] * gsd;
       }
     }
-  __syncwarp();
-  if (lane == 0) {
-    __threadfence();
-    atomicAdd(a.cmb + b, 1);
-  }
 }
 
 // The combine, spread over every consumer warp of the grid: task (128-wide
 // slice b, token t) waits until slice b is complete for every touched expert
-// (8 U down epilogue warps), then out[t][slice] = sum_j w[t][j] *
+// (U down items), then out[t][slice] = sum_j w[t][j] *
 // y[pos(t, j)][slice] in slot order j = 0..k-1 (lane l: features 4l..4l+3).
 __device__ void combine_tasks(const StreamArgs& a, const StreamSmem& ss, int wg, int W, int lane) {
-  const int nsl = a.H / 128, target = dstr::kConsumers * ss.U;
+  const int nsl = a.H / 128, target = ss.U;
   for (int task = wg; task < nsl * a.T; task += W) {
     const int t = task / nsl, b = task - t * nsl;
     int ok = 1;
@@ -538,7 +597,7 @@ __device__ void combine_tasks(const StreamArgs& a, const StreamSmem& ss, int wg,
 }
 
 // ---------------------------------------------------------------------------
-// The kernel.  Shared memory: StreamSmem | x rows (xs mode) | ring
+// The kernel.  Shared memory: StreamSmem | pair sums | ring
 // [stages][stage_bytes].
 // ---------------------------------------------------------------------------
 template <int NG>
@@ -547,12 +606,12 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
   StreamSmem& ss = *reinterpret_cast<StreamSmem*>(smem);
   const size_t base = (sizeof(StreamSmem) + 127) & ~size_t(127);
   const int nchH = a.H / 64, nchI = a.I / 64;
-  const size_t xs_bytes = a.xs ? (size_t)nchH * a.T * dstr::kRow : 0;
-  uint8_t* xs = smem + base;
-  uint8_t* ring = smem + base + ((xs_bytes + 127) & ~size_t(127));
+  float* red = reinterpret_cast<float*>(smem + base);  // [2][8][32][4 NG]
+  uint8_t* ring = reinterpret_cast<uint8_t*>(red) + 2 * 8 * 32 * 4 * NG * sizeof(float);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = a.T, S = a.stages;
   constexpr int rows_pad = 8 * NG;
+  const int apitch = T * dstr::kRow;  // a stage's activation rows per chunk
   // trace (NVFP4_MOE_TRACE=1): [0] entry, [1] routed, [2] first stage issued, [3] first stage
   // consumed (warp 0), [4] last stage posted, [5] warp 0 done, [6] exit, [7] items, [8] producer ns
   // waiting for free stages, [9] producer ns waiting for h / x, [10] warp 0 ns waiting for full
@@ -560,42 +619,45 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
   // logits requested, [15] routing: experts chosen
   unsigned long long* tr = a.trace ? a.trace + (size_t)blockIdx.x * 16 : nullptr;
   if (tr && tid == 0) tr[0] = gtime();
+  float lval[2][8];
+  stream_route_issue(a, lval);
 
   // x words this warp converts (loads issued before routing so their latency overlaps it)
-  uint32_t xw[dstr::kXsPairs];
-  const int npairs = T * nchH;
-  if (!a.route_only && a.x && warp < dstr::kConsumers) {
-    if (a.xs) {
+  uint32_t xw[dstr::kXChunks];
+  if (!a.route_only && a.x && warp < T) {
 #pragma unroll
-      for (int i = 0; i < dstr::kXsPairs; ++i) {
-        const int p = warp + dstr::kConsumers * i;  // pair p: token p % T, chunk p / T
-        if (p < npairs)
-          xw[i] = __ldg(reinterpret_cast<const uint32_t*>(a.x + (size_t)(p % T) * a.H + 64 * (p / T)) + lane);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < dstr::kXsPairs; ++i) {
-        // this CTA's chunks of x: chunk blockIdx.x + (i / 2) * gridDim.x, token warp + 8 (i % 2)
-        const int c = blockIdx.x + (i >> 1) * gridDim.x, t = warp + dstr::kConsumers * (i & 1);
-        if (c < nchH && t < T) xw[i] = __ldg(reinterpret_cast<const uint32_t*>(a.x + (size_t)t * a.H + 64 * c) + lane);
-      }
+    for (int i = 0; i < dstr::kXChunks; ++i) {
+      // this CTA's chunks of x: chunk blockIdx.x + i * gridDim.x, token `warp`
+      const int c = blockIdx.x + i * gridDim.x;
+      if (c < nchH) xw[i] = __ldg(reinterpret_cast<const uint32_t*>(a.x + (size_t)warp * a.H + 64 * c) + lane);
     }
   }
   if (tid == 0 && !a.route_only) {
     for (int s = 0; s < S; ++s) {
       mb_init(&ss.full[s], 1);
-      mb_init(&ss.empty[s], dstr::kConsumers);
+      mb_init(&ss.empty[s], dstr::kGroupWarps);  // each stage goes to one group
     }
+    for (int g = 0; g < 2; ++g)
+      for (int q = 0; q < dstr::kSig; ++q) {
+        mb_init(&ss.sig_full[g][q], dstr::kGroupWarps);
+        mb_init(&ss.sig_empty[g][q], 1);
+      }
+    for (int p = 0; p < 2; ++p)
+      for (int q = 0; q < 8; ++q) {
+        mb_init(&ss.red_full[p][q], 1);
+        mb_init(&ss.red_empty[p][q], 1);
+      }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  stream_route(a, ss, tr);  // ends with __syncthreads: tables and barriers are ready
+  stream_route(a, ss, lval, tr);  // ends with __syncthreads: tables and barriers are ready
   if (a.route_only) return;
   if (tr && tid == 0) tr[1] = gtime();
 
   const int U = ss.U;
   const int gu_per = nchI, dn_per = a.H / 128;  // items per expert
   const int n_gu = U * gu_per, n_items = n_gu + U * dn_per;
-  const int nst_gu = (nchH + dstr::kCPS - 1) / dstr::kCPS, nst_dn = (nchI + dstr::kCPS - 1) / dstr::kCPS;
+  const int cps = a.cps;
+  const int nst_gu = (nchH + cps - 1) / cps, nst_dn = (nchI + cps - 1) / cps;  // both >= 2
 
   if (warp == dstr::kProducer) {
     // ---------------- producer ----------------
@@ -613,14 +675,19 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
     } else {
       int item = blockIdx.x;
       unsigned long long w_empty = 0, w_dep = 0, n_items_done = 0, n_dn = 0;
-      bool x_ok = a.xs != 0;  // every chunk of act_x converted (known once, then for good)
+      bool x_ok = false;      // every chunk of act_x converted (known once, then for good)
       int ready_u = -1;       // the last expert whose h is known complete
       while (!dead) {
-        if (item >= n_items) {  // no work left: a stage that tells the consumers to stop
+        if (item >= n_items) {  // no work left: a stage for each group that tells it to stop
           if (lane == 0) {
-            if (wait_phase(&ss.empty[slot], ph ^ 1u, a.st, 500)) {
+            for (int r = 0; r < 2; ++r) {
+              if (!wait_phase(&ss.empty[slot], ph ^ 1u, a.st, 500)) break;
               ss.meta[slot][0] = -1;
               mb_arrive(&ss.full[slot]);
+              if (++slot == S) {
+                slot = 0;
+                ph ^= 1u;
+              }
             }
             if (tr) {
               tr[4] = gtime();
@@ -650,53 +717,66 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
         const uint8_t* codes = eb + (gu ? a.nib13 : a.nib2) + (size_t)b * nch * 4096;
         const uint8_t* scl = eb + (gu ? a.sc13 : a.sc2) + (size_t)b * nch * 512;
         const int32_t* dep = a.done_c + (size_t)u * nchI;
-        // the item's inputs: a down item needs all of its expert's h (every gate/up epilogue warp of
-        // each chunk), a gate/up item every chunk of act_x; one parallel check, then never again
-        {
-          const uint64_t td0 = tr ? gtime() : 0;
-          if (!gu && ready_u != u) {
-            if (tr && n_dn == 0 && lane == 0) tr[13] = gtime();
-            if (warp_wait_all(dep, nchI, dstr::kConsumers, a.st, 600 + (unsigned)u)) ready_u = u;
-            else dead = true;
-          } else if (gu && !x_ok) {
-            if (warp_wait_all(a.x_ready, nchH, T, a.st, 700)) x_ok = true;
-            else dead = true;
-          }
-          // the inputs were written through the generic proxy; the copies read them through the async proxy
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-          if (tr && lane == 0) w_dep += gtime() - td0;
-        }
+        // the item's inputs: a down item needs all of its expert's h (every chunk), a gate/up
+        // item every chunk of act_x -- one parallel check, made once the first stage's weight
+        // copies (which need nothing) are on their way
+        bool need = gu ? !x_ok : ready_u != u;
         for (int s = 0; s < nst && !dead; ++s) {
           uint8_t* stg = ring + (size_t)slot * a.stage_bytes;
           uint64_t* full = &ss.full[slot];
-          const int c0 = dstr::kCPS * s, nc = min(dstr::kCPS, nch - c0);
+          const int c0 = cps * s, nc = min(cps, nch - c0);
           int ok = 1;
           if (lane == 0) {
             const uint64_t t0 = tr ? gtime() : 0;
             ok = wait_phase(&ss.empty[slot], ph ^ 1u, a.st, 501);
             const uint64_t t1 = tr ? gtime() : 0;
             w_empty += t1 - t0;
-            // activation rows of the stage's chunks (none when x is in shared memory)
-            const uint32_t act = !gu ? (uint32_t)(nc * m * dstr::kRow) : a.xs ? 0u : (uint32_t)(nc * rows_pad * dstr::kRow);
             (void)t1;
             if (tr && it == 0) tr[2] = gtime();
             if (ok) {
               ss.meta[slot][0] = item;
               ss.meta[slot][1] = s;
               ss.meta[slot][2] = nc;
-              mb_expect(full, (uint32_t)nc * (4096u + 512u) + act);
+              // the stage's activation rows: nc chunks x (T tokens or the expert's m rows)
+              mb_expect(full, (uint32_t)nc * (4096u + 512u) + (uint32_t)(nc * (gu ? T : m) * dstr::kRow));
               bulk_g2s(stg, codes + (size_t)c0 * 4096, (uint32_t)nc * 4096u, full);
               bulk_g2s(stg + dstr::kCodes, scl + (size_t)c0 * 512, (uint32_t)nc * 512u, full);
-              if (act && gu) {
-                bulk_g2s(stg + dstr::kAct, a.act_x + (size_t)c0 * rows_pad * dstr::kRow, act, full);
-              } else if (act) {
-                for (int c = 0; c < nc; ++c)
-                  bulk_g2s(stg + dstr::kAct + c * rows_pad * dstr::kRow,
-                           a.act_h + ((size_t)(c0 + c) * a.rdec + row0) * dstr::kRow, (uint32_t)(m * dstr::kRow), full);
+              // the weights a ring's depth further on into L2: more bytes in flight than the ring holds
+              const int pf = s + a.pf_dist;
+              if (a.pf_dist > 0 && pf < nst) {
+                const int p0 = cps * pf, pn = min(cps, nch - p0);
+                prefetch_l2(codes + (size_t)p0 * 4096, (uint32_t)pn * 4096u);
+                prefetch_l2(scl + (size_t)p0 * 512, (uint32_t)pn * 512u);
               }
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
+          bool late = false;  // the inputs never became ready (the run is aborted)
+          if (ok && need) {  // the readiness check, by the whole warp
+            const uint64_t td0 = tr ? gtime() : 0;
+            if (!gu && tr && n_dn == 0 && lane == 0) tr[13] = td0;
+            late = !(gu ? warp_wait_all(a.x_ready, nchH, T, a.st, 700)
+                        : warp_wait_all(dep, nchI, 1, a.st, 600 + (unsigned)u));
+            if (!late) {
+              if (gu) x_ok = true;
+              else ready_u = u;
+            }
+            need = false;
+            // the inputs were written through the generic proxy; the copies read them through the async proxy
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            if (tr && lane == 0) w_dep += gtime() - td0;
+          }
+          // issued even when late: the rows are in the workspace either way, and the stage's
+          // transaction count must complete so that the drain below ends
+          if (ok && lane == 0) {
+            if (gu) {
+              bulk_g2s(stg + dstr::kAct, a.act_x + (size_t)c0 * apitch, (uint32_t)(nc * apitch), full);
+            } else {
+              for (int c = 0; c < nc; ++c)
+                bulk_g2s(stg + dstr::kAct + c * apitch, a.act_h + ((size_t)(c0 + c) * a.rdec + row0) * dstr::kRow,
+                         (uint32_t)(m * dstr::kRow), full);
+            }
+          }
           if (!ok) {
             dead = true;
           } else {
@@ -705,6 +785,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
               slot = 0;
               ph ^= 1u;
             }
+            dead = late;
           }
         }
         ++n_items_done;
@@ -722,50 +803,89 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
       }
       __syncwarp();
     }
-  } else {
-    // ---------------- consumers ----------------
-    const int sb = warp;
-    if (a.x) {  // this CTA's share of the x conversion
-      if (a.xs) {
+  } else if (warp == dstr::kSignaller) {
+    // ---------------- signal warp: publishes what the consumers completed ----------------
+    // The consumers' stores come before their arrivals on sig_full (release,
+    // CTA scope); this warp's fence then orders them before the count that
+    // other CTAs acquire, so no consumer ever waits for its own stores.  It
+    // serves both groups' queues, each in order, until both have ended.
+    uint32_t n[2] = {0, 0};
+    bool open[2] = {true, true};
+    uint64_t t0 = gtime();
+    while (open[0] || open[1]) {
+      bool any = false;
 #pragma unroll
-        for (int i = 0; i < dstr::kXsPairs; ++i) {
-          const int p = warp + dstr::kConsumers * i;
-          if (p < npairs) convert_chunk_row(xw[i], xs + ((size_t)(p / T) * T + p % T) * dstr::kRow, lane);
+      for (int g = 0; g < 2; ++g) {
+        if (!open[g]) continue;
+        const int q = (int)(n[g] % dstr::kSig);
+        if (!mb_try(&ss.sig_full[g][q], (n[g] / dstr::kSig) & 1u)) continue;
+        any = true;
+        const int v = ss.sig[g][q];
+        if (v < 0) {
+          open[g] = false;
+          continue;
         }
+        if (lane == 0) {
+          __threadfence();
+          if (v < n_gu) atomicAdd(a.done_c + (size_t)(v / gu_per) * nchI + (v % gu_per), 1);
+          else atomicAdd(a.cmb + (v - n_gu) % dn_per, 1);
+          mb_arrive(&ss.sig_empty[g][q]);
+        }
+        __syncwarp();
+        ++n[g];
+      }
+      if (any) {
+        t0 = gtime();
       } else {
-        bool any = false;
-#pragma unroll
-        for (int i = 0; i < dstr::kXsPairs; ++i) {
-          const int c = blockIdx.x + (i >> 1) * gridDim.x, t = warp + dstr::kConsumers * (i & 1);
-          if (c < nchH && t < T) {
-            convert_chunk_row(xw[i], a.act_x + ((size_t)c * rows_pad + t) * dstr::kRow, lane);
-            any = true;
-          }
+        if (is_aborted(a.st)) break;
+        if (gtime() - t0 > dstr::kTimeoutNs) {
+          if (lane == 0) report(a.st, kFlagTimeout, 320);
+          break;
         }
-        // (chunks beyond the ones loaded above: only when the grid is small)
-        for (int c = blockIdx.x + (dstr::kXsPairs / 2) * gridDim.x; c < nchH; c += gridDim.x)
-          for (int t = warp; t < T; t += dstr::kConsumers) {
-            const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(a.x + (size_t)t * a.H + 64 * c) + lane);
-            convert_chunk_row(w, a.act_x + ((size_t)c * rows_pad + t) * dstr::kRow, lane);
-            any = true;
-          }
-        if (any) {
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) {
-            __threadfence();
-            for (int c = blockIdx.x; c < nchH; c += gridDim.x)
-              for (int t = warp; t < T; t += dstr::kConsumers) atomicAdd(a.x_ready + c, 1);
-          }
-        }
+        __nanosleep(32);
       }
     }
-    named_sync(2, dstr::kConsumers * 32);  // the shared x rows are complete
+  } else {
+    // ---------------- consumers ----------------
+    // group grp takes the stages of even (0) or odd (1) global index; warp sb
+    // of a group takes 16-row group sb of each of its stages
+    const int grp = warp / dstr::kGroupWarps, sb = warp % dstr::kGroupWarps;
+    if (a.x && warp < T) {  // this CTA's share of the x conversion: token `warp` of its chunks
+#pragma unroll
+      for (int i = 0; i < dstr::kXChunks; ++i) {
+        const int c = blockIdx.x + i * gridDim.x;
+        if (c < nchH) convert_chunk_row(xw[i], a.act_x + ((size_t)c * T + warp) * dstr::kRow, lane);
+      }
+      // (chunks beyond the ones loaded above: only when the grid is small)
+      for (int c = blockIdx.x + dstr::kXChunks * gridDim.x; c < nchH; c += gridDim.x) {
+        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(a.x + (size_t)warp * a.H + 64 * c) + lane);
+        convert_chunk_row(w, a.act_x + ((size_t)c * T + warp) * dstr::kRow, lane);
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        for (int c = blockIdx.x; c < nchH; c += gridDim.x) atomicAdd(a.x_ready + c, 1);
+      }
+    }
 
     float acc[NG][4];
-    int slot = 0;
-    uint32_t ph = 0, it = 0;
+    int slot = grp;
+    uint32_t ph = 0, it = 0, nsig = 0, nitem = 0;
     unsigned long long w_full = 0, w_epi = 0;
+    // hands item v (or -1: the end) to the signal warp through the group's
+    // queue: warp 0 of the group fills the entry once the signal warp has
+    // freed it, then every warp of the group arrives
+    auto post = [&](int v) {
+      const int q = (int)(nsig % dstr::kSig);
+      if (sb == 0 && lane == 0) {
+        wait_phase(&ss.sig_empty[grp][q], ((nsig / dstr::kSig) & 1u) ^ 1u, a.st, 330);
+        ss.sig[grp][q] = v;
+      }
+      __syncwarp();
+      if (lane == 0) mb_arrive(&ss.sig_full[grp][q]);
+      ++nsig;
+    };
     for (;;) {
       const uint64_t tw0 = (tr && warp == 0) ? gtime() : 0;
       if (!wait_phase(&ss.full[slot], ph, a.st, 300)) break;
@@ -778,37 +898,71 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
       if (item < 0) break;
       const int s = ss.meta[slot][1], nc = ss.meta[slot][2];
       const bool gu = item < n_gu;
-      if (s == 0) {
+      if (s < 2) {  // this group's first stage of the item
 #pragma unroll
         for (int gi = 0; gi < NG; ++gi)
 #pragma unroll
           for (int z = 0; z < 4; ++z) acc[gi][z] = 0.f;
       }
       const uint8_t* stg = ring + (size_t)slot * a.stage_bytes;
-      const size_t xpitch = (size_t)T * dstr::kRow;
-      const uint8_t* xtile = (gu && a.xs) ? xs + (size_t)(dstr::kCPS * s) * xpitch : nullptr;
-      if (nc == dstr::kCPS) {
-        consume_stage<NG, dstr::kCPS>(stg, xtile, xpitch, sb, acc, lane);
-      } else {  // an item's last stage with two chunks (K/64 is even, not a multiple of 4)
-        consume_stage<NG, 2>(stg, xtile, xpitch, sb, acc, lane);
+      // operands into registers, the math, then the stage back to the producer
+      if (nc == 4) {
+        StageRegs<NG, 4> r;
+        load_stage<NG, 4>(stg, apitch, sb, lane, r);
+        compute_stage<NG, 4>(r, acc);
+      } else if (nc == 2) {
+        StageRegs<NG, 2> r;
+        load_stage<NG, 2>(stg, apitch, sb, lane, r);
+        compute_stage<NG, 2>(r, acc);
+      } else {
+        StageRegs<NG, 1> r;
+        load_stage<NG, 1>(stg, apitch, sb, lane, r);
+        compute_stage<NG, 1>(r, acc);
       }
       __syncwarp();
       if (lane == 0) mb_arrive(&ss.empty[slot]);
       ++it;
-      if (++slot == S) {
-        slot = 0;
+      slot += 2;
+      if (slot >= S) {
+        slot -= S;
         ph ^= 1u;
       }
-      if (s != (gu ? nst_gu : nst_dn) - 1) continue;
-      // the item's last stage: this warp's 16-row group is complete
+      const int nst = gu ? nst_gu : nst_dn;
+      if (s + 2 < nst) continue;
+      // this group's last stage of the item: the two warps of the 16-row group
+      // (one per group) add their halves; the one with the item's last stage
+      // finishes it
+      const int par = nitem & 1;
+      const uint32_t use = nitem >> 1;
+      ++nitem;
+      float* rb = red + ((size_t)(par * 8 + sb) * 32 + lane) * 4 * NG;
+      if (s != nst - 1) {
+        wait_phase(&ss.red_empty[par][sb], (use & 1u) ^ 1u, a.st, 310);
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+          for (int z = 0; z < 4; ++z) rb[4 * gi + z] = acc[gi][z];
+        __syncwarp();
+        if (lane == 0) mb_arrive(&ss.red_full[par][sb]);
+        continue;
+      }
+      wait_phase(&ss.red_full[par][sb], use & 1u, a.st, 311);
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+        for (int z = 0; z < 4; ++z) acc[gi][z] += rb[4 * gi + z];
+      __syncwarp();
+      if (lane == 0) mb_arrive(&ss.red_empty[par][sb]);
       const int ii = gu ? item : item - n_gu;
       const int u = gu ? ii / gu_per : ii / dn_per;
       const int b = gu ? ii - u * gu_per : ii - u * dn_per;
       const uint64_t te0 = (tr && warp == 0) ? gtime() : 0;
-      if (gu) epilogue_gateup<NG>(a, ss, u, b, sb, acc, lane);
+      if (gu) epilogue_gateup<NG>(a, ss, u, b, sb, grp, acc, lane);
       else epilogue_down<NG>(a, ss, u, b, sb, acc, lane);
+      post(item);
       if (tr && warp == 0) w_epi += gtime() - te0;
     }
+    post(-1);
     if (tr && warp == 0 && lane == 0) {
       tr[5] = gtime();
       tr[10] = w_full;
@@ -881,18 +1035,18 @@ size_t stream_act_h_bytes(int I, int rows) { return (size_t)(I / 64) * rows * ds
 size_t stream_act_x_bytes(int H) { return (size_t)(H / 64) * kDecodeMaxTokens * dstr::kRow; }
 
 struct StreamPlan {
-  int xs, stages, stage_bytes;
+  int stages, stage_bytes;
   size_t smem;
 };
 
 static StreamPlan stream_plan(int T, int H, int smem_max) {
   const int NG = T <= 8 ? 1 : 2;
+  (void)H;
   StreamPlan p{};
-  const int nch = H / 64;
-  p.xs = T * nch <= dstr::kConsumers * dstr::kXsPairs;
-  p.stage_bytes = dstr::kAct + dstr::kCPS * 8 * NG * dstr::kRow;
-  const size_t fixed = ((sizeof(StreamSmem) + 127) & ~size_t(127)) +
-                       ((p.xs ? (size_t)nch * T * dstr::kRow : 0) + 127) / 128 * 128;
+  // codes, scales, and T activation rows per chunk
+  p.stage_bytes = (dstr::kAct + dstr::kCPS * T * dstr::kRow + 15) / 16 * 16;
+  // + the pair sums, and a tail pad: the last stage's reads past its rows stay inside
+  const size_t fixed = ((sizeof(StreamSmem) + 127) & ~size_t(127)) + 2 * 8 * 32 * 4 * NG * 4 + 8 * NG * dstr::kRow;
   const int room = (int)(((size_t)smem_max > fixed ? (size_t)smem_max - fixed : 0) / p.stage_bytes);
   p.stages = room < dstr::kMaxStages ? room : dstr::kMaxStages;
   p.smem = fixed + (size_t)p.stages * p.stage_bytes;
@@ -972,9 +1126,15 @@ cudaError_t launch_decode_stream(const LayerDims& d, const uint8_t* blob, const 
   a.fault = fault;
   a.stages = plan.stages;
   a.stage_bytes = plan.stage_bytes;
-  a.xs = plan.xs;
+  // chunks per stage: 4, or fewer so that every item has at least two stages (one per consumer group)
+  a.cps = (d.H / 64 >= 8 && d.I / 64 >= 8) ? 4 : (d.H / 64 >= 4 && d.I / 64 >= 4) ? 2 : 1;
   a.checks = d.checks;
   a.trace = ws.trace;
+  static const int pf_dist = [] {
+    const char* e = getenv("NVFP4_MOE_DECODE_PREFETCH");
+    return e ? atoi(e) : 0;
+  }();
+  a.pf_dist = pf_dist;
   if (!route_only && T * (k + d.S) > ws.act_rows) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(route_only ? 1 : num_sms);

@@ -50,9 +50,18 @@ namespace pf {
 //   B   : routed activation rows (TMA, 128B swizzle), up to 256 rows
 //   RAW : packed FP4 codes + scales of 128 weight rows (bulk copy) -- deep,
 //         so the HBM latency of the weight stream is covered
-constexpr int kAStages = 2;
-constexpr int kBStages = 4;
-constexpr int kRawStages = 10;
+#ifndef NVFP4_MOE_PF_STAGES_A
+#define NVFP4_MOE_PF_STAGES_A 2
+#endif
+#ifndef NVFP4_MOE_PF_STAGES_B
+#define NVFP4_MOE_PF_STAGES_B 4
+#endif
+#ifndef NVFP4_MOE_PF_STAGES_RAW
+#define NVFP4_MOE_PF_STAGES_RAW 10
+#endif
+constexpr int kAStages = NVFP4_MOE_PF_STAGES_A;
+constexpr int kBStages = NVFP4_MOE_PF_STAGES_B;
+constexpr int kRawStages = NVFP4_MOE_PF_STAGES_RAW;
 constexpr int kBlocks = 2;                // 128-row weight blocks per work unit
 constexpr int kABlockBytes = 16384;       // one block's chunk: 128 rows x 128 B (BF16)
 constexpr int kAStageBytes = kBlocks * kABlockBytes;
