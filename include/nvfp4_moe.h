@@ -119,11 +119,13 @@ typedef struct nvfp4_moe* nvfp4_moe_t;
 nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* config, nvfp4_moe_t* out);
 
 /* Copy the experts into the handle's device layout: for every 128 weight rows
- * and 64-element K chunk, 4096 bytes of codes ordered so that each 16-byte
- * vector holds two rows x 16 elements (one scale group each), followed
- * elsewhere by the matching 512 bytes of scales; the gate and up rows are
- * interleaved in groups of 8.  Loads of this layout are 16-byte vectorised
- * and fully coalesced on both the decode and the prefill path.
+ * and 64-element K chunk, one 4608-byte tile of 4096 bytes of codes, ordered
+ * so that each 16-byte vector holds two rows x 16 elements (one scale group
+ * each), followed by the matching 512 bytes of scales; a row block's tiles
+ * follow one another along K, so any run of its chunks is one contiguous
+ * bulk copy; the gate and up rows are interleaved in groups of 8.  Loads of
+ * this layout are 16-byte vectorised and fully coalesced on both the decode
+ * and the prefill path.
  * All inputs are DEVICE pointers in the canonical layout, per expert e (E
  * below counts the shared expert too when the handle has one: it is the last):
  *   w13_q [E][2I][H/2]  uint8  E2M1 codes, gate rows 0..I-1 then up rows
@@ -299,9 +301,9 @@ nvfp4_moe_status nvfp4_moe_debug_route(nvfp4_moe_t h, const void* router_logits,
                                        int32_t* perm, cudaStream_t stream);
 
 /* Copy the handle's packed expert blob (E * 3*H*I*9/16 bytes, the layout
- * described at nvfp4_moe_pack; per expert: gate/up codes [2I*H/2], down codes
- * [H*I/2], gate/up scales [2I*H/16], down scales [H*I/16]) into a caller
- * DEVICE buffer of at least that many bytes. */
+ * described at nvfp4_moe_pack; per expert: the gate/up matrix's tiles
+ * [2I/128][H/64][4608 B], then the down matrix's [H/128][I/64][4608 B]) into
+ * a caller DEVICE buffer of at least that many bytes. */
 nvfp4_moe_status nvfp4_moe_debug_packed_blob(nvfp4_moe_t h, void* dst, size_t dst_bytes, cudaStream_t stream);
 
 /* Phase timeline of the decode kernel (handles created with the environment

@@ -26,23 +26,33 @@ __device__ __forceinline__ void report(DeviceStatus* st, unsigned int flag, unsi
 // ---------------------------------------------------------------------------
 // Packed-weight layout constants.
 //   Matrix W [N][K], N % 128 == 0, K % 64 == 0.  A "chunk" is 64 K-elements.
-//   Nibbles: for row block rb (128 rows), chunk c, sub-block sb (16 rows),
-//   lane t (0..31): 16 bytes at ((rb*nch + c)*8 + sb)*512 + t*16 holding
+//   The matrix is a sequence of 4608-byte tiles, one per (row block rb of 128
+//   rows, chunk c), tile rb*nch + c: 4096 bytes of codes, then 512 of scales,
+//   so that any run of chunks of one row block is one contiguous range.
+//   Codes: for sub-block sb (16 rows), lane t (0..31): 16 bytes at
+//   sb*512 + t*16 of the tile, holding
 //     bytes 0..7 : row rb*128+sb*16+t/4,   K elements 64c+16(t%4) .. +15
 //     bytes 8..15: the row 8 below, same K elements
 //   (byte j of each half holds elements 2j / 2j+1 in its low / high nibble).
-//   Scales: 2 bytes at ((rb*nch + c)*8 + sb)*64 + t*2: the E4M3 scale of the
+//   Scales: 2 bytes at 4096 + sb*64 + t*2 of the tile: the E4M3 scale of the
 //   two rows' 16-element group.
+//   Segment s = ((rb*nch + c)*8 + sb)*32 + t names one lane's 16 code bytes
+//   and 2 scale bytes (code_byte / scale_byte below).
 //   The gate/up matrix is stored row-interleaved: packed row 16g+r is gate
 //   feature 8g+r for r < 8 and up feature 8g+r-8 for r >= 8.
 // ---------------------------------------------------------------------------
 constexpr int kChunk = 64;
 constexpr int kSegBytes = 16;
 constexpr int kBlockRows = 128;
+constexpr int kTileCodes = 4096;  // one tile's codes
+constexpr int kTileBytes = 4608;  // codes + scales
+
+__host__ __device__ inline size_t code_byte(size_t s) { return (s >> 8) * kTileBytes + (s & 255) * 16; }
+__host__ __device__ inline size_t scale_byte(size_t s) { return (s >> 8) * kTileBytes + kTileCodes + (s & 255) * 2; }
 
 struct ExpertLayout {
-  // byte offsets inside one expert's blob
-  size_t w13_nib, w2_nib, w13_sc, w2_sc, stride;
+  // byte offsets inside one expert's blob: the gate/up matrix, the down matrix
+  size_t w13, w2, stride;
 };
 
 // A dense linear W [N][K] packed on its own, like an expert's down matrix
@@ -50,10 +60,8 @@ struct ExpertLayout {
 __host__ __device__ inline ExpertLayout linear_layout(int N, int K) {
   ExpertLayout L;
   const size_t n = (size_t)N * K;
-  L.w13_nib = 0;
-  L.w13_sc = 0;
-  L.w2_nib = 0;
-  L.w2_sc = n / 2;
+  L.w13 = 0;
+  L.w2 = 0;
   L.stride = n / 2 + n / 16;
   return L;
 }
@@ -61,11 +69,9 @@ __host__ __device__ inline ExpertLayout linear_layout(int N, int K) {
 __host__ __device__ inline ExpertLayout expert_layout(int H, int I) {
   ExpertLayout L;
   size_t n13 = (size_t)2 * I * H, n2 = (size_t)H * I;
-  L.w13_nib = 0;
-  L.w2_nib = n13 / 2;
-  L.w13_sc = L.w2_nib + n2 / 2;
-  L.w2_sc = L.w13_sc + n13 / 16;
-  L.stride = L.w2_sc + n2 / 16;
+  L.w13 = 0;
+  L.w2 = n13 / 2 + n13 / 16;
+  L.stride = L.w2 + n2 / 2 + n2 / 16;
   return L;
 }
 

@@ -89,7 +89,7 @@ struct RouteSmem {
 struct FusedArgs {
   const uint8_t* blob;
   size_t expert_stride;
-  size_t nib13, sc13, nib2, sc2;
+  size_t w13, w2;  // byte offsets of the gate/up and down matrices in an expert's blob
   const float* gscale;
   int E, H, I, T, k;  // E experts (routed + shared), k slots per token (top_k + shared)
   int Er, topk;       // routed experts (logits per token), routed choices per token
@@ -592,8 +592,7 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
   const int nch = cw.nch;
   const int gu_units = 2 * a.I / 16;
   const int scol = a.slot_cols;  // token columns of a shared-memory slot
-  const size_t nib_off = kGateUp ? a.nib13 : a.nib2;
-  const size_t sc_off = kGateUp ? a.sc13 : a.sc2;
+  const size_t mat_off = kGateUp ? a.w13 : a.w2;
   // without shared-memory slots or global partial buffers: whole pieces per warp
   const bool whole_only = a.no_split && part_s == nullptr;
   int ibeg, iend;
@@ -614,16 +613,14 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
   // activation copies, S-1 items ahead of the consumer ----
   int wpp = ibeg / nch, wpc = ibeg - (ibeg / nch) * nch, wp_cur = -1, w_cnt = 0, w_m = 0;
   size_t w_seg = 0;
-  const uint8_t* w_nib = nullptr;
-  const uint8_t* w_sc = nullptr;
+  const uint8_t* w_mat = nullptr;
   auto issue_w = [&](uint32_t it) {
     if (wpp != wp_cur) {
       int u, b, rg0, cnt;
       cw.piece(wpp, &u, &b, &rg0, &cnt);
       const int e = rs.tch_e[u];
       w_m = kActCopies ? min(rs.tch_m[u], 8 * NG) : 0;
-      w_nib = a.blob + (size_t)e * a.expert_stride + nib_off;
-      w_sc = a.blob + (size_t)e * a.expert_stride + sc_off;
+      w_mat = a.blob + (size_t)e * a.expert_stride + mat_off;
       // 16-row group g of 128-row block B2 at K chunk c is 512-byte segment
       // (B2 * nch + c) * 8 + (g & 7); 64-row block b is groups 4(b&1)..+3 of B2 = b >> 1
       w_seg = (size_t)(b >> 1) * nch * 8 + 4 * (b & 1) + rg0;
@@ -637,8 +634,10 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (lane == 0 && !a.fault) {
       mbar_expect_tx(bar, (uint32_t)w_cnt * (512u + 64u) + 128u * (uint32_t)w_m);
-      bulk_copy(st + dec::kStA, w_nib + seg0 * 512, 512u * (uint32_t)w_cnt, bar);
-      bulk_copy(st + dec::kStS, w_sc + seg0 * 64, 64u * (uint32_t)w_cnt, bar);
+      // the piece's 16-row groups (seg0 & 7 ..) lie inside tile seg0 >> 3: codes, then scales
+      const uint8_t* tile = w_mat + (seg0 >> 3) * kTileBytes;
+      bulk_copy(st + dec::kStA, tile + (seg0 & 7) * 512, 512u * (uint32_t)w_cnt, bar);
+      bulk_copy(st + dec::kStS, tile + kTileCodes + (seg0 & 7) * 64, 64u * (uint32_t)w_cnt, bar);
     }
     if (++wpc == nch) {
       wpc = 0;
@@ -1203,10 +1202,8 @@ cudaError_t launch_decode_forward(const LayerDims& d, const uint8_t* blob, const
   FusedArgs a{};
   a.blob = blob;
   a.expert_stride = L.stride;
-  a.nib13 = L.w13_nib;
-  a.sc13 = L.w13_sc;
-  a.nib2 = L.w2_nib;
-  a.sc2 = L.w2_sc;
+  a.w13 = L.w13;
+  a.w2 = L.w2;
   a.gscale = gscale;
   a.E = d.E;
   a.Er = d.Er;

@@ -61,10 +61,11 @@ constexpr int kThreads = (kConsumers + 2) * 32;   // + one producer warp + one s
 constexpr int kProducer = kConsumers;             // the producer's warp index
 constexpr int kSignaller = kConsumers + 1;        // the signal warp's index
 constexpr int kSig = 8;                           // depth of each group's completion queue
-constexpr int kCPS = 4;                           // 64-wide K chunks per stage (at most)
-constexpr int kCodes = kCPS * 4096;               // 128 rows x 4 chunks of E2M1 codes
-constexpr int kScales = kCPS * 512;               // their E4M3 scales
-constexpr int kAct = kCodes + kScales;            // activation rows of the stage's chunks
+#ifndef NVFP4_MOE_DEC_CPS
+#define NVFP4_MOE_DEC_CPS 8
+#endif
+constexpr int kCPS = NVFP4_MOE_DEC_CPS;           // 64-wide K chunks per stage (at most): 4 or 8
+constexpr int kAct = kCPS * kTileBytes;          // after the stage's weight tiles (codes + scales): its activation rows
 constexpr int kRow = 144;                         // one activation row of a chunk: 64 FP16, float scale at +128
 constexpr int kMaxSlots = 17;                     // slots per token: top_k <= 16 + one shared expert
 constexpr int kMaxR = kDecodeMaxTokens * kMaxSlots;
@@ -99,7 +100,7 @@ struct StreamSmem {
 
 struct StreamArgs {
   const uint8_t* blob;
-  size_t expert_stride, nib13, sc13, nib2, sc2;
+  size_t expert_stride, w13, w2;  // an expert's bytes; its gate/up and down matrices' offsets
   const float* gscale;
   int E, Er, H, I, T, k, topk;  // E experts in the blob, k slots per token (top_k + shared)
   RouteParams rp;
@@ -114,7 +115,8 @@ struct StreamArgs {
   int32_t* offsets;
   int32_t* perm;
   int32_t* inv;
-  uint8_t* act_h;     // [I/64][rdec][kRow]: h rows per chunk, FP16 with their scale
+  uint8_t* act_h;     // h rows, FP16 with their scale: touched expert u's m rows from row0 form
+                      // block [I/64][m][kRow] at row0 * I/64 rows
   uint8_t* act_x;     // [H/64][T][kRow]: x rows per chunk
   int rdec;           // rows of act_h per chunk
   float* y;           // [R][H] expert outputs, position order
@@ -129,7 +131,7 @@ struct StreamArgs {
   int stages, stage_bytes;
   int checks;         // 1: check table-derived indices (kFlagBounds; the access is skipped)
   int pf_dist;        // stages ahead of the ring whose weights are prefetched into L2 (0: none)
-  int cps;            // 64-wide K chunks per stage (4, or fewer for small H and I: two or more stages per item)
+  int cps;            // 64-wide K chunks per stage (kCPS, or fewer for small H and I: two or more stages per item)
   unsigned long long* trace;  // optional: [cta][16] phase stamps (see decode_stream_kernel)
 };
 
@@ -257,7 +259,11 @@ __device__ __forceinline__ void stream_route_issue(const StreamArgs& a, float (&
     if (warp + r * nw < a.T) warp_issue_logits(a.logits, a.logits_bf16, a.Er, warp + r * nw, val[r]);
 }
 
-__device__ void stream_route(const StreamArgs& a, StreamSmem& ss, float (&val)[2][8], unsigned long long* tr) {
+// `mid` runs on every thread between the expert choice and the tables (the
+// warps that choose no experts do their other early work there).
+template <class Mid>
+__device__ void stream_route(const StreamArgs& a, StreamSmem& ss, float (&val)[2][8], unsigned long long* tr,
+                             Mid&& mid) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
   const int T = a.T, k = a.k, E = a.E, Er = a.Er, topk = a.topk, R = T * k;
   uint32_t key[2][8];
@@ -292,6 +298,7 @@ __device__ void stream_route(const StreamArgs& a, StreamSmem& ss, float (&val)[2
     }
     if (lane == 0 && nt) atomicAdd(&ss.nan, nt);
   }
+  mid();
   __syncthreads();
   if (tr && tid == 0) tr[15] = gtime();
   if (warp == 0) {
@@ -425,13 +432,14 @@ struct StageRegs {
 // of kRow bytes); reads past a chunk's rows land in the next chunk's rows or
 // the ring's tail pad -- MMA columns that no epilogue keeps.
 template <int NG, int NC>
-__device__ __forceinline__ void load_stage(const uint8_t* stg, int pitch, int sb, int lane, StageRegs<NG, NC>& r) {
+__device__ __forceinline__ void load_stage(const uint8_t* stg, int cb, int pitch, int sb, int lane,
+                                           StageRegs<NG, NC>& r) {
   const int g = lane >> 2, q = lane & 3;
 #pragma unroll
-  for (int c = 0; c < NC; ++c) {
-    r.raw[c] = *reinterpret_cast<const uint4*>(stg + c * 4096 + sb * 512 + lane * 16);
-    r.sc[c] = *reinterpret_cast<const uint16_t*>(stg + dstr::kCodes + c * 512 + sb * 64 + lane * 2);
-    const uint8_t* tile = stg + dstr::kAct + c * pitch;
+  for (int c = 0; c < NC; ++c) {  // the stage's chunk cb + c
+    r.raw[c] = *reinterpret_cast<const uint4*>(stg + (cb + c) * kTileBytes + sb * 512 + lane * 16);
+    r.sc[c] = *reinterpret_cast<const uint16_t*>(stg + (cb + c) * kTileBytes + kTileCodes + sb * 64 + lane * 2);
+    const uint8_t* tile = stg + dstr::kAct + (cb + c) * pitch;
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
       const uint8_t* pb = tile + (8 * gi + g) * dstr::kRow + q * 32;
@@ -483,7 +491,7 @@ __device__ __forceinline__ void compute_stage(const StageRegs<NG, NC>& r, float 
 template <int NG>
 __device__ void epilogue_gateup(const StreamArgs& a, StreamSmem& ss, int u, int b, int sb, int grp,
                                 const float (&acc)[NG][4], int lane) {
-  const int e = ss.tch_e[u], row0 = ss.tch_r0[u];
+  const int e = ss.tch_e[u], row0 = ss.tch_r0[u], m_u = ss.tch_m[u];
   const unsigned mask = ss.tch_mask[u];
   const int g = lane >> 2, q = lane & 3;
   const float gsg = __ldg(a.gscale + 3 * e), gsu = __ldg(a.gscale + 3 * e + 1);
@@ -515,12 +523,13 @@ __device__ void epilogue_gateup(const StreamArgs& a, StreamSmem& ss, int u, int 
       for (int s = 0; s < 8; ++s) m = fmaxf(m, ss.cmax[grp][s][t]);
       const int p = max(-126, min(126, prescale_exp(m)));
       const int pos = row0 + __popc(mask & ((1u << t) - 1u));
-      if (a.checks && (pos < 0 || pos >= a.T * a.k)) {
+      if (a.checks && (pos < 0 || pos >= a.T * a.k || pos - row0 >= m_u)) {
         report(a.st, kFlagBounds, 802);
         continue;
       }
       const int f = 8 * sb + g;  // feature within the chunk
-      uint8_t* row = a.act_h + ((size_t)b * a.rdec + pos) * dstr::kRow;
+      // the expert's rows are one block, chunk-major: [I/64][m][row]
+      uint8_t* row = a.act_h + ((size_t)row0 * (a.I / 64) + (size_t)b * m_u + (pos - row0)) * dstr::kRow;
       *reinterpret_cast<__half*>(row + 2 * f) = __float2half_rn(hv[gi][c] * exp2i(-p));
       if (sb == 0 && g == 0) *reinterpret_cast<float*>(row + 128) = exp2i(p);
     }
@@ -618,18 +627,26 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
   // stages, [11] warp 0 ns in epilogues, [12] down items, [13] first down item started, [14] routing:
   // logits requested, [15] routing: experts chosen
   unsigned long long* tr = a.trace ? a.trace + (size_t)blockIdx.x * 16 : nullptr;
+  // per-stage timeline of the first 8 CTAs (256 stages each, 8 words): producer before the
+  // empty wait, after it, after the weight copies, after the activation copies, item<<8|stage;
+  // the consumer group's wait end, its release
+  unsigned long long* tl = (a.trace && blockIdx.x < 8) ? a.trace + (size_t)gridDim.x * 16 + blockIdx.x * 2048 : nullptr;
   if (tr && tid == 0) tr[0] = gtime();
   float lval[2][8];
   stream_route_issue(a, lval);
 
-  // x words this warp converts (loads issued before routing so their latency overlaps it)
+  // this CTA's share of the x conversion: token tx = 15 - warp of its chunks (chunk
+  // blockIdx.x + i * gridDim.x), on the consumer warps from the top down -- for T <= 8
+  // none of them chooses experts, so the conversion runs beside the routing; the loads
+  // are issued first thing
+  const int tx = dstr::kConsumers - 1 - warp;
+  const bool xconv = !a.route_only && a.x && tx >= 0 && tx < T;
   uint32_t xw[dstr::kXChunks];
-  if (!a.route_only && a.x && warp < T) {
+  if (xconv) {
 #pragma unroll
     for (int i = 0; i < dstr::kXChunks; ++i) {
-      // this CTA's chunks of x: chunk blockIdx.x + i * gridDim.x, token `warp`
       const int c = blockIdx.x + i * gridDim.x;
-      if (c < nchH) xw[i] = __ldg(reinterpret_cast<const uint32_t*>(a.x + (size_t)warp * a.H + 64 * c) + lane);
+      if (c < nchH) xw[i] = __ldg(reinterpret_cast<const uint32_t*>(a.x + (size_t)tx * a.H + 64 * c) + lane);
     }
   }
   if (tid == 0 && !a.route_only) {
@@ -649,7 +666,26 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
       }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  stream_route(a, ss, lval, tr);  // ends with __syncthreads: tables and barriers are ready
+  stream_route(a, ss, lval, tr, [&] {
+    if (!xconv) return;
+#pragma unroll
+    for (int i = 0; i < dstr::kXChunks; ++i) {
+      const int c = blockIdx.x + i * gridDim.x;
+      if (c < nchH) convert_chunk_row(xw[i], a.act_x + ((size_t)c * T + tx) * dstr::kRow, lane);
+    }
+    // (chunks beyond the ones loaded above: only when the grid is small)
+    for (int c = blockIdx.x + dstr::kXChunks * gridDim.x; c < nchH; c += gridDim.x) {
+      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(a.x + (size_t)tx * a.H + 64 * c) + lane);
+      convert_chunk_row(w, a.act_x + ((size_t)c * T + tx) * dstr::kRow, lane);
+    }
+    // the rows are read by other CTAs' bulk copies (the async proxy) once x_ready counts them
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      for (int c = blockIdx.x; c < nchH; c += gridDim.x) atomicAdd(a.x_ready + c, 1);
+    }
+  });  // ends with __syncthreads: tables and barriers are ready
   if (a.route_only) return;
   if (tr && tid == 0) tr[1] = gtime();
 
@@ -714,8 +750,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
           break;
         }
         const uint8_t* eb = a.blob + (size_t)e * a.expert_stride;
-        const uint8_t* codes = eb + (gu ? a.nib13 : a.nib2) + (size_t)b * nch * 4096;
-        const uint8_t* scl = eb + (gu ? a.sc13 : a.sc2) + (size_t)b * nch * 512;
+        const uint8_t* tiles = eb + (gu ? a.w13 : a.w2) + (size_t)b * nch * kTileBytes;  // row block b's tiles
         const int32_t* dep = a.done_c + (size_t)u * nchI;
         // the item's inputs: a down item needs all of its expert's h (every chunk), a gate/up
         // item every chunk of act_x -- one parallel check, made once the first stage's weight
@@ -728,26 +763,30 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
           int ok = 1;
           if (lane == 0) {
             const uint64_t t0 = tr ? gtime() : 0;
+            if (tl && it < 256) tl[8 * it] = t0;
             ok = wait_phase(&ss.empty[slot], ph ^ 1u, a.st, 501);
             const uint64_t t1 = tr ? gtime() : 0;
             w_empty += t1 - t0;
             (void)t1;
             if (tr && it == 0) tr[2] = gtime();
+            if (tl && it < 256) {
+              tl[8 * it + 1] = gtime();
+              tl[8 * it + 4] = ((unsigned long long)item << 8) | (unsigned)s;
+            }
             if (ok) {
               ss.meta[slot][0] = item;
               ss.meta[slot][1] = s;
               ss.meta[slot][2] = nc;
               // the stage's activation rows: nc chunks x (T tokens or the expert's m rows)
-              mb_expect(full, (uint32_t)nc * (4096u + 512u) + (uint32_t)(nc * (gu ? T : m) * dstr::kRow));
-              bulk_g2s(stg, codes + (size_t)c0 * 4096, (uint32_t)nc * 4096u, full);
-              bulk_g2s(stg + dstr::kCodes, scl + (size_t)c0 * 512, (uint32_t)nc * 512u, full);
+              mb_expect(full, (uint32_t)(nc * kTileBytes + nc * (gu ? T : m) * dstr::kRow));
+              bulk_g2s(stg, tiles + (size_t)c0 * kTileBytes, (uint32_t)(nc * kTileBytes), full);
               // the weights a ring's depth further on into L2: more bytes in flight than the ring holds
               const int pf = s + a.pf_dist;
               if (a.pf_dist > 0 && pf < nst) {
                 const int p0 = cps * pf, pn = min(cps, nch - p0);
-                prefetch_l2(codes + (size_t)p0 * 4096, (uint32_t)pn * 4096u);
-                prefetch_l2(scl + (size_t)p0 * 512, (uint32_t)pn * 512u);
+                prefetch_l2(tiles + (size_t)p0 * kTileBytes, (uint32_t)(pn * kTileBytes));
               }
+              if (tl && it < 256) tl[8 * it + 2] = gtime();
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -771,11 +810,11 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
           if (ok && lane == 0) {
             if (gu) {
               bulk_g2s(stg + dstr::kAct, a.act_x + (size_t)c0 * apitch, (uint32_t)(nc * apitch), full);
-            } else {
-              for (int c = 0; c < nc; ++c)
-                bulk_g2s(stg + dstr::kAct + c * apitch, a.act_h + ((size_t)(c0 + c) * a.rdec + row0) * dstr::kRow,
-                         (uint32_t)(m * dstr::kRow), full);
+            } else {  // the expert's h rows of chunks c0.. are one range
+              bulk_g2s(stg + dstr::kAct, a.act_h + ((size_t)row0 * nchI + (size_t)c0 * m) * dstr::kRow,
+                       (uint32_t)(nc * m * dstr::kRow), full);
             }
+            if (tl && it < 256) tl[8 * it + 3] = gtime();
           }
           if (!ok) {
             dead = true;
@@ -850,24 +889,6 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
     // group grp takes the stages of even (0) or odd (1) global index; warp sb
     // of a group takes 16-row group sb of each of its stages
     const int grp = warp / dstr::kGroupWarps, sb = warp % dstr::kGroupWarps;
-    if (a.x && warp < T) {  // this CTA's share of the x conversion: token `warp` of its chunks
-#pragma unroll
-      for (int i = 0; i < dstr::kXChunks; ++i) {
-        const int c = blockIdx.x + i * gridDim.x;
-        if (c < nchH) convert_chunk_row(xw[i], a.act_x + ((size_t)c * T + warp) * dstr::kRow, lane);
-      }
-      // (chunks beyond the ones loaded above: only when the grid is small)
-      for (int c = blockIdx.x + dstr::kXChunks * gridDim.x; c < nchH; c += gridDim.x) {
-        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(a.x + (size_t)warp * a.H + 64 * c) + lane);
-        convert_chunk_row(w, a.act_x + ((size_t)c * T + warp) * dstr::kRow, lane);
-      }
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence();
-        for (int c = blockIdx.x; c < nchH; c += gridDim.x) atomicAdd(a.x_ready + c, 1);
-      }
-    }
 
     float acc[NG][4];
     int slot = grp;
@@ -894,6 +915,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
         w_full += tw1 - tw0;
         if (it == 0) tr[3] = tw1;
       }
+      if (tl && sb == 0 && lane == 0 && 2 * it + grp < 256) tl[8 * (2 * it + grp) + 5] = gtime();
       const int item = ss.meta[slot][0];
       if (item < 0) break;
       const int s = ss.meta[slot][1], nc = ss.meta[slot][2];
@@ -905,22 +927,30 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
           for (int z = 0; z < 4; ++z) acc[gi][z] = 0.f;
       }
       const uint8_t* stg = ring + (size_t)slot * a.stage_bytes;
-      // operands into registers, the math, then the stage back to the producer
-      if (nc == 4) {
-        StageRegs<NG, 4> r;
-        load_stage<NG, 4>(stg, apitch, sb, lane, r);
-        compute_stage<NG, 4>(r, acc);
-      } else if (nc == 2) {
-        StageRegs<NG, 2> r;
-        load_stage<NG, 2>(stg, apitch, sb, lane, r);
-        compute_stage<NG, 2>(r, acc);
-      } else {
-        StageRegs<NG, 1> r;
-        load_stage<NG, 1>(stg, apitch, sb, lane, r);
-        compute_stage<NG, 1>(r, acc);
+      // a chunk's activation rows: the T tokens, or the down item's expert's m rows
+      const int pitch = gu ? apitch : ss.tch_m[(item - n_gu) / dn_per] * dstr::kRow;
+      // operands into registers, the math (4, 2 or 1 chunks at a time), then the stage back to the producer
+      for (int cb = 0; cb < nc;) {
+        if (nc - cb >= 4) {
+          StageRegs<NG, 4> r;
+          load_stage<NG, 4>(stg, cb, pitch, sb, lane, r);
+          compute_stage<NG, 4>(r, acc);
+          cb += 4;
+        } else if (nc - cb >= 2) {
+          StageRegs<NG, 2> r;
+          load_stage<NG, 2>(stg, cb, pitch, sb, lane, r);
+          compute_stage<NG, 2>(r, acc);
+          cb += 2;
+        } else {
+          StageRegs<NG, 1> r;
+          load_stage<NG, 1>(stg, cb, pitch, sb, lane, r);
+          compute_stage<NG, 1>(r, acc);
+          cb += 1;
+        }
       }
       __syncwarp();
       if (lane == 0) mb_arrive(&ss.empty[slot]);
+      if (tl && sb == 0 && lane == 0 && 2 * it + grp < 256) tl[8 * (2 * it + grp) + 6] = gtime();
       ++it;
       slot += 2;
       if (slot >= S) {
@@ -1001,8 +1031,9 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
 // src 0 -- BF16 rows in h; src 1 -- the streaming decode kernel's FP16 chunk
 // rows with their scale (act_h); src 2 -- the prefill GEMMs' FP16 rows in h,
 // row p scaled by 2^-pexp_h[p].
-__global__ void hidden_to_f32_kernel(const __nv_bfloat16* h, const uint8_t* act_h, const int32_t* pexp_h, int rdec,
-                                     int src, int R, int I, float* out) {
+__global__ void hidden_to_f32_kernel(const __nv_bfloat16* h, const uint8_t* act_h, const int32_t* pexp_h,
+                                     const int32_t* ids, const int32_t* perm, const int32_t* offsets, int src, int R,
+                                     int I, float* out) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (size_t)R * I) return;
   const int r = (int)(i / I), f = (int)(i - (size_t)r * I);
@@ -1011,15 +1042,17 @@ __global__ void hidden_to_f32_kernel(const __nv_bfloat16* h, const uint8_t* act_
   } else if (src == 2) {
     out[i] = __half2float(reinterpret_cast<const __half*>(h)[i]) * __int_as_float((127 + pexp_h[r]) << 23);
   } else {
-    const uint8_t* row = act_h + ((size_t)(f / 64) * rdec + r) * dstr::kRow;
+    // row r's expert block: rows offsets[e] .. offsets[e + 1], chunk-major
+    const int e = ids[perm[r]], row0 = offsets[e], m = offsets[e + 1] - row0;
+    const uint8_t* row = act_h + ((size_t)row0 * (I / 64) + (size_t)(f / 64) * m + (r - row0)) * dstr::kRow;
     out[i] = __half2float(*reinterpret_cast<const __half*>(row + 2 * (f % 64))) * *reinterpret_cast<const float*>(row + 128);
   }
 }
 
 cudaError_t launch_hidden_to_f32(const Workspace& ws, int src, int R, int I, float* out, cudaStream_t st) {
   const size_t n = (size_t)R * I;
-  hidden_to_f32_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(ws.h, ws.act_h, ws.pexp_h, ws.act_rows, src, R, I,
-                                                                    out);
+  hidden_to_f32_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(ws.h, ws.act_h, ws.pexp_h, ws.ids, ws.perm,
+                                                                    ws.offsets, src, R, I, out);
   return cudaGetLastError();
 }
 
@@ -1088,10 +1121,8 @@ cudaError_t launch_decode_stream(const LayerDims& d, const uint8_t* blob, const 
   StreamArgs a{};
   a.blob = blob;
   a.expert_stride = L.stride;
-  a.nib13 = L.w13_nib;
-  a.sc13 = L.w13_sc;
-  a.nib2 = L.w2_nib;
-  a.sc2 = L.w2_sc;
+  a.w13 = L.w13;
+  a.w2 = L.w2;
   a.gscale = gscale;
   a.E = d.E;
   a.Er = d.Er;
@@ -1127,7 +1158,10 @@ cudaError_t launch_decode_stream(const LayerDims& d, const uint8_t* blob, const 
   a.stages = plan.stages;
   a.stage_bytes = plan.stage_bytes;
   // chunks per stage: 4, or fewer so that every item has at least two stages (one per consumer group)
-  a.cps = (d.H / 64 >= 8 && d.I / 64 >= 8) ? 4 : (d.H / 64 >= 4 && d.I / 64 >= 4) ? 2 : 1;
+  a.cps = (d.H / 64 >= 2 * dstr::kCPS && d.I / 64 >= 2 * dstr::kCPS) ? dstr::kCPS
+          : (d.H / 64 >= 8 && d.I / 64 >= 8)                        ? 4
+          : (d.H / 64 >= 4 && d.I / 64 >= 4)                        ? 2
+                                                                     : 1;
   a.checks = d.checks;
   a.trace = ws.trace;
   static const int pf_dist = [] {

@@ -42,7 +42,8 @@ struct Workspace {
   int32_t* tile_rows;
   int32_t* num_tiles;    // [1]
   // streaming decode kernel (decode_stream.cu)
-  uint8_t* act_h;       // [I/64][act_rows][144 B] h rows per 64-wide chunk: FP16 times 2^-p, float 2^p at +128
+  uint8_t* act_h;       // h rows of the streaming decode, 144 B per (row, 64-wide chunk): FP16 times 2^-p, float
+                        // 2^p at +128; an expert's m rows from row0 form block [I/64][m] at row row0 * I/64
   uint8_t* act_x;       // [H/64][T <= 16][144 B] x rows per chunk, same form
   int act_rows;         // rows of act_h per chunk (>= T * slots of any decode step)
   int32_t* wctr;        // [1] work items claimed beyond the first one per CTA

@@ -12,8 +12,8 @@ namespace nvfp4moe {
 
 // One thread per 16-byte packed segment (32 weights, two rows x 16).
 __global__ void pack_matrix_kernel(const uint8_t* __restrict__ src_q, const uint8_t* __restrict__ src_s,
-                                   uint8_t* __restrict__ blob, size_t expert_stride, size_t nib_off,
-                                   size_t sc_off, int N, int K, int interleave_gate_up,
+                                   uint8_t* __restrict__ blob, size_t expert_stride, size_t mat_off,
+                                   int N, int K, int interleave_gate_up,
                                    size_t src_q_expert_stride, size_t src_s_expert_stride, int n_valid) {
   const int e = blockIdx.y;
   const size_t nseg = (size_t)N * K / 32;
@@ -43,11 +43,11 @@ __global__ void pack_matrix_kernel(const uint8_t* __restrict__ src_q, const uint
   const bool v0 = crow0 < n_valid, v1 = crow1 < n_valid;
   const uint2 lo = v0 ? *reinterpret_cast<const uint2*>(q_e + crow0 * kb + 32 * c + 8 * q) : make_uint2(0u, 0u);
   const uint2 hi = v1 ? *reinterpret_cast<const uint2*>(q_e + crow1 * kb + 32 * c + 8 * q) : make_uint2(0u, 0u);
-  uint8_t* dst = blob + (size_t)e * expert_stride;
-  *reinterpret_cast<uint4*>(dst + nib_off + s * 16) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+  uint8_t* dst = blob + (size_t)e * expert_stride + mat_off;
+  *reinterpret_cast<uint4*>(dst + code_byte(s)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
   const uint8_t s0 = v0 ? s_e[crow0 * ks + 4 * c + q] : 0;
   const uint8_t s1 = v1 ? s_e[crow1 * ks + 4 * c + q] : 0;
-  *reinterpret_cast<uint16_t*>(dst + sc_off + s * 2) = (uint16_t)(s0 | (s1 << 8));
+  *reinterpret_cast<uint16_t*>(dst + scale_byte(s)) = (uint16_t)(s0 | (s1 << 8));
 }
 
 // Dequantise one tensor of one expert from the packed blob:
@@ -68,8 +68,8 @@ __global__ void debug_dequant_kernel(const uint8_t* __restrict__ blob_e, const f
   const int rb = (int)(s / (256 * (size_t)nch));
   const int q = t & 3;
   const int R0 = rb * kBlockRows + sb * 16 + (t >> 2);
-  const uint8_t* nib = blob_e + (down ? L.w2_nib : L.w13_nib) + s * 16;
-  const uint8_t* sc = blob_e + (down ? L.w2_sc : L.w13_sc) + s * 2;
+  const uint8_t* nib = blob_e + (down ? L.w2 : L.w13) + code_byte(s);
+  const uint8_t* sc = blob_e + (down ? L.w2 : L.w13) + scale_byte(s);
   const uint4 raw = *reinterpret_cast<const uint4*>(nib);
   const uint32_t s2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sc));
   const float g = gs_e[which];
@@ -158,13 +158,13 @@ cudaError_t launch_pack(const uint8_t* w13_q, const uint8_t* w13_s, const uint8_
   {
     const size_t nseg = (size_t)2 * I * H / 32;
     dim3 grid((unsigned)((nseg + thr - 1) / thr), E);
-    pack_matrix_kernel<<<grid, thr, 0, st>>>(w13_q, w13_s, blob, L.stride, L.w13_nib, L.w13_sc, 2 * I, H, 1,
+    pack_matrix_kernel<<<grid, thr, 0, st>>>(w13_q, w13_s, blob, L.stride, L.w13, 2 * I, H, 1,
                                              (size_t)2 * I * H / 2, (size_t)2 * I * H / 16, 2 * I);
   }
   {
     const size_t nseg = (size_t)H * I / 32;
     dim3 grid((unsigned)((nseg + thr - 1) / thr), E);
-    pack_matrix_kernel<<<grid, thr, 0, st>>>(w2_q, w2_s, blob, L.stride, L.w2_nib, L.w2_sc, H, I, 0,
+    pack_matrix_kernel<<<grid, thr, 0, st>>>(w2_q, w2_s, blob, L.stride, L.w2, H, I, 0,
                                              (size_t)H * I / 2, (size_t)H * I / 16, H);
   }
   return cudaGetLastError();
@@ -175,7 +175,7 @@ cudaError_t launch_pack_linear(const uint8_t* w_q, const uint8_t* w_s, uint8_t* 
   const ExpertLayout L = linear_layout(Np, K);
   const int thr = 256;
   const size_t nseg = (size_t)Np * K / 32;
-  pack_matrix_kernel<<<(unsigned)((nseg + thr - 1) / thr), thr, 0, st>>>(w_q, w_s, blob, L.stride, L.w2_nib, L.w2_sc,
+  pack_matrix_kernel<<<(unsigned)((nseg + thr - 1) / thr), thr, 0, st>>>(w_q, w_s, blob, L.stride, L.w2,
                                                                          Np, K, 0, 0, 0, N);
   return cudaGetLastError();
 }

@@ -92,7 +92,7 @@ size_t prefill_smem_bytes() { return pf::kSmemBytes; }
 struct PrefillArgs {
   const uint8_t* blob;
   size_t expert_stride;
-  size_t nib_off, sc_off;
+  size_t mat_off;  // the matrix's byte offset in an expert's blob
   const float* gscale;
   int K;      // reduction length (H for gate/up, I for down)
   int NB;     // 128-row weight blocks per expert
@@ -345,18 +345,15 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           *abort_flag = 1;
           break;
         }
-        const uint8_t* src_nib = a.blob + (size_t)e * a.expert_stride + a.nib_off + (size_t)nb0 * nch * 4096;
-        const uint8_t* src_sc = a.blob + (size_t)e * a.expert_stride + a.sc_off + (size_t)nb0 * nch * 512;
+        const uint8_t* src = a.blob + (size_t)e * a.expert_stride + a.mat_off + (size_t)nb0 * nch * kTileBytes;
         for (int c = 0; c < nch; ++c, ++it) {
           const int s = it % pf::kRawStages;
           const uint32_t ph = (it / pf::kRawStages) & 1u;
           if (!mbar_wait(raw_empty + s, ph ^ 1u, abort_flag, a.st, 1)) break;
           uint8_t* st = smem + pf::kRawOff + s * pf::kRawStageBytes;
           mbar_arrive_expect_tx(raw_full + s, (uint32_t)nblk * (4096u + 512u));
-          for (int j = 0; j < nblk; ++j) {  // block nb0 + j's chunk c: 4096 B codes, 512 B scales
-            bulk_g2s(st + j * pf::kRawBlockBytes, src_nib + ((size_t)j * nch + c) * 4096, 4096, raw_full + s);
-            bulk_g2s(st + j * pf::kRawBlockBytes + 4096, src_sc + ((size_t)j * nch + c) * 512, 512, raw_full + s);
-          }
+          for (int j = 0; j < nblk; ++j)  // block nb0 + j's chunk c: one tile, 4096 B codes + 512 B scales
+            bulk_g2s(st + j * pf::kRawBlockBytes, src + ((size_t)j * nch + c) * kTileBytes, kTileBytes, raw_full + s);
         }
       }
     }
@@ -624,16 +621,14 @@ cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const fl
   a.E = d.E;
   a.R = T * (k + d.S);
   if (!d.linear) {  // gate/up: 2I interleaved rows, K = H (FP16 operands)
-    a.nib_off = L.w13_nib;
-    a.sc_off = L.w13_sc;
+    a.mat_off = L.w13;
     a.K = d.H;
     a.NB = 2 * d.I / 128;
     prefill_gemm_kernel<true, false, true><<<num_sms, pf::kThreads, pf::kSmemBytes, st>>>(maps.x_perm, maps.x_perm, a);
   }
   if (mid) cudaEventRecord(mid, st);
   // down: H rows, K = I
-  a.nib_off = L.w2_nib;
-  a.sc_off = L.w2_sc;
+  a.mat_off = L.w2;
   a.K = d.I;
   a.NB = d.H / 128;
   if (d.linear)  // the caller's BF16 x

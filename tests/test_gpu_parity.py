@@ -187,10 +187,10 @@ def _host_repack_expert(w13_q, w13_s, w2_q, w2_s, H, I):
         nib = qb.transpose(0, 4, 1, 3, 5, 2, 6)       # rb, c, sb, t4, q, half, bytes
         sb_ = ss.reshape(N // 128, 8, 2, 8, nch, 4)
         sc = sb_.transpose(0, 4, 1, 3, 5, 2)          # rb, c, sb, t4, q, half
-        return nib.reshape(-1), sc.reshape(-1)
-    n13, s13 = pack(w13_q, w13_s, 2 * I, H, True)
-    n2, s2 = pack(w2_q, w2_s, H, I, False)
-    return np.concatenate([n13, n2, s13, s2])
+        # one tile per (rb, c): its 4096 code bytes, then its 512 scale bytes
+        tiles = np.concatenate([nib.reshape(N // 128, nch, 4096), sc.reshape(N // 128, nch, 512)], axis=2)
+        return tiles.reshape(-1)
+    return np.concatenate([pack(w13_q, w13_s, 2 * I, H, True), pack(w2_q, w2_s, H, I, False)])
 
 
 @pytest.mark.parametrize("name,experts", [("tiny", None), ("decode_mtp", (0, 64, 127))])
