@@ -121,7 +121,8 @@ nvfp4_moe_status nvfp4_moe_create(const nvfp4_moe_config* config, nvfp4_moe_t* o
 /* Copy the experts into the handle's device layout: for every 128 weight rows
  * and 64-element K chunk, one 4608-byte tile of 4096 bytes of codes, ordered
  * so that each 16-byte vector holds two rows x 16 elements (one scale group
- * each), followed by the matching 512 bytes of scales; a row block's tiles
+ * each; a 16-row group's vectors ordered by K group, then row), followed by
+ * the matching 512 bytes of scales; a row block's tiles
  * follow one another along K, so any run of its chunks is one contiguous
  * bulk copy; the gate and up rows are interleaved in groups of 8.  Loads of
  * this layout are 16-byte vectorised and fully coalesced on both the decode

@@ -30,12 +30,16 @@ __device__ __forceinline__ void report(DeviceStatus* st, unsigned int flag, unsi
 //   rows, chunk c), tile rb*nch + c: 4096 bytes of codes, then 512 of scales,
 //   so that any run of chunks of one row block is one contiguous range.
 //   Codes: for sub-block sb (16 rows), lane t (0..31): 16 bytes at
-//   sb*512 + t*16 of the tile, holding
+//   sb*512 + P(t)*16 of the tile, holding
 //     bytes 0..7 : row rb*128+sb*16+t/4,   K elements 64c+16(t%4) .. +15
 //     bytes 8..15: the row 8 below, same K elements
 //   (byte j of each half holds elements 2j / 2j+1 in its low / high nibble).
-//   Scales: 2 bytes at 4096 + sb*64 + t*2 of the tile: the E4M3 scale of the
-//   two rows' 16-element group.
+//   Scales: 2 bytes at 4096 + sb*64 + P(t)*2 of the tile: the E4M3 scale of
+//   the two rows' 16-element group.
+//   P(t) = 8*(t%4) + t/4 orders a sub-block's segments by K group: a lane
+//   reading its mma fragment (segment t) and a thread reading one row's four
+//   groups (rows r, r+8 of group q: 16-byte slots 8q .. 8q+7) both hit every
+//   shared-memory bank once.
 //   Segment s = ((rb*nch + c)*8 + sb)*32 + t names one lane's 16 code bytes
 //   and 2 scale bytes (code_byte / scale_byte below).
 //   The gate/up matrix is stored row-interleaved: packed row 16g+r is gate
@@ -47,8 +51,13 @@ constexpr int kBlockRows = 128;
 constexpr int kTileCodes = 4096;  // one tile's codes
 constexpr int kTileBytes = 4608;  // codes + scales
 
-__host__ __device__ inline size_t code_byte(size_t s) { return (s >> 8) * kTileBytes + (s & 255) * 16; }
-__host__ __device__ inline size_t scale_byte(size_t s) { return (s >> 8) * kTileBytes + kTileCodes + (s & 255) * 2; }
+__host__ __device__ inline int seg_pos(int t) { return 8 * (t & 3) + (t >> 2); }  // P(t)
+__host__ __device__ inline size_t code_byte(size_t s) {
+  return (s >> 8) * kTileBytes + ((s >> 5) & 7) * 512 + (size_t)seg_pos((int)(s & 31)) * 16;
+}
+__host__ __device__ inline size_t scale_byte(size_t s) {
+  return (s >> 8) * kTileBytes + kTileCodes + ((s >> 5) & 7) * 64 + (size_t)seg_pos((int)(s & 31)) * 2;
+}
 
 struct ExpertLayout {
   // byte offsets inside one expert's blob: the gate/up matrix, the down matrix

@@ -796,8 +796,9 @@ __device__ void run_phase(const FusedArgs& a, RouteSmem& rs, uint8_t* ring, uint
 #pragma unroll
     for (int rg = 0; rg < dec::kRG; ++rg) {
       if (rg >= ccnt) break;
-      const uint4 raw = *reinterpret_cast<const uint4*>(st + dec::kStA + rg * 512 + lane * 16);
-      const uint32_t s2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(st + dec::kStS + rg * 64 + lane * 2));
+      const uint4 raw = *reinterpret_cast<const uint4*>(st + dec::kStA + rg * 512 + seg_pos(lane) * 16);
+      const uint32_t s2 =
+          e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(st + dec::kStS + rg * 64 + seg_pos(lane) * 2));
       const uint32_t s0 = dup_lo(s2), s1 = dup_hi(s2);
       uint32_t cx[4], cy[4], cz[4], cw4[4];
       e2m1x8_to_f16(raw.x, cx);

@@ -437,8 +437,9 @@ __device__ __forceinline__ void load_stage(const uint8_t* stg, int cb, int pitch
   const int g = lane >> 2, q = lane & 3;
 #pragma unroll
   for (int c = 0; c < NC; ++c) {  // the stage's chunk cb + c
-    r.raw[c] = *reinterpret_cast<const uint4*>(stg + (cb + c) * kTileBytes + sb * 512 + lane * 16);
-    r.sc[c] = *reinterpret_cast<const uint16_t*>(stg + (cb + c) * kTileBytes + kTileCodes + sb * 64 + lane * 2);
+    r.raw[c] = *reinterpret_cast<const uint4*>(stg + (cb + c) * kTileBytes + sb * 512 + seg_pos(lane) * 16);
+    r.sc[c] =
+        *reinterpret_cast<const uint16_t*>(stg + (cb + c) * kTileBytes + kTileCodes + sb * 64 + seg_pos(lane) * 2);
     const uint8_t* tile = stg + dstr::kAct + (cb + c) * pitch;
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {

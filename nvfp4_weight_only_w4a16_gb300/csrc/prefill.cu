@@ -47,43 +47,56 @@ namespace nvfp4moe {
 namespace pf {
 // Shared-memory rings (each stage is one 64-wide K chunk of one work unit):
 //   A   : BF16 operand written by the dequantisers, read by tcgen05.mma
-//   B   : routed activation rows (TMA, 128B swizzle), up to 256 rows
+//   B   : routed activation rows (TMA, 128B swizzle), up to 128 rows
 //   RAW : packed FP4 codes + scales of 128 weight rows (bulk copy) -- deep,
 //         so the HBM latency of the weight stream is covered
-#ifndef NVFP4_MOE_PF_STAGES_A
-#define NVFP4_MOE_PF_STAGES_A 2
-#endif
 #ifndef NVFP4_MOE_PF_STAGES_B
 #define NVFP4_MOE_PF_STAGES_B 4
 #endif
 #ifndef NVFP4_MOE_PF_STAGES_RAW
-#define NVFP4_MOE_PF_STAGES_RAW 10
+#define NVFP4_MOE_PF_STAGES_RAW 9
 #endif
-constexpr int kAStages = NVFP4_MOE_PF_STAGES_A;
+// Packed weights: the dequantised operand lives in TMEM (tcgen05.mma with A
+// from tensor memory), kAStagesT stages of two 64-wide K chunks x two blocks
+// (32 columns per chunk and block: 64 16-bit values per row) in columns
+// 256..511; the accumulator (two blocks x 128 columns) takes columns 0..255,
+// one buffer.  The MMA issuer syncs once per stage (16 MMAs): every wait,
+// fence and commit stalls its queue for a few hundred cycles.
+// Shared memory: [B ring, kBStages x 2 chunks x 16 KB][RAW ring, one chunk
+// per stage][row exponents][barriers].
+// BF16 weights (the router) keep a shared-memory operand ring and two
+// accumulator buffers: B takes 4 stages, operand stages 0, 1 the rest of the
+// B region, 2, 3 the RAW region.
 constexpr int kBStages = NVFP4_MOE_PF_STAGES_B;
+constexpr int kBStagesW = 4;
 constexpr int kRawStages = NVFP4_MOE_PF_STAGES_RAW;
 constexpr int kBlocks = 2;                // 128-row weight blocks per work unit
-constexpr int kABlockBytes = 16384;       // one block's chunk: 128 rows x 128 B (BF16)
+constexpr int kABlockBytes = 16384;       // BF16 mode: one block's chunk, 128 rows x 128 B
 constexpr int kAStageBytes = kBlocks * kABlockBytes;
-constexpr int kBStageBytes = 16384;       // up to 128 routed rows x 128 B
+constexpr int kBStageBytes = 16384;       // one chunk of up to 128 routed rows x 128 B
+constexpr int kKS = 2;                    // packed weights: chunks per operand and activation stage
 constexpr int kRawBlockBytes = 4608;      // one block's chunk: 4096 B codes + 512 B scales
 constexpr int kRawStageBytes = kBlocks * kRawBlockBytes;
-constexpr int kAOff = 0;
-constexpr int kBOff = kAOff + kAStages * kAStageBytes;
-constexpr int kRawOff = kBOff + kBStages * kBStageBytes;
-constexpr int kBarOff = kRawOff + kRawStages * kRawStageBytes;
+constexpr int kBOff = 0;
+constexpr int kRawOff = kBOff + kBStages * kKS * kBStageBytes;
+constexpr int kPexOff = kRawOff + kRawStages * kRawStageBytes;  // per epilogue warp [2][128] int: row exponents
+constexpr int kBarOff = kPexOff + 8 * 1024;
 constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
-// BF16-weight mode (no packed ring): the operand ring takes the packed ring's
-// space too -- stages 0, 1 in the A region, 2, 3 in the RAW region.
-constexpr int kAStagesW = kAStages + (kRawStages * kRawStageBytes) / kAStageBytes;
+constexpr int kAStagesW = 2 + (kRawStages * kRawStageBytes) / kAStageBytes;
+static_assert(kBStagesW * kBStageBytes + 2 * kAStageBytes <= kRawOff, "BF16 mode: B and two operand stages fit the B region");
 static_assert(kAStagesW <= kRawStages, "BF16-mode operand barriers reuse the packed ring's");
 static_assert(kRawOff % 1024 == 0 && kAStageBytes % 1024 == 0, "128B-swizzled stages need 1024-byte alignment");
+static_assert(kSmemBytes <= 232448, "shared memory");
 __host__ __device__ constexpr int a_stage_off(int s) {
-  return s < kAStages ? kAOff + s * kAStageBytes : kRawOff + (s - kAStages) * kAStageBytes;
+  return s < 2 ? kBStagesW * kBStageBytes + s * kAStageBytes : kRawOff + (s - 2) * kAStageBytes;
 }
-constexpr int kThreads = 480;                     // 15 warps
 constexpr int kDequantWarps = 8;
+constexpr int kEpiWarps = 8;                      // two per TMEM lane quarter: one per weight block
+constexpr int kThreads = (3 + kDequantWarps + kEpiWarps) * 32;  // 19 warps
 constexpr int kTmemCols = 512;
+constexpr int kAStagesT = 2;
+constexpr int kAColT = 256;
+constexpr int kABars = kAStagesT;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // a wait longer than 2 s is a fault
 }  // namespace pf
 
@@ -115,6 +128,11 @@ struct PrefillArgs {
   const int32_t* pexp_h;  // [R] and h row p by 2^-pexp_h[p]
   int checks;             // 1: check the m-tile table against its ranges (kFlagBounds; the unit is skipped)
   int E, R;               // experts in the blob, routed rows (for the checks)
+  // optional role timeline of CTA 0 (gate/up GEMM): per K chunk n < 256 at [4n] the MMA
+  // issue, [4n+1] / [4n+2] dequantiser warp 3's start / end, [4n+3] the weight copy
+  // issue; per unit u < 16 at [1024 + 4u] the MMA's accumulator wait end, the epilogue's
+  // start and end (block 0), the epilogue's end (block 1)
+  unsigned long long* trace;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -197,6 +215,14 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t 
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+// A from tensor memory (a_tmem: lane 0, the K step's first column), B from shared memory
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -204,6 +230,13 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+__device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -217,33 +250,47 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// Dequantise one packed 16-byte segment (rows R0, R0+8; K elements 16q..16q+15
-// of the chunk) into the swizzled 16-bit operand tile at a_base (FP16 when
-// kF16, else BF16; both exact).
-template <bool kF16>
-__device__ __forceinline__ void dequant_segment(const uint8_t* raw_stage, uint32_t a_base, int seg) {
-  const uint4 raw = *reinterpret_cast<const uint4*>(raw_stage + seg * 16);
-  const uint32_t sc = *reinterpret_cast<const uint16_t*>(raw_stage + 4096 + seg * 2);
-  const uint32_t s2 = e4m3x2_to_f16x2(sc);
-  const int R0 = (seg >> 5) * 16 + ((seg & 31) >> 2);
-  const int q = seg & 3;
+// One weight row's bytes of one packed chunk (a 4608-byte tile: codes, then
+// scales): its four 16-element groups' codes and E4M3 scales.  Row r sits in
+// 16-row group r / 16 as the low (r % 16 < 8) or high half of segments
+// 4 (r % 8) + q, stored at slots 8 q + r % 8.
+struct RowRaw {
+  uint2 c[4];
+  uint32_t s[4];
+};
+__device__ __forceinline__ void load_row_raw(const uint8_t* tile, int r, RowRaw& w) {
+  const int g16 = r >> 4, hf = (r >> 3) & 1, rr = r & 7;
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int R = R0 + 8 * half;
-    const uint32_t sx = half ? dup_hi(s2) : dup_lo(s2);
-    const uint32_t w0 = half ? raw.z : raw.x, w1 = half ? raw.w : raw.y;
-    uint32_t o[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t byte = (j < 4 ? w0 : w1) >> (8 * (j & 3));
-      const uint32_t v = hmul2_u32(e2m1x2_to_f16x2(byte), sx);
-      o[j] = kF16 ? v : f16x2_to_bf16x2(v);
-    }
-    const uint32_t row_base = a_base + (uint32_t)((R >> 3) * 1024 + (R & 7) * 128);
-    const uint32_t c0 = (uint32_t)((2 * q) ^ (R & 7)), c1 = (uint32_t)((2 * q + 1) ^ (R & 7));
-    sts128(row_base + c0 * 16, o[0], o[1], o[2], o[3]);
-    sts128(row_base + c1 * 16, o[4], o[5], o[6], o[7]);
+  for (int q = 0; q < 4; ++q) {
+    const int p = 8 * q + rr;
+    w.c[q] = *reinterpret_cast<const uint2*>(tile + g16 * 512 + p * 16 + 8 * hf);
+    w.s[q] = tile[4096 + g16 * 64 + p * 2 + hf];
   }
+}
+// Dequantise the row into 32 TMEM columns of the thread's lane: column c holds
+// K elements 2c (low half) and 2c + 1 (high half) of the chunk, FP16 when
+// kF16, else BF16 (both exact).  All 32 lanes of the warp call it; the caller
+// waits for the store (tcgen05.wait::st).
+template <bool kF16>
+__device__ __forceinline__ void store_row_tmem(const RowRaw& raw, uint32_t taddr) {
+  uint32_t w[32];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {  // K elements 16 q .. 16 q + 15
+    const uint32_t sx = dup_lo(e4m3x2_to_f16x2(raw.s[q]));
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const uint32_t v = hmul2_u32(e2m1x2_to_f16x2((b < 4 ? raw.c[q].x : raw.c[q].y) >> (8 * (b & 3))), sx);
+      w[8 * q + b] = kF16 ? v : f16x2_to_bf16x2(v);
+    }
+  }
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]), "r"(w[9]),
+      "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]), "r"(w[16]), "r"(w[17]), "r"(w[18]),
+      "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]), "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]),
+      "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31])
+      : "memory");
 }
 
 // kBf16W: the weights are a plain BF16 matrix (the router): warp 0 moves its
@@ -258,35 +305,45 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + pf::kBarOff);
   uint64_t* raw_empty = raw_full + pf::kRawStages;
   uint64_t* a_full = raw_empty + pf::kRawStages;
-  uint64_t* a_empty = a_full + pf::kAStages;
-  uint64_t* b_full = a_empty + pf::kAStages;
+  uint64_t* a_empty = a_full + pf::kABars;
+  uint64_t* b_full = a_empty + pf::kABars;
   // the operand ring's barriers and depth (BF16 mode: the packed ring's barriers)
   uint64_t* af = kBf16W ? raw_full : a_full;
   uint64_t* ae = kBf16W ? raw_empty : a_empty;
-  constexpr int nAS = kBf16W ? pf::kAStagesW : pf::kAStages;
+  constexpr int nAS = kBf16W ? pf::kAStagesW : pf::kAStagesT;
+  constexpr int nBS = kBf16W ? pf::kBStagesW : pf::kBStages;
+  constexpr int kCS = kBf16W ? 1 : pf::kKS;  // K chunks per operand / activation stage
+  static_assert(pf::kBStagesW <= pf::kBStages, "B barriers");
+  // accumulator buffers: two with a shared-memory operand, one with the TMEM operand
+  constexpr uint32_t nBuf = kBf16W ? 2u : 1u;
   uint64_t* b_empty = b_full + pf::kBStages;
   uint64_t* accfull = b_empty + pf::kBStages;
   uint64_t* accempty = accfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // epilogue warp w's copy of the unit's x and h row exponents (kF16)
+  int* pex = reinterpret_cast<int*>(smem + pf::kPexOff) + 256 * max(0, warp - 3 - pf::kDequantWarps);
+  int* peh = pex + 128;
+  unsigned long long* tl = (kGateUp && a.trace && blockIdx.x == 0) ? a.trace : nullptr;
   if (threadIdx.x == 0) {
     for (int s = 0; s < pf::kRawStages; ++s) {
       mbar_init(raw_full + s, 1);
       mbar_init(raw_empty + s, kBf16W ? 1 : pf::kDequantWarps);
     }
-    for (int s = 0; s < pf::kAStages; ++s) {
+    for (int s = 0; s < pf::kABars; ++s) {
       mbar_init(a_full + s, kBf16W ? 1 : pf::kDequantWarps);
       mbar_init(a_empty + s, 1);
     }
-    for (int s = 0; s < pf::kBStages; ++s) {
+    for (int s = 0; s < nBS; ++s) {
       mbar_init(b_full + s, 1);
       mbar_init(b_empty + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accfull + b, 1);
-      mbar_init(accempty + b, 4);
+      mbar_init(accempty + b, pf::kEpiWarps);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -350,6 +407,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           const int s = it % pf::kRawStages;
           const uint32_t ph = (it / pf::kRawStages) & 1u;
           if (!mbar_wait(raw_empty + s, ph ^ 1u, abort_flag, a.st, 1)) break;
+          if (tl && it < 256) tl[4 * it + 3] = globaltimer_ns();
           uint8_t* st = smem + pf::kRawOff + s * pf::kRawStageBytes;
           mbar_arrive_expect_tx(raw_full + s, (uint32_t)nblk * (4096u + 512u));
           for (int j = 0; j < nblk; ++j)  // block nb0 + j's chunk c: one tile, 4096 B codes + 512 B scales
@@ -367,27 +425,44 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const int rows = a.tile_rows[tile];
         const int N = (rows + 15) & ~15;
         const uint32_t idesc = kF16 ? idesc_f16(128, N) : idesc_bf16(128, N);
-        const uint32_t buf = j & 1u, aph = (j >> 1) & 1u;
+        const uint32_t buf = j % nBuf, aph = (j / nBuf) & 1u;
         if (!mbar_wait(accempty + buf, aph ^ 1u, abort_flag, a.st, 2)) break;
+        if (tl && j < 16) tl[1024 + 4 * j] = globaltimer_ns();
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * 256u;  // block b's accumulator at + 128 b
         bool ok = true;
-        for (int c = 0; c < nch; ++c, ++ia, ++ib) {
-          const int sa = ia % nAS, sb = ib % pf::kBStages;
+        for (int c = 0; c < nch; c += kCS, ++ia, ++ib) {  // one stage: kCS chunks
+          const int sa = ia % nAS, sb = ib % nBS;
           if (!mbar_wait(af + sa, (ia / nAS) & 1u, abort_flag, a.st, 3) ||
-              !mbar_wait(b_full + sb, (ib / pf::kBStages) & 1u, abort_flag, a.st, 4)) {
+              !mbar_wait(b_full + sb, (ib / nBS) & 1u, abort_flag, a.st, 4)) {
             ok = false;
             break;
           }
+          if (tl && ia < 256) tl[4 * ia] = globaltimer_ns();
           tc_fence_after();
-          const uint64_t ad = sw128_desc(smem_u32(smem + pf::a_stage_off(sa)));
-          const uint64_t bd = sw128_desc(smem_u32(smem + pf::kBOff + sb * pf::kBStageBytes));
+          const uint64_t bd = sw128_desc(smem_u32(smem + pf::kBOff + sb * kCS * pf::kBStageBytes));
+          if (kBf16W) {
+            const uint64_t ad = sw128_desc(smem_u32(smem + pf::a_stage_off(sa)));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acc = (c | kk) != 0 ? 1u : 0u;
-            umma_bf16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, acc);
-            if (nblk > 1)  // block 1's operand tile is 16 KB further (1024 in the 16-byte units)
-              umma_bf16(d_tmem + 128u, ad + (uint64_t)(pf::kABlockBytes >> 4) + 2u * kk, bd + 2u * kk, idesc, acc);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t acc = (c | kk) != 0 ? 1u : 0u;
+              umma_bf16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, acc);
+              if (nblk > 1)  // block 1's operand tile is 16 KB further (1024 in the 16-byte units)
+                umma_bf16(d_tmem + 128u, ad + (uint64_t)(pf::kABlockBytes >> 4) + 2u * kk, bd + 2u * kk, idesc, acc);
+            }
+          } else {
+            // TMEM operand stage sa: chunk h, block j, K step kk at columns + 64 h + 32 j + 8 kk;
+            // the stage's chunk h of B is 16 KB (1024 16-byte units) further
+            const uint32_t at = tmem_base + (uint32_t)(pf::kAColT + sa * 64 * pf::kKS);
+#pragma unroll
+            for (int h = 0; h < pf::kKS; ++h)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t acc = (c | h | kk) != 0 ? 1u : 0u;
+                const uint64_t bk = bd + (uint64_t)(h * (pf::kBStageBytes >> 4)) + 2u * kk;
+                umma_ts(d_tmem, at + 64u * h + 8u * kk, bk, idesc, acc);
+                if (nblk > 1) umma_ts(d_tmem + 128u, at + 64u * h + 32u + 8u * kk, bk, idesc, acc);
+              }
           }
           umma_commit(ae + sa);
           umma_commit(b_empty + sb);
@@ -404,21 +479,24 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const int row0 = a.tile_row0[tile], rows = a.tile_rows[tile];
       const int nbox = (rows + 15) >> 4;
       bool ok = true;
-      for (int c = 0; c < nch; ++c, ++it) {
-        const int s = it % pf::kBStages;
-        const uint32_t ph = (it / pf::kBStages) & 1u;
+      for (int c = 0; c < nch; c += kCS, ++it) {  // one stage: kCS chunks
+        const int s = it % nBS;
+        const uint32_t ph = (it / nBS) & 1u;
         int got = 1;
         if (lane == 0) {
           got = mbar_wait(b_empty + s, ph ^ 1u, abort_flag, a.st, 7);
-          if (got) mbar_arrive_expect_tx(b_full + s, (uint32_t)nbox * 2048u);
+          if (got) mbar_arrive_expect_tx(b_full + s, (uint32_t)(kCS * nbox) * 2048u);
         }
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) {
           ok = false;
           break;
         }
-        uint8_t* st = smem + pf::kBOff + s * pf::kBStageBytes;
-        if (lane < nbox) tma_2d(st + lane * 2048, &tmap_b, c * kChunk, row0 + 16 * lane, b_full + s);
+        uint8_t* st = smem + pf::kBOff + s * kCS * pf::kBStageBytes;
+        if (lane < nbox)
+#pragma unroll
+          for (int h = 0; h < kCS; ++h)
+            tma_2d(st + h * pf::kBStageBytes + lane * 2048, &tmap_b, (c + h) * kChunk, row0 + 16 * lane, b_full + s);
         __syncwarp();
       }
       if (!ok) break;
@@ -426,35 +504,52 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   } else if (kBf16W && warp < 3 + pf::kDequantWarps) {
     // BF16 weights: nothing to dequantise
   } else if (warp < 3 + pf::kDequantWarps) {
-    // ---------------- dequantisers (256 threads; per chunk, one 16-byte segment of each block) ----------------
-    const int tau = threadIdx.x - 96;
+    // ---------------- dequantisers: warp (block j, TMEM lane quarter Q); thread = one weight row ----------------
+    const int j = (warp - 3) >> 2, Q = warp & 3;
+    const int r = 32 * Q + lane;  // the row of block j this thread fills (its TMEM lane)
+    const uint32_t t_row = tmem_base + ((uint32_t)(32 * Q) << 16) + (uint32_t)(pf::kAColT + 32 * j);
     uint32_t ir = 0, ia = 0;
     for (int unit = blockIdx.x; unit < total_units && !*abort_flag; unit += gridDim.x) {
       const int nblk = 2 * (unit % NP) + 1 < a.NB ? 2 : 1;
       bool ok = true;
-      for (int c = 0; c < nch; ++c, ++ir, ++ia) {
-        const int sr = ir % pf::kRawStages, sa = ia % pf::kAStages;
-        if (!mbar_wait(raw_full + sr, (ir / pf::kRawStages) & 1u, abort_flag, a.st, 5) ||
-            !mbar_wait(a_empty + sa, ((ia / pf::kAStages) & 1u) ^ 1u, abort_flag, a.st, 8)) {
+      for (int c = 0; c < nch; c += pf::kKS, ++ia) {  // one TMEM stage: kKS chunks
+        // the stage's packed chunks into registers first (their ring slots go straight back),
+        // then the TMEM stage once the MMAs that read it last have completed
+        RowRaw raw[pf::kKS];
+        for (int h = 0; h < pf::kKS && ok; ++h, ++ir) {
+          const int sr = ir % pf::kRawStages;
+          if (!mbar_wait(raw_full + sr, (ir / pf::kRawStages) & 1u, abort_flag, a.st, 5)) {
+            ok = false;
+            break;
+          }
+          if (j < nblk) load_row_raw(smem + pf::kRawOff + sr * pf::kRawStageBytes + j * pf::kRawBlockBytes, r, raw[h]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(raw_empty + sr);
+        }
+        const int sa = ia % pf::kAStagesT;
+        if (!ok || !mbar_wait(a_empty + sa, ((ia / pf::kAStagesT) & 1u) ^ 1u, abort_flag, a.st, 8)) {
           ok = false;
           break;
         }
-        const uint8_t* raw_stage = smem + pf::kRawOff + sr * pf::kRawStageBytes;
-        const uint32_t a_base = smem_u32(smem + pf::kAOff + sa * pf::kAStageBytes);
-        dequant_segment<kF16>(raw_stage, a_base, tau);
-        if (nblk > 1) dequant_segment<kF16>(raw_stage + pf::kRawBlockBytes, a_base + pf::kABlockBytes, tau);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (tl && warp == 3 && lane == 0 && ia < 256) tl[4 * ia + 1] = globaltimer_ns();
+        tc_fence_after();
+        if (j < nblk) {
+#pragma unroll
+          for (int h = 0; h < pf::kKS; ++h) store_row_tmem<kF16>(raw[h], t_row + (uint32_t)(sa * 64 * pf::kKS + 64 * h));
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        }
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) {
+          if (tl && warp == 3 && ia < 256) tl[4 * ia + 2] = globaltimer_ns();
           mbar_arrive(a_full + sa);
-          mbar_arrive(raw_empty + sr);
         }
       }
       if (!ok) break;
     }
   } else {
-    // ---------------- epilogue (128 threads; warp w reads TMEM lanes 32 (w % 4) ..) ----------------
-    const int quarter = warp & 3;
+    // ---------------- epilogue (256 threads; warp w reads TMEM lanes 32 (w % 4) .. of block (w - 11) / 4) ----------------
+    const int quarter = warp & 3, blk = (warp - 3 - pf::kDequantWarps) >> 2;
     const int i = 32 * quarter + lane;  // accumulator row (TMEM lane)
     uint32_t j = 0;
     for (int unit = blockIdx.x; unit < total_units && !*abort_flag; unit += gridDim.x, ++j) {
@@ -462,16 +557,36 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const int nblk = nb0 + 1 < a.NB ? 2 : 1;
       const int e = a.tile_expert[tile], row0 = a.tile_row0[tile], rows = a.tile_rows[tile];
       const int N = (rows + 15) & ~15;
-      const uint32_t buf = j & 1u, aph = (j >> 1) & 1u;
+      const uint32_t buf = j % nBuf, aph = (j / nBuf) & 1u;
       if (!mbar_wait(accfull + buf, aph, abort_flag, a.st, 6)) break;
+      if (tl && warp == 11 && lane == 0 && j < 16) tl[1024 + 4 * j + 1] = globaltimer_ns();
       tc_fence_after();
       const float* gs = a.gscale + 3 * e;
-      for (int blk = 0; blk < nblk; ++blk) {
+      if (kF16) {  // the tile's row exponents, once per unit, into this warp's shared-memory copy
+        __syncwarp();  // done with the previous unit's
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int rr = 32 * q + lane;
+          pex[rr] = rr < rows ? __ldg(a.pexp_x + row0 + rr) : 0;
+          peh[rr] = rr < rows ? __ldg(a.pexp_h + row0 + rr) : 0;
+        }
+        __syncwarp();
+      }
+      if (blk < nblk) {
         const int nb = nb0 + blk;
         const uint32_t tbase = tmem_base + ((uint32_t)(32 * quarter) << 16) + buf * 256u + (uint32_t)(128 * blk);
-        for (int col = 0; col < N; col += 16) {
-          uint32_t v[16];
-          tmem_ld16(tbase + (uint32_t)col, v);
+        // 32 columns per TMEM round trip: two loads, one wait
+        for (int col2 = 0; col2 < N; col2 += 32) {
+          uint32_t vv[2][16];
+          const bool two = col2 + 16 < N;
+          tmem_ld16_nw(tbase + (uint32_t)col2, vv[0]);
+          if (two) tmem_ld16_nw(tbase + (uint32_t)col2 + 16u, vv[1]);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+          if (hh == 1 && !two) break;
+          const int col = col2 + 16 * hh;
+          const uint32_t* v = vv[hh];
           if (kGateUp) {
             const int R = 128 * nb + i;
             const int f = 8 * (R >> 4) + (R & 7);
@@ -482,8 +597,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             // the x rows entered scaled by 2^-pexp_x (FP16 operands): undo it per column
             float sx[16];
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-              sx[jj] = (kF16 && col + jj < rows) ? __int_as_float((127 + __ldg(a.pexp_x + row0 + col + jj)) << 23) : 1.0f;
+            for (int jj = 0; jj < 16; ++jj) sx[jj] = kF16 ? __int_as_float((127 + pex[col + jj]) << 23) : 1.0f;
             if (a.in_scale != nullptr && e < a.Er) {
               const float is1 = __ldg(a.in_scale + 2 * e + 1), inv6 = act_inv6(is1);
               float hv[16], am[16];
@@ -511,18 +625,22 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 }
               }
             } else {
+              // every lane finishes 8 of the 16 tokens: the gate lane tokens 0..7 (its up
+              // partner, 8 lanes away, sends those u), the up lane tokens 8..15
 #pragma unroll
-              for (int jj = 0; jj < 16; ++jj) {
-                const float mine = __uint_as_float(v[jj]) * sx[jj];
-                const float partner = __shfl_xor_sync(0xffffffffu, mine, 8);
-                if (is_gate && col + jj < rows) {
-                  const float g = gsg * mine, u = gsu * partner;
-                  const size_t o = (size_t)(row0 + col + jj) * a.I + f;
+              for (int jj = 0; jj < 8; ++jj) {
+                const float lo = __uint_as_float(v[jj]) * sx[jj], hi = __uint_as_float(v[8 + jj]) * sx[8 + jj];
+                const float recv = __shfl_xor_sync(0xffffffffu, is_gate ? hi : lo, 8);
+                const int t = is_gate ? jj : 8 + jj;
+                if (col + t < rows) {
+                  const float g = gsg * (is_gate ? lo : recv), u = gsu * (is_gate ? recv : hi);
+                  const size_t o = (size_t)(row0 + col + t) * a.I + f;
+                  // (fast exp and divide: a few FP32 ulp, far below h's FP16 / BF16 rounding)
+                  const float sg = __fdividef(g, 1.0f + __expf(-g));
                   if (kF16)  // h times 2^-pexp_h as the down GEMM's FP16 operand (11 significant bits)
-                    reinterpret_cast<__half*>(a.h)[o] = __float2half_rn(
-                        silu(g) * u * __int_as_float((127 - __ldg(a.pexp_h + row0 + col + jj)) << 23));
+                    reinterpret_cast<__half*>(a.h)[o] = __float2half_rn(sg * u * __int_as_float((127 - peh[col + t]) << 23));
                   else
-                    a.h[o] = __float2bfloat16_rn(silu(g) * u);
+                    a.h[o] = __float2bfloat16_rn(sg * u);
                 }
               }
             }
@@ -545,15 +663,17 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
               for (int jj = 0; jj < 16; ++jj)
                 if (col + jj < rows) {
                   // h row p entered scaled by 2^-pexp_h[p]
-                  const float sh = kF16 ? __int_as_float((127 + __ldg(a.pexp_h + row0 + col + jj)) << 23) : 1.0f;
+                  const float sh = kF16 ? __int_as_float((127 + peh[col + jj]) << 23) : 1.0f;
                   a.y[(size_t)(row0 + col + jj) * a.H + d] = gsd * (__uint_as_float(v[jj]) * sh);
                 }
             }
+          }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
+      if (tl && (warp == 11 || warp == 15) && lane == 0 && j < 16) tl[1024 + 4 * j + (warp == 11 ? 2 : 3)] = globaltimer_ns();
       if (lane == 0) mbar_arrive(accempty + buf);
     }
   }
@@ -618,6 +738,7 @@ cudaError_t launch_prefill_ffn(const LayerDims& d, const uint8_t* blob, const fl
   a.pexp_x = ws.pexp_x;
   a.pexp_h = ws.pexp_h;
   a.checks = d.checks;
+  a.trace = ws.trace;
   a.E = d.E;
   a.R = T * (k + d.S);
   if (!d.linear) {  // gate/up: 2I interleaved rows, K = H (FP16 operands)

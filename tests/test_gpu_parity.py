@@ -182,11 +182,12 @@ def _host_repack_expert(w13_q, w13_s, w2_q, w2_s, H, I):
         else:
             src = rows
         qq, ss = q[src], s[src]                      # rows in packed order
-        # [rb 128][sb 8][r 2][t4 8] x [c][q 4][8 bytes]
+        # [rb 128][sb 8][r 2][t4 8] x [c][q 4][8 bytes]; inside a 16-row sub-block the
+        # segments (t4, q) are stored K group first: slot 8 q + t4
         qb = qq.reshape(N // 128, 8, 2, 8, nch, 4, 8)
-        nib = qb.transpose(0, 4, 1, 3, 5, 2, 6)       # rb, c, sb, t4, q, half, bytes
+        nib = qb.transpose(0, 4, 1, 5, 3, 2, 6)       # rb, c, sb, q, t4, half, bytes
         sb_ = ss.reshape(N // 128, 8, 2, 8, nch, 4)
-        sc = sb_.transpose(0, 4, 1, 3, 5, 2)          # rb, c, sb, t4, q, half
+        sc = sb_.transpose(0, 4, 1, 5, 3, 2)          # rb, c, sb, q, t4, half
         # one tile per (rb, c): its 4096 code bytes, then its 512 scale bytes
         tiles = np.concatenate([nib.reshape(N // 128, nch, 4096), sc.reshape(N // 128, nch, 512)], axis=2)
         return tiles.reshape(-1)
