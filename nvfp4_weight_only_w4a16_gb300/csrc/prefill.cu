@@ -97,6 +97,8 @@ constexpr int kTmemCols = 512;
 constexpr int kAStagesT = 2;
 constexpr int kAColT = 256;
 constexpr int kABars = kAStagesT;
+static_assert(kBStages % kAStagesT == 0 && kBStages >= 2 * kAStagesT,
+              "packed mode: a TMEM slot's previous stage is tracked on the B ring's barriers");
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // a wait longer than 2 s is a fault
 }  // namespace pf
 
@@ -338,7 +340,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       mbar_init(a_empty + s, 1);
     }
     for (int s = 0; s < nBS; ++s) {
-      mbar_init(b_full + s, 1);
+      // packed weights: stage s is ready when its activation tiles have landed and all
+      // eight dequantisers have filled its TMEM operand slot (one wait for the MMA
+      // issuer); b_empty then also frees the TMEM slot (one commit per stage)
+      mbar_init(b_full + s, kBf16W ? 1 : 1 + pf::kDequantWarps);
       mbar_init(b_empty + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -433,7 +438,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         bool ok = true;
         for (int c = 0; c < nch; c += kCS, ++ia, ++ib) {  // one stage: kCS chunks
           const int sa = ia % nAS, sb = ib % nBS;
-          if (!mbar_wait(af + sa, (ia / nAS) & 1u, abort_flag, a.st, 3) ||
+          if ((kBf16W && !mbar_wait(af + sa, (ia / nAS) & 1u, abort_flag, a.st, 3)) ||
               !mbar_wait(b_full + sb, (ib / nBS) & 1u, abort_flag, a.st, 4)) {
             ok = false;
             break;
@@ -464,7 +469,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                 if (nblk > 1) umma_ts(d_tmem + 128u, at + 64u * h + 32u + 8u * kk, bk, idesc, acc);
               }
           }
-          umma_commit(ae + sa);
+          if (kBf16W) umma_commit(ae + sa);
           umma_commit(b_empty + sb);
         }
         if (!ok) break;
@@ -526,8 +531,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(raw_empty + sr);
         }
+        // TMEM slot sa last held stage ia - kAStagesT: wait until its MMAs have completed
+        // (that stage's b_empty commit; B slots cycle kBStages >= kAStagesT, so the phase
+        // parity is that stage's)
         const int sa = ia % pf::kAStagesT;
-        if (!ok || !mbar_wait(a_empty + sa, ((ia / pf::kAStagesT) & 1u) ^ 1u, abort_flag, a.st, 8)) {
+        const uint32_t prev = ia - pf::kAStagesT;
+        if (!ok || (ia >= (uint32_t)pf::kAStagesT &&
+                    !mbar_wait(b_empty + prev % pf::kBStages, (prev / pf::kBStages) & 1u, abort_flag, a.st, 8))) {
           ok = false;
           break;
         }
@@ -542,7 +552,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           if (tl && warp == 3 && ia < 256) tl[4 * ia + 2] = globaltimer_ns();
-          mbar_arrive(a_full + sa);
+          mbar_arrive(b_full + ia % pf::kBStages);
         }
       }
       if (!ok) break;
