@@ -92,7 +92,8 @@ __host__ __device__ constexpr int a_stage_off(int s) {
 }
 constexpr int kDequantWarps = 8;
 constexpr int kEpiWarps = 8;                      // two per TMEM lane quarter: one per weight block
-constexpr int kThreads = (3 + kDequantWarps + kEpiWarps) * 32;  // 19 warps
+constexpr int kMma2Warp = 3 + kDequantWarps + kEpiWarps;       // packed weights: block 1's MMA issuer
+constexpr int kThreads = (kMma2Warp + 1) * 32;                   // 20 warps
 constexpr int kTmemCols = 512;
 constexpr int kAStagesT = 2;
 constexpr int kAColT = 256;
@@ -344,10 +345,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       // eight dequantisers have filled its TMEM operand slot (one wait for the MMA
       // issuer); b_empty then also frees the TMEM slot (one commit per stage)
       mbar_init(b_full + s, kBf16W ? 1 : 1 + pf::kDequantWarps);
-      mbar_init(b_empty + s, 1);
+      mbar_init(b_empty + s, kBf16W ? 1 : 2);  // packed: one commit per MMA issuer
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(accfull + b, 1);
+      mbar_init(accfull + b, kBf16W ? 1 : 2);
       mbar_init(accempty + b, pf::kEpiWarps);
     }
     *abort_flag = 0;
@@ -420,9 +421,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (!kBf16W && warp == pf::kMma2Warp)) {
     if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+      // ---------------- MMA issuers ----------------
+      // BF16 weights: warp 1 issues both blocks.  Packed weights: warp 1 issues block 0's
+      // MMAs and warp kMma2Warp block 1's, into their own accumulators -- while one
+      // issuer stalls on a wait or a commit, the other's MMAs keep the tensor pipe busy
+      const int mb = warp == 1 ? 0 : 1;
       uint32_t ia = 0, ib = 0, j = 0;
       for (int unit = blockIdx.x; unit < total_units && !*abort_flag; unit += gridDim.x, ++j) {
         const int tile = unit / NP, nb0 = 2 * (unit % NP);
@@ -432,7 +437,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const uint32_t idesc = kF16 ? idesc_f16(128, N) : idesc_bf16(128, N);
         const uint32_t buf = j % nBuf, aph = (j / nBuf) & 1u;
         if (!mbar_wait(accempty + buf, aph ^ 1u, abort_flag, a.st, 2)) break;
-        if (tl && j < 16) tl[1024 + 4 * j] = globaltimer_ns();
+        if (tl && mb == 0 && j < 16) tl[1024 + 4 * j] = globaltimer_ns();
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * 256u;  // block b's accumulator at + 128 b
         bool ok = true;
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             ok = false;
             break;
           }
-          if (tl && ia < 256) tl[4 * ia] = globaltimer_ns();
+          if (tl && mb == 0 && ia < 256) tl[4 * ia] = globaltimer_ns();
           tc_fence_after();
           const uint64_t bd = sw128_desc(smem_u32(smem + pf::kBOff + sb * kCS * pf::kBStageBytes));
           if (kBf16W) {
@@ -455,18 +460,17 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
               if (nblk > 1)  // block 1's operand tile is 16 KB further (1024 in the 16-byte units)
                 umma_bf16(d_tmem + 128u, ad + (uint64_t)(pf::kABlockBytes >> 4) + 2u * kk, bd + 2u * kk, idesc, acc);
             }
-          } else {
-            // TMEM operand stage sa: chunk h, block j, K step kk at columns + 64 h + 32 j + 8 kk;
+          } else if (mb < nblk) {
+            // TMEM operand stage sa: chunk h, block mb, K step kk at columns + 64 h + 32 mb + 8 kk;
             // the stage's chunk h of B is 16 KB (1024 16-byte units) further
-            const uint32_t at = tmem_base + (uint32_t)(pf::kAColT + sa * 64 * pf::kKS);
+            const uint32_t at = tmem_base + (uint32_t)(pf::kAColT + sa * 64 * pf::kKS + 32 * mb);
+            const uint32_t dt = d_tmem + 128u * (uint32_t)mb;
 #pragma unroll
             for (int h = 0; h < pf::kKS; ++h)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t acc = (c | h | kk) != 0 ? 1u : 0u;
-                const uint64_t bk = bd + (uint64_t)(h * (pf::kBStageBytes >> 4)) + 2u * kk;
-                umma_ts(d_tmem, at + 64u * h + 8u * kk, bk, idesc, acc);
-                if (nblk > 1) umma_ts(d_tmem + 128u, at + 64u * h + 32u + 8u * kk, bk, idesc, acc);
+                umma_ts(dt, at + 64u * h + 8u * kk, bd + (uint64_t)(h * (pf::kBStageBytes >> 4)) + 2u * kk, idesc, acc);
               }
           }
           if (kBf16W) umma_commit(ae + sa);
@@ -506,8 +510,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       }
       if (!ok) break;
     }
-  } else if (kBf16W && warp < 3 + pf::kDequantWarps) {
-    // BF16 weights: nothing to dequantise
+  } else if (warp == pf::kMma2Warp || (kBf16W && warp < 3 + pf::kDequantWarps)) {
+    // BF16 weights: one MMA issuer, nothing to dequantise
   } else if (warp < 3 + pf::kDequantWarps) {
     // ---------------- dequantisers: warp (block j, TMEM lane quarter Q); thread = one weight row ----------------
     const int j = (warp - 3) >> 2, Q = warp & 3;
