@@ -36,10 +36,11 @@ __device__ __forceinline__ void report(DeviceStatus* st, unsigned int flag, unsi
 //   (byte j of each half holds elements 2j / 2j+1 in its low / high nibble).
 //   Scales: 2 bytes at 4096 + sb*64 + P(t)*2 of the tile: the E4M3 scale of
 //   the two rows' 16-element group.
-//   P(t) = 8*(t%4) + t/4 orders a sub-block's segments by K group: a lane
-//   reading its mma fragment (segment t) and a thread reading one row's four
-//   groups (rows r, r+8 of group q: 16-byte slots 8q .. 8q+7) both hit every
-//   shared-memory bank once.
+//   P(t) = 8*(t%4) + (t/4 + 2*(t%4)) % 8 orders a sub-block's segments by K
+//   group (group q in 16-byte slots 8q .. 8q+7, rotated by 2q): each 8-lane
+//   phase of a 16-byte fragment read (segments t = 8p .. 8p+7) and each
+//   thread-per-row read of one group (rows r, r+8 of group q) cover all 32
+//   shared-memory banks once.
 //   Segment s = ((rb*nch + c)*8 + sb)*32 + t names one lane's 16 code bytes
 //   and 2 scale bytes (code_byte / scale_byte below).
 //   The gate/up matrix is stored row-interleaved: packed row 16g+r is gate
@@ -51,7 +52,7 @@ constexpr int kBlockRows = 128;
 constexpr int kTileCodes = 4096;  // one tile's codes
 constexpr int kTileBytes = 4608;  // codes + scales
 
-__host__ __device__ inline int seg_pos(int t) { return 8 * (t & 3) + (t >> 2); }  // P(t)
+__host__ __device__ inline int seg_pos(int t) { return 8 * (t & 3) + (((t >> 2) + 2 * (t & 3)) & 7); }  // P(t)
 __host__ __device__ inline size_t code_byte(size_t s) {
   return (s >> 8) * kTileBytes + ((s >> 5) & 7) * 512 + (size_t)seg_pos((int)(s & 31)) * 16;
 }

@@ -256,7 +256,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 // One weight row's bytes of one packed chunk (a 4608-byte tile: codes, then
 // scales): its four 16-element groups' codes and E4M3 scales.  Row r sits in
 // 16-row group r / 16 as the low (r % 16 < 8) or high half of segments
-// 4 (r % 8) + q, stored at slots 8 q + r % 8.
+// t = 4 (r % 8) + q, stored at slots seg_pos(t).
 struct RowRaw {
   uint2 c[4];
   uint32_t s[4];
@@ -265,7 +265,7 @@ __device__ __forceinline__ void load_row_raw(const uint8_t* tile, int r, RowRaw&
   const int g16 = r >> 4, hf = (r >> 3) & 1, rr = r & 7;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const int p = 8 * q + rr;
+    const int p = seg_pos(4 * rr + q);
     w.c[q] = *reinterpret_cast<const uint2*>(tile + g16 * 512 + p * 16 + 8 * hf);
     w.s[q] = tile[4096 + g16 * 64 + p * 2 + hf];
   }

@@ -120,9 +120,16 @@ def test_linear_packed_blob_is_the_down_layout_with_zero_padding():
     s = np.zeros((Np, K // 16), np.uint8)
     q[:N], s[:N] = inp.w_q, inp.w_s
     nch = K // 64
-    # per tile [rb][c]: codes [sb 8][q 4][t4 8][half 2][8 bytes], then the scales in the same order
-    nib = q.reshape(Np // 128, 8, 2, 8, nch, 4, 8).transpose(0, 4, 1, 5, 3, 2, 6).reshape(Np // 128, nch, 4096)
-    sc = s.reshape(Np // 128, 8, 2, 8, nch, 4).transpose(0, 4, 1, 5, 3, 2).reshape(Np // 128, nch, 512)
+    # per tile [rb][c]: codes [sb 8][slot 32][half 2][8 bytes], then the scales in the same order;
+    # segment t = 4 t4 + q of a 16-row sub-block sits at slot 8 q + (t4 + 2 q) % 8
+    seg = q.reshape(Np // 128, 8, 2, 8, nch, 4, 8).transpose(0, 4, 1, 3, 5, 2, 6).reshape(Np // 128, nch, 8, 32, 16)
+    sseg = s.reshape(Np // 128, 8, 2, 8, nch, 4).transpose(0, 4, 1, 3, 5, 2).reshape(Np // 128, nch, 8, 32, 2)
+    t = np.arange(32)
+    slot = 8 * (t % 4) + (t // 4 + 2 * (t % 4)) % 8
+    nib_s, sc_s = np.empty_like(seg), np.empty_like(sseg)
+    nib_s[:, :, :, slot] = seg
+    sc_s[:, :, :, slot] = sseg
+    nib, sc = nib_s.reshape(Np // 128, nch, 4096), sc_s.reshape(Np // 128, nch, 512)
     assert np.array_equal(blob, np.concatenate([nib, sc], axis=2).reshape(-1))
 
 

@@ -182,12 +182,18 @@ def _host_repack_expert(w13_q, w13_s, w2_q, w2_s, H, I):
         else:
             src = rows
         qq, ss = q[src], s[src]                      # rows in packed order
-        # [rb 128][sb 8][r 2][t4 8] x [c][q 4][8 bytes]; inside a 16-row sub-block the
-        # segments (t4, q) are stored K group first: slot 8 q + t4
+        # [rb 128][sb 8][r 2][t4 8] x [c][q 4][8 bytes]; segment t = 4 t4 + q of a 16-row
+        # sub-block is stored at slot 8 q + (t4 + 2 q) % 8
         qb = qq.reshape(N // 128, 8, 2, 8, nch, 4, 8)
-        nib = qb.transpose(0, 4, 1, 5, 3, 2, 6)       # rb, c, sb, q, t4, half, bytes
+        seg = qb.transpose(0, 4, 1, 3, 5, 2, 6).reshape(N // 128, nch, 8, 32, 16)   # rb, c, sb, t, 16 bytes
         sb_ = ss.reshape(N // 128, 8, 2, 8, nch, 4)
-        sc = sb_.transpose(0, 4, 1, 5, 3, 2)          # rb, c, sb, q, t4, half
+        sseg = sb_.transpose(0, 4, 1, 3, 5, 2).reshape(N // 128, nch, 8, 32, 2)     # rb, c, sb, t, 2 bytes
+        t = np.arange(32)
+        slot = 8 * (t % 4) + (t // 4 + 2 * (t % 4)) % 8
+        nib = np.empty_like(seg)
+        nib[:, :, :, slot] = seg
+        sc = np.empty_like(sseg)
+        sc[:, :, :, slot] = sseg
         # one tile per (rb, c): its 4096 code bytes, then its 512 scale bytes
         tiles = np.concatenate([nib.reshape(N // 128, nch, 4096), sc.reshape(N // 128, nch, 512)], axis=2)
         return tiles.reshape(-1)
