@@ -61,6 +61,8 @@ constexpr int kThreads = (kConsumers + 2) * 32;   // + one producer warp + one s
 constexpr int kProducer = kConsumers;             // the producer's warp index
 constexpr int kSignaller = kConsumers + 1;        // the signal warp's index
 constexpr int kSig = 8;                           // depth of each group's completion queue
+constexpr int kSigCombineT = 4;                   // up to this many tokens the signal warp that completes
+                                                  // an output slice combines it; beyond, every consumer warp
 #ifndef NVFP4_MOE_DEC_CPS
 #define NVFP4_MOE_DEC_CPS 8
 #endif
@@ -260,10 +262,13 @@ __device__ __forceinline__ void stream_route_issue(const StreamArgs& a, float (&
 }
 
 // `mid` runs on every thread between the expert choice and the tables (the
-// warps that choose no experts do their other early work there).
+// warps that choose no experts do their other early work there).  Warp
+// `early` (or none: -1) leaves as soon as the touched-expert list is built --
+// the weight producer needs nothing else -- and the other warps finish the
+// tables behind a named barrier.
 template <class Mid>
 __device__ void stream_route(const StreamArgs& a, StreamSmem& ss, float (&val)[2][8], unsigned long long* tr,
-                             Mid&& mid) {
+                             Mid&& mid, int early) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
   const int T = a.T, k = a.k, E = a.E, Er = a.Er, topk = a.topk, R = T * k;
   uint32_t key[2][8];
@@ -343,7 +348,11 @@ __device__ void stream_route(const StreamArgs& a, StreamSmem& ss, float (&val)[2
     }
   }
   __syncthreads();
-  for (int r = tid; r < R; r += blockDim.x) {  // expert-major position: rank among the earlier rows of the same expert
+  if (warp == early) return;
+  // the remaining threads, renumbered without warp `early`
+  const int nthr = (int)blockDim.x - (early >= 0 ? 32 : 0);
+  const int idx = (early >= 0 && warp > early) ? tid - 32 : tid;
+  for (int r = idx; r < R; r += nthr) {  // expert-major position: rank among the earlier rows of the same expert
     const int e = ss.ids[r];
     int rank = 0;
     for (int j = 0; j < r; ++j) rank += (ss.ids[j] == e);
@@ -352,16 +361,17 @@ __device__ void stream_route(const StreamArgs& a, StreamSmem& ss, float (&val)[2
     ss.inv[r] = pos;
     atomicOr(&ss.tch_mask[ss.slot_of[e]], 1u << (r / k));
   }
-  __syncthreads();
+  if (early >= 0) asm volatile("bar.sync 3, %0;" ::"r"(nthr) : "memory");
+  else __syncthreads();
   if (blockIdx.x == 0) {  // the tables, for inspection
-    for (int i = tid; i < R; i += blockDim.x) {
+    for (int i = idx; i < R; i += nthr) {
       a.ids[i] = ss.ids[i];
       a.wts[i] = ss.wts[i];
       a.perm[i] = ss.perm[i];
       a.inv[i] = ss.inv[i];
     }
-    for (int i = tid; i <= E; i += blockDim.x) a.offsets[i] = ss.off[i];
-    if (tid == 0 && ss.nan) atomicAdd(&a.st->nan_logits, (unsigned)ss.nan);
+    for (int i = idx; i <= E; i += nthr) a.offsets[i] = ss.off[i];
+    if (idx == 0 && ss.nan) atomicAdd(&a.st->nan_logits, (unsigned)ss.nan);
   }
 }
 
@@ -560,49 +570,58 @@ __device__ void epilogue_down(const StreamArgs& a, const StreamSmem& ss, int u, 
     }
 }
 
-// The combine, spread over every consumer warp of the grid: task (128-wide
-// slice b, token t) waits until slice b is complete for every touched expert
-// (U down items), then out[t][slice] = sum_j w[t][j] *
-// y[pos(t, j)][slice] in slot order j = 0..k-1 (lane l: features 4l..4l+3).
-__device__ void combine_tasks(const StreamArgs& a, const StreamSmem& ss, int wg, int W, int lane) {
-  const int nsl = a.H / 128, target = ss.U;
-  for (int task = wg; task < nsl * a.T; task += W) {
-    const int t = task / nsl, b = task - t * nsl;
-    int ok = 1;
-    if (lane == 0) ok = wait_count(a.cmb + b, target, a.st, 400 + (unsigned)b);
-    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-    __threadfence();
-    const int d = 128 * b + 4 * lane;
-    float4 yy[dstr::kMaxSlots];
+// The combine of one 128-wide output slice b for token t, on one warp (lane l:
+// features 128 b + 4l .. 4l+3): out[t][slice] = sum_j w[t][j] * y[pos(t, j)][slice]
+// in slot order j = 0..k-1.  The caller has seen slice b complete for every
+// touched expert (U down items counted in, then a fence).
+__device__ void combine_slice(const StreamArgs& a, const StreamSmem& ss, int b, int t, int lane) {
+  const int d = 128 * b + 4 * lane;
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  for (int j0 = 0; j0 < a.k; j0 += 4) {  // four slots' loads in flight at a time
+    float4 yy[4];
 #pragma unroll
-    for (int j = 0; j < dstr::kMaxSlots; ++j)
-      if (j < a.k) {
-        int pos = ss.inv[t * a.k + j];
+    for (int u = 0; u < 4; ++u)
+      if (j0 + u < a.k) {
+        int pos = ss.inv[t * a.k + j0 + u];
         if (a.checks && (pos < 0 || pos >= a.T * a.k)) {
           report(a.st, kFlagBounds, 803);
           pos = 0;
         }
-        yy[j] = __ldcg(reinterpret_cast<const float4*>(a.y + (size_t)pos * a.H + d));
+        yy[u] = __ldcg(reinterpret_cast<const float4*>(a.y + (size_t)pos * a.H + d));
       }
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-    for (int j = 0; j < dstr::kMaxSlots; ++j)
-      if (j < a.k) {
-        const float w = ss.wts[t * a.k + j];
-        s0 = fmaf(w, yy[j].x, s0);
-        s1 = fmaf(w, yy[j].y, s1);
-        s2 = fmaf(w, yy[j].z, s2);
-        s3 = fmaf(w, yy[j].w, s3);
+    for (int u = 0; u < 4; ++u)
+      if (j0 + u < a.k) {
+        const float w = ss.wts[t * a.k + j0 + u];
+        s0 = fmaf(w, yy[u].x, s0);
+        s1 = fmaf(w, yy[u].y, s1);
+        s2 = fmaf(w, yy[u].z, s2);
+        s3 = fmaf(w, yy[u].w, s3);
       }
-    if (a.out_f32) {
-      *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + (size_t)t * a.H + d) = make_float4(s0, s1, s2, s3);
-    } else {
-      const __nv_bfloat162 p0 = __floats2bfloat162_rn(s0, s1), p1 = __floats2bfloat162_rn(s2, s3);
-      uint2 v;
-      v.x = *reinterpret_cast<const uint32_t*>(&p0);
-      v.y = *reinterpret_cast<const uint32_t*>(&p1);
-      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + (size_t)t * a.H + d) = v;
-    }
+  }
+  if (a.out_f32) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + (size_t)t * a.H + d) = make_float4(s0, s1, s2, s3);
+  } else {
+    const __nv_bfloat162 p0 = __floats2bfloat162_rn(s0, s1), p1 = __floats2bfloat162_rn(s2, s3);
+    uint2 v;
+    v.x = *reinterpret_cast<const uint32_t*>(&p0);
+    v.y = *reinterpret_cast<const uint32_t*>(&p1);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + (size_t)t * a.H + d) = v;
+  }
+}
+
+// For more than kSigCombineT tokens the combine is spread over every consumer
+// warp of the grid instead: task (slice b, token t) waits until slice b is
+// complete for every touched expert, then combines it.
+__device__ void combine_tasks(const StreamArgs& a, const StreamSmem& ss, int wg, int W, int lane) {
+  const int nsl = a.H / 128;
+  for (int task = wg; task < nsl * a.T; task += W) {
+    const int t = task / nsl, b = task - t * nsl;
+    int ok = 1;
+    if (lane == 0) ok = wait_count(a.cmb + b, ss.U, a.st, 400 + (unsigned)b);
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    __threadfence();
+    combine_slice(a, ss, b, t, lane);
   }
 }
 
@@ -686,7 +705,9 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
       __threadfence();
       for (int c = blockIdx.x; c < nchH; c += gridDim.x) atomicAdd(a.x_ready + c, 1);
     }
-  });  // ends with __syncthreads: tables and barriers are ready
+  }, a.route_only ? -1 : dstr::kProducer);
+  // the barriers and the touched-expert list are ready; except in the producer warp, so
+  // are the positions, masks and (CTA 0) the tables written out
   if (a.route_only) return;
   if (tr && tid == 0) tr[1] = gtime();
 
@@ -865,13 +886,21 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
           open[g] = false;
           continue;
         }
+        // a down item completes output slice b for its expert; the item that completes
+        // it for the last touched expert combines the slice here, at once
+        const int b = v < n_gu ? -1 : (v - n_gu) % dn_per;
+        int last = 0;
         if (lane == 0) {
           __threadfence();
-          if (v < n_gu) atomicAdd(a.done_c + (size_t)(v / gu_per) * nchI + (v % gu_per), 1);
-          else atomicAdd(a.cmb + (v - n_gu) % dn_per, 1);
+          if (b < 0) atomicAdd(a.done_c + (size_t)(v / gu_per) * nchI + (v % gu_per), 1);
+          else last = atomicAdd(a.cmb + b, 1) == ss.U - 1;
           mb_arrive(&ss.sig_empty[g][q]);
         }
-        __syncwarp();
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last && T <= dstr::kSigCombineT) {
+          __threadfence();  // the other CTAs' y rows, fenced before their counts
+          for (int t = 0; t < T; ++t) combine_slice(a, ss, b, t, lane);
+        }
         ++n[g];
       }
       if (any) {
@@ -999,7 +1028,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
       tr[10] = w_full;
       tr[11] = w_epi;
     }
-    if (!is_aborted(a.st))
+    if (T > dstr::kSigCombineT && !is_aborted(a.st))
       combine_tasks(a, ss, (int)blockIdx.x * dstr::kConsumers + warp, (int)gridDim.x * dstr::kConsumers, lane);
   }
 
