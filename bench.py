@@ -344,8 +344,9 @@ def measure_layer(name, steps, warmup, dev, flush, barrier, ws=1, router=False, 
     layer_bytes = distinct * cfg.expert_bytes + T * H * 2 * 2 + T * E * 4
     layer_flops = 2.0 * T * (k + S) * 3 * H * I
     if decode:
-        # decode: one kernel streams every touched expert's weights once
-        kernel = "decode_stream_kernel"
+        # decode: one kernel streams every touched expert's weights once (the W4A4 variant
+        # runs on the earlier decode kernel)
+        kernel = "decode_fused_kernel" if w4a4 else "decode_stream_kernel"
         kern_ms = stage_ms[1]
         algo = layer_bytes
         achieved = algo / (kern_ms / 1e3) / 1e9
@@ -353,7 +354,7 @@ def measure_layer(name, steps, warmup, dev, flush, barrier, ws=1, router=False, 
         peak, peak_src = _peak("hbm_gbs", 6800.0)
         traffic = _traffic_for(os.path.join(ROOT, "nvfp4_weight_only_w4a16_gb300", "csrc", "decode_stream.cu")) \
             if name == WORKLOAD and not (router or w4a4) else None
-        stages = {"decode_stream_kernel (route + gate/up + down + combine)": kern_ms}
+        stages = {kernel + " (route + gate/up + down + combine)": kern_ms}
     else:
         # prefill: the gate/up GEMM's dense flops on the tensor cores
         kernel = "prefill_gemm_kernel<gate/up>"
