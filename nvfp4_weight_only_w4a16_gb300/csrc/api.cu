@@ -339,6 +339,7 @@ nvfp4_moe_status create_handle(const nvfp4_moe_config* c, bool linear, int lin_n
   cv.add(&w.wctr, 1);
   cv.add(&w.done_c, maxU * (I / 64));
   cv.add(&w.x_ready, H / 64);
+  cv.add(&w.logit_ready, 1);
   cv.add(&w.blk_counts, ncta * E, true);
   cv.add(&w.blk_base, ncta * E, true);
   cv.add(&w.local_rank, Rm, true);
@@ -575,7 +576,9 @@ nvfp4_moe_status forward_impl(nvfp4_moe* h, const void* logits, int T, int top_k
   LayerDims d = dims_of(h);
   const float* gsc = h->w4a4 ? h->gs_eff : h->gscale;  // W4A4: input scales folded in
   cudaError_t e;
-  if (routed) {  // the router linear, timed with route + permute
+  // the streaming decode kernel computes the router logits itself (one launch for the layer)
+  const bool fused_router = routed && path == NVFP4_MOE_PATH_DECODE && use_stream(h, d, T, top_k);
+  if (routed && !fused_router) {  // the router linear, timed with route + permute
     const int Er = h->cfg.num_experts, H = h->cfg.hidden;
     if (T <= kDecodeMaxTokens) {
       e = launch_router_gemv(x, h->w_router, T, Er, H, h->ws.logits, st);
@@ -588,6 +591,8 @@ nvfp4_moe_status forward_impl(nvfp4_moe* h, const void* logits, int T, int top_k
         e = launch_router_gemm(x_map, h->w_router_map, Er, H, h->num_sms, h->ws.ones3, h->ws, h->ws.logits, st);
     }
     if (e != cudaSuccess) return cuda_fail(h, e, "router launch");
+  }
+  if (routed) {
     logits = h->ws.logits;
     d.logits_bf16 = 0;
   }
@@ -595,7 +600,8 @@ nvfp4_moe_status forward_impl(nvfp4_moe* h, const void* logits, int T, int top_k
     // one fused kernel: its time is reported as the gate/up stage
     if (ev[1]) cudaEventRecord(ev[1], st);
     const bool stream = use_stream(h, d, T, top_k);
-    e = stream ? launch_decode_stream(d, h->blob, gsc, logits, x, T, top_k, out, 0, h->num_sms, h->ws, h->fault, st)
+    e = stream ? launch_decode_stream(d, h->blob, gsc, logits, x, T, top_k, out, 0, h->num_sms, h->ws, h->fault, st,
+                                      fused_router ? h->w_router : nullptr)
                : launch_decode_forward(d, h->blob, gsc, logits, x, T, top_k, out, 0, h->num_sms, h->ws, h->fault, st);
     h->last_hsrc = stream ? 1 : 0;
     if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");

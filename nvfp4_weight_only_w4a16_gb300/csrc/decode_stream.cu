@@ -90,6 +90,7 @@ struct StreamSmem {
   unsigned tch_mask[dstr::kMaxE];  // tokens routed to the touched expert
   float cmax[2][8][16];             // gate/up epilogue, per group: per 16-row group, per column, max |h|
   int meta[dstr::kMaxStages][4];   // item, stage within the item, chunks in the stage
+  float rpart[dstr::kConsumers][16];  // router linear: per consumer warp, per token
   int sig[2][dstr::kSig];          // per group: completed items for the signal warp (-1: no more)
   int U, nan, last_cta;
   alignas(8) uint64_t full[dstr::kMaxStages];
@@ -108,6 +109,9 @@ struct StreamArgs {
   RouteParams rp;
   const void* logits;
   int logits_bf16;
+  const __nv_bfloat16* router_w;  // BF16 [Er][H]: the kernel computes the logits (else NULL)
+  float* logits_w;                // [T][Er] FP32: where it writes them
+  int32_t* logit_ready;           // experts whose logits are written (reset by the last CTA)
   const __nv_bfloat16* x;
   void* out;
   int out_f32;
@@ -252,13 +256,78 @@ __device__ __forceinline__ void convert_chunk_row(uint32_t two_bf16, uint8_t* ds
 // touched-expert list with each expert's token mask.  CTA 0 also writes the
 // tables out.
 // ---------------------------------------------------------------------------
+// The router linear inside the kernel: CTA c computes the logits of experts
+// c, c + grid, ... for every token (logit = sum_h x[t][h] * W_r[e][h] in FP32,
+// BF16 inputs; the 16 consumer warps split H, then sum in warp order), writes
+// them to logits_w, and counts them in; every CTA then waits (bounded) until
+// all Er experts' logits are in.  All threads of the CTA call it.
+__device__ void stream_router(const StreamArgs& a, StreamSmem& ss) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, T = a.T, H = a.H;
+  int mine = 0;
+  for (int e = blockIdx.x; e < a.Er; e += gridDim.x, ++mine) {
+    if (warp < dstr::kConsumers) {
+      float acc[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) acc[t] = 0.f;
+      const uint4* wr = reinterpret_cast<const uint4*>(a.router_w + (size_t)e * H);
+      for (int p = tid; p < H / 8; p += dstr::kConsumers * 32) {
+        const uint4 wv = __ldg(wr + p);
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          if (t >= T) break;
+          const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * H) + p);
+          const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[t] = fmaf(__uint_as_float(xx[q] << 16), __uint_as_float(ww[q] << 16), acc[t]);
+            acc[t] = fmaf(__uint_as_float(xx[q] & 0xFFFF0000u), __uint_as_float(ww[q] & 0xFFFF0000u), acc[t]);
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        if (t >= T) break;
+        float v = acc[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) ss.rpart[warp][t] = v;
+      }
+    }
+    __syncthreads();
+    if (tid < T) {
+      float v = 0.f;
+      for (int w = 0; w < dstr::kConsumers; ++w) v += ss.rpart[w][tid];
+      a.logits_w[(size_t)tid * a.Er + e] = v;
+      __threadfence();
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    if (mine) atomicAdd(a.logit_ready, mine);
+    wait_count(a.logit_ready, a.Er, a.st, 900);
+  }
+  __syncthreads();
+}
+
 // The logit loads of this warp's tokens (issued first thing, so their latency
 // overlaps everything else the kernel does before routing).
 __device__ __forceinline__ void stream_route_issue(const StreamArgs& a, float (&val)[2][8]) {
-  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
-  for (int r = 0; r < 2; ++r)
-    if (warp + r * nw < a.T) warp_issue_logits(a.logits, a.logits_bf16, a.Er, warp + r * nw, val[r]);
+  for (int r = 0; r < 2; ++r) {
+    const int t = warp + r * nw;
+    if (t >= a.T) continue;
+    if (a.router_w) {  // written by this kernel's other CTAs: read from L2
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        val[r][i] = e < a.Er ? __ldcg(a.logits_w + (size_t)t * a.Er + e) : 0.f;
+      }
+    } else {
+      warp_issue_logits(a.logits, a.logits_bf16, a.Er, t, val[r]);
+    }
+  }
 }
 
 // `mid` runs on every thread between the expert choice and the tables (the
@@ -653,7 +722,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
   unsigned long long* tl = (a.trace && blockIdx.x < 8) ? a.trace + (size_t)gridDim.x * 16 + blockIdx.x * 2048 : nullptr;
   if (tr && tid == 0) tr[0] = gtime();
   float lval[2][8];
-  stream_route_issue(a, lval);
+  if (!a.router_w) stream_route_issue(a, lval);
 
   // this CTA's share of the x conversion: token tx = 15 - warp of its chunks (chunk
   // blockIdx.x + i * gridDim.x), on the consumer warps from the top down -- for T <= 8
@@ -685,6 +754,10 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
         mb_init(&ss.red_empty[p][q], 1);
       }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (a.router_w) {  // the router linear first, then the logits it wrote
+    stream_router(a, ss);
+    stream_route_issue(a, lval);
   }
   stream_route(a, ss, lval, tr, [&] {
     if (!xconv) return;
@@ -1054,6 +1127,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
   if (tid == 0) {
     *a.wctr = 0;
     *a.exit_cnt = 0;
+    if (a.router_w) *a.logit_ready = 0;
   }
 }
 
@@ -1139,7 +1213,7 @@ cudaError_t stream_prepare_device(int dev, int* smem_max) {
 
 cudaError_t launch_decode_stream(const LayerDims& d, const uint8_t* blob, const float* gscale, const void* logits,
                                  const void* x, int T, int k, void* out, int route_only, int num_sms,
-                                 const Workspace& ws, int fault, cudaStream_t st) {
+                                 const Workspace& ws, int fault, cudaStream_t st, const void* router_w) {
   if (!stream_supported(d, T, k)) return cudaErrorInvalidValue;
   int dev = 0, smem_max = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1164,6 +1238,14 @@ cudaError_t launch_decode_stream(const LayerDims& d, const uint8_t* blob, const 
   a.rp = d.rp;
   a.logits = logits;
   a.logits_bf16 = d.logits_bf16;
+  if (router_w) {
+    if (!x || route_only || !ws.logits || !ws.logit_ready) return cudaErrorInvalidValue;
+    a.router_w = reinterpret_cast<const __nv_bfloat16*>(router_w);
+    a.logits_w = ws.logits;
+    a.logit_ready = ws.logit_ready;
+    a.logits = ws.logits;
+    a.logits_bf16 = 0;
+  }
   a.x = reinterpret_cast<const __nv_bfloat16*>(x);
   a.out = out;
   a.out_f32 = d.out_f32;

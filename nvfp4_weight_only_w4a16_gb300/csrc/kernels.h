@@ -49,6 +49,7 @@ struct Workspace {
   int32_t* wctr;        // [1] work items claimed beyond the first one per CTA
   int32_t* done_c;      // [maxU][I/64] gate/up epilogue warps done per (touched expert, chunk of h)
   int32_t* x_ready;     // [H/64] tokens of act_x converted per chunk
+  int32_t* logit_ready; // [1] router experts whose logits the streaming decode kernel has written
   DeviceStatus* status;
   DeviceStatus* status_sticky;  // optional (decode): a status word that outlives the launch's own
   float* logits;         // [max_tokens][Er] router logits (nvfp4_moe_forward_routed)
@@ -122,9 +123,11 @@ cudaError_t decode_prepare_device(int dev, int* smem_max);
 // whether a layer and step can take it (W4A16 routed experts, not a dense
 // linear, top_k + shared <= 17).
 bool stream_supported(const LayerDims& d, int T, int k);
+// router_w (BF16 [Er][H], or NULL): the kernel computes the router logits itself into ws.logits
+// (logits is then ignored).
 cudaError_t launch_decode_stream(const LayerDims& d, const uint8_t* blob, const float* gscale, const void* logits,
                                  const void* x, int T, int k, void* out, int route_only, int num_sms,
-                                 const Workspace& ws, int fault, cudaStream_t st);
+                                 const Workspace& ws, int fault, cudaStream_t st, const void* router_w = nullptr);
 cudaError_t stream_prepare_device(int dev, int* smem_max);
 size_t stream_act_h_bytes(int I, int rows);
 // The hidden activations the last forward consumed, as FP32 [R][I]: src 0 --

@@ -108,6 +108,7 @@ size_t carve(uint8_t* base, int E, int H, int I, int T, int k, int num_sms, Work
   w.wctr = r.take<int32_t>(b, 1);
   w.done_c = r.take<int32_t>(b, maxU * (I / 64));
   w.x_ready = r.take<int32_t>(b, H / 64);
+  w.logit_ready = r.take<int32_t>(b, 1);
   w.status = r.take<DeviceStatus>(b, 1);
   *zero_end = (r.off + 255) & ~size_t(255);
   // no split-K partial-sum buffers here: with part_gu == nullptr the decode
