@@ -88,7 +88,8 @@ struct StreamSmem {
   int tch_r0[dstr::kMaxE];
   int tch_m[dstr::kMaxE];
   unsigned tch_mask[dstr::kMaxE];  // tokens routed to the touched expert
-  float cmax[2][8][16];             // gate/up epilogue, per group: per 16-row group, per column, max |h|
+  float cmax[2][2][8][16];          // gate/up epilogue, [parity][group]: per 16-row group, per column, max |h|
+  int epi_cnt[2];                   // per group: warps arrived at its gate/up epilogues (8 per epilogue)
   int meta[dstr::kMaxStages][4];   // item, stage within the item, chunks in the stage
   float rpart[dstr::kConsumers][16];  // router linear: per consumer warp, per token
   int sig[2][dstr::kSig];          // per group: completed items for the signal warp (-1: no more)
@@ -136,7 +137,6 @@ struct StreamArgs {
   int fault;          // 1: the producer issues nothing (tests the bounded waits)
   int stages, stage_bytes;
   int checks;         // 1: check table-derived indices (kFlagBounds; the access is skipped)
-  int pf_dist;        // stages ahead of the ring whose weights are prefetched into L2 (0: none)
   int cps;            // 64-wide K chunks per stage (kCPS, or fewer for small H and I: two or more stages per item)
   unsigned long long* trace;  // optional: [cta][16] phase stamps (see decode_stream_kernel)
 };
@@ -170,9 +170,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                "l"(src), "r"(bytes), "r"(saddr(bar))
                : "memory");
 }
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ uint64_t gtime() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -185,9 +182,6 @@ __device__ __forceinline__ int ld_acq(const int32_t* p) {
 }
 __device__ __forceinline__ bool is_aborted(const DeviceStatus* st) {
   return (*reinterpret_cast<const volatile unsigned*>(&st->flags) & kFlagTimeout) != 0;
-}
-__device__ __forceinline__ void named_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 __device__ __forceinline__ float exp2i(int p) { return __int_as_float((127 + max(-126, min(127, p))) << 23); }
 
@@ -570,7 +564,8 @@ __device__ __forceinline__ void compute_stage(const StageRegs<NG, NC>& r, float 
 // chunk rows with their scale in act_h (published by the signal warp).
 template <int NG>
 __device__ void epilogue_gateup(const StreamArgs& a, StreamSmem& ss, int u, int b, int sb, int grp,
-                                const float (&acc)[NG][4], int lane) {
+                                const float (&acc)[NG][4], int lane, uint32_t nepi) {
+  const int par = (int)(nepi & 1u);  // this group's nepi-th gate/up epilogue
   const int e = ss.tch_e[u], row0 = ss.tch_r0[u], m_u = ss.tch_m[u];
   const unsigned mask = ss.tch_mask[u];
   const int g = lane >> 2, q = lane & 3;
@@ -589,9 +584,26 @@ __device__ void epilogue_gateup(const StreamArgs& a, StreamSmem& ss, int u, int 
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-      if (g == 0) ss.cmax[grp][sb][t] = m;
+      if (g == 0) ss.cmax[par][grp][sb][t] = m;
     }
-  named_sync(1 + grp, dstr::kGroupWarps * 32);
+  // every warp of the group has written its maxima: an arrival count in shared memory, with a
+  // bounded wait (a peer that gave up on a timed-out stage must not hang the others); the
+  // maxima alternate between two buffers, so a warp one epilogue ahead writes the other one
+  __threadfence_block();
+  __syncwarp();
+  if (lane == 0) {
+    atomicAdd(&ss.epi_cnt[grp], 1);
+    const int target = dstr::kGroupWarps * (int)(nepi + 1u);
+    const uint64_t t0 = gtime();
+    while (*reinterpret_cast<volatile int*>(&ss.epi_cnt[grp]) < target) {
+      if (gtime() - t0 > dstr::kTimeoutNs) {
+        report(a.st, kFlagTimeout, 340);
+        break;
+      }
+    }
+  }
+  __syncwarp();
+  __threadfence_block();
 #pragma unroll
   for (int gi = 0; gi < NG; ++gi)
 #pragma unroll
@@ -600,7 +612,7 @@ __device__ void epilogue_gateup(const StreamArgs& a, StreamSmem& ss, int u, int 
       if (t >= a.T || !((mask >> t) & 1u)) continue;
       float m = 0.f;
 #pragma unroll
-      for (int s = 0; s < 8; ++s) m = fmaxf(m, ss.cmax[grp][s][t]);
+      for (int s = 0; s < 8; ++s) m = fmaxf(m, ss.cmax[par][grp][s][t]);
       const int p = max(-126, min(126, prescale_exp(m)));
       const int pos = row0 + __popc(mask & ((1u << t) - 1u));
       if (a.checks && (pos < 0 || pos >= a.T * a.k || pos - row0 >= m_u)) {
@@ -739,6 +751,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
     }
   }
   if (tid == 0 && !a.route_only) {
+    ss.epi_cnt[0] = ss.epi_cnt[1] = 0;
     for (int s = 0; s < S; ++s) {
       mb_init(&ss.full[s], 1);
       mb_init(&ss.empty[s], dstr::kGroupWarps);  // each stage goes to one group
@@ -875,12 +888,6 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
               // the stage's activation rows: nc chunks x (T tokens or the expert's m rows)
               mb_expect(full, (uint32_t)(nc * kTileBytes + nc * (gu ? T : m) * dstr::kRow));
               bulk_g2s(stg, tiles + (size_t)c0 * kTileBytes, (uint32_t)(nc * kTileBytes), full);
-              // the weights a ring's depth further on into L2: more bytes in flight than the ring holds
-              const int pf = s + a.pf_dist;
-              if (a.pf_dist > 0 && pf < nst) {
-                const int p0 = cps * pf, pn = min(cps, nch - p0);
-                prefetch_l2(tiles + (size_t)p0 * kTileBytes, (uint32_t)(pn * kTileBytes));
-              }
               if (tl && it < 256) tl[8 * it + 2] = gtime();
             }
           }
@@ -995,7 +1002,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
 
     float acc[NG][4];
     int slot = grp;
-    uint32_t ph = 0, it = 0, nsig = 0, nitem = 0;
+    uint32_t ph = 0, it = 0, nsig = 0, nitem = 0, nepi = 0;
     unsigned long long w_full = 0, w_epi = 0;
     // hands item v (or -1: the end) to the signal warp through the group's
     // queue: warp 0 of the group fills the entry once the signal warp has
@@ -1090,7 +1097,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
       const int u = gu ? ii / gu_per : ii / dn_per;
       const int b = gu ? ii - u * gu_per : ii - u * dn_per;
       const uint64_t te0 = (tr && warp == 0) ? gtime() : 0;
-      if (gu) epilogue_gateup<NG>(a, ss, u, b, sb, grp, acc, lane);
+      if (gu) epilogue_gateup<NG>(a, ss, u, b, sb, grp, acc, lane, nepi++);
       else epilogue_down<NG>(a, ss, u, b, sb, acc, lane);
       post(item);
       if (tr && warp == 0) w_epi += gtime() - te0;
@@ -1276,11 +1283,6 @@ cudaError_t launch_decode_stream(const LayerDims& d, const uint8_t* blob, const 
                                                                      : 1;
   a.checks = d.checks;
   a.trace = ws.trace;
-  static const int pf_dist = [] {
-    const char* e = getenv("NVFP4_MOE_DECODE_PREFETCH");
-    return e ? atoi(e) : 0;
-  }();
-  a.pf_dist = pf_dist;
   if (!route_only && T * (k + d.S) > ws.act_rows) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(route_only ? 1 : num_sms);
