@@ -168,10 +168,10 @@ nvfp4_moe_status nvfp4_moe_set_path(nvfp4_moe_t h, int path);
 
 /* Decode forward that allocates nothing.  The GLM-5.3-Flash pages have no
  * counterpart to this call; it exists for callers that cannot call
- * cudaMalloc and so cannot create a handle: code running while a CUDA graph
- * is captured in global mode, plugins whose host framework owns and budgets
- * every device byte, and static-memory runtimes that forbid allocation after
- * start-up.  It computes what nvfp4_moe_forward computes on the decode path,
+ * cudaMalloc and so cannot create a handle: plugins whose host framework owns
+ * and budgets every device byte, static-memory runtimes that forbid
+ * allocation after start-up, and code that must not allocate while a graph
+ * is being captured (this build's tests do not capture it).  It computes what nvfp4_moe_forward computes on the decode path,
  * from caller memory only:
  *   packed_experts  DEVICE, 16-byte aligned, E * 3*H*I*9/16 bytes in the
  *                   layout nvfp4_moe_pack writes (see nvfp4_moe_debug_packed_blob)
