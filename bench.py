@@ -609,7 +609,7 @@ def run_linear(args):
     kern_ms = stage_ms[2] / max(nfwd, 1)   # the GEMV / GEMM launch (tables kernel excluded)
     wbytes = cfg.weight_bytes
     if decode:
-        kernel, bound, unit, peak_key = "decode_fused_kernel (linear)", "hbm", "GB/s", "hbm_gbs"
+        kernel, bound, unit, peak_key = "decode_stream_kernel (linear)", "hbm", "GB/s", "hbm_gbs"
         algo = wbytes + T * K * 2 + T * N * 2
         achieved = algo / (kern_ms / 1e3) / 1e9
     else:

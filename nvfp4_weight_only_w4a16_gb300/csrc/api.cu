@@ -333,8 +333,8 @@ nvfp4_moe_status create_handle(const nvfp4_moe_config* c, bool linear, int lin_n
   cv.add(&w.done_gu, maxU);
   cv.add(&w.cmb, H / 64);
   cv.add(&w.exit_cnt, 1);
-  w.act_rows = kDecodeMaxTokens * K;
-  cv.add(&w.act_h, linear ? 16 : stream_act_h_bytes(I, w.act_rows), true);
+  w.act_rows = kDecodeMaxTokens * K;  // a dense linear: K = 1, its x rows as the "h" rows
+  cv.add(&w.act_h, stream_act_h_bytes(I, w.act_rows), true);
   cv.add(&w.act_x, linear ? 16 : stream_act_x_bytes(H), true);
   cv.add(&w.wctr, 1);
   cv.add(&w.done_c, maxU * (I / 64));
@@ -843,7 +843,9 @@ nvfp4_moe_status nvfp4_linear_forward(nvfp4_moe_t h, int T, const void* x, void*
   if (path == NVFP4_MOE_PATH_DECODE) {
     if (ev[1]) cudaEventRecord(ev[1], st);
     if (ev[2]) cudaEventRecord(ev[2], st);
-    e = launch_decode_forward(d, h->blob, h->gscale, nullptr, x, T, 1, out, 0, h->num_sms, h->ws, h->fault, st);
+    e = stream_supported(d, T, 1)
+            ? launch_decode_stream(d, h->blob, h->gscale, nullptr, x, T, 1, out, 0, h->num_sms, h->ws, h->fault, st)
+            : launch_decode_forward(d, h->blob, h->gscale, nullptr, x, T, 1, out, 0, h->num_sms, h->ws, h->fault, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "linear decode launch");
   } else {
     e = launch_route_linear(T, kTileRows, h->ws, st);

@@ -110,6 +110,8 @@ struct StreamArgs {
   RouteParams rp;
   const void* logits;
   int logits_bf16;
+  int linear;                     // 1: a dense linear out = gs W x (one "expert", down matrix only, x [T][I])
+  int n_out;                      // a dense linear's output features (out is [T][n_out])
   const __nv_bfloat16* router_w;  // BF16 [Er][H]: the kernel computes the logits (else NULL)
   float* logits_w;                // [T][Er] FP32: where it writes them
   int32_t* logit_ready;           // experts whose logits are written (reset by the last CTA)
@@ -301,6 +303,32 @@ __device__ void stream_router(const StreamArgs& a, StreamSmem& ss) {
     if (mine) atomicAdd(a.logit_ready, mine);
     wait_count(a.logit_ready, a.Er, a.st, 900);
   }
+  __syncthreads();
+}
+
+// A dense linear's tables, every CTA: one touched "expert" holding all T rows in token
+// order with weight 1.  `mid` as in stream_route.
+template <class Mid>
+__device__ void stream_route_linear(const StreamArgs& a, StreamSmem& ss, Mid&& mid) {
+  const int tid = threadIdx.x, T = a.T;
+  if (tid == 0) {
+    ss.U = 1;
+    ss.nan = 0;
+    ss.off[0] = 0;
+    ss.off[1] = T;
+    ss.slot_of[0] = 0;
+    ss.tch_e[0] = 0;
+    ss.tch_r0[0] = 0;
+    ss.tch_m[0] = T;
+    ss.tch_mask[0] = T >= 32 ? ~0u : (1u << T) - 1u;
+  }
+  if (tid < T) {
+    ss.ids[tid] = 0;
+    ss.wts[tid] = 1.0f;
+    ss.perm[tid] = tid;
+    ss.inv[tid] = tid;
+  }
+  mid();
   __syncthreads();
 }
 
@@ -643,7 +671,16 @@ __device__ void epilogue_down(const StreamArgs& a, const StreamSmem& ss, int u, 
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int j = 8 * gi + 2 * q + c;
-      if (j < m) {
+      if (j < m && a.linear) {  // a dense linear: row j is token j, written straight to out
+#pragma unroll
+        for (int h8 = 0; h8 < 2; ++h8) {
+          const int d = d0 + 8 * h8;
+          if (d >= a.n_out) continue;
+          const float v = acc[gi][2 * h8 + c] * gsd;
+          if (a.out_f32) reinterpret_cast<float*>(a.out)[(size_t)j * a.n_out + d] = v;
+          else reinterpret_cast<__nv_bfloat16*>(a.out)[(size_t)j * a.n_out + d] = __float2bfloat16_rn(v);
+        }
+      } else if (j < m) {
         float* yr = a.y + (size_t)(row0 + j) * a.H;
         yr[d0] = acc[gi][c] * gsd;
         yr[d0 + 8] = acc[gi][2 + c] * gsd;
@@ -734,20 +771,25 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
   unsigned long long* tl = (a.trace && blockIdx.x < 8) ? a.trace + (size_t)gridDim.x * 16 + blockIdx.x * 2048 : nullptr;
   if (tr && tid == 0) tr[0] = gtime();
   float lval[2][8];
-  if (!a.router_w) stream_route_issue(a, lval);
+  if (!a.router_w && !a.linear) stream_route_issue(a, lval);
 
   // this CTA's share of the x conversion: token tx = 15 - warp of its chunks (chunk
   // blockIdx.x + i * gridDim.x), on the consumer warps from the top down -- for T <= 8
   // none of them chooses experts, so the conversion runs beside the routing; the loads
-  // are issued first thing
+  // are issued first thing.  A dense linear's x ([T][I]) becomes the h rows of its one
+  // "expert" (act_h, counted in done_c); the layer's x ([T][H]) the gate/up rows (act_x,
+  // counted in x_ready)
   const int tx = dstr::kConsumers - 1 - warp;
   const bool xconv = !a.route_only && a.x && tx >= 0 && tx < T;
+  const int xlen = a.linear ? a.I : a.H, nchX = a.linear ? nchI : nchH;
+  uint8_t* const xdst = a.linear ? a.act_h : a.act_x;
+  int32_t* const xcnt = a.linear ? a.done_c : a.x_ready;
   uint32_t xw[dstr::kXChunks];
   if (xconv) {
 #pragma unroll
     for (int i = 0; i < dstr::kXChunks; ++i) {
       const int c = blockIdx.x + i * gridDim.x;
-      if (c < nchH) xw[i] = __ldg(reinterpret_cast<const uint32_t*>(a.x + (size_t)tx * a.H + 64 * c) + lane);
+      if (c < nchX) xw[i] = __ldg(reinterpret_cast<const uint32_t*>(a.x + (size_t)tx * xlen + 64 * c) + lane);
     }
   }
   if (tid == 0 && !a.route_only) {
@@ -772,33 +814,35 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
     stream_router(a, ss);
     stream_route_issue(a, lval);
   }
-  stream_route(a, ss, lval, tr, [&] {
+  auto convert_x = [&] {
     if (!xconv) return;
 #pragma unroll
     for (int i = 0; i < dstr::kXChunks; ++i) {
       const int c = blockIdx.x + i * gridDim.x;
-      if (c < nchH) convert_chunk_row(xw[i], a.act_x + ((size_t)c * T + tx) * dstr::kRow, lane);
+      if (c < nchX) convert_chunk_row(xw[i], xdst + ((size_t)c * T + tx) * dstr::kRow, lane);
     }
     // (chunks beyond the ones loaded above: only when the grid is small)
-    for (int c = blockIdx.x + dstr::kXChunks * gridDim.x; c < nchH; c += gridDim.x) {
-      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(a.x + (size_t)tx * a.H + 64 * c) + lane);
-      convert_chunk_row(w, a.act_x + ((size_t)c * T + tx) * dstr::kRow, lane);
+    for (int c = blockIdx.x + dstr::kXChunks * gridDim.x; c < nchX; c += gridDim.x) {
+      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(a.x + (size_t)tx * xlen + 64 * c) + lane);
+      convert_chunk_row(w, xdst + ((size_t)c * T + tx) * dstr::kRow, lane);
     }
-    // the rows are read by other CTAs' bulk copies (the async proxy) once x_ready counts them
+    // the rows are read by other CTAs' bulk copies (the async proxy) once counted in
     asm volatile("fence.proxy.async.global;" ::: "memory");
     __syncwarp();
     if (lane == 0) {
       __threadfence();
-      for (int c = blockIdx.x; c < nchH; c += gridDim.x) atomicAdd(a.x_ready + c, 1);
+      for (int c = blockIdx.x; c < nchX; c += gridDim.x) atomicAdd(xcnt + c, 1);
     }
-  }, a.route_only ? -1 : dstr::kProducer);
+  };
+  if (a.linear) stream_route_linear(a, ss, convert_x);
+  else stream_route(a, ss, lval, tr, convert_x, a.route_only ? -1 : dstr::kProducer);
   // the barriers and the touched-expert list are ready; except in the producer warp, so
   // are the positions, masks and (CTA 0) the tables written out
   if (a.route_only) return;
   if (tr && tid == 0) tr[1] = gtime();
 
   const int U = ss.U;
-  const int gu_per = nchI, dn_per = a.H / 128;  // items per expert
+  const int gu_per = a.linear ? 0 : nchI, dn_per = a.H / 128;  // items per expert (a linear: down only)
   const int n_gu = U * gu_per, n_items = n_gu + U * dn_per;
   const int cps = a.cps;
   const int nst_gu = (nchH + cps - 1) / cps, nst_dn = (nchI + cps - 1) / cps;  // both >= 2
@@ -897,7 +941,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
             const uint64_t td0 = tr ? gtime() : 0;
             if (!gu && tr && n_dn == 0 && lane == 0) tr[13] = td0;
             late = !(gu ? warp_wait_all(a.x_ready, nchH, T, a.st, 700)
-                        : warp_wait_all(dep, nchI, 1, a.st, 600 + (unsigned)u));
+                        : warp_wait_all(dep, nchI, a.linear ? T : 1, a.st, 600 + (unsigned)u));
             if (!late) {
               if (gu) x_ok = true;
               else ready_u = u;
@@ -977,7 +1021,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
           mb_arrive(&ss.sig_empty[g][q]);
         }
         last = __shfl_sync(0xffffffffu, last, 0);
-        if (last && T <= dstr::kSigCombineT) {
+        if (last && T <= dstr::kSigCombineT && !a.linear) {
           __threadfence();  // the other CTAs' y rows, fenced before their counts
           for (int t = 0; t < T; ++t) combine_slice(a, ss, b, t, lane);
         }
@@ -1108,7 +1152,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
       tr[10] = w_full;
       tr[11] = w_epi;
     }
-    if (T > dstr::kSigCombineT && !is_aborted(a.st))
+    if (T > dstr::kSigCombineT && !a.linear && !is_aborted(a.st))
       combine_tasks(a, ss, (int)blockIdx.x * dstr::kConsumers + warp, (int)gridDim.x * dstr::kConsumers, lane);
   }
 
@@ -1171,7 +1215,7 @@ cudaError_t launch_hidden_to_f32(const Workspace& ws, int src, int R, int I, flo
 // Host side
 // ---------------------------------------------------------------------------
 bool stream_supported(const LayerDims& d, int T, int k) {
-  return !d.linear && d.in_scale == nullptr && T >= 1 && T <= kDecodeMaxTokens && k + d.S <= dstr::kMaxSlots &&
+  return d.in_scale == nullptr && T >= 1 && T <= kDecodeMaxTokens && k + d.S <= dstr::kMaxSlots &&
          d.E <= dstr::kMaxE && d.H % 128 == 0 && d.I % 128 == 0 && d.H <= 16384 && d.I <= 16384;
 }
 
@@ -1228,7 +1272,7 @@ cudaError_t launch_decode_stream(const LayerDims& d, const uint8_t* blob, const 
   if (e != cudaSuccess) return e;
   const StreamPlan plan = stream_plan(T, d.H, smem_max);
   if (plan.stages < 3 || plan.smem > (size_t)smem_max) return cudaErrorInvalidConfiguration;
-  const ExpertLayout L = expert_layout(d.H, d.I);
+  const ExpertLayout L = d.linear ? linear_layout(d.H, d.I) : expert_layout(d.H, d.I);
   StreamArgs a{};
   a.blob = blob;
   a.expert_stride = L.stride;
@@ -1245,6 +1289,9 @@ cudaError_t launch_decode_stream(const LayerDims& d, const uint8_t* blob, const 
   a.rp = d.rp;
   a.logits = logits;
   a.logits_bf16 = d.logits_bf16;
+  a.linear = d.linear;
+  a.n_out = d.n_out;
+  if (d.linear && (router_w || route_only || !x)) return cudaErrorInvalidValue;
   if (router_w) {
     if (!x || route_only || !ws.logits || !ws.logit_ready) return cudaErrorInvalidValue;
     a.router_w = reinterpret_cast<const __nv_bfloat16*>(router_w);
