@@ -658,8 +658,9 @@ __device__ void epilogue_gateup(const StreamArgs& a, StreamSmem& ss, int u, int 
 }
 
 // Down epilogue of item (u, b): y rows 128 b + 16 sb + g (+8) for the
-// expert's routed rows (counted in for output slice b by the signal warp).
-template <int NG>
+// expert's routed rows (counted in for output slice b by the signal warp);
+// a dense linear (kLin) writes its output rows instead.
+template <int NG, bool kLin>
 __device__ void epilogue_down(const StreamArgs& a, const StreamSmem& ss, int u, int b, int sb,
                               const float (&acc)[NG][4], int lane) {
   const int e = ss.tch_e[u], row0 = ss.tch_r0[u], m = ss.tch_m[u];
@@ -671,7 +672,7 @@ __device__ void epilogue_down(const StreamArgs& a, const StreamSmem& ss, int u, 
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int j = 8 * gi + 2 * q + c;
-      if (j < m && a.linear) {  // a dense linear: row j is token j, written straight to out
+      if (kLin && j < m) {  // a dense linear: row j is token j, written straight to out
 #pragma unroll
         for (int h8 = 0; h8 < 2; ++h8) {
           const int d = d0 + 8 * h8;
@@ -680,7 +681,7 @@ __device__ void epilogue_down(const StreamArgs& a, const StreamSmem& ss, int u, 
           if (a.out_f32) reinterpret_cast<float*>(a.out)[(size_t)j * a.n_out + d] = v;
           else reinterpret_cast<__nv_bfloat16*>(a.out)[(size_t)j * a.n_out + d] = __float2bfloat16_rn(v);
         }
-      } else if (j < m) {
+      } else if (!kLin && j < m) {
         float* yr = a.y + (size_t)(row0 + j) * a.H;
         yr[d0] = acc[gi][c] * gsd;
         yr[d0 + 8] = acc[gi][2 + c] * gsd;
@@ -747,7 +748,8 @@ __device__ void combine_tasks(const StreamArgs& a, const StreamSmem& ss, int wg,
 // The kernel.  Shared memory: StreamSmem | pair sums | ring
 // [stages][stage_bytes].
 // ---------------------------------------------------------------------------
-template <int NG>
+// kLin: a dense linear (down-only, no routing); the MoE instantiations carry none of its code.
+template <int NG, bool kLin>
 __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(StreamArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   StreamSmem& ss = *reinterpret_cast<StreamSmem*>(smem);
@@ -771,7 +773,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
   unsigned long long* tl = (a.trace && blockIdx.x < 8) ? a.trace + (size_t)gridDim.x * 16 + blockIdx.x * 2048 : nullptr;
   if (tr && tid == 0) tr[0] = gtime();
   float lval[2][8];
-  if (!a.router_w && !a.linear) stream_route_issue(a, lval);
+  if (!kLin && !a.router_w) stream_route_issue(a, lval);
 
   // this CTA's share of the x conversion: token tx = 15 - warp of its chunks (chunk
   // blockIdx.x + i * gridDim.x), on the consumer warps from the top down -- for T <= 8
@@ -781,9 +783,9 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
   // counted in x_ready)
   const int tx = dstr::kConsumers - 1 - warp;
   const bool xconv = !a.route_only && a.x && tx >= 0 && tx < T;
-  const int xlen = a.linear ? a.I : a.H, nchX = a.linear ? nchI : nchH;
-  uint8_t* const xdst = a.linear ? a.act_h : a.act_x;
-  int32_t* const xcnt = a.linear ? a.done_c : a.x_ready;
+  const int xlen = kLin ? a.I : a.H, nchX = kLin ? nchI : nchH;
+  uint8_t* const xdst = kLin ? a.act_h : a.act_x;
+  int32_t* const xcnt = kLin ? a.done_c : a.x_ready;
   uint32_t xw[dstr::kXChunks];
   if (xconv) {
 #pragma unroll
@@ -834,7 +836,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
       for (int c = blockIdx.x; c < nchX; c += gridDim.x) atomicAdd(xcnt + c, 1);
     }
   };
-  if (a.linear) stream_route_linear(a, ss, convert_x);
+  if (kLin) stream_route_linear(a, ss, convert_x);
   else stream_route(a, ss, lval, tr, convert_x, a.route_only ? -1 : dstr::kProducer);
   // the barriers and the touched-expert list are ready; except in the producer warp, so
   // are the positions, masks and (CTA 0) the tables written out
@@ -842,7 +844,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
   if (tr && tid == 0) tr[1] = gtime();
 
   const int U = ss.U;
-  const int gu_per = a.linear ? 0 : nchI, dn_per = a.H / 128;  // items per expert (a linear: down only)
+  const int gu_per = kLin ? 0 : nchI, dn_per = a.H / 128;  // items per expert (a linear: down only)
   const int n_gu = U * gu_per, n_items = n_gu + U * dn_per;
   const int cps = a.cps;
   const int nst_gu = (nchH + cps - 1) / cps, nst_dn = (nchI + cps - 1) / cps;  // both >= 2
@@ -941,7 +943,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
             const uint64_t td0 = tr ? gtime() : 0;
             if (!gu && tr && n_dn == 0 && lane == 0) tr[13] = td0;
             late = !(gu ? warp_wait_all(a.x_ready, nchH, T, a.st, 700)
-                        : warp_wait_all(dep, nchI, a.linear ? T : 1, a.st, 600 + (unsigned)u));
+                        : warp_wait_all(dep, nchI, kLin ? T : 1, a.st, 600 + (unsigned)u));
             if (!late) {
               if (gu) x_ok = true;
               else ready_u = u;
@@ -1021,7 +1023,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
           mb_arrive(&ss.sig_empty[g][q]);
         }
         last = __shfl_sync(0xffffffffu, last, 0);
-        if (last && T <= dstr::kSigCombineT && !a.linear) {
+        if (!kLin && last && T <= dstr::kSigCombineT) {
           __threadfence();  // the other CTAs' y rows, fenced before their counts
           for (int t = 0; t < T; ++t) combine_slice(a, ss, b, t, lane);
         }
@@ -1142,7 +1144,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
       const int b = gu ? ii - u * gu_per : ii - u * dn_per;
       const uint64_t te0 = (tr && warp == 0) ? gtime() : 0;
       if (gu) epilogue_gateup<NG>(a, ss, u, b, sb, grp, acc, lane, nepi++);
-      else epilogue_down<NG>(a, ss, u, b, sb, acc, lane);
+      else epilogue_down<NG, kLin>(a, ss, u, b, sb, acc, lane);
       post(item);
       if (tr && warp == 0) w_epi += gtime() - te0;
     }
@@ -1152,7 +1154,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
       tr[10] = w_full;
       tr[11] = w_epi;
     }
-    if (T > dstr::kSigCombineT && !a.linear && !is_aborted(a.st))
+    if (!kLin && T > dstr::kSigCombineT && !is_aborted(a.st))
       combine_tasks(a, ss, (int)blockIdx.x * dstr::kConsumers + warp, (int)gridDim.x * dstr::kConsumers, lane);
   }
 
@@ -1253,9 +1255,13 @@ cudaError_t stream_prepare_device(int dev, int* smem_max) {
   int optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute((const void*)decode_stream_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    e = cudaFuncSetAttribute((const void*)decode_stream_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute((const void*)decode_stream_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    e = cudaFuncSetAttribute((const void*)decode_stream_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute((const void*)decode_stream_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute((const void*)decode_stream_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < kCached) cached[dev] = optin;
   *smem_max = optin;
@@ -1341,8 +1347,11 @@ cudaError_t launch_decode_stream(const LayerDims& d, const uint8_t* blob, const 
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = route_only ? 0 : 1;
-  return T <= 8 ? cudaLaunchKernelEx(&cfg, decode_stream_kernel<1>, a)
-                : cudaLaunchKernelEx(&cfg, decode_stream_kernel<2>, a);
+  if (d.linear)
+    return T <= 8 ? cudaLaunchKernelEx(&cfg, decode_stream_kernel<1, true>, a)
+                  : cudaLaunchKernelEx(&cfg, decode_stream_kernel<2, true>, a);
+  return T <= 8 ? cudaLaunchKernelEx(&cfg, decode_stream_kernel<1, false>, a)
+                : cudaLaunchKernelEx(&cfg, decode_stream_kernel<2, false>, a);
 }
 
 }  // namespace nvfp4moe
