@@ -172,6 +172,22 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                "l"(src), "r"(bytes), "r"(saddr(bar))
                : "memory");
 }
+// The same copy with an L2 eviction-priority hint.  The weight tiles are read once per
+// step, so they take evict_first: L2 gives up their lines before those of the rows every
+// CTA keeps re-reading (x, h, the routing tables).  Measured on the MTP and 16-token steps:
+// ~2-3 us less per step than with the default policy.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          saddr(dst)),
+      "l"(src), "r"(bytes), "r"(saddr(bar)), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ uint64_t gtime() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -864,6 +880,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
       __syncwarp();
     } else {
       int item = blockIdx.x;
+      const uint64_t once = l2_evict_first_policy();  // the weight tiles' L2 policy
       unsigned long long w_empty = 0, w_dep = 0, n_items_done = 0, n_dn = 0;
       bool x_ok = false;      // every chunk of act_x converted (known once, then for good)
       int ready_u = -1;       // the last expert whose h is known complete
@@ -933,7 +950,7 @@ __global__ void __launch_bounds__(dstr::kThreads, 1) decode_stream_kernel(Stream
               ss.meta[slot][2] = nc;
               // the stage's activation rows: nc chunks x (T tokens or the expert's m rows)
               mb_expect(full, (uint32_t)(nc * kTileBytes + nc * (gu ? T : m) * dstr::kRow));
-              bulk_g2s(stg, tiles + (size_t)c0 * kTileBytes, (uint32_t)(nc * kTileBytes), full);
+              bulk_g2s_hint(stg, tiles + (size_t)c0 * kTileBytes, (uint32_t)(nc * kTileBytes), full, once);
               if (tl && it < 256) tl[8 * it + 2] = gtime();
             }
           }
