@@ -79,7 +79,7 @@ def _check(gpu, ref, abs_sum, K, bf16_out):
 
 
 @pytest.mark.parametrize("path", [P.PATH_DECODE, P.PATH_PREFILL])
-@pytest.mark.parametrize("T", [1, 5, 16])
+@pytest.mark.parametrize("T", [1, 5, 8, 9, 16])
 def test_linear_tiny(path, T):
     cfg = LINEAR_CONFIGS["linear_tiny"]
     inp = make_linear_inputs(cfg, tokens=T)

@@ -356,6 +356,25 @@ def test_forward_prefill_every_token(name, out_f32):
         check_rows(L, inp, rows)
 
 
+# The decode kernel's code paths change with the token count: up to 4 tokens the signal warp
+# that completes an output slice combines it, above that every consumer warp takes (slice,
+# token) tasks; up to 8 tokens one 8-column MMA group, above that two; T consumer warps route
+# and T convert x rows.  Every T of the decode range, on the tiny layer (small stages) and on
+# a layer with the full H and I (8-chunk stages) but 8 experts, so the oracle stays quick.
+DECODE_FULL_DIMS = LayerConfig("decode_full_dims", 8, 4096, 1536, 4, 16)
+
+
+@pytest.mark.parametrize("T", range(1, 17))
+def test_decode_every_token_count(T):
+    for base in (CONFIGS["tiny"], DECODE_FULL_DIMS):
+        cfg = base.with_tokens(T)
+        inp = make_inputs(cfg)
+        L = _layer(base, max_tokens=16)
+        gpu = _forward(L, inp.logits, inp.x_bits, cfg.top_k, P.PATH_DECODE)
+        ref = O.moe_forward(inp.logits, inp.x_bits, inp.weights, cfg.top_k)
+        assert_layer_close(gpu, ref)
+
+
 @pytest.mark.parametrize("T,path", [(1, P.PATH_DECODE), (1, P.PATH_PREFILL), (37, P.PATH_PREFILL),
                                     (300, P.PATH_PREFILL), (16, P.PATH_DECODE)])
 def test_forward_ragged_and_degenerate(T, path):
