@@ -156,6 +156,26 @@ nvfp4_moe_status nvfp4_moe_pack(nvfp4_moe_t h, const uint8_t* w13_q, const uint8
 nvfp4_moe_status nvfp4_moe_forward(nvfp4_moe_t h, const void* router_logits, int T, int top_k,
                                    const void* x, void* out, cudaStream_t stream);
 
+/* The same forward (the layer above) with router_logits, x and out in HOST
+ * memory that CUDA has mapped into the device's address space: page-locked
+ * buffers from cudaHostAlloc / cudaMallocHost (mapped, at the same address,
+ * whenever addressing is unified, as on every 64-bit system) or from
+ * cudaHostRegister with cudaHostRegisterMapped.  Layouts, alignment and
+ * ranges as for nvfp4_moe_forward.  The decode kernel reads the logits and x
+ * and writes out in place -- on a Grace-Blackwell node over the coherent
+ * CPU-GPU link -- so a step moves its inputs and its result without a
+ * copy-engine transfer or a staging buffer.
+ * Decode only: the W4A16 streaming decode kernel, T <= decode_max_tokens.  A
+ * call that would take another path (T above that, a path forced to prefill,
+ * W4A4 activation quantisation) returns NVFP4_MOE_ERR_UNSUPPORTED_SHAPE; a
+ * pointer that is not mapped page-locked host memory (pageable, managed or
+ * device memory) returns NVFP4_MOE_ERR_INVALID_ARG.  Both before anything is
+ * enqueued.  Asynchronous like nvfp4_moe_forward: out holds the result once
+ * `stream` has completed, and until then the host must neither write the
+ * inputs nor read out. */
+nvfp4_moe_status nvfp4_moe_forward_host(nvfp4_moe_t h, const void* router_logits, int T, int top_k,
+                                        const void* x, void* out, cudaStream_t stream);
+
 /* Synchronous: waits for the device, then reports the device-side status word
  * accumulated since the last call (and clears it).  Returns NVFP4_MOE_OK,
  * NVFP4_MOE_ERR_TIMEOUT or NVFP4_MOE_ERR_DEVICE_CHECK; *nan_logits (may be

@@ -68,6 +68,7 @@ def load_library(path: str | None = None):
         "nvfp4_moe_create": (i, [ctypes.POINTER(Config), ctypes.POINTER(vp)]),
         "nvfp4_moe_pack": (i, [vp, vp, vp, vp, vp, vp, vp]),
         "nvfp4_moe_forward": (i, [vp, vp, i, i, vp, vp, vp]),
+        "nvfp4_moe_forward_host": (i, [vp, vp, i, i, vp, vp, vp]),
         "nvfp4_moe_get_status": (i, [vp, ctypes.POINTER(ctypes.c_uint32)]),
         "nvfp4_moe_set_path": (i, [vp, i]),
         "nvfp4_moe_status_string": (ctypes.c_char_p, [i]),
@@ -110,6 +111,15 @@ def _ptr(t):
         return None
     if not t.is_cuda:
         raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_ptr(t):
+    """A page-locked CPU tensor's address (the library checks that CUDA maps it)."""
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError("expected a page-locked (pinned) CPU tensor")
     if not t.is_contiguous():
         raise ValueError("expected a contiguous tensor")
     return ctypes.c_void_p(t.data_ptr())
@@ -164,6 +174,14 @@ class MoELayer:
         T = x.shape[0]
         st = self.lib.nvfp4_moe_forward(self.h, _ptr(logits), T, top_k, _ptr(x), _ptr(out), _stream(stream))
         self._check(st, "nvfp4_moe_forward")
+        return out
+
+    def nvfp4_moe_forward_host(self, logits, x, top_k, out, stream=None):
+        """nvfp4_moe_forward on pinned CPU tensors, read and written in place by the decode kernel."""
+        T = x.shape[0]
+        st = self.lib.nvfp4_moe_forward_host(self.h, _host_ptr(logits), T, top_k, _host_ptr(x), _host_ptr(out),
+                                             _stream(stream))
+        self._check(st, "nvfp4_moe_forward_host")
         return out
 
     def nvfp4_moe_forward_raw(self, logits_ptr, T, top_k, x_ptr, out_ptr, stream_handle):

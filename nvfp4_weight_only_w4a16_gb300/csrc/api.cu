@@ -635,6 +635,43 @@ nvfp4_moe_status nvfp4_moe_forward(nvfp4_moe_t h, const void* logits, int T, int
   return forward_impl(h, logits, T, top_k, x, out, st, false);
 }
 
+}  // extern "C"
+
+namespace {
+// The device address of host memory the device may read and write in place: page-locked memory
+// that CUDA has mapped into the device's address space (under unified addressing, the same
+// pointer).  NULL for pageable, managed or device memory.
+const void* mapped_host(const void* p) {
+  if (!p) return nullptr;
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return attr.type == cudaMemoryTypeHost ? attr.devicePointer : nullptr;
+}
+}  // namespace
+
+extern "C" {
+
+nvfp4_moe_status nvfp4_moe_forward_host(nvfp4_moe_t h, const void* logits, int T, int top_k, const void* x,
+                                        void* out, cudaStream_t st) {
+  if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
+  if (h->linear) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "forward_host: the handle is a dense linear");
+  DeviceGuard g(h->cfg.device);
+  // the streaming decode kernel reads logits and x and writes out with plain loads and stores
+  // only, so those may live in host memory; the other paths copy x and logits in bulk
+  if (choose_path(h, T, top_k) != NVFP4_MOE_PATH_DECODE || !use_stream(h, dims_of(h), T, top_k))
+    return fail(h, NVFP4_MOE_ERR_UNSUPPORTED_SHAPE,
+                "forward_host: host buffers are read in place by the W4A16 decode kernel only (T <= decode_max_tokens)");
+  const void* dl = mapped_host(logits);
+  const void* dx = mapped_host(x);
+  void* dout = const_cast<void*>(mapped_host(out));
+  if (!dl || !dx || !dout)
+    return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "forward_host: logits, x and out must be mapped page-locked host memory");
+  return forward_impl(h, dl, T, top_k, dx, dout, st, false);
+}
+
 nvfp4_moe_status nvfp4_moe_set_router(nvfp4_moe_t h, const void* w_router, cudaStream_t st) {
   if (!h) return NVFP4_MOE_ERR_INVALID_ARG;
   if (h->linear) return fail(h, NVFP4_MOE_ERR_INVALID_ARG, "set_router: a dense linear has no router");
