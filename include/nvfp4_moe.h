@@ -23,12 +23,14 @@
  * (config.num_shared_experts), the routing variants (nvfp4_moe_set_scoring),
  * the BF16 router linear on the GPU (nvfp4_moe_set_router /
  * nvfp4_moe_forward_routed), the W4A4 comparison variant
- * (nvfp4_moe_set_act_quant), a dense W4A16 NVFP4 linear (nvfp4_linear_*) and
- * an allocation-free decode forward (nvfp4_moe_forward_decode_static).
+ * (nvfp4_moe_set_act_quant), a dense W4A16 NVFP4 linear (nvfp4_linear_*), an
+ * allocation-free decode forward (nvfp4_moe_forward_decode_static) and a
+ * decode forward on pinned host buffers (nvfp4_moe_forward_host).
  *
  * Conventions for every call:
  *   - returns a status, never throws, never prints unless NVFP4_MOE_LOG=1;
- *   - device pointers are CUDA global-memory pointers on the handle's device;
+ *   - device pointers are CUDA global-memory pointers on the handle's device
+ *     (nvfp4_moe_forward_host alone takes host pointers);
  *     the caller keeps ownership of every pointer it passes;
  *   - work is enqueued on `stream`; only calls documented as synchronous
  *     wait for the GPU;
