@@ -77,8 +77,8 @@ typedef enum nvfp4_moe_score {
 
 typedef enum nvfp4_moe_path {
   NVFP4_MOE_PATH_AUTO = 0,     /* T <= decode_max_tokens -> decode, else prefill */
-  NVFP4_MOE_PATH_DECODE = 1,   /* grouped GEMV, dequantised in registers          */
-  NVFP4_MOE_PATH_PREFILL = 2   /* grouped tcgen05 GEMM, dequantised in shared mem */
+  NVFP4_MOE_PATH_DECODE = 1,   /* one streaming kernel, dequantised in registers  */
+  NVFP4_MOE_PATH_PREFILL = 2   /* grouped tcgen05 GEMM, dequantised into TMEM     */
 } nvfp4_moe_path;
 
 /* Layer shape and limits, fixed at create.
