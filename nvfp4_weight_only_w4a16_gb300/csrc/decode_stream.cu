@@ -12,36 +12,46 @@
 // garbage).
 //
 // Design (GB300):
+//  * routing first, in every CTA: the logits (or, with a router weight, the
+//    router linear itself, each CTA a share of the experts, counted in) go
+//    through a warp top-k per token; one warp's scan builds the touched-expert
+//    list, and the producer starts on it while the other warps finish the
+//    permutation tables; warps that route no token meanwhile convert this
+//    CTA's share of x into 16-bit chunk rows in global memory;
 //  * work items are claimed dynamically from one global counter: first every
 //    gate/up item (expert u, 128 packed rows = 64 features, all of K = H),
 //    then every down item (expert u, 128 output rows, all of K = I), each
 //    group expert-major.  A CTA's first item is its index, later ones come
 //    from the counter (claimed one item ahead, so the atomic's latency hides
-//    behind the current item).  Fast SMs simply take more items, and a down
-//    item waits only for the chunks of h it reads, chunk by chunk, so the
-//    phases overlap instead of meeting at a barrier;
+//    behind the current item).  Fast SMs simply take more items; a down item
+//    waits (bounded) until every chunk of its expert's h is published;
 //  * one producer warp per CTA streams each item through a shared-memory ring
-//    of stages (four 64-wide K chunks of one 128-row block: 16 KB of codes
-//    and 2 KB of scales, each one contiguous cp.async.bulk, plus the chunks'
-//    activation rows) completed on mbarriers; 8 consumer warps each take one
-//    16-row group of a stage, all four chunks (four independent MMA chains),
-//    dequantise in registers (hardware E2M1 -> FP16 converts times the E4M3
-//    group scale, exact) and run mma.sync m16n8k16 (FP16 in, FP32
-//    accumulate);
+//    of stages of eight 64-wide K chunks: one cp.async.bulk of the chunks'
+//    packed tiles (codes and scales, 36 KB, with an L2 evict_first hint: the
+//    weights are read once per step) and one of their activation rows,
+//    completed on mbarriers;
+//  * two groups of 8 consumer warps take alternate stages; warp sb of a group
+//    takes 16-row group sb of each chunk, dequantises in registers (hardware
+//    E2M1 -> FP16 converts times the E4M3 group scale, exact) and runs
+//    mma.sync m16n8k16 (FP16 in, FP32 accumulate); at an item's end the two
+//    groups' partial sums meet in shared memory and one warp runs the
+//    epilogue (gate/up: SwiGLU into h rows; down: FP32 y rows);
 //  * activations enter the MMA as FP16 rows of one 64-wide chunk with their
 //    own power-of-two scale (the chunk's largest magnitude in [2^13, 2^14):
 //    exact for every value within 2^31 of it that has at most 11 significant
 //    bits), stored next to the row; each chunk's partial sums are multiplied
-//    back by the scale in FP32.  x is converted once per chunk, by one CTA,
-//    into global memory, and each stage carries its chunks' T token rows; the
-//    gate/up epilogue of an item produces one whole chunk of h (its 64
-//    features), so it writes h in that form: FP16, 11 significant bits;
+//    back by the scale in FP32.  The gate/up epilogue of an item produces one
+//    whole chunk of h (its 64 features) in that form: FP16, 11 significant
+//    bits;
 //  * gate/up columns are the step's tokens (every token through every touched
 //    expert's MMA columns; only the routed ones are kept), down columns are
 //    the expert's routed rows;
-//  * the combine: once the work runs out, every warp of the grid takes
-//    (128-wide output slice, token) tasks, each starting when its slice is
-//    complete for every touched expert, and sums the k slots in slot order;
+//  * a signal warp publishes finished items (a fence, then a count per
+//    (expert, chunk) of h or per 128-wide output slice), so no consumer waits
+//    on its own fence; up to 4 tokens the signal warp that completes a slice
+//    for the last touched expert combines it, above that every consumer warp
+//    takes (slice, token) tasks once the work runs out; the k slots are summed
+//    in slot order;
 //  * every wait is bounded (2 s): a wait that gives up records a timeout in the
 //    status word and the kernel unwinds without a trap.
 #include <cstdlib>
