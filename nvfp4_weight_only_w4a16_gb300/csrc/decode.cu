@@ -1,6 +1,8 @@
-// Decode path (1..16 tokens): one cooperative persistent kernel that routes,
-// runs the grouped gate/up GEMV with SwiGLU, the grouped down GEMV and the
-// weighted combine, dequantising NVFP4 in registers.
+// The earlier decode kernel (1..16 tokens): one cooperative persistent kernel
+// that routes, runs the grouped gate/up GEMV with SwiGLU, the grouped down GEMV
+// and the weighted combine, dequantising NVFP4 in registers.  The W4A16 decode
+// path runs the streaming kernel (decode_stream.cu); this one serves the W4A4
+// comparison variant's decode and any shape the streaming kernel does not take.
 //
 // At decode sizes every expert a token picks is streamed from HBM once per
 // step -- "the memory-bandwidth wall for an 18B-active model" ("GLM-5.3-Flash

@@ -1,8 +1,8 @@
 // Prefill routing (top-k + softmax over the chosen logits, per-CTA
 // histograms, one-CTA scan into offsets and m-tiles, stable scatter and x
 // gather) and the weighted combine of the prefill path.  The decode path
-// routes inside its fused kernel (decode.cu) with the same primitives
-// (route_common.cuh).
+// routes inside its kernel (decode_stream.cu; decode.cu for the W4A4 variant)
+// with the same primitives (route_common.cuh).
 #include "common.cuh"
 #include "kernels.h"
 #include "route_common.cuh"

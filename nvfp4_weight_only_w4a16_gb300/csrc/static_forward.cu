@@ -6,11 +6,10 @@
 // budget), and static-memory runtimes that allocate everything once at start
 // and forbid allocation afterwards.  They cannot create a handle, because
 // nvfp4_moe_create allocates the weight blob and the workspace.  This entry
-// point runs the decode path (one fused kernel: route, gate/up GEMV, down
-// GEMV, combine) with
-// the caller's own weight blob, activations and output; every intermediate
-// (routing tables, h, y, the GEMVs' split-K partial sums and counters) lives
-// in one file-scope __device__ array of kStaticScratchBytes.
+// point runs the decode path (the streaming decode kernel: route, gate/up,
+// down, combine, in one launch) with the caller's own weight blob, activations
+// and output; every intermediate (routing tables, x and h rows, y, counters)
+// lives in one file-scope __device__ array of kStaticScratchBytes.
 //
 // Consequences a caller must know:
 //  * every GPU that loads this library reserves the array until the process
@@ -111,8 +110,9 @@ size_t carve(uint8_t* base, int E, int H, int I, int T, int k, int num_sms, Work
   w.logit_ready = r.take<int32_t>(b, 1);
   w.status = r.take<DeviceStatus>(b, 1);
   *zero_end = (r.off + 255) & ~size_t(255);
-  // no split-K partial-sum buffers here: with part_gu == nullptr the decode
-  // kernel gives every warp whole blocks
+  // no split-K partial-sum buffers here: with part_gu == nullptr the earlier
+  // decode kernel (the fallback for shapes the streaming kernel does not take)
+  // gives every warp whole blocks
   w.part_gu = nullptr;
   w.part_dn = nullptr;
   (void)num_sms;
