@@ -13,20 +13,23 @@
 // keeps 11 significant bits between the GEMMs.  The dense linear and the
 // router GEMM stay on BF16 operands (the caller's BF16 x, the BF16 router).
 //
-// One persistent CTA per SM, 15 warps, warp-specialised:
-//   warp 0      weight producer: cp.async.bulk of the packed FP4 chunks (+
-//               scales) of a unit's two 128-row weight blocks into a
-//               10-stage ring, completion on mbarriers;
-//   warp 1      MMA issuer (one thread): per 64-wide K chunk 2 x 4
-//               tcgen05.mma (K=16), one per weight block, both reading the
-//               same activation tile; accumulators double-buffered in TMEM
-//               (2 buffers x 2 blocks x 128 columns); also owns the TMEM
-//               allocation;
+// One persistent CTA per SM, 20 warps, warp-specialised:
+//   warp 0      weight producer: cp.async.bulk of the packed FP4 chunks (codes +
+//               scales) of a unit's two 128-row weight blocks into a 9-stage
+//               ring, completion on mbarriers;
+//   warps 1, 19 MMA issuers, one thread each, one per weight block: per stage of
+//               two 64-wide K chunks 2 x 4 tcgen05.mma (K=16) with the weights
+//               (A) from TMEM and the activation tile (B) from shared memory;
+//               warp 1 also owns the TMEM allocation;
 //   warp 2      activation producer: TMA (128B swizzle) boxes of 16 routed rows;
-//   warps 3-10  dequantisers: E2M1 x E4M3 -> BF16 (exact) written straight
-//               into the 128B-swizzled K-major operand layout;
-//   warps 11-14 epilogue: tcgen05.ld of the accumulators, tensor scales,
+//   warps 3-10  dequantisers, one per (weight block, TMEM lane quarter), one
+//               thread per weight row: E2M1 x E4M3 -> FP16 (BF16 for the W4A4
+//               variant), exact, straight into the TMEM operand stage
+//               (tcgen05.st);
+//   warps 11-18 epilogue: tcgen05.ld of the accumulators, tensor scales,
 //               SwiGLU (gate/up) or the down-projection store.
+// (BF16 weights -- the router -- take a shared-memory operand ring filled by
+// warp 0's TMA instead, one issuer, two accumulator buffers, no dequantisers.)
 // Work unit = (m-tile of <= 128 routed rows of one expert, two 128-row weight
 // blocks).  MMA orientation: weights are the 128-row M operand, routed tokens
 // the N operand (16..128).  Two weight blocks per activation tile halve the
@@ -131,9 +134,9 @@ struct PrefillArgs {
   const int32_t* pexp_h;  // [R] and h row p by 2^-pexp_h[p]
   int checks;             // 1: check the m-tile table against its ranges (kFlagBounds; the unit is skipped)
   int E, R;               // experts in the blob, routed rows (for the checks)
-  // optional role timeline of CTA 0 (gate/up GEMM): per K chunk n < 256 at [4n] the MMA
-  // issue, [4n+1] / [4n+2] dequantiser warp 3's start / end, [4n+3] the weight copy
-  // issue; per unit u < 16 at [1024 + 4u] the MMA's accumulator wait end, the epilogue's
+  // optional role timeline of CTA 0 (gate/up GEMM): per stage n < 256 at [4n] the MMA
+  // issue, [4n+1] / [4n+2] dequantiser warp 3's start / end; per K chunk n < 256 at
+  // [4n+3] the weight copy issue; per unit u < 16 at [1024 + 4u] the MMA's accumulator wait end, the epilogue's
   // start and end (block 0), the epilogue's end (block 1)
   unsigned long long* trace;
 };
