@@ -30,7 +30,7 @@ def _close(got, ref):
     assert err.mean() / np.abs(ref).mean() <= 5e-3
 
 
-def _north_star(got, ref):
+def _assert_layer_bounds(got, ref):
     # the layer bounds against the oracle: max|err| <= 2e-2 RMS (plus the BF16
     # output rounding, 2^-8 of each value), mean relative error <= 5e-3
     err = np.abs(got - ref)
@@ -69,7 +69,7 @@ def _run_both(name, token_slices):
         got64 = got.float().cpu().numpy().astype(np.float64)
         _close(got64, ref.float().cpu().numpy().astype(np.float64))
         # and against the oracle itself (the whole-piece schedule for T > 8 is this path's own)
-        _north_star(got64, O.moe_forward(inp.logits[sl], inp.x_bits[sl], inp.weights, cfg.top_k))
+        _assert_layer_bounds(got64, O.moe_forward(inp.logits[sl], inp.x_bits[sl], inp.weights, cfg.top_k))
     st, nan = P.binding.nvfp4_moe_static_get_status()
     assert st == 0 and nan == 0, (P.STATUS[st], nan)
     layer.close()
@@ -130,6 +130,6 @@ def test_static_status_reports_nan_logits_and_timeouts():
     good = torch.full_like(x, float("nan"))
     _static(blob, gscale, cfg, torch.from_numpy(inp.logits).to(DEV), x, good)
     assert P.binding.nvfp4_moe_static_get_status() == (0, 0)
-    _north_star(good.float().cpu().numpy().astype(np.float64),
+    _assert_layer_bounds(good.float().cpu().numpy().astype(np.float64),
                 O.moe_forward(inp.logits, inp.x_bits, inp.weights, cfg.top_k))
     layer.close()
