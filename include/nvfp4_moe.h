@@ -193,8 +193,8 @@ nvfp4_moe_status nvfp4_moe_set_path(nvfp4_moe_t h, int path);
  * cudaMalloc and so cannot create a handle: plugins whose host framework owns
  * and budgets every device byte, static-memory runtimes that forbid
  * allocation after start-up, and code that must not allocate while a graph
- * is being captured (this build's tests do not capture it).  It computes what nvfp4_moe_forward computes on the decode path,
- * from caller memory only:
+ * is being captured (no test in tests/ captures it).  It computes what
+ * nvfp4_moe_forward computes on the decode path, from caller memory only:
  *   packed_experts  DEVICE, 16-byte aligned, E * 3*H*I*9/16 bytes in the
  *                   layout nvfp4_moe_pack writes (see nvfp4_moe_debug_packed_blob)
  *   gscale [E][3]   DEVICE float tensor scales (finite, > 0: not re-checked)
